@@ -1,0 +1,88 @@
+"""Independent formulations used to pin the oracle (test helpers, numpy fp64).
+
+* ``closed_form_states`` -- the unrolled product form of the KDA recurrence
+  ("Kimi K3: architecture and SGLang Day-0 Support", KDA math box: S_t is the sum
+  over s <= t of [prod_{u=s+1..t} (I - beta_u k_u k_u^T) Diag(alpha_u)] beta_s k_s v_s^T),
+  plus the initial-state term (prod_{u<=t} M_u) S_0 that the same unrolling gives
+  for a nonzero S_0.  Every M_u is an explicit dk x dk matrix.
+* ``chunked`` -- a second, chunk-parallel formulation (UT/WY form with a unit
+  lower-triangular solve and decay-rescaled keys), derived from the recurrence
+  by induction over the tokens of a chunk.  It is the algebra the CUDA kernels
+  use, checked here in fp64 against the sequential oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def token_transition(k, g, beta):
+    """M = (I - beta k k^T) Diag(exp(g)) for one token (k, g: [dk])."""
+    k = np.asarray(k, np.float64)
+    dk = k.shape[0]
+    return (np.eye(dk) - beta * np.outer(k, k)) @ np.diag(np.exp(np.asarray(g, np.float64)))
+
+
+def closed_form_states(k, v, g, beta, S0):
+    """States S_1..S_T of one head by the unrolled product form.  k, g: [T, dk]; v: [T, dv]; beta: [T]."""
+    T, dk = k.shape
+    Ms = [token_transition(k[t], g[t], beta[t]) for t in range(T)]
+    out = []
+    for t in range(T):
+        P = np.eye(dk)
+        for u in range(t + 1):
+            P = Ms[u] @ P
+        S = P @ S0
+        for s in range(t + 1):
+            Q = np.eye(dk)
+            for u in range(s + 1, t + 1):
+                Q = Ms[u] @ Q
+            S = S + Q @ (beta[s] * np.outer(k[s], v[s]))
+        out.append(S)
+    return np.stack(out)
+
+
+def chunked(q, k, v, g, beta, S0, C=64, L=16, dtype=np.float64):
+    """Chunk-parallel KDA for one head.  q, k, g: [T, dk]; v: [T, dv]; beta: [T]; S0: [dk, dv].
+
+    Per chunk of up to C tokens with entry state S0 and in-chunk cumulative log-decay
+    G_t = sum_{u<=t} g_u:
+      A_ts = beta_t sum_j k_t[j] k_s[j] exp(G_t[j] - G_s[j])   (s < t)
+      P_ts = sum_j q_t[j] k_s[j] exp(G_t[j] - G_s[j])          (s <= t)
+      (I + A) U = diag(beta) (V - (K o exp(G)) S0)               (unit lower-triangular solve)
+      O  = (Q o exp(G)) S0 + P U
+      S' = Diag(exp(G_C)) S0 + (K o exp(G_C - G))^T U
+    The pair decays exp(G_t - G_s) are split at a per-column-block reference
+    r = last token of s's L-token block: exp(G_t - G_r) * exp(G_r - G_s), so no
+    factor exceeds exp(L * |g|max) (finite in fp32 for |g| <= 5, L = 16).
+    Returns (O [T, dv], S_T [dk, dv]) computed in `dtype`.
+    """
+    f = lambda x: np.asarray(x, dtype)
+    q, k, v, g, beta, S = f(q), f(k), f(v), f(g), f(beta), f(S0).copy()
+    T = q.shape[0]
+    O = np.zeros((T, v.shape[1]), dtype)
+    for c0 in range(0, T, C):
+        c1 = min(c0 + C, T)
+        n = c1 - c0
+        qc, kc, vc, gc, bc = q[c0:c1], k[c0:c1], v[c0:c1], g[c0:c1], beta[c0:c1]
+        G = np.cumsum(gc, axis=0, dtype=dtype)
+        A = np.zeros((n, n), dtype)
+        P = np.zeros((n, n), dtype)
+        for b0 in range(0, n, L):
+            b1 = min(b0 + L, n)
+            Gr = G[b1 - 1]                                  # reference: last token of the column block
+            kminus = kc[b0:b1] * np.exp(Gr - G[b0:b1])      # <= 1
+            kplus = kc[b0:] * np.exp(G[b0:] - Gr)           # rows t >= b0 (up to exp(L*5) inside the block)
+            qplus = qc[b0:] * np.exp(G[b0:] - Gr)
+            A[b0:, b0:b1] = kplus @ kminus.T
+            P[b0:, b0:b1] = qplus @ kminus.T
+        A = np.tril(A, -1) * bc[:, None]
+        P = np.tril(P, 0)
+        gam = np.exp(G)
+        rhs = bc[:, None] * (vc - (kc * gam) @ S)
+        U = np.zeros_like(rhs)
+        for t in range(n):                                  # forward substitution, unit diagonal
+            U[t] = rhs[t] - A[t, :t] @ U[:t]
+        O[c0:c1] = (qc * gam) @ S + P @ U
+        khat = kc * np.exp(G[-1] - G)
+        S = np.exp(G[-1])[:, None] * S + khat.T @ U
+    return O, S
