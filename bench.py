@@ -1,0 +1,461 @@
+#!/usr/bin/env python3
+"""KDA hot-path benchmark on one GB300 (or N independent replicas under torchrun).
+
+Headline (`value`): prefill tokens/s per layer on the single-request prefill workload (B=1, T=8192, H=12,
+d=128, bf16 q/k/v, fp32 gates and state, S0 ~ N(0, 0.02), bf16 outputs + final fp32 state).  One step is
+one pass of the prefill path over that batch: the copy-on-write restore of the checkpoint into the working
+slot followed by the chunked (or segmented) prefill.  Inputs are resident in HBM; L2 is flushed (a 512 MB
+write) between timed steps.
+
+Also reported (`decode_verify`): state GB/s of the decode step, the 8-token speculative verify and the
+replay fold on the batched workload (256 requests, 1024-slot pool), against the measured HBM peak.
+
+`--impl reference` times the fp64 CPU oracle (the baseline arm) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+BYTES_PER_TOKEN_HEAD = 3 * 256 + 512 + 4 + 256  # q, k, v bf16 + g fp32 + beta fp32 in; o bf16 out (d = 128)
+STATE_BYTES = 128 * 128 * 4
+RECORD_BYTES = 256 + 256 + 512 + 4  # k, v bf16 + g fp32 + beta fp32
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--path", choices=["auto", "varlen", "segmented"], default="auto")
+    ap.add_argument("--segment-len", type=int, default=1024)
+    ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Weak scaling: every rank processes its own copy of the workload; the job rate is the units of all
+    ranks over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------- clocks
+
+class Clocks:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    import kda_gated_delta_rule_gb300 as kda
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init(world, "nccl")
+    kda.load()
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "")) or None
+    if uuid and not uuid.startswith("GPU-"):
+        uuid = "GPU-" + uuid
+    pk, pk_kind = peaks()
+    stream = torch.cuda.current_stream()
+
+    def to_dev(x):
+        t = torch.from_numpy(np.ascontiguousarray(x))
+        return (t.view(torch.bfloat16) if x.dtype == np.uint16 else t).to(dev)
+
+    # ---- single-request prefill workload
+    prob = synth.prefill_8k()
+    T, H, d = prob.T, prob.H, prob.dk
+    q, k, v, g, beta = (to_dev(x) for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    cu = to_dev(prob.cu_seqlens.astype(np.int32))
+    ckpt = to_dev(prob.pool)              # the checkpoint (committed prefix state)
+    pool = torch.zeros_like(ckpt)         # the working slot
+    slot = to_dev(np.array([0], np.int32))
+    out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(2, dtype=torch.int32, device=dev)
+    pargs = (q, k, v, g, beta, cu, T, pool, slot, out)
+    seg_len = args.segment_len
+    ws_bytes = kda.kda_segmented_workspace_size(*pargs, seg_len)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def restore():
+        kda.kda_state_copy(ckpt, slot, pool, slot)
+
+    def prefill(path):
+        if path == "varlen":
+            kda.kda_prefill_varlen(*pargs, dev_status=status)
+        else:
+            kda.kda_prefill_segmented(*pargs, seg_len, ws, dev_status=status)
+
+    kernels_per_step = {"varlen": 2, "segmented": 4}
+
+    def time_calls(fn, n, flush_between=True):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for i in range(n):
+            if flush_between:
+                flush.zero_()
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    # choose the path (both are parity-tested): the faster one on a few untimed calls
+    paths = ["varlen", "segmented"] if args.path == "auto" else [args.path]
+    trial = {}
+    for pth in paths:
+        for _ in range(2):
+            restore()
+            prefill(pth)
+        torch.cuda.synchronize()
+        trial[pth] = statistics.median(time_calls(lambda: (restore(), prefill(pth)), 3))
+    path = min(trial, key=trial.get)
+
+    def step():
+        restore()
+        prefill(path)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    status.zero_()
+
+    clocks = Clocks(uuid).start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    step_ms = time_calls(step, args.steps)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    st = status.cpu().numpy()
+    if st[0] != 0 or st[1] == 0:
+        raise RuntimeError(f"device status {st.tolist()} after the timed region (flags set or no work done)")
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, world, dev)
+    value = whole_job_value(T, world, ms_max / 1e3)
+
+    # ---- per-kernel durations of one step (events between the launches of the step)
+    def phase_times(n=10):
+        res = {}
+        if path == "varlen":
+            res["kda_state_copy"] = statistics.mean(time_calls(restore, n))
+            res["prefill_seq_kernel"] = statistics.mean(time_calls(lambda: (restore(), prefill("varlen")), n)) - \
+                res["kda_state_copy"]
+        else:
+            res["kda_state_copy"] = statistics.mean(time_calls(restore, n))
+            res["seg_fragments"] = statistics.mean(
+                time_calls(lambda: kda.kda_segment_fragments(*pargs, seg_len, ws), n))
+            res["seg_scan"] = statistics.mean(time_calls(lambda: kda.kda_fragment_scan(*pargs, seg_len, ws), n))
+            res["seg_outputs"] = statistics.mean(time_calls(lambda: kda.kda_segment_outputs(*pargs, seg_len, ws), n))
+        return res
+
+    phases = phase_times()
+    dominant = max((kname for kname in phases if kname != "kda_state_copy"), key=lambda kname: phases[kname])
+    n_seg = -(-T // seg_len)
+    alg = {
+        "prefill_seq_kernel": T * H * BYTES_PER_TOKEN_HEAD + 2 * H * STATE_BYTES,
+        # fragments: k, v, g, beta of all but the last segment; writes (S~, M) per segment and head
+        "seg_fragments": (T - seg_len) * H * (256 + 256 + 512 + 4) + (n_seg - 1) * H * 2 * STATE_BYTES,
+        "seg_scan": (n_seg - 1) * H * 2 * STATE_BYTES + n_seg * H * STATE_BYTES + H * STATE_BYTES,
+        "seg_outputs": T * H * BYTES_PER_TOKEN_HEAD + n_seg * H * STATE_BYTES + H * STATE_BYTES,
+    }
+    achieved = alg[dominant] / (phases[dominant] / 1e3) / 1e9
+    roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5), "traffic": None,
+                "peak_source": pk_kind, "algorithmic_bytes": alg[dominant],
+                "kernel_ms": round(phases[dominant], 4), "phase_ms": {kk: round(vv, 4) for kk, vv in phases.items()}}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    hq, hk, hv, hg, hb = (torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in
+                          (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    hs0 = torch.from_numpy(prob.pool).pin_memory()
+    ho = torch.empty(T, H, d, dtype=torch.bfloat16).pin_memory()
+    hsf = torch.empty_like(hs0).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hs0))
+    d2h = ho.numel() * ho.element_size() + hsf.numel() * hsf.element_size()
+
+    def e2e_step():
+        q.view(torch.int16).copy_(hq.view(torch.int16), non_blocking=True)
+        k.view(torch.int16).copy_(hk.view(torch.int16), non_blocking=True)
+        v.view(torch.int16).copy_(hv.view(torch.int16), non_blocking=True)
+        g.copy_(hg, non_blocking=True)
+        beta.copy_(hb, non_blocking=True)
+        ckpt.copy_(hs0, non_blocking=True)
+        step()
+        ho.copy_(out, non_blocking=True)
+        hsf.copy_(pool, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = statistics.mean(time_calls(e2e_step, max(5, min(args.steps, 20))))
+    e2e_value = whole_job_value(T, world, max_over_ranks(e2e_ms, world, dev) / 1e3)
+
+    # ---- decode / verify / fold on the batched workload
+    dv_report = None
+    if not args.no_decode:
+        dv_report = decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world)
+
+    line = {
+        "metric": "KDA prefill tokens/s/layer (H=12,d=128); decode+verify state GB/s vs HBM peak",
+        "value": round(value, 1),
+        "unit": "tokens/s/layer",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": "single-request prefill: B=1, T=8192, H=12, dk=dv=128, bf16 q/k/v, fp32 g/beta, "
+                        "fp32 state S0~N(0,0.02), bf16 o + final fp32 state; step = COW restore + prefill",
+            "path": path, "segment_len": seg_len if path == "segmented" else None,
+            "path_trial_ms": {kk: round(vv, 4) for kk, vv in trial.items()},
+            "l2": "flushed between timed steps (512 MB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "roofline": roofline,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s/layer", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps * kernels_per_step[path],
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if dv_report:
+        line["decode_verify"] = dv_report
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(prob, sample_tokens=T)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
+    p = synth.decode_verify()
+    B, W, H, d = p.B, p.W, p.H, p.dk
+    pool = to_dev(p.pool)
+    slots = to_dev(p.slot_ids)
+    q, k, v, g, beta = (to_dev(x) for x in (p.q, p.k, p.v, p.g, p.beta))
+    wq, wk, wv, wg, wb = (to_dev(x) for x in (p.wq, p.wk, p.wv, p.wg, p.wbeta))
+    out = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+    wout = torch.empty(B, W, H, d, dtype=torch.bfloat16, device=dev)
+    rec = torch.empty(kda.kda_replay_bytes(B, W, H, d, d, p.in_dtype), dtype=torch.uint8, device=dev)
+    acc = to_dev(p.accepted)
+    ckpt_slots = to_dev(synth.distinct_slots(p.seed, 99, B, p.pool.shape[0]))
+
+    def dec():
+        kda.kda_decode_step(q, k, v, g, beta, pool, slots, out)
+
+    def ver():
+        kda.kda_verify(wq, wk, wv, wg, wb, pool, slots, wout, rec)
+
+    def fold():
+        kda.kda_verify_replay(pool, slots, rec, acc, W, H, d, d, p.in_dtype)
+
+    def copy():
+        kda.kda_state_copy(pool, ckpt_slots, pool, slots)
+
+    for fn in (dec, ver, fold, copy):
+        for _ in range(3):
+            fn()
+    torch.cuda.synchronize()
+    n = 20
+    t = {name: statistics.mean(time_calls(fn, n)) for name, fn in
+         (("decode", dec), ("verify", ver), ("fold", fold), ("state_copy", copy))}
+    heads = B * H
+    n_acc = p.accepted.astype(np.int64)
+    alg = {
+        "decode": heads * (2 * STATE_BYTES + BYTES_PER_TOKEN_HEAD),
+        "verify": heads * (STATE_BYTES + W * (BYTES_PER_TOKEN_HEAD + RECORD_BYTES)),
+        "fold": int(H * sum(2 * STATE_BYTES + nn * RECORD_BYTES for nn in n_acc if nn > 0)),
+        "state_copy": B * 2 * H * STATE_BYTES,
+    }
+    rep = {"workload": "batched decode + speculative verify: 256 requests, 1024-slot pool, H=12, d=128, "
+                       "W=8, accepted ~ min(Poisson(2.7), 8)", "peak_gbs": pk["hbm_gbs"]}
+    for name in t:
+        gbs = alg[name] / (t[name] / 1e3) / 1e9
+        rep[name] = {"ms": round(t[name], 5), "algorithmic_bytes": alg[name], "gbs": round(gbs, 1),
+                     "frac": round(gbs / pk["hbm_gbs"], 4)}
+    return rep
+
+
+# ---------------------------------------------------------------- CPU baseline (the oracle)
+
+def cpu_baseline(prob, sample_tokens):
+    import oracle
+    q, k, v, g, beta = (x[:sample_tokens] for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    s0 = prob.pool[prob.slot_ids].astype(np.float64)
+    t0 = time.perf_counter()
+    r = oracle.recurrence(q, k, v, g, beta, [0, sample_tokens], s0=s0)
+    dt = time.perf_counter() - t0
+    return {"value": round(sample_tokens / dt, 2), "unit": "tokens/s/layer", "cores": r["threads"],
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"first {sample_tokens} tokens x 12 heads of the single-request prefill workload (fp64 "
+                      f"sequential recurrence, all outputs + final state)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    prob = synth.prefill_8k()
+    sample = 2048
+    q, k, v, g, beta = (x[:sample] for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    s0 = prob.pool[prob.slot_ids].astype(np.float64)
+
+    def step():
+        return oracle.recurrence(q, k, v, g, beta, [0, sample], s0=s0)
+
+    for _ in range(max(args.warmup, 3)):
+        r = step()
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    wall = time.perf_counter() - t_all
+    s = statistics.mean(times)
+    value = sample / s
+    line = {
+        "impl": "reference",
+        "metric": "KDA prefill tokens/s/layer (H=12,d=128); decode+verify state GB/s vs HBM peak",
+        "value": round(value, 2), "unit": "tokens/s/layer", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "single-request prefill: B=1, T=8192, H=12, dk=dv=128 (bounded sample: first "
+                               f"{sample} tokens per step)", "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s/layer", "cores": r["threads"],
+                         "kind": "oracle", "sample": f"first {sample} tokens x 12 heads per step"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s/layer", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s_timed_region": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

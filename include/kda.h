@@ -1,0 +1,216 @@
+/*
+ * kda.h -- C ABI of the KDA (Kimi Delta Attention) hot path on one NVIDIA GB300 (sm_103a).
+ *
+ * The recurrence (per sequence and head; S is dk x dv fp32, row j of S belongs to key channel j):
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,   o_t = S_t^T q_t
+ * with alpha_t = exp(g_t) a per-channel decay (g is passed as the log-decay) and beta_t a scalar.
+ * Source: "Kimi K3: Architecture and SGLang Day-0 Support" (AI-Infra-Visualized lesson), section
+ * "attention mechanism explained: KDA", math box (full update; gate, read along the key, delta write);
+ * section "linear attention" for the read-out o = S^T q after the write.  No 1/sqrt(dk) scale is applied.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * * Every pointer argument is a DEVICE pointer owned by the caller unless stated otherwise.  The library
+ *   never allocates, frees or retains memory; it keeps no state between calls.
+ * * Every call is asynchronous: it validates its host-visible arguments, enqueues its kernels on `stream`
+ *   (a cudaStream_t; NULL is the legacy default stream) and returns.  Stream order is the only ordering:
+ *   a copy-on-write restore, a forward pass and a snapshot enqueued on one stream happen in that order.
+ * * Return value: KDA_OK, or an error code; on an error nothing was enqueued, except KDA_ERR_CUDA, which
+ *   reports a launch failure (the error of cudaGetLastError()).
+ * * State pools are fp32, laid out [num_slots][H][dk][dv] row-major; a slot is H*dk*dv*4 bytes.
+ * * Token-major inputs: q, k [T][H][dk]; v [T][H][dv] (fp32 or bf16, `in_dtype`); g [T][H][dk] fp32
+ *   (log-decay, <= 0; the pages bound it below by -5); beta [T][H] fp32 in (0, 1).
+ * * Outputs o [T][H][dv] in `out_dtype` (fp32 or bf16, round to nearest even).
+ * * Supported head sizes: dk == dv in {16, 32, 64, 128}.  Anything else returns KDA_ERR_UNSUPPORTED.
+ * * Alignment: every array base must be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
+ * * dev_status (optional, may be NULL): int32[2] in device memory.  Kernels OR error flags
+ *   (KDA_DEV_*) into dev_status[0] and add the number of (token x head) state updates they performed
+ *   to dev_status[1] (wrapping 32-bit counter; a test that sees 0 work knows it tested nothing).
+ *   A slot id or accepted length out of range sets its flag; that unit is skipped without touching memory.
+ * * Slot ids within one call must be distinct; a source and a destination slot of one copy must not be
+ *   the same memory.  Violations are not detected and give undefined results.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kda_stream_t; /* == cudaStream_t */
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, negative or inconsistent size */
+  KDA_ERR_UNSUPPORTED = 2, /* head size or dtype combination not built */
+  KDA_ERR_WORKSPACE = 3,   /* workspace or record buffer too small */
+  KDA_ERR_CUDA = 4         /* a kernel launch failed */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+/* dev_status[0] flags */
+#define KDA_DEV_SLOT_OOB 1   /* a slot id outside [0, num_slots) */
+#define KDA_DEV_SEQ_OOB 2    /* cu_seqlens not non-decreasing within [0, T], or a sequence longer than max_seqlen */
+#define KDA_DEV_TIMEOUT 4    /* a bounded wait inside a kernel gave up */
+#define KDA_DEV_ACCEPT_OOB 8 /* an accepted length outside [0, W] */
+
+/* Human-readable name of a status code (static storage). */
+const char* kda_status_string(kda_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int kda_version(void);
+
+/* Bytes of one head's state: dk*dv*4 (64 KB at dk = dv = 128, the figure the ReplaySSM section of
+ * "SGLang and Miles: day-0 support for Kimi K3" gives per request, layer and head). */
+size_t kda_state_bytes_per_head(int dk, int dv);
+
+/*
+ * kda_state_copy -- copy whole slot states: dst_pool[dst_slots[i]] = src_pool[src_slots[i]], i < n.
+ * Source: "SGLang and Miles: day-0 support for Kimi K3", section "hybrid KDA memory management",
+ * "three state movements on the forward stream": the copy-on-write restore (checkpoint -> working slot)
+ * and the snapshot (working slot -> extra buffer) are kernels on the serial forward stream, so stream
+ * order gives the happens-before.  Donating a slot moves no bytes and needs no call.
+ *   src_pool [src_num_slots][state_elems], dst_pool [dst_num_slots][state_elems], fp32;
+ *   state_elems = H*dk*dv (a multiple of 4);  src_slots, dst_slots: int32[n] device arrays.
+ * Byte-exact.  An out-of-range slot id sets KDA_DEV_SLOT_OOB and that pair is skipped.
+ */
+kda_status kda_state_copy(const float* src_pool, int32_t src_num_slots, const int32_t* src_slots, float* dst_pool,
+                          int32_t dst_num_slots, const int32_t* dst_slots, int32_t n, int64_t state_elems,
+                          int32_t* dev_status, kda_stream_t stream);
+
+/*
+ * kda_decode_step -- one token per request, state updated in place in the pool.
+ * Source: the KDA math box of "Kimi K3: Architecture and SGLang Day-0 Support" (gate-then-delta form:
+ * S~ = Diag(alpha) S, r_old = S~^T k, S = S~ + beta k (v - r_old)^T) and the fused decode kernel named in
+ * "SGLang and Miles: day-0 support for Kimi K3", section "kernels".
+ *   q, k, g [B][H][dk]; v [B][H][dv]; beta [B][H]; out [B][H][dv];
+ *   pool [num_slots][H][dk][dv] (read and written once per (request, head)); slot_ids int32[B].
+ * The output is computed as o = S~^T q + (q . k) u with u = beta (v - r_old), which equals S_t^T q.
+ * Decode, verify and replay run one shared per-token routine, so n decode steps and a replay of n
+ * window tokens give bit-identical states.
+ */
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta, int B,
+                           int H, int dk, int dv, kda_dtype in_dtype, float* pool, int32_t num_slots,
+                           const int32_t* slot_ids, void* out, kda_dtype out_dtype, int32_t* dev_status,
+                           kda_stream_t stream);
+
+/*
+ * kda_replay_bytes -- size of the raw-input record buffer for a W-token draft window.
+ * Layout (each sub-array starts at a 256-byte aligned offset, in this order):
+ *   k    [B][W][H][dk]  in_dtype      v    [B][W][H][dv]  in_dtype
+ *   g    [B][W][H][dk]  fp32          beta [B][W][H]      fp32
+ * i.e. the step inputs S_i = (v_i, k_i, gk_i, beta_i) of the ReplaySSM section (q is not needed to
+ * advance the state): 1028 bytes per token and head at d = 128 with bf16 k and v.
+ */
+size_t kda_replay_bytes(int B, int W, int H, int dk, int dv, kda_dtype in_dtype);
+
+/*
+ * kda_verify -- speculative verify of a W-token draft window from the committed states.
+ * Source: "SGLang and Miles: day-0 support for Kimi K3", section "ReplaySSM: raw-input replay for KDA
+ * state": the verify kernel reads the committed checkpoint but never writes it, and stores each step's
+ * raw inputs; rejected drafts are never replayed.
+ *   q, k, g [B][W][H][dk]; v [B][W][H][dv]; beta [B][W][H]; out [B][W][H][dv];
+ *   pool is read only; replay: record buffer of replay_bytes >= kda_replay_bytes(B, W, H, dk, dv, in_dtype);
+ *   snapshot_out: NULL, or fp32 [B][W][H][dk][dv] receiving the state after every window token (the
+ *   snapshot-every-draft-step baseline the section replaces; for tests and comparisons).
+ */
+kda_status kda_verify(const void* q, const void* k, const void* v, const float* g, const float* beta, int B, int W,
+                      int H, int dk, int dv, kda_dtype in_dtype, const float* pool, int32_t num_slots,
+                      const int32_t* slot_ids, void* out, kda_dtype out_dtype, void* replay, size_t replay_bytes,
+                      float* snapshot_out, int32_t* dev_status, kda_stream_t stream);
+
+/*
+ * kda_verify_replay -- commit the accepted prefix of each window (the fold).
+ * Source: same ReplaySSM section: one fold kernel over all heads replays only the accepted prefix from
+ * the checkpoint, in place, consuming the gate values the verify kernel stored, so the rebuilt state is
+ * bit-identical to the recurrence baseline.
+ *   pool [num_slots][H][dk][dv], slot_ids int32[B] (the same slots verify read);
+ *   replay: the record buffer written by kda_verify with the same B, W, H, dk, dv, in_dtype;
+ *   accepted_len int32[B] device, each in [0, W]: tokens 1..n of the window are committed; n = 0 leaves
+ *   the slot untouched (no read, no write).  A value outside [0, W] sets KDA_DEV_ACCEPT_OOB, skipped.
+ */
+kda_status kda_verify_replay(float* pool, int32_t num_slots, const int32_t* slot_ids, int B, int W, int H, int dk,
+                             int dv, kda_dtype in_dtype, const void* replay, size_t replay_bytes,
+                             const int32_t* accepted_len, int32_t* dev_status, kda_stream_t stream);
+
+/* Arguments of a packed variable-length prefill. */
+typedef struct {
+  const void* q;          /* [T][H][dk] in_dtype */
+  const void* k;          /* [T][H][dk] in_dtype */
+  const void* v;          /* [T][H][dv] in_dtype */
+  const float* g;         /* [T][H][dk] log-decay */
+  const float* beta;      /* [T][H] */
+  kda_dtype in_dtype;
+  int64_t T;              /* total packed tokens (host) */
+  int H, dk, dv;
+  int N;                  /* number of sequences (host) */
+  const int32_t* cu_seqlens; /* int32[N+1] device: sequence i is tokens [cu[i], cu[i+1]) */
+  int32_t max_seqlen;     /* host: an upper bound on every sequence length (work sizing) */
+  float* pool;            /* [num_slots][H][dk][dv]: initial states read from, final states written to */
+  int32_t num_slots;
+  const int32_t* slot_ids; /* int32[N] device */
+  int init_zero;          /* nonzero: start every sequence from a zero state instead of pool[slot] */
+  void* out;              /* [T][H][dv] out_dtype */
+  kda_dtype out_dtype;
+  float* extra_pool;      /* optional snapshot pool [num_extra_slots][H][dk][dv], or NULL */
+  int32_t num_extra_slots;
+  const int32_t* extra_slot_ids; /* int32[N][2] device: the ping-pong pair of each sequence */
+  int32_t snapshot_every_chunks; /* 0: no snapshots; else a snapshot every this many 64-token chunks */
+  void* workspace;        /* scratch device memory, >= the matching *_workspace_size() bytes, or NULL if 0 */
+  size_t workspace_bytes;
+  int32_t* dev_status;    /* optional int32[2] */
+} kda_prefill_args;
+
+/* sizeof(kda_prefill_args), so a binding can check its mirror of the struct. */
+size_t kda_prefill_args_bytes(void);
+
+/*
+ * kda_prefill_varlen -- chunked prefill over packed sequences.
+ * Source: the recurrence above; chunked computation with keys rescaled by the reciprocal cumulative decay,
+ * made safe for dense tensor-core tiles by the log-decay floor g >= -5 ("Kimi K3: Architecture and SGLang
+ * Day-0 Support", KDA math box); per-chunk snapshots into a ping-pong extra buffer ("SGLang and Miles:
+ * day-0 support for Kimi K3", "three state movements on the forward stream").
+ * Sequence i starts from pool[slot_ids[i]] (or zero) and its final state is written to pool[slot_ids[i]].
+ * Snapshots (when extra_pool != NULL and snapshot_every_chunks > 0): after every p = 64 * m *
+ * snapshot_every_chunks tokens of sequence i (p <= its length, counted from the sequence start), the
+ * state is written to extra_pool[extra_slot_ids[2*i + ((m - 1) & 1)]]; the latest snapshot is in entry
+ * ((n_snap - 1) & 1).  Sequences shorter than one interval leave their extra slots untouched.
+ */
+kda_status kda_prefill_varlen(const kda_prefill_args* a, kda_stream_t stream);
+size_t kda_prefill_workspace_size(const kda_prefill_args* a);
+
+/*
+ * kda_prefill_segmented -- the same result as kda_prefill_varlen, computed by splitting every sequence into
+ * segments of segment_len tokens (a multiple of 64) that run in parallel.
+ * Source: "Kimi K3 training and serving infra" (marsggbo blog), section 4.2 "KCP: pass fixed-size
+ * transition information": each segment computes its cumulative transition M and the state S~ it produces
+ * from a zero input state; the true entry state of the next segment is S_in2 = M1 S_in1 + S~1; a prefix scan
+ * over the segments recovers every entry state, and the outputs are then computed from them.  Here all
+ * segments live on one GPU.  Three phases on `stream`: fragments, scan, outputs.
+ * Needs workspace_bytes >= kda_segmented_workspace_size(a, segment_len).  Snapshots are supported.
+ */
+kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
+size_t kda_segmented_workspace_size(const kda_prefill_args* a, int32_t segment_len);
+
+/*
+ * Phases of kda_prefill_segmented, exported for tests.  Workspace layout (fp32, 256-byte aligned parts):
+ *   frag  [N][P][H][dk][dv + dk]  per segment: columns 0..dv-1 hold S~ (zero input state),
+ *                                 columns dv..dv+dk-1 hold M (cumulative transition)
+ *   entry [N][P][H][dk][dv]       entry state of every segment (segment 0: the initial state)
+ * with P = ceil(max_seqlen / segment_len).  kda_segment_fragments writes frag;
+ * kda_fragment_scan writes entry from frag and the initial states; kda_segment_outputs reads entry.
+ */
+kda_status kda_segment_fragments(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
+kda_status kda_fragment_scan(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
+/* Third phase: outputs, snapshots and final states of every segment from the entry states in the workspace. */
+kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,261 @@
+"""Python binding of the KDA CUDA library (libkda.so, C ABI in include/kda.h).
+
+Argument marshalling only: every function takes torch CUDA tensors, passes their device pointers and the
+current CUDA stream to the C entry point of the same name, and raises KdaError on a non-OK status.  There
+is no CPU fallback: if the library is not built, every call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "KdaError", "load", "lib_path", "KDA_OK", "KDA_DEV_SLOT_OOB", "KDA_DEV_SEQ_OOB", "KDA_DEV_TIMEOUT",
+    "KDA_DEV_ACCEPT_OOB", "kda_status_string", "kda_version", "kda_state_bytes_per_head", "kda_state_copy",
+    "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
+    "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
+    "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "EXPORTED_SYMBOLS",
+]
+
+KDA_OK = 0
+KDA_DEV_SLOT_OOB, KDA_DEV_SEQ_OOB, KDA_DEV_TIMEOUT, KDA_DEV_ACCEPT_OOB = 1, 2, 4, 8
+F32, BF16 = 0, 1
+
+# every function include/kda.h declares
+EXPORTED_SYMBOLS = (
+    "kda_status_string", "kda_version", "kda_state_bytes_per_head", "kda_prefill_args_bytes", "kda_state_copy",
+    "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
+    "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
+    "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs",
+)
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn} failed: {kda_status_string(code)} ({code})")
+        self.code = code
+
+
+class PrefillArgs(ctypes.Structure):
+    """Mirror of kda_prefill_args."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("g", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("in_dtype", ctypes.c_int), ("T", ctypes.c_int64), ("H", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("N", ctypes.c_int), ("cu_seqlens", ctypes.c_void_p),
+        ("max_seqlen", ctypes.c_int32), ("pool", ctypes.c_void_p), ("num_slots", ctypes.c_int32),
+        ("slot_ids", ctypes.c_void_p), ("init_zero", ctypes.c_int), ("out", ctypes.c_void_p),
+        ("out_dtype", ctypes.c_int), ("extra_pool", ctypes.c_void_p), ("num_extra_slots", ctypes.c_int32),
+        ("extra_slot_ids", ctypes.c_void_p), ("snapshot_every_chunks", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t), ("dev_status", ctypes.c_void_p),
+    ]
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Loads libkda.so; raises if it is not built (no fallback path exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        if not build_if_missing:
+            raise RuntimeError(f"KDA CUDA library not built ({_build.LIB}); run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i32, i64, sz, c_int = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    sig = {
+        "kda_status_string": (ctypes.c_char_p, [c_int]),
+        "kda_version": (c_int, []),
+        "kda_state_bytes_per_head": (sz, [c_int, c_int]),
+        "kda_prefill_args_bytes": (sz, []),
+        "kda_state_copy": (c_int, [vp, i32, vp, vp, i32, vp, i32, i64, vp, vp]),
+        "kda_decode_step": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, vp, i32, vp, vp, c_int,
+                                    vp, vp]),
+        "kda_replay_bytes": (sz, [c_int, c_int, c_int, c_int, c_int, c_int]),
+        "kda_verify": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, i32, vp, vp, c_int,
+                               vp, sz, vp, vp, vp]),
+        "kda_verify_replay": (c_int, [vp, i32, vp, c_int, c_int, c_int, c_int, c_int, c_int, vp, sz, vp, vp, vp]),
+        "kda_prefill_varlen": (c_int, [ctypes.POINTER(PrefillArgs), vp]),
+        "kda_prefill_workspace_size": (sz, [ctypes.POINTER(PrefillArgs)]),
+        "kda_prefill_segmented": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
+        "kda_segmented_workspace_size": (sz, [ctypes.POINTER(PrefillArgs), i32]),
+        "kda_segment_fragments": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
+        "kda_fragment_scan": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
+        "kda_segment_outputs": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.kda_prefill_args_bytes() != ctypes.sizeof(PrefillArgs):
+        raise RuntimeError("kda_prefill_args layout mismatch between include/kda.h and the binding")
+    _lib = lib
+    return lib
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("expected contiguous CUDA tensors")
+
+
+def _ok(fn: str, code: int):
+    if code != KDA_OK:
+        raise KdaError(fn, code)
+
+
+# ---------------------------------------------------------------- entry points
+
+def kda_status_string(code: int) -> str:
+    return load().kda_status_string(code).decode()
+
+
+def kda_version() -> int:
+    return load().kda_version()
+
+
+def kda_state_bytes_per_head(dk: int, dv: int) -> int:
+    return load().kda_state_bytes_per_head(dk, dv)
+
+
+def kda_state_copy(src_pool, src_slots, dst_pool, dst_slots, dev_status=None, stream=None):
+    """dst_pool[dst_slots[i]] = src_pool[src_slots[i]] (pools [slots, H, dk, dv] fp32)."""
+    _check(src_pool, src_slots, dst_pool, dst_slots, dev_status)
+    n = src_slots.numel()
+    elems = src_pool[0].numel() if src_pool.shape[0] else dst_pool[0].numel()
+    _ok("kda_state_copy", load().kda_state_copy(_p(src_pool), src_pool.shape[0], _p(src_slots), _p(dst_pool),
+                                                dst_pool.shape[0], _p(dst_slots), n, elems, _p(dev_status),
+                                                _stream(stream)))
+
+
+def kda_decode_step(q, k, v, g, beta, pool, slot_ids, out, dev_status=None, stream=None):
+    """One token per request; q, k, g [B, H, dk]; v, out [B, H, dv]; beta [B, H]; pool updated in place."""
+    _check(q, k, v, g, beta, pool, slot_ids, out, dev_status)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _ok("kda_decode_step", load().kda_decode_step(_p(q), _p(k), _p(v), _p(g), _p(beta), B, H, dk, dv, _dt(q),
+                                                  _p(pool), pool.shape[0], _p(slot_ids), _p(out), _dt(out),
+                                                  _p(dev_status), _stream(stream)))
+
+
+def kda_replay_bytes(B: int, W: int, H: int, dk: int, dv: int, in_dtype: int) -> int:
+    return load().kda_replay_bytes(B, W, H, dk, dv, in_dtype)
+
+
+def kda_verify(q, k, v, g, beta, pool, slot_ids, out, replay, snapshot_out=None, dev_status=None, stream=None):
+    """Draft window: q, k, g [B, W, H, dk]; v, out [B, W, H, dv]; beta [B, W, H]; replay: uint8 record buffer."""
+    _check(q, k, v, g, beta, pool, slot_ids, out, replay, snapshot_out, dev_status)
+    B, W, H, dk = q.shape
+    dv = v.shape[-1]
+    _ok("kda_verify", load().kda_verify(_p(q), _p(k), _p(v), _p(g), _p(beta), B, W, H, dk, dv, _dt(q), _p(pool),
+                                        pool.shape[0], _p(slot_ids), _p(out), _dt(out), _p(replay),
+                                        replay.numel() * replay.element_size(), _p(snapshot_out), _p(dev_status),
+                                        _stream(stream)))
+
+
+def kda_verify_replay(pool, slot_ids, replay, accepted_len, W, H, dk, dv, in_dtype, dev_status=None, stream=None):
+    """Commits tokens 1..accepted_len[b] of each window into pool[slot_ids[b]]."""
+    _check(pool, slot_ids, replay, accepted_len, dev_status)
+    B = slot_ids.numel()
+    _ok("kda_verify_replay", load().kda_verify_replay(_p(pool), pool.shape[0], _p(slot_ids), B, W, H, dk, dv,
+                                                      in_dtype, _p(replay), replay.numel() * replay.element_size(),
+                                                      _p(accepted_len), _p(dev_status), _stream(stream)))
+
+
+def _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero=False,
+                    extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0, workspace=None, dev_status=None):
+    _check(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out, extra_pool, extra_slot_ids, workspace, dev_status)
+    T, H, dk = q.shape
+    a = PrefillArgs()
+    a.q, a.k, a.v, a.g, a.beta = (t.data_ptr() for t in (q, k, v, g, beta))
+    a.in_dtype = _dt(q)
+    a.T, a.H, a.dk, a.dv = T, H, dk, v.shape[-1]
+    a.N = cu_seqlens.numel() - 1
+    a.cu_seqlens = cu_seqlens.data_ptr()
+    a.max_seqlen = int(max_seqlen)
+    a.pool, a.num_slots, a.slot_ids = pool.data_ptr(), pool.shape[0], slot_ids.data_ptr()
+    a.init_zero = int(bool(init_zero))
+    a.out, a.out_dtype = out.data_ptr(), _dt(out)
+    if extra_pool is not None:
+        a.extra_pool, a.num_extra_slots = extra_pool.data_ptr(), extra_pool.shape[0]
+        a.extra_slot_ids = extra_slot_ids.data_ptr()
+        a.snapshot_every_chunks = int(snapshot_every_chunks)
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        a.dev_status = dev_status.data_ptr()
+    return a
+
+
+def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero=False,
+                       extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0, workspace=None,
+                       dev_status=None, stream=None):
+    """Packed prefill: q, k, g [T, H, dk]; v, out [T, H, dv]; beta [T, H]; cu_seqlens int32 [N+1]."""
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero, extra_pool,
+                        extra_slot_ids, snapshot_every_chunks, workspace, dev_status)
+    _ok("kda_prefill_varlen", load().kda_prefill_varlen(ctypes.byref(a), _stream(stream)))
+
+
+def kda_prefill_workspace_size(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, **kw) -> int:
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, **kw)
+    return load().kda_prefill_workspace_size(ctypes.byref(a))
+
+
+def kda_segmented_workspace_size(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, segment_len,
+                                 **kw) -> int:
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, **kw)
+    return load().kda_segmented_workspace_size(ctypes.byref(a), int(segment_len))
+
+
+def _segmented(fn, q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, segment_len, workspace,
+               init_zero=False, extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0, dev_status=None,
+               stream=None):
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero, extra_pool,
+                        extra_slot_ids, snapshot_every_chunks, workspace, dev_status)
+    _ok(fn, getattr(load(), fn)(ctypes.byref(a), int(segment_len), _stream(stream)))
+
+
+def kda_prefill_segmented(*args, **kw):
+    """Segmented (KCP) prefill; same arguments as kda_prefill_varlen plus segment_len and workspace."""
+    _segmented("kda_prefill_segmented", *args, **kw)
+
+
+def kda_segment_fragments(*args, **kw):
+    _segmented("kda_segment_fragments", *args, **kw)
+
+
+def kda_fragment_scan(*args, **kw):
+    _segmented("kda_fragment_scan", *args, **kw)
+
+
+def kda_segment_outputs(*args, **kw):
+    _segmented("kda_segment_outputs", *args, **kw)

@@ -1,0 +1,267 @@
+// C ABI of the KDA library: host-side validation, workspace sizing and dispatch to the kernels.
+// The declarations, argument meaning, layouts and error behaviour are documented in include/kda.h.
+#include <stdint.h>
+
+#include "../../include/kda.h"
+#include "launch.h"
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dtype_ok(kda_dtype t) { return t == KDA_DTYPE_F32 || t == KDA_DTYPE_BF16; }
+bool head_ok(int dk, int dv) { return dk == dv && (dk == 16 || dk == 32 || dk == 64 || dk == 128); }
+size_t esize(kda_dtype t) { return t == KDA_DTYPE_BF16 ? 2 : 4; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+struct ReplayLayout {
+  size_t off_k, off_v, off_g, off_beta, total;
+};
+
+ReplayLayout replay_layout(int B, int W, int H, int dk, int dv, kda_dtype t) {
+  const size_t rows = (size_t)B * W * H;
+  ReplayLayout L;
+  L.off_k = 0;
+  L.off_v = L.off_k + align256(rows * dk * esize(t));
+  L.off_g = L.off_v + align256(rows * dv * esize(t));
+  L.off_beta = L.off_g + align256(rows * dk * 4);
+  L.total = L.off_beta + align256(rows * 4);
+  return L;
+}
+
+kda::ReplayPtrs replay_ptrs(void* base, const ReplayLayout& L) {
+  char* b = static_cast<char*>(base);
+  return kda::ReplayPtrs{b + L.off_k, b + L.off_v, reinterpret_cast<float*>(b + L.off_g),
+                         reinterpret_cast<float*>(b + L.off_beta)};
+}
+
+// Validates the parts of a prefill call shared by the plain and segmented paths.
+kda_status check_prefill(const kda_prefill_args* a) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(a->in_dtype) || !dtype_ok(a->out_dtype)) return KDA_ERR_INVALID_ARG;
+  if (a->H <= 0 || a->N < 0 || a->T < 0 || a->max_seqlen < 0 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
+  if (!head_ok(a->dk, a->dv)) return KDA_ERR_UNSUPPORTED;
+  if (a->N > 65535) return KDA_ERR_INVALID_ARG;
+  if (!a->cu_seqlens || !a->pool || !a->slot_ids) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(a->pool) || !aligned16(a->cu_seqlens) || !aligned16(a->slot_ids)) return KDA_ERR_INVALID_ARG;
+  if (a->T > 0) {
+    if (!a->q || !a->k || !a->v || !a->g || !a->beta || !a->out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->g) || !aligned16(a->beta) ||
+        !aligned16(a->out))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if (a->extra_pool) {
+    if (a->snapshot_every_chunks < 0 || a->num_extra_slots < 0 || !a->extra_slot_ids) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(a->extra_pool)) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)a->snapshot_every_chunks * 64 > 0x7fffffff) return KDA_ERR_INVALID_ARG;
+  }
+  return KDA_OK;
+}
+
+kda::PrefillArgs to_internal(const kda_prefill_args* a) {
+  kda::PrefillArgs p{};
+  p.q = a->q;
+  p.k = a->k;
+  p.v = a->v;
+  p.g = a->g;
+  p.beta = a->beta;
+  p.in_bf16 = a->in_dtype == KDA_DTYPE_BF16;
+  p.out_bf16 = a->out_dtype == KDA_DTYPE_BF16;
+  p.T = a->T;
+  p.H = a->H;
+  p.d = a->dk;
+  p.N = a->N;
+  p.cu = a->cu_seqlens;
+  p.max_seqlen = a->max_seqlen;
+  p.pool = a->pool;
+  p.num_slots = a->num_slots;
+  p.slot_ids = a->slot_ids;
+  p.init_zero = a->init_zero != 0;
+  p.out = a->out;
+  p.extra_pool = (a->extra_pool && a->snapshot_every_chunks > 0) ? a->extra_pool : nullptr;
+  p.num_extra = a->num_extra_slots;
+  p.extra_slots = a->extra_slot_ids;
+  p.snap_every_tokens = p.extra_pool ? a->snapshot_every_chunks * 64 : 0;
+  p.status = a->dev_status;
+  return p;
+}
+
+struct SegLayout {
+  int P;
+  size_t frag_bytes, entry_bytes, total;
+};
+
+SegLayout seg_layout(const kda_prefill_args* a, int32_t seg_len) {
+  SegLayout L{};
+  L.P = a->max_seqlen > 0 ? (int)((a->max_seqlen + (int64_t)seg_len - 1) / seg_len) : 1;
+  const size_t heads = (size_t)a->N * L.P * a->H;
+  L.frag_bytes = align256(heads * a->dk * (size_t)(a->dv + a->dk) * 4);
+  L.entry_bytes = align256(heads * a->dk * (size_t)a->dv * 4);
+  L.total = L.frag_bytes + L.entry_bytes;
+  return L;
+}
+
+kda_status seg_prepare(const kda_prefill_args* a, int32_t seg_len, kda::PrefillArgs* p) {
+  kda_status st = check_prefill(a);
+  if (st != KDA_OK) return st;
+  if (seg_len <= 0 || seg_len % 64 != 0) return KDA_ERR_INVALID_ARG;
+  const SegLayout L = seg_layout(a, seg_len);
+  if (L.P > 65535) return KDA_ERR_INVALID_ARG;
+  if (!a->workspace || a->workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+  if (!aligned16(a->workspace)) return KDA_ERR_INVALID_ARG;
+  *p = to_internal(a);
+  p->seg_len = seg_len;
+  p->P = L.P;
+  p->frag = static_cast<float*>(a->workspace);
+  p->entry = reinterpret_cast<float*>(static_cast<char*>(a->workspace) + L.frag_bytes);
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+int kda_version(void) { return kVersion; }
+
+size_t kda_state_bytes_per_head(int dk, int dv) { return (dk > 0 && dv > 0) ? (size_t)dk * dv * 4 : 0; }
+
+kda_status kda_state_copy(const float* src_pool, int32_t src_num_slots, const int32_t* src_slots, float* dst_pool,
+                          int32_t dst_num_slots, const int32_t* dst_slots, int32_t n, int64_t state_elems,
+                          int32_t* dev_status, kda_stream_t stream) {
+  if (n < 0 || state_elems <= 0 || state_elems % 4 != 0 || src_num_slots < 0 || dst_num_slots < 0)
+    return KDA_ERR_INVALID_ARG;
+  if (n == 0) return KDA_OK;
+  if (!src_pool || !dst_pool || !src_slots || !dst_slots) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(src_pool) || !aligned16(dst_pool) || !aligned16(src_slots) || !aligned16(dst_slots))
+    return KDA_ERR_INVALID_ARG;
+  kda::CopyArgs c{src_pool, src_num_slots, src_slots, dst_pool, dst_num_slots, dst_slots, n, state_elems, dev_status};
+  return from_cuda(kda::launch_state_copy(c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta, int B,
+                           int H, int dk, int dv, kda_dtype in_dtype, float* pool, int32_t num_slots,
+                           const int32_t* slot_ids, void* out, kda_dtype out_dtype, int32_t* dev_status,
+                           kda_stream_t stream) {
+  if (B < 0 || H <= 0 || num_slots < 0 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_INVALID_ARG;
+  if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  if ((int64_t)B * H > 0x7fffffff) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, pool, slot_ids, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda::DecodeArgs a{q,    k,         v,        g,   beta,      B, H, dk, in_dtype == KDA_DTYPE_BF16,
+                    out_dtype == KDA_DTYPE_BF16, pool, num_slots, slot_ids, out, dev_status};
+  return from_cuda(kda::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_replay_bytes(int B, int W, int H, int dk, int dv, kda_dtype in_dtype) {
+  if (B < 0 || W < 0 || H <= 0 || dk <= 0 || dv <= 0 || !dtype_ok(in_dtype)) return 0;
+  return replay_layout(B, W, H, dk, dv, in_dtype).total;
+}
+
+kda_status kda_verify(const void* q, const void* k, const void* v, const float* g, const float* beta, int B, int W,
+                      int H, int dk, int dv, kda_dtype in_dtype, const float* pool, int32_t num_slots,
+                      const int32_t* slot_ids, void* out, kda_dtype out_dtype, void* replay, size_t replay_bytes,
+                      float* snapshot_out, int32_t* dev_status, kda_stream_t stream) {
+  if (B < 0 || W < 0 || H <= 0 || num_slots < 0 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+    return KDA_ERR_INVALID_ARG;
+  if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (B == 0 || W == 0) return KDA_OK;
+  if ((int64_t)B * H > 0x7fffffff) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, pool, slot_ids, out, replay};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if (snapshot_out && !aligned16(snapshot_out)) return KDA_ERR_INVALID_ARG;
+  const ReplayLayout L = replay_layout(B, W, H, dk, dv, in_dtype);
+  if (replay_bytes < L.total) return KDA_ERR_WORKSPACE;
+  kda::VerifyArgs a{q,         k,        v,   g,   beta,   B, W, H, dk, in_dtype == KDA_DTYPE_BF16,
+                    out_dtype == KDA_DTYPE_BF16, pool, num_slots, slot_ids, out, replay_ptrs(replay, L),
+                    snapshot_out, dev_status};
+  return from_cuda(kda::launch_verify(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_verify_replay(float* pool, int32_t num_slots, const int32_t* slot_ids, int B, int W, int H, int dk,
+                             int dv, kda_dtype in_dtype, const void* replay, size_t replay_bytes,
+                             const int32_t* accepted_len, int32_t* dev_status, kda_stream_t stream) {
+  if (B < 0 || W < 0 || H <= 0 || num_slots < 0 || !dtype_ok(in_dtype)) return KDA_ERR_INVALID_ARG;
+  if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  if ((int64_t)B * H > 0x7fffffff) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {pool, slot_ids, replay, accepted_len};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  const ReplayLayout L = replay_layout(B, W, H, dk, dv, in_dtype);
+  if (replay_bytes < L.total) return KDA_ERR_WORKSPACE;
+  kda::FoldArgs a{pool, num_slots, slot_ids, B, W, H, dk, in_dtype == KDA_DTYPE_BF16,
+                  replay_ptrs(const_cast<void*>(replay), L), accepted_len, dev_status};
+  return from_cuda(kda::launch_fold(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_prefill_args_bytes(void) { return sizeof(kda_prefill_args); }
+
+size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
+  (void)a;
+  return 0;
+}
+
+kda_status kda_prefill_varlen(const kda_prefill_args* a, kda_stream_t stream) {
+  kda_status st = check_prefill(a);
+  if (st != KDA_OK) return st;
+  if (a->N == 0) return KDA_OK;
+  const kda::PrefillArgs p = to_internal(a);
+  return from_cuda(kda::launch_prefill_seq(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t kda_segmented_workspace_size(const kda_prefill_args* a, int32_t segment_len) {
+  if (!a || segment_len <= 0 || segment_len % 64 != 0 || a->N < 0 || a->H <= 0 || a->dk <= 0 || a->dv <= 0)
+    return 0;
+  return seg_layout(a, segment_len).total;
+}
+
+kda_status kda_segment_fragments(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = seg_prepare(a, segment_len, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  return from_cuda(kda::launch_seg_fragments(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_fragment_scan(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = seg_prepare(a, segment_len, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  return from_cuda(kda::launch_seg_scan(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = seg_prepare(a, segment_len, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  return from_cuda(kda::launch_seg_outputs(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = seg_prepare(a, segment_len, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = kda::launch_seg_fragments(p, s);
+  if (e == cudaSuccess) e = kda::launch_seg_scan(p, s);
+  if (e == cudaSuccess) e = kda::launch_seg_outputs(p, s);
+  return from_cuda(e);
+}
+
+}  // extern "C"

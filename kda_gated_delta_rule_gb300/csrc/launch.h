@@ -1,0 +1,105 @@
+// Internal launch interface between the C ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Raw-input record of a draft window (see kda_replay_bytes in include/kda.h).
+struct ReplayPtrs {
+  void* k;      // [B][W][H][dk] in dtype
+  void* v;      // [B][W][H][dv] in dtype
+  float* g;     // [B][W][H][dk]
+  float* beta;  // [B][W][H]
+};
+
+struct DecodeArgs {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  int B, H, d;
+  bool in_bf16, out_bf16;
+  float* pool;
+  int num_slots;
+  const int32_t* slot_ids;
+  void* out;
+  int32_t* status;
+};
+
+struct VerifyArgs {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  int B, W, H, d;
+  bool in_bf16, out_bf16;
+  const float* pool;
+  int num_slots;
+  const int32_t* slot_ids;
+  void* out;
+  ReplayPtrs rec;
+  float* snapshot_out;
+  int32_t* status;
+};
+
+struct FoldArgs {
+  float* pool;
+  int num_slots;
+  const int32_t* slot_ids;
+  int B, W, H, d;
+  bool in_bf16;
+  ReplayPtrs rec;
+  const int32_t* accepted;
+  int32_t* status;
+};
+
+struct CopyArgs {
+  const float* src;
+  int src_num_slots;
+  const int32_t* src_slots;
+  float* dst;
+  int dst_num_slots;
+  const int32_t* dst_slots;
+  int n;
+  int64_t state_elems;
+  int32_t* status;
+};
+
+// Prefill over packed sequences; also drives the three phases of the segmented (KCP) path.
+struct PrefillArgs {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  bool in_bf16, out_bf16;
+  int64_t T;
+  int H, d, N;
+  const int32_t* cu;
+  int max_seqlen;
+  float* pool;
+  int num_slots;
+  const int32_t* slot_ids;
+  bool init_zero;
+  void* out;
+  float* extra_pool;
+  int num_extra;
+  const int32_t* extra_slots;
+  int snap_every_tokens;  // 0 = no snapshots
+  int32_t* status;
+  // segmented path
+  int seg_len;  // tokens per segment (multiple of 64)
+  int P;        // segments per sequence = ceil(max_seqlen / seg_len)
+  float* frag;  // [N][P][H][d][2d]
+  float* entry; // [N][P][H][d][d]
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_fold(const FoldArgs& a, cudaStream_t s);
+cudaError_t launch_state_copy(const CopyArgs& a, cudaStream_t s);
+
+// Sequential (token-by-token, CUDA-core) prefill; mode 0 = whole sequences.
+cudaError_t launch_prefill_seq(const PrefillArgs& a, cudaStream_t s);
+// Segmented path phases.
+cudaError_t launch_seg_fragments(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_seg_scan(const PrefillArgs& a, cudaStream_t s);
+cudaError_t launch_seg_outputs(const PrefillArgs& a, cudaStream_t s);
+
+}  // namespace kda

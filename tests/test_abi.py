@@ -1,0 +1,94 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared symbol, and rejects bad
+arguments on the host before any launch."""
+import ctypes
+import re
+import os
+
+import pytest
+
+import kda_gated_delta_rule_gb300 as kda
+from kda_gated_delta_rule_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return kda.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding_list():
+    assert declared_functions() == sorted(kda.EXPORTED_SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_sizes(lib):
+    assert kda.kda_status_string(0) == "KDA_OK"
+    assert kda.kda_status_string(3) == "KDA_ERR_WORKSPACE"
+    assert kda.kda_version() >= 10000
+    assert kda.kda_state_bytes_per_head(128, 128) == 64 * 1024
+    assert lib.kda_prefill_args_bytes() == ctypes.sizeof(kda.PrefillArgs)
+    # raw-input record: 1028 bytes per token and head at d = 128, bf16 k/v (256 + 256 + 512 + 4)
+    b = kda.kda_replay_bytes(256, 8, 12, 128, 128, 1)
+    assert b >= 256 * 8 * 12 * 1028 and b - 256 * 8 * 12 * 1028 < 4 * 256
+
+
+def test_host_validation_rejects_before_launch(lib):
+    """Invalid arguments return an error code; nothing is launched (no GPU is needed to check this)."""
+    null = None
+    # unsupported head size
+    assert lib.kda_decode_step(16, 16, 16, 16, 16, 4, 2, 48, 48, 1, 16, 8, 16, 16, 1, null, null) == 2
+    # null pointer
+    assert lib.kda_decode_step(null, 16, 16, 16, 16, 4, 2, 128, 128, 1, 16, 8, 16, 16, 1, null, null) == 1
+    # misaligned pointer
+    assert lib.kda_decode_step(18, 16, 16, 16, 16, 4, 2, 128, 128, 1, 16, 8, 16, 16, 1, null, null) == 1
+    # bad dtype
+    assert lib.kda_decode_step(16, 16, 16, 16, 16, 4, 2, 128, 128, 7, 16, 8, 16, 16, 1, null, null) == 1
+    # replay buffer too small
+    assert lib.kda_verify(16, 16, 16, 16, 16, 4, 8, 2, 128, 128, 1, 16, 8, 16, 16, 1, 16, 100, null, null,
+                          null) == 3
+    # empty batches are no-ops
+    assert lib.kda_decode_step(null, null, null, null, null, 0, 2, 128, 128, 1, null, 0, null, null, 1, null,
+                               null) == 0
+    assert lib.kda_state_copy(null, 0, null, null, 0, null, 0, 16, null, null) == 0
+    assert lib.kda_state_copy(16, 4, 16, 16, 4, 16, 1, 18, null, null) == 1  # state_elems not a multiple of 4
+
+
+def test_prefill_validation(lib):
+    a = kda.PrefillArgs()
+    a.q = a.k = a.v = a.g = a.beta = a.out = 16
+    a.cu_seqlens = a.pool = a.slot_ids = 16
+    a.in_dtype, a.out_dtype = 1, 1
+    a.T, a.H, a.dk, a.dv, a.N, a.max_seqlen, a.num_slots = 64, 2, 128, 128, 1, 64, 1
+    a.dk = a.dv = 96
+    assert lib.kda_prefill_varlen(ctypes.byref(a), None) == 2
+    a.dk = a.dv = 128
+    # segment length must be a positive multiple of 64, and the workspace must be large enough
+    assert lib.kda_prefill_segmented(ctypes.byref(a), 100, None) == 1
+    assert lib.kda_prefill_segmented(ctypes.byref(a), 64, None) == 3
+    need = lib.kda_segmented_workspace_size(ctypes.byref(a), 64)
+    # frag [N][P][H][dk][dv+dk] + entry [N][P][H][dk][dv], fp32, P = ceil(64/64) = 1
+    assert need == 2 * 128 * 256 * 4 + 2 * 128 * 128 * 4
+    a.workspace, a.workspace_bytes = 16, need - 1
+    assert lib.kda_prefill_segmented(ctypes.byref(a), 64, None) == 3
+    a.N = -1
+    assert lib.kda_prefill_varlen(ctypes.byref(a), None) == 1
+
+
+def test_library_fails_loudly_when_missing(tmp_path, monkeypatch):
+    """Without the built library there is no fallback: loading raises."""
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "absent" / "libkda.so"))
+    monkeypatch.setattr(kda, "_lib", None)
+    with pytest.raises(RuntimeError):
+        kda.load()

@@ -1,0 +1,190 @@
+"""GPU parity: decode step, speculative verify, replay fold and slot copies against the oracle, through the
+C ABI.  Full-size workload: 256 requests in a 1024-slot pool, H = 12, d = 128, an 8-token window with
+accepted lengths min(Poisson(2.7), 8)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests._gpu import bf16_bits, dev, host, rel_err, status
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16_IN = 2e-3  # max|d|/rms for bf16 inputs
+TOL_F32_IN = 1e-5   # max|d|/rms for the fp32-input path
+
+
+def _tol(dtype):
+    return TOL_BF16_IN if dtype == synth.BF16 else TOL_F32_IN
+
+
+CASES = [
+    dict(B=256, W=8, H=12, d=128, num_slots=1024, dtype=synth.BF16),  # the full decode+verify workload
+    dict(B=37, W=5, H=3, d=64, num_slots=50, dtype=synth.F32),
+    dict(B=9, W=3, H=2, d=32, num_slots=9, dtype=synth.BF16),
+    dict(B=5, W=8, H=2, d=16, num_slots=11, dtype=synth.F32),
+]
+
+
+def _ids(c):
+    return f"B{c['B']}_W{c['W']}_H{c['H']}_d{c['d']}_{'bf16' if c['dtype'] == synth.BF16 else 'f32'}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_decode_step(cuda, case):
+    kda = cuda
+    p = synth.decode_verify(B=case["B"], W=case["W"], H=case["H"], d=case["d"], num_slots=case["num_slots"],
+                            dtype=case["dtype"])
+    q, k, v, g, beta = dev(p.q), dev(p.k), dev(p.v), dev(p.g), dev(p.beta)
+    slots = dev(p.slot_ids)
+    pool0 = dev(p.pool)
+    pool = pool0.clone()
+    out = torch.empty(p.B, p.H, p.dv, dtype=torch.float32, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_decode_step(q, k, v, g, beta, pool, slots, out, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (0, p.B * p.H)
+    ref_o, ref_s = oracle.decode(p.pool, p.slot_ids, p.q, p.k, p.v, p.g, p.beta)
+    assert rel_err(host(out), ref_o) <= _tol(p.in_dtype)
+    assert rel_err(host(pool[slots.long()]), ref_s) <= _tol(p.in_dtype)
+    untouched = torch.ones(p.pool.shape[0], dtype=torch.bool, device="cuda")
+    untouched[slots.long()] = False
+    assert torch.equal(pool[untouched], pool0[untouched])
+    # bf16 output is the round-to-nearest-even of the fp32 output, bit for bit
+    pool2 = pool0.clone()
+    out16 = torch.empty(p.B, p.H, p.dv, dtype=torch.bfloat16, device="cuda")
+    kda.kda_decode_step(q, k, v, g, beta, pool2, slots, out16)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(out16), synth.f32_to_bf16(out.cpu().numpy()))
+    assert torch.equal(pool2, pool)  # deterministic: the same state bits on a repeat
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_verify_and_fold(cuda, case):
+    kda = cuda
+    p = synth.decode_verify(B=case["B"], W=case["W"], H=case["H"], d=case["d"], num_slots=case["num_slots"],
+                            dtype=case["dtype"])
+    B, W, H, d = p.B, p.W, p.H, p.dk
+    wq, wk, wv, wg, wb = dev(p.wq), dev(p.wk), dev(p.wv), dev(p.wg), dev(p.wbeta)
+    slots = dev(p.slot_ids)
+    pool0 = dev(p.pool)
+    pool = pool0.clone()
+    out = torch.empty(B, W, H, d, dtype=torch.float32, device="cuda")
+    rec = torch.zeros(kda.kda_replay_bytes(B, W, H, d, d, p.in_dtype), dtype=torch.uint8, device="cuda")
+    snaps = torch.empty(B, W, H, d, d, dtype=torch.float32, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_verify(wq, wk, wv, wg, wb, pool, slots, out, rec, snapshot_out=snaps, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (0, B * H * W)
+    assert torch.equal(pool, pool0), "verify must never write the committed state"
+    ref_o, ref_states = oracle.verify(p.pool, p.slot_ids, p.wq, p.wk, p.wv, p.wg, p.wbeta)
+    assert rel_err(host(out), ref_o) <= _tol(p.in_dtype)
+    assert rel_err(host(snaps), ref_states) <= _tol(p.in_dtype)
+
+    # the record holds the exact input bits (k, v, g, beta)
+    esz = 2 if p.in_dtype == synth.BF16 else 4
+    a256 = lambda x: (x + 255) // 256 * 256
+    rows = B * W * H
+    raw = rec.cpu().numpy()
+    off_v = a256(rows * d * esz)
+    off_g = off_v + a256(rows * d * esz)
+    off_b = off_g + a256(rows * d * 4)
+    assert raw[:rows * d * esz].tobytes() == p.wk.tobytes()
+    assert raw[off_v:off_v + rows * d * esz].tobytes() == p.wv.tobytes()
+    assert raw[off_g:off_g + rows * d * 4].tobytes() == p.wg.tobytes()
+    assert raw[off_b:off_b + rows * 4].tobytes() == p.wbeta.tobytes()
+
+    # n decode steps from the committed states give the snapshot-after-n states bit for bit
+    dpool = pool0.clone()
+    dout = torch.empty(B, H, d, dtype=torch.float32, device="cuda")
+    for w in range(W):
+        kda.kda_decode_step(wq[:, w].contiguous(), wk[:, w].contiguous(), wv[:, w].contiguous(),
+                            wg[:, w].contiguous(), wb[:, w].contiguous(), dpool, slots, dout)
+        torch.cuda.synchronize()
+        assert torch.equal(dpool[slots.long()], snaps[:, w]), f"decode step {w} differs from verify's state"
+        assert torch.equal(dout, out[:, w])
+
+    # fold: commit accepted prefixes
+    acc = dev(p.accepted)
+    st.zero_()
+    kda.kda_verify_replay(pool, slots, rec, acc, W, H, d, d, p.in_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (0, int(p.accepted.sum()) * H)
+    for b in range(B):
+        n = int(p.accepted[b])
+        got = pool[slots[b].long()]
+        expect = pool0[slots[b].long()] if n == 0 else snaps[b, n - 1]
+        assert torch.equal(got, expect), f"request {b}: fold({n}) is not bit-identical to the recurrence"
+    ref_fold = oracle.fold(p.pool, p.slot_ids, p.wq, p.wk, p.wv, p.wg, p.wbeta, p.accepted)
+    assert rel_err(host(pool[slots.long()]), ref_fold) <= _tol(p.in_dtype)
+    untouched = torch.ones(p.pool.shape[0], dtype=torch.bool, device="cuda")
+    untouched[slots.long()] = False
+    assert torch.equal(pool[untouched], pool0[untouched])
+
+    # bf16 outputs are the RNE rounding of the fp32 outputs
+    out16 = torch.empty(B, W, H, d, dtype=torch.bfloat16, device="cuda")
+    kda.kda_verify(wq, wk, wv, wg, wb, pool0, slots, out16, rec)
+    torch.cuda.synchronize()
+    assert np.array_equal(bf16_bits(out16), synth.f32_to_bf16(out.cpu().numpy()))
+
+
+def test_out_of_range_ids_are_flagged_and_skipped(cuda):
+    kda = cuda
+    p = synth.decode_verify(B=4, W=3, H=2, d=16, num_slots=8, dtype=synth.F32)
+    q, k, v, g, beta = dev(p.q), dev(p.k), dev(p.v), dev(p.g), dev(p.beta)
+    pool0 = dev(p.pool)
+    pool = pool0.clone()
+    bad = p.slot_ids.copy()
+    bad[2] = 8  # == num_slots
+    out = torch.zeros(4, 2, 16, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_decode_step(q, k, v, g, beta, pool, dev(bad), out, dev_status=st)
+    torch.cuda.synchronize()
+    flags, work = status(st)
+    assert flags == kda.KDA_DEV_SLOT_OOB and work == 3 * 2
+    touched = set(bad[[0, 1, 3]].tolist())
+    for s in range(8):
+        if s not in touched:
+            assert torch.equal(pool[s], pool0[s])
+    # accepted length out of range: flagged, slot untouched
+    W, H, d = p.W, p.H, p.dk
+    rec = torch.zeros(kda.kda_replay_bytes(4, W, H, d, d, p.in_dtype), dtype=torch.uint8, device="cuda")
+    wout = torch.zeros(4, W, H, d, device="cuda")
+    kda.kda_verify(dev(p.wq), dev(p.wk), dev(p.wv), dev(p.wg), dev(p.wbeta), pool0, dev(p.slot_ids), wout, rec)
+    pool = pool0.clone()
+    st.zero_()
+    acc = dev(np.array([1, W + 1, -1, 0], np.int32))
+    kda.kda_verify_replay(pool, dev(p.slot_ids), rec, acc, W, H, d, d, p.in_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    flags, work = status(st)
+    assert flags == kda.KDA_DEV_ACCEPT_OOB and work == 1 * H
+    for b in (1, 2, 3):
+        assert torch.equal(pool[int(p.slot_ids[b])], pool0[int(p.slot_ids[b])])
+
+
+def test_state_copy(cuda):
+    kda = cuda
+    H, d = 12, 128
+    src = dev(synth.normal(7, 1, (40, H, d, d), std=0.02))
+    dst0 = dev(synth.normal(7, 2, (64, H, d, d), std=0.02))
+    dst = dst0.clone()
+    ss = dev(synth.distinct_slots(7, 3, 16, 40))
+    ds = dev(synth.distinct_slots(7, 4, 16, 64))
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_state_copy(src, ss, dst, ds, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (0, 16)
+    assert torch.equal(dst[ds.long()], src[ss.long()])
+    keep = torch.ones(64, dtype=torch.bool, device="cuda")
+    keep[ds.long()] = False
+    assert torch.equal(dst[keep], dst0[keep])
+    # an out-of-range pair is flagged and skipped
+    st.zero_()
+    dst = dst0.clone()
+    bad = ds.clone()
+    bad[0] = 64
+    kda.kda_state_copy(src, ss, dst, bad, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (kda.KDA_DEV_SLOT_OOB, 15)
+    assert torch.equal(dst[bad[1:].long()], src[ss[1:].long()])

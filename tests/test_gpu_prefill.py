@@ -1,0 +1,148 @@
+"""GPU parity: packed varlen prefill and the segmented (KCP) prefill against the oracle, through the C ABI.
+
+Small cases span several 64-token chunks with ragged tails, empty and one-token sequences, and the
+snapshot ping-pong; the full-size workloads (single 8K request, 16-sequence varlen, 1M tokens) follow in
+test_gpu_fullsize.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests._gpu import PrefillRun, bf16_bits, dev, expected_extra_pool, host, oracle_prefill, rel_err, status
+
+pytestmark = pytest.mark.gpu
+
+TOL = {synth.BF16: 2e-3, synth.F32: 1e-5}
+
+
+def _check_against_oracle(run: PrefillRun, ref, tol):
+    prob = run.prob
+    assert rel_err(host(run.out), ref["o"]) <= tol
+    got = host(run.pool[run.slots.long()])
+    assert rel_err(got, ref["s_final"]) <= tol
+    untouched = np.ones(prob.pool.shape[0], bool)
+    untouched[prob.slot_ids] = False
+    assert np.array_equal(run.pool.cpu().numpy()[untouched], prob.pool[untouched])
+    if run.extra is not None:
+        exp = expected_extra_pool(prob, ref)
+        got_extra = host(run.extra)
+        assert rel_err(got_extra, exp) <= tol
+        written = np.zeros(prob.extra_pool.shape[0], bool)
+        for i, s in enumerate(ref["snaps"]):
+            for m in range(1, min(len(s), 2) + 1):
+                written[prob.extra_slot_ids[i, (len(s) - m) & 1]] = True
+        assert np.all(got_extra[~written] == 0), "extra slots without a snapshot must stay untouched"
+
+
+def test_tiny_fp32(cuda):
+    """1 sequence, T = 64, H = 2, d = 16, fp32, zero initial state: all outputs and the final state."""
+    prob = synth.tiny()
+    run = PrefillRun(prob).run_varlen(cuda)
+    ref = oracle_prefill(prob)
+    assert status(run.status) == (0, prob.T * prob.H)
+    _check_against_oracle(run, ref, TOL[synth.F32])
+
+
+VARLEN_CASES = [
+    # lengths chosen to hit: empty, single token, chunk-1, chunk, chunk+1, several chunks + tail, and
+    # snapshot intervals (every 2 chunks = 128 tokens) with odd and even snapshot counts
+    dict(d=128, dtype=synth.BF16, lengths=[0, 1, 63, 64, 65, 200, 300, 513], snap=2, H=3),
+    dict(d=64, dtype=synth.F32, lengths=[129, 7, 256, 64], snap=1, H=2),
+    dict(d=32, dtype=synth.BF16, lengths=[384, 5], snap=3, H=2),
+    dict(d=16, dtype=synth.F32, lengths=[1000, 17, 0], snap=4, H=4),
+]
+
+
+def _vid(c):
+    return f"d{c['d']}_{'bf16' if c['dtype'] == synth.BF16 else 'f32'}_n{len(c['lengths'])}"
+
+
+def _varlen(c, seed=31):
+    n = len(c["lengths"])
+    return synth.varlen(seed=seed, H=c["H"], d=c["d"], num_slots=2 * n + 3, num_extra=2 * n + 5,
+                        snapshot_every_chunks=c["snap"], dtype=c["dtype"], lengths=c["lengths"])
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=_vid)
+def test_varlen_with_snapshots(cuda, case):
+    prob = _varlen(case)
+    run = PrefillRun(prob).run_varlen(cuda)
+    ref = oracle_prefill(prob)
+    assert status(run.status) == (0, prob.T * prob.H)
+    _check_against_oracle(run, ref, TOL[prob.in_dtype])
+
+
+@pytest.mark.parametrize("case", VARLEN_CASES, ids=_vid)
+@pytest.mark.parametrize("segment_len", [64, 192])
+def test_segmented_matches_oracle(cuda, case, segment_len):
+    prob = _varlen(case, seed=32)
+    run = PrefillRun(prob).run_segmented(cuda, segment_len)
+    ref = oracle_prefill(prob)
+    assert status(run.status)[0] == 0
+    _check_against_oracle(run, ref, TOL[prob.in_dtype])
+
+
+def test_init_zero_and_bf16_output(cuda):
+    prob = synth.varlen(seed=33, H=2, d=128, num_slots=6, num_extra=4, snapshot_every_chunks=0,
+                        lengths=[100, 250])
+    prob.init_zero = True
+    run32 = PrefillRun(prob).run_varlen(cuda)
+    ref = oracle_prefill(prob)
+    _check_against_oracle(run32, ref, TOL[synth.BF16])
+    run16 = PrefillRun(prob, out_dtype=torch.bfloat16).run_varlen(cuda)
+    assert np.array_equal(bf16_bits(run16.out), synth.f32_to_bf16(run32.out.cpu().numpy()))
+    assert torch.equal(run16.pool, run32.pool)
+
+
+def test_segment_fragments_and_scan(cuda):
+    """Phase outputs of the segmented path: per segment, S~ (zero input state) and the cumulative
+    transition M; the scan's entry states equal the oracle's states at the segment boundaries."""
+    kda = cuda
+    seg = 128
+    prob = synth.varlen(seed=34, H=2, d=32, num_slots=4, num_extra=4, snapshot_every_chunks=0,
+                        lengths=[300, 128, 70], dtype=synth.F32)
+    run = PrefillRun(prob)
+    ws = run.workspace_for(kda, seg)
+    c = {k: v for k, v in run.common().items()}
+    kda.kda_segment_fragments(*run.args(), seg, ws, **c)
+    kda.kda_fragment_scan(*run.args(), seg, ws, **c)
+    torch.cuda.synchronize()
+    N, H, d = prob.N, prob.H, prob.dk
+    P = -(-int(prob.lengths.max()) // seg)
+    frag_elems = N * P * H * d * 2 * d
+    frag_bytes = -(-frag_elems * 4 // 256) * 256
+    wsf = ws.view(torch.float32)
+    frag = host(wsf[:frag_elems]).reshape(N, P, H, d, 2 * d)
+    entry = host(wsf[frag_bytes // 4:frag_bytes // 4 + N * P * H * d * d]).reshape(N, P, H, d, d)
+    cu = prob.cu_seqlens.astype(np.int64)
+    for i in range(N):
+        n_seg = -(-int(prob.lengths[i]) // seg)
+        bounds = [int(cu[i]) + p * seg for p in range(n_seg)] + [int(cu[i + 1])]
+        M = oracle.transition(prob.k, prob.g, prob.beta, bounds)
+        zero = oracle.recurrence(prob.q, prob.k, prob.v, prob.g, prob.beta, bounds, s0=None, want_o=False)
+        for p in range(n_seg - 1):  # the last segment's fragment is not needed and not computed
+            assert rel_err(frag[i, p, :, :, d:], M[p]) <= 1e-5
+            assert rel_err(frag[i, p, :, :, :d], zero["s_final"][p]) <= 1e-5
+        # entry states: oracle states at the segment starts
+        full = oracle.recurrence(prob.q[cu[i]:cu[i + 1]], prob.k[cu[i]:cu[i + 1]], prob.v[cu[i]:cu[i + 1]],
+                                 prob.g[cu[i]:cu[i + 1]], prob.beta[cu[i]:cu[i + 1]], [0, int(prob.lengths[i])],
+                                 s0=prob.pool[prob.slot_ids[i]][None].astype(np.float64), snap_every=seg,
+                                 want_o=False)
+        expect = [prob.pool[prob.slot_ids[i]].astype(np.float64)] + list(full["snaps"][0])
+        for p in range(n_seg):
+            assert rel_err(entry[i, p], expect[p]) <= 1e-5
+
+
+def test_bad_cu_seqlens_flagged(cuda):
+    kda = cuda
+    prob = synth.varlen(seed=35, H=2, d=16, num_slots=4, num_extra=4, snapshot_every_chunks=0,
+                        lengths=[40, 30], dtype=synth.F32)
+    run = PrefillRun(prob)
+    run.cu = dev(np.array([0, 50, 40], np.int32))  # decreasing: sequence 1 is invalid
+    pool0 = run.pool.clone()
+    kda.kda_prefill_varlen(*run.args(), **run.common())
+    torch.cuda.synchronize()
+    flags, work = status(run.status)
+    assert flags & kda.KDA_DEV_SEQ_OOB
+    assert torch.equal(run.pool[int(prob.slot_ids[1])], pool0[int(prob.slot_ids[1])])
