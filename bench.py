@@ -39,10 +39,10 @@ RECORD_BYTES = 256 + 256 + 512 + 4  # k, v bf16 + g fp32 + beta fp32
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--path", choices=["auto", "varlen", "segmented"], default="auto")
+    ap.add_argument("--path", choices=["auto", "varlen", "segmented"], default="segmented")
     ap.add_argument("--segment-len", type=int, default=1024)
     ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -113,7 +113,7 @@ class Clocks:
             os.close(fd)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self

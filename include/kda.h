@@ -178,7 +178,9 @@ size_t kda_prefill_args_bytes(void);
  * Snapshots (when extra_pool != NULL and snapshot_every_chunks > 0): after every p = 64 * m *
  * snapshot_every_chunks tokens of sequence i (p <= its length, counted from the sequence start), the
  * state is written to extra_pool[extra_slot_ids[2*i + ((m - 1) & 1)]]; the latest snapshot is in entry
- * ((n_snap - 1) & 1).  Sequences shorter than one interval leave their extra slots untouched.
+ * ((n_snap - 1) & 1).  Sequences shorter than one interval leave their extra slots untouched.  Only the final
+ * contents of the extra pool are defined: snapshots that a later snapshot of the same call overwrites (all but
+ * the last two of a sequence) are not written.
  */
 kda_status kda_prefill_varlen(const kda_prefill_args* a, kda_stream_t stream);
 size_t kda_prefill_workspace_size(const kda_prefill_args* a);

@@ -132,8 +132,13 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT) prefill_seq_kernel(const Prefil
     if (WANT_O) {
       if (tid < DVT) static_cast<Tout*>(a.out)[((size_t)t * a.H + h) * D + col0 + tid] = from_f32<Tout>(o);
       if (a.extra_pool && a.snap_every_tokens > 0) {
+        // Snapshot m goes to ping-pong entry (m - 1) & 1.  Only the last two snapshots of a sequence
+        // survive the call (an earlier one is overwritten by the snapshot two intervals later), so only
+        // those are written: same final extra-pool contents, fewer bytes, and no two concurrent segments
+        // ever write the same entry.
         const int64_t pos = t - s0 + 1;
-        if (pos % a.snap_every_tokens == 0) {
+        const int64_t n_snap = (s1 - s0) / a.snap_every_tokens;
+        if (pos % a.snap_every_tokens == 0 && pos / a.snap_every_tokens + 1 >= n_snap) {
           const int64_t m = pos / a.snap_every_tokens;
           const int es = a.extra_slots[2 * (size_t)i + ((m - 1) & 1)];
           if (es >= 0 && es < a.num_extra)

@@ -92,7 +92,7 @@ def expected_extra_pool(prob: synth.Prefill, ref) -> np.ndarray:
     """Contents of the ping-pong extra pool after the prefill: snapshot m of sequence i sits in entry
     (m - 1) & 1 of its pair; later snapshots overwrite earlier ones in the same entry."""
     extra = prob.extra_pool.astype(np.float64).copy()
-    for i, snaps in enumerate(ref["snaps"]):
+    for i, snaps in enumerate(ref.get("snaps", [])):
         for m in range(1, len(snaps) + 1):
             extra[prob.extra_slot_ids[i, (m - 1) & 1]] = snaps[m - 1]
     return extra

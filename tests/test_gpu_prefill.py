@@ -24,7 +24,9 @@ def _check_against_oracle(run: PrefillRun, ref, tol):
     untouched = np.ones(prob.pool.shape[0], bool)
     untouched[prob.slot_ids] = False
     assert np.array_equal(run.pool.cpu().numpy()[untouched], prob.pool[untouched])
-    if run.extra is not None:
+    if run.extra is not None and not prob.snapshot_every_chunks:
+        assert np.array_equal(run.extra.cpu().numpy(), prob.extra_pool), "no snapshots were requested"
+    elif run.extra is not None:
         exp = expected_extra_pool(prob, ref)
         got_extra = host(run.extra)
         assert rel_err(got_extra, exp) <= tol
@@ -100,7 +102,7 @@ def test_segment_fragments_and_scan(cuda):
     transition M; the scan's entry states equal the oracle's states at the segment boundaries."""
     kda = cuda
     seg = 128
-    prob = synth.varlen(seed=34, H=2, d=32, num_slots=4, num_extra=4, snapshot_every_chunks=0,
+    prob = synth.varlen(seed=34, H=2, d=32, num_slots=4, num_extra=8, snapshot_every_chunks=0,
                         lengths=[300, 128, 70], dtype=synth.F32)
     run = PrefillRun(prob)
     ws = run.workspace_for(kda, seg)
