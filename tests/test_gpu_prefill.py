@@ -120,9 +120,12 @@ def test_segment_fragments_and_scan(cuda):
     cu = prob.cu_seqlens.astype(np.int64)
     for i in range(N):
         n_seg = -(-int(prob.lengths[i]) // seg)
-        bounds = [int(cu[i]) + p * seg for p in range(n_seg)] + [int(cu[i + 1])]
-        M = oracle.transition(prob.k, prob.g, prob.beta, bounds)
-        zero = oracle.recurrence(prob.q, prob.k, prob.v, prob.g, prob.beta, bounds, s0=None, want_o=False)
+        a, b = int(cu[i]), int(cu[i + 1])
+        bounds = [p * seg for p in range(n_seg)] + [b - a]  # relative to the sequence start
+        sl = lambda x: np.ascontiguousarray(x[a:b])
+        M = oracle.transition(sl(prob.k), sl(prob.g), sl(prob.beta), bounds)
+        zero = oracle.recurrence(sl(prob.q), sl(prob.k), sl(prob.v), sl(prob.g), sl(prob.beta), bounds, s0=None,
+                                 want_o=False)
         for p in range(n_seg - 1):  # the last segment's fragment is not needed and not computed
             assert rel_err(frag[i, p, :, :, d:], M[p]) <= 1e-5
             assert rel_err(frag[i, p, :, :, :d], zero["s_final"][p]) <= 1e-5
