@@ -211,6 +211,25 @@ kda_status kda_fragment_scan(const kda_prefill_args* a, int32_t segment_len, kda
 /* Third phase: outputs, snapshots and final states of every segment from the entry states in the workspace. */
 kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
 
+/*
+ * kda_prefill_segmented_noalloc -- kda_prefill_segmented for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment convenience of this library.
+ * Some callers cannot pass a workspace: a plugin inside an inference server that owns all device memory
+ * through its own pool and offers plugins no allocation hook, or a serving loop that must not call
+ * cudaMalloc after start-up.  This call takes its scratch (the fragment and entry-state arrays described
+ * above) from a fixed 32 MiB array inside the library instead; a->workspace and a->workspace_bytes are
+ * ignored.  Everything else (arguments, results, errors) is as for kda_prefill_segmented.
+ *   * A problem whose scratch (kda_segmented_workspace_size) exceeds 32 MiB returns KDA_ERR_WORKSPACE.
+ *     Example: one 8192-token sequence, H = 12, d = 128, segment_len = 1024 needs 18 MiB.
+ *   * The array occupies 32 MiB of device memory on every GPU that loads this code, until the process
+ *     exits.
+ *   * The first call on a device looks up the array's device address (with that device current); make
+ *     that first call before any stream capture.
+ *   * All calls share the array and it keeps the last call's contents (no clearing is needed: every
+ *     byte read is first written by the same call).  Calls whose kernels overlap on the GPU race on it.
+ */
+kda_status kda_prefill_segmented_noalloc(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,8 @@ __all__ = [
     "KDA_DEV_ACCEPT_OOB", "kda_status_string", "kda_version", "kda_state_bytes_per_head", "kda_state_copy",
     "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
-    "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "EXPORTED_SYMBOLS",
+    "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
+    "EXPORTED_SYMBOLS",
 ]
 
 KDA_OK = 0
@@ -30,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "kda_status_string", "kda_version", "kda_state_bytes_per_head", "kda_prefill_args_bytes", "kda_state_copy",
     "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
-    "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs",
+    "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
 )
 
 
@@ -91,6 +92,7 @@ def load(build_if_missing: bool = False):
         "kda_segment_fragments": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
         "kda_fragment_scan": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
         "kda_segment_outputs": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
+        "kda_prefill_segmented_noalloc": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -259,3 +261,14 @@ def kda_fragment_scan(*args, **kw):
 
 def kda_segment_outputs(*args, **kw):
     _segmented("kda_segment_outputs", *args, **kw)
+
+
+def kda_prefill_segmented_noalloc(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, segment_len,
+                                  init_zero=False, extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0,
+                                  dev_status=None, stream=None):
+    """kda_prefill_segmented without a caller workspace: for callers that cannot allocate device memory,
+    the scratch comes from a fixed 32 MiB array inside the library (see include/kda.h)."""
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero, extra_pool,
+                        extra_slot_ids, snapshot_every_chunks, None, dev_status)
+    _ok("kda_prefill_segmented_noalloc",
+        load().kda_prefill_segmented_noalloc(ctypes.byref(a), int(segment_len), _stream(stream)))

@@ -1,0 +1,44 @@
+"""The allocation-free segmented prefill (kda_prefill_segmented_noalloc) against the existing entry point.
+
+Callers such as a plugin inside an inference server (which owns all device memory and gives plugins no
+allocation hook), or a serving loop that may not call cudaMalloc after start-up, cannot pass a workspace;
+this entry point takes its scratch from a fixed 32 MiB array inside the library.  This file is collected
+last on purpose: if it fails, a run that stops at the first failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests._gpu import PrefillRun, host, rel_err, status
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3
+SEGMENT = 1024  # one 8192-token sequence, H = 12, d = 128: 18 MiB of scratch
+
+
+def test_noalloc_matches_workspace_entry_point_twice(cuda):
+    kda = cuda
+    prob = synth.prefill_8k()
+    ref = PrefillRun(prob).run_segmented(kda, SEGMENT)  # the existing entry point, caller workspace
+    assert status(ref.status)[0] == 0
+    for call in range(2):  # two calls in a row: the second reuses the array as the first left it
+        run = PrefillRun(prob)
+        kda.kda_prefill_segmented_noalloc(*run.args(), SEGMENT, **run.common())
+        torch.cuda.synchronize()
+        assert status(run.status)[0] == 0 and status(run.status)[1] > 0
+        assert rel_err(host(run.out), host(ref.out)) <= TOL, f"call {call}: outputs differ"
+        assert rel_err(host(run.pool), host(ref.pool)) <= TOL, f"call {call}: final state differs"
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch(cuda):
+    kda = cuda
+    prob = synth.prefill_8k(T=2048, H=12)
+    run = PrefillRun(prob)
+    pool0 = run.pool.clone()
+    # 64-token segments: 32 segments x 12 heads x 192 KB of scratch = 72 MiB > 32 MiB
+    with pytest.raises(kda.KdaError) as e:
+        kda.kda_prefill_segmented_noalloc(*run.args(), 64, **run.common())
+    assert e.value.code == 3  # KDA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.equal(run.pool, pool0) and status(run.status) == (0, 0)
