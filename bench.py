@@ -34,6 +34,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 BYTES_PER_TOKEN_HEAD = 3 * 256 + 512 + 4 + 256  # q, k, v bf16 + g fp32 + beta fp32 in; o bf16 out (d = 128)
 STATE_BYTES = 128 * 128 * 4
 RECORD_BYTES = 256 + 256 + 512 + 4  # k, v bf16 + g fp32 + beta fp32
+# chunk-form algorithmic FLOPs per token and head at d = 128, C = 64: 2 (3 d^2 + 2.5 C d + C^2 / 6)
+ALG_FLOP_PER_TOKEN_HEAD = 2 * (3 * 128 * 128 + 2.5 * 64 * 128 + 64 * 64 / 6)
 
 
 def parse():
@@ -181,8 +183,8 @@ def run_ours(args):
     status = torch.zeros(2, dtype=torch.int32, device=dev)
     pargs = (q, k, v, g, beta, cu, T, pool, slot, out)
     seg_len = args.segment_len
-    ws_bytes = kda.kda_segmented_workspace_size(*pargs, seg_len)
-    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(kda.kda_segmented_workspace_size(*pargs, seg_len), 256), dtype=torch.uint8, device=dev)
+    ws_var = torch.empty(max(kda.kda_prefill_workspace_size(*pargs), 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
     def restore():
@@ -190,11 +192,11 @@ def run_ours(args):
 
     def prefill(path):
         if path == "varlen":
-            kda.kda_prefill_varlen(*pargs, dev_status=status)
+            kda.kda_prefill_varlen(*pargs, workspace=ws_var, dev_status=status)
         else:
             kda.kda_prefill_segmented(*pargs, seg_len, ws, dev_status=status)
 
-    kernels_per_step = {"varlen": 2, "segmented": 4}
+    kernels_per_step = {"varlen": 3, "segmented": 5}  # state copy + the path's kernels
 
     def time_calls(fn, n, flush_between=True):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
@@ -244,35 +246,37 @@ def run_ours(args):
     value = whole_job_value(T, world, ms_max / 1e3)
 
     # ---- per-kernel durations of one step (events between the launches of the step)
+    # ---- per-kernel durations of one step: the path's phases, each timed alone with events
     def phase_times(n=10):
-        res = {}
+        res = {"kda_state_copy": statistics.mean(time_calls(restore, n))}
         if path == "varlen":
-            res["kda_state_copy"] = statistics.mean(time_calls(restore, n))
-            res["prefill_seq_kernel"] = statistics.mean(time_calls(lambda: (restore(), prefill("varlen")), n)) - \
-                res["kda_state_copy"]
+            res["tc_prep_kernel"] = statistics.mean(
+                time_calls(lambda: kda.kda_prefill_records(*pargs, workspace=ws_var), n))
+            res["tc_chain_kernel<plain>"] = statistics.mean(
+                time_calls(lambda: (kda.kda_prefill_chain(*pargs, workspace=ws_var)), n))
         else:
-            res["kda_state_copy"] = statistics.mean(time_calls(restore, n))
-            res["seg_fragments"] = statistics.mean(
+            res["tc_prep_kernel"] = statistics.mean(time_calls(lambda: kda.kda_prefill_records(*pargs, workspace=ws), n))
+            res["tc_chain_kernel<frag>"] = statistics.mean(
                 time_calls(lambda: kda.kda_segment_fragments(*pargs, seg_len, ws), n))
-            res["seg_scan"] = statistics.mean(time_calls(lambda: kda.kda_fragment_scan(*pargs, seg_len, ws), n))
-            res["seg_outputs"] = statistics.mean(time_calls(lambda: kda.kda_segment_outputs(*pargs, seg_len, ws), n))
+            res["seg_scan_kernel"] = statistics.mean(time_calls(lambda: kda.kda_fragment_scan(*pargs, seg_len, ws), n))
+            res["tc_chain_kernel<segout>"] = statistics.mean(
+                time_calls(lambda: kda.kda_segment_outputs(*pargs, seg_len, ws), n))
         return res
 
     phases = phase_times()
     dominant = max((kname for kname in phases if kname != "kda_state_copy"), key=lambda kname: phases[kname])
-    n_seg = -(-T // seg_len)
-    alg = {
-        "prefill_seq_kernel": T * H * BYTES_PER_TOKEN_HEAD + 2 * H * STATE_BYTES,
-        # fragments: k, v, g, beta of all but the last segment; writes (S~, M) per segment and head
-        "seg_fragments": (T - seg_len) * H * (256 + 256 + 512 + 4) + (n_seg - 1) * H * 2 * STATE_BYTES,
-        "seg_scan": (n_seg - 1) * H * 2 * STATE_BYTES + n_seg * H * STATE_BYTES + H * STATE_BYTES,
-        "seg_outputs": T * H * BYTES_PER_TOKEN_HEAD + n_seg * H * STATE_BYTES + H * STATE_BYTES,
-    }
-    achieved = alg[dominant] / (phases[dominant] / 1e3) / 1e9
+    # algorithmic bytes of the prefill: 1540 B per token and head (q, k, v, o bf16; g, beta fp32) plus the
+    # initial and final state of every head; achieved = those bytes / the dominant kernel's duration
+    alg_bytes = T * H * BYTES_PER_TOKEN_HEAD + 2 * H * STATE_BYTES
+    achieved = alg_bytes / (phases[dominant] / 1e3) / 1e9
+    path_gbs = alg_bytes / (ms_max / 1e3) / 1e9
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5), "traffic": None,
-                "peak_source": pk_kind, "algorithmic_bytes": alg[dominant],
-                "kernel_ms": round(phases[dominant], 4), "phase_ms": {kk: round(vv, 4) for kk, vv in phases.items()}}
+                "peak_source": pk_kind, "algorithmic_bytes": alg_bytes,
+                "kernel_ms": round(phases[dominant], 4),
+                "phase_ms": {kk: round(vv, 4) for kk, vv in phases.items()},
+                "step_gbs": round(path_gbs, 2), "step_frac": round(path_gbs / pk["hbm_gbs"], 5),
+                "algorithmic_tflops_step": round(T * H * ALG_FLOP_PER_TOKEN_HEAD / (ms_max / 1e3) / 1e12, 3)}
 
     # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
     hq, hk, hv, hg, hb = (torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in
@@ -316,7 +320,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "bf16x3",
         "data": "synthetic",
         "config": {
             "workload": "single-request prefill: B=1, T=8192, H=12, dk=dv=128, bf16 q/k/v, fp32 g/beta, "

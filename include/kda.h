@@ -169,6 +169,12 @@ typedef struct {
 size_t kda_prefill_args_bytes(void);
 
 /*
+ * Workspace of kda_prefill_varlen.  bf16 inputs with dk = dv = 128 run the chunked tensor-core path, which
+ * needs (ceil(T/64) + N) * H * 148480 bytes (16-byte aligned) for the per-chunk operand records; every
+ * other combination runs the token-sequential path and needs none (0).
+ */
+
+/*
  * kda_prefill_varlen -- chunked prefill over packed sequences.
  * Source: the recurrence above; chunked computation with keys rescaled by the reciprocal cumulative decay,
  * made safe for dense tensor-core tiles by the log-decay floor g >= -5 ("Kimi K3: Architecture and SGLang
@@ -183,7 +189,17 @@ size_t kda_prefill_args_bytes(void);
  * the last two of a sequence) are not written.
  */
 kda_status kda_prefill_varlen(const kda_prefill_args* a, kda_stream_t stream);
-size_t kda_prefill_workspace_size(const kda_prefill_args* a);
+size_t kda_prefill_workspace_size(const kda_prefill_args* a);  /* see above; KDA_ERR_WORKSPACE if too small */
+
+/*
+ * The two phases of kda_prefill_varlen on the tensor-core path, exported so callers (and the benchmark)
+ * can time or schedule them separately.  kda_prefill_records writes the per-chunk operand records into
+ * a->workspace (all chunks of all sequences in parallel; a no-op returning KDA_OK where no records are
+ * needed); kda_prefill_chain then carries the state through the chunks of each sequence from those
+ * records (KDA_ERR_UNSUPPORTED where the token-sequential path applies).
+ */
+kda_status kda_prefill_records(const kda_prefill_args* a, kda_stream_t stream);
+kda_status kda_prefill_chain(const kda_prefill_args* a, kda_stream_t stream);
 
 /*
  * kda_prefill_segmented -- the same result as kda_prefill_varlen, computed by splitting every sequence into
@@ -199,12 +215,17 @@ kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len,
 size_t kda_segmented_workspace_size(const kda_prefill_args* a, int32_t segment_len);
 
 /*
- * Phases of kda_prefill_segmented, exported for tests.  Workspace layout (fp32, 256-byte aligned parts):
- *   frag  [N][P][H][dk][dv + dk]  per segment: columns 0..dv-1 hold S~ (zero input state),
+ * Phases of kda_prefill_segmented, exported for tests and timing.  Workspace layout, in this order:
+ *   records                       the per-chunk operand records of the tensor-core path, as for
+ *                                 kda_prefill_varlen (absent, 0 bytes, on the token-sequential path)
+ *   frag  [N][P][H][dk][dv + dk]  fp32, per segment: columns 0..dv-1 hold S~ (zero input state),
  *                                 columns dv..dv+dk-1 hold M (cumulative transition)
- *   entry [N][P][H][dk][dv]       entry state of every segment (segment 0: the initial state)
- * with P = ceil(max_seqlen / segment_len).  kda_segment_fragments writes frag;
- * kda_fragment_scan writes entry from frag and the initial states; kda_segment_outputs reads entry.
+ *   entry [N][P][H][dk][dv]       fp32, entry state of every segment (segment 0: the initial state)
+ * with P = ceil(max_seqlen / segment_len) and frag, entry starting on 256-byte boundaries after the
+ * records.  kda_prefill_segmented = kda_prefill_records, kda_segment_fragments, kda_fragment_scan,
+ * kda_segment_outputs: the fragments and outputs phases read the records (tensor-core path),
+ * kda_segment_fragments writes frag, kda_fragment_scan writes entry from frag and the initial states, and
+ * kda_segment_outputs reads entry.
  */
 kda_status kda_segment_fragments(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
 kda_status kda_fragment_scan(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
@@ -220,7 +241,7 @@ kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, k
  * above) from a fixed 32 MiB array inside the library instead; a->workspace and a->workspace_bytes are
  * ignored.  Everything else (arguments, results, errors) is as for kda_prefill_segmented.
  *   * A problem whose scratch (kda_segmented_workspace_size) exceeds 32 MiB returns KDA_ERR_WORKSPACE.
- *     Example: one 8192-token sequence, H = 12, d = 128, segment_len = 1024 needs 18 MiB.
+ *     Example: one 1024-token sequence, H = 4, d = 128 (bf16), segment_len = 256 needs about 13 MiB.
  *   * The array occupies 32 MiB of device memory on every GPU that loads this code, until the process
  *     exits.
  *   * The first call on a device looks up the array's device address (with that device current); make

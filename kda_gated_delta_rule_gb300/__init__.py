@@ -19,7 +19,7 @@ __all__ = [
     "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
-    "EXPORTED_SYMBOLS",
+    "kda_prefill_records", "kda_prefill_chain", "EXPORTED_SYMBOLS",
 ]
 
 KDA_OK = 0
@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
+    "kda_prefill_records", "kda_prefill_chain",
 )
 
 
@@ -93,6 +94,8 @@ def load(build_if_missing: bool = False):
         "kda_fragment_scan": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
         "kda_segment_outputs": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
         "kda_prefill_segmented_noalloc": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
+        "kda_prefill_records": (c_int, [ctypes.POINTER(PrefillArgs), vp]),
+        "kda_prefill_chain": (c_int, [ctypes.POINTER(PrefillArgs), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -225,6 +228,24 @@ def kda_prefill_varlen(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids,
     a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero, extra_pool,
                         extra_slot_ids, snapshot_every_chunks, workspace, dev_status)
     _ok("kda_prefill_varlen", load().kda_prefill_varlen(ctypes.byref(a), _stream(stream)))
+
+
+def kda_prefill_records(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero=False,
+                        extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0, workspace=None,
+                        dev_status=None, stream=None):
+    """Phase 1 of the tensor-core prefill: per-chunk operand records into `workspace`."""
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero, extra_pool,
+                        extra_slot_ids, snapshot_every_chunks, workspace, dev_status)
+    _ok("kda_prefill_records", load().kda_prefill_records(ctypes.byref(a), _stream(stream)))
+
+
+def kda_prefill_chain(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero=False,
+                      extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0, workspace=None,
+                      dev_status=None, stream=None):
+    """Phase 2 of the tensor-core prefill: the state carry over the chunks, from the records."""
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero, extra_pool,
+                        extra_slot_ids, snapshot_every_chunks, workspace, dev_status)
+    _ok("kda_prefill_chain", load().kda_prefill_chain(ctypes.byref(a), _stream(stream)))
 
 
 def kda_prefill_workspace_size(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, **kw) -> int:

@@ -89,18 +89,31 @@ kda::PrefillArgs to_internal(const kda_prefill_args* a) {
   return p;
 }
 
+// The tensor-core chunked path serves bf16 inputs at dk = dv = 128; everything else runs the
+// token-sequential CUDA-core path.
+bool use_tc(const kda_prefill_args* a) { return a->in_dtype == KDA_DTYPE_BF16 && a->dk == 128 && a->dv == 128; }
+
+size_t align1024(size_t x) { return (x + 1023) & ~size_t(1023); }
+
+// Per (chunk, head) operand records of the tensor-core path (0 for the CUDA-core path).
+size_t record_bytes(const kda_prefill_args* a) {
+  return use_tc(a) ? align1024(kda::tc_record_bytes(a->T, a->N, a->H)) : 0;
+}
+
 struct SegLayout {
   int P;
-  size_t frag_bytes, entry_bytes, total;
+  size_t rec_bytes, frag_bytes, entry_bytes, total;
 };
 
+// Segmented workspace: [records][frag][entry].
 SegLayout seg_layout(const kda_prefill_args* a, int32_t seg_len) {
   SegLayout L{};
   L.P = a->max_seqlen > 0 ? (int)((a->max_seqlen + (int64_t)seg_len - 1) / seg_len) : 1;
   const size_t heads = (size_t)a->N * L.P * a->H;
+  L.rec_bytes = record_bytes(a);
   L.frag_bytes = align256(heads * a->dk * (size_t)(a->dv + a->dk) * 4);
   L.entry_bytes = align256(heads * a->dk * (size_t)a->dv * 4);
-  L.total = L.frag_bytes + L.entry_bytes;
+  L.total = L.rec_bytes + L.frag_bytes + L.entry_bytes;
   return L;
 }
 
@@ -115,9 +128,32 @@ kda_status seg_prepare(const kda_prefill_args* a, int32_t seg_len, kda::PrefillA
   *p = to_internal(a);
   p->seg_len = seg_len;
   p->P = L.P;
-  p->frag = static_cast<float*>(a->workspace);
-  p->entry = reinterpret_cast<float*>(static_cast<char*>(a->workspace) + L.frag_bytes);
+  char* w = static_cast<char*>(a->workspace);
+  p->records = L.rec_bytes ? reinterpret_cast<uint8_t*>(w) : nullptr;
+  p->frag = reinterpret_cast<float*>(w + L.rec_bytes);
+  p->entry = reinterpret_cast<float*>(w + L.rec_bytes + L.frag_bytes);
   return KDA_OK;
+}
+
+cudaError_t run_fragments(const kda::PrefillArgs& p, cudaStream_t s) {
+  return p.records ? kda::launch_tc_chain_frag(p, p.records, s) : kda::launch_seg_fragments(p, s);
+}
+
+// Validates a varlen call's workspace for the tensor-core path and fills p.records (nullptr if none needed).
+kda_status varlen_prepare(const kda_prefill_args* a, kda::PrefillArgs* p) {
+  kda_status st = check_prefill(a);
+  if (st != KDA_OK) return st;
+  *p = to_internal(a);
+  const size_t need = record_bytes(a);
+  if (need == 0) return KDA_OK;
+  if (!a->workspace || a->workspace_bytes < need) return KDA_ERR_WORKSPACE;
+  if (!aligned16(a->workspace)) return KDA_ERR_INVALID_ARG;
+  p->records = static_cast<uint8_t*>(a->workspace);
+  return KDA_OK;
+}
+
+cudaError_t run_outputs(const kda::PrefillArgs& p, cudaStream_t s) {
+  return p.records ? kda::launch_tc_chain_segout(p, p.records, s) : kda::launch_seg_outputs(p, s);
 }
 
 }  // namespace
@@ -214,16 +250,34 @@ kda_status kda_verify_replay(float* pool, int32_t num_slots, const int32_t* slot
 size_t kda_prefill_args_bytes(void) { return sizeof(kda_prefill_args); }
 
 size_t kda_prefill_workspace_size(const kda_prefill_args* a) {
-  (void)a;
-  return 0;
+  if (!a || a->N < 0 || a->H <= 0 || a->T < 0) return 0;
+  return record_bytes(a);
 }
 
 kda_status kda_prefill_varlen(const kda_prefill_args* a, kda_stream_t stream) {
-  kda_status st = check_prefill(a);
-  if (st != KDA_OK) return st;
-  if (a->N == 0) return KDA_OK;
-  const kda::PrefillArgs p = to_internal(a);
-  return from_cuda(kda::launch_prefill_seq(p, reinterpret_cast<cudaStream_t>(stream)));
+  kda::PrefillArgs p;
+  kda_status st = varlen_prepare(a, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!p.records) return from_cuda(kda::launch_prefill_seq(p, s));
+  cudaError_t e = kda::launch_tc_prep(p, p.records, s);
+  if (e == cudaSuccess) e = kda::launch_tc_chain_plain(p, p.records, s);
+  return from_cuda(e);
+}
+
+kda_status kda_prefill_records(const kda_prefill_args* a, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = varlen_prepare(a, &p);
+  if (st != KDA_OK || a->N == 0 || !p.records) return st;
+  return from_cuda(kda::launch_tc_prep(p, p.records, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_prefill_chain(const kda_prefill_args* a, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = varlen_prepare(a, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  if (!p.records) return KDA_ERR_UNSUPPORTED;
+  return from_cuda(kda::launch_tc_chain_plain(p, p.records, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t kda_segmented_workspace_size(const kda_prefill_args* a, int32_t segment_len) {
@@ -236,7 +290,7 @@ kda_status kda_segment_fragments(const kda_prefill_args* a, int32_t segment_len,
   kda::PrefillArgs p;
   kda_status st = seg_prepare(a, segment_len, &p);
   if (st != KDA_OK || a->N == 0) return st;
-  return from_cuda(kda::launch_seg_fragments(p, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(run_fragments(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_fragment_scan(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream) {
@@ -250,7 +304,7 @@ kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, k
   kda::PrefillArgs p;
   kda_status st = seg_prepare(a, segment_len, &p);
   if (st != KDA_OK || a->N == 0) return st;
-  return from_cuda(kda::launch_seg_outputs(p, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(run_outputs(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream) {
@@ -258,9 +312,10 @@ kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len,
   kda_status st = seg_prepare(a, segment_len, &p);
   if (st != KDA_OK || a->N == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = kda::launch_seg_fragments(p, s);
+  cudaError_t e = p.records ? kda::launch_tc_prep(p, p.records, s) : cudaSuccess;
+  if (e == cudaSuccess) e = run_fragments(p, s);
   if (e == cudaSuccess) e = kda::launch_seg_scan(p, s);
-  if (e == cudaSuccess) e = kda::launch_seg_outputs(p, s);
+  if (e == cudaSuccess) e = run_outputs(p, s);
   return from_cuda(e);
 }
 

@@ -88,6 +88,8 @@ struct PrefillArgs {
   int P;        // segments per sequence = ceil(max_seqlen / seg_len)
   float* frag;  // [N][P][H][d][2d]
   float* entry; // [N][P][H][d][d]
+  // tensor-core path: per (chunk, head) operand records written by the prep kernel
+  uint8_t* records;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
@@ -101,5 +103,13 @@ cudaError_t launch_prefill_seq(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_seg_fragments(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_seg_scan(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_seg_outputs(const PrefillArgs& a, cudaStream_t s);
+
+// Tensor-core chunked path (bf16 inputs, d = 128).
+bool tc_supported(const PrefillArgs& a);
+size_t tc_record_bytes(int64_t T, int N, int H);
+cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t s);
+cudaError_t launch_tc_chain_plain(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
+cudaError_t launch_tc_chain_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
+cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 
 }  // namespace kda

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT) prefill_seq_kernel(const Prefil
 // entry_{p+1} = M_p entry_p + S~_p, with entry_0 the initial state.
 template <int D>
 struct ScanCfg {
-  static constexpr int CT = D < 32 ? D : 32;  // state columns per CTA
+  static constexpr int CT = 16;  // state columns per CTA (D / 16 CTAs per head)
   static constexpr int RGS = D / 4, CGS = CT / 4, NT = RGS * CGS;
   static constexpr size_t SMEM = sizeof(float) * ((size_t)D * (D + 1) + (size_t)D * CT);
 };
@@ -202,9 +202,27 @@ __global__ void __launch_bounds__(ScanCfg<D>::NT) seg_scan_kernel(const PrefillA
   for (int p = 0; p + 1 < nseg; ++p) {
     const float* fr = a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2;  // [D][2D]
     __syncthreads();  // Sin complete; previous Ms reads done
-    for (int e = tid; e < D * D; e += C::NT) {
-      const int r = e / D, l = e % D;
-      Ms[r * (D + 1) + l] = fr[(size_t)r * 2 * D + D + l];
+    // stage M (columns D..2D-1 of the fragment) with independent 128-bit loads
+    constexpr int V4 = D * D / 4 / C::NT;  // float4 per thread
+#pragma unroll
+    for (int b = 0; b < V4; b += 8) {
+      float4 x[8];
+#pragma unroll
+      for (int u = 0; u < 8 && b + u < V4; ++u) {
+        const int e = (b + u) * C::NT + tid;
+        const int r = e / (D / 4), l4 = e % (D / 4);
+        x[u] = *reinterpret_cast<const float4*>(fr + (size_t)r * 2 * D + D + 4 * l4);
+      }
+#pragma unroll
+      for (int u = 0; u < 8 && b + u < V4; ++u) {
+        const int e = (b + u) * C::NT + tid;
+        const int r = e / (D / 4), l4 = e % (D / 4);
+        float* dst = Ms + r * (D + 1) + 4 * l4;
+        dst[0] = x[u].x;
+        dst[1] = x[u].y;
+        dst[2] = x[u].z;
+        dst[3] = x[u].w;
+      }
     }
     float acc[4][4];
 #pragma unroll

@@ -1,0 +1,875 @@
+// Chunked prefill on the tensor cores: chunk 64, bf16 q/k/v, dk = dv = 128, fp32 state and gates.
+//
+// Sources: the KDA update S_t = (I - beta k k^T) Diag(alpha) S_{t-1} + beta k v^T, o_t = S_t^T q_t
+// ("Kimi K3: Architecture and SGLang Day-0 Support", KDA math box), computed chunkwise with keys rescaled
+// by cumulative decays; the log-decay floor g >= -5 keeps every rescaling factor inside fp32/bf16 range so
+// all tiles are dense matrix products (same math box).
+//
+// Chunk algebra (derived from the recurrence by induction over a chunk; entry state S, in-chunk cumulative
+// log-decay G_t = g_1 + ... + g_t, gamma_t = exp(G_t)):
+//   A_ts = beta_t sum_j k_t[j] k_s[j] exp(G_t[j] - G_s[j])  (s < t),   P_ts = sum_j q_t[j] k_s[j] exp(...)  (s <= t)
+//   (I + A) [W | U~] = diag(beta) [K o gamma | V]             (unit lower-triangular forward substitution)
+//   U  = U~ - W S
+//   O  = (Q o gamma) S + P U
+//   S' = Diag(gamma_C) S + (K o exp(G_C - G))^T U
+// Precision: every product takes fp32-derived operands as a two-term bf16 split x = hi + lo and sums
+// hi*hi + hi*lo + lo*hi on the tensor cores (fp32 accumulate); raw bf16 operands are used as they are.
+//
+// Two kernels:
+//  * prep (one CTA per chunk and head, all chunks in parallel): G, the Gram matrices A and P as one
+//    tcgen05 MMA, the forward substitution in fp32, and the chunk's operand tiles written to a workspace
+//    record already split and swizzled: [W; Q o gamma] (hi, lo), P (hi, lo), (K o exp(G_C - G))^T (hi, lo),
+//    U~ (fp32) and gamma_C.
+//  * chain (one CTA per sequence or segment and head): walks the chunks in order with the transposed state
+//    S^T in tensor memory (lane = value channel c, column = key channel j); each chunk's record is
+//    bulk-copied into a double-buffered shared-memory stage ahead of use.
+// The pair decays exp(G_t - G_s) are split at a reference token r as exp(G_t - G_r) exp(G_r - G_s): r is
+// the chunk's last token when the chunk's decay span is at most 80 (both factors within exp(+-80)), and
+// otherwise the last token of s's 16-token block, one MMA per block (|g| <= 5 keeps 16 tokens within 80).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_ptx.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int C = 64;   // chunk length
+constexpr int D = 128;  // dk = dv
+constexpr float SPAN_MAX = 80.f;
+
+// workspace record of one (chunk, head); the first REC_STAGE bytes are the chain's shared-memory stage
+constexpr uint32_t REC_B1HI = 0;        // [128 rows (W: 0..63, Q o gamma: 64..127)][K = 128], two 16 KB K-blocks
+constexpr uint32_t REC_B1LO = 32768;
+constexpr uint32_t REC_PHI = 65536;     // P [64 t][K = 64 s]
+constexpr uint32_t REC_PLO = 73728;
+constexpr uint32_t REC_KHHI = 81920;    // (K o exp(G_C - G))^T [128 j][K = 64 s]
+constexpr uint32_t REC_KHLO = 98304;
+constexpr uint32_t REC_STAGE = 114688;
+constexpr uint32_t REC_U = 114688;      // U~ [64 t][128 c] fp32
+constexpr uint32_t REC_GAMMA = 147456;  // gamma_C [128] fp32
+constexpr uint32_t REC_BYTES = 148480;
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ uint4 pack8(const __nv_bfloat16* v) {
+  uint4 r;
+  r.x = tc::pack2(v[0], v[1]);
+  r.y = tc::pack2(v[2], v[3]);
+  r.z = tc::pack2(v[4], v[5]);
+  r.w = tc::pack2(v[6], v[7]);
+  return r;
+}
+
+__device__ __forceinline__ void unpack8(uint4 r, float* x) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+// ---------------------------------------------------------------- prep
+
+// shared-memory layout of the prep kernel (offsets from a 1024-aligned base)
+constexpr uint32_t PS_XHI = 0;          // X [128][128] bf16: (K; Q) o exp(G_t - G_ref), hi then lo
+constexpr uint32_t PS_XLO = 32768;
+// once the Gram product has completed, the X region is reused for:
+constexpr uint32_t PS_A = 0;            // A [64][64] fp32 (beta folded in, strictly lower)
+constexpr uint32_t PS_T = 16384;        // T = (I + A)^-1 [64][64] fp32 (upper blocks: scratch)
+constexpr uint32_t PS_TBHI = 32768;     // T diag(beta) [64 t][K = 64 s] bf16, hi then lo
+constexpr uint32_t PS_TBLO = 40960;
+constexpr uint32_t PS_VT = 49152;       // V^T [128 c][K = 64 s] bf16
+constexpr uint32_t PS_YHI = 65536;      // Y [64][128] bf16: K o exp(G_ref - G_s), hi then lo
+constexpr uint32_t PS_YLO = 81920;
+constexpr uint32_t PS_KPHI = 98304;     // (K o gamma)^T [128 j][K = 64 s] bf16, hi then lo
+constexpr uint32_t PS_KPLO = 114688;
+constexpr uint32_t PS_K = 131072;       // raw k [64][128] bf16
+constexpr uint32_t PS_Q = 147456;       // raw q [64][128] bf16
+constexpr uint32_t PS_V = 163840;       // raw v [64][128] bf16
+constexpr uint32_t PS_G = 180224;       // g, then G (in place) [64][128] fp32
+constexpr uint32_t PS_BETA = 212992;    // beta [64]
+constexpr uint32_t PS_GTOT = 213248;    // per-channel sum of the first 32 tokens [128]
+constexpr uint32_t PS_BAR = 213760;     // three mbarriers: inputs, Gram product, W/U products
+constexpr uint32_t PS_SLOT = 213784;
+constexpr uint32_t PS_BYTES = 213800 + 1024;
+constexpr int PREP_NT = 256;
+
+// two-term split of a pair: (a, b) ~= hi + lo, packed bf16x2 (a in the low half)
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// splits 8 floats and stores the hi and lo 16-byte chunks
+__device__ __forceinline__ void split8_store(void* hi_dst, void* lo_dst, const float* v) {
+  uint4 h, l;
+  split_pair(v[0], v[1], h.x, l.x);
+  split_pair(v[2], v[3], h.y, l.y);
+  split_pair(v[4], v[5], h.z, l.z);
+  split_pair(v[6], v[7], h.w, l.w);
+  *reinterpret_cast<uint4*>(hi_dst) = h;
+  *reinterpret_cast<uint4*>(lo_dst) = l;
+}
+
+__device__ __forceinline__ void load8f(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// X rows r = 0..127 (K part, then Q part) for decay reference ref_row; rows t < row_min are zero.
+__device__ __forceinline__ void build_x_chunk(uint8_t* sm, int r, int cc, int ref_row, int row_min) {
+  const int t = r & 63;
+  float v[8];
+  if (t < row_min) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
+  } else {
+    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(sm + (r < 64 ? PS_K : PS_Q));
+    const float* G = reinterpret_cast<const float*>(sm + PS_G);
+    float gt[8], gr[8];
+    unpack8(*reinterpret_cast<const uint4*>(src + t * D + cc * 8), v);
+    load8f(G + t * D + cc * 8, gt);
+    load8f(G + ref_row * D + cc * 8, gr);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] *= __expf(gt[e] - gr[e]);
+  }
+  const uint32_t off = (uint32_t)(cc >> 3) * 16384u + tc::sw128_chunk(r, cc & 7);
+  split8_store(sm + PS_XHI + off, sm + PS_XLO + off, v);
+}
+
+// Y row s (key s rescaled to reference token ref_row), 16-byte chunk cc.
+__device__ __forceinline__ void build_y_chunk(uint8_t* sm, int s, int cc, int ref_row) {
+  const __nv_bfloat16* K = reinterpret_cast<const __nv_bfloat16*>(sm + PS_K);
+  const float* G = reinterpret_cast<const float*>(sm + PS_G);
+  float v[8], gs[8], gr[8];
+  unpack8(*reinterpret_cast<const uint4*>(K + s * D + cc * 8), v);
+  load8f(G + s * D + cc * 8, gs);
+  load8f(G + ref_row * D + cc * 8, gr);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] *= __expf(gr[e] - gs[e]);
+  const uint32_t off = (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(s, cc & 7);
+  split8_store(sm + PS_YHI + off, sm + PS_YLO + off, v);
+}
+
+// D[:, col0 : col0 + N] = X Y[row0 : row0 + N]^T with the three split products (A, B from shared memory).
+__device__ __forceinline__ void issue_gram(uint8_t* sm, uint32_t d_tmem, int row0, int N) {
+  const uint32_t base = tc::smem_u32(sm);
+  const uint32_t idesc = tc::idesc_bf16(128, N);
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const uint32_t xa = base + (part == 2 ? PS_XLO : PS_XHI);
+    const uint32_t yb = base + (part == 1 ? PS_YLO : PS_YHI) + (uint32_t)row0 * 128u;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+      const uint32_t koff_y = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
+      tc::mma_ss(d_tmem, tc::sdesc(xa + koff), tc::sdesc(yb + koff_y), idesc, (part | ks) != 0);
+    }
+  }
+}
+
+// [W | U~] = T diag(beta) [K o gamma | V]: M = 64 rows t, N = 128, K = 64 tokens s.
+__device__ __forceinline__ void issue_wu(uint8_t* sm, uint32_t tm) {
+  const uint32_t base = tc::smem_u32(sm);
+  const uint32_t idesc = tc::idesc_bf16(64, 128);
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const uint32_t ta = base + (part == 2 ? PS_TBLO : PS_TBHI);
+    const uint32_t kb = base + (part == 1 ? PS_KPLO : PS_KPHI);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      tc::mma_ss(tm, tc::sdesc(ta + (uint32_t)ks * 32u), tc::sdesc(kb + (uint32_t)ks * 32u), idesc, (part | ks) != 0);
+  }
+#pragma unroll
+  for (int part = 0; part < 2; ++part) {  // V is exact in bf16: split T diag(beta) only
+    const uint32_t ta = base + (part == 1 ? PS_TBLO : PS_TBHI);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      tc::mma_ss(tm + 128, tc::sdesc(ta + (uint32_t)ks * 32u), tc::sdesc(base + PS_VT + (uint32_t)ks * 32u), idesc,
+                 (part | ks) != 0);
+  }
+}
+
+// Tensor maps of the token-major inputs, each viewed as [T][H][128] with a 64-token x 1-head x 128 box.
+struct PrepMaps {
+  CUtensorMap q, k, v, g;
+};
+
+__global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a, uint8_t* __restrict__ ws,
+                                                              const __grid_constant__ PrepMaps maps) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(sm + PS_K);
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm + PS_Q);
+  float* sG = reinterpret_cast<float*>(sm + PS_G);
+  float* sA = reinterpret_cast<float*>(sm + PS_A);
+  float* sT = reinterpret_cast<float*>(sm + PS_T);
+  float* sbeta = reinterpret_cast<float*>(sm + PS_BETA);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + PS_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PS_SLOT);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int cidx = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
+  const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
+  if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
+    if (tid == 0 && cidx == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
+    return;
+  }
+  const int64_t t0 = s0 + (int64_t)cidx * C;
+  if (t0 >= s1) return;
+  const int n = (int)((s1 - t0) < C ? (s1 - t0) : C);
+  uint8_t* rec = ws + ((size_t)(t0 / C + i) * a.H + h) * REC_BYTES;
+
+  if (warp == 0) tc::tmem_alloc(tslot, 256);
+  if (tid == 0) {
+    for (int b = 0; b < 3; ++b) tc::bar_init(bar + b, 1);
+    tc::bar_fence_init();
+  }
+  __syncthreads();
+  // stage the chunk's k, q, v and g tiles (64 tokens x 128 channels of head h) with four TMA loads
+  if (tid == 0) {
+    tc::bar_arrive_expect_tx(bar + 2, 3 * 16384 + 32768);
+    tc::tma_load_3d(sK, &maps.k, 0, h, (int)t0, bar + 2);
+    tc::tma_load_3d(sQ, &maps.q, 0, h, (int)t0, bar + 2);
+    tc::tma_load_3d(sm + PS_V, &maps.v, 0, h, (int)t0, bar + 2);
+    tc::tma_load_3d(sG, &maps.g, 0, h, (int)t0, bar + 2);
+  }
+  bool ok = __syncthreads_and(tc::bar_wait(bar + 2, 0));
+  // rows past the chunk's valid tokens (the next sequence's, or beyond T) are zero: k = q = v = g = 0
+  for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
+    const int t = n + (e >> 4), cc = e & 15;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(sK + t * D + cc * 8) = z;
+    *reinterpret_cast<uint4*>(sQ + t * D + cc * 8) = z;
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(sm + PS_V) + t * D + cc * 8) = z;
+    *reinterpret_cast<float4*>(sG + t * D + cc * 8) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(sG + t * D + cc * 8 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (tid >= D && tid < D + C) {
+    const int t = tid - D;
+    sbeta[t] = t < n ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
+  }
+  __syncthreads();
+  // cumulative log-decay in place: thread (j, half) scans 32 tokens, the upper half then adds the lower
+  // half's total; the decay span of channel j (including the chunk start, G = 0) decides the path
+  float span = 0.f;
+  {
+    const int j = tid & (D - 1), half = tid >> 7;
+    float* gtot = reinterpret_cast<float*>(sm + PS_GTOT);
+    float* ext = reinterpret_cast<float*>(sm + PS_XHI);  // scratch for the extremes, before X is built
+    float x[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u) x[u] = sG[(32 * half + u) * D + j];
+#pragma unroll
+    for (int u = 1; u < 32; ++u) x[u] = __fadd_rn(x[u - 1], x[u]);
+    if (half == 0) gtot[j] = x[31];
+    __syncthreads();
+    const float off = half ? gtot[j] : 0.f;
+    float gmin = 0.f, gmax = 0.f;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const float gval = half ? __fadd_rn(off, x[u]) : x[u];
+      sG[(32 * half + u) * D + j] = gval;
+      gmin = fminf(gmin, gval);
+      gmax = fmaxf(gmax, gval);
+    }
+    ext[2 * tid] = gmin;
+    ext[2 * tid + 1] = gmax;
+    __syncthreads();
+    if (half == 0) span = fmaxf(gmax, ext[2 * (tid + 128) + 1]) - fminf(gmin, ext[2 * (tid + 128)]);
+  }
+  tc::fence_before_sync();
+  const bool slow = __syncthreads_or(span > SPAN_MAX);
+  tc::fence_after_sync();
+  const uint32_t tm = *tslot;
+
+  // per (token t, 8 channels): Q o gamma (output), (K o gamma)^T (operand), and in the common case X, Y
+  for (int task = tid; task < C * 16; task += PREP_NT) {
+    const int t = task >> 4, cc = task & 15;
+    float kx[8], qx[8], gt[8], e2[8], v[8];
+    unpack8(*reinterpret_cast<const uint4*>(sK + t * D + cc * 8), kx);
+    unpack8(*reinterpret_cast<const uint4*>(sQ + t * D + cc * 8), qx);
+    load8f(sG + t * D + cc * 8, gt);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) e2[e] = __expf(gt[e]);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = qx[e] * e2[e];
+    const uint32_t ob = (uint32_t)(cc >> 3) * 16384u + tc::sw128_chunk(64 + t, cc & 7);
+    split8_store(rec + REC_B1HI + ob, rec + REC_B1LO + ob, v);
+    if (!slow) {
+      float gc[8], e1[8];
+      load8f(sG + (C - 1) * D + cc * 8, gc);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) e1[e] = __expf(gt[e] - gc[e]);
+      const uint32_t xo = (uint32_t)(cc >> 3) * 16384u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = kx[e] * e1[e];
+      split8_store(sm + PS_XHI + xo + tc::sw128_chunk(t, cc & 7), sm + PS_XLO + xo + tc::sw128_chunk(t, cc & 7), v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = qx[e] * e1[e];
+      split8_store(sm + PS_XHI + xo + tc::sw128_chunk(64 + t, cc & 7), sm + PS_XLO + xo + tc::sw128_chunk(64 + t, cc & 7),
+                   v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = kx[e] * __expf(gc[e] - gt[e]);
+      const uint32_t yo = (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(t, cc & 7);
+      split8_store(sm + PS_YHI + yo, sm + PS_YLO + yo, v);
+    }
+  }
+  // (K o gamma)^T, the B operand of W: row j, two threads per row (32 tokens each)
+  {
+    const int j = tid & (D - 1), half = tid >> 7;
+#pragma unroll
+    for (int sc = 4 * half; sc < 4 * half + 4; ++sc) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int s2 = 8 * sc + e;
+        v[e] = __bfloat162float(sK[s2 * D + j]) * __expf(sG[s2 * D + j]);
+      }
+      split8_store(sm + PS_KPHI + tc::sw128_chunk(j, sc), sm + PS_KPLO + tc::sw128_chunk(j, sc), v);
+    }
+  }
+  if (tid < D) reinterpret_cast<float*>(rec + REC_GAMMA)[tid] = __expf(sG[(C - 1) * D + tid]);
+
+  // Gram matrices in TMEM columns 0..63: lanes 0..63 = A rows (before beta), lanes 64..127 = P rows
+  if (ok && !slow) {
+    tc::fence_proxy_async();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      issue_gram(sm, tm, 0, 64);
+      tc::commit(bar);
+    }
+    ok = __syncthreads_and(tc::bar_wait(bar, 0));
+  } else if (ok) {
+    for (int e = tid; e < C * 16; e += PREP_NT) {
+      const int s = e >> 4;
+      build_y_chunk(sm, s, e & 15, (s & ~15) + 15);
+    }
+    for (int b = 0; b < 4; ++b) {
+      for (int e = tid; e < 128 * 16; e += PREP_NT) build_x_chunk(sm, e >> 4, e & 15, 16 * b + 15, 16 * b);
+      tc::fence_proxy_async();
+      __syncthreads();
+      if (tid == 0) {
+        tc::fence_after_sync();
+        issue_gram(sm, tm + 16 * b, 16 * b, 16);
+        tc::commit(bar);
+      }
+      ok = __syncthreads_and(tc::bar_wait(bar, b & 1));  // block-uniform, so no thread leaves the loop alone
+      if (!ok) break;
+    }
+  }
+
+  if (ok) {
+    tc::fence_after_sync();
+    if (warp < 4) {  // A (beta, strictly lower) to shared memory; P (lower incl. diagonal) to the record
+      float v[64];
+      const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16);
+      tc::tmem_ld32(trow, v);
+      tc::tmem_ld32(trow + 32, v + 32);
+      if (tid < 64) {
+        const int t = tid;
+        const float bt = sbeta[t];
+#pragma unroll
+        for (int s = 0; s < 64; s += 4) {
+          float4 r;
+          r.x = s + 0 < t ? bt * v[s + 0] : 0.f;
+          r.y = s + 1 < t ? bt * v[s + 1] : 0.f;
+          r.z = s + 2 < t ? bt * v[s + 2] : 0.f;
+          r.w = s + 3 < t ? bt * v[s + 3] : 0.f;
+          *reinterpret_cast<float4*>(sA + t * 64 + s) = r;
+        }
+      } else {
+        const int t = tid - 64;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          float pv[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) pv[e] = 8 * cc + e <= t ? v[8 * cc + e] : 0.f;
+          split8_store(rec + REC_PHI + tc::sw128_chunk(t, cc), rec + REC_PLO + tc::sw128_chunk(t, cc), pv);
+        }
+      }
+    } else {  // V^T operand (raw bf16) and the (K o exp(G_C - G))^T record tile, one row per thread
+      const int c = tid - 128;
+#pragma unroll
+      for (int sc = 0; sc < 8; ++sc) {
+        __nv_bfloat16 vv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vv[e] = reinterpret_cast<const __nv_bfloat16*>(sm + PS_V)[(8 * sc + e) * D + c];
+        *reinterpret_cast<uint4*>(sm + PS_VT + tc::sw128_chunk(c, sc)) = pack8(vv);
+      }
+      const float gc = sG[(C - 1) * D + c];
+#pragma unroll
+      for (int sc = 0; sc < 8; ++sc) {
+        float kv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int s = 8 * sc + e;
+          kv[e] = __bfloat162float(sK[s * D + c]) * __expf(gc - sG[s * D + c]);
+        }
+        split8_store(rec + REC_KHHI + tc::sw128_chunk(c, sc), rec + REC_KHLO + tc::sw128_chunk(c, sc), kv);
+      }
+    }
+  }
+  __syncthreads();
+
+  if (ok) {
+    // T = (I + A)^-1, blocked by 16: diagonal blocks by forward substitution (threads 0..63, one column each)
+    if (tid < 64) {
+      const int b = tid >> 4, cc = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < r; ++u) acc = fmaf(sA[(16 * b + r) * 64 + 16 * b + u], x[u], acc);
+        x[r] = r == cc ? 1.f : (r < cc ? 0.f : -acc);
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sT[(16 * b + r) * 64 + 16 * b + cc] = x[r];
+    }
+    __syncthreads();
+    // off-diagonal blocks by distance d: Z = sum_k A_ik T_kj (kept in the unused upper block (j, i)),
+    // then T_ij = -T_ii Z
+#pragma unroll 1
+    for (int d = 1; d < 4; ++d) {
+      const int nb = 4 - d;
+      for (int o = tid; o < nb * 256; o += PREP_NT) {
+        const int bi = d + (o >> 8), bj = bi - d, r = (o >> 4) & 15, c = o & 15;
+        float acc = 0.f;
+        for (int bk = bj; bk < bi; ++bk)
+#pragma unroll
+          for (int u = 0; u < 16; ++u)
+            acc = fmaf(sA[(16 * bi + r) * 64 + 16 * bk + u], sT[(16 * bk + u) * 64 + 16 * bj + c], acc);
+        sT[(16 * bj + r) * 64 + 16 * bi + c] = acc;
+      }
+      __syncthreads();
+      for (int o = tid; o < nb * 256; o += PREP_NT) {
+        const int bi = d + (o >> 8), bj = bi - d, r = (o >> 4) & 15, c = o & 15;
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          if (u <= r) acc = fmaf(sT[(16 * bi + r) * 64 + 16 * bi + u], sT[(16 * bj + u) * 64 + 16 * bi + c], acc);
+        sT[(16 * bi + r) * 64 + 16 * bj + c] = -acc;
+      }
+      __syncthreads();
+    }
+    // T diag(beta) as the A operand (lower triangle only)
+    for (int task = tid; task < C * 8; task += PREP_NT) {
+      const int t = task >> 3, cc = task & 7;
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int s = 8 * cc + e;
+        v[e] = s <= t ? sT[t * 64 + s] * sbeta[s] : 0.f;
+      }
+      split8_store(sm + PS_TBHI + tc::sw128_chunk(t, cc), sm + PS_TBLO + tc::sw128_chunk(t, cc), v);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      issue_wu(sm, tm);
+      tc::commit(bar + 1);
+    }
+    ok = __syncthreads_and(tc::bar_wait(bar + 1, 0));
+  }
+
+  if (ok) {
+    // W rows t of the stacked B operand and U~ rows t; M = 64 accumulator rows sit in lanes 0..15 of each
+    // 32-lane quarter.  Warps w and w + 4 share a quarter and split the 128 columns.
+    tc::fence_after_sync();
+    const int q = warp & 3, half = warp >> 2, l = tid & 31;
+    const uint32_t trow = tm + ((uint32_t)(q * 32) << 16);
+    float w[64], u[64];
+    tc::tmem_ld32(trow + 64 * half, w);
+    tc::tmem_ld32(trow + 64 * half + 32, w + 32);
+    tc::tmem_ld32(trow + 128 + 64 * half, u);
+    tc::tmem_ld32(trow + 128 + 64 * half + 32, u + 32);
+    if (l < 16) {
+      const int t = 16 * q + l;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint32_t o = (uint32_t)half * 16384u + tc::sw128_chunk(t, cc);
+        split8_store(rec + REC_B1HI + o, rec + REC_B1LO + o, w + 8 * cc);
+      }
+      float4* U = reinterpret_cast<float4*>(rec + REC_U + ((size_t)t * D + 64 * half) * 4);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) U[e] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+    }
+  } else if (tid == 0) {
+    flag_status(a.status, KDA_DEV_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tm, 256);
+}
+
+// ---------------------------------------------------------------- chain
+
+constexpr uint32_t COL_D1 = 0;     // [W S | Q S + P U]^T: 128 columns
+constexpr uint32_t COL_D2 = 128;   // S^T (fp32 state): 128 columns
+constexpr uint32_t COL_STHI = 256; // S^T as the A operand, bf16 pairs: 64 columns each
+constexpr uint32_t COL_STLO = 320;
+constexpr uint32_t COL_UTHI = 384; // U^T as the A operand: 32 columns each
+constexpr uint32_t COL_UTLO = 416;
+
+constexpr uint32_t CS_GAMMA = 2 * REC_STAGE;      // gamma [2][128] fp32
+constexpr uint32_t CS_BAR = CS_GAMMA + 1024;      // full[2], mma1, mma2
+constexpr uint32_t CS_SLOT = CS_BAR + 32;
+constexpr uint32_t CS_BYTES = CS_SLOT + 16 + 1024;
+
+enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2 };
+
+template <typename Tout, int MODE>
+__global__ void __launch_bounds__(128, 1) tc_chain_kernel(const PrefillArgs a, const uint8_t* __restrict__ ws) {
+  constexpr bool WANT_O = MODE != MODE_FRAG;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  float* sgam = reinterpret_cast<float*>(sm + CS_GAMMA);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + CS_BAR);
+  uint64_t* bar1 = full + 2;
+  uint64_t* bar2 = full + 3;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CS_SLOT);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tile = (MODE == MODE_FRAG) ? (blockIdx.x & 1) : 0;
+  const int h = (MODE == MODE_FRAG) ? (blockIdx.x >> 1) : blockIdx.x;
+  const int p = blockIdx.y, i = blockIdx.z;
+
+  const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
+  if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
+    return;
+  }
+  int64_t t0 = s0, t1 = s1;
+  if (MODE != MODE_PLAIN) {
+    t0 = s0 + (int64_t)p * a.seg_len;
+    t1 = t0 + a.seg_len < s1 ? t0 + a.seg_len : s1;
+    if (MODE == MODE_FRAG) {
+      if (t1 >= s1) return;
+    } else if (t0 >= s1 && !(p == 0 && s1 == s0)) {
+      return;
+    }
+  }
+  const bool writes_pool = (MODE == MODE_PLAIN) || (MODE == MODE_SEGOUT && t1 == s1);
+  const bool reads_pool = (MODE == MODE_PLAIN) && !a.init_zero;
+  int slot = 0;
+  if (writes_pool || reads_pool) {
+    slot = a.slot_ids[i];
+    if (slot < 0 || slot >= a.num_slots) {
+      if (tid == 0) flag_status(a.status, KDA_DEV_SLOT_OOB);
+      return;
+    }
+  }
+  const int nch = (int)((t1 - t0 + C - 1) / C);
+  const int c_first = (int)((t0 - s0) / C);
+  const size_t head_elems = (size_t)D * D;
+
+  if (warp == 0) tc::tmem_alloc(tslot, 512);
+  if (tid == 0) {
+    for (int b = 0; b < 4; ++b) tc::bar_init(full + b, 1);
+    tc::bar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *tslot;
+  const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16);
+
+  auto rec_of = [&](int cc) -> const uint8_t* {
+    const int64_t tc0 = s0 + (int64_t)(c_first + cc) * C;
+    return ws + ((size_t)(tc0 / C + i) * a.H + h) * REC_BYTES;
+  };
+  auto issue = [&](int cc) {
+    const int st = cc & 1;
+    const uint8_t* rec = rec_of(cc);
+    tc::bar_arrive_expect_tx(full + st, REC_STAGE + 512);
+    tc::bulk_g2s(sm + st * REC_STAGE, rec, REC_STAGE, full + st);
+    tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
+  };
+  int issued = nch < 2 ? nch : 2;  // chunks whose copies have been issued (thread 0's view)
+  if (tid == 0) {
+    if (nch > 0) issue(0);
+    if (nch > 1) issue(1);
+  }
+
+  // initial state, transposed into tensor memory: lane c holds column c of S
+  {
+    const float* src = nullptr;
+    if (MODE == MODE_PLAIN && !a.init_zero) src = a.pool + ((size_t)slot * a.H + h) * head_elems;
+    if (MODE == MODE_SEGOUT) src = a.entry + (((size_t)i * a.P + p) * a.H + h) * head_elems;
+#pragma unroll 1
+    for (int jb = 0; jb < 4; ++jb) {
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = 32 * jb + e;
+        v[e] = src ? src[(size_t)j * D + tid] : ((MODE == MODE_FRAG && tile == 1 && j == tid) ? 1.f : 0.f);
+      }
+      tc::tmem_st32f(trow + COL_D2 + 32 * jb, v);
+    }
+    tc::tmem_wait_st();
+  }
+
+  const bool zero_u = (MODE == MODE_FRAG && tile == 1);  // transition columns: V = 0
+  const int64_t len = s1 - s0;
+  const int64_t every = a.snap_every_tokens;
+  const int64_t n_snap = (a.extra_pool && every > 0) ? len / every : 0;
+  bool ok = true;
+  int cc = 0;
+#pragma unroll 1
+  for (; cc < nch && ok; ++cc) {
+    const int st = cc & 1;
+    const uint32_t fpar = (uint32_t)(cc >> 1) & 1u, mpar = (uint32_t)cc & 1u;
+    const uint8_t* rec = rec_of(cc);
+    const int64_t tc0 = s0 + (int64_t)(c_first + cc) * C;
+    const int nv = (int)((t1 - tc0) < C ? (t1 - tc0) : C);
+    float ut[C];
+    {
+      const float* U = reinterpret_cast<const float*>(rec + REC_U);
+#pragma unroll
+      for (int t = 0; t < C; ++t) ut[t] = zero_u ? 0.f : U[t * D + tid];
+    }
+    ok = __syncthreads_and(tc::bar_wait(full + st, fpar));
+    if (!ok) break;
+    // split the state into the MMA operand, then apply this chunk's decay to the fp32 copy
+#pragma unroll 1
+    for (int jb = 0; jb < 4; ++jb) {
+      float s[32];
+      tc::tmem_ld32(trow + COL_D2 + 32 * jb, s);
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        tc::split2(s[2 * e], h0, l0);
+        tc::split2(s[2 * e + 1], h1, l1);
+        hi[e] = tc::pack2(h0, h1);
+        lo[e] = tc::pack2(l0, l1);
+      }
+      tc::tmem_st16(trow + COL_STHI + 16 * jb, hi);
+      tc::tmem_st16(trow + COL_STLO + 16 * jb, lo);
+      const float* gm = sgam + 128 * st + 32 * jb;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) s[e] *= gm[e];
+      tc::tmem_st32f(trow + COL_D2 + 32 * jb, s);
+    }
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+    __syncthreads();
+    const uint32_t sbase = tc::smem_u32(sm + st * REC_STAGE);
+    if (tid == 0) {
+      tc::fence_after_sync();
+      // D1 = S^T [W; Q o gamma]^T  (N = 128 with outputs, 64 without)
+      constexpr int N1 = WANT_O ? 128 : 64;
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
+        const uint32_t bb = sbase + (part == 1 ? REC_B1LO : REC_B1HI);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_ts(tm + COL_D1, acol + ks * 8,
+                     tc::sdesc(bb + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u), tc::idesc_bf16(128, N1),
+                     (part | ks) != 0);
+      }
+      tc::commit(bar1);
+    }
+    ok = __syncthreads_and(tc::bar_wait(bar1, mpar));
+    if (!ok) break;
+    tc::fence_after_sync();
+    // U = U~ - W S, split into the A operand of the next two products
+    {
+      float w[C];
+      tc::tmem_ld32(trow + COL_D1, w);
+      tc::tmem_ld32(trow + COL_D1 + 32, w + 32);
+      uint32_t hi[32], lo[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        __nv_bfloat16 h0, l0, h1, l1;
+        tc::split2(ut[2 * e] - w[2 * e], h0, l0);
+        tc::split2(ut[2 * e + 1] - w[2 * e + 1], h1, l1);
+        hi[e] = tc::pack2(h0, h1);
+        lo[e] = tc::pack2(l0, l1);
+      }
+      tc::tmem_st16(trow + COL_UTHI, hi);
+      tc::tmem_st16(trow + COL_UTHI + 16, hi + 16);
+      tc::tmem_st16(trow + COL_UTLO, lo);
+      tc::tmem_st16(trow + COL_UTLO + 16, lo + 16);
+    }
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {
+        const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
+        if (WANT_O) {  // D1[:, 64:128] += U^T P^T
+          const uint32_t pb = sbase + (part == 1 ? REC_PLO : REC_PHI);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_ts(tm + COL_D1 + 64, acol + ks * 8, tc::sdesc(pb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 64), 1);
+        }
+        // D2 += U^T (K o exp(G_C - G))
+        const uint32_t kb = sbase + (part == 1 ? REC_KHLO : REC_KHHI);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_ts(tm + COL_D2, acol + ks * 8, tc::sdesc(kb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 128), 1);
+      }
+      tc::commit(bar2);
+    }
+    ok = __syncthreads_and(tc::bar_wait(bar2, mpar));
+    if (!ok) break;
+    tc::fence_after_sync();
+    if (tid == 0 && cc + 2 < nch) {
+      issue(cc + 2);
+      issued = cc + 3;
+    }
+    if (WANT_O) {
+      float o[C];
+      tc::tmem_ld32(trow + COL_D1 + 64, o);
+      tc::tmem_ld32(trow + COL_D1 + 96, o + 32);
+      Tout* out = static_cast<Tout*>(a.out) + ((size_t)tc0 * a.H + h) * D + tid;
+#pragma unroll
+      for (int t = 0; t < C; ++t)
+        if (t < nv) out[(size_t)t * a.H * D] = from_f32<Tout>(o[t]);
+      // ping-pong snapshot at this chunk's end, if it is one of the sequence's last two
+      if (n_snap > 0 && nv == C) {
+        const int64_t pos = tc0 + C - s0;
+        if (pos % every == 0 && pos / every + 1 >= n_snap) {
+          const int64_t m = pos / every;
+          const int es = a.extra_slots[2 * (size_t)i + ((m - 1) & 1)];
+          if (es >= 0 && es < a.num_extra) {
+            float* dst = a.extra_pool + ((size_t)es * a.H + h) * head_elems + tid;
+#pragma unroll 1
+            for (int jb = 0; jb < 4; ++jb) {
+              float s[32];
+              tc::tmem_ld32(trow + COL_D2 + 32 * jb, s);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) dst[(size_t)(32 * jb + e) * D] = s[e];
+            }
+          } else if (tid == 0) {
+            flag_status(a.status, KDA_DEV_SLOT_OOB);
+          }
+        }
+      }
+    }
+  }
+
+  if (ok) {
+    float* dst = nullptr;
+    size_t ld = D;
+    if (MODE == MODE_FRAG) {
+      dst = a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2 + (size_t)tile * D + tid;
+      ld = 2 * D;
+    } else if (writes_pool) {
+      dst = a.pool + ((size_t)slot * a.H + h) * head_elems + tid;
+    }
+    if (dst) {
+#pragma unroll 1
+      for (int jb = 0; jb < 4; ++jb) {
+        float s[32];
+        tc::tmem_ld32(trow + COL_D2 + 32 * jb, s);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dst[(size_t)(32 * jb + e) * ld] = s[e];
+      }
+    }
+    if (tid == 0 && tile == 0) add_work(a.status, (int32_t)(t1 - t0));
+  } else if (tid == 0) {
+    flag_status(a.status, KDA_DEV_TIMEOUT);
+    // wait (bounded) for the copies still in flight into this CTA's shared memory before it is released
+    for (int q = cc; q < issued; ++q) tc::bar_wait(full + (q & 1), (uint32_t)(q >> 1) & 1u);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
+template <typename Tout, int MODE>
+cudaError_t launch_chain_t(const PrefillArgs& a, const uint8_t* ws, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(tc_chain_kernel<Tout, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)CS_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(MODE == MODE_FRAG ? 2 * a.H : a.H, MODE == MODE_PLAIN ? 1 : a.P, a.N);
+  tc_chain_kernel<Tout, MODE><<<grid, 128, CS_BYTES, s>>>(a, ws);
+  return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_chain(const PrefillArgs& a, const uint8_t* ws, cudaStream_t s) {
+  return a.out_bf16 ? launch_chain_t<bf16, MODE>(a, ws, s) : launch_chain_t<float, MODE>(a, ws, s);
+}
+
+}  // namespace
+
+bool tc_supported(const PrefillArgs& a) { return a.in_bf16 && a.d == D; }
+
+size_t tc_record_bytes(int64_t T, int N, int H) {
+  return ((size_t)((T + C - 1) / C) + (size_t)N) * (size_t)H * REC_BYTES;
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [T][H][128] token-major tensor, box = 128 channels x 1 head x 64 tokens, no swizzle, zero fill outside
+bool encode_tokens(CUtensorMap* map, const void* base, bool f32, int64_t T, int H) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[2] = {D * es, (cuuint64_t)H * D * es};
+  const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t s) {
+  if (a.max_seqlen <= 0 || a.T <= 0) return cudaSuccess;
+  if (a.T > 0x7fffffff) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
+  PrepMaps maps;
+  if (!encode_tokens(&maps.q, a.q, false, a.T, a.H) || !encode_tokens(&maps.k, a.k, false, a.T, a.H) ||
+      !encode_tokens(&maps.v, a.v, false, a.T, a.H) || !encode_tokens(&maps.g, a.g, true, a.T, a.H))
+    return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((a.max_seqlen + C - 1) / C), a.H, a.N);
+  tc_prep_kernel<<<grid, PREP_NT, PS_BYTES, s>>>(a, records, maps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_chain_plain(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
+  return launch_chain<MODE_PLAIN>(a, records, s);
+}
+cudaError_t launch_tc_chain_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
+  return launch_chain<MODE_FRAG>(a, records, s);
+}
+cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
+  return launch_chain<MODE_SEGOUT>(a, records, s);
+}
+
+}  // namespace kda

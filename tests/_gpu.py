@@ -64,8 +64,13 @@ class PrefillRun:
     def args(self):
         return (self.q, self.k, self.v, self.g, self.beta, self.cu, self.max_seqlen, self.pool, self.slots, self.out)
 
+    def varlen_workspace(self, kda):
+        n = kda.kda_prefill_workspace_size(*self.args(),
+                                           **{k: v for k, v in self.common().items() if k != "dev_status"})
+        return torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
+
     def run_varlen(self, kda):
-        kda.kda_prefill_varlen(*self.args(), **self.common())
+        kda.kda_prefill_varlen(*self.args(), workspace=self.varlen_workspace(kda), **self.common())
         torch.cuda.synchronize()
         return self
 

@@ -78,10 +78,20 @@ def test_prefill_validation(lib):
     assert lib.kda_prefill_segmented(ctypes.byref(a), 100, None) == 1
     assert lib.kda_prefill_segmented(ctypes.byref(a), 64, None) == 3
     need = lib.kda_segmented_workspace_size(ctypes.byref(a), 64)
-    # frag [N][P][H][dk][dv+dk] + entry [N][P][H][dk][dv], fp32, P = ceil(64/64) = 1
-    assert need == 2 * 128 * 256 * 4 + 2 * 128 * 128 * 4
+    # bf16, d = 128: chunk records (ceil(T/64) + N) * H * 148480, then frag [N][P][H][dk][dv+dk] and
+    # entry [N][P][H][dk][dv] in fp32 with P = ceil(64/64) = 1
+    records = (1 + 1) * 2 * 148480
+    assert lib.kda_prefill_workspace_size(ctypes.byref(a)) == records
+    assert need == records + 2 * 128 * 256 * 4 + 2 * 128 * 128 * 4
+    a.in_dtype = 0  # fp32 inputs take the token-sequential path: no records
+    assert lib.kda_prefill_workspace_size(ctypes.byref(a)) == 0
+    assert lib.kda_segmented_workspace_size(ctypes.byref(a), 64) == 2 * 128 * 256 * 4 + 2 * 128 * 128 * 4
+    a.in_dtype = 1
     a.workspace, a.workspace_bytes = 16, need - 1
     assert lib.kda_prefill_segmented(ctypes.byref(a), 64, None) == 3
+    # the tensor-core varlen path needs its records too
+    a.workspace, a.workspace_bytes = 0, 0
+    assert lib.kda_prefill_varlen(ctypes.byref(a), None) == 3
     a.N = -1
     assert lib.kda_prefill_varlen(ctypes.byref(a), None) == 1
 

@@ -85,6 +85,23 @@ def test_segmented_matches_oracle(cuda, case, segment_len):
     _check_against_oracle(run, ref, TOL[prob.in_dtype])
 
 
+@pytest.mark.parametrize("path", ["varlen", "segmented"])
+def test_decay_floor_uses_block_references(cuda, path):
+    """Log-decay at the floor g = -5 in some chunks: their decay span exceeds 80, so the pair decays use
+    16-token block references; other chunks keep the single-reference form."""
+    prob = synth.varlen(seed=36, H=2, d=128, num_slots=5, num_extra=6, snapshot_every_chunks=1,
+                        lengths=[150, 64, 200])
+    g = prob.g.copy()
+    g[20:100] = -5.0         # spans two chunks of the first sequence
+    g[214:230, 1] = -5.0     # one head only, inside the second sequence's chunk
+    prob.g = g
+    run = PrefillRun(prob)
+    run = run.run_varlen(cuda) if path == "varlen" else run.run_segmented(cuda, 128)
+    ref = oracle_prefill(prob)
+    assert status(run.status)[0] == 0
+    _check_against_oracle(run, ref, TOL[synth.BF16])
+
+
 def test_init_zero_and_bf16_output(cuda):
     prob = synth.varlen(seed=33, H=2, d=128, num_slots=6, num_extra=4, snapshot_every_chunks=0,
                         lengths=[100, 250])
@@ -149,7 +166,7 @@ def test_bad_cu_seqlens_flagged(cuda):
     run = PrefillRun(prob)
     run.cu = dev(np.array([0, 50, 40], np.int32))  # decreasing: sequence 1 is invalid
     pool0 = run.pool.clone()
-    kda.kda_prefill_varlen(*run.args(), **run.common())
+    kda.kda_prefill_varlen(*run.args(), workspace=run.varlen_workspace(kda), **run.common())
     torch.cuda.synchronize()
     flags, work = status(run.status)
     assert flags & kda.KDA_DEV_SEQ_OOB

@@ -14,12 +14,12 @@ from tests._gpu import PrefillRun, host, rel_err, status
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
-SEGMENT = 1024  # one 8192-token sequence, H = 12, d = 128: 18 MiB of scratch
+SEGMENT = 256  # one 1024-token sequence, H = 4, d = 128: about 13 MiB of scratch
 
 
 def test_noalloc_matches_workspace_entry_point_twice(cuda):
     kda = cuda
-    prob = synth.prefill_8k()
+    prob = synth.prefill_8k(T=1024, H=4)
     ref = PrefillRun(prob).run_segmented(kda, SEGMENT)  # the existing entry point, caller workspace
     assert status(ref.status)[0] == 0
     for call in range(2):  # two calls in a row: the second reuses the array as the first left it
@@ -36,7 +36,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(cuda):
     prob = synth.prefill_8k(T=2048, H=12)
     run = PrefillRun(prob)
     pool0 = run.pool.clone()
-    # 64-token segments: 32 segments x 12 heads x 192 KB of scratch = 72 MiB > 32 MiB
+    # 2048 tokens x 12 heads: the chunk operand records alone take about 58 MiB > 32 MiB
     with pytest.raises(kda.KdaError) as e:
         kda.kda_prefill_segmented_noalloc(*run.args(), 64, **run.common())
     assert e.value.code == 3  # KDA_ERR_WORKSPACE
