@@ -517,31 +517,39 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 
 // ---------------------------------------------------------------- chain
 
-constexpr uint32_t COL_D1 = 0;     // [W S | Q S + P U]^T: 128 columns
-constexpr uint32_t COL_D2 = 128;   // S^T (fp32 state): 128 columns
-constexpr uint32_t COL_STHI = 256; // S^T as the A operand, bf16 pairs: 64 columns each
-constexpr uint32_t COL_STLO = 320;
-constexpr uint32_t COL_UTHI = 384; // U^T as the A operand: 32 columns each
-constexpr uint32_t COL_UTLO = 416;
+// tensor memory columns of the chain kernel (all 512 allocated)
+constexpr uint32_t COL_WS = 0;      // (W S)^T: 64 columns (tokens)
+constexpr uint32_t COL_O = 64;      // (Q S + P U)^T, double-buffered by chunk parity: 2 x 64 columns
+constexpr uint32_t COL_S = 192;     // S^T, the fp32 state: 128 columns
+constexpr uint32_t COL_STHI = 320;  // S^T as the A operand, bf16 pairs: 64 columns each
+constexpr uint32_t COL_STLO = 384;
+constexpr uint32_t COL_UTHI = 448;  // U^T as the A operand: 32 columns each
+constexpr uint32_t COL_UTLO = 480;
 
 constexpr uint32_t CS_GAMMA = 2 * REC_STAGE;      // gamma [2][128] fp32
-constexpr uint32_t CS_BAR = CS_GAMMA + 1024;      // full[2], mma1, mma2
-constexpr uint32_t CS_SLOT = CS_BAR + 32;
+constexpr uint32_t CS_BAR = CS_GAMMA + 1024;      // full[2], ws, state, out[2]
+constexpr uint32_t CS_SLOT = CS_BAR + 64;
 constexpr uint32_t CS_BYTES = CS_SLOT + 16 + 1024;
+constexpr int CHAIN_NT = 256;
 
 enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2 };
 
+// Two warpgroups: thread (value channel c = TMEM lane, warpgroup wg) handles half of every TMEM row it
+// touches.  Per chunk: split the state (E1) -> [W; Q o gamma] S -> U = U~ - W S (E2) -> state update
+// K^T U and output P U; the outputs of a chunk are read back while the next chunk's first product runs.
 template <typename Tout, int MODE>
-__global__ void __launch_bounds__(128, 1) tc_chain_kernel(const PrefillArgs a, const uint8_t* __restrict__ ws) {
+__global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs a, const uint8_t* __restrict__ ws) {
   constexpr bool WANT_O = MODE != MODE_FRAG;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   float* sgam = reinterpret_cast<float*>(sm + CS_GAMMA);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + CS_BAR);
-  uint64_t* bar1 = full + 2;
-  uint64_t* bar2 = full + 3;
+  uint64_t* bar_ws = full + 2;
+  uint64_t* bar_st = full + 3;
+  uint64_t* bar_o = full + 4;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CS_SLOT);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, wg = warp >> 2;
+  const int c = tid & 127;  // value channel = TMEM lane
   const int tile = (MODE == MODE_FRAG) ? (blockIdx.x & 1) : 0;
   const int h = (MODE == MODE_FRAG) ? (blockIdx.x >> 1) : blockIdx.x;
   const int p = blockIdx.y, i = blockIdx.z;
@@ -577,27 +585,28 @@ __global__ void __launch_bounds__(128, 1) tc_chain_kernel(const PrefillArgs a, c
 
   if (warp == 0) tc::tmem_alloc(tslot, 512);
   if (tid == 0) {
-    for (int b = 0; b < 4; ++b) tc::bar_init(full + b, 1);
+    for (int b = 0; b < 6; ++b) tc::bar_init(full + b, 1);
     tc::bar_fence_init();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = *tslot;
-  const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16);
+  const uint32_t trow = tm + ((uint32_t)((warp & 3) * 32) << 16);
 
+  auto chunk_t0 = [&](int cc) -> int64_t { return s0 + (int64_t)(c_first + cc) * C; };
   auto rec_of = [&](int cc) -> const uint8_t* {
-    const int64_t tc0 = s0 + (int64_t)(c_first + cc) * C;
-    return ws + ((size_t)(tc0 / C + i) * a.H + h) * REC_BYTES;
+    return ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * REC_BYTES;
   };
+  int issued = 0;  // chunks whose stage copies have been issued (thread 0's view)
   auto issue = [&](int cc) {
     const int st = cc & 1;
     const uint8_t* rec = rec_of(cc);
     tc::bar_arrive_expect_tx(full + st, REC_STAGE + 512);
     tc::bulk_g2s(sm + st * REC_STAGE, rec, REC_STAGE, full + st);
     tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
+    issued = cc + 1;
   };
-  int issued = nch < 2 ? nch : 2;  // chunks whose copies have been issued (thread 0's view)
   if (tid == 0) {
     if (nch > 0) issue(0);
     if (nch > 1) issue(1);
@@ -609,59 +618,96 @@ __global__ void __launch_bounds__(128, 1) tc_chain_kernel(const PrefillArgs a, c
     if (MODE == MODE_PLAIN && !a.init_zero) src = a.pool + ((size_t)slot * a.H + h) * head_elems;
     if (MODE == MODE_SEGOUT) src = a.entry + (((size_t)i * a.P + p) * a.H + h) * head_elems;
 #pragma unroll 1
-    for (int jb = 0; jb < 4; ++jb) {
+    for (int jb = 0; jb < 2; ++jb) {
+      const int j0 = 64 * wg + 32 * jb;
       float v[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const int j = 32 * jb + e;
-        v[e] = src ? src[(size_t)j * D + tid] : ((MODE == MODE_FRAG && tile == 1 && j == tid) ? 1.f : 0.f);
+        const int j = j0 + e;
+        v[e] = src ? src[(size_t)j * D + c] : ((MODE == MODE_FRAG && tile == 1 && j == c) ? 1.f : 0.f);
       }
-      tc::tmem_st32f(trow + COL_D2 + 32 * jb, v);
+      tc::tmem_st32f(trow + COL_S + j0, v);
     }
     tc::tmem_wait_st();
   }
 
-  const bool zero_u = (MODE == MODE_FRAG && tile == 1);  // transition columns: V = 0
+  // state S^T -> global [j][c] rows j in this thread's half (dst points at column c)
+  auto store_state = [&](float* dst, size_t ld) {
+#pragma unroll 1
+    for (int jb = 0; jb < 2; ++jb) {
+      const int j0 = 64 * wg + 32 * jb;
+      float s[32];
+      tc::tmem_ld32(trow + COL_S + j0, s);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dst[(size_t)(j0 + e) * ld] = s[e];
+    }
+  };
   const int64_t len = s1 - s0;
   const int64_t every = a.snap_every_tokens;
   const int64_t n_snap = (a.extra_pool && every > 0) ? len / every : 0;
+  // ping-pong snapshot of the state after chunk cc (if its end is one of the sequence's last two)
+  auto snapshot = [&](int cc) {
+    if (n_snap <= 0) return;
+    const int64_t end = chunk_t0(cc) + C;
+    if (end > t1) return;
+    const int64_t pos = end - s0;
+    if (pos % every != 0 || pos / every + 1 < n_snap) return;
+    const int64_t m = pos / every;
+    const int es = a.extra_slots[2 * (size_t)i + ((m - 1) & 1)];
+    if (es >= 0 && es < a.num_extra)
+      store_state(a.extra_pool + ((size_t)es * a.H + h) * head_elems + c, D);
+    else if (tid == 0)
+      flag_status(a.status, KDA_DEV_SLOT_OOB);
+  };
+  // outputs of chunk cc from its accumulator (this thread's 32 tokens)
+  auto emit = [&](int cc) {
+    const int64_t tc0 = chunk_t0(cc);
+    const int nv = (int)((t1 - tc0) < C ? (t1 - tc0) : C);
+    float o[32];
+    tc::tmem_ld32(trow + COL_O + 64 * (cc & 1) + 32 * wg, o);
+    Tout* out = static_cast<Tout*>(a.out) + ((size_t)tc0 * a.H + h) * D + c;
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (32 * wg + e < nv) out[(size_t)(32 * wg + e) * a.H * D] = from_f32<Tout>(o[e]);
+  };
+
+  const bool zero_u = (MODE == MODE_FRAG && tile == 1);  // transition columns: V = 0
   bool ok = true;
   int cc = 0;
 #pragma unroll 1
-  for (; cc < nch && ok; ++cc) {
+  for (; cc < nch; ++cc) {
     const int st = cc & 1;
-    const uint32_t fpar = (uint32_t)(cc >> 1) & 1u, mpar = (uint32_t)cc & 1u;
-    const uint8_t* rec = rec_of(cc);
-    const int64_t tc0 = s0 + (int64_t)(c_first + cc) * C;
-    const int nv = (int)((t1 - tc0) < C ? (t1 - tc0) : C);
-    float ut[C];
+    const uint32_t par = (uint32_t)cc & 1u;
+    float ut[32];
     {
-      const float* U = reinterpret_cast<const float*>(rec + REC_U);
+      const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D + c;
 #pragma unroll
-      for (int t = 0; t < C; ++t) ut[t] = zero_u ? 0.f : U[t * D + tid];
+      for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D];
     }
-    ok = __syncthreads_and(tc::bar_wait(full + st, fpar));
+    bool w_ok = tc::bar_wait(full + st, (uint32_t)(cc >> 1) & 1u);
+    if (cc > 0) w_ok = w_ok && tc::bar_wait(bar_st, par ^ 1u);  // the previous chunk's state update
+    ok = __syncthreads_and(w_ok);
     if (!ok) break;
-    // split the state into the MMA operand, then apply this chunk's decay to the fp32 copy
+    tc::fence_after_sync();
+    if (cc > 0) {
+      snapshot(cc - 1);
+      if (!WANT_O && tid == 0 && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
+    }
+    // E1: split the state into the MMA operand, then apply this chunk's decay to the fp32 copy
 #pragma unroll 1
-    for (int jb = 0; jb < 4; ++jb) {
+    for (int jb = 0; jb < 2; ++jb) {
+      const int j0 = 64 * wg + 32 * jb;
       float s[32];
-      tc::tmem_ld32(trow + COL_D2 + 32 * jb, s);
+      tc::tmem_ld32(trow + COL_S + j0, s);
       uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        tc::split2(s[2 * e], h0, l0);
-        tc::split2(s[2 * e + 1], h1, l1);
-        hi[e] = tc::pack2(h0, h1);
-        lo[e] = tc::pack2(l0, l1);
-      }
-      tc::tmem_st16(trow + COL_STHI + 16 * jb, hi);
-      tc::tmem_st16(trow + COL_STLO + 16 * jb, lo);
-      const float* gm = sgam + 128 * st + 32 * jb;
+      for (int e = 0; e < 16; ++e) split_pair(s[2 * e], s[2 * e + 1], hi[e], lo[e]);
+      tc::tmem_st16(trow + COL_STHI + j0 / 2, hi);
+      tc::tmem_st16(trow + COL_STLO + j0 / 2, lo);
+      const float* gm = sgam + 128 * st + j0;
 #pragma unroll
       for (int e = 0; e < 32; ++e) s[e] *= gm[e];
-      tc::tmem_st32f(trow + COL_D2 + 32 * jb, s);
+      tc::tmem_st32f(trow + COL_S + j0, s);
     }
     tc::tmem_wait_st();
     tc::fence_before_sync();
@@ -669,41 +715,49 @@ __global__ void __launch_bounds__(128, 1) tc_chain_kernel(const PrefillArgs a, c
     const uint32_t sbase = tc::smem_u32(sm + st * REC_STAGE);
     if (tid == 0) {
       tc::fence_after_sync();
-      // D1 = S^T [W; Q o gamma]^T  (N = 128 with outputs, 64 without)
-      constexpr int N1 = WANT_O ? 128 : 64;
+      // (W S)^T = S^T W^T, then (Q o gamma S)^T into this chunk's output accumulator
 #pragma unroll
       for (int part = 0; part < 3; ++part) {
         const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
         const uint32_t bb = sbase + (part == 1 ? REC_B1LO : REC_B1HI);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc::mma_ts(tm + COL_D1, acol + ks * 8,
-                     tc::sdesc(bb + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u), tc::idesc_bf16(128, N1),
+          tc::mma_ts(tm + COL_WS, acol + ks * 8,
+                     tc::sdesc(bb + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u), tc::idesc_bf16(128, 64),
                      (part | ks) != 0);
       }
-      tc::commit(bar1);
+      tc::commit(bar_ws);
+      if (WANT_O) {
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
+          const uint32_t bb = sbase + (part == 1 ? REC_B1LO : REC_B1HI) + 64u * 128u;  // rows 64..127
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8,
+                       tc::sdesc(bb + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u),
+                       tc::idesc_bf16(128, 64), (part | ks) != 0);
+        }
+      }
     }
-    ok = __syncthreads_and(tc::bar_wait(bar1, mpar));
+    if (WANT_O && cc > 0) {  // the previous chunk's outputs, while this chunk's products run
+      ok = tc::bar_wait(bar_o + (st ^ 1), (uint32_t)((cc - 1) >> 1) & 1u);
+      tc::fence_after_sync();
+      if (ok) emit(cc - 1);
+      if (tid == 0 && ok && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
+    }
+    ok = __syncthreads_and(ok && tc::bar_wait(bar_ws, par));
     if (!ok) break;
     tc::fence_after_sync();
-    // U = U~ - W S, split into the A operand of the next two products
+    // E2: U = U~ - W S for this thread's 32 tokens, split into the A operand of the next two products
     {
-      float w[C];
-      tc::tmem_ld32(trow + COL_D1, w);
-      tc::tmem_ld32(trow + COL_D1 + 32, w + 32);
-      uint32_t hi[32], lo[32];
+      float w[32];
+      tc::tmem_ld32(trow + COL_WS + 32 * wg, w);
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        __nv_bfloat16 h0, l0, h1, l1;
-        tc::split2(ut[2 * e] - w[2 * e], h0, l0);
-        tc::split2(ut[2 * e + 1] - w[2 * e + 1], h1, l1);
-        hi[e] = tc::pack2(h0, h1);
-        lo[e] = tc::pack2(l0, l1);
-      }
-      tc::tmem_st16(trow + COL_UTHI, hi);
-      tc::tmem_st16(trow + COL_UTHI + 16, hi + 16);
-      tc::tmem_st16(trow + COL_UTLO, lo);
-      tc::tmem_st16(trow + COL_UTLO + 16, lo + 16);
+      for (int e = 0; e < 16; ++e) split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
+      tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
+      tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
     }
     tc::tmem_wait_st();
     tc::fence_before_sync();
@@ -711,78 +765,44 @@ __global__ void __launch_bounds__(128, 1) tc_chain_kernel(const PrefillArgs a, c
     if (tid == 0) {
       tc::fence_after_sync();
 #pragma unroll
-      for (int part = 0; part < 3; ++part) {
+      for (int part = 0; part < 3; ++part) {  // state: S^T += U^T (K o exp(G_C - G))
         const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
-        if (WANT_O) {  // D1[:, 64:128] += U^T P^T
-          const uint32_t pb = sbase + (part == 1 ? REC_PLO : REC_PHI);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_ts(tm + COL_D1 + 64, acol + ks * 8, tc::sdesc(pb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 64), 1);
-        }
-        // D2 += U^T (K o exp(G_C - G))
         const uint32_t kb = sbase + (part == 1 ? REC_KHLO : REC_KHHI);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          tc::mma_ts(tm + COL_D2, acol + ks * 8, tc::sdesc(kb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 128), 1);
+          tc::mma_ts(tm + COL_S, acol + ks * 8, tc::sdesc(kb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 128), 1);
       }
-      tc::commit(bar2);
-    }
-    ok = __syncthreads_and(tc::bar_wait(bar2, mpar));
-    if (!ok) break;
-    tc::fence_after_sync();
-    if (tid == 0 && cc + 2 < nch) {
-      issue(cc + 2);
-      issued = cc + 3;
-    }
-    if (WANT_O) {
-      float o[C];
-      tc::tmem_ld32(trow + COL_D1 + 64, o);
-      tc::tmem_ld32(trow + COL_D1 + 96, o + 32);
-      Tout* out = static_cast<Tout*>(a.out) + ((size_t)tc0 * a.H + h) * D + tid;
+      tc::commit(bar_st);
+      if (WANT_O) {
 #pragma unroll
-      for (int t = 0; t < C; ++t)
-        if (t < nv) out[(size_t)t * a.H * D] = from_f32<Tout>(o[t]);
-      // ping-pong snapshot at this chunk's end, if it is one of the sequence's last two
-      if (n_snap > 0 && nv == C) {
-        const int64_t pos = tc0 + C - s0;
-        if (pos % every == 0 && pos / every + 1 >= n_snap) {
-          const int64_t m = pos / every;
-          const int es = a.extra_slots[2 * (size_t)i + ((m - 1) & 1)];
-          if (es >= 0 && es < a.num_extra) {
-            float* dst = a.extra_pool + ((size_t)es * a.H + h) * head_elems + tid;
-#pragma unroll 1
-            for (int jb = 0; jb < 4; ++jb) {
-              float s[32];
-              tc::tmem_ld32(trow + COL_D2 + 32 * jb, s);
+        for (int part = 0; part < 3; ++part) {  // outputs: O^T += U^T P^T
+          const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
+          const uint32_t pb = sbase + (part == 1 ? REC_PLO : REC_PHI);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) dst[(size_t)(32 * jb + e) * D] = s[e];
-            }
-          } else if (tid == 0) {
-            flag_status(a.status, KDA_DEV_SLOT_OOB);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, tc::sdesc(pb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 64), 1);
         }
+        tc::commit(bar_o + st);
       }
     }
   }
 
+  if (ok && nch > 0) {  // drain: the last chunk's state update and outputs
+    const int last = nch - 1;
+    bool w_ok = tc::bar_wait(bar_st, (uint32_t)last & 1u);
+    if (WANT_O) w_ok = w_ok && tc::bar_wait(bar_o + (last & 1), (uint32_t)(last >> 1) & 1u);
+    ok = __syncthreads_and(w_ok);
+    if (ok) {
+      tc::fence_after_sync();
+      snapshot(last);
+      if (WANT_O) emit(last);
+    }
+  }
   if (ok) {
-    float* dst = nullptr;
-    size_t ld = D;
-    if (MODE == MODE_FRAG) {
-      dst = a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2 + (size_t)tile * D + tid;
-      ld = 2 * D;
-    } else if (writes_pool) {
-      dst = a.pool + ((size_t)slot * a.H + h) * head_elems + tid;
-    }
-    if (dst) {
-#pragma unroll 1
-      for (int jb = 0; jb < 4; ++jb) {
-        float s[32];
-        tc::tmem_ld32(trow + COL_D2 + 32 * jb, s);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) dst[(size_t)(32 * jb + e) * ld] = s[e];
-      }
-    }
+    if (MODE == MODE_FRAG)
+      store_state(a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2 + (size_t)tile * D + c, 2 * D);
+    else if (writes_pool)
+      store_state(a.pool + ((size_t)slot * a.H + h) * head_elems + c, D);
     if (tid == 0 && tile == 0) add_work(a.status, (int32_t)(t1 - t0));
   } else if (tid == 0) {
     flag_status(a.status, KDA_DEV_TIMEOUT);
@@ -800,7 +820,7 @@ cudaError_t launch_chain_t(const PrefillArgs& a, const uint8_t* ws, cudaStream_t
                                        (int)CS_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(MODE == MODE_FRAG ? 2 * a.H : a.H, MODE == MODE_PLAIN ? 1 : a.P, a.N);
-  tc_chain_kernel<Tout, MODE><<<grid, 128, CS_BYTES, s>>>(a, ws);
+  tc_chain_kernel<Tout, MODE><<<grid, CHAIN_NT, CS_BYTES, s>>>(a, ws);
   return cudaGetLastError();
 }
 
