@@ -6,37 +6,109 @@
 // (v, k, gk, beta); the fold replays only the accepted prefix in place with the stored gate values, so
 // the rebuilt state is bit-identical to the recurrence baseline).
 //
-// One CTA per (request, head) holds the whole D x D state in registers (2*D threads, 128-bit loads of
-// row segments), so each 64 KB state (D = 128) is read once and written at most once per launch.
+// One CTA per (request, head) holds the whole D x D state in registers (D/16 warps, each owning 16 value
+// columns; 128-bit loads of row segments), so each 64 KB state (D = 128) is read once and written at most
+// once per launch.  The window's inputs are staged in shared memory before the dependent token steps.
 #include "launch.h"
-#include "step.cuh"
+#include "wstep.cuh"
 
 namespace kda {
 
-// Loads one token of one head (element offset `base` for the D-vectors, `bidx` for beta) into smem.
+// Tokens of a window staged in shared memory at once (processed in groups of WGRP) by all threads, so
+// the dependent per-token steps never wait on global memory; one block barrier per group.
+constexpr int WGRP = 8;
+
+// Raw bits of a group of window tokens, as loaded from global memory.
+template <int D, typename Tin>
+struct __align__(16) RawGroup {
+  alignas(16) Tin k[WGRP][D];
+  alignas(16) Tin q[WGRP][D];
+  alignas(16) Tin v[WGRP][D];
+  alignas(16) float g[WGRP][D];
+  float beta[WGRP];
+};
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Issues asynchronous copies of tokens row0 + u * rstride, u < cnt (element offset row * D), into `raw`.
+// No registers are held while the copies are in flight.
 template <int D, typename Tin, bool WITH_Q>
-__device__ __forceinline__ void load_token(TokenSmem<D, D>& tok, const Tin* k, const Tin* q, const Tin* v,
-                                           const float* g, const float* beta, size_t base, size_t bidx, int tid) {
-  if (tid < D) {
-    tok.k[tid] = to_f32(k[base + tid]);
-    if (WITH_Q) tok.q[tid] = to_f32(q[base + tid]);
-    tok.a[tid] = expf(g[base + tid]);
-    tok.v[tid] = to_f32(v[base + tid]);
+__device__ __forceinline__ void fetch_tokens(RawGroup<D, Tin>* raw, const Tin* k, const Tin* q, const Tin* v,
+                                             const float* g, const float* beta, size_t row0, size_t rstride,
+                                             int cnt, int tid, int nt) {
+  constexpr int CH = D * (int)sizeof(Tin) / 16;  // 16-byte chunks per row of k, q, v
+  constexpr int CG = D * 4 / 16;                 // per row of g
+  for (int e = tid; e < cnt * (3 * CH + CG); e += nt) {
+    const int u = e / (3 * CH + CG), r = e % (3 * CH + CG);
+    const size_t off = (row0 + (size_t)u * rstride) * D;
+    if (r < CH) {
+      cp_async16(reinterpret_cast<uint8_t*>(raw->k[u]) + 16 * r, reinterpret_cast<const uint8_t*>(k + off) + 16 * r);
+    } else if (r < 2 * CH) {
+      if (WITH_Q)
+        cp_async16(reinterpret_cast<uint8_t*>(raw->q[u]) + 16 * (r - CH),
+                   reinterpret_cast<const uint8_t*>(q + off) + 16 * (r - CH));
+    } else if (r < 3 * CH) {
+      cp_async16(reinterpret_cast<uint8_t*>(raw->v[u]) + 16 * (r - 2 * CH),
+                 reinterpret_cast<const uint8_t*>(v + off) + 16 * (r - 2 * CH));
+    } else {
+      cp_async16(reinterpret_cast<uint8_t*>(raw->g[u]) + 16 * (r - 3 * CH),
+                 reinterpret_cast<const uint8_t*>(g + off) + 16 * (r - 3 * CH));
+    }
   }
-  if (tid == 0) tok.beta = beta[bidx];
+  if (tid < cnt) cp_async4(&raw->beta[tid], beta + row0 + (size_t)tid * rstride);
+}
+
+// Converts a fetched group into the step's fp32 token layout and, with RECORD, writes the raw bits of
+// (k, v, g, beta) to the replay record.  Call after cp_async_wait_all and a barrier.
+template <int D, typename Tin, bool WITH_Q, bool RECORD>
+__device__ __forceinline__ void unpack_tokens(WTok<D>* tok, const RawGroup<D, Tin>* raw, size_t row0, size_t rstride,
+                                              int cnt, int tid, const ReplayPtrs* rec) {
+  if (tid < D) {
+    const int pj = wperm(tid, D);  // lane order of the warp step
+#pragma unroll
+    for (int u = 0; u < WGRP; ++u) {
+      if (u < cnt) {
+        const Tin kv = raw->k[u][tid], vv = raw->v[u][tid];
+        const float gv = raw->g[u][tid];
+        tok[u].k[pj] = to_f32(kv);
+        if (WITH_Q) tok[u].q[pj] = to_f32(raw->q[u][tid]);
+        tok[u].a[pj] = expf(gv);
+        tok[u].v[tid] = to_f32(vv);
+        if (RECORD) {
+          const size_t e = (row0 + u * rstride) * D + tid;
+          static_cast<Tin*>(rec->k)[e] = kv;
+          static_cast<Tin*>(rec->v)[e] = vv;
+          rec->g[e] = gv;
+        }
+      }
+    }
+  } else if (tid < D + WGRP) {
+    const int u = tid - D;
+    if (u < cnt) {
+      tok[u].beta = raw->beta[u];
+      if (RECORD) rec->beta[row0 + u * rstride] = raw->beta[u];
+    }
+  }
 }
 
 template <int D, typename Tin, typename Tout>
-__global__ void __launch_bounds__(2 * D, 2) decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
-                                                       const Tin* __restrict__ v, const float* __restrict__ g,
-                                                       const float* __restrict__ beta, int H, float* pool,
-                                                       int num_slots, const int32_t* __restrict__ slot_ids,
-                                                       Tout* __restrict__ out, int32_t* status) {
-  constexpr int NT = 2 * D;
-  using TL = Tile<D, D, NT>;
-  __shared__ TokenSmem<D, D> tok;
-  __shared__ StepSmem<D, D, NT> sm;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(WCfg<D>::NT, 2) decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                                 const Tin* __restrict__ v,
+                                                                 const float* __restrict__ g,
+                                                                 const float* __restrict__ beta, int H, float* pool,
+                                                                 int num_slots, const int32_t* __restrict__ slot_ids,
+                                                                 Tout* __restrict__ out, int32_t* status) {
+  __shared__ WTok<D> tok[1];
+  __shared__ RawGroup<D, Tin> raw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int slot = slot_ids[b];
   if (slot < 0 || slot >= num_slots) {
@@ -44,69 +116,68 @@ __global__ void __launch_bounds__(2 * D, 2) decode_kernel(const Tin* __restrict_
     return;
   }
   float* Sg = pool + ((size_t)slot * H + h) * D * D;
-  float S[TL::ROWS][4];
-  load_tile<D, D, NT>(S, Sg, D, 0, tid);
-  const size_t base = ((size_t)b * H + h) * D;
-  load_token<D, Tin, true>(tok, k, q, v, g, beta, base, (size_t)b * H + h, tid);
+  const size_t row = (size_t)b * H + h;
+  fetch_tokens<D, Tin, true>(&raw, k, q, v, g, beta, row, 0, 1, tid, WCfg<D>::NT);
+  float2 S[WRows<D>::P][4];
+  wload<D>(S, Sg, warp, lane);
+  cp_async_wait_all();
   __syncthreads();
-  const float o = step<D, D, NT, true>(S, tok, sm, tid);
-  if (tid < D) out[base + tid] = from_f32<Tout>(o);
-  store_tile<D, D, NT>(S, Sg, D, 0, tid);
+  unpack_tokens<D, Tin, true, false>(tok, &raw, row, 0, 1, tid, nullptr);
+  __syncthreads();
+  const float o = wstep<D, true>(S, tok[0], warp, lane);
+  if (((lane >> 2) & 1) == 0) out[row * D + wstep_out_col(warp, lane)] = from_f32<Tout>(o);
+  wstore<D>(S, Sg, warp, lane);
   if (tid == 0) add_work(status, 1);
 }
 
 template <int D, typename Tin, typename Tout>
-__global__ void __launch_bounds__(2 * D, 2) verify_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
-                                                       const Tin* __restrict__ v, const float* __restrict__ g,
-                                                       const float* __restrict__ beta, int W, int H,
-                                                       const float* __restrict__ pool, int num_slots,
-                                                       const int32_t* __restrict__ slot_ids, Tout* __restrict__ out,
-                                                       ReplayPtrs rec, float* __restrict__ snapshot_out,
-                                                       int32_t* status) {
-  constexpr int NT = 2 * D;
-  using TL = Tile<D, D, NT>;
-  __shared__ TokenSmem<D, D> tok[2];
-  __shared__ StepSmem<D, D, NT> sm;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(WCfg<D>::NT, 2) verify_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                                 const Tin* __restrict__ v,
+                                                                 const float* __restrict__ g,
+                                                                 const float* __restrict__ beta, int W, int H,
+                                                                 const float* __restrict__ pool, int num_slots,
+                                                                 const int32_t* __restrict__ slot_ids,
+                                                                 Tout* __restrict__ out, ReplayPtrs rec,
+                                                                 float* __restrict__ snapshot_out, int32_t* status) {
+  __shared__ WTok<D> tok[WGRP];
+  __shared__ RawGroup<D, Tin> raw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int slot = slot_ids[b];
   if (slot < 0 || slot >= num_slots) {
     if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
     return;
   }
-  float S[TL::ROWS][4];
-  load_tile<D, D, NT>(S, pool + ((size_t)slot * H + h) * D * D, D, 0, tid);
-  Tin* rk = static_cast<Tin*>(rec.k);
-  Tin* rv = static_cast<Tin*>(rec.v);
-  for (int w = 0; w < W; ++w) {
-    const size_t row = ((size_t)b * W + w) * H + h;
-    const size_t base = row * D;
-    TokenSmem<D, D>& t = tok[w & 1];
-    load_token<D, Tin, true>(t, k, q, v, g, beta, base, row, tid);
-    // raw-input record: the exact stored bits the fold will consume
-    if (tid < D) {
-      rk[base + tid] = k[base + tid];
-      rv[base + tid] = v[base + tid];
-      rec.g[base + tid] = g[base + tid];
-    }
-    if (tid == 0) rec.beta[row] = beta[row];
+  float2 S[WRows<D>::P][4];
+  for (int w0 = 0; w0 < W; w0 += WGRP) {
+    const int cnt = W - w0 < WGRP ? W - w0 : WGRP;
+    if (w0 > 0) __syncthreads();  // the previous group's steps have finished reading tok[]
+    const size_t row0 = ((size_t)b * W + w0) * H + h;
+    fetch_tokens<D, Tin, true>(&raw, k, q, v, g, beta, row0, H, cnt, tid, WCfg<D>::NT);
+    if (w0 == 0) wload<D>(S, pool + ((size_t)slot * H + h) * D * D, warp, lane);
+    cp_async_wait_all();
     __syncthreads();
-    const float o = step<D, D, NT, true>(S, t, sm, tid);
-    if (tid < D) out[base + tid] = from_f32<Tout>(o);
-    if (snapshot_out) store_tile<D, D, NT>(S, snapshot_out + row * D * D, D, 0, tid);
+    // the group's inputs, and their raw-input record: the exact stored bits the fold consumes
+    unpack_tokens<D, Tin, true, true>(tok, &raw, row0, H, cnt, tid, &rec);
+    __syncthreads();
+    for (int u = 0; u < cnt; ++u) {
+      const size_t row = row0 + (size_t)u * H;
+      const float o = wstep<D, true>(S, tok[u], warp, lane);
+      if (((lane >> 2) & 1) == 0) out[row * D + wstep_out_col(warp, lane)] = from_f32<Tout>(o);
+      if (snapshot_out) wstore<D>(S, snapshot_out + row * D * D, warp, lane);
+    }
   }
   if (tid == 0) add_work(status, W);
 }
 
 template <int D, typename Tin>
-__global__ void __launch_bounds__(2 * D, 2) fold_kernel(float* pool, int num_slots, const int32_t* __restrict__ slot_ids,
-                                                     int W, int H, ReplayPtrs rec,
-                                                     const int32_t* __restrict__ accepted, int32_t* status) {
-  constexpr int NT = 2 * D;
-  using TL = Tile<D, D, NT>;
-  __shared__ TokenSmem<D, D> tok[2];
-  __shared__ StepSmem<D, D, NT> sm;
-  const int tid = threadIdx.x;
+__global__ void __launch_bounds__(WCfg<D>::NT, 2) fold_kernel(float* pool, int num_slots,
+                                                               const int32_t* __restrict__ slot_ids, int W, int H,
+                                                               ReplayPtrs rec, const int32_t* __restrict__ accepted,
+                                                               int32_t* status) {
+  __shared__ WTok<D> tok[WGRP];
+  __shared__ RawGroup<D, Tin> raw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / H, h = blockIdx.x % H;
   const int n = accepted[b];
   if (n < 0 || n > W) {
@@ -120,18 +191,22 @@ __global__ void __launch_bounds__(2 * D, 2) fold_kernel(float* pool, int num_slo
     return;
   }
   float* Sg = pool + ((size_t)slot * H + h) * D * D;
-  float S[TL::ROWS][4];
-  load_tile<D, D, NT>(S, Sg, D, 0, tid);
+  float2 S[WRows<D>::P][4];
   const Tin* rk = static_cast<const Tin*>(rec.k);
   const Tin* rv = static_cast<const Tin*>(rec.v);
-  for (int w = 0; w < n; ++w) {
-    const size_t row = ((size_t)b * W + w) * H + h;
-    TokenSmem<D, D>& t = tok[w & 1];
-    load_token<D, Tin, false>(t, rk, nullptr, rv, rec.g, rec.beta, row * D, row, tid);
+  for (int w0 = 0; w0 < n; w0 += WGRP) {
+    const int cnt = n - w0 < WGRP ? n - w0 : WGRP;
+    if (w0 > 0) __syncthreads();
+    const size_t row0 = ((size_t)b * W + w0) * H + h;
+    fetch_tokens<D, Tin, false>(&raw, rk, nullptr, rv, rec.g, rec.beta, row0, H, cnt, tid, WCfg<D>::NT);
+    if (w0 == 0) wload<D>(S, Sg, warp, lane);
+    cp_async_wait_all();
     __syncthreads();
-    step<D, D, NT, false>(S, t, sm, tid);
+    unpack_tokens<D, Tin, false, false>(tok, &raw, row0, H, cnt, tid, nullptr);
+    __syncthreads();
+    for (int u = 0; u < cnt; ++u) wstep<D, false>(S, tok[u], warp, lane);
   }
-  store_tile<D, D, NT>(S, Sg, D, 0, tid);
+  wstore<D>(S, Sg, warp, lane);
   if (tid == 0) add_work(status, n);
 }
 
@@ -139,7 +214,7 @@ __global__ void __launch_bounds__(2 * D, 2) fold_kernel(float* pool, int num_slo
 
 template <int D, typename Tin, typename Tout>
 static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
-  decode_kernel<D, Tin, Tout><<<a.B * a.H, 2 * D, 0, s>>>(
+  decode_kernel<D, Tin, Tout><<<a.B * a.H, WCfg<D>::NT, 0, s>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.H,
       a.pool, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.status);
   return cudaGetLastError();
@@ -147,7 +222,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
 
 template <int D, typename Tin, typename Tout>
 static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s) {
-  verify_kernel<D, Tin, Tout><<<a.B * a.H, 2 * D, 0, s>>>(
+  verify_kernel<D, Tin, Tout><<<a.B * a.H, WCfg<D>::NT, 0, s>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.W, a.H,
       a.pool, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.rec, a.snapshot_out, a.status);
   return cudaGetLastError();
@@ -155,7 +230,7 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s) {
 
 template <int D, typename Tin>
 static cudaError_t launch_fold_t(const FoldArgs& a, cudaStream_t s) {
-  fold_kernel<D, Tin><<<a.B * a.H, 2 * D, 0, s>>>(a.pool, a.num_slots, a.slot_ids, a.W, a.H, a.rec, a.accepted,
+  fold_kernel<D, Tin><<<a.B * a.H, WCfg<D>::NT, 0, s>>>(a.pool, a.num_slots, a.slot_ids, a.W, a.H, a.rec, a.accepted,
                                                   a.status);
   return cudaGetLastError();
 }

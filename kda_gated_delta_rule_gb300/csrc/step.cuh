@@ -9,8 +9,9 @@
 // (rg, lane) owns rows rg*ROWS .. rg*ROWS+ROWS-1 and the four columns 4*lane .. 4*lane+3.  Loads and
 // stores of a row segment are 128-bit and coalesced across the lanes.  The reductions over rows are
 // partial sums per thread (fixed row order), combined across row groups through shared memory in a fixed
-// group order.  Every floating-point operation is an explicit round-to-nearest intrinsic, so decode,
-// verify, replay and the sequential prefill produce bit-identical states from identical inputs.
+// group order.  Every floating-point operation is an explicit round-to-nearest intrinsic (scalar, or the
+// packed fp32x2 form, which rounds each lane the same way), so decode, verify, replay and the sequential
+// prefill produce bit-identical states from identical inputs.
 #pragma once
 
 #include "common.cuh"
@@ -54,26 +55,33 @@ __device__ __forceinline__ float step(float (&S)[Tile<D, DVT, NT>::ROWS][4], con
   using TL = Tile<D, DVT, NT>;
   const int lane = tid % TL::LANES;
   const int rg = tid / TL::LANES;
-  float r[4] = {0.f, 0.f, 0.f, 0.f};
-  float sq[4] = {0.f, 0.f, 0.f, 0.f};
+  // column pairs (0,1) and (2,3) use the packed fp32x2 pipe; every lane rounds like the scalar op
+  float2 r01 = make_float2(0.f, 0.f), r23 = r01, q01 = r01, q23 = r01;
   float qk = 0.f;
 #pragma unroll
   for (int i = 0; i < TL::ROWS; ++i) {
     const int j = rg * TL::ROWS + i;
-    const float a = tok.a[j];
-    const float kj = tok.k[j];
-    const float qj = WANT_O ? tok.q[j] : 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      S[i][c] = __fmul_rn(a, S[i][c]);
-      r[c] = __fmaf_rn(S[i][c], kj, r[c]);
-      if (WANT_O) sq[c] = __fmaf_rn(S[i][c], qj, sq[c]);
+    const float2 a2 = make_float2(tok.a[j], tok.a[j]);
+    const float2 k2 = make_float2(tok.k[j], tok.k[j]);
+    float2 s01 = __fmul2_rn(a2, make_float2(S[i][0], S[i][1]));
+    float2 s23 = __fmul2_rn(a2, make_float2(S[i][2], S[i][3]));
+    r01 = __ffma2_rn(s01, k2, r01);
+    r23 = __ffma2_rn(s23, k2, r23);
+    if (WANT_O) {
+      const float qj = tok.q[j];
+      const float2 q2 = make_float2(qj, qj);
+      q01 = __ffma2_rn(s01, q2, q01);
+      q23 = __ffma2_rn(s23, q2, q23);
+      qk = __fmaf_rn(qj, tok.k[j], qk);
     }
-    if (WANT_O) qk = __fmaf_rn(qj, kj, qk);
+    S[i][0] = s01.x;
+    S[i][1] = s01.y;
+    S[i][2] = s23.x;
+    S[i][3] = s23.y;
   }
-  *reinterpret_cast<float4*>(&sm.red_r[rg][4 * lane]) = make_float4(r[0], r[1], r[2], r[3]);
+  *reinterpret_cast<float4*>(&sm.red_r[rg][4 * lane]) = make_float4(r01.x, r01.y, r23.x, r23.y);
   if (WANT_O) {
-    *reinterpret_cast<float4*>(&sm.red_q[rg][4 * lane]) = make_float4(sq[0], sq[1], sq[2], sq[3]);
+    *reinterpret_cast<float4*>(&sm.red_q[rg][4 * lane]) = make_float4(q01.x, q01.y, q23.x, q23.y);
     if (lane == 0) sm.red_qk[rg] = qk;
   }
   __syncthreads();
@@ -94,12 +102,17 @@ __device__ __forceinline__ float step(float (&S)[Tile<D, DVT, NT>::ROWS][4], con
   }
   __syncthreads();
   const float4 u4 = *reinterpret_cast<const float4*>(&sm.u[4 * lane]);
-  const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+  const float2 u01 = make_float2(u4.x, u4.y), u23 = make_float2(u4.z, u4.w);
 #pragma unroll
   for (int i = 0; i < TL::ROWS; ++i) {
     const float kj = tok.k[rg * TL::ROWS + i];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) S[i][c] = __fmaf_rn(kj, uu[c], S[i][c]);
+    const float2 k2 = make_float2(kj, kj);
+    const float2 s01 = __ffma2_rn(k2, u01, make_float2(S[i][0], S[i][1]));
+    const float2 s23 = __ffma2_rn(k2, u23, make_float2(S[i][2], S[i][3]));
+    S[i][0] = s01.x;
+    S[i][1] = s01.y;
+    S[i][2] = s23.x;
+    S[i][3] = s23.y;
   }
   return o;
 }
