@@ -274,6 +274,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
+  if (verify_tc_supported(a)) return launch_verify_tc(a, s);
   if (a.in_bf16) return a.out_bf16 ? verify_d<bf16, bf16>(a, s) : verify_d<bf16, float>(a, s);
   return a.out_bf16 ? verify_d<float, bf16>(a, s) : verify_d<float, float>(a, s);
 }

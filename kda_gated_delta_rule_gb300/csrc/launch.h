@@ -94,6 +94,9 @@ struct PrefillArgs {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
+// Tensor-core verify (bf16 inputs, d = 128, W <= 16, no per-token snapshots).
+bool verify_tc_supported(const VerifyArgs& a);
+cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_fold(const FoldArgs& a, cudaStream_t s);
 cudaError_t launch_state_copy(const CopyArgs& a, cudaStream_t s);
 

@@ -26,13 +26,10 @@
 // The pair decays exp(G_t - G_s) are split at a reference token r as exp(G_t - G_r) exp(G_r - G_s): r is
 // the chunk's last token when the chunk's decay span is at most 80 (both factors within exp(+-80)), and
 // otherwise the last token of s's 16-token block, one MMA per block (|g| <= 5 keeps 16 tokens within 80).
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "common.cuh"
 #include "launch.h"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace kda {
 namespace {
@@ -837,43 +834,12 @@ size_t tc_record_bytes(int64_t T, int N, int H) {
   return ((size_t)((T + C - 1) / C) + (size_t)N) * (size_t)H * REC_BYTES;
 }
 
-namespace {
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// [T][H][128] token-major tensor, box = 128 channels x 1 head x 64 tokens, no swizzle, zero fill outside
-bool encode_tokens(CUtensorMap* map, const void* base, bool f32, int64_t T, int H) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t es = f32 ? 4 : 2;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-  const cuuint64_t strides[2] = {D * es, (cuuint64_t)H * D * es};
-  const cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)C};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base),
-             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace
-
 cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t s) {
   if (a.max_seqlen <= 0 || a.T <= 0) return cudaSuccess;
   if (a.T > 0x7fffffff) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   PrepMaps maps;
-  if (!encode_tokens(&maps.q, a.q, false, a.T, a.H) || !encode_tokens(&maps.k, a.k, false, a.T, a.H) ||
-      !encode_tokens(&maps.v, a.v, false, a.T, a.H) || !encode_tokens(&maps.g, a.g, true, a.T, a.H))
+  if (!encode_token_map(&maps.q, a.q, false, a.T, a.H, C) || !encode_token_map(&maps.k, a.k, false, a.T, a.H, C) ||
+      !encode_token_map(&maps.v, a.v, false, a.T, a.H, C) || !encode_token_map(&maps.g, a.g, true, a.T, a.H, C))
     return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_BYTES);
   if (e != cudaSuccess) return e;

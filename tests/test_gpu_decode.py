@@ -70,17 +70,40 @@ def test_verify_and_fold(cuda, case):
     slots = dev(p.slot_ids)
     pool0 = dev(p.pool)
     pool = pool0.clone()
-    out = torch.empty(B, W, H, d, dtype=torch.float32, device="cuda")
-    rec = torch.zeros(kda.kda_replay_bytes(B, W, H, d, d, p.in_dtype), dtype=torch.uint8, device="cuda")
+    ref_o, ref_states = oracle.verify(p.pool, p.slot_ids, p.wq, p.wk, p.wv, p.wg, p.wbeta)
+
+    # with per-token snapshots: the token-sequential kernel
+    out_s = torch.empty(B, W, H, d, dtype=torch.float32, device="cuda")
+    rec_s = torch.zeros(kda.kda_replay_bytes(B, W, H, d, d, p.in_dtype), dtype=torch.uint8, device="cuda")
     snaps = torch.empty(B, W, H, d, d, dtype=torch.float32, device="cuda")
     st = torch.zeros(2, dtype=torch.int32, device="cuda")
-    kda.kda_verify(wq, wk, wv, wg, wb, pool, slots, out, rec, snapshot_out=snaps, dev_status=st)
+    kda.kda_verify(wq, wk, wv, wg, wb, pool, slots, out_s, rec_s, snapshot_out=snaps, dev_status=st)
     torch.cuda.synchronize()
     assert status(st) == (0, B * H * W)
     assert torch.equal(pool, pool0), "verify must never write the committed state"
-    ref_o, ref_states = oracle.verify(p.pool, p.slot_ids, p.wq, p.wk, p.wv, p.wg, p.wbeta)
-    assert rel_err(host(out), ref_o) <= _tol(p.in_dtype)
+    assert rel_err(host(out_s), ref_o) <= _tol(p.in_dtype)
     assert rel_err(host(snaps), ref_states) <= _tol(p.in_dtype)
+
+    # n decode steps from the committed states give the snapshot-after-n states (and outputs) bit for bit
+    dpool = pool0.clone()
+    dout = torch.empty(B, H, d, dtype=torch.float32, device="cuda")
+    for w in range(W):
+        kda.kda_decode_step(wq[:, w].contiguous(), wk[:, w].contiguous(), wv[:, w].contiguous(),
+                            wg[:, w].contiguous(), wb[:, w].contiguous(), dpool, slots, dout)
+        torch.cuda.synchronize()
+        assert torch.equal(dpool[slots.long()], snaps[:, w]), f"decode step {w} differs from verify's state"
+        assert torch.equal(dout, out_s[:, w])
+
+    # without snapshots (the serving call; the tensor-core kernel for bf16 inputs at d = 128)
+    out = torch.empty(B, W, H, d, dtype=torch.float32, device="cuda")
+    rec = torch.zeros_like(rec_s)
+    st.zero_()
+    kda.kda_verify(wq, wk, wv, wg, wb, pool, slots, out, rec, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (0, B * H * W)
+    assert torch.equal(pool, pool0), "verify must never write the committed state"
+    assert rel_err(host(out), ref_o) <= _tol(p.in_dtype)
+    assert torch.equal(rec, rec_s)
 
     # the record holds the exact input bits (k, v, g, beta)
     esz = 2 if p.in_dtype == synth.BF16 else 4
@@ -94,16 +117,6 @@ def test_verify_and_fold(cuda, case):
     assert raw[off_v:off_v + rows * d * esz].tobytes() == p.wv.tobytes()
     assert raw[off_g:off_g + rows * d * 4].tobytes() == p.wg.tobytes()
     assert raw[off_b:off_b + rows * 4].tobytes() == p.wbeta.tobytes()
-
-    # n decode steps from the committed states give the snapshot-after-n states bit for bit
-    dpool = pool0.clone()
-    dout = torch.empty(B, H, d, dtype=torch.float32, device="cuda")
-    for w in range(W):
-        kda.kda_decode_step(wq[:, w].contiguous(), wk[:, w].contiguous(), wv[:, w].contiguous(),
-                            wg[:, w].contiguous(), wb[:, w].contiguous(), dpool, slots, dout)
-        torch.cuda.synchronize()
-        assert torch.equal(dpool[slots.long()], snaps[:, w]), f"decode step {w} differs from verify's state"
-        assert torch.equal(dout, out[:, w])
 
     # fold: commit accepted prefixes
     acc = dev(p.accepted)
@@ -122,11 +135,47 @@ def test_verify_and_fold(cuda, case):
     untouched[slots.long()] = False
     assert torch.equal(pool[untouched], pool0[untouched])
 
-    # bf16 outputs are the RNE rounding of the fp32 outputs
+    # bf16 outputs are the RNE rounding of the fp32 outputs of the same call
     out16 = torch.empty(B, W, H, d, dtype=torch.bfloat16, device="cuda")
     kda.kda_verify(wq, wk, wv, wg, wb, pool0, slots, out16, rec)
     torch.cuda.synchronize()
     assert np.array_equal(bf16_bits(out16), synth.f32_to_bf16(out.cpu().numpy()))
+
+
+# windows the tensor-core verify takes (W <= 16, padded to 8 or 16 tokens) and one past it
+@pytest.mark.parametrize("W", [1, 3, 8, 9, 13, 16, 17])
+def test_verify_window_sizes(cuda, W):
+    kda = cuda
+    p = synth.decode_verify(seed=40 + W, B=19, W=W, H=3, d=128, num_slots=40, dtype=synth.BF16)
+    slots = dev(p.slot_ids)
+    pool0 = dev(p.pool)
+    out = torch.empty(p.B, W, p.H, p.dv, dtype=torch.float32, device="cuda")
+    rec = torch.zeros(kda.kda_replay_bytes(p.B, W, p.H, p.dk, p.dv, p.in_dtype), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_verify(dev(p.wq), dev(p.wk), dev(p.wv), dev(p.wg), dev(p.wbeta), pool0, slots, out, rec, dev_status=st)
+    torch.cuda.synchronize()
+    assert status(st) == (0, p.B * p.H * W)
+    ref_o, _ = oracle.verify(p.pool, p.slot_ids, p.wq, p.wk, p.wv, p.wg, p.wbeta)
+    assert rel_err(host(out), ref_o) <= TOL_BF16_IN
+    assert torch.equal(pool0, dev(p.pool))
+
+
+def test_verify_steep_gates(cuda):
+    """Log-decays of -12 per token: the window's decay spans 192 nats, far beyond fp32's exponent range for
+    any single rescaling reference; every factor the verify forms is exp(G_t - G_s) with s <= t."""
+    kda = cuda
+    p = synth.decode_verify(seed=77, B=6, W=16, H=2, d=128, num_slots=6, dtype=synth.BF16)
+    wg = np.full_like(p.wg, -12.0)
+    wg[..., ::3] = -0.01  # slow channels keep the state's contribution visible
+    slots = dev(p.slot_ids)
+    out = torch.empty(p.B, p.W, p.H, p.dv, dtype=torch.float32, device="cuda")
+    rec = torch.zeros(kda.kda_replay_bytes(p.B, p.W, p.H, p.dk, p.dv, p.in_dtype), dtype=torch.uint8, device="cuda")
+    kda.kda_verify(dev(p.wq), dev(p.wk), dev(p.wv), dev(wg), dev(p.wbeta), dev(p.pool), slots, out, rec)
+    torch.cuda.synchronize()
+    ref_o, _ = oracle.verify(p.pool, p.slot_ids, p.wq, p.wk, p.wv, wg, p.wbeta)
+    got = host(out)
+    assert np.isfinite(got).all()
+    assert rel_err(got, ref_o) <= TOL_BF16_IN
 
 
 def test_out_of_range_ids_are_flagged_and_skipped(cuda):
@@ -161,6 +210,33 @@ def test_out_of_range_ids_are_flagged_and_skipped(cuda):
     assert flags == kda.KDA_DEV_ACCEPT_OOB and work == 1 * H
     for b in (1, 2, 3):
         assert torch.equal(pool[int(p.slot_ids[b])], pool0[int(p.slot_ids[b])])
+
+
+def test_verify_out_of_range_slot_is_flagged_and_skipped(cuda):
+    """A bad slot id in the tensor-core verify: flagged, its outputs and record untouched, the rest correct
+    (more (request, head) items than SMs, so persistent CTAs step over the bad item mid-stream)."""
+    kda = cuda
+    p = synth.decode_verify(seed=61, B=160, W=6, H=2, d=128, num_slots=200, dtype=synth.BF16)
+    bad = p.slot_ids.copy()
+    bad[[3, 97]] = [200, -1]
+    out = torch.zeros(p.B, p.W, p.H, p.dv, dtype=torch.float32, device="cuda")
+    rec = torch.zeros(kda.kda_replay_bytes(p.B, p.W, p.H, p.dk, p.dv, p.in_dtype), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_verify(dev(p.wq), dev(p.wk), dev(p.wv), dev(p.wg), dev(p.wbeta), dev(p.pool), dev(bad), out, rec,
+                   dev_status=st)
+    torch.cuda.synchronize()
+    flags, work = status(st)
+    assert flags == kda.KDA_DEV_SLOT_OOB and work == (p.B - 2) * p.H * p.W
+    good = np.array([b for b in range(p.B) if b not in (3, 97)])
+    ref_o, _ = oracle.verify(p.pool, p.slot_ids[good], p.wq[good], p.wk[good], p.wv[good], p.wg[good],
+                             p.wbeta[good])
+    got = host(out)
+    assert rel_err(got[good], ref_o) <= TOL_BF16_IN
+    assert not got[[3, 97]].any()
+    rows = p.B * p.W * p.H
+    kbytes = rec.cpu().numpy()[:rows * p.dk * 2].view(np.uint16).reshape(p.B, p.W, p.H, p.dk)
+    assert not kbytes[[3, 97]].any()
+    assert np.array_equal(kbytes[good], p.wk[good])
 
 
 def test_state_copy(cuda):
