@@ -36,6 +36,10 @@ STATE_BYTES = 128 * 128 * 4
 RECORD_BYTES = 256 + 256 + 512 + 4  # k, v bf16 + g fp32 + beta fp32
 # chunk-form algorithmic FLOPs per token and head at d = 128, C = 64: 2 (3 d^2 + 2.5 C d + C^2 / 6)
 ALG_FLOP_PER_TOKEN_HEAD = 2 * (3 * 128 * 128 + 2.5 * 64 * 128 + 64 * 64 / 6)
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one tc_prep_kernel launch on the 8K
+# workload, from one ncu --set full capture of the current kernel (126.67 MB read + 170.54 MB written);
+# reported as the roofline's traffic while that kernel is unchanged
+PREP_DRAM_BYTES = 126_673_152 + 170_542_848
 
 
 def parse():
@@ -45,7 +49,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--path", choices=["auto", "varlen", "segmented"], default="segmented")
-    ap.add_argument("--segment-len", type=int, default=1024)
+    ap.add_argument("--segment-len", type=int, default=0,
+                    help="tokens per segment of the segmented path (multiple of 64); 0 = the shortest segment whose "
+                         "fragment phase (2 CTAs per head and segment but the last) fits one wave on this GPU")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -183,6 +189,11 @@ def run_ours(args):
     status = torch.zeros(2, dtype=torch.int32, device=dev)
     pargs = (q, k, v, g, beta, cu, T, pool, slot, out)
     seg_len = args.segment_len
+    if seg_len <= 0:
+        # fragment phase: 2 x H CTAs for each segment but the last, one CTA per SM
+        segments = props.multi_processor_count // (2 * H) + 1
+        per_segment = -(-T // segments)
+        seg_len = -(-per_segment // 64) * 64
     ws = torch.empty(max(kda.kda_segmented_workspace_size(*pargs, seg_len), 256), dtype=torch.uint8, device=dev)
     ws_var = torch.empty(max(kda.kda_prefill_workspace_size(*pargs), 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -220,9 +231,39 @@ def run_ours(args):
         trial[pth] = statistics.median(time_calls(lambda: (restore(), prefill(pth)), 3))
     path = min(trial, key=trial.get)
 
+    # the step's launches, phase by phase (exactly the kernels kda_prefill_varlen / kda_prefill_segmented
+    # enqueue), so the timed steps also give each kernel's duration from events between its launches
+    if path == "varlen":
+        phase_fns = [("kda_state_copy", restore),
+                     ("tc_prep_kernel", lambda: kda.kda_prefill_records(*pargs, workspace=ws_var, dev_status=status)),
+                     ("tc_chain_kernel<plain>",
+                      lambda: kda.kda_prefill_chain(*pargs, workspace=ws_var, dev_status=status))]
+    else:
+        phase_fns = [("kda_state_copy", restore),
+                     ("tc_prep_kernel", lambda: kda.kda_prefill_records(*pargs, workspace=ws, dev_status=status)),
+                     ("tc_chain_kernel<frag>",
+                      lambda: kda.kda_segment_fragments(*pargs, seg_len, ws, dev_status=status)),
+                     ("seg_scan_kernel", lambda: kda.kda_fragment_scan(*pargs, seg_len, ws, dev_status=status)),
+                     ("tc_chain_kernel<segout>",
+                      lambda: kda.kda_segment_outputs(*pargs, seg_len, ws, dev_status=status))]
+
     def step():
-        restore()
-        prefill(path)
+        for _, fn in phase_fns:
+            fn()
+
+    def time_steps(n):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phase_fns) + 1)] for _ in range(n)]
+        for i in range(n):
+            flush.zero_()
+            evs[i][0].record(stream)
+            for j, (_, fn) in enumerate(phase_fns):
+                fn()
+                evs[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+        steps_ms = [e[0].elapsed_time(e[-1]) for e in evs]
+        per_phase = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+                     for j, (name, _) in enumerate(phase_fns)}
+        return steps_ms, per_phase
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -233,7 +274,7 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    step_ms = time_calls(step, args.steps)
+    step_ms, phases = time_steps(args.steps)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
@@ -245,25 +286,7 @@ def run_ours(args):
     ms_max = max_over_ranks(ms, world, dev)
     value = whole_job_value(T, world, ms_max / 1e3)
 
-    # ---- per-kernel durations of one step (events between the launches of the step)
-    # ---- per-kernel durations of one step: the path's phases, each timed alone with events
-    def phase_times(n=10):
-        res = {"kda_state_copy": statistics.mean(time_calls(restore, n))}
-        if path == "varlen":
-            res["tc_prep_kernel"] = statistics.mean(
-                time_calls(lambda: kda.kda_prefill_records(*pargs, workspace=ws_var), n))
-            res["tc_chain_kernel<plain>"] = statistics.mean(
-                time_calls(lambda: (kda.kda_prefill_chain(*pargs, workspace=ws_var)), n))
-        else:
-            res["tc_prep_kernel"] = statistics.mean(time_calls(lambda: kda.kda_prefill_records(*pargs, workspace=ws), n))
-            res["tc_chain_kernel<frag>"] = statistics.mean(
-                time_calls(lambda: kda.kda_segment_fragments(*pargs, seg_len, ws), n))
-            res["seg_scan_kernel"] = statistics.mean(time_calls(lambda: kda.kda_fragment_scan(*pargs, seg_len, ws), n))
-            res["tc_chain_kernel<segout>"] = statistics.mean(
-                time_calls(lambda: kda.kda_segment_outputs(*pargs, seg_len, ws), n))
-        return res
-
-    phases = phase_times()
+    # ---- per-kernel durations: events between the launches of the timed steps (phases above)
     dominant = max((kname for kname in phases if kname != "kda_state_copy"), key=lambda kname: phases[kname])
     # algorithmic bytes of the prefill: 1540 B per token and head (q, k, v, o bf16; g, beta fp32) plus the
     # initial and final state of every head; achieved = those bytes / the dominant kernel's duration
@@ -271,7 +294,8 @@ def run_ours(args):
     achieved = alg_bytes / (phases[dominant] / 1e3) / 1e9
     path_gbs = alg_bytes / (ms_max / 1e3) / 1e9
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5), "traffic": None,
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5),
+                "traffic": PREP_DRAM_BYTES if dominant == "tc_prep_kernel" and T == 8192 else None,
                 "peak_source": pk_kind, "algorithmic_bytes": alg_bytes,
                 "kernel_ms": round(phases[dominant], 4),
                 "phase_ms": {kk: round(vv, 4) for kk, vv in phases.items()},

@@ -46,7 +46,7 @@ constexpr uint32_t REC_PLO = 73728;
 constexpr uint32_t REC_KHHI = 81920;    // (K o exp(G_C - G))^T [128 j][K = 64 s]
 constexpr uint32_t REC_KHLO = 98304;
 constexpr uint32_t REC_STAGE = 114688;
-constexpr uint32_t REC_U = 114688;      // U~ [64 t][128 c] fp32
+constexpr uint32_t REC_U = 114688;      // U~ [64 t][128 c] fp32, row t's 16-byte chunk q stored at q ^ (t % 8)
 constexpr uint32_t REC_GAMMA = 147456;  // gamma_C [128] fp32
 constexpr uint32_t REC_BYTES = 148480;
 
@@ -87,16 +87,20 @@ constexpr uint32_t PS_YHI = 65536;      // Y [64][128] bf16: K o exp(G_ref - G_s
 constexpr uint32_t PS_YLO = 81920;
 constexpr uint32_t PS_KPHI = 98304;     // (K o gamma)^T [128 j][K = 64 s] bf16, hi then lo
 constexpr uint32_t PS_KPLO = 114688;
+// after the Gram product the dead regions stage record tiles for bulk stores: P hi and lo in the raw q
+// region, (K o exp(G_C - G))^T hi and lo in the Y region; after the W / U~ product, W hi and lo rows in the
+// first 32 KB (A and T) and U~ in the g region
 constexpr uint32_t PS_K = 131072;       // raw k [64][128] bf16
 constexpr uint32_t PS_Q = 147456;       // raw q [64][128] bf16
 constexpr uint32_t PS_V = 163840;       // raw v [64][128] bf16
 constexpr uint32_t PS_G = 180224;       // g, then G (in place) [64][128] fp32
 constexpr uint32_t PS_BETA = 212992;    // beta [64]
-constexpr uint32_t PS_GTOT = 213248;    // per-channel sum of the first 32 tokens [128]
+constexpr uint32_t PS_GTOT = 213248;    // (unused)
 constexpr uint32_t PS_BAR = 213760;     // three mbarriers: inputs, Gram product, W/U products
 constexpr uint32_t PS_SLOT = 213784;
 constexpr uint32_t PS_BYTES = 213800 + 1024;
-constexpr int PREP_NT = 256;
+constexpr int PREP_NT = 512;
+constexpr int PREP_PARTS = PREP_NT / D;  // threads per channel in the per-channel phases
 
 // two-term split of a pair: (a, b) ~= hi + lo, packed bf16x2 (a in the low half)
 __device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
@@ -256,33 +260,42 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     sbeta[t] = t < n ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
   }
   __syncthreads();
-  // cumulative log-decay in place: thread (j, half) scans 32 tokens, the upper half then adds the lower
-  // half's total; the decay span of channel j (including the chunk start, G = 0) decides the path
+  // cumulative log-decay in place: thread (j, part) scans 16 tokens and adds the totals of the parts
+  // before it; the decay span of channel j (including the chunk start, G = 0) decides the path
   float span = 0.f;
   {
-    const int j = tid & (D - 1), half = tid >> 7;
-    float* gtot = reinterpret_cast<float*>(sm + PS_GTOT);
-    float* ext = reinterpret_cast<float*>(sm + PS_XHI);  // scratch for the extremes, before X is built
-    float x[32];
+    constexpr int TQ = C / PREP_PARTS;
+    const int j = tid & (D - 1), part = tid / D;
+    float* ext = reinterpret_cast<float*>(sm + PS_XHI);           // extremes, before X is built
+    float* gpart = reinterpret_cast<float*>(sm + PS_XHI + 8192);  // part totals [PREP_PARTS][D]
+    float x[TQ];
 #pragma unroll
-    for (int u = 0; u < 32; ++u) x[u] = sG[(32 * half + u) * D + j];
+    for (int u = 0; u < TQ; ++u) x[u] = sG[(TQ * part + u) * D + j];
 #pragma unroll
-    for (int u = 1; u < 32; ++u) x[u] = __fadd_rn(x[u - 1], x[u]);
-    if (half == 0) gtot[j] = x[31];
+    for (int u = 1; u < TQ; ++u) x[u] = __fadd_rn(x[u - 1], x[u]);
+    gpart[part * D + j] = x[TQ - 1];
     __syncthreads();
-    const float off = half ? gtot[j] : 0.f;
+    float off = 0.f;
+    for (int pp = 0; pp < part; ++pp) off = __fadd_rn(off, gpart[pp * D + j]);
     float gmin = 0.f, gmax = 0.f;
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      const float gval = half ? __fadd_rn(off, x[u]) : x[u];
-      sG[(32 * half + u) * D + j] = gval;
+    for (int u = 0; u < TQ; ++u) {
+      const float gval = part ? __fadd_rn(off, x[u]) : x[u];
+      sG[(TQ * part + u) * D + j] = gval;
       gmin = fminf(gmin, gval);
       gmax = fmaxf(gmax, gval);
     }
     ext[2 * tid] = gmin;
     ext[2 * tid + 1] = gmax;
     __syncthreads();
-    if (half == 0) span = fmaxf(gmax, ext[2 * (tid + 128) + 1]) - fminf(gmin, ext[2 * (tid + 128)]);
+    if (part == 0) {
+#pragma unroll
+      for (int pp = 1; pp < PREP_PARTS; ++pp) {
+        gmin = fminf(gmin, ext[2 * (tid + D * pp)]);
+        gmax = fmaxf(gmax, ext[2 * (tid + D * pp) + 1]);
+      }
+      span = gmax - gmin;
+    }
   }
   tc::fence_before_sync();
   const bool slow = __syncthreads_or(span > SPAN_MAX);
@@ -321,11 +334,12 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       split8_store(sm + PS_YHI + yo, sm + PS_YLO + yo, v);
     }
   }
-  // (K o gamma)^T, the B operand of W: row j, two threads per row (32 tokens each)
+  // (K o gamma)^T, the B operand of W: row j, PREP_PARTS threads per row
   {
-    const int j = tid & (D - 1), half = tid >> 7;
+    constexpr int SCP = 8 / PREP_PARTS;
+    const int j = tid & (D - 1), part = tid / D;
 #pragma unroll
-    for (int sc = 4 * half; sc < 4 * half + 4; ++sc) {
+    for (int sc = SCP * part; sc < SCP * part + SCP; ++sc) {
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -368,37 +382,41 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 
   if (ok) {
     tc::fence_after_sync();
-    if (warp < 4) {  // A (beta, strictly lower) to shared memory; P (lower incl. diagonal) to the record
-      float v[64];
-      const uint32_t trow = tm + ((uint32_t)(warp * 32) << 16);
-      tc::tmem_ld32(trow, v);
-      tc::tmem_ld32(trow + 32, v + 32);
-      if (tid < 64) {
-        const int t = tid;
+    if (warp < 8) {
+      // A (beta, strictly lower) to shared memory and P (lower incl. diagonal) to the record: lane row
+      // 32 (warp % 4) + lane (rows 0..63 = A, 64..127 = P), columns 32 (warp / 4) .. + 31
+      const int q = warp & 3, ch = warp >> 2, row = 32 * q + (tid & 31);
+      float v[32];
+      tc::tmem_ld32(tm + ((uint32_t)(q * 32) << 16) + 32 * ch, v);
+      if (row < 64) {
+        const int t = row;
         const float bt = sbeta[t];
 #pragma unroll
-        for (int s = 0; s < 64; s += 4) {
+        for (int i = 0; i < 32; i += 4) {
+          const int s0c = 32 * ch + i;
           float4 r;
-          r.x = s + 0 < t ? bt * v[s + 0] : 0.f;
-          r.y = s + 1 < t ? bt * v[s + 1] : 0.f;
-          r.z = s + 2 < t ? bt * v[s + 2] : 0.f;
-          r.w = s + 3 < t ? bt * v[s + 3] : 0.f;
-          *reinterpret_cast<float4*>(sA + t * 64 + s) = r;
+          r.x = s0c + 0 < t ? bt * v[i + 0] : 0.f;
+          r.y = s0c + 1 < t ? bt * v[i + 1] : 0.f;
+          r.z = s0c + 2 < t ? bt * v[i + 2] : 0.f;
+          r.w = s0c + 3 < t ? bt * v[i + 3] : 0.f;
+          *reinterpret_cast<float4*>(sA + t * 64 + s0c) = r;
         }
       } else {
-        const int t = tid - 64;
+        const int t = row - 64;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
+        for (int i = 0; i < 4; ++i) {
+          const int cc = 4 * ch + i;
           float pv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pv[e] = 8 * cc + e <= t ? v[8 * cc + e] : 0.f;
-          split8_store(rec + REC_PHI + tc::sw128_chunk(t, cc), rec + REC_PLO + tc::sw128_chunk(t, cc), pv);
+          for (int e = 0; e < 8; ++e) pv[e] = 8 * cc + e <= t ? v[8 * i + e] : 0.f;
+          split8_store(sm + PS_Q + tc::sw128_chunk(t, cc), sm + PS_Q + (REC_PLO - REC_PHI) + tc::sw128_chunk(t, cc), pv);
         }
       }
-    } else {  // V^T operand (raw bf16) and the (K o exp(G_C - G))^T record tile, one row per thread
-      const int c = tid - 128;
+    } else {
+      // V^T operand (raw bf16) and the (K o exp(G_C - G))^T record tile: row c, two threads per row
+      const int c = (tid - 256) & (D - 1), sh = (tid - 256) >> 7;
 #pragma unroll
-      for (int sc = 0; sc < 8; ++sc) {
+      for (int sc = 4 * sh; sc < 4 * sh + 4; ++sc) {
         __nv_bfloat16 vv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) vv[e] = reinterpret_cast<const __nv_bfloat16*>(sm + PS_V)[(8 * sc + e) * D + c];
@@ -406,18 +424,25 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       }
       const float gc = sG[(C - 1) * D + c];
 #pragma unroll
-      for (int sc = 0; sc < 8; ++sc) {
+      for (int sc = 4 * sh; sc < 4 * sh + 4; ++sc) {
         float kv[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int s = 8 * sc + e;
           kv[e] = __bfloat162float(sK[s * D + c]) * __expf(gc - sG[s * D + c]);
         }
-        split8_store(rec + REC_KHHI + tc::sw128_chunk(c, sc), rec + REC_KHLO + tc::sw128_chunk(c, sc), kv);
+        split8_store(sm + PS_YHI + tc::sw128_chunk(c, sc), sm + PS_YHI + (REC_KHLO - REC_KHHI) + tc::sw128_chunk(c, sc),
+                     kv);
       }
     }
+    tc::fence_proxy_async();
   }
   __syncthreads();
+  if (ok && tid == 0) {
+    tc::bulk_s2g(rec + REC_PHI, sm + PS_Q, REC_KHHI - REC_PHI);
+    tc::bulk_s2g(rec + REC_KHHI, sm + PS_YHI, REC_STAGE - REC_KHHI);
+    tc::bulk_commit();
+  }
 
   if (ok) {
     // T = (I + A)^-1, blocked by 16: diagonal blocks by forward substitution (threads 0..63, one column each)
@@ -484,31 +509,43 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 
   if (ok) {
     // W rows t of the stacked B operand and U~ rows t; M = 64 accumulator rows sit in lanes 0..15 of each
-    // 32-lane quarter.  Warps w and w + 4 share a quarter and split the 128 columns.
+    // 32-lane quarter.  The four warps of a quarter split the columns: 32 of W and 32 of U~ each.
     tc::fence_after_sync();
-    const int q = warp & 3, half = warp >> 2, l = tid & 31;
+    const int q = warp & 3, part = warp >> 2, l = tid & 31;
     const uint32_t trow = tm + ((uint32_t)(q * 32) << 16);
-    float w[64], u[64];
-    tc::tmem_ld32(trow + 64 * half, w);
-    tc::tmem_ld32(trow + 64 * half + 32, w + 32);
-    tc::tmem_ld32(trow + 128 + 64 * half, u);
-    tc::tmem_ld32(trow + 128 + 64 * half + 32, u + 32);
+    float w[32], u[32];
+    tc::tmem_ld32(trow + 32 * part, w);
+    tc::tmem_ld32(trow + 128 + 32 * part, u);
     if (l < 16) {
+      // staging: W rows 0..63 of K-block kb at (hi: 0, lo: 16 KB) + kb * 8 KB; U~ rows at 512 B each
       const int t = 16 * q + l;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint32_t o = (uint32_t)half * 16384u + tc::sw128_chunk(t, cc);
-        split8_store(rec + REC_B1HI + o, rec + REC_B1LO + o, w + 8 * cc);
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t o = (uint32_t)(part >> 1) * 8192u + tc::sw128_chunk(t, 4 * (part & 1) + i);
+        split8_store(sm + o, sm + 16384 + o, w + 8 * i);
       }
-      float4* U = reinterpret_cast<float4*>(rec + REC_U + ((size_t)t * D + 64 * half) * 4);
+      float4* U = reinterpret_cast<float4*>(sm + PS_G + t * D * 4);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) U[e] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+      for (int e = 0; e < 8; ++e) U[(8 * part + e) ^ (t & 7)] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
     }
+    tc::fence_proxy_async();
   } else if (tid == 0) {
     flag_status(a.status, KDA_DEV_TIMEOUT);
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (tid == 0) {
+    if (ok) {
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {
+        tc::bulk_s2g(rec + REC_B1HI + kb * 16384, sm + kb * 8192, 8192);
+        tc::bulk_s2g(rec + REC_B1LO + kb * 16384, sm + 16384 + kb * 8192, 8192);
+      }
+      tc::bulk_s2g(rec + REC_U, sm + PS_G, REC_GAMMA - REC_U);
+      tc::bulk_commit();
+    }
+    tc::bulk_wait_all();  // the staged tiles must be read (and written) before the CTA's memory is released
+  }
   if (warp == 0) tc::tmem_dealloc(tm, 256);
 }
 
@@ -677,9 +714,9 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     const uint32_t par = (uint32_t)cc & 1u;
     float ut[32];
     {
-      const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D + c;
+      const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D];
+      for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D + (c ^ ((e & 7) << 2))];
     }
     bool w_ok = tc::bar_wait(full + st, (uint32_t)(cc >> 1) & 1u);
     if (cc > 0) w_ok = w_ok && tc::bar_wait(bar_st, par ^ 1u);  // the previous chunk's state update
@@ -859,3 +896,4 @@ cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records,
 }
 
 }  // namespace kda
+

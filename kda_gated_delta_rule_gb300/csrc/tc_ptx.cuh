@@ -178,6 +178,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_global,
       : "memory");
 }
 
+// Bulk copy shared -> global (16-byte aligned addresses, size a multiple of 16), tracked by bulk groups.
+__device__ __forceinline__ void bulk_s2g(void* dst_global, const void* src_smem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_global), "r"(smem_u32(src_smem)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// waits until every committed bulk group of this thread has completed (its writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Tiled TMA load of a 3-D box at coordinates (x, y, z) (innermost first) described by `map`; elements
 // outside the tensor read as zero.  The box's full byte count completes on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* map, int x, int y, int z,
