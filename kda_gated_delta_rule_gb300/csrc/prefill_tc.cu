@@ -28,6 +28,7 @@
 // otherwise the last token of s's 16-token block, one MMA per block (|g| <= 5 keeps 16 tokens within 80).
 #include "common.cuh"
 #include "launch.h"
+#include "device.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
@@ -89,13 +90,13 @@ constexpr uint32_t PS_KPHI = 98304;     // (K o gamma)^T [128 j][K = 64 s] bf16,
 constexpr uint32_t PS_KPLO = 114688;
 // after the Gram product the dead regions stage record tiles for bulk stores: P hi and lo in the raw q
 // region, (K o exp(G_C - G))^T hi and lo in the Y region; after the W / U~ product, W hi and lo rows in the
-// first 32 KB (A and T) and U~ in the g region
+// first 32 KB (A and T) and U~ in the next 32 KB (T diag(beta), V^T).  The raw k, q, v, g regions are free
+// once the A / P epilogue is done: the next task's inputs land there while this task finishes.
 constexpr uint32_t PS_K = 131072;       // raw k [64][128] bf16
 constexpr uint32_t PS_Q = 147456;       // raw q [64][128] bf16
 constexpr uint32_t PS_V = 163840;       // raw v [64][128] bf16
 constexpr uint32_t PS_G = 180224;       // g, then G (in place) [64][128] fp32
-constexpr uint32_t PS_BETA = 212992;    // beta [64]
-constexpr uint32_t PS_GTOT = 213248;    // (unused)
+constexpr uint32_t PS_BETA = 212992;    // beta [2][64], double-buffered by task parity
 constexpr uint32_t PS_BAR = 213760;     // three mbarriers: inputs, Gram product, W/U products
 constexpr uint32_t PS_SLOT = 213784;
 constexpr uint32_t PS_BYTES = 213800 + 1024;
@@ -206,8 +207,15 @@ struct PrepMaps {
   CUtensorMap q, k, v, g;
 };
 
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+
+// Persistent: each CTA walks the task list (task = (sequence i, head h, chunk slot cidx)) with stride
+// gridDim.x, skipping empty chunk slots, and prefetches the next task's inputs while it finishes one.
 __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a, uint8_t* __restrict__ ws,
-                                                              const __grid_constant__ PrepMaps maps) {
+                                                              const __grid_constant__ PrepMaps maps, int nchunk) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(sm + PS_K);
@@ -215,36 +223,87 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   float* sG = reinterpret_cast<float*>(sm + PS_G);
   float* sA = reinterpret_cast<float*>(sm + PS_A);
   float* sT = reinterpret_cast<float*>(sm + PS_T);
-  float* sbeta = reinterpret_cast<float*>(sm + PS_BETA);
+  float* const sbeta_all = reinterpret_cast<float*>(sm + PS_BETA);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + PS_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PS_SLOT);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int cidx = blockIdx.x, h = blockIdx.y, i = blockIdx.z;
-  const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
-  if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
-    if (tid == 0 && cidx == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
-    return;
-  }
-  const int64_t t0 = s0 + (int64_t)cidx * C;
-  if (t0 >= s1) return;
-  const int n = (int)((s1 - t0) < C ? (s1 - t0) : C);
-  uint8_t* rec = ws + ((size_t)(t0 / C + i) * a.H + h) * REC_BYTES;
+  constexpr int DUTY = PREP_NT - 1;  // issues the bulk stores and the next task's tensor-map loads
+  const int total = nchunk * a.H * a.N;
+  struct Task {
+    int64_t t0;
+    int n, h, i;  // n = valid tokens (0: empty slot or malformed cu_seqlens)
+  };
+  auto task_at = [&](int t) {
+    Task r;
+    const int cidx = t % nchunk;
+    r.h = (t / nchunk) % a.H;
+    r.i = t / (nchunk * a.H);
+    r.n = 0;
+    r.t0 = 0;
+    const int64_t s0 = a.cu[r.i], s1 = a.cu[r.i + 1];
+    if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
+      if (tid == 0 && cidx == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
+      return r;
+    }
+    r.t0 = s0 + (int64_t)cidx * C;
+    if (r.t0 < s1) r.n = (int)((s1 - r.t0) < C ? (s1 - r.t0) : C);
+    return r;
+  };
+  auto next_task = [&](int t) {
+    while (t < total && task_at(t).n == 0) t += (int)gridDim.x;
+    return t;
+  };
+  // the chunk's k, q, v and g tiles (64 tokens x 128 channels of head h) with four TMA loads; beta with
+  // 4-byte copies that arrive on the same barrier
+  auto fetch = [&](const Task& tk, int k) {
+    uint64_t* fb = bar + 2;
+    if (tid == DUTY) {
+      tc::bar_arrive_expect_tx(fb, 3 * 16384 + 32768);
+      tc::tma_load_3d(sK, &maps.k, 0, tk.h, (int)tk.t0, fb);
+      tc::tma_load_3d(sQ, &maps.q, 0, tk.h, (int)tk.t0, fb);
+      tc::tma_load_3d(sm + PS_V, &maps.v, 0, tk.h, (int)tk.t0, fb);
+      tc::tma_load_3d(sG, &maps.g, 0, tk.h, (int)tk.t0, fb);
+    }
+    if (tid >= D && tid < D + C) {
+      const int t = tid - D;
+      float* sb = sbeta_all + C * (k & 1);
+      if (t < tk.n) cp_async4(&sb[t], a.beta + (size_t)(tk.t0 + t) * a.H + tk.h);
+      else sb[t] = 0.f;
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(fb)) : "memory");
+    }
+  };
 
   if (warp == 0) tc::tmem_alloc(tslot, 256);
   if (tid == 0) {
-    for (int b = 0; b < 3; ++b) tc::bar_init(bar + b, 1);
+    tc::bar_init(bar + 0, 1);
+    tc::bar_init(bar + 1, 1);
+    tc::bar_init(bar + 2, 1 + C);  // the TMA issuer + one arrival per beta thread
     tc::bar_fence_init();
   }
+  tc::fence_before_sync();
   __syncthreads();
-  // stage the chunk's k, q, v and g tiles (64 tokens x 128 channels of head h) with four TMA loads
-  if (tid == 0) {
-    tc::bar_arrive_expect_tx(bar + 2, 3 * 16384 + 32768);
-    tc::tma_load_3d(sK, &maps.k, 0, h, (int)t0, bar + 2);
-    tc::tma_load_3d(sQ, &maps.q, 0, h, (int)t0, bar + 2);
-    tc::tma_load_3d(sm + PS_V, &maps.v, 0, h, (int)t0, bar + 2);
-    tc::tma_load_3d(sG, &maps.g, 0, h, (int)t0, bar + 2);
+  tc::fence_after_sync();
+  const uint32_t tm = *tslot;
+  uint32_t gram_uses = 0;
+  int cur = next_task((int)blockIdx.x);
+  int inflight = -1;  // local index of a task whose inputs are requested but not yet waited for
+  if (cur < total) {
+    fetch(task_at(cur), 0);
+    inflight = 0;
   }
-  bool ok = __syncthreads_and(tc::bar_wait(bar + 2, 0));
+  bool ok = true;
+  int k = 0;
+#pragma unroll 1
+  for (; cur < total; ++k) {
+  const Task tk = task_at(cur);
+  const int nxt = next_task(cur + (int)gridDim.x);
+  const int h = tk.h, i = tk.i, n = tk.n;
+  const int64_t t0 = tk.t0;
+  uint8_t* rec = ws + ((size_t)(t0 / C + i) * a.H + h) * REC_BYTES;
+  float* const sbeta = sbeta_all + C * (k & 1);
+  ok = __syncthreads_and(tc::bar_wait(bar + 2, (uint32_t)k & 1u));
+  if (!ok) break;
+  inflight = -1;
   // rows past the chunk's valid tokens (the next sequence's, or beyond T) are zero: k = q = v = g = 0
   for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
     const int t = n + (e >> 4), cc = e & 15;
@@ -255,10 +314,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     *reinterpret_cast<float4*>(sG + t * D + cc * 8) = make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4*>(sG + t * D + cc * 8 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (tid >= D && tid < D + C) {
-    const int t = tid - D;
-    sbeta[t] = t < n ? a.beta[(size_t)(t0 + t) * a.H + h] : 0.f;
-  }
+  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's staged tiles (X, Y regions) have been read
   __syncthreads();
   // cumulative log-decay in place: thread (j, part) scans 16 tokens and adds the totals of the parts
   // before it; the decay span of channel j (including the chunk start, G = 0) decides the path
@@ -300,7 +356,6 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   tc::fence_before_sync();
   const bool slow = __syncthreads_or(span > SPAN_MAX);
   tc::fence_after_sync();
-  const uint32_t tm = *tslot;
 
   // per (token t, 8 channels): Q o gamma (output), (K o gamma)^T (operand), and in the common case X, Y
   for (int task = tid; task < C * 16; task += PREP_NT) {
@@ -360,7 +415,8 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       issue_gram(sm, tm, 0, 64);
       tc::commit(bar);
     }
-    ok = __syncthreads_and(tc::bar_wait(bar, 0));
+    ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));
+    ++gram_uses;
   } else if (ok) {
     for (int e = tid; e < C * 16; e += PREP_NT) {
       const int s = e >> 4;
@@ -375,7 +431,8 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
         issue_gram(sm, tm + 16 * b, 16 * b, 16);
         tc::commit(bar);
       }
-      ok = __syncthreads_and(tc::bar_wait(bar, b & 1));  // block-uniform, so no thread leaves the loop alone
+      ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));  // block-uniform: no thread leaves alone
+      ++gram_uses;
       if (!ok) break;
     }
   }
@@ -438,10 +495,16 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     tc::fence_proxy_async();
   }
   __syncthreads();
-  if (ok && tid == 0) {
+  if (ok && tid == DUTY) {
     tc::bulk_s2g(rec + REC_PHI, sm + PS_Q, REC_KHHI - REC_PHI);
     tc::bulk_s2g(rec + REC_KHHI, sm + PS_YHI, REC_STAGE - REC_KHHI);
     tc::bulk_commit();
+    tc::bulk_wait_read0();  // P (staged in the raw q region) read before the next task's loads land there
+  }
+  // raw k, q, v, g are dead: the next task's inputs
+  if (ok && nxt < total) {
+    fetch(task_at(nxt), k + 1);
+    inflight = k + 1;
   }
 
   if (ok) {
@@ -504,7 +567,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       issue_wu(sm, tm);
       tc::commit(bar + 1);
     }
-    ok = __syncthreads_and(tc::bar_wait(bar + 1, 0));
+    ok = __syncthreads_and(tc::bar_wait(bar + 1, (uint32_t)k & 1u));
   }
 
   if (ok) {
@@ -524,28 +587,33 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
         const uint32_t o = (uint32_t)(part >> 1) * 8192u + tc::sw128_chunk(t, 4 * (part & 1) + i);
         split8_store(sm + o, sm + 16384 + o, w + 8 * i);
       }
-      float4* U = reinterpret_cast<float4*>(sm + PS_G + t * D * 4);
+      float4* U = reinterpret_cast<float4*>(sm + PS_TBHI + t * D * 4);
 #pragma unroll
       for (int e = 0; e < 8; ++e) U[(8 * part + e) ^ (t & 7)] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
     }
     tc::fence_proxy_async();
-  } else if (tid == 0) {
-    flag_status(a.status, KDA_DEV_TIMEOUT);
   }
   tc::fence_before_sync();
   __syncthreads();
-  if (tid == 0) {
-    if (ok) {
+  if (ok && tid == DUTY) {
 #pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        tc::bulk_s2g(rec + REC_B1HI + kb * 16384, sm + kb * 8192, 8192);
-        tc::bulk_s2g(rec + REC_B1LO + kb * 16384, sm + 16384 + kb * 8192, 8192);
-      }
-      tc::bulk_s2g(rec + REC_U, sm + PS_G, REC_GAMMA - REC_U);
-      tc::bulk_commit();
+    for (int kb = 0; kb < 2; ++kb) {
+      tc::bulk_s2g(rec + REC_B1HI + kb * 16384, sm + kb * 8192, 8192);
+      tc::bulk_s2g(rec + REC_B1LO + kb * 16384, sm + 16384 + kb * 8192, 8192);
     }
-    tc::bulk_wait_all();  // the staged tiles must be read (and written) before the CTA's memory is released
+    tc::bulk_s2g(rec + REC_U, sm + PS_TBHI, REC_GAMMA - REC_U);
+    tc::bulk_commit();
   }
+  if (!ok) break;
+  cur = nxt;
+  }  // task loop
+  if (!ok) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
+    if (inflight >= 0) tc::bar_wait(bar + 2, (uint32_t)inflight & 1u);  // bounded: let loads in flight land
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == DUTY) tc::bulk_wait_all();  // every record tile written before the CTA's memory is released
   if (warp == 0) tc::tmem_dealloc(tm, 256);
 }
 
@@ -880,8 +948,12 @@ cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t 
     return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)((a.max_seqlen + C - 1) / C), a.H, a.N);
-  tc_prep_kernel<<<grid, PREP_NT, PS_BYTES, s>>>(a, records, maps);
+  const int nchunk = (a.max_seqlen + C - 1) / C, sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const long long tasks = (long long)nchunk * a.H * a.N;
+  if (tasks > 0x7fffffff) return cudaErrorInvalidValue;
+  const int grid = tasks < sms ? (int)tasks : sms;
+  tc_prep_kernel<<<grid, PREP_NT, PS_BYTES, s>>>(a, records, maps, nchunk);
   return cudaGetLastError();
 }
 

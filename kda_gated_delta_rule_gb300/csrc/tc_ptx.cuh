@@ -187,6 +187,9 @@ __device__ __forceinline__ void bulk_s2g(void* dst_global, const void* src_smem,
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // waits until every committed bulk group of this thread has completed (its writes performed)
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// waits until every committed bulk group of this thread has finished reading its source (shared memory
+// may be reused; the global writes may still be in flight)
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // Tiled TMA load of a 3-D box at coordinates (x, y, z) (innermost first) described by `map`; elements
 // outside the tensor read as zero.  The box's full byte count completes on `bar`.

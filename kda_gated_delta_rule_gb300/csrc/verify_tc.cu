@@ -30,6 +30,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tc_ptx.cuh"
+#include "device.h"
 #include "tmap.h"
 
 namespace kda {
@@ -456,17 +457,6 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 8) tc::tmem_dealloc(tm, TMEM_COLS);
-}
-
-int sm_count() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cached[dev] = n;
-  return n;
 }
 
 template <int WP, typename Tout>
