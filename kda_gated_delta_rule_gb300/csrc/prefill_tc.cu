@@ -815,29 +815,30 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     tc::fence_before_sync();
     __syncthreads();
     const uint32_t sbase = tc::smem_u32(sm + st * REC_STAGE);
+    // shared-memory descriptors of this stage's tiles: a descriptor of base + off is the base descriptor
+    // + off / 16 (start-address field), so each K step is a constant offset
+    const uint64_t dstage = tc::sdesc(sbase);
     if (tid == 0) {
       tc::fence_after_sync();
       // (W S)^T = S^T W^T, then (Q o gamma S)^T into this chunk's output accumulator
 #pragma unroll
       for (int part = 0; part < 3; ++part) {
         const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
-        const uint32_t bb = sbase + (part == 1 ? REC_B1LO : REC_B1HI);
+        const uint64_t bd = dstage + ((part == 1 ? REC_B1LO : REC_B1HI) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc::mma_ts(tm + COL_WS, acol + ks * 8,
-                     tc::sdesc(bb + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u), tc::idesc_bf16(128, 64),
-                     (part | ks) != 0);
+          tc::mma_ts(tm + COL_WS, acol + ks * 8, bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4),
+                     tc::idesc_bf16(128, 64), (part | ks) != 0);
       }
       tc::commit(bar_ws);
       if (WANT_O) {
 #pragma unroll
         for (int part = 0; part < 3; ++part) {
           const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
-          const uint32_t bb = sbase + (part == 1 ? REC_B1LO : REC_B1HI) + 64u * 128u;  // rows 64..127
+          const uint64_t bd = dstage + (((part == 1 ? REC_B1LO : REC_B1HI) + 64u * 128u) >> 4);  // rows 64..127
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8,
-                       tc::sdesc(bb + (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u),
+            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4),
                        tc::idesc_bf16(128, 64), (part | ks) != 0);
         }
       }
@@ -869,20 +870,19 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
 #pragma unroll
       for (int part = 0; part < 3; ++part) {  // state: S^T += U^T (K o exp(G_C - G))
         const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
-        const uint32_t kb = sbase + (part == 1 ? REC_KHLO : REC_KHHI);
+        const uint64_t kd = dstage + ((part == 1 ? REC_KHLO : REC_KHHI) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          tc::mma_ts(tm + COL_S, acol + ks * 8, tc::sdesc(kb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 128), 1);
+        for (int ks = 0; ks < 4; ++ks) tc::mma_ts(tm + COL_S, acol + ks * 8, kd + 2u * ks, tc::idesc_bf16(128, 128), 1);
       }
       tc::commit(bar_st);
       if (WANT_O) {
 #pragma unroll
         for (int part = 0; part < 3; ++part) {  // outputs: O^T += U^T P^T
           const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
-          const uint32_t pb = sbase + (part == 1 ? REC_PLO : REC_PHI);
+          const uint64_t pd = dstage + ((part == 1 ? REC_PLO : REC_PHI) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, tc::sdesc(pb + (uint32_t)ks * 32u), tc::idesc_bf16(128, 64), 1);
+            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, pd + 2u * ks, tc::idesc_bf16(128, 64), 1);
         }
         tc::commit(bar_o + st);
       }
