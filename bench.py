@@ -397,13 +397,26 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
     def copy():
         kda.kda_state_copy(pool, ckpt_slots, pool, slots)
 
-    for fn in (dec, ver, fold, copy):
+    # CF-BI decode: open-chunk row counts uniform in [0, 16) (seeded), row caches in their own pool
+    CH, RF = kda.CFBI_CHUNK, kda.CFBI_ROW_FLOATS
+    n_open = (synth.uniform(p.seed, 98, p.pool.shape[0] * H) * CH).astype(np.int32).reshape(p.pool.shape[0], H)
+    counts0 = to_dev(np.minimum(n_open, CH - 1))
+    cache = torch.zeros(p.pool.shape[0], H, CH, RF, dtype=torch.float32, device=dev)
+    cache[..., 256:384] = -0.1 * torch.arange(CH, device=dev, dtype=torch.float32).view(1, 1, CH, 1)
+    counts = counts0.clone()
+    cf_out = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+
+    def cfbi():
+        counts.copy_(counts0)  # the same open-chunk positions every call (a 1.5 MB copy, timed with it)
+        kda.kda_cfbi_decode(q, k, v, g, beta, pool, cache, counts, slots, cf_out)
+
+    for fn in (dec, ver, fold, copy, cfbi):
         for _ in range(3):
             fn()
     torch.cuda.synchronize()
     n = 20
     t = {name: statistics.mean(time_calls(fn, n)) for name, fn in
-         (("decode", dec), ("verify", ver), ("fold", fold), ("state_copy", copy))}
+         (("decode", dec), ("verify", ver), ("fold", fold), ("state_copy", copy), ("cfbi_decode", cfbi))}
     heads = B * H
     n_acc = p.accepted.astype(np.int64)
     alg = {
@@ -411,6 +424,10 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
         "verify": heads * (STATE_BYTES + W * (BYTES_PER_TOKEN_HEAD + RECORD_BYTES)),
         "fold": int(H * sum(2 * STATE_BYTES + nn * RECORD_BYTES for nn in n_acc if nn > 0)),
         "state_copy": B * 2 * H * STATE_BYTES,
+        # entry state read, L cached rows read, then the new row written (or, completing a chunk, the state
+        # written), plus the token's inputs and output
+        "cfbi_decode": int(sum(STATE_BYTES + BYTES_PER_TOKEN_HEAD + nl * RF * 4 + (RF * 4 if nl < CH - 1 else STATE_BYTES)
+                               for nl in np.minimum(n_open, CH - 1)[p.slot_ids].ravel())),
     }
     rep = {"workload": "batched decode + speculative verify: 256 requests, 1024-slot pool, H=12, d=128, "
                        "W=8, accepted ~ min(Poisson(2.7), 8)", "peak_gbs": pk["hbm_gbs"]}

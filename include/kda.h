@@ -251,6 +251,58 @@ kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, k
  */
 kda_status kda_prefill_segmented_noalloc(const kda_prefill_args* a, int32_t segment_len, kda_stream_t stream);
 
+/*
+ * CF-BI: one row-level computation contract for prefill and decode (batch-invariant outputs).
+ * Source: "Kimi K3.1 inference zero mismatch" (LLMNews), section 6.1: prefill and decode follow one
+ * row-level contract -- a position's output depends on the entry state of its chunk and the rows before it
+ * in that chunk, prefill computes the rows in bulk and decode the new row, in the same operation order; the
+ * open chunk's row cache and position are kept besides the recurrent state; 16-token chunks, an fp32 row
+ * cache per head.  Row t of a chunk with entry state S_c (G the in-chunk cumulative log-decay):
+ *   A_tu = beta_t sum_j k_t k_u e^{G_t - G_u} (u < t),  P_tu = sum_j q_t k_u e^{G_t - G_u} (u <= t),
+ *   R_t = row t of P (I + A)^-1 diag(beta),
+ *   o_t = S_c^T (q_t o e^{G_t} - sum_u R_tu k_u o e^{G_u}) + sum_u R_tu v_u,
+ * and a full chunk advances S_c with U = (I + A)^-1 diag(beta) (V - (K o e^G) S_c):
+ *   S_{c+1} = Diag(e^{G_15}) S_c + (K o e^{G_15 - G})^T U.
+ * The same device routines run in both calls, in fp32 with round-to-nearest operations in a fixed order,
+ * so a token's output and the state are bit-identical whether it was prefilled or decoded, whatever the
+ * batch and wherever a sequence is split between prefill and decode.  Values agree with the recurrence
+ * above (kda_decode_step) to rounding, not bit for bit.
+ *
+ * Per (slot, head) state: S_c in `pool` ([num_slots][H][128][128] fp32, the usual layout), the open chunk's
+ * rows in `cache` ([num_slots][H][KDA_CFBI_CHUNK][KDA_CFBI_ROW_FLOATS] fp32: k[128] | v[128] | G[128] |
+ * A_t[16] (beta folded in) | beta | padding) and their number in `counts` ([num_slots][H] int32, 0..15).
+ * A fresh sequence starts from S_0 in its pool slot with counts = 0 (cache contents then unused).
+ * dk = dv = 128 only (KDA_ERR_UNSUPPORTED otherwise).  A count outside [0, 16) sets KDA_DEV_SLOT_OOB and that
+ * unit is skipped.
+ */
+#define KDA_CFBI_CHUNK 16
+#define KDA_CFBI_ROW_FLOATS 416
+
+/* Bytes of one head's row cache: KDA_CFBI_CHUNK * KDA_CFBI_ROW_FLOATS * 4 at dk = dv = 128, else 0. */
+size_t kda_cfbi_cache_bytes_per_head(int dk, int dv);
+
+/*
+ * kda_cfbi_prefill -- packed sequences through the CF-BI contract; sequence i continues from the state of
+ * slot_ids[i] (pool, cache, counts) and leaves its state there.  One CTA per (sequence, head) walks the
+ * tokens in order.  q, k [T][H][128], v [T][H][128] (in_dtype), g [T][H][128], beta [T][H] fp32,
+ * cu_seqlens int32[N + 1] (device), out [T][H][128] (out_dtype).
+ */
+kda_status kda_cfbi_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const int32_t* cu_seqlens, int32_t N, int64_t T, int32_t max_seqlen, int H, int dk,
+                            int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
+                            int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
+                            int32_t* dev_status, kda_stream_t stream);
+
+/*
+ * kda_cfbi_decode -- one token per request through the CF-BI contract.  q, k, v [B][H][128] (in_dtype),
+ * g [B][H][128], beta [B][H] fp32, out [B][H][128] (out_dtype).  Reads the entry state; writes it only when
+ * the token completes a chunk (then counts returns to 0).
+ */
+kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, int B,
+                           int H, int dk, int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
+                           int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
+                           int32_t* dev_status, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,12 +19,14 @@ __all__ = [
     "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
-    "kda_prefill_records", "kda_prefill_chain", "EXPORTED_SYMBOLS",
+    "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
+    "kda_cfbi_decode", "CFBI_CHUNK", "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
 ]
 
 KDA_OK = 0
 KDA_DEV_SLOT_OOB, KDA_DEV_SEQ_OOB, KDA_DEV_TIMEOUT, KDA_DEV_ACCEPT_OOB = 1, 2, 4, 8
 F32, BF16 = 0, 1
+CFBI_CHUNK, CFBI_ROW_FLOATS = 16, 416  # KDA_CFBI_CHUNK, KDA_CFBI_ROW_FLOATS
 
 # every function include/kda.h declares
 EXPORTED_SYMBOLS = (
@@ -32,7 +34,8 @@ EXPORTED_SYMBOLS = (
     "kda_decode_step", "kda_replay_bytes", "kda_verify", "kda_verify_replay", "kda_prefill_varlen",
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
-    "kda_prefill_records", "kda_prefill_chain",
+    "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
+    "kda_cfbi_decode",
 )
 
 
@@ -96,6 +99,11 @@ def load(build_if_missing: bool = False):
         "kda_prefill_segmented_noalloc": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp]),
         "kda_prefill_records": (c_int, [ctypes.POINTER(PrefillArgs), vp]),
         "kda_prefill_chain": (c_int, [ctypes.POINTER(PrefillArgs), vp]),
+        "kda_cfbi_cache_bytes_per_head": (sz, [c_int, c_int]),
+        "kda_cfbi_prefill": (c_int, [vp, vp, vp, vp, vp, vp, i32, i64, i32, c_int, c_int, c_int, c_int, vp, vp, vp,
+                                     i32, vp, vp, c_int, vp, vp]),
+        "kda_cfbi_decode": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, i32, vp, vp,
+                                    c_int, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -170,6 +178,34 @@ def kda_decode_step(q, k, v, g, beta, pool, slot_ids, out, dev_status=None, stre
     _ok("kda_decode_step", load().kda_decode_step(_p(q), _p(k), _p(v), _p(g), _p(beta), B, H, dk, dv, _dt(q),
                                                   _p(pool), pool.shape[0], _p(slot_ids), _p(out), _dt(out),
                                                   _p(dev_status), _stream(stream)))
+
+
+def kda_cfbi_cache_bytes_per_head(dk: int = 128, dv: int = 128) -> int:
+    return load().kda_cfbi_cache_bytes_per_head(dk, dv)
+
+
+def kda_cfbi_prefill(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, cache, counts, slot_ids, out, dev_status=None,
+                     stream=None):
+    """CF-BI prefill over packed sequences: q, k, g [T, H, 128]; v, out [T, H, 128]; beta [T, H];
+    cu_seqlens int32 [N + 1]; pool [S, H, 128, 128]; cache [S, H, 16, 416] fp32; counts [S, H] int32."""
+    _check(q, k, v, g, beta, cu_seqlens, pool, cache, counts, slot_ids, out, dev_status)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    _ok("kda_cfbi_prefill", load().kda_cfbi_prefill(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), N, T,
+                                                    int(max_seqlen), H, dk, dv, _dt(q), _p(pool), _p(cache),
+                                                    _p(counts), pool.shape[0], _p(slot_ids), _p(out), _dt(out),
+                                                    _p(dev_status), _stream(stream)))
+
+
+def kda_cfbi_decode(q, k, v, g, beta, pool, cache, counts, slot_ids, out, dev_status=None, stream=None):
+    """CF-BI decode, one token per request: q, k, g [B, H, 128]; v, out [B, H, 128]; beta [B, H]."""
+    _check(q, k, v, g, beta, pool, cache, counts, slot_ids, out, dev_status)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    _ok("kda_cfbi_decode", load().kda_cfbi_decode(_p(q), _p(k), _p(v), _p(g), _p(beta), B, H, dk, dv, _dt(q),
+                                                  _p(pool), _p(cache), _p(counts), pool.shape[0], _p(slot_ids),
+                                                  _p(out), _dt(out), _p(dev_status), _stream(stream)))
 
 
 def kda_replay_bytes(B: int, W: int, H: int, dk: int, dv: int, in_dtype: int) -> int:

@@ -319,4 +319,49 @@ kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len,
   return from_cuda(e);
 }
 
+size_t kda_cfbi_cache_bytes_per_head(int dk, int dv) {
+  return (dk == 128 && dv == 128) ? (size_t)KDA_CFBI_CHUNK * KDA_CFBI_ROW_FLOATS * 4 : 0;
+}
+
+kda_status kda_cfbi_prefill(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const int32_t* cu_seqlens, int32_t N, int64_t T, int32_t max_seqlen, int H, int dk,
+                            int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
+                            int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
+                            int32_t* dev_status, kda_stream_t stream) {
+  if (N < 0 || T < 0 || max_seqlen < 0 || H <= 0 || num_slots < 0 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+    return KDA_ERR_INVALID_ARG;
+  if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+  if (N == 0) return KDA_OK;
+  if (N > 65535 || H > 65535) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {cu_seqlens, pool, cache, counts, slot_ids};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if (T > 0) {
+    const void* tp[] = {q, k, v, g, beta, out};
+    for (const void* p : tp)
+      if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  }
+  kda::CfbiArgs a{q,   k,    v,     g,     beta,  0,         N,        T,     max_seqlen,
+                  cu_seqlens, H, in_dtype == KDA_DTYPE_BF16, out_dtype == KDA_DTYPE_BF16, pool, cache, counts,
+                  num_slots,   slot_ids,  out,   dev_status};
+  return from_cuda(kda::launch_cfbi_prefill(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, int B,
+                           int H, int dk, int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
+                           int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
+                           int32_t* dev_status, kda_stream_t stream) {
+  if (B < 0 || H <= 0 || num_slots < 0 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return KDA_ERR_INVALID_ARG;
+  if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+  if (B == 0) return KDA_OK;
+  if ((int64_t)B * H > 0x7fffffff) return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, pool, cache, counts, slot_ids, out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda::CfbiArgs a{q,       k,        v,    g,        beta, B,         0,  0,         0,
+                  nullptr, H, in_dtype == KDA_DTYPE_BF16, out_dtype == KDA_DTYPE_BF16, pool, cache, counts,
+                  num_slots, slot_ids, out,  dev_status};
+  return from_cuda(kda::launch_cfbi_decode(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

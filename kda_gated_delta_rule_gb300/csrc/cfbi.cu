@@ -1,0 +1,316 @@
+// Batch-invariant prefill / decode: one row-level computation contract for both paths.
+//
+// Source: "Kimi K3.1 inference zero mismatch" (LLMNews), section 6.1 (CF-BI): prefill and decode follow
+// one row-level contract -- the output of a position depends on the entry state of its chunk and the
+// rows before it in that chunk, prefill computes the rows in bulk and decode computes the new row, both in
+// the same operation order; besides the recurrent state, the open chunk's row cache and position are kept.
+// The current contract uses 16-token chunks with an fp32 row cache per head.  The arithmetic of a row is
+// the KDA update of "Kimi K3: Architecture and SGLang Day-0 Support" (KDA math box) unrolled over the open
+// chunk from its entry state S_c (rows u = 0 .. t of the chunk, G_u the in-chunk cumulative log-decay):
+//   A_tu = beta_t sum_j k_t[j] k_u[j] exp(G_t[j] - G_u[j])  (u < t),
+//   P_tu =        sum_j q_t[j] k_u[j] exp(G_t[j] - G_u[j])  (u <= t),
+//   R_t  = row t of P (I + A)^-1 diag(beta)  (back substitution over u = t .. 0),
+//   o_t  = S_c^T (q_t o e^{G_t} - sum_u R_tu k_u o e^{G_u}) + sum_u R_tu v_u,
+// and when the chunk is full the entry state advances:
+//   U = (I + A)^-1 diag(beta) (V - (K o e^G) S_c),   S_{c+1} = Diag(e^{G_15}) S_c + (K o e^{G_15 - G})^T U.
+// Every operation is an explicit round-to-nearest fp32 intrinsic in a fixed order and the two kernels run
+// the same device functions with the same thread mapping, so a token's output and the state bits are the
+// same whichever path (or batch, or split of a sequence into prefill and decode) computed them.
+#include "common.cuh"
+#include "launch.h"
+
+namespace kda {
+namespace {
+
+constexpr int D = 128;
+constexpr int NT = 256;
+constexpr int CH = KDA_CFBI_CHUNK;       // rows per chunk
+constexpr int RF = KDA_CFBI_ROW_FLOATS;  // floats per cached row
+// cached row layout: k | v | G (in-chunk cumulative log-decay) | A_t[u] (beta folded in, u < t) | beta
+constexpr int R_K = 0, R_V = 128, R_G = 256, R_A = 384, R_BETA = 400;
+static_assert(R_BETA + 1 <= RF && RF % 4 == 0, "row layout");
+
+struct Scratch {
+  float q[D];           // q_t (fp32)
+  float qh[D];          // q_t o e^{G_t} - sum_u R_tu k_u o e^{G_u}
+  float oh[D];          // sum_u R_tu v_u
+  float part[2][D];     // partial sums of the read-out over the two key halves
+  float p[CH];          // P_t[u]
+  float r[CH];          // R_t[u]
+  float kp[CH][D];      // fold: k_u o e^{G_u}
+  float kh[CH][D];      // fold: k_u o e^{G_15 - G_u}
+  float ws[2][CH][D];   // fold: partial (K o e^G) S_c over the two key halves
+  float u[CH][D];       // fold: U
+};
+
+// Row t of the open chunk (rows[0 .. t-1] cached; rows[t] holds k_t, v_t, g_t in the G slot and beta_t;
+// scr.q holds q_t).  Completes rows[t] (G_t, A_t), and returns o_t[c] on threads c < 128.
+// S_c is read through a generic pointer ([128][128] fp32, row j = key channel j): shared or global memory.
+__device__ float cfbi_row(float* rows, Scratch& scr, int t, const float* Sc, int tid) {
+  float* rt = rows + t * RF;
+  const int warp = tid >> 5, lane = tid & 31;
+  // 1. G_t = G_{t-1} + g_t
+  if (tid < D) rt[R_G + tid] = __fadd_rn(t > 0 ? rows[(t - 1) * RF + R_G + tid] : 0.f, rt[R_G + tid]);
+  __syncthreads();
+  // 2. A_t[u] (u < t) and P_t[u] (u <= t): warp w takes u = w, w + 8; lane l channels 4l .. 4l+3 in order,
+  //    then a fixed xor butterfly; lane 0's sum is the value
+  for (int u = warp; u <= t; u += NT / 32) {
+    const float* ru = rows + u * RF;
+    float a = 0.f, p = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 4 * lane + i;
+      const float kk = __fmul_rn(ru[R_K + j], __expf(__fsub_rn(rt[R_G + j], ru[R_G + j])));
+      a = __fmaf_rn(rt[R_K + j], kk, a);
+      p = __fmaf_rn(scr.q[j], kk, p);
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) {
+      a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, m));
+      p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, m));
+    }
+    if (lane == 0) {
+      if (u < t) rt[R_A + u] = __fmul_rn(rt[R_BETA], a);
+      scr.p[u] = p;
+    }
+  }
+  __syncthreads();
+  // 3. R_t: z (I + A) = P_t by back substitution, R_t = z diag(beta)
+  if (tid == 0) {
+    float z[CH];
+#pragma unroll
+    for (int v = CH - 1; v >= 0; --v) {
+      if (v > t) continue;
+      float acc = scr.p[v];
+      for (int w = v + 1; w <= t; ++w) acc = __fmaf_rn(-z[w], rows[w * RF + R_A + v], acc);
+      z[v] = acc;
+      scr.r[v] = __fmul_rn(acc, rows[v * RF + R_BETA]);
+    }
+  }
+  __syncthreads();
+  // 4. qh (key channel j = tid) and oh (value column c = tid - 128)
+  if (tid < D) {
+    const int j = tid;
+    float acc = __fmul_rn(scr.q[j], __expf(rt[R_G + j]));
+    for (int u = 0; u <= t; ++u)
+      acc = __fmaf_rn(-scr.r[u], __fmul_rn(rows[u * RF + R_K + j], __expf(rows[u * RF + R_G + j])), acc);
+    scr.qh[j] = acc;
+  } else {
+    const int c = tid - D;
+    float acc = 0.f;
+    for (int u = 0; u <= t; ++u) acc = __fmaf_rn(scr.r[u], rows[u * RF + R_V + c], acc);
+    scr.oh[c] = acc;
+  }
+  __syncthreads();
+  // 5. o_t = S_c^T qh + oh: thread (c, half) sums its 64 key rows in order; then part0 + part1 + oh
+  {
+    const int c = tid & (D - 1), half = tid >> 7;
+    float acc = 0.f;
+    for (int j = 64 * half; j < 64 * half + 64; ++j) acc = __fmaf_rn(scr.qh[j], Sc[j * D + c], acc);
+    scr.part[half][c] = acc;
+  }
+  __syncthreads();
+  return tid < D ? __fadd_rn(__fadd_rn(scr.part[0][tid], scr.part[1][tid]), scr.oh[tid]) : 0.f;
+}
+
+// Advances the entry state over the full chunk in rows[0 .. 15]; Sc through a generic pointer.
+__device__ void cfbi_fold(const float* rows, Scratch& scr, float* Sc, int tid) {
+  const float* last = rows + (CH - 1) * RF;
+  for (int e = tid; e < CH * D; e += NT) {
+    const int u = e / D, j = e % D;
+    const float* ru = rows + u * RF;
+    scr.kp[u][j] = __fmul_rn(ru[R_K + j], __expf(ru[R_G + j]));
+    scr.kh[u][j] = __fmul_rn(ru[R_K + j], __expf(__fsub_rn(last[R_G + j], ru[R_G + j])));
+  }
+  __syncthreads();
+  // (K o e^G) S_c: thread (c, half) over its 64 key rows in order, for every row u
+  {
+    const int c = tid & (D - 1), half = tid >> 7;
+    float acc[CH];
+#pragma unroll
+    for (int u = 0; u < CH; ++u) acc[u] = 0.f;
+    for (int j = 64 * half; j < 64 * half + 64; ++j) {
+      const float s = Sc[j * D + c];
+#pragma unroll
+      for (int u = 0; u < CH; ++u) acc[u] = __fmaf_rn(scr.kp[u][j], s, acc[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < CH; ++u) scr.ws[half][u][c] = acc[u];
+  }
+  __syncthreads();
+  // U by forward substitution (value column c)
+  if (tid < D) {
+    const int c = tid;
+    for (int u = 0; u < CH; ++u) {
+      const float* ru = rows + u * RF;
+      const float ws = __fadd_rn(scr.ws[0][u][c], scr.ws[1][u][c]);
+      float acc = __fmul_rn(ru[R_BETA], __fsub_rn(ru[R_V + c], ws));
+      for (int w = 0; w < u; ++w) acc = __fmaf_rn(-ru[R_A + w], scr.u[w][c], acc);
+      scr.u[u][c] = acc;
+    }
+  }
+  __syncthreads();
+  // S_{c+1}[j][c] = e^{G_15[j]} S_c[j][c] + sum_u k_u[j] e^{G_15[j] - G_u[j]} U[u][c]
+  {
+    const int c = tid & (D - 1), half = tid >> 7;
+    for (int j = 64 * half; j < 64 * half + 64; ++j) {
+      float s = __fmul_rn(__expf(last[R_G + j]), Sc[j * D + c]);
+#pragma unroll
+      for (int u = 0; u < CH; ++u) s = __fmaf_rn(scr.kh[u][j], scr.u[u][c], s);
+      Sc[j * D + c] = s;
+    }
+  }
+  __syncthreads();
+}
+
+// The new token's inputs into rows[t] (k, v, g in the G slot, beta) and scr.q.
+template <typename Tin>
+__device__ __forceinline__ void cfbi_load_token(float* rows, Scratch& scr, int t, const Tin* q, const Tin* k,
+                                                const Tin* v, const float* g, const float* beta, size_t row, int tid) {
+  float* rt = rows + t * RF;
+  if (tid < D) {
+    rt[R_K + tid] = to_f32(k[row * D + tid]);
+    rt[R_G + tid] = g[row * D + tid];
+    scr.q[tid] = to_f32(q[row * D + tid]);
+  } else {
+    const int c = tid - D;
+    rt[R_V + c] = to_f32(v[row * D + c]);
+    if (c == 0) rt[R_BETA] = beta[row];
+  }
+  __syncthreads();
+}
+
+struct CfbiSmem {
+  alignas(16) float rows[CH * RF];
+  Scratch scr;
+  alignas(16) float sc[D * D];  // prefill only: the entry state staged in shared memory
+};
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(NT, 1) cfbi_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                             const Tin* __restrict__ v, const float* __restrict__ g,
+                                                             const float* __restrict__ beta, const int32_t* cu,
+                                                             int64_t T, int max_seqlen, int H, float* pool,
+                                                             float* cache, int32_t* counts, int num_slots,
+                                                             const int32_t* __restrict__ slot_ids,
+                                                             Tout* __restrict__ out, int32_t* status) {
+  extern __shared__ float4 smem4[];
+  CfbiSmem& s = *reinterpret_cast<CfbiSmem*>(smem4);
+  const int tid = threadIdx.x, h = blockIdx.x, i = blockIdx.y;
+  const int64_t s0 = cu[i], s1 = cu[i + 1];
+  if (s0 < 0 || s1 < s0 || s1 > T || s1 - s0 > (int64_t)max_seqlen) {
+    if (tid == 0) flag_status(status, KDA_DEV_SEQ_OOB);
+    return;
+  }
+  const int slot = slot_ids[i];
+  if (slot < 0 || slot >= num_slots) {
+    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    return;
+  }
+  float* Sg = pool + ((size_t)slot * H + h) * D * D;
+  float* cg = cache + ((size_t)slot * H + h) * CH * RF;
+  int32_t* cnt = counts + (size_t)slot * H + h;
+  int L = *cnt;
+  if (L < 0 || L >= CH) {
+    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    return;
+  }
+  for (int e = tid; e < D * D / 4; e += NT) reinterpret_cast<float4*>(s.sc)[e] = reinterpret_cast<const float4*>(Sg)[e];
+  for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(s.rows)[e] = reinterpret_cast<const float4*>(cg)[e];
+  __syncthreads();
+  for (int64_t t = s0; t < s1; ++t) {
+    const size_t row = (size_t)t * H + h;
+    cfbi_load_token(s.rows, s.scr, L, q, k, v, g, beta, row, tid);
+    const float o = cfbi_row(s.rows, s.scr, L, s.sc, tid);
+    if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
+    if (++L == CH) {
+      cfbi_fold(s.rows, s.scr, s.sc, tid);
+      L = 0;
+    }
+  }
+  for (int e = tid; e < D * D / 4; e += NT) reinterpret_cast<float4*>(Sg)[e] = reinterpret_cast<const float4*>(s.sc)[e];
+  for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(cg)[e] = reinterpret_cast<const float4*>(s.rows)[e];
+  if (tid == 0) {
+    *cnt = L;
+    add_work(status, (int32_t)(s1 - s0));
+  }
+}
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(NT, 1) cfbi_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                            const Tin* __restrict__ v, const float* __restrict__ g,
+                                                            const float* __restrict__ beta, int H, float* pool,
+                                                            float* cache, int32_t* counts, int num_slots,
+                                                            const int32_t* __restrict__ slot_ids,
+                                                            Tout* __restrict__ out, int32_t* status) {
+  extern __shared__ float4 smem4[];
+  CfbiSmem& s = *reinterpret_cast<CfbiSmem*>(smem4);
+  const int tid = threadIdx.x, b = blockIdx.x / H, h = blockIdx.x % H;
+  const int slot = slot_ids[b];
+  if (slot < 0 || slot >= num_slots) {
+    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    return;
+  }
+  float* Sg = pool + ((size_t)slot * H + h) * D * D;
+  float* cg = cache + ((size_t)slot * H + h) * CH * RF;
+  int32_t* cnt = counts + (size_t)slot * H + h;
+  const int L = *cnt;
+  if (L < 0 || L >= CH) {
+    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    return;
+  }
+  for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(s.rows)[e] = reinterpret_cast<const float4*>(cg)[e];
+  const size_t row = (size_t)b * H + h;
+  cfbi_load_token(s.rows, s.scr, L, q, k, v, g, beta, row, tid);  // (ends with a barrier)
+  const float o = cfbi_row(s.rows, s.scr, L, Sg, tid);
+  if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
+  if (L + 1 == CH) {
+    cfbi_fold(s.rows, s.scr, Sg, tid);
+    if (tid == 0) *cnt = 0;
+  } else {
+    for (int e = tid; e < RF / 4; e += NT)
+      reinterpret_cast<float4*>(cg + L * RF)[e] = reinterpret_cast<const float4*>(s.rows + L * RF)[e];
+    if (tid == 0) *cnt = L + 1;
+  }
+  if (tid == 0) add_work(status, 1);
+}
+
+constexpr size_t PREFILL_SMEM = sizeof(CfbiSmem);
+constexpr size_t DECODE_SMEM = offsetof(CfbiSmem, sc);
+
+template <typename Tin, typename Tout>
+cudaError_t launch_prefill_t(const CfbiArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(cfbi_prefill_kernel<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)PREFILL_SMEM);
+  if (e != cudaSuccess) return e;
+  cfbi_prefill_kernel<Tin, Tout><<<dim3(a.H, a.N), NT, PREFILL_SMEM, st>>>(
+      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.cu,
+      a.T, a.max_seqlen, a.H, a.pool, a.cache, a.counts, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out),
+      a.status);
+  return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_decode_t(const CfbiArgs& a, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(cfbi_decode_kernel<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)DECODE_SMEM);
+  if (e != cudaSuccess) return e;
+  cfbi_decode_kernel<Tin, Tout><<<a.B * a.H, NT, DECODE_SMEM, st>>>(
+      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.H,
+      a.pool, a.cache, a.counts, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_cfbi_prefill(const CfbiArgs& a, cudaStream_t st) {
+  if (a.in_bf16) return a.out_bf16 ? launch_prefill_t<bf16, bf16>(a, st) : launch_prefill_t<bf16, float>(a, st);
+  return a.out_bf16 ? launch_prefill_t<float, bf16>(a, st) : launch_prefill_t<float, float>(a, st);
+}
+
+cudaError_t launch_cfbi_decode(const CfbiArgs& a, cudaStream_t st) {
+  if (a.in_bf16) return a.out_bf16 ? launch_decode_t<bf16, bf16>(a, st) : launch_decode_t<bf16, float>(a, st);
+  return a.out_bf16 ? launch_decode_t<float, bf16>(a, st) : launch_decode_t<float, float>(a, st);
+}
+
+}  // namespace kda

@@ -92,12 +92,34 @@ struct PrefillArgs {
   uint8_t* records;
 };
 
+// Batch-invariant (CF-BI) prefill and decode (d = 128).
+struct CfbiArgs {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  int B;                // decode: requests
+  int N;                // prefill: sequences
+  int64_t T;            // prefill: packed tokens
+  int max_seqlen;       // prefill
+  const int32_t* cu;    // prefill: cu_seqlens[N + 1]
+  int H;
+  bool in_bf16, out_bf16;
+  float* pool;
+  float* cache;
+  int32_t* counts;
+  int num_slots;
+  const int32_t* slot_ids;
+  void* out;
+  int32_t* status;
+};
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 // Tensor-core verify (bf16 inputs, d = 128, W <= 16, no per-token snapshots).
 bool verify_tc_supported(const VerifyArgs& a);
 cudaError_t launch_verify_tc(const VerifyArgs& a, cudaStream_t s);
 cudaError_t launch_fold(const FoldArgs& a, cudaStream_t s);
+cudaError_t launch_cfbi_prefill(const CfbiArgs& a, cudaStream_t s);
+cudaError_t launch_cfbi_decode(const CfbiArgs& a, cudaStream_t s);
 cudaError_t launch_state_copy(const CopyArgs& a, cudaStream_t s);
 
 // Sequential (token-by-token, CUDA-core) prefill; mode 0 = whole sequences.
