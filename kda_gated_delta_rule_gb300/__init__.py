@@ -26,7 +26,7 @@ __all__ = [
 KDA_OK = 0
 KDA_DEV_SLOT_OOB, KDA_DEV_SEQ_OOB, KDA_DEV_TIMEOUT, KDA_DEV_ACCEPT_OOB = 1, 2, 4, 8
 F32, BF16 = 0, 1
-CFBI_CHUNK, CFBI_ROW_FLOATS = 16, 416  # KDA_CFBI_CHUNK, KDA_CFBI_ROW_FLOATS
+CFBI_CHUNK, CFBI_ROW_FLOATS = 16, 420  # KDA_CFBI_CHUNK, KDA_CFBI_ROW_FLOATS
 
 # every function include/kda.h declares
 EXPORTED_SYMBOLS = (

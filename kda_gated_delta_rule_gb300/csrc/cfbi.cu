@@ -9,7 +9,7 @@
 // chunk from its entry state S_c (rows u = 0 .. t of the chunk, G_u the in-chunk cumulative log-decay):
 //   A_tu = beta_t sum_j k_t[j] k_u[j] exp(G_t[j] - G_u[j])  (u < t),
 //   P_tu =        sum_j q_t[j] k_u[j] exp(G_t[j] - G_u[j])  (u <= t),
-//   R_t  = row t of P (I + A)^-1 diag(beta)  (back substitution over u = t .. 0),
+//   R_t  = row t of P (I + A)^-1 diag(beta)  (rows of (I + A)^-1 extended one per row and cached),
 //   o_t  = S_c^T (q_t o e^{G_t} - sum_u R_tu k_u o e^{G_u}) + sum_u R_tu v_u,
 // and when the chunk is full the entry state advances:
 //   U = (I + A)^-1 diag(beta) (V - (K o e^G) S_c),   S_{c+1} = Diag(e^{G_15}) S_c + (K o e^{G_15 - G})^T U.
@@ -26,9 +26,10 @@ constexpr int D = 128;
 constexpr int NT = 256;
 constexpr int CH = KDA_CFBI_CHUNK;       // rows per chunk
 constexpr int RF = KDA_CFBI_ROW_FLOATS;  // floats per cached row
-// cached row layout: k | v | G (in-chunk cumulative log-decay) | A_t[u] (beta folded in, u < t) | beta
-constexpr int R_K = 0, R_V = 128, R_G = 256, R_A = 384, R_BETA = 400;
-static_assert(R_BETA + 1 <= RF && RF % 4 == 0, "row layout");
+// cached row layout: k | v | G (in-chunk cumulative log-decay) | A_t[u] (beta folded in, u < t) | beta |
+// T_t[v] = row t of (I + A)^-1 (v <= t)
+constexpr int R_K = 0, R_V = 128, R_G = 256, R_A = 384, R_BETA = 400, R_T = 401;
+static_assert(R_T + CH <= RF && RF % 4 == 0, "row layout");
 
 struct Scratch {
   float q[D];           // q_t (fp32)
@@ -44,9 +45,9 @@ struct Scratch {
 };
 
 // Row t of the open chunk (rows[0 .. t-1] cached; rows[t] holds k_t, v_t, g_t in the G slot and beta_t;
-// scr.q holds q_t).  Completes rows[t] (G_t, A_t), and returns o_t[c] on threads c < 128.
-// S_c is read through a generic pointer ([128][128] fp32, row j = key channel j): shared or global memory.
-__device__ float cfbi_row(float* rows, Scratch& scr, int t, const float* Sc, int tid) {
+// scr.q holds q_t).  Completes rows[t] (G_t, A_t, T_t), and returns o_t[c] on threads c < 128.
+// sv: this thread's part of the entry state, S_c[64 * half + e][c] for e < 64 (c = tid % 128, half = tid / 128).
+__device__ __forceinline__ float cfbi_row(float* rows, Scratch& scr, int t, const float (&sv)[64], int tid) {
   float* rt = rows + t * RF;
   const int warp = tid >> 5, lane = tid & 31;
   // 1. G_t = G_{t-1} + g_t
@@ -75,17 +76,20 @@ __device__ float cfbi_row(float* rows, Scratch& scr, int t, const float* Sc, int
     }
   }
   __syncthreads();
-  // 3. R_t: z (I + A) = P_t by back substitution, R_t = z diag(beta)
-  if (tid == 0) {
-    float z[CH];
-#pragma unroll
-    for (int v = CH - 1; v >= 0; --v) {
-      if (v > t) continue;
-      float acc = scr.p[v];
-      for (int w = v + 1; w <= t; ++w) acc = __fmaf_rn(-z[w], rows[w * RF + R_A + v], acc);
-      z[v] = acc;
-      scr.r[v] = __fmul_rn(acc, rows[v * RF + R_BETA]);
-    }
+  // 3. row t of T = (I + A)^-1 from the cached rows (lane v: T_t[v] = [v == t] - sum_{u=v}^{t-1} A_tu T_u[v]),
+  //    then z = P_t T (lane v: sum_{w=v}^{t} P_t[w] T_w[v]) and R_t = z diag(beta)
+  if (warp == 0 && lane < CH) {
+    const int v = lane;
+    float acc = v == t ? 1.f : 0.f;
+    for (int u = v; u < t; ++u) acc = __fmaf_rn(-rt[R_A + u], rows[u * RF + R_T + v], acc);
+    if (v <= t) rt[R_T + v] = acc;
+  }
+  __syncwarp();
+  if (warp == 0 && lane < CH) {
+    const int v = lane;
+    float acc = 0.f;
+    for (int w = v; w <= t; ++w) acc = __fmaf_rn(scr.p[w], rows[w * RF + R_T + v], acc);
+    scr.r[v] = v <= t ? __fmul_rn(acc, rows[v * RF + R_BETA]) : 0.f;
   }
   __syncthreads();
   // 4. qh (key channel j = tid) and oh (value column c = tid - 128)
@@ -106,15 +110,16 @@ __device__ float cfbi_row(float* rows, Scratch& scr, int t, const float* Sc, int
   {
     const int c = tid & (D - 1), half = tid >> 7;
     float acc = 0.f;
-    for (int j = 64 * half; j < 64 * half + 64; ++j) acc = __fmaf_rn(scr.qh[j], Sc[j * D + c], acc);
+#pragma unroll
+    for (int e = 0; e < 64; ++e) acc = __fmaf_rn(scr.qh[64 * half + e], sv[e], acc);
     scr.part[half][c] = acc;
   }
   __syncthreads();
   return tid < D ? __fadd_rn(__fadd_rn(scr.part[0][tid], scr.part[1][tid]), scr.oh[tid]) : 0.f;
 }
 
-// Advances the entry state over the full chunk in rows[0 .. 15]; Sc through a generic pointer.
-__device__ void cfbi_fold(const float* rows, Scratch& scr, float* Sc, int tid) {
+// Advances the entry state (this thread's part sv, as in cfbi_row) over the full chunk in rows[0 .. 15].
+__device__ __forceinline__ void cfbi_fold(const float* rows, Scratch& scr, float (&sv)[64], int tid) {
   const float* last = rows + (CH - 1) * RF;
   for (int e = tid; e < CH * D; e += NT) {
     const int u = e / D, j = e % D;
@@ -129,23 +134,33 @@ __device__ void cfbi_fold(const float* rows, Scratch& scr, float* Sc, int tid) {
     float acc[CH];
 #pragma unroll
     for (int u = 0; u < CH; ++u) acc[u] = 0.f;
-    for (int j = 64 * half; j < 64 * half + 64; ++j) {
-      const float s = Sc[j * D + c];
 #pragma unroll
-      for (int u = 0; u < CH; ++u) acc[u] = __fmaf_rn(scr.kp[u][j], s, acc[u]);
+    for (int e = 0; e < 64; ++e) {
+      const int j = 64 * half + e;
+#pragma unroll
+      for (int u = 0; u < CH; ++u) acc[u] = __fmaf_rn(scr.kp[u][j], sv[e], acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < CH; ++u) scr.ws[half][u][c] = acc[u];
   }
   __syncthreads();
-  // U by forward substitution (value column c)
-  if (tid < D) {
-    const int c = tid;
-    for (int u = 0; u < CH; ++u) {
+  // U = T diag(beta) (V - (K o e^G) S_c): value column c; thread (c, half) forms rows u of its half
+  {
+    const int c = tid & (D - 1), half = tid >> 7;
+    float y[CH];
+#pragma unroll
+    for (int w = 0; w < CH; ++w) {
+      const float* rw = rows + w * RF;
+      y[w] = __fmul_rn(rw[R_BETA], __fsub_rn(rw[R_V + c], __fadd_rn(scr.ws[0][w][c], scr.ws[1][w][c])));
+    }
+#pragma unroll
+    for (int uu = 0; uu < CH / 2; ++uu) {
+      const int u = (CH / 2) * half + uu;
       const float* ru = rows + u * RF;
-      const float ws = __fadd_rn(scr.ws[0][u][c], scr.ws[1][u][c]);
-      float acc = __fmul_rn(ru[R_BETA], __fsub_rn(ru[R_V + c], ws));
-      for (int w = 0; w < u; ++w) acc = __fmaf_rn(-ru[R_A + w], scr.u[w][c], acc);
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < CH; ++w)
+        if (w <= u) acc = __fmaf_rn(ru[R_T + w], y[w], acc);
       scr.u[u][c] = acc;
     }
   }
@@ -153,11 +168,16 @@ __device__ void cfbi_fold(const float* rows, Scratch& scr, float* Sc, int tid) {
   // S_{c+1}[j][c] = e^{G_15[j]} S_c[j][c] + sum_u k_u[j] e^{G_15[j] - G_u[j]} U[u][c]
   {
     const int c = tid & (D - 1), half = tid >> 7;
-    for (int j = 64 * half; j < 64 * half + 64; ++j) {
-      float s = __fmul_rn(__expf(last[R_G + j]), Sc[j * D + c]);
+    float uc[CH];
 #pragma unroll
-      for (int u = 0; u < CH; ++u) s = __fmaf_rn(scr.kh[u][j], scr.u[u][c], s);
-      Sc[j * D + c] = s;
+    for (int u = 0; u < CH; ++u) uc[u] = scr.u[u][c];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) {
+      const int j = 64 * half + e;
+      float s = __fmul_rn(__expf(last[R_G + j]), sv[e]);
+#pragma unroll
+      for (int u = 0; u < CH; ++u) s = __fmaf_rn(scr.kh[u][j], uc[u], s);
+      sv[e] = s;
     }
   }
   __syncthreads();
@@ -183,8 +203,19 @@ __device__ __forceinline__ void cfbi_load_token(float* rows, Scratch& scr, int t
 struct CfbiSmem {
   alignas(16) float rows[CH * RF];
   Scratch scr;
-  alignas(16) float sc[D * D];  // prefill only: the entry state staged in shared memory
 };
+
+// this thread's part of a [128][128] state: rows 64 * half .. +63 of column c
+__device__ __forceinline__ void load_part(float (&sv)[64], const float* S, int tid) {
+  const float* p = S + (size_t)64 * (tid >> 7) * D + (tid & (D - 1));
+#pragma unroll
+  for (int e = 0; e < 64; ++e) sv[e] = p[(size_t)e * D];
+}
+__device__ __forceinline__ void store_part(const float (&sv)[64], float* S, int tid) {
+  float* p = S + (size_t)64 * (tid >> 7) * D + (tid & (D - 1));
+#pragma unroll
+  for (int e = 0; e < 64; ++e) p[(size_t)e * D] = sv[e];
+}
 
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(NT, 1) cfbi_prefill_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
@@ -215,20 +246,21 @@ __global__ void __launch_bounds__(NT, 1) cfbi_prefill_kernel(const Tin* __restri
     if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
     return;
   }
-  for (int e = tid; e < D * D / 4; e += NT) reinterpret_cast<float4*>(s.sc)[e] = reinterpret_cast<const float4*>(Sg)[e];
+  float sv[64];
+  load_part(sv, Sg, tid);
   for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(s.rows)[e] = reinterpret_cast<const float4*>(cg)[e];
   __syncthreads();
   for (int64_t t = s0; t < s1; ++t) {
     const size_t row = (size_t)t * H + h;
     cfbi_load_token(s.rows, s.scr, L, q, k, v, g, beta, row, tid);
-    const float o = cfbi_row(s.rows, s.scr, L, s.sc, tid);
+    const float o = cfbi_row(s.rows, s.scr, L, sv, tid);
     if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
     if (++L == CH) {
-      cfbi_fold(s.rows, s.scr, s.sc, tid);
+      cfbi_fold(s.rows, s.scr, sv, tid);
       L = 0;
     }
   }
-  for (int e = tid; e < D * D / 4; e += NT) reinterpret_cast<float4*>(Sg)[e] = reinterpret_cast<const float4*>(s.sc)[e];
+  store_part(sv, Sg, tid);
   for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(cg)[e] = reinterpret_cast<const float4*>(s.rows)[e];
   if (tid == 0) {
     *cnt = L;
@@ -237,7 +269,7 @@ __global__ void __launch_bounds__(NT, 1) cfbi_prefill_kernel(const Tin* __restri
 }
 
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(NT, 1) cfbi_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+__global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
                                                             const Tin* __restrict__ v, const float* __restrict__ g,
                                                             const float* __restrict__ beta, int H, float* pool,
                                                             float* cache, int32_t* counts, int num_slots,
@@ -259,13 +291,16 @@ __global__ void __launch_bounds__(NT, 1) cfbi_decode_kernel(const Tin* __restric
     if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
     return;
   }
+  float sv[64];
+  load_part(sv, Sg, tid);  // in flight while the row's own quantities are formed
   for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(s.rows)[e] = reinterpret_cast<const float4*>(cg)[e];
   const size_t row = (size_t)b * H + h;
   cfbi_load_token(s.rows, s.scr, L, q, k, v, g, beta, row, tid);  // (ends with a barrier)
-  const float o = cfbi_row(s.rows, s.scr, L, Sg, tid);
+  const float o = cfbi_row(s.rows, s.scr, L, sv, tid);
   if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
   if (L + 1 == CH) {
-    cfbi_fold(s.rows, s.scr, Sg, tid);
+    cfbi_fold(s.rows, s.scr, sv, tid);
+    store_part(sv, Sg, tid);
     if (tid == 0) *cnt = 0;
   } else {
     for (int e = tid; e < RF / 4; e += NT)
@@ -276,7 +311,7 @@ __global__ void __launch_bounds__(NT, 1) cfbi_decode_kernel(const Tin* __restric
 }
 
 constexpr size_t PREFILL_SMEM = sizeof(CfbiSmem);
-constexpr size_t DECODE_SMEM = offsetof(CfbiSmem, sc);
+constexpr size_t DECODE_SMEM = sizeof(CfbiSmem);
 
 template <typename Tin, typename Tout>
 cudaError_t launch_prefill_t(const CfbiArgs& a, cudaStream_t st) {

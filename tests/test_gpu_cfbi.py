@@ -16,7 +16,7 @@ from tests._gpu import dev, host, rel_err, status
 
 pytestmark = pytest.mark.gpu
 
-CH, RF = 16, 416
+CH, RF = 16, 420
 
 
 def _problem(lengths, H, dtype, seed):
