@@ -14,6 +14,9 @@ Functions follow these passages:
 * ``transition`` -- "Kimi K3 infra report reading", sections 4.1-4.2 (the
   per-token transition M_t = (I - beta k k^T) Diag(alpha) and a segment's
   cumulative transition M, the first KCP fragment).
+* ``backward`` -- the vector-Jacobian product of ``recurrence`` (every forward
+  line of the KDA math box differentiated in reverse order), the gradient the
+  training side of "Kimi K3 infra report reading", section 7, needs.
 * ``decode``, ``verify``, ``fold`` -- the same recurrence over 1 or W tokens;
   "SGLang and Miles day-0 support for Kimi K3", section "ReplaySSM": verify
   reads the committed state and never writes it, fold replays only the accepted
@@ -70,6 +73,9 @@ def _load():
         lib.kda_oracle_recurrence.restype = i32
         lib.kda_oracle_recurrence.argtypes = [i32, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp,
                                               vp, i64, vp, vp, i32, i32]
+        lib.kda_oracle_backward.restype = i32
+        lib.kda_oracle_backward.argtypes = [i32, vp, i32, i32, i32, i32, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp,
+                                            vp, vp, vp, vp, vp, vp, i32, i32]
         lib.kda_oracle_transition.restype = i32
         lib.kda_oracle_transition.argtypes = [i32, vp, i32, i32, i32, vp, i32, vp, vp, vp, i32]
         _lib = lib
@@ -153,6 +159,58 @@ def recurrence(q, k, v, g, beta, cu_seqlens, s0=None, want_o=True, sample_t=None
     out = {"o": o, "o_samples": osamp, "s_final": s_final, "threads": rc}
     if snap_every > 0:
         out["snaps"] = [snaps[base[i]:base[i] + lens[i] // snap_every] for i in range(N)]
+    return out
+
+
+BACKWARD_MUTATIONS = {
+    "none": 0,
+    "no_out_grad": 1,
+    "no_read_grad": 2,
+    "dg_no_alpha": 3,
+    "dk_no_read": 4,
+    "dbeta_sign": 5,
+    "no_gate_carry": 6,
+    "dq_pre_write": 7,
+}
+
+
+def backward(q, k, v, g, beta, cu_seqlens, do, s0=None, ds_final=None, mutation="none", threads=0):
+    """Gradients of L = sum_t <do_t, o_t> + <ds_final, S_T> through the fp64 recurrence.
+
+    Inputs as for ``recurrence``; do: [T, H, dv] (float32, bf16 bits as uint16, or float64);
+    ds_final: [N, H, dk, dv] or None (zero).  Returns a dict of fp64 arrays 'dq', 'dk' [T,H,dk],
+    'dv' [T,H,dv], 'dg' [T,H,dk], 'dbeta' [T,H], 'ds0' [N,H,dk,dv] and 'threads'.
+    """
+    q, k, v, do = (np.ascontiguousarray(x) for x in (q, k, v, do))
+    g, beta = np.ascontiguousarray(g), np.ascontiguousarray(beta)
+    xd = _xdtype(q)
+    if _xdtype(k) != xd or _xdtype(v) != xd:
+        raise TypeError("q, k, v must share a dtype")
+    gd = _gdtype(g)
+    if _gdtype(beta) != gd:
+        raise TypeError("g and beta must share a dtype")
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    if (k.shape != (T, H, dk) or v.shape[:2] != (T, H) or g.shape != (T, H, dk) or beta.shape != (T, H)
+            or do.shape != (T, H, dv)):
+        raise ValueError("shape mismatch")
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, np.int64))
+    N = len(cu) - 1
+    if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("bad cu_seqlens")
+    f64 = lambda x: None if x is None else np.ascontiguousarray(np.asarray(x, np.float64).reshape(N, H, dk, dv))
+    s0d, dsd = f64(s0), f64(ds_final)
+    out = {"dq": np.zeros((T, H, dk)), "dk": np.zeros((T, H, dk)), "dv": np.zeros((T, H, dv)),
+           "dg": np.zeros((T, H, dk)), "dbeta": np.zeros((T, H)), "ds0": np.zeros((N, H, dk, dv))}
+    rc = _load().kda_oracle_backward(N, cu.ctypes.data, H, dk, dv, xd, q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                     gd, g.ctypes.data, beta.ctypes.data, _ptr(s0d), _xdtype(do), do.ctypes.data,
+                                     _ptr(dsd), *(out[n].ctypes.data for n in ("dq", "dk", "dv", "dg", "dbeta", "ds0")),
+                                     BACKWARD_MUTATIONS[mutation], int(threads))
+    if rc == -2:
+        raise MemoryError("oracle backward ran out of host memory")
+    if rc < 0:
+        raise ValueError("oracle rejected its arguments")
+    out["threads"] = rc
     return out
 
 

@@ -9,6 +9,9 @@
   lower-triangular solve and decay-rescaled keys), derived from the recurrence
   by induction over the tokens of a chunk.  It is the algebra the CUDA kernels
   use, checked here in fp64 against the sequential oracle.
+* ``chunked_backward`` -- the reverse-mode derivative of that chunk algebra (the
+  backward kernels' algebra), checked in fp64 against the oracle's sequential
+  backward.
 """
 from __future__ import annotations
 
@@ -86,3 +89,94 @@ def chunked(q, k, v, g, beta, S0, C=64, L=16, dtype=np.float64):
         khat = kc * np.exp(G[-1] - G)
         S = np.exp(G[-1])[:, None] * S + khat.T @ U
     return O, S
+
+
+def chunked_backward(q, k, v, g, beta, S0, dO, dST, C=64):
+    """Chunk-parallel gradients of L = sum_t <dO_t, o_t> + <dST, S_T> for one head (fp64).
+
+    The reverse-mode derivative of ``chunked``'s algebra, with the pair decays taken pairwise,
+    E_ts = exp(G_t - G_s) <= 1 for s <= t.  Per chunk with entry state S and
+    K+ = K o e^G, Q+ = Q o e^G, K^ = K o e^(G_C - G), a_ts = sum_j k_t k_s E_ts (s < t), A = diag(beta) a,
+    P_ts = sum_j q_t k_s E_ts (s <= t), T = (I + A)^-1, W = T diag(beta) K+, U = T diag(beta) V - W S:
+      dU = P^T dO + K^ dS'                      dS  = Q+^T dO + Diag(e^G_C) dS' - W^T dU
+      dP = tril(dO U^T)   dQ+ = dO S^T   dK^ = U dS'^T   dW = -dU S^T   d(e^G_C) = rowsum(dS' o S)
+      dT = dW (diag(beta) K+)^T + dU (diag(beta) V)^T      dA = -T^T dT T^T (strictly lower part)
+    then the chain rule through beta, the e^G factors and the pair decays, and dg = the in-chunk reverse
+    cumulative sum of dG.  The entry states run forward over the chunks and dS backward.
+    Returns dict dq, dk, dv, dg [T, .], dbeta [T], ds0 [dk, dv].
+    """
+    f = lambda x: np.asarray(x, np.float64)
+    q, k, v, g, beta, dO = f(q), f(k), f(v), f(g), f(beta), f(dO)
+    T, dk = q.shape
+    dv = v.shape[1]
+    starts = list(range(0, T, C))
+    # forward: entry state of every chunk
+    S = f(S0).copy()
+    entry, parts = [], []
+    for c0 in starts:
+        c1 = min(c0 + C, T)
+        n = c1 - c0
+        kc, vc, qc, bc = k[c0:c1], v[c0:c1], q[c0:c1], beta[c0:c1]
+        G = np.cumsum(g[c0:c1], axis=0)
+        E = np.exp(G[:, None, :] - G[None, :, :])        # [t, s, j]; used only where s <= t
+        low = np.tril(np.ones((n, n)), -1)
+        a = np.einsum("tj,sj,tsj->ts", kc, kc, E) * low
+        P = np.einsum("tj,sj,tsj->ts", qc, kc, E) * np.tril(np.ones((n, n)))
+        A = bc[:, None] * a
+        Tm = np.linalg.inv(np.eye(n) + A)
+        kp, qp, kh = kc * np.exp(G), qc * np.exp(G), kc * np.exp(G[-1] - G)
+        BK, BV = bc[:, None] * kp, bc[:, None] * vc
+        W = Tm @ BK
+        U = Tm @ BV - W @ S
+        entry.append(S)
+        parts.append(dict(G=G, E=E, a=a, P=P, Tm=Tm, kp=kp, qp=qp, kh=kh, BK=BK, BV=BV, W=W, U=U))
+        S = np.exp(G[-1])[:, None] * S + kh.T @ U
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v), dg=np.zeros_like(g),
+               dbeta=np.zeros_like(beta))
+    dS = f(dST).copy()
+    for ci in range(len(starts) - 1, -1, -1):
+        c0 = starts[ci]
+        c1 = min(c0 + C, T)
+        n = c1 - c0
+        z = parts[ci]
+        S = entry[ci]
+        kc, vc, qc, bc, dOc = k[c0:c1], v[c0:c1], q[c0:c1], beta[c0:c1], dO[c0:c1]
+        dU = z["P"].T @ dOc + z["kh"] @ dS
+        dP = np.tril(dOc @ z["U"].T)
+        dqp = dOc @ S.T
+        dkh = z["U"] @ dS.T
+        dgamC = (dS * S).sum(axis=1)
+        dW = -dU @ S.T
+        dT = dW @ z["BK"].T + dU @ z["BV"].T
+        dBK = z["Tm"].T @ dW
+        dBV = z["Tm"].T @ dU
+        dA = np.tril(-z["Tm"].T @ dT @ z["Tm"].T, -1)
+        dS_entry = z["qp"].T @ dOc + np.exp(z["G"][-1])[:, None] * dS - z["W"].T @ dU
+        dbeta = (dA * z["a"]).sum(axis=1) + (dBK * z["kp"]).sum(axis=1) + (dBV * vc).sum(axis=1)
+        da = bc[:, None] * dA
+        dkp = bc[:, None] * dBK
+        dvc = bc[:, None] * dBV
+        eG = np.exp(z["G"])
+        dqc = dqp * eG
+        dkc = dkp * eG + dkh * np.exp(z["G"][-1] - z["G"])
+        dG = dqp * z["qp"] + dkp * z["kp"] - dkh * z["kh"]
+        dGC = (dkh * z["kh"]).sum(axis=0) + dgamC * np.exp(z["G"][-1])
+        E = z["E"]
+        # a_ts = sum_j k_t k_s E_ts (s < t)
+        X = da[:, :, None] * kc[:, None, :] * kc[None, :, :] * E
+        dkc += np.einsum("ts,sj,tsj->tj", da, kc, E) + np.einsum("ts,tj,tsj->sj", da, kc, E)
+        dG += X.sum(axis=1) - X.sum(axis=0)
+        # P_ts = sum_j q_t k_s E_ts (s <= t)
+        Y = dP[:, :, None] * qc[:, None, :] * kc[None, :, :] * E
+        dqc += np.einsum("ts,sj,tsj->tj", dP, kc, E)
+        dkc += np.einsum("ts,tj,tsj->sj", dP, qc, E)
+        dG += Y.sum(axis=1) - Y.sum(axis=0)
+        dG[-1] += dGC
+        out["dq"][c0:c1] = dqc
+        out["dk"][c0:c1] = dkc
+        out["dv"][c0:c1] = dvc
+        out["dbeta"][c0:c1] = dbeta
+        out["dg"][c0:c1] = np.cumsum(dG[::-1], axis=0)[::-1]
+        dS = dS_entry
+    out["ds0"] = dS
+    return out
