@@ -303,6 +303,60 @@ kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const fl
                            int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
                            int32_t* dev_status, kda_stream_t stream);
 
+/*
+ * Backward (vector-Jacobian product) of a packed prefill.
+ * Source: the recurrence above ("Kimi K3: Architecture and SGLang Day-0 Support", KDA math box), whose
+ * gradient the training side needs ("Kimi K3 training and serving infra" (marsggbo blog), section 7).
+ * For the loss L = sum_t <d_out_t, o_t> + sum_i <d_final_i, S_T(i)>, where o and S_T(i) are the outputs and
+ * final states kda_prefill_varlen computes from the same inputs, it returns dL/dq, dL/dk, dL/dv, dL/dg,
+ * dL/dbeta and dL/dS_0.  The forward is recomputed inside the call (nothing is saved between the two);
+ * the chunk algebra it differentiates is the one of kda_prefill_varlen, taken in fp32 on the CUDA cores.
+ * Pair decays e^(G_t - G_s) are split at 16-token references while every factor stays below e^80, which
+ * holds whenever g >= -5; a block of a chunk that would exceed it takes them one by one.
+ */
+typedef struct {
+  const void* q;             /* [T][H][dk] in_dtype */
+  const void* k;             /* [T][H][dk] in_dtype */
+  const void* v;             /* [T][H][dv] in_dtype */
+  const float* g;            /* [T][H][dk] log-decay, <= 0 */
+  const float* beta;         /* [T][H] */
+  kda_dtype in_dtype;        /* also the dtype of d_out */
+  int64_t T;                 /* total packed tokens (host) */
+  int H, dk, dv;             /* dk = dv = 128 (KDA_ERR_UNSUPPORTED otherwise) */
+  int N;                     /* sequences (host), <= 65535 */
+  const int32_t* cu_seqlens; /* int32[N+1] device */
+  int32_t max_seqlen;        /* host: an upper bound on every sequence length */
+  const float* pool;         /* [num_slots][H][dk][dv]: initial states (read only), unless init_zero */
+  int32_t num_slots;
+  const int32_t* slot_ids;   /* int32[N] device, unless init_zero */
+  int init_zero;             /* nonzero: every sequence starts from a zero state (pool, slot_ids unused) */
+  const void* d_out;         /* [T][H][dv] in_dtype: dL/do */
+  const float* d_final;      /* [N][H][dk][dv] fp32 dL/dS_T, or NULL for zero */
+  float* dq;                 /* [T][H][dk] fp32 outputs */
+  float* dk_out;             /* [T][H][dk] */
+  float* dv_out;             /* [T][H][dv] */
+  float* dg;                 /* [T][H][dk] */
+  float* dbeta;              /* [T][H] */
+  float* d_init;             /* [N][H][dk][dv] fp32 dL/dS_0, or NULL (not written) */
+  void* workspace;           /* >= kda_backward_workspace_size(a) bytes of device scratch, 256-byte aligned */
+  size_t workspace_bytes;
+  int32_t* dev_status;       /* optional int32[2] */
+} kda_backward_args;
+
+/* sizeof(kda_backward_args), so a binding can check its mirror of the struct. */
+size_t kda_backward_args_bytes(void);
+
+/* Workspace of kda_prefill_backward: (ceil(T/64) + N) * H * 574720 bytes (fp32 intermediates per chunk). */
+size_t kda_backward_workspace_size(const kda_backward_args* a);
+
+/*
+ * kda_prefill_backward -- enqueue the backward.  Every output element of a token of a listed sequence is
+ * written; dq, dk, dg are written for all dk channels.  A slot id out of range sets KDA_DEV_SLOT_OOB and
+ * that sequence is differentiated from a zero initial state; malformed cu_seqlens set KDA_DEV_SEQ_OOB and
+ * that sequence's outputs are not written.  The work counter counts (token x head) pairs.
+ */
+kda_status kda_prefill_backward(const kda_backward_args* a, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

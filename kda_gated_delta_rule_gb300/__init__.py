@@ -20,7 +20,8 @@ __all__ = [
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
-    "kda_cfbi_decode", "CFBI_CHUNK", "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
+    "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "CFBI_CHUNK", "CFBI_ROW_FLOATS",
+    "EXPORTED_SYMBOLS",
 ]
 
 KDA_OK = 0
@@ -35,7 +36,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
-    "kda_cfbi_decode",
+    "kda_cfbi_decode", "kda_backward_args_bytes", "kda_backward_workspace_size", "kda_prefill_backward",
 )
 
 
@@ -56,6 +57,21 @@ class PrefillArgs(ctypes.Structure):
         ("out_dtype", ctypes.c_int), ("extra_pool", ctypes.c_void_p), ("num_extra_slots", ctypes.c_int32),
         ("extra_slot_ids", ctypes.c_void_p), ("snapshot_every_chunks", ctypes.c_int32),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t), ("dev_status", ctypes.c_void_p),
+    ]
+
+
+class BackwardArgs(ctypes.Structure):
+    """Mirror of kda_backward_args."""
+    _fields_ = [
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("g", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("in_dtype", ctypes.c_int), ("T", ctypes.c_int64), ("H", ctypes.c_int),
+        ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("N", ctypes.c_int), ("cu_seqlens", ctypes.c_void_p),
+        ("max_seqlen", ctypes.c_int32), ("pool", ctypes.c_void_p), ("num_slots", ctypes.c_int32),
+        ("slot_ids", ctypes.c_void_p), ("init_zero", ctypes.c_int), ("d_out", ctypes.c_void_p),
+        ("d_final", ctypes.c_void_p), ("dq", ctypes.c_void_p), ("dk_out", ctypes.c_void_p),
+        ("dv_out", ctypes.c_void_p), ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p),
+        ("d_init", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("dev_status", ctypes.c_void_p),
     ]
 
 
@@ -104,6 +120,9 @@ def load(build_if_missing: bool = False):
                                      i32, vp, vp, c_int, vp, vp]),
         "kda_cfbi_decode": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, i32, vp, vp,
                                     c_int, vp, vp]),
+        "kda_backward_args_bytes": (sz, []),
+        "kda_backward_workspace_size": (sz, [ctypes.POINTER(BackwardArgs)]),
+        "kda_prefill_backward": (c_int, [ctypes.POINTER(BackwardArgs), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -111,6 +130,8 @@ def load(build_if_missing: bool = False):
         fn.argtypes = args
     if lib.kda_prefill_args_bytes() != ctypes.sizeof(PrefillArgs):
         raise RuntimeError("kda_prefill_args layout mismatch between include/kda.h and the binding")
+    if lib.kda_backward_args_bytes() != ctypes.sizeof(BackwardArgs):
+        raise RuntimeError("kda_backward_args layout mismatch between include/kda.h and the binding")
     _lib = lib
     return lib
 
@@ -187,7 +208,7 @@ def kda_cfbi_cache_bytes_per_head(dk: int = 128, dv: int = 128) -> int:
 def kda_cfbi_prefill(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, cache, counts, slot_ids, out, dev_status=None,
                      stream=None):
     """CF-BI prefill over packed sequences: q, k, g [T, H, 128]; v, out [T, H, 128]; beta [T, H];
-    cu_seqlens int32 [N + 1]; pool [S, H, 128, 128]; cache [S, H, 16, 416] fp32; counts [S, H] int32."""
+    cu_seqlens int32 [N + 1]; pool [S, H, 128, 128]; cache [S, H, 16, 420] fp32; counts [S, H] int32."""
     _check(q, k, v, g, beta, cu_seqlens, pool, cache, counts, slot_ids, out, dev_status)
     T, H, dk = q.shape
     dv = v.shape[-1]
@@ -329,3 +350,51 @@ def kda_prefill_segmented_noalloc(q, k, v, g, beta, cu_seqlens, max_seqlen, pool
                         extra_slot_ids, snapshot_every_chunks, None, dev_status)
     _ok("kda_prefill_segmented_noalloc",
         load().kda_prefill_segmented_noalloc(ctypes.byref(a), int(segment_len), _stream(stream)))
+
+
+def _backward_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, d_out, dq, dk, dv, dg, dbeta, pool=None,
+                     slot_ids=None, d_final=None, d_init=None, workspace=None, dev_status=None):
+    _check(q, k, v, g, beta, cu_seqlens, d_out, dq, dk, dv, dg, dbeta, pool, slot_ids, d_final, d_init, workspace,
+           dev_status)
+    T, H, dkk = q.shape
+    a = BackwardArgs()
+    a.q, a.k, a.v, a.g, a.beta = (t.data_ptr() for t in (q, k, v, g, beta))
+    a.in_dtype = _dt(q)
+    a.T, a.H, a.dk, a.dv = T, H, dkk, v.shape[-1]
+    a.N = cu_seqlens.numel() - 1
+    a.cu_seqlens = cu_seqlens.data_ptr()
+    a.max_seqlen = int(max_seqlen)
+    if pool is None:
+        a.init_zero = 1
+    else:
+        a.pool, a.num_slots, a.slot_ids = pool.data_ptr(), pool.shape[0], slot_ids.data_ptr()
+    a.d_out = d_out.data_ptr()
+    a.dq, a.dk_out, a.dv_out, a.dg, a.dbeta = (t.data_ptr() for t in (dq, dk, dv, dg, dbeta))
+    if d_final is not None:
+        a.d_final = d_final.data_ptr()
+    if d_init is not None:
+        a.d_init = d_init.data_ptr()
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    if dev_status is not None:
+        a.dev_status = dev_status.data_ptr()
+    return a
+
+
+def kda_backward_workspace_size(T: int, N: int, H: int, dk: int = 128, dv: int = 128) -> int:
+    a = BackwardArgs()
+    a.T, a.N, a.H, a.dk, a.dv = T, N, H, dk, dv
+    return load().kda_backward_workspace_size(ctypes.byref(a))
+
+
+def kda_prefill_backward(q, k, v, g, beta, cu_seqlens, max_seqlen, d_out, dq, dk, dv, dg, dbeta, workspace,
+                         pool=None, slot_ids=None, d_final=None, d_init=None, dev_status=None, stream=None):
+    """Gradients of sum <d_out, o> + <d_final, S_T> through the packed prefill of (q, k, v, g, beta).
+
+    q, k, g, dq, dk, dg [T, H, 128]; v, d_out, dv [T, H, 128]; beta, dbeta [T, H]; cu_seqlens int32 [N + 1];
+    initial states pool[slot_ids] (or zero when pool is None); d_final, d_init [N, H, 128, 128] fp32 or None;
+    workspace: >= kda_backward_workspace_size(T, N, H) bytes.  Outputs are fp32.
+    """
+    a = _backward_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, d_out, dq, dk, dv, dg, dbeta, pool, slot_ids,
+                         d_final, d_init, workspace, dev_status)
+    _ok("kda_prefill_backward", load().kda_prefill_backward(ctypes.byref(a), _stream(stream)))

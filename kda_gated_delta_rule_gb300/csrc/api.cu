@@ -365,3 +365,61 @@ kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const fl
 }
 
 }  // extern "C"
+
+extern "C" {
+
+size_t kda_backward_args_bytes(void) { return sizeof(kda_backward_args); }
+
+size_t kda_backward_workspace_size(const kda_backward_args* a) {
+  if (!a || a->T < 0 || a->N < 0 || a->H <= 0) return 0;
+  return kda::backward_ws_bytes(a->T, a->N, a->H);
+}
+
+kda_status kda_prefill_backward(const kda_backward_args* a, kda_stream_t stream) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(a->in_dtype)) return KDA_ERR_INVALID_ARG;
+  if (a->H <= 0 || a->N < 0 || a->T < 0 || a->max_seqlen < 0 || a->num_slots < 0 || a->N > 65535 || a->H > 32767)
+    return KDA_ERR_INVALID_ARG;
+  if (a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED;
+  if (!a->cu_seqlens || !aligned16(a->cu_seqlens)) return KDA_ERR_INVALID_ARG;
+  if (!a->init_zero && (!a->pool || !a->slot_ids || !aligned16(a->pool) || !aligned16(a->slot_ids)))
+    return KDA_ERR_INVALID_ARG;
+  const void* dense[] = {a->q, a->k, a->v, a->g, a->beta, a->d_out, a->dq, a->dk_out, a->dv_out, a->dg, a->dbeta};
+  if (a->T > 0)
+    for (const void* p : dense)
+      if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if ((a->d_final && !aligned16(a->d_final)) || (a->d_init && !aligned16(a->d_init))) return KDA_ERR_INVALID_ARG;
+  if (a->N == 0) return KDA_OK;
+  const size_t need = kda::backward_ws_bytes(a->T, a->N, a->H);
+  if (a->workspace_bytes < need || !a->workspace || (reinterpret_cast<uintptr_t>(a->workspace) & 255u))
+    return KDA_ERR_WORKSPACE;
+  kda::BackwardArgs b{};
+  b.q = a->q;
+  b.k = a->k;
+  b.v = a->v;
+  b.g = a->g;
+  b.beta = a->beta;
+  b.in_bf16 = a->in_dtype == KDA_DTYPE_BF16;
+  b.T = a->T;
+  b.H = a->H;
+  b.N = a->N;
+  b.cu = a->cu_seqlens;
+  b.max_seqlen = a->max_seqlen;
+  b.pool = a->pool;
+  b.num_slots = a->num_slots;
+  b.slot_ids = a->slot_ids;
+  b.init_zero = a->init_zero != 0;
+  b.d_out = a->d_out;
+  b.d_final = a->d_final;
+  b.dq = a->dq;
+  b.dk = a->dk_out;
+  b.dv = a->dv_out;
+  b.dg = a->dg;
+  b.dbeta = a->dbeta;
+  b.d_init = a->d_init;
+  b.ws = static_cast<float*>(a->workspace);
+  b.status = a->dev_status;
+  return from_cuda(kda::launch_backward(b, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

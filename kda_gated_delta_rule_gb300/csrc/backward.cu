@@ -1,0 +1,915 @@
+// Chunked backward (vector-Jacobian product) of the KDA recurrence, dk = dv = 128, 64-token chunks.
+//
+// The forward recurrence is the KDA math box of "Kimi K3: Architecture and SGLang Day-0 Support"
+// (gate, read along the key, delta write; o = S^T q after the write); the training side that needs its
+// gradient is "Kimi K3 training and serving infra" (marsggbo blog), section 7.  The chunk algebra below is
+// derived from the recurrence by induction over a chunk (it is not printed on the pages).  Per chunk with
+// entry state S and in-chunk cumulative log-decay G (G_C its last row):
+//   K+ = K o e^G,  Q+ = Q o e^G,  K^ = K o e^(G_C - G),  a_ts = sum_j k_t k_s e^(G_t - G_s) (s < t),
+//   P_ts = sum_j q_t k_s e^(G_t - G_s) (s <= t),  T = (I + diag(beta) a)^-1,
+//   W = T diag(beta) K+,  U~ = T diag(beta) V,  U = U~ - W S,
+//   O = Q+ S + P U,  S' = Diag(e^G_C) S + K^^T U.
+// Its reverse, with dS' the gradient at the chunk's exit state:
+//   dU = P^T dO + K^ dS',   dS = Q+^T dO + Diag(e^G_C) dS' - W^T dU          (the carry, chunk to chunk)
+//   dQ+ = dO S^T,  dW = -dU S^T,  dK^ = U dS'^T,  dP = tril(dO U^T),  d(e^G_C) = rowsum(dS' o S)
+//   dT = dW (diag(beta) K+)^T + dU (diag(beta) V)^T,  dA = -T^T dT T^T (strictly lower)
+//   dK+ = diag(beta) T^T dW,  dv = diag(beta) T^T dU
+// and the chain rule through beta, the e^G factors and the pair decays e^(G_t - G_s); dg is the in-chunk
+// reverse cumulative sum of dG.  Pair decays are split at a reference token r per 16-token block of s,
+// e^(G_t - G_s) = e^(G_t - G_r) e^(G_r - G_s), while every factor stays below e^80 (always when g >= -5, the
+// pages' floor); a block that would exceed it takes the pair decays one by one.
+//
+// Six kernels, all in fp32 on the CUDA cores, handing over through a per-(chunk, head) fp32 workspace:
+//   prep (chunk-parallel) -> forward chain (entry states, U) -> reverse chain (dS', dU)
+//   -> state products -> WY backward -> per-channel assembly (chunk-parallel).
+#include "common.cuh"
+#include "launch.h"
+
+namespace kda {
+namespace {
+
+constexpr int C = 64;      // chunk length
+constexpr int D = 128;     // dk = dv
+constexpr int NT = 256;    // threads per CTA
+constexpr int LD = D + 1;  // shared row stride of [rows][128] tiles (odd: row and column walks are conflict-free)
+constexpr int LC = C + 1;  // shared row stride of [64][64] tiles
+constexpr int HC = 64;     // channels per CTA of the assembly kernel
+constexpr int CB = 16;     // value columns per CTA of the chain kernels
+constexpr float SPAN_MAX = 80.f;
+
+// Workspace record of one (chunk, head), fp32 element offsets.  All [64][128] / [128][128] / [64][64] tiles
+// are dense row-major.
+constexpr uint32_t BW_G = 0;                    // G [64][128]
+constexpr uint32_t BW_W = BW_G + C * D;         // W = T diag(beta) K+
+constexpr uint32_t BW_UT = BW_W + C * D;        // U~ = T diag(beta) V
+constexpr uint32_t BW_KH = BW_UT + C * D;       // K^ = K o e^(G_C - G)
+constexpr uint32_t BW_QP = BW_KH + C * D;       // Q+ = Q o e^G
+constexpr uint32_t BW_P = BW_QP + C * D;        // P [64][64] (s <= t)
+constexpr uint32_t BW_T = BW_P + C * C;         // T = (I + diag(beta) a)^-1 [64][64]
+constexpr uint32_t BW_A = BW_T + C * C;         // a [64][64] (s < t)
+constexpr uint32_t BW_GAM = BW_A + C * C;       // e^(G_C) [128]
+constexpr uint32_t BW_H = BW_GAM + D;           // entry state S [128][128]
+constexpr uint32_t BW_U = BW_H + D * D;         // U [64][128]
+constexpr uint32_t BW_DS = BW_U + C * D;        // dS' (gradient at the exit state) [128][128]
+constexpr uint32_t BW_DU = BW_DS + D * D;       // dU [64][128]
+constexpr uint32_t BW_DQP = BW_DU + C * D;      // dQ+ [64][128]
+constexpr uint32_t BW_DW = BW_DQP + C * D;      // dW [64][128]
+constexpr uint32_t BW_DKH = BW_DW + C * D;      // dK^ [64][128]
+constexpr uint32_t BW_DP = BW_DKH + C * D;      // dP [64][64]
+constexpr uint32_t BW_DGAM = BW_DP + C * C;     // d(e^G_C) [128]
+constexpr uint32_t BW_DKP = BW_DGAM + D;        // dK+ [64][128]
+constexpr uint32_t BW_DA = BW_DKP + C * D;      // dA [64][64]
+constexpr uint32_t BW_DBETA = BW_DA + C * C;    // dbeta through W and U~ [64]
+constexpr uint32_t BW_FLOATS = BW_DBETA + C;
+
+__device__ __forceinline__ void ld4(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+}
+__device__ __forceinline__ void ld4(const bf16* p, float (&x)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
+}
+
+// rows [0, rows) x columns [c0, c0 + ncols) of a row-major source (row r at src + r * stride) into shared
+// memory as fp32 with row stride ld; rows >= n are zero.
+template <typename Tin>
+__device__ __forceinline__ void load_rows(float* dst, int ld, const Tin* src, int64_t stride, int rows, int n, int c0,
+                                          int ncols) {
+  const int q4 = ncols / 4;
+  for (int e = threadIdx.x; e < rows * q4; e += NT) {
+    const int r = e / q4, c = (e % q4) * 4;
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (r < n) ld4(src + r * stride + c0 + c, x);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[r * ld + c + u] = x[u];
+  }
+}
+
+struct Seq {
+  int bos, eos;
+};
+
+// Bounds of sequence i; false (and the flag) when cu_seqlens is malformed.
+__device__ __forceinline__ bool seq_bounds(const BackwardArgs& a, int i, Seq& s, bool report) {
+  s.bos = a.cu[i];
+  s.eos = a.cu[i + 1];
+  if (s.bos < 0 || s.eos < s.bos || s.eos > a.T || s.eos - s.bos > a.max_seqlen) {
+    if (report && threadIdx.x == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
+    return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float* record(const BackwardArgs& a, int t0, int i, int h) {
+  return a.ws + ((size_t)(t0 / C + i) * a.H + h) * BW_FLOATS;
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 1. prep: G, a, P, T, W, U~, K^, Q+, e^G_C of one (chunk, head)
+// ---------------------------------------------------------------------------------------------------
+constexpr size_t PREP_SMEM = (5 * C * LD + 16 * LD + 3 * C * LC + C) * sizeof(float);
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
+  const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x;
+  Seq sq;
+  if (!seq_bounds(a, i, sq, c == 0 && h == 0)) return;
+  const int t0 = sq.bos + c * C;
+  if (t0 >= sq.eos) return;
+  const int n = min(C, sq.eos - t0);
+  float* w = record(a, t0, i, h);
+  extern __shared__ float sm[];
+  float* sK = sm;              // k [64][LD]
+  float* sQ = sK + C * LD;     // q
+  float* sG = sQ + C * LD;     // g, then G
+  float* sX = sG + C * LD;     // k o e^(G_t - G_r) of the current block; later diag(beta) K+, then diag(beta) V
+  float* sY = sX + C * LD;     // q o e^(G_t - G_r) of the current block
+  float* sM = sY + C * LD;     // k o e^(G_r - G_s) of the current block [16][LD]
+  float* sA = sM + 16 * LD;    // a [64][LC]
+  float* sP = sA + C * LC;     // P [64][LC]
+  float* sT = sP + C * LC;     // T [64][LC]
+  float* sB = sT + C * LC;     // beta [64]
+  const int64_t rs = (int64_t)a.H * D;
+  load_rows(sK, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows(sQ, LD, reinterpret_cast<const Tin*>(a.q) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows(sG, LD, a.g + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
+  for (int e = tid; e < C * LC; e += NT) sA[e] = 0.f, sP[e] = 0.f;
+  __syncthreads();
+  if (tid < D) {  // in-chunk cumulative sum, one thread per channel
+    float acc = 0.f;
+    for (int t = 0; t < C; ++t) {
+      acc += sG[t * LD + tid];
+      sG[t * LD + tid] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) add_work(a.status, n);
+
+  // a and P, one 16-column block of s at a time
+  for (int b0 = 0; b0 < n; b0 += 16) {
+    const int r = min(b0 + 15, n - 1);
+    bool wide = false;
+    if (tid < D) {
+      const float gr = sG[r * LD + tid];
+      for (int t = b0; t < C; ++t) wide |= sG[t * LD + tid] - gr > SPAN_MAX;
+      for (int s = b0; s <= r; ++s) wide |= gr - sG[s * LD + tid] > SPAN_MAX;
+    }
+    wide = __syncthreads_or(wide);
+    // thread -> row t = b0 + tid / 4, columns s = b0 + tid % 4 + 4m
+    const int t = b0 + (tid >> 2), sl = tid & 3;
+    if (!wide) {
+      for (int e = tid; e < 16 * D; e += NT) {
+        const int s = e / D, j = e % D;
+        sM[s * LD + j] = sK[(b0 + s) * LD + j] * __expf(sG[r * LD + j] - sG[(b0 + s) * LD + j]);
+      }
+      for (int e = tid; e < (C - b0) * D; e += NT) {
+        const int tt = b0 + e / D, j = e % D;
+        const float f = __expf(sG[tt * LD + j] - sG[r * LD + j]);
+        sX[tt * LD + j] = sK[tt * LD + j] * f;
+        sY[tt * LD + j] = sQ[tt * LD + j] * f;
+      }
+      __syncthreads();
+      if (t < C) {
+        float ac[4] = {0.f, 0.f, 0.f, 0.f}, pc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < D; ++j) {
+          const float x = sX[t * LD + j], y = sY[t * LD + j];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float km = sM[(sl + 4 * m) * LD + j];
+            ac[m] = fmaf(x, km, ac[m]);
+            pc[m] = fmaf(y, km, pc[m]);
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int s = b0 + sl + 4 * m;
+          sA[t * LC + s] = s < t ? ac[m] : 0.f;
+          sP[t * LC + s] = s <= t ? pc[m] : 0.f;
+        }
+      }
+    } else if (t < C) {
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+        const int s = b0 + sl + 4 * m;
+        float ac = 0.f, pc = 0.f;
+        if (s <= t)
+          for (int j = 0; j < D; ++j) {
+            const float e = __expf(sG[t * LD + j] - sG[s * LD + j]) * sK[s * LD + j];
+            ac = fmaf(sK[t * LD + j], e, ac);
+            pc = fmaf(sQ[t * LD + j], e, pc);
+          }
+        sA[t * LC + s] = s < t ? ac : 0.f;
+        sP[t * LC + s] = s <= t ? pc : 0.f;
+      }
+    }
+    __syncthreads();
+  }
+
+  // T = (I + diag(beta) a)^-1 by forward substitution, one column per lane of warps 0-1 (no barriers:
+  // column v only reads its own earlier entries).  Warps 2-7 meanwhile form diag(beta) K+ in sX.
+  if (tid < C) {
+    const int v = tid;
+    for (int u = 0; u < C; ++u) sT[u * LC + v] = u == v ? 1.f : 0.f;
+    for (int t = 1; t < C; ++t) {
+      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+      int u = 0;
+      for (; u + 3 < t; u += 4) {
+        s0 = fmaf(sA[t * LC + u], sT[u * LC + v], s0);
+        s1 = fmaf(sA[t * LC + u + 1], sT[(u + 1) * LC + v], s1);
+        s2 = fmaf(sA[t * LC + u + 2], sT[(u + 2) * LC + v], s2);
+        s3 = fmaf(sA[t * LC + u + 3], sT[(u + 3) * LC + v], s3);
+      }
+      for (; u < t; ++u) s0 = fmaf(sA[t * LC + u], sT[u * LC + v], s0);
+      if (t > v) sT[t * LC + v] = -sB[t] * ((s0 + s1) + (s2 + s3));
+    }
+  } else {
+    for (int e = tid - C; e < C * D; e += NT - C) {
+      const int s = e / D, j = e % D;
+      sX[s * LD + j] = sB[s] * sK[s * LD + j] * __expf(sG[s * LD + j]);
+    }
+  }
+  __syncthreads();
+
+  // records: G, a, P, T, e^G_C, K^, Q+ (elementwise), then W = T diag(beta) K+ and U~ = T diag(beta) V
+  for (int e = tid; e < C * D; e += NT) {
+    const int t = e / D, j = e % D;
+    const float G = sG[t * LD + j], GC = sG[(n - 1) * LD + j];
+    w[BW_G + e] = G;
+    w[BW_KH + e] = sK[t * LD + j] * __expf(GC - G);
+    w[BW_QP + e] = sQ[t * LD + j] * __expf(G);
+  }
+  for (int e = tid; e < C * C; e += NT) {
+    const int t = e / C, s = e % C;
+    w[BW_P + e] = sP[t * LC + s];
+    w[BW_T + e] = sT[t * LC + s];
+    w[BW_A + e] = sA[t * LC + s];
+  }
+  if (tid < D) w[BW_GAM + tid] = __expf(sG[(n - 1) * LD + tid]);
+  const int ty = tid >> 4, tx = tid & 15;  // rows ty + 16i, columns tx + 16m
+  {
+    float acc[4][8] = {};
+    for (int s = 0; s < C; ++s) {
+      float x[4], y[8];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[(ty + 16 * ii) * LC + s];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) y[m] = sX[s * LD + tx + 16 * m];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 8; ++m) w[BW_W + (ty + 16 * ii) * D + tx + 16 * m] = acc[ii][m];
+  }
+  __syncthreads();
+  load_rows(sX, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  __syncthreads();
+  {
+    float acc[4][8] = {};
+    for (int s = 0; s < C; ++s) {
+      float x[4], y[8];
+      const float bs = sB[s];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[(ty + 16 * ii) * LC + s] * bs;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) y[m] = sX[s * LD + tx + 16 * m];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 8; ++m) w[BW_UT + (ty + 16 * ii) * D + tx + 16 * m] = acc[ii][m];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 2. forward chain over the chunks of one (sequence, head, 16 value columns): entry states and U
+// ---------------------------------------------------------------------------------------------------
+constexpr size_t FWD_SMEM = (2 * C * LD + C * CB + D * CB + C * CB + D) * sizeof(float);
+
+__global__ void __launch_bounds__(NT) bwd_fwd_chain_kernel(BackwardArgs a) {
+  const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
+  Seq sq;
+  if (!seq_bounds(a, i, sq, false)) return;
+  extern __shared__ float sm[];
+  float* sW = sm;               // W [64][LD]
+  float* sKh = sW + C * LD;     // K^ [64][LD]
+  float* sUt = sKh + C * LD;    // U~ columns [64][CB]
+  float* sS = sUt + C * CB;     // state columns [128][CB]
+  float* sU = sS + D * CB;      // U columns [64][CB]
+  float* sGam = sU + C * CB;    // e^G_C [128]
+  const float* s0 = nullptr;
+  if (!a.init_zero) {
+    const int slot = a.slot_ids[i];
+    if (slot < 0 || slot >= a.num_slots) {
+      if (tid == 0 && cb == 0) flag_status(a.status, KDA_DEV_SLOT_OOB);
+    } else {
+      s0 = a.pool + ((size_t)slot * a.H + h) * D * D;
+    }
+  }
+  for (int e = tid; e < D * CB; e += NT) {
+    const int j = e / CB, cc = e % CB;
+    sS[e] = s0 ? s0[j * D + c0 + cc] : 0.f;
+  }
+  const int nc = (sq.eos - sq.bos + C - 1) / C;
+  for (int c = 0; c < nc; ++c) {
+    const int t0 = sq.bos + c * C;
+    float* w = record(a, t0, i, h);
+    load_rows(sW, LD, w + BW_W, D, C, C, 0, D);
+    load_rows(sKh, LD, w + BW_KH, D, C, C, 0, D);
+    load_rows(sUt, CB, w + BW_UT, D, C, C, c0, CB);
+    if (tid < D) sGam[tid] = w[BW_GAM + tid];
+    __syncthreads();
+    for (int e = tid; e < D * CB; e += NT) w[BW_H + (e / CB) * D + c0 + e % CB] = sS[e];
+    {  // U = U~ - W S: row t = tid / 4, columns tid % 4 + 4m
+      const int t = tid >> 2, cl = tid & 3;
+      float acc[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) acc[m] = 0.f;
+      for (int j = 0; j < D; ++j) {
+        const float x = sW[t * LD + j];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sS[j * CB + cl + 4 * m], acc[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int cc = cl + 4 * m;
+        const float u = sUt[t * CB + cc] - acc[m];
+        sU[t * CB + cc] = u;
+        w[BW_U + t * D + c0 + cc] = u;
+      }
+    }
+    __syncthreads();
+    {  // S = Diag(e^G_C) S + K^^T U: row j = tid / 2, columns tid % 2 + 2m (own elements only: in place)
+      const int j = tid >> 1, cl = tid & 1;
+      float acc[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+      for (int t = 0; t < C; ++t) {
+        const float x = sKh[t * LD + j];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[m] = fmaf(x, sU[t * CB + cl + 2 * m], acc[m]);
+      }
+      const float gm = sGam[j];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int cc = cl + 2 * m;
+        sS[j * CB + cc] = fmaf(gm, sS[j * CB + cc], acc[m]);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 3. reverse chain: dS' at every chunk exit, dU, and dS_0
+// ---------------------------------------------------------------------------------------------------
+constexpr size_t REV_SMEM = (C * LC + 3 * C * LD + C * CB + D * CB + C * CB + D) * sizeof(float);
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT) bwd_rev_chain_kernel(BackwardArgs a) {
+  const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
+  Seq sq;
+  if (!seq_bounds(a, i, sq, false)) return;
+  extern __shared__ float sm[];
+  float* sP = sm;               // P [64][LC]
+  float* sKh = sP + C * LC;     // K^ [64][LD]
+  float* sQp = sKh + C * LD;    // Q+ [64][LD]
+  float* sW = sQp + C * LD;     // W [64][LD]
+  float* sDO = sW + C * LD;     // dO columns [64][CB]
+  float* sdS = sDO + C * CB;    // dS columns [128][CB]
+  float* sdU = sdS + D * CB;    // dU columns [64][CB]
+  float* sGam = sdU + C * CB;   // e^G_C [128]
+  const float* dfin = a.d_final ? a.d_final + ((size_t)i * a.H + h) * D * D : nullptr;
+  for (int e = tid; e < D * CB; e += NT) sdS[e] = dfin ? dfin[(e / CB) * D + c0 + e % CB] : 0.f;
+  const int nc = (sq.eos - sq.bos + C - 1) / C;
+  const int64_t rs = (int64_t)a.H * D;
+  for (int c = nc - 1; c >= 0; --c) {
+    const int t0 = sq.bos + c * C, n = min(C, sq.eos - t0);
+    float* w = record(a, t0, i, h);
+    load_rows(sP, LC, w + BW_P, C, C, C, 0, C);
+    load_rows(sKh, LD, w + BW_KH, D, C, C, 0, D);
+    load_rows(sQp, LD, w + BW_QP, D, C, C, 0, D);
+    load_rows(sW, LD, w + BW_W, D, C, C, 0, D);
+    load_rows(sDO, CB, reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D, rs, C, n, c0, CB);
+    if (tid < D) sGam[tid] = w[BW_GAM + tid];
+    __syncthreads();
+    for (int e = tid; e < D * CB; e += NT) w[BW_DS + (e / CB) * D + c0 + e % CB] = sdS[e];
+    {  // dU = P^T dO + K^ dS': row t = tid / 4, columns tid % 4 + 4m
+      const int t = tid >> 2, cl = tid & 3;
+      float acc[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) acc[m] = 0.f;
+      for (int s = t; s < C; ++s) {
+        const float x = sP[s * LC + t];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sDO[s * CB + cl + 4 * m], acc[m]);
+      }
+      for (int j = 0; j < D; ++j) {
+        const float x = sKh[t * LD + j];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sdS[j * CB + cl + 4 * m], acc[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int cc = cl + 4 * m;
+        sdU[t * CB + cc] = acc[m];
+        w[BW_DU + t * D + c0 + cc] = acc[m];
+      }
+    }
+    __syncthreads();
+    {  // dS = Q+^T dO + Diag(e^G_C) dS' - W^T dU: row j = tid / 2, columns tid % 2 + 2m (in place)
+      const int j = tid >> 1, cl = tid & 1;
+      float acc[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+      for (int t = 0; t < C; ++t) {
+        const float x = sQp[t * LD + j], y = sW[t * LD + j];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          const int cc = cl + 2 * m;
+          acc[m] = fmaf(x, sDO[t * CB + cc], acc[m]);
+          acc[m] = fmaf(-y, sdU[t * CB + cc], acc[m]);
+        }
+      }
+      const float gm = sGam[j];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int cc = cl + 2 * m;
+        sdS[j * CB + cc] = fmaf(gm, sdS[j * CB + cc], acc[m]);
+      }
+    }
+    __syncthreads();
+  }
+  if (a.d_init) {
+    float* dst = a.d_init + ((size_t)i * a.H + h) * D * D;
+    for (int e = tid; e < D * CB; e += NT) dst[(e / CB) * D + c0 + e % CB] = sdS[e];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 4. state products of one (chunk, head): dQ+ = dO S^T, dW = -dU S^T, d(e^G_C), dP = tril(dO U^T), dK^ = U dS'^T
+// ---------------------------------------------------------------------------------------------------
+constexpr size_t STATE_SMEM = (D * LD + 2 * C * LD) * sizeof(float);
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) bwd_state_grads_kernel(BackwardArgs a) {
+  const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x;
+  Seq sq;
+  if (!seq_bounds(a, i, sq, false)) return;
+  const int t0 = sq.bos + c * C;
+  if (t0 >= sq.eos) return;
+  const int n = min(C, sq.eos - t0);
+  float* w = record(a, t0, i, h);
+  extern __shared__ float sm[];
+  float* sH = sm;               // S, later dS' [128][LD]
+  float* sD = sH + D * LD;      // dO [64][LD]
+  float* sE = sD + C * LD;      // dU, later U [64][LD]
+  load_rows(sH, LD, w + BW_H, D, D, D, 0, D);
+  load_rows(sD, LD, reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D, (int64_t)a.H * D, C, n, 0,
+            D);
+  load_rows(sE, LD, w + BW_DU, D, C, C, 0, D);
+  __syncthreads();
+  const int ty = tid >> 4, tx = tid & 15;  // rows ty + 16i, columns tx + 16m
+  {
+    float aq[4][8] = {}, aw[4][8] = {};
+    for (int l = 0; l < D; ++l) {
+      float x[4], y[4], z[8];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sD[(ty + 16 * ii) * LD + l], y[ii] = sE[(ty + 16 * ii) * LD + l];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) z[m] = sH[(tx + 16 * m) * LD + l];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          aq[ii][m] = fmaf(x[ii], z[m], aq[ii][m]);
+          aw[ii][m] = fmaf(y[ii], z[m], aw[ii][m]);
+        }
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int o = (ty + 16 * ii) * D + tx + 16 * m;
+        w[BW_DQP + o] = aq[ii][m];
+        w[BW_DW + o] = -aw[ii][m];
+      }
+  }
+  {  // d(e^G_C)_j = sum_l dS'_jl S_jl: warp per row, dS' streamed from the record
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int j = warp; j < D; j += NT / 32) {
+      float x[4];
+      ld4(w + BW_DS + j * D + 4 * lane, x);
+      float s = 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s = fmaf(x[u], sH[j * LD + 4 * lane + u], s);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) w[BW_DGAM + j] = s;
+    }
+  }
+  __syncthreads();
+  load_rows(sE, LD, w + BW_U, D, C, C, 0, D);
+  load_rows(sH, LD, w + BW_DS, D, D, D, 0, D);
+  __syncthreads();
+  {  // dP = tril(dO U^T)
+    float acc[4][4] = {};
+    for (int l = 0; l < D; ++l) {
+      float x[4], y[4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sD[(ty + 16 * ii) * LD + l];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) y[m] = sE[(tx + 16 * m) * LD + l];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int t = ty + 16 * ii, s = tx + 16 * m;
+        w[BW_DP + t * C + s] = s <= t ? acc[ii][m] : 0.f;
+      }
+  }
+  {  // dK^ = U dS'^T
+    float acc[4][8] = {};
+    for (int l = 0; l < D; ++l) {
+      float x[4], z[8];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sE[(ty + 16 * ii) * LD + l];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) z[m] = sH[(tx + 16 * m) * LD + l];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) acc[ii][m] = fmaf(x[ii], z[m], acc[ii][m]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 8; ++m) w[BW_DKH + (ty + 16 * ii) * D + tx + 16 * m] = acc[ii][m];
+  }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 5. WY backward of one (chunk, head): dT, dA, dK+ = diag(beta) T^T dW, dv = diag(beta) T^T dU, dbeta part
+// ---------------------------------------------------------------------------------------------------
+constexpr size_t WY_SMEM = (2 * C * LC + 4 * C * LD + C) * sizeof(float);
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
+  const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x;
+  Seq sq;
+  if (!seq_bounds(a, i, sq, false)) return;
+  const int t0 = sq.bos + c * C;
+  if (t0 >= sq.eos) return;
+  const int n = min(C, sq.eos - t0);
+  float* w = record(a, t0, i, h);
+  extern __shared__ float sm[];
+  float* sT = sm;                // T [64][LC]
+  float* sM = sT + C * LC;       // dT [64][LC]
+  float* sKp = sM + C * LC;      // K+ [64][LD]; later T^T dT [64][LC]
+  float* sV = sKp + C * LD;      // V [64][LD]
+  float* sDW = sV + C * LD;      // dW [64][LD]
+  float* sDU = sDW + C * LD;     // dU [64][LD]
+  float* sB = sDU + C * LD;      // beta [64]
+  const int64_t rs = (int64_t)a.H * D;
+  load_rows(sT, LC, w + BW_T, C, C, C, 0, C);
+  load_rows(sKp, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows(sV, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows(sDW, LD, w + BW_DW, D, C, C, 0, D);
+  load_rows(sDU, LD, w + BW_DU, D, C, C, 0, D);
+  if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
+  __syncthreads();
+  for (int e = tid; e < C * D; e += NT) sKp[(e / D) * LD + e % D] *= __expf(w[BW_G + e]);
+  __syncthreads();
+  const int ty = tid >> 4, tx = tid & 15;
+  {  // dT_ts = beta_s (dW_t . K+_s + dU_t . V_s)
+    float acc[4][4] = {};
+    for (int j = 0; j < D; ++j) {
+      float x[4], y[4], p[4], q[4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sDW[(ty + 16 * ii) * LD + j], y[ii] = sDU[(ty + 16 * ii) * LD + j];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) p[m] = sKp[(tx + 16 * m) * LD + j], q[m] = sV[(tx + 16 * m) * LD + j];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], p[m], fmaf(y[ii], q[m], acc[ii][m]));
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int s = tx + 16 * m;
+        sM[(ty + 16 * ii) * LC + s] = sB[s] * acc[ii][m];
+      }
+  }
+  {  // dB_K = T^T dW, dB_V = T^T dU (rows s, columns j); dK+ = beta dB_K, dv = beta dB_V, dbeta part
+    float bk[4][8] = {}, bv[4][8] = {};
+    for (int t = 0; t < C; ++t) {
+      float x[4], y[8], z[8];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[t * LC + ty + 16 * ii];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) y[m] = sDW[t * LD + tx + 16 * m], z[m] = sDU[t * LD + tx + 16 * m];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+          bk[ii][m] = fmaf(x[ii], y[m], bk[ii][m]);
+          bv[ii][m] = fmaf(x[ii], z[m], bv[ii][m]);
+        }
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+      const int s = ty + 16 * ii;
+      const float b = sB[s];
+      float part = 0.f;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int j = tx + 16 * m;
+        part = fmaf(bk[ii][m], sKp[s * LD + j], part);
+        part = fmaf(bv[ii][m], sV[s * LD + j], part);
+        w[BW_DKP + s * D + j] = b * bk[ii][m];
+        if (s < n) a.dv[((int64_t)(t0 + s) * a.H + h) * D + j] = b * bv[ii][m];
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      if (tx == 0) w[BW_DBETA + s] = part;
+    }
+  }
+  __syncthreads();
+  float* sN = sKp;  // T^T dT [64][LC]
+  {
+    float acc[4][4] = {};
+    for (int t = 0; t < C; ++t) {
+      float x[4], y[4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[t * LC + ty + 16 * ii];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) y[m] = sM[t * LC + tx + 16 * m];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) sN[(ty + 16 * ii) * LC + tx + 16 * m] = acc[ii][m];
+  }
+  __syncthreads();
+  {  // dA = -(T^T dT) T^T, strictly lower
+    float acc[4][4] = {};
+    for (int t = 0; t < C; ++t) {
+      float x[4], y[4];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) x[ii] = sN[(ty + 16 * ii) * LC + t];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) y[m] = sT[(tx + 16 * m) * LC + t];
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+    }
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int s = ty + 16 * ii, u = tx + 16 * m;
+        w[BW_DA + s * C + u] = u < s ? -acc[ii][m] : 0.f;
+      }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------------
+// 6. assembly of one (chunk, head, 64 channels): pair-decay terms, dq, dk, dg, dbeta
+// ---------------------------------------------------------------------------------------------------
+constexpr size_t ASM_SMEM = (6 * C * LC + 2 * 16 * LC + C) * sizeof(float);
+
+template <typename Tin>
+__global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
+  const int c = blockIdx.x, h = blockIdx.y >> 1, half = blockIdx.y & 1, i = blockIdx.z, tid = threadIdx.x;
+  Seq sq;
+  if (!seq_bounds(a, i, sq, false)) return;
+  const int t0 = sq.bos + c * C;
+  if (t0 >= sq.eos) return;
+  const int n = min(C, sq.eos - t0);
+  const int j0 = half * HC;
+  float* w = record(a, t0, i, h);
+  extern __shared__ float sm[];
+  float* sK = sm;               // k [64][LC] (this CTA's 64 channels)
+  float* sQ = sK + C * LC;      // q
+  float* sG = sQ + C * LC;      // G
+  float* sEp = sG + C * LC;     // e^(G_t - G_r) of the current block; later dG
+  float* sDP = sEp + C * LC;    // dP; later the G_C terms dK^ o K^
+  float* sDA = sDP + C * LC;    // dA (beta not folded in)
+  float* sKm = sDA + C * LC;    // k o e^(G_r - G_s) of the current block [16][LC]
+  float* sEm = sKm + 16 * LC;   // e^(G_r - G_s) [16][LC]
+  float* sB = sEm + 16 * LC;    // beta [64]
+  const int64_t rs = (int64_t)a.H * D;
+  const int64_t in0 = ((int64_t)t0 * a.H + h) * D;
+  load_rows(sK, LC, reinterpret_cast<const Tin*>(a.k) + in0, rs, C, n, j0, HC);
+  load_rows(sQ, LC, reinterpret_cast<const Tin*>(a.q) + in0, rs, C, n, j0, HC);
+  load_rows(sG, LC, w + BW_G, D, C, C, j0, HC);
+  load_rows(sDP, LC, w + BW_DP, C, C, C, 0, C);
+  load_rows(sDA, LC, w + BW_DA, C, C, C, 0, C);
+  if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
+  __syncthreads();
+  const int ty = tid >> 4, tx = tid & 15;  // own elements: rows ty + 16i, channels tx + 16m
+  float dqp[4][4] = {}, dkr[4][4] = {}, dkc[4][4] = {};
+  for (int bi = 0; bi * 16 < n; ++bi) {
+    const int b0 = bi * 16, r = min(b0 + 15, n - 1);
+    bool wide = false;
+    if (tid < HC) {
+      const float gr = sG[r * LC + tid];
+      for (int t = b0; t < C; ++t) wide |= sG[t * LC + tid] - gr > SPAN_MAX;
+      for (int s = b0; s <= r; ++s) wide |= gr - sG[s * LC + tid] > SPAN_MAX;
+    }
+    wide = __syncthreads_or(wide);
+    if (!wide) {
+      for (int e = tid; e < (C - b0) * HC; e += NT) {
+        const int t = b0 + e / HC, j = e % HC;
+        sEp[t * LC + j] = __expf(sG[t * LC + j] - sG[r * LC + j]);
+      }
+      for (int e = tid; e < 16 * HC; e += NT) {
+        const int s = e / HC, j = e % HC;
+        const float em = __expf(sG[r * LC + j] - sG[(b0 + s) * LC + j]);
+        sEm[s * LC + j] = em;
+        sKm[s * LC + j] = sK[(b0 + s) * LC + j] * em;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const int t = ty + 16 * ii;
+        if (t >= b0) {  // rows t: sum over s in the block (dP, dA masked below the diagonal already)
+          float r1[4] = {}, r2[4] = {};
+          for (int s = 0; s < 16; ++s) {
+            const float p = sDP[t * LC + b0 + s], q = sDA[t * LC + b0 + s];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const float km = sKm[s * LC + tx + 16 * m];
+              r1[m] = fmaf(p, km, r1[m]);
+              r2[m] = fmaf(q, km, r2[m]);
+            }
+          }
+          const float bt = sB[t];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const float ep = sEp[t * LC + tx + 16 * m];
+            dqp[ii][m] = fmaf(r1[m], ep, dqp[ii][m]);
+            dkr[ii][m] = fmaf(bt * r2[m], ep, dkr[ii][m]);
+          }
+        }
+      }
+      {  // own row s = ty + 16 bi lies in this block: sums over t >= b0
+        const int s = ty + 16 * bi;
+        float r3[4] = {};
+        for (int t = b0; t < C; ++t) {
+          const float p = sDP[t * LC + s], q = sB[t] * sDA[t * LC + s];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int j = tx + 16 * m;
+            const float ep = sEp[t * LC + j];
+            r3[m] = fmaf(p, sQ[t * LC + j] * ep, fmaf(q, sK[t * LC + j] * ep, r3[m]));
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) dkc[bi][m] = fmaf(r3[m], sEm[(s - b0) * LC + tx + 16 * m], dkc[bi][m]);
+      }
+      __syncthreads();
+    } else {  // pair decays one by one
+#pragma unroll
+      for (int ii = 0; ii < 4; ++ii) {
+        const int t = ty + 16 * ii;
+        if (t >= b0) {
+          const float bt = sB[t];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int j = tx + 16 * m;
+            float r1 = 0.f, r2 = 0.f;
+            for (int s = b0; s < b0 + 16 && s <= t; ++s) {
+              const float e = __expf(sG[t * LC + j] - sG[s * LC + j]) * sK[s * LC + j];
+              r1 = fmaf(sDP[t * LC + s], e, r1);
+              r2 = fmaf(sDA[t * LC + s], e, r2);
+            }
+            dqp[ii][m] += r1;
+            dkr[ii][m] = fmaf(bt, r2, dkr[ii][m]);
+          }
+        }
+      }
+      const int s = ty + 16 * bi;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int j = tx + 16 * m;
+        float r3 = 0.f;
+        for (int t = s; t < C; ++t) {
+          const float e = __expf(sG[t * LC + j] - sG[s * LC + j]);
+          r3 = fmaf(sDP[t * LC + s], sQ[t * LC + j] * e, fmaf(sB[t] * sDA[t * LC + s], sK[t * LC + j] * e, r3));
+        }
+        dkc[bi][m] += r3;
+      }
+      __syncthreads();
+    }
+  }
+  // final values of the own elements; dG and the G_C terms go to shared memory for the reverse cumsum
+  float* sDG = sEp;
+  float* sXC = sDP;
+  __syncthreads();
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int t = ty + 16 * ii;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int jl = tx + 16 * m, j = j0 + jl;
+      float dG = 0.f, xc = 0.f;
+      if (t < n) {
+        const float G = sG[t * LC + jl], GC = sG[(n - 1) * LC + jl];
+        const float e0 = __expf(G), ec = __expf(GC - G);
+        const float kk = sK[t * LC + jl], qq = sQ[t * LC + jl];
+        const float gq = w[BW_DQP + t * D + j], gk = w[BW_DKP + t * D + j], gh = w[BW_DKH + t * D + j];
+        const int64_t o = ((int64_t)(t0 + t) * a.H + h) * D + j;
+        a.dq[o] = fmaf(gq, e0, dqp[ii][m]);
+        a.dk[o] = fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkc[ii][m]));
+        xc = gh * kk * ec;
+        dG = (gq * qq + gk * kk) * e0 - xc + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkc[ii][m]);
+      }
+      sDG[t * LC + jl] = dG;
+      sXC[t * LC + jl] = xc;
+    }
+  }
+  __syncthreads();
+  if (tid < HC) {  // dg_u = sum_{t >= u} dG_t + dG_C, dG_C = sum_t dK^_t K^_t + d(e^G_C) e^G_C
+    const int j = j0 + tid;
+    float run = w[BW_DGAM + j] * w[BW_GAM + j];
+    for (int t = 0; t < n; ++t) run += sXC[t * LC + tid];
+    for (int t = n - 1; t >= 0; --t) {
+      run += sDG[t * LC + tid];
+      a.dg[((int64_t)(t0 + t) * a.H + h) * D + j] = run;
+    }
+  } else if (half == 0 && tid < HC + C) {  // dbeta_t = (W, U~ part) + sum_s dA_ts a_ts
+    const int t = tid - HC;
+    if (t < n) {
+      float s = w[BW_DBETA + t];
+      for (int u = 0; u < t; ++u) s = fmaf(sDA[t * LC + u], w[BW_A + t * C + u], s);
+      a.dbeta[(int64_t)(t0 + t) * a.H + h] = s;
+    }
+  }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename Tin>
+cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
+  cudaError_t e;
+  if ((e = set_smem(bwd_prep_kernel<Tin>, PREP_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_fwd_chain_kernel, FWD_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_rev_chain_kernel<Tin>, REV_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_state_grads_kernel<Tin>, STATE_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_wy_grads_kernel<Tin>, WY_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_assemble_kernel<Tin>, ASM_SMEM)) != cudaSuccess) return e;
+  const int nch = (a.max_seqlen + C - 1) / C;
+  const dim3 chunks(nch, a.H, a.N), halves(nch, 2 * a.H, a.N), chains(D / CB, a.H, a.N);
+  if (nch > 0) {
+    bwd_prep_kernel<Tin><<<chunks, NT, PREP_SMEM, s>>>(a);
+    bwd_fwd_chain_kernel<<<chains, NT, FWD_SMEM, s>>>(a);
+  }
+  bwd_rev_chain_kernel<Tin><<<chains, NT, REV_SMEM, s>>>(a);
+  if (nch > 0) {
+    bwd_state_grads_kernel<Tin><<<chunks, NT, STATE_SMEM, s>>>(a);
+    bwd_wy_grads_kernel<Tin><<<chunks, NT, WY_SMEM, s>>>(a);
+    bwd_assemble_kernel<Tin><<<halves, NT, ASM_SMEM, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t backward_ws_bytes(int64_t T, int N, int H) {
+  return (size_t)((T + C - 1) / C + N) * H * BW_FLOATS * sizeof(float);
+}
+
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s) {
+  if (a.N == 0) return cudaSuccess;
+  return a.in_bf16 ? launch_backward_t<bf16>(a, s) : launch_backward_t<float>(a, s);
+}
+
+}  // namespace kda

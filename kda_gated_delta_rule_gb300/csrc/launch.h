@@ -112,6 +112,30 @@ struct CfbiArgs {
   int32_t* status;
 };
 
+// Chunked backward (d = 128): gradients of sum <d_out, o> + <d_final, S_T> through a packed prefill.
+struct BackwardArgs {
+  const void *q, *k, *v;
+  const float *g, *beta;
+  bool in_bf16;
+  int64_t T;
+  int H, N;
+  const int32_t* cu;
+  int max_seqlen;
+  const float* pool;
+  int num_slots;
+  const int32_t* slot_ids;
+  bool init_zero;
+  const void* d_out;     // [T][H][128] in dtype
+  const float* d_final;  // [N][H][128][128] or null
+  float *dq, *dk, *dv, *dg, *dbeta;
+  float* d_init;         // [N][H][128][128] or null
+  float* ws;             // backward_ws_bytes(T, N, H)
+  int32_t* status;
+};
+
+size_t backward_ws_bytes(int64_t T, int N, int H);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
+
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s);
 // Tensor-core verify (bf16 inputs, d = 128, W <= 16, no per-token snapshots).

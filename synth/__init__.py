@@ -43,6 +43,7 @@ G_MIN = -5.0
 S_Q, S_K, S_V, S_G, S_BETA, S_S0 = 1, 2, 3, 4, 5, 6
 S_LEN, S_SLOTS, S_ACCEPT, S_SAMPLES, S_EXTRA = 7, 8, 9, 10, 11
 S_WQ, S_WK, S_WV, S_WG, S_WBETA = 21, 22, 23, 24, 25
+S_DO, S_DFINAL = 31, 32
 
 
 def build(force: bool = False) -> str:
@@ -247,6 +248,14 @@ def long_1m(seed: int = 5, T: int = 1 << 20, H: int = 12, d: int = 128, segment_
     samp = np.sort(np.argsort(uniform(seed, S_SAMPLES, T), kind="stable")[:n_samples]).astype(np.int64)
     return Prefill("long_1m", seed, H, d, d, dtype, q, k, v, g, beta, np.array([0, T], np.int32), pool,
                    np.array([0], np.int32), init_zero=False, segment_len=segment_len, sample_t=samp)
+
+
+def output_grads(prob: Prefill, seed: int):
+    """Seeded upstream gradients for a backward pass over `prob`: dL/do [T, H, dv] N(0, 1) in the input
+    dtype and dL/dS_T [N, H, dk, dv] N(0, 0.1) fp32."""
+    d_out = normal(seed, S_DO, (prob.T, prob.H, prob.dv), dtype=prob.in_dtype)
+    d_final = normal(seed, S_DFINAL, (prob.N, prob.H, prob.dk, prob.dv), 0.0, 0.1, F32)
+    return d_out, d_final
 
 
 @dataclass
