@@ -8,7 +8,8 @@ slot followed by the chunked (or segmented) prefill.  Inputs are resident in HBM
 write) between timed steps.
 
 Also reported (`decode_verify`): state GB/s of the decode step, the 8-token speculative verify and the
-replay fold on the batched workload (256 requests, 1024-slot pool), against the measured HBM peak.
+replay fold on the batched workload (256 requests, 1024-slot pool), against the measured HBM peak; and
+(`backward`) the prefill backward (all input and initial-state gradients) on the single-request workload.
 
 `--impl reference` times the fp64 CPU oracle (the baseline arm) on a bounded sample of the same workload.
 """
@@ -53,6 +54,7 @@ def parse():
                     help="tokens per segment of the segmented path (multiple of 64); 0 = the shortest segment whose "
                          "fragment phase (2 CTAs per head and segment but the last) fits one wave on this GPU")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -333,6 +335,10 @@ def run_ours(args):
     if not args.no_decode:
         dv_report = decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world)
 
+    bw_report = None
+    if not args.no_backward:
+        bw_report = backward_report(kda, torch, dev, to_dev, time_calls, pk, prob)
+
     line = {
         "metric": "KDA prefill tokens/s/layer (H=12,d=128); decode+verify state GB/s vs HBM peak",
         "value": round(value, 1),
@@ -363,6 +369,8 @@ def run_ours(args):
     }
     if dv_report:
         line["decode_verify"] = dv_report
+    if bw_report:
+        line["backward"] = bw_report
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, sample_tokens=T)
     if rank == 0:
@@ -436,6 +444,42 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
         rep[name] = {"ms": round(t[name], 5), "algorithmic_bytes": alg[name], "gbs": round(gbs, 1),
                      "frac": round(gbs / pk["hbm_gbs"], 4)}
     return rep
+
+
+# gradient bytes per token and head of the backward: q, k, v, d_out bf16 + g, beta fp32 in; dq, dk, dv, dg, dbeta
+# fp32 out (d = 128)
+BW_BYTES_PER_TOKEN_HEAD = 4 * 256 + 512 + 4 + 4 * 512 + 4
+
+
+def backward_report(kda, torch, dev, to_dev, time_calls, pk, prob):
+    """The prefill backward on the single-request workload: one call = all six kernels."""
+    T, H, N = prob.T, prob.H, prob.N
+    d_out, d_final = synth.output_grads(prob, prob.seed)
+    q, k, v, g, beta, dout = (to_dev(x) for x in (prob.q, prob.k, prob.v, prob.g, prob.beta, d_out))
+    dfin = to_dev(d_final)
+    cu = to_dev(prob.cu_seqlens.astype(np.int32))
+    pool, slots = to_dev(prob.pool), to_dev(prob.slot_ids)
+    grads = [torch.empty(T, H, 128, device=dev) for _ in range(4)]
+    dbeta = torch.empty(T, H, device=dev)
+    dinit = torch.empty(N, H, 128, 128, device=dev)
+    ws = torch.empty(kda.kda_backward_workspace_size(T, N, H), dtype=torch.uint8, device=dev)
+    max_len = int(prob.lengths.max())
+
+    def call():
+        kda.kda_prefill_backward(q, k, v, g, beta, cu, max_len, dout, *grads, dbeta, ws, pool=pool, slot_ids=slots,
+                                 d_final=dfin, d_init=dinit)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ms = statistics.mean(time_calls(call, 20))
+    alg = T * H * BW_BYTES_PER_TOKEN_HEAD + N * H * 3 * STATE_BYTES
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"workload": "prefill backward: B=1, T=8192, H=12, d=128, bf16 q/k/v/d_out, fp32 gradients out, "
+                        "S0 and dL/dS_T given, dL/dS0 out; L2 flushed between calls",
+            "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "algorithmic_bytes": alg,
+            "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "kernels_per_call": 6,
+            "workspace_bytes": ws.numel()}
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)

@@ -19,7 +19,8 @@
 // e^(G_t - G_s) = e^(G_t - G_r) e^(G_r - G_s), while every factor stays below e^80 (always when g >= -5, the
 // pages' floor); a block that would exceed it takes the pair decays one by one.
 //
-// Six kernels, all in fp32 on the CUDA cores, handing over through a per-(chunk, head) fp32 workspace:
+// Six kernels, all in fp32 on the CUDA cores, handing over through a per-(chunk, head) fp32 workspace
+// (tiles move into shared memory by asynchronous 16-byte copies):
 //   prep (chunk-parallel) -> forward chain (entry states, U) -> reverse chain (dS', dU)
 //   -> state products -> WY backward -> per-channel assembly (chunk-parallel).
 #include "common.cuh"
@@ -31,8 +32,9 @@ namespace {
 constexpr int C = 64;      // chunk length
 constexpr int D = 128;     // dk = dv
 constexpr int NT = 256;    // threads per CTA
-constexpr int LD = D + 1;  // shared row stride of [rows][128] tiles (odd: row and column walks are conflict-free)
-constexpr int LC = C + 1;  // shared row stride of [64][64] tiles
+constexpr int NTC = 512;   // threads per CTA of the chain kernels
+constexpr int LD = D + 4;  // shared row stride of [rows][128] tiles (16-byte rows; 8 consecutive rows hit distinct banks)
+constexpr int LC = C + 4;  // shared row stride of [64][64] tiles
 constexpr int HC = 64;     // channels per CTA of the assembly kernel
 constexpr int CB = 16;     // value columns per CTA of the chain kernels
 constexpr float SPAN_MAX = 80.f;
@@ -73,18 +75,52 @@ __device__ __forceinline__ void ld4(const bf16* p, float (&x)[4]) {
   x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
 }
 
+// 16-byte asynchronous global -> shared copy; src_bytes = 0 writes zeros (the source is not read)
+__device__ __forceinline__ void cp_async16(float* dst, const float* src, int src_bytes) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
 // rows [0, rows) x columns [c0, c0 + ncols) of a row-major source (row r at src + r * stride) into shared
-// memory as fp32 with row stride ld; rows >= n are zero.
-template <typename Tin>
-__device__ __forceinline__ void load_rows(float* dst, int ld, const Tin* src, int64_t stride, int rows, int n, int c0,
-                                          int ncols) {
+// memory as fp32 with row stride ld (a multiple of 4); rows >= n are zero.  fp32 sources are copied
+// asynchronously (complete with cp_async_commit / cp_async_wait); bf16 sources are widened through
+// registers, all of a thread's loads issued before its stores.
+template <int NTH>
+__device__ __forceinline__ void load_rows(float* dst, int ld, const float* src, int64_t stride, int rows, int n,
+                                          int c0, int ncols) {
   const int q4 = ncols / 4;
-  for (int e = threadIdx.x; e < rows * q4; e += NT) {
+  for (int e = threadIdx.x; e < rows * q4; e += NTH) {
     const int r = e / q4, c = (e % q4) * 4;
-    float x[4] = {0.f, 0.f, 0.f, 0.f};
-    if (r < n) ld4(src + r * stride + c0 + c, x);
+    cp_async16(dst + r * ld + c, src + (r < n ? r : 0) * stride + c0 + c, r < n ? 16 : 0);
+  }
+}
+template <int NTH>
+__device__ __forceinline__ void load_rows(float* dst, int ld, const bf16* src, int64_t stride, int rows, int n,
+                                          int c0, int ncols) {
+  constexpr int MAXIT = 8;
+  const int q4 = ncols / 4, total = rows * q4;
+  for (int base = 0; base < total; base += MAXIT * NTH) {
+    float x[MAXIT][4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) dst[r * ld + c + u] = x[u];
+    for (int it = 0; it < MAXIT; ++it) {
+      const int e = base + it * NTH + threadIdx.x;
+      const int r = e / q4, c = (e % q4) * 4;
+      x[it][0] = x[it][1] = x[it][2] = x[it][3] = 0.f;
+      if (e < total && r < n) ld4(src + r * stride + c0 + c, x[it]);
+    }
+#pragma unroll
+    for (int it = 0; it < MAXIT; ++it) {
+      const int e = base + it * NTH + threadIdx.x;
+      if (e < total) {
+        const int r = e / q4, c = (e % q4) * 4;
+        *reinterpret_cast<float4*>(dst + r * ld + c) = make_float4(x[it][0], x[it][1], x[it][2], x[it][3]);
+      }
+    }
   }
 }
 
@@ -133,11 +169,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
   float* sT = sP + C * LC;     // T [64][LC]
   float* sB = sT + C * LC;     // beta [64]
   const int64_t rs = (int64_t)a.H * D;
-  load_rows(sK, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
-  load_rows(sQ, LD, reinterpret_cast<const Tin*>(a.q) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
-  load_rows(sG, LD, a.g + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows<NT>(sK, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows<NT>(sQ, LD, reinterpret_cast<const Tin*>(a.q) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows<NT>(sG, LD, a.g + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
   if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
   for (int e = tid; e < C * LC; e += NT) sA[e] = 0.f, sP[e] = 0.f;
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   if (tid < D) {  // in-chunk cumulative sum, one thread per channel
     float acc = 0.f;
@@ -269,7 +307,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
       for (int m = 0; m < 8; ++m) w[BW_W + (ty + 16 * ii) * D + tx + 16 * m] = acc[ii][m];
   }
   __syncthreads();
-  load_rows(sX, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows<NT>(sX, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   {
     float acc[4][8] = {};
@@ -293,21 +333,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// 2. forward chain over the chunks of one (sequence, head, 16 value columns): entry states and U
+// 2. forward chain over the chunks of one (sequence, head, 16 value columns): entry states and U.
+//    The next chunk's operands are copied in while the current one is processed (two stages).
 // ---------------------------------------------------------------------------------------------------
-constexpr size_t FWD_SMEM = (2 * C * LD + C * CB + D * CB + C * CB + D) * sizeof(float);
+constexpr int FS_STAGE = 2 * C * LD + C * CB + D;  // W, K^, U~ columns, e^G_C
+constexpr size_t FWD_SMEM = (2 * FS_STAGE + D * CB + C * CB) * sizeof(float);
 
-__global__ void __launch_bounds__(NT) bwd_fwd_chain_kernel(BackwardArgs a) {
+__global__ void __launch_bounds__(NTC, 1) bwd_fwd_chain_kernel(BackwardArgs a) {
   const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
   extern __shared__ float sm[];
-  float* sW = sm;               // W [64][LD]
-  float* sKh = sW + C * LD;     // K^ [64][LD]
-  float* sUt = sKh + C * LD;    // U~ columns [64][CB]
-  float* sS = sUt + C * CB;     // state columns [128][CB]
-  float* sU = sS + D * CB;      // U columns [64][CB]
-  float* sGam = sU + C * CB;    // e^G_C [128]
+  float* sS = sm + 2 * FS_STAGE;  // state columns [128][CB]
+  float* sU = sS + D * CB;        // U columns [64][CB]
   const float* s0 = nullptr;
   if (!a.init_zero) {
     const int slot = a.slot_ids[i];
@@ -317,53 +355,61 @@ __global__ void __launch_bounds__(NT) bwd_fwd_chain_kernel(BackwardArgs a) {
       s0 = a.pool + ((size_t)slot * a.H + h) * D * D;
     }
   }
-  for (int e = tid; e < D * CB; e += NT) {
-    const int j = e / CB, cc = e % CB;
-    sS[e] = s0 ? s0[j * D + c0 + cc] : 0.f;
-  }
+  for (int e = tid; e < D * CB; e += NTC) sS[e] = s0 ? s0[(e / CB) * D + c0 + e % CB] : 0.f;
   const int nc = (sq.eos - sq.bos + C - 1) / C;
+  auto issue = [&](int c) {
+    float* st = sm + (c & 1) * FS_STAGE;
+    const float* w = record(a, sq.bos + c * C, i, h);
+    load_rows<NTC>(st, LD, w + BW_W, D, C, C, 0, D);
+    load_rows<NTC>(st + C * LD, LD, w + BW_KH, D, C, C, 0, D);
+    load_rows<NTC>(st + 2 * C * LD, CB, w + BW_UT, D, C, C, c0, CB);
+    load_rows<NTC>(st + 2 * C * LD + C * CB, D, w + BW_GAM, D, 1, 1, 0, D);
+    cp_async_commit();
+  };
+  if (nc > 0) issue(0);
   for (int c = 0; c < nc; ++c) {
-    const int t0 = sq.bos + c * C;
-    float* w = record(a, t0, i, h);
-    load_rows(sW, LD, w + BW_W, D, C, C, 0, D);
-    load_rows(sKh, LD, w + BW_KH, D, C, C, 0, D);
-    load_rows(sUt, CB, w + BW_UT, D, C, C, c0, CB);
-    if (tid < D) sGam[tid] = w[BW_GAM + tid];
-    __syncthreads();
-    for (int e = tid; e < D * CB; e += NT) w[BW_H + (e / CB) * D + c0 + e % CB] = sS[e];
-    {  // U = U~ - W S: row t = tid / 4, columns tid % 4 + 4m
-      const int t = tid >> 2, cl = tid & 3;
-      float acc[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) acc[m] = 0.f;
-      for (int j = 0; j < D; ++j) {
-        const float x = sW[t * LD + j];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sS[j * CB + cl + 4 * m], acc[m]);
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int cc = cl + 4 * m;
-        const float u = sUt[t * CB + cc] - acc[m];
-        sU[t * CB + cc] = u;
-        w[BW_U + t * D + c0 + cc] = u;
-      }
+    if (c + 1 < nc) {
+      issue(c + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    {  // S = Diag(e^G_C) S + K^^T U: row j = tid / 2, columns tid % 2 + 2m (own elements only: in place)
-      const int j = tid >> 1, cl = tid & 1;
-      float acc[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    const float* sW = sm + (c & 1) * FS_STAGE;
+    const float* sKh = sW + C * LD;
+    const float* sUt = sKh + C * LD;
+    const float* sGam = sUt + C * CB;
+    float* w = record(a, sq.bos + c * C, i, h);
+    for (int e = tid; e < D * CB; e += NTC) w[BW_H + (e / CB) * D + c0 + e % CB] = sS[e];
+    {  // U = U~ - W S: row t = tid / 8, columns tid % 8 + 8m
+      const int t = tid >> 3, cl = tid & 7;
+      float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < D; ++j) {
+        const float x = sW[t * LD + j];
+        acc0 = fmaf(x, sS[j * CB + cl], acc0);
+        acc1 = fmaf(x, sS[j * CB + cl + 8], acc1);
+      }
+      const float u0 = sUt[t * CB + cl] - acc0, u1 = sUt[t * CB + cl + 8] - acc1;
+      sU[t * CB + cl] = u0;
+      sU[t * CB + cl + 8] = u1;
+      w[BW_U + t * D + c0 + cl] = u0;
+      w[BW_U + t * D + c0 + cl + 8] = u1;
+    }
+    __syncthreads();
+    {  // S = Diag(e^G_C) S + K^^T U: row j = tid / 4, columns tid % 4 + 4m (own elements only: in place)
+      const int j = tid >> 2, cl = tid & 3;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
       for (int t = 0; t < C; ++t) {
         const float x = sKh[t * LD + j];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc[m] = fmaf(x, sU[t * CB + cl + 2 * m], acc[m]);
+        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sU[t * CB + cl + 4 * m], acc[m]);
       }
       const float gm = sGam[j];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int cc = cl + 2 * m;
+      for (int m = 0; m < 4; ++m) {
+        const int cc = cl + 4 * m;
         sS[j * CB + cc] = fmaf(gm, sS[j * CB + cc], acc[m]);
       }
     }
@@ -372,88 +418,117 @@ __global__ void __launch_bounds__(NT) bwd_fwd_chain_kernel(BackwardArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// 3. reverse chain: dS' at every chunk exit, dU, and dS_0
+// 3. reverse chain: dS' at every chunk exit, dU, and dS_0.  Stage A (P, K^, dO columns, e^G_C) is
+//    double-buffered and copied in a chunk ahead; stage B (Q+, W) is copied in during the previous
+//    chunk's dU step.
 // ---------------------------------------------------------------------------------------------------
-constexpr size_t REV_SMEM = (C * LC + 3 * C * LD + C * CB + D * CB + C * CB + D) * sizeof(float);
+constexpr int RS_A = C * LC + C * LD + C * CB + D;  // P, K^, raw dO columns (<= 64 x 16 fp32), e^G_C
+constexpr int RS_B = 2 * C * LD;                    // Q+, W
+constexpr size_t REV_SMEM = (2 * RS_A + RS_B + D * CB + C * CB) * sizeof(float);
 
 template <typename Tin>
-__global__ void __launch_bounds__(NT) bwd_rev_chain_kernel(BackwardArgs a) {
+__global__ void __launch_bounds__(NTC, 1) bwd_rev_chain_kernel(BackwardArgs a) {
   const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
   extern __shared__ float sm[];
-  float* sP = sm;               // P [64][LC]
-  float* sKh = sP + C * LC;     // K^ [64][LD]
-  float* sQp = sKh + C * LD;    // Q+ [64][LD]
-  float* sW = sQp + C * LD;     // W [64][LD]
-  float* sDO = sW + C * LD;     // dO columns [64][CB]
-  float* sdS = sDO + C * CB;    // dS columns [128][CB]
-  float* sdU = sdS + D * CB;    // dU columns [64][CB]
-  float* sGam = sdU + C * CB;   // e^G_C [128]
+  float* sB = sm + 2 * RS_A;     // Q+, W
+  float* sdS = sB + RS_B;        // dS columns [128][CB]
+  float* sdU = sdS + D * CB;     // dU columns [64][CB]
   const float* dfin = a.d_final ? a.d_final + ((size_t)i * a.H + h) * D * D : nullptr;
-  for (int e = tid; e < D * CB; e += NT) sdS[e] = dfin ? dfin[(e / CB) * D + c0 + e % CB] : 0.f;
+  for (int e = tid; e < D * CB; e += NTC) sdS[e] = dfin ? dfin[(e / CB) * D + c0 + e % CB] : 0.f;
   const int nc = (sq.eos - sq.bos + C - 1) / C;
   const int64_t rs = (int64_t)a.H * D;
-  for (int c = nc - 1; c >= 0; --c) {
+  constexpr int DO_Q = CB * (int)sizeof(Tin) / 16;  // 16-byte pieces of one dO row slice
+  auto issue_a = [&](int c, int buf) {
+    float* st = sm + buf * RS_A;
     const int t0 = sq.bos + c * C, n = min(C, sq.eos - t0);
-    float* w = record(a, t0, i, h);
-    load_rows(sP, LC, w + BW_P, C, C, C, 0, C);
-    load_rows(sKh, LD, w + BW_KH, D, C, C, 0, D);
-    load_rows(sQp, LD, w + BW_QP, D, C, C, 0, D);
-    load_rows(sW, LD, w + BW_W, D, C, C, 0, D);
-    load_rows(sDO, CB, reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D, rs, C, n, c0, CB);
-    if (tid < D) sGam[tid] = w[BW_GAM + tid];
+    const float* w = record(a, t0, i, h);
+    load_rows<NTC>(st, LC, w + BW_P, C, C, C, 0, C);
+    load_rows<NTC>(st + C * LC, LD, w + BW_KH, D, C, C, 0, D);
+    const Tin* src = reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D + c0;
+    Tin* dst = reinterpret_cast<Tin*>(st + C * LC + C * LD);
+    for (int e = tid; e < C * DO_Q; e += NTC) {
+      const int r = e / DO_Q, q = e % DO_Q;
+      cp_async16(reinterpret_cast<float*>(dst + r * CB + q * (16 / (int)sizeof(Tin))),
+                 reinterpret_cast<const float*>(src + (r < n ? r : 0) * rs + q * (16 / (int)sizeof(Tin))),
+                 r < n ? 16 : 0);
+    }
+    load_rows<NTC>(st + C * LC + C * LD + C * CB, D, w + BW_GAM, D, 1, 1, 0, D);
+    cp_async_commit();
+  };
+  auto issue_b = [&](int c) {
+    const float* w = record(a, sq.bos + c * C, i, h);
+    load_rows<NTC>(sB, LD, w + BW_QP, D, C, C, 0, D);
+    load_rows<NTC>(sB + C * LD, LD, w + BW_W, D, C, C, 0, D);
+    cp_async_commit();
+  };
+  if (nc > 0) {
+    issue_a(nc - 1, 0);
+    issue_b(nc - 1);
+  }
+  for (int c = nc - 1, k = 0; c >= 0; --c, ++k) {
+    cp_async_wait<1>();  // stage A of chunk c has landed (stage B may still be in flight)
     __syncthreads();
-    for (int e = tid; e < D * CB; e += NT) w[BW_DS + (e / CB) * D + c0 + e % CB] = sdS[e];
-    {  // dU = P^T dO + K^ dS': row t = tid / 4, columns tid % 4 + 4m
-      const int t = tid >> 2, cl = tid & 3;
-      float acc[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) acc[m] = 0.f;
+    if (c > 0) issue_a(c - 1, (k + 1) & 1);
+    const float* sP = sm + (k & 1) * RS_A;
+    const float* sKh = sP + C * LC;
+    const Tin* sDO = reinterpret_cast<const Tin*>(sKh + C * LD);
+    const float* sGam = sKh + C * LD + C * CB;
+    const float* sQp = sB;
+    const float* sW = sB + C * LD;
+    float* w = record(a, sq.bos + c * C, i, h);
+    for (int e = tid; e < D * CB; e += NTC) w[BW_DS + (e / CB) * D + c0 + e % CB] = sdS[e];
+    {  // dU = P^T dO + K^ dS': row t = tid / 8, columns tid % 8 + 8m
+      const int t = tid >> 3, cl = tid & 7;
+      float acc0 = 0.f, acc1 = 0.f;
       for (int s = t; s < C; ++s) {
         const float x = sP[s * LC + t];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sDO[s * CB + cl + 4 * m], acc[m]);
+        acc0 = fmaf(x, to_f32(sDO[s * CB + cl]), acc0);
+        acc1 = fmaf(x, to_f32(sDO[s * CB + cl + 8]), acc1);
       }
+#pragma unroll 8
       for (int j = 0; j < D; ++j) {
         const float x = sKh[t * LD + j];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sdS[j * CB + cl + 4 * m], acc[m]);
+        acc0 = fmaf(x, sdS[j * CB + cl], acc0);
+        acc1 = fmaf(x, sdS[j * CB + cl + 8], acc1);
       }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int cc = cl + 4 * m;
-        sdU[t * CB + cc] = acc[m];
-        w[BW_DU + t * D + c0 + cc] = acc[m];
-      }
+      sdU[t * CB + cl] = acc0;
+      sdU[t * CB + cl + 8] = acc1;
+      w[BW_DU + t * D + c0 + cl] = acc0;
+      w[BW_DU + t * D + c0 + cl + 8] = acc1;
     }
+    if (c > 0)
+      cp_async_wait<1>();  // stage B of chunk c has landed (the next stage A may still be in flight)
+    else
+      cp_async_wait<0>();
     __syncthreads();
-    {  // dS = Q+^T dO + Diag(e^G_C) dS' - W^T dU: row j = tid / 2, columns tid % 2 + 2m (in place)
-      const int j = tid >> 1, cl = tid & 1;
-      float acc[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    {  // dS = Q+^T dO + Diag(e^G_C) dS' - W^T dU: row j = tid / 4, columns tid % 4 + 4m (in place)
+      const int j = tid >> 2, cl = tid & 3;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
       for (int t = 0; t < C; ++t) {
         const float x = sQp[t * LD + j], y = sW[t * LD + j];
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          const int cc = cl + 2 * m;
-          acc[m] = fmaf(x, sDO[t * CB + cc], acc[m]);
+        for (int m = 0; m < 4; ++m) {
+          const int cc = cl + 4 * m;
+          acc[m] = fmaf(x, to_f32(sDO[t * CB + cc]), acc[m]);
           acc[m] = fmaf(-y, sdU[t * CB + cc], acc[m]);
         }
       }
       const float gm = sGam[j];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int cc = cl + 2 * m;
+      for (int m = 0; m < 4; ++m) {
+        const int cc = cl + 4 * m;
         sdS[j * CB + cc] = fmaf(gm, sdS[j * CB + cc], acc[m]);
       }
     }
     __syncthreads();
+    if (c > 0) issue_b(c - 1);
   }
   if (a.d_init) {
     float* dst = a.d_init + ((size_t)i * a.H + h) * D * D;
-    for (int e = tid; e < D * CB; e += NT) dst[(e / CB) * D + c0 + e % CB] = sdS[e];
+    for (int e = tid; e < D * CB; e += NTC) dst[(e / CB) * D + c0 + e % CB] = sdS[e];
   }
 }
 
@@ -475,10 +550,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_state_grads_kernel(BackwardArgs a) 
   float* sH = sm;               // S, later dS' [128][LD]
   float* sD = sH + D * LD;      // dO [64][LD]
   float* sE = sD + C * LD;      // dU, later U [64][LD]
-  load_rows(sH, LD, w + BW_H, D, D, D, 0, D);
-  load_rows(sD, LD, reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D, (int64_t)a.H * D, C, n, 0,
+  load_rows<NT>(sH, LD, w + BW_H, D, D, D, 0, D);
+  load_rows<NT>(sD, LD, reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D, (int64_t)a.H * D, C, n, 0,
             D);
-  load_rows(sE, LD, w + BW_DU, D, C, C, 0, D);
+  load_rows<NT>(sE, LD, w + BW_DU, D, C, C, 0, D);
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   const int ty = tid >> 4, tx = tid & 15;  // rows ty + 16i, columns tx + 16m
   {
@@ -520,8 +597,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_state_grads_kernel(BackwardArgs a) 
     }
   }
   __syncthreads();
-  load_rows(sE, LD, w + BW_U, D, C, C, 0, D);
-  load_rows(sH, LD, w + BW_DS, D, D, D, 0, D);
+  load_rows<NT>(sE, LD, w + BW_U, D, C, C, 0, D);
+  load_rows<NT>(sH, LD, w + BW_DS, D, D, D, 0, D);
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   {  // dP = tril(dO U^T)
     float acc[4][4] = {};
@@ -587,12 +666,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
   float* sDU = sDW + C * LD;     // dU [64][LD]
   float* sB = sDU + C * LD;      // beta [64]
   const int64_t rs = (int64_t)a.H * D;
-  load_rows(sT, LC, w + BW_T, C, C, C, 0, C);
-  load_rows(sKp, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
-  load_rows(sV, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
-  load_rows(sDW, LD, w + BW_DW, D, C, C, 0, D);
-  load_rows(sDU, LD, w + BW_DU, D, C, C, 0, D);
+  load_rows<NT>(sT, LC, w + BW_T, C, C, C, 0, C);
+  load_rows<NT>(sKp, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows<NT>(sV, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
+  load_rows<NT>(sDW, LD, w + BW_DW, D, C, C, 0, D);
+  load_rows<NT>(sDU, LD, w + BW_DU, D, C, C, 0, D);
   if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
+  cp_async_commit();
+  cp_async_wait<0>();
   __syncthreads();
   for (int e = tid; e < C * D; e += NT) sKp[(e / D) * LD + e % D] *= __expf(w[BW_G + e]);
   __syncthreads();
@@ -700,7 +781,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
 // ---------------------------------------------------------------------------------------------------
 // 6. assembly of one (chunk, head, 64 channels): pair-decay terms, dq, dk, dg, dbeta
 // ---------------------------------------------------------------------------------------------------
-constexpr size_t ASM_SMEM = (6 * C * LC + 2 * 16 * LC + C) * sizeof(float);
+constexpr size_t ASM_SMEM = (6 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
@@ -722,14 +803,23 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
   float* sKm = sDA + C * LC;    // k o e^(G_r - G_s) of the current block [16][LC]
   float* sEm = sKm + 16 * LC;   // e^(G_r - G_s) [16][LC]
   float* sB = sEm + 16 * LC;    // beta [64]
+  float* sDiag = sB + C;        // dP_tt [64] (the diagonal is kept out of the pair sums: in dG its two
+                                // contributions, through q_t and through k_t, cancel exactly)
   const int64_t rs = (int64_t)a.H * D;
   const int64_t in0 = ((int64_t)t0 * a.H + h) * D;
-  load_rows(sK, LC, reinterpret_cast<const Tin*>(a.k) + in0, rs, C, n, j0, HC);
-  load_rows(sQ, LC, reinterpret_cast<const Tin*>(a.q) + in0, rs, C, n, j0, HC);
-  load_rows(sG, LC, w + BW_G, D, C, C, j0, HC);
-  load_rows(sDP, LC, w + BW_DP, C, C, C, 0, C);
-  load_rows(sDA, LC, w + BW_DA, C, C, C, 0, C);
+  load_rows<NT>(sK, LC, reinterpret_cast<const Tin*>(a.k) + in0, rs, C, n, j0, HC);
+  load_rows<NT>(sQ, LC, reinterpret_cast<const Tin*>(a.q) + in0, rs, C, n, j0, HC);
+  load_rows<NT>(sG, LC, w + BW_G, D, C, C, j0, HC);
+  load_rows<NT>(sDP, LC, w + BW_DP, C, C, C, 0, C);
+  load_rows<NT>(sDA, LC, w + BW_DA, C, C, C, 0, C);
   if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  if (tid < C) {
+    sDiag[tid] = sDP[tid * LC + tid];
+    sDP[tid * LC + tid] = 0.f;
+  }
   __syncthreads();
   const int ty = tid >> 4, tx = tid & 15;  // own elements: rows ty + 16i, channels tx + 16m
   float dqp[4][4] = {}, dkr[4][4] = {}, dkc[4][4] = {};
@@ -844,23 +934,32 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
         const float kk = sK[t * LC + jl], qq = sQ[t * LC + jl];
         const float gq = w[BW_DQP + t * D + j], gk = w[BW_DKP + t * D + j], gh = w[BW_DKH + t * D + j];
         const int64_t o = ((int64_t)(t0 + t) * a.H + h) * D + j;
-        a.dq[o] = fmaf(gq, e0, dqp[ii][m]);
-        a.dk[o] = fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkc[ii][m]));
+        const float dpt = sDiag[t];
+        a.dq[o] = fmaf(dpt, kk, fmaf(gq, e0, dqp[ii][m]));
+        a.dk[o] = fmaf(dpt, qq, fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkc[ii][m])));
         xc = gh * kk * ec;
-        dG = (gq * qq + gk * kk) * e0 - xc + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkc[ii][m]);
+        dG = (gq * qq + gk * kk) * e0 + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkc[ii][m]);
       }
       sDG[t * LC + jl] = dG;
       sXC[t * LC + jl] = xc;
     }
   }
   __syncthreads();
-  if (tid < HC) {  // dg_u = sum_{t >= u} dG_t + dG_C, dG_C = sum_t dK^_t K^_t + d(e^G_C) e^G_C
+  if (tid < HC) {
+    // dg_u = sum_{t >= u} (dG_t - X_t) + dG_C with X_t = dK^_t K^_t and dG_C = sum_t X_t + d(e^G_C) e^G_C;
+    // the X terms are summed directly as sum_{t < u} X_t (a prefix, not the total minus a suffix), and
+    // sDG holds dG_t without -X_t
     const int j = j0 + tid;
+    float pre = 0.f;
+    for (int t = 0; t < n; ++t) {
+      const float x = sXC[t * LC + tid];
+      sXC[t * LC + tid] = pre;
+      pre += x;
+    }
     float run = w[BW_DGAM + j] * w[BW_GAM + j];
-    for (int t = 0; t < n; ++t) run += sXC[t * LC + tid];
     for (int t = n - 1; t >= 0; --t) {
       run += sDG[t * LC + tid];
-      a.dg[((int64_t)(t0 + t) * a.H + h) * D + j] = run;
+      a.dg[((int64_t)(t0 + t) * a.H + h) * D + j] = run + sXC[t * LC + tid];
     }
   } else if (half == 0 && tid < HC + C) {  // dbeta_t = (W, U~ part) + sum_s dA_ts a_ts
     const int t = tid - HC;
@@ -890,9 +989,9 @@ cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
   const dim3 chunks(nch, a.H, a.N), halves(nch, 2 * a.H, a.N), chains(D / CB, a.H, a.N);
   if (nch > 0) {
     bwd_prep_kernel<Tin><<<chunks, NT, PREP_SMEM, s>>>(a);
-    bwd_fwd_chain_kernel<<<chains, NT, FWD_SMEM, s>>>(a);
+    bwd_fwd_chain_kernel<<<chains, NTC, FWD_SMEM, s>>>(a);
   }
-  bwd_rev_chain_kernel<Tin><<<chains, NT, REV_SMEM, s>>>(a);
+  bwd_rev_chain_kernel<Tin><<<chains, NTC, REV_SMEM, s>>>(a);
   if (nch > 0) {
     bwd_state_grads_kernel<Tin><<<chunks, NT, STATE_SMEM, s>>>(a);
     bwd_wy_grads_kernel<Tin><<<chunks, NT, WY_SMEM, s>>>(a);

@@ -2,9 +2,11 @@
 
 The loss is L = sum_t <d_out_t, o_t> + sum_i <d_final_i, S_T(i)> with seeded upstream gradients; every
 gradient the library returns (dq, dk, dv, dg, dbeta, dS_0) is compared element by element with the oracle's
-on the same input bits.  Tolerance: max |difference| <= TOL x rms(oracle) per gradient tensor, the bar the
-forward outputs meet; the library computes in fp32 from exactly widened inputs, so its error is fp32
-rounding accumulated through the chunk chain (about 1e-5 here), far inside it.
+on the same input bits.  Tolerance: max |difference| <= TOL x rms(oracle) per gradient tensor.  The library
+computes every step in fp32 from exactly widened inputs, so its error is fp32 rounding (unit 6e-8)
+accumulated over sums of up to 128 terms per product, a few products per chunk and the carry through the
+chunk chain; measured about 1e-5 of the rms on the 8192-token workload, so TOL = 1e-4 leaves a 10x margin
+while a wrong term (a dropped product, a wrong decay factor) gives errors of order 1.
 """
 import numpy as np
 import pytest
@@ -16,7 +18,7 @@ from tests._gpu import PrefillRun, dev, host, rel_err, status
 
 pytestmark = pytest.mark.gpu
 
-TOL = 2e-3
+TOL = 1e-4
 NAMES = ("dq", "dk", "dv", "dg", "dbeta", "ds0")
 
 
@@ -52,9 +54,9 @@ def oracle_grads(prob, d_out, d_final, init_zero=False):
                            ds_final=d_final)
 
 
-def check(got, ref, tol=TOL):
+def check(got, ref, tol=TOL, tol_dg=None):
     errs = {n: rel_err(got[n], ref[n]) for n in NAMES}
-    bad = {n: e for n, e in errs.items() if not e <= tol}
+    bad = {n: e for n, e in errs.items() if not e <= (tol_dg if n == "dg" and tol_dg else tol)}
     assert not bad, f"errors {errs}"
     return errs
 
@@ -90,12 +92,15 @@ def test_backward_empty_sequences_pass_the_state_gradient_through(cuda):
 
 def test_backward_steep_gates_take_pairwise_decays(cuda):
     """Gates far below the pages' floor (g ~ -7): a 16-token block spans more than e^80, so the kernels take
-    the pair decays one by one there; values still match."""
+    the pair decays one by one there; values still match.  dg is held to 5e-4: the in-chunk cumulative
+    log-decay reaches |G| ~ 450, where fp32 spacing is 3e-5, so each pair decay e^(G_t - G_s) carries a
+    relative error near 1e-4 (the chunk algebra run in fp64 with only G rounded to fp32 shows 1.2e-4), and
+    here the gradients with respect to g are small (rms 5e-5) next to the terms they are summed from."""
     prob = synth.varlen(seed=64, lengths=[150], H=2, num_slots=2, num_extra=2)
     prob.g = (prob.g * 0 - 7.0 + 0.5 * np.cos(np.arange(prob.g.size)).reshape(prob.g.shape)).astype(np.float32)
     d_out, d_final = synth.output_grads(prob, 64)
     got = BackwardRun(cuda, prob, d_out, d_final).run(cuda)
-    check(got, oracle_grads(prob, d_out, d_final))
+    check(got, oracle_grads(prob, d_out, d_final), tol_dg=5e-4)
 
 
 def test_backward_bad_slot_is_flagged(cuda):
