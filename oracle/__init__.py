@@ -17,6 +17,9 @@ Functions follow these passages:
 * ``backward`` -- the vector-Jacobian product of ``recurrence`` (every forward
   line of the KDA math box differentiated in reverse order), the gradient the
   training side of "Kimi K3 infra report reading", section 7, needs.
+* ``short_conv_step``, ``fused_decode`` -- the decode token with its short causal convolution in front
+  and the gated output norm behind ("SGLang and Miles: day-0 support for Kimi K3", kernels: the fused
+  Conv + KDA + Onorm decode kernel; the stages' formulas are this package's reading, see the docstring).
 * ``decode``, ``verify``, ``fold`` -- the same recurrence over 1 or W tokens;
   "SGLang and Miles day-0 support for Kimi K3", section "ReplaySSM": verify
   reads the committed state and never writes it, fold replays only the accepted
@@ -267,3 +270,71 @@ def fold(pool, slot_ids, wq, wk, wv, wg, wbeta, accepted, threads=0):
         if n > 0:
             out[b] = states[b, n - 1]
     return out
+
+
+# ------------------------------------------------------------------ fused decode front/back-end
+
+G_MIN = -5.0     # lower bound of the log-decay
+CONV_WIDTH = 4   # taps of the short causal convolution
+L2_EPS = 1e-6    # inside the square root of the q / k normalisation
+
+
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def _widen(x):
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)
+
+
+def short_conv_step(x, conv_state, w):
+    """One token of a depthwise causal convolution followed by SiLU.
+
+    x [..., C] the token's input; conv_state [..., C, W-1] the previous W-1 inputs, oldest first;
+    w [C, W] the taps, w[c, W-1] multiplying the current input.  Returns (SiLU(y), new state) with
+    y_c = sum_tau w[c, tau] * window[c, tau] over the window (state, x).
+    """
+    window = np.concatenate([conv_state, x[..., None]], axis=-1)
+    y = (window * w).sum(axis=-1)
+    return y * _sigmoid(y), window[..., 1:]
+
+
+def fused_decode(pool, conv_state, slot_ids, xq, xk, xv, a, b, z, conv_w, norm_w, eps, threads=0):
+    """One decode token per request through the short convolution, the KDA step and the gated output norm.
+
+    Reading of "SGLang and Miles: day-0 support for Kimi K3" (kernels: the fused Conv + KDA + Onorm decode
+    kernel), "Kimi K3: Architecture and SGLang Day-0 Support" (KDA math box: the log-decay kept above
+    g_min = -5 by a scaled sigmoid; the output gate a full-rank projection of the input) and "Kimi K3
+    infra report reading" section 7 (the recurrent state and the conv edges are the two carried parts):
+      q, k, v = SiLU(causal conv_4(x_q, x_k, x_v))           (per channel, window = 3 carried inputs + x)
+      q, k    = q / sqrt(|q|^2 + 1e-6), k / sqrt(|k|^2 + 1e-6)
+      g = G_MIN * sigmoid(a),  beta = sigmoid(b)
+      o = the KDA step (``recurrence`` over one token) from pool[slot]
+      y = o / sqrt(mean(o^2) + eps) * norm_w * sigmoid(z)
+    xq, xk, xv, z [B, H, d] (fp32, bf16 bits or fp64), a [B, H, dk], b [B, H]; pool [S, H, dk, dv];
+    conv_state [S, H, 3, W-1, d] (streams q, k, v; taps oldest first); conv_w [3, H, d, W]; norm_w [dv].
+    Returns (y [B, H, dv], new states [B, H, dk, dv], new conv states [B, H, 3, W-1, d]) in fp64.
+    """
+    slot_ids = np.asarray(slot_ids)
+    xs = [_widen(t) for t in (xq, xk, xv)]
+    cs = _widen(conv_state)[slot_ids]                  # [B, H, 3, W-1, d]
+    cw = _widen(conv_w)                                # [3, H, d, W]
+    outs, new_cs = [], np.empty_like(cs)
+    for s in range(3):
+        st = np.moveaxis(cs[:, :, s], -2, -1)         # [B, H, d, W-1]
+        y, nst = short_conv_step(xs[s], st, cw[s])    # w [H, d, W] broadcasts over B
+        outs.append(y)
+        new_cs[:, :, s] = np.moveaxis(nst, -1, -2)
+    q, k, v = outs
+    q = q / np.sqrt((q * q).sum(-1, keepdims=True) + L2_EPS)
+    k = k / np.sqrt((k * k).sum(-1, keepdims=True) + L2_EPS)
+    g = G_MIN * _sigmoid(_widen(a))
+    beta = _sigmoid(_widen(b))
+    B = q.shape[0]
+    r = recurrence(q, k, v, g, beta, np.arange(B + 1), s0=_widen(pool)[slot_ids], threads=threads)
+    o = r["o"]
+    y = o / np.sqrt((o * o).mean(-1, keepdims=True) + eps) * _widen(norm_w) * _sigmoid(_widen(z))
+    return y, r["s_final"], new_cs
