@@ -418,13 +418,23 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
         counts.copy_(counts0)  # the same open-chunk positions every call (a 1.5 MB copy, timed with it)
         kda.kda_cfbi_decode(q, k, v, g, beta, pool, cache, counts, slots, cf_out)
 
-    for fn in (dec, ver, fold, copy, cfbi):
+    # fused decode (short convolution + KDA step + gated output norm) on the same pool and slots
+    fz = synth.fused_decode_inputs(p.seed, B, H, d, p.pool.shape[0], 1, p.in_dtype, with_pool=False)
+    fx = [to_dev(fz[nm][0]) for nm in ("xq", "xk", "xv", "a", "b", "z")]
+    fcs, fcw, fnw = to_dev(fz["conv_state"]), to_dev(fz["conv_w"]), to_dev(fz["norm_w"])
+    f_out = torch.empty(B, H, d, dtype=torch.bfloat16, device=dev)
+
+    def fused():
+        kda.kda_fused_decode(*fx, pool, slots, fcs, fcw, fnw, f_out)
+
+    for fn in (dec, ver, fold, copy, cfbi, fused):
         for _ in range(3):
             fn()
     torch.cuda.synchronize()
     n = 20
     t = {name: statistics.mean(time_calls(fn, n)) for name, fn in
-         (("decode", dec), ("verify", ver), ("fold", fold), ("state_copy", copy), ("cfbi_decode", cfbi))}
+         (("decode", dec), ("verify", ver), ("fold", fold), ("state_copy", copy), ("cfbi_decode", cfbi),
+          ("fused_decode", fused))}
     heads = B * H
     n_acc = p.accepted.astype(np.int64)
     alg = {
@@ -436,6 +446,9 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
         # written), plus the token's inputs and output
         "cfbi_decode": int(sum(STATE_BYTES + BYTES_PER_TOKEN_HEAD + nl * RF * 4 + (RF * 4 if nl < CH - 1 else STATE_BYTES)
                                for nl in np.minimum(n_open, CH - 1)[p.slot_ids].ravel())),
+        # state and carried convolution inputs (3 streams x 3 taps x d fp32) read and written; xq, xk, xv, z
+        # bf16, a fp32, b in; out bf16
+        "fused_decode": heads * (2 * STATE_BYTES + 2 * 9 * d * 4 + 4 * 2 * d + 4 * d + 4 + 2 * d),
     }
     rep = {"workload": "batched decode + speculative verify: 256 requests, 1024-slot pool, H=12, d=128, "
                        "W=8, accepted ~ min(Poisson(2.7), 8)", "peak_gbs": pk["hbm_gbs"]}

@@ -357,6 +357,49 @@ size_t kda_backward_workspace_size(const kda_backward_args* a);
  */
 kda_status kda_prefill_backward(const kda_backward_args* a, kda_stream_t stream);
 
+/*
+ * Fused decode front/back-end: one decode token through the short causal convolution, the KDA step and the
+ * gated output norm in one launch.
+ * Source: "SGLang and Miles: day-0 support for Kimi K3", section "kernels" (the fused Conv + KDA + Onorm
+ * decode kernel); "Kimi K3: Architecture and SGLang Day-0 Support", KDA math box (the log-decay kept above
+ * g_min = -5 by a scaled sigmoid; an input-dependent full-rank output gate).  The pages give no formula for
+ * the convolution or the norm; this library's reading, per request b and head:
+ *   q, k, v = SiLU(conv(x_q)), SiLU(conv(x_k)), SiLU(conv(x_v)), conv(x)_c = sum_tau w[c][tau] x_{t-3+tau, c}
+ *             (the three previous inputs x_{t-3..t-1} of each stream come from conv_state, which then
+ *             advances by one token);
+ *   q <- q / sqrt(|q|^2 + 1e-6),  k <- k / sqrt(|k|^2 + 1e-6);  g = -5 sigmoid(a);  beta = sigmoid(b);
+ *   o = the KDA step from pool[slot] (as kda_decode_step; pool updated in place);
+ *   out = o / sqrt(mean_c o_c^2 + norm_eps) * norm_w * sigmoid(z).
+ */
+typedef struct {
+  const void* xq;         /* [B][H][128] in_dtype: projected query, before the convolution */
+  const void* xk;         /* [B][H][128] in_dtype */
+  const void* xv;         /* [B][H][128] in_dtype */
+  const float* a;         /* [B][H][128] decay logits */
+  const float* b;         /* [B][H] write-strength logits */
+  const void* z;          /* [B][H][128] in_dtype: output-gate logits */
+  kda_dtype in_dtype;
+  int B, H, dk, dv;       /* dk = dv = 128 (KDA_ERR_UNSUPPORTED otherwise) */
+  float* pool;            /* [num_slots][H][128][128] */
+  int32_t num_slots;
+  const int32_t* slot_ids; /* int32[B] device */
+  float* conv_state;      /* [num_slots][H][3][3][128] fp32: per stream (q, k, v) the 3 previous inputs,
+                             oldest first; read and advanced in place */
+  const float* conv_w;    /* [3][H][128][4] fp32 taps; tap 3 multiplies the current input */
+  const float* norm_w;    /* [128] fp32 */
+  float norm_eps;
+  void* out;              /* [B][H][128] out_dtype */
+  kda_dtype out_dtype;
+  int32_t* dev_status;    /* optional int32[2]; the work counter counts (request x head) units */
+} kda_fused_decode_args;
+
+/* sizeof(kda_fused_decode_args), so a binding can check its mirror of the struct. */
+size_t kda_fused_decode_args_bytes(void);
+
+/* kda_fused_decode -- enqueue the fused decode; an out-of-range slot id sets KDA_DEV_SLOT_OOB and that
+ * request is skipped (no state, carried input or output touched). */
+kda_status kda_fused_decode(const kda_fused_decode_args* a, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,8 +20,8 @@ __all__ = [
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
-    "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "CFBI_CHUNK", "CFBI_ROW_FLOATS",
-    "EXPORTED_SYMBOLS",
+    "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "kda_fused_decode", "CFBI_CHUNK",
+    "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
 ]
 
 KDA_OK = 0
@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
     "kda_cfbi_decode", "kda_backward_args_bytes", "kda_backward_workspace_size", "kda_prefill_backward",
+    "kda_fused_decode_args_bytes", "kda_fused_decode",
 )
 
 
@@ -72,6 +73,18 @@ class BackwardArgs(ctypes.Structure):
         ("dv_out", ctypes.c_void_p), ("dg", ctypes.c_void_p), ("dbeta", ctypes.c_void_p),
         ("d_init", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("dev_status", ctypes.c_void_p),
+    ]
+
+
+class FusedDecodeArgs(ctypes.Structure):
+    """Mirror of kda_fused_decode_args."""
+    _fields_ = [
+        ("xq", ctypes.c_void_p), ("xk", ctypes.c_void_p), ("xv", ctypes.c_void_p), ("a", ctypes.c_void_p),
+        ("b", ctypes.c_void_p), ("z", ctypes.c_void_p), ("in_dtype", ctypes.c_int), ("B", ctypes.c_int),
+        ("H", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("pool", ctypes.c_void_p),
+        ("num_slots", ctypes.c_int32), ("slot_ids", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
+        ("conv_w", ctypes.c_void_p), ("norm_w", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+        ("out", ctypes.c_void_p), ("out_dtype", ctypes.c_int), ("dev_status", ctypes.c_void_p),
     ]
 
 
@@ -123,6 +136,8 @@ def load(build_if_missing: bool = False):
         "kda_backward_args_bytes": (sz, []),
         "kda_backward_workspace_size": (sz, [ctypes.POINTER(BackwardArgs)]),
         "kda_prefill_backward": (c_int, [ctypes.POINTER(BackwardArgs), vp]),
+        "kda_fused_decode_args_bytes": (sz, []),
+        "kda_fused_decode": (c_int, [ctypes.POINTER(FusedDecodeArgs), vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -132,6 +147,8 @@ def load(build_if_missing: bool = False):
         raise RuntimeError("kda_prefill_args layout mismatch between include/kda.h and the binding")
     if lib.kda_backward_args_bytes() != ctypes.sizeof(BackwardArgs):
         raise RuntimeError("kda_backward_args layout mismatch between include/kda.h and the binding")
+    if lib.kda_fused_decode_args_bytes() != ctypes.sizeof(FusedDecodeArgs):
+        raise RuntimeError("kda_fused_decode_args layout mismatch between include/kda.h and the binding")
     _lib = lib
     return lib
 
@@ -398,3 +415,25 @@ def kda_prefill_backward(q, k, v, g, beta, cu_seqlens, max_seqlen, d_out, dq, dk
     a = _backward_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, d_out, dq, dk, dv, dg, dbeta, pool, slot_ids,
                          d_final, d_init, workspace, dev_status)
     _ok("kda_prefill_backward", load().kda_prefill_backward(ctypes.byref(a), _stream(stream)))
+
+
+def kda_fused_decode(xq, xk, xv, a, b, z, pool, slot_ids, conv_state, conv_w, norm_w, out, norm_eps=1e-5,
+                     dev_status=None, stream=None):
+    """One decode token per request through the short convolution, the KDA step and the gated output norm.
+
+    xq, xk, xv, z, out [B, H, 128]; a [B, H, 128]; b [B, H]; pool [S, H, 128, 128];
+    conv_state [S, H, 3, 3, 128] fp32 (advanced in place); conv_w [3, H, 128, 4]; norm_w [128].
+    """
+    _check(xq, xk, xv, a, b, z, pool, slot_ids, conv_state, conv_w, norm_w, out, dev_status)
+    B, H, d = xq.shape
+    f = FusedDecodeArgs()
+    f.xq, f.xk, f.xv, f.a, f.b, f.z = (t.data_ptr() for t in (xq, xk, xv, a, b, z))
+    f.in_dtype = _dt(xq)
+    f.B, f.H, f.dk, f.dv = B, H, d, d
+    f.pool, f.num_slots, f.slot_ids = pool.data_ptr(), pool.shape[0], slot_ids.data_ptr()
+    f.conv_state, f.conv_w, f.norm_w = conv_state.data_ptr(), conv_w.data_ptr(), norm_w.data_ptr()
+    f.norm_eps = float(norm_eps)
+    f.out, f.out_dtype = out.data_ptr(), _dt(out)
+    if dev_status is not None:
+        f.dev_status = dev_status.data_ptr()
+    _ok("kda_fused_decode", load().kda_fused_decode(ctypes.byref(f), _stream(stream)))

@@ -423,3 +423,43 @@ kda_status kda_prefill_backward(const kda_backward_args* a, kda_stream_t stream)
 }
 
 }  // extern "C"
+
+extern "C" {
+
+size_t kda_fused_decode_args_bytes(void) { return sizeof(kda_fused_decode_args); }
+
+kda_status kda_fused_decode(const kda_fused_decode_args* a, kda_stream_t stream) {
+  if (!a) return KDA_ERR_INVALID_ARG;
+  if (!dtype_ok(a->in_dtype) || !dtype_ok(a->out_dtype)) return KDA_ERR_INVALID_ARG;
+  if (a->B < 0 || a->H <= 0 || a->num_slots < 0 || !(a->norm_eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if ((int64_t)a->B * a->H > 0x7fffffff) return KDA_ERR_INVALID_ARG;
+  if (a->dk != 128 || a->dv != 128) return KDA_ERR_UNSUPPORTED;
+  if (a->B == 0) return KDA_OK;
+  const void* ptrs[] = {a->xq, a->xk, a->xv, a->a, a->b, a->z, a->pool, a->slot_ids, a->conv_state, a->conv_w,
+                        a->norm_w, a->out};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda::FusedDecodeArgs f{};
+  f.xq = a->xq;
+  f.xk = a->xk;
+  f.xv = a->xv;
+  f.a = a->a;
+  f.b = a->b;
+  f.z = a->z;
+  f.in_bf16 = a->in_dtype == KDA_DTYPE_BF16;
+  f.out_bf16 = a->out_dtype == KDA_DTYPE_BF16;
+  f.B = a->B;
+  f.H = a->H;
+  f.pool = a->pool;
+  f.num_slots = a->num_slots;
+  f.slot_ids = a->slot_ids;
+  f.conv_state = a->conv_state;
+  f.conv_w = a->conv_w;
+  f.norm_w = a->norm_w;
+  f.eps = a->norm_eps;
+  f.out = a->out;
+  f.status = a->dev_status;
+  return from_cuda(kda::launch_fused_decode(f, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -134,6 +134,27 @@ struct BackwardArgs {
 };
 
 size_t backward_ws_bytes(int64_t T, int N, int H);
+
+// Fused decode: short convolution + KDA step + gated output norm (d = 128).
+struct FusedDecodeArgs {
+  const void *xq, *xk, *xv;  // [B][H][128] pre-convolution projections
+  const float* a;            // [B][H][128] decay logits
+  const float* b;            // [B][H] write-strength logits
+  const void* z;             // [B][H][128] output-gate logits
+  bool in_bf16, out_bf16;
+  int B, H;
+  float* pool;
+  int num_slots;
+  const int32_t* slot_ids;
+  float* conv_state;         // [num_slots][H][3][3][128]
+  const float* conv_w;       // [3][H][128][4]
+  const float* norm_w;       // [128]
+  float eps;
+  void* out;
+  int32_t* status;
+};
+
+cudaError_t launch_fused_decode(const FusedDecodeArgs& a, cudaStream_t s);
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s);
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);

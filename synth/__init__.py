@@ -44,6 +44,7 @@ S_Q, S_K, S_V, S_G, S_BETA, S_S0 = 1, 2, 3, 4, 5, 6
 S_LEN, S_SLOTS, S_ACCEPT, S_SAMPLES, S_EXTRA = 7, 8, 9, 10, 11
 S_WQ, S_WK, S_WV, S_WG, S_WBETA = 21, 22, 23, 24, 25
 S_DO, S_DFINAL = 31, 32
+S_FX, S_FA, S_FB, S_FZ, S_FCS, S_FCW, S_FNW = 41, 42, 43, 44, 45, 46, 47
 
 
 def build(force: bool = False) -> str:
@@ -256,6 +257,25 @@ def output_grads(prob: Prefill, seed: int):
     d_out = normal(seed, S_DO, (prob.T, prob.H, prob.dv), dtype=prob.in_dtype)
     d_final = normal(seed, S_DFINAL, (prob.N, prob.H, prob.dk, prob.dv), 0.0, 0.1, F32)
     return d_out, d_final
+
+
+def fused_decode_inputs(seed: int, B: int, H: int, d: int, num_slots: int, steps: int = 1, dtype: int = BF16,
+                        with_pool: bool = True, threads: int = 0) -> dict:
+    """Seeded inputs of `steps` consecutive fused decode tokens for B requests: pre-convolution projections
+    xq, xk, xv [steps, B, H, d] N(0, 1) and output-gate logits z (input dtype); decay logits a [steps, B, H, d]
+    and write-strength logits b [steps, B, H] N(0, 1) fp32; carried convolution inputs
+    [num_slots, H, 3, 3, d] N(0, 1), taps [3, H, d, 4] N(0, 0.5), norm weight [d] U(0.5, 1.5) (fp32); a state
+    pool [num_slots, H, d, d] N(0, 0.02) (None without with_pool) and B distinct slots."""
+    x = normal(seed, S_FX, (3, steps, B, H, d), dtype=dtype, threads=threads)
+    return dict(xq=x[0], xk=x[1], xv=x[2],
+                a=normal(seed, S_FA, (steps, B, H, d), threads=threads),
+                b=normal(seed, S_FB, (steps, B, H), threads=threads),
+                z=normal(seed, S_FZ, (steps, B, H, d), dtype=dtype, threads=threads),
+                conv_state=normal(seed, S_FCS, (num_slots, H, 3, 3, d), threads=threads),
+                conv_w=normal(seed, S_FCW, (3, H, d, 4), 0.0, 0.5, threads=threads),
+                norm_w=(0.5 + uniform(seed, S_FNW, d)).astype(np.float32),
+                pool=normal(seed, S_S0, (num_slots, H, d, d), 0.0, 0.02, F32, threads) if with_pool else None,
+                slot_ids=distinct_slots(seed, S_SLOTS, B, num_slots))
 
 
 @dataclass
