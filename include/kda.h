@@ -400,6 +400,30 @@ size_t kda_fused_decode_args_bytes(void);
  * request is skipped (no state, carried input or output touched). */
 kda_status kda_fused_decode(const kda_fused_decode_args* a, kda_stream_t stream);
 
+/*
+ * KCP across GPUs: one sequence split into contiguous shards held by W GPUs (ranks), rank r holding the
+ * tokens after those of ranks 0..r-1.
+ * Source: "Kimi K3 training and serving infra" (marsggbo blog), section 4.2 "KCP: pass fixed-size
+ * transition information": each rank computes its shard's cumulative transition M and the state S~ it
+ * produces from a zero input state; one all-gather of these fixed-size fragments (2 x 64 KB per head at
+ * d = 128) and a local prefix scan give every rank its exact entry state; each rank then computes its
+ * outputs.  The exchange itself is the caller's (e.g. torch.distributed); these calls are the per-rank
+ * compute around it.  Per rank (kda_prefill_args describing the rank's shard as N sequences, normally one):
+ *   1. kda_prefill_records (tensor-core path), then kda_kcp_fragments: the fragment of every segment of
+ *      every sequence, the last included, into frag_out [N][P][H][dk][dv + dk] (S~ | M), P as for
+ *      kda_prefill_segmented (one segment when segment_len >= the shard length);
+ *   2. all-gather the fragments of all ranks (rank order);
+ *   3. kda_kcp_scan over the gathered fragments: entries[0] = s0, entries[p+1] = M_p entries[p] + S~_p;
+ *   4. kda_kcp_outputs: outputs and final states from the rank's entry states (entries [N][P][H][dk][dv]),
+ *      reusing the records of step 1 (same workspace); the final state goes to pool[slot_ids[i]].
+ */
+kda_status kda_kcp_fragments(const kda_prefill_args* a, int32_t segment_len, float* frag_out, kda_stream_t stream);
+/* frags [P][H][dk][dv + dk] fp32; s0 [H][dk][dv] fp32 or NULL (zero); entries [P][H][dk][dv] fp32. */
+kda_status kda_kcp_scan(const float* frags, int32_t P, int H, int dk, int dv, const float* s0, float* entries,
+                        int32_t* dev_status, kda_stream_t stream);
+kda_status kda_kcp_outputs(const kda_prefill_args* a, int32_t segment_len, const float* entries,
+                           kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -20,7 +20,8 @@ __all__ = [
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
-    "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "kda_fused_decode", "CFBI_CHUNK",
+    "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "kda_fused_decode",
+    "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs", "CFBI_CHUNK",
     "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
 ]
 
@@ -37,7 +38,7 @@ EXPORTED_SYMBOLS = (
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
     "kda_cfbi_decode", "kda_backward_args_bytes", "kda_backward_workspace_size", "kda_prefill_backward",
-    "kda_fused_decode_args_bytes", "kda_fused_decode",
+    "kda_fused_decode_args_bytes", "kda_fused_decode", "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs",
 )
 
 
@@ -138,6 +139,9 @@ def load(build_if_missing: bool = False):
         "kda_prefill_backward": (c_int, [ctypes.POINTER(BackwardArgs), vp]),
         "kda_fused_decode_args_bytes": (sz, []),
         "kda_fused_decode": (c_int, [ctypes.POINTER(FusedDecodeArgs), vp]),
+        "kda_kcp_fragments": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp, vp]),
+        "kda_kcp_scan": (c_int, [vp, i32, c_int, c_int, c_int, vp, vp, vp, vp]),
+        "kda_kcp_outputs": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -437,3 +441,31 @@ def kda_fused_decode(xq, xk, xv, a, b, z, pool, slot_ids, conv_state, conv_w, no
     if dev_status is not None:
         f.dev_status = dev_status.data_ptr()
     _ok("kda_fused_decode", load().kda_fused_decode(ctypes.byref(f), _stream(stream)))
+
+
+def kda_kcp_fragments(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, segment_len, workspace, frag_out,
+                      dev_status=None, stream=None):
+    """Fragments (S~ | M) of every segment of the shard's sequences, the last included, into frag_out
+    [N, P, H, dk, dv + dk]; run kda_prefill_records on the same workspace first (tensor-core path)."""
+    _check(frag_out)
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, workspace=workspace,
+                        dev_status=dev_status)
+    _ok("kda_kcp_fragments", load().kda_kcp_fragments(ctypes.byref(a), int(segment_len), _p(frag_out),
+                                                      _stream(stream)))
+
+
+def kda_kcp_scan(frags, s0, entries, dev_status=None, stream=None):
+    """entries[0] = s0, entries[p + 1] = M_p entries[p] + S~_p over gathered fragments [P, H, dk, dv + dk]."""
+    _check(frags, s0, entries, dev_status)
+    P, H, dk, w = frags.shape
+    _ok("kda_kcp_scan", load().kda_kcp_scan(_p(frags), P, H, dk, w - dk, _p(s0), _p(entries), _p(dev_status),
+                                            _stream(stream)))
+
+
+def kda_kcp_outputs(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, segment_len, workspace, entries,
+                    dev_status=None, stream=None):
+    """Outputs and final states of the shard from its entry states [N, P, H, dk, dv]."""
+    _check(entries)
+    a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, workspace=workspace,
+                        dev_status=dev_status)
+    _ok("kda_kcp_outputs", load().kda_kcp_outputs(ctypes.byref(a), int(segment_len), _p(entries), _stream(stream)))

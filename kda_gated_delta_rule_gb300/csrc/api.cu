@@ -463,3 +463,47 @@ kda_status kda_fused_decode(const kda_fused_decode_args* a, kda_stream_t stream)
 }
 
 }  // extern "C"
+
+extern "C" {
+
+kda_status kda_kcp_fragments(const kda_prefill_args* a, int32_t segment_len, float* frag_out, kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = seg_prepare(a, segment_len, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  if (!frag_out || !aligned16(frag_out)) return KDA_ERR_INVALID_ARG;
+  p.frag = frag_out;
+  p.frag_all = true;
+  return from_cuda(run_fragments(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_kcp_scan(const float* frags, int32_t P, int H, int dk, int dv, const float* s0, float* entries,
+                        int32_t* dev_status, kda_stream_t stream) {
+  if (P <= 0 || P > 65535 || H <= 0 || H > 65535) return KDA_ERR_INVALID_ARG;
+  if (!head_ok(dk, dv)) return KDA_ERR_UNSUPPORTED;
+  if (!frags || !entries || !aligned16(frags) || !aligned16(entries) || (s0 && !aligned16(s0)))
+    return KDA_ERR_INVALID_ARG;
+  kda::PrefillArgs p{};
+  p.H = H;
+  p.d = dk;
+  p.N = 1;
+  p.P = P;
+  p.seg_len = 1;
+  p.frag = const_cast<float*>(frags);
+  p.entry = entries;
+  p.scan_nseg = P;
+  p.scan_s0 = s0;
+  p.status = dev_status;
+  return from_cuda(kda::launch_seg_scan(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_kcp_outputs(const kda_prefill_args* a, int32_t segment_len, const float* entries,
+                           kda_stream_t stream) {
+  kda::PrefillArgs p;
+  kda_status st = seg_prepare(a, segment_len, &p);
+  if (st != KDA_OK || a->N == 0) return st;
+  if (!entries || !aligned16(entries)) return KDA_ERR_INVALID_ARG;
+  p.entry = const_cast<float*>(entries);
+  return from_cuda(run_outputs(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -90,6 +90,11 @@ struct PrefillArgs {
   float* entry; // [N][P][H][d][d]
   // tensor-core path: per (chunk, head) operand records written by the prep kernel
   uint8_t* records;
+  // sequence split across GPUs (KCP between ranks): fragments also for the last segment of each sequence;
+  // a scan over scan_nseg given fragments (N = 1, no cu_seqlens) from scan_s0 [H][d][d] (null: zero)
+  bool frag_all;
+  int scan_nseg;
+  const float* scan_s0;
 };
 
 // Batch-invariant (CF-BI) prefill and decode (d = 128).

@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT) prefill_seq_kernel(const Prefil
     t0 = s0 + (int64_t)p * a.seg_len;
     t1 = t0 + a.seg_len < s1 ? t0 + a.seg_len : s1;
     if (MODE == MODE_FRAG) {
-      if (t1 >= s1) return;  // the last segment's fragment is never used (also: segments past the end)
+      // the last segment's fragment is never used on one GPU (also: segments past the end)
+      if (t0 >= s1 || (t1 >= s1 && !a.frag_all)) return;
     } else if (t0 >= s1 && !(p == 0 && s1 == s0)) {
       return;  // past the end; an empty sequence keeps segment 0 to write its final state
     }
@@ -175,26 +176,33 @@ __global__ void __launch_bounds__(ScanCfg<D>::NT) seg_scan_kernel(const PrefillA
   float* Sin = smem + D * (D + 1);     // [D][CT]
   const int tid = threadIdx.x;
   const int ct = blockIdx.x % (D / CT), h = blockIdx.x / (D / CT), i = blockIdx.y;
-  const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
-  if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
-    if (tid == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
-    return;
-  }
-  const int nseg = (int)((s1 - s0 + a.seg_len - 1) / a.seg_len);
-  int slot = 0;
-  if (!a.init_zero) {
-    slot = a.slot_ids[i];
-    if (slot < 0 || slot >= a.num_slots) {
-      if (tid == 0) flag_status(a.status, KDA_DEV_SLOT_OOB);
+  const size_t head_elems = (size_t)D * D;
+  int nseg;
+  const float* init = nullptr;  // this head's initial state (null: zero)
+  if (a.scan_nseg > 0) {        // fragments gathered from several GPUs: the count and initial state are given
+    nseg = a.scan_nseg;
+    if (a.scan_s0) init = a.scan_s0 + (size_t)h * head_elems;
+  } else {
+    const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
+    if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
+      if (tid == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
       return;
     }
+    nseg = (int)((s1 - s0 + a.seg_len - 1) / a.seg_len);
+    if (!a.init_zero) {
+      const int slot = a.slot_ids[i];
+      if (slot < 0 || slot >= a.num_slots) {
+        if (tid == 0) flag_status(a.status, KDA_DEV_SLOT_OOB);
+        return;
+      }
+      init = a.pool + ((size_t)slot * a.H + h) * head_elems;
+    }
   }
-  const size_t head_elems = (size_t)D * D;
   const int c0 = ct * CT;
   float* entry_i = a.entry + (size_t)i * a.P * a.H * head_elems;
   for (int e = tid; e < D * CT; e += C::NT) {
     const int r = e / CT, c = e % CT;
-    const float x = a.init_zero ? 0.f : a.pool[((size_t)slot * a.H + h) * head_elems + (size_t)r * D + c0 + c];
+    const float x = init ? init[(size_t)r * D + c0 + c] : 0.f;
     Sin[r * CT + c] = x;
     entry_i[(size_t)h * head_elems + (size_t)r * D + c0 + c] = x;
   }

@@ -666,7 +666,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     t0 = s0 + (int64_t)p * a.seg_len;
     t1 = t0 + a.seg_len < s1 ? t0 + a.seg_len : s1;
     if (MODE == MODE_FRAG) {
-      if (t1 >= s1) return;
+      if (t0 >= s1 || (t1 >= s1 && !a.frag_all)) return;
     } else if (t0 >= s1 && !(p == 0 && s1 == s0)) {
       return;
     }

@@ -1,0 +1,104 @@
+"""KCP across ranks: the host-side exchange of kcp_prefill, run as two gloo processes on the CPU.
+
+Each rank holds one contiguous shard of a sequence.  The per-rank compute is done by the fp64 oracle here
+(the fragment: the shard's state from a zero input state and its cumulative transition; the outputs: the
+recurrence from the entry state); the exchange, its rank order and the entry selection are the library's
+kcp_prefill.  Every rank's outputs and the last rank's final state must equal the unsplit recurrence, and
+all ranks must hold identical entry states.
+"""
+import os
+import socket
+import sys
+
+import numpy as np
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _problem():
+    rng = np.random.default_rng(21)
+    T, H, d = 150, 2, 8
+    k = rng.standard_normal((T, H, d))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    return dict(q=rng.standard_normal((T, H, d)), k=k, v=rng.standard_normal((T, H, d)),
+                g=-np.abs(rng.standard_normal((T, H, d))) * 0.3, beta=rng.uniform(0.05, 0.95, (T, H))), \
+        rng.standard_normal((H, d, d)) * 0.1
+
+
+class OracleOps:
+    """The per-rank compute of KCP by the fp64 oracle (test stand-in for the GPU kernels)."""
+
+    def __init__(self, shard):
+        self.shard = shard
+        self.out = self.final = None
+
+    def fragments(self):
+        import oracle
+        s = self.shard
+        L = s["q"].shape[0]
+        zero = oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], [0, L])["s_final"][0]
+        M = oracle.transition(s["k"], s["g"], s["beta"], [0, L])[0]
+        return torch.from_numpy(np.concatenate([zero, M], axis=-1))  # [H, d, 2d]: S~ | M
+
+    def scan(self, frags, s0):
+        f = frags.numpy()
+        d = f.shape[2]
+        e = [np.zeros_like(f[0, :, :, :d]) if s0 is None else s0.numpy()]
+        for p in range(f.shape[0] - 1):
+            e.append(np.einsum("hij,hjc->hic", f[p, :, :, d:], e[-1]) + f[p, :, :, :d])
+        return torch.from_numpy(np.stack(e))
+
+    def outputs(self, entry):
+        import oracle
+        s = self.shard
+        r = oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], [0, s["q"].shape[0]],
+                              s0=entry.numpy()[None])
+        self.out, self.final = r["o"], r["s_final"][0]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    from kda_gated_delta_rule_gb300.kcp import kcp_prefill, shard_bounds
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    full, s0 = _problem()
+    b = shard_bounds(full["q"].shape[0], world)
+    ops = OracleOps({n: x[b[rank]:b[rank + 1]] for n, x in full.items()})
+    entries = kcp_prefill(ops, torch.from_numpy(s0))
+    q.put((rank, entries.numpy(), ops.out, ops.final))
+    dist.destroy_process_group()
+
+
+def test_two_ranks_reproduce_the_unsplit_recurrence():
+    import oracle
+    from kda_gated_delta_rule_gb300.kcp import shard_bounds
+
+    world = 2
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+    assert all(p.exitcode == 0 for p in procs)
+    full, s0 = _problem()
+    T = full["q"].shape[0]
+    ref = oracle.recurrence(*(full[n] for n in ("q", "k", "v", "g", "beta")), [0, T], s0=s0[None])
+    b = shard_bounds(T, world)
+    np.testing.assert_array_equal(res[0][1], res[1][1])  # identical entry states on every rank
+    for rank, entries, out, final in res:
+        np.testing.assert_allclose(out, ref["o"][b[rank]:b[rank + 1]], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(res[-1][3], ref["s_final"][0], rtol=0, atol=1e-11)
+    # the scan's entry state of rank 1 is the state after rank 0's tokens
+    head = oracle.recurrence(*(full[n][:b[1]] for n in ("q", "k", "v", "g", "beta")), [0, b[1]], s0=s0[None])
+    np.testing.assert_allclose(res[0][1][1], head["s_final"][0], rtol=0, atol=1e-11)
