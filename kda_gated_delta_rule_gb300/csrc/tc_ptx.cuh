@@ -202,6 +202,18 @@ __device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* m
       : "memory");
 }
 
+// Tiled TMA store of a 3-D box from shared memory to coordinates (x, y, z) described by `map`, as part of this
+// thread's bulk group (bulk_commit; the source may be reused after a wait on the group's reads).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, const void* src_smem) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(smem_u32(src_smem))
+               : "memory");
+}
+
+// waits until every committed bulk group of this thread but the most recent has finished reading its source
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 // ---- bf16 two-term split: x ~= hi + lo with hi = bf16(x), lo = bf16(x - hi)
 __device__ __forceinline__ void split2(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);

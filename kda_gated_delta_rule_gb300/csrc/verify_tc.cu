@@ -22,8 +22,9 @@
 // exp(G_t - G_s) directly, which never exceeds 1 for s <= t.
 //
 // Schedule: one persistent CTA per SM walks (request, head) items.  Warps 0-7 ("math") receive each
-// window's raw inputs one item ahead (TMA tensor-map loads of k, q, v, g; cp.async for beta) and compute
-// Qh (into a double-buffered B tile), Oh and the raw-input record.  Warps 8-15 ("state") receive each committed state by a 64 KB bulk copy into a
+// window's raw inputs one item ahead (TMA tensor-map loads of k, q, v, g; cp.async for beta), write the
+// raw-input record straight from those buffers (TMA tensor-map stores, issued as soon as they land) and
+// compute Qh (into a double-buffered B tile) and Oh.  Warps 8-15 ("state") receive each committed state by a 64 KB bulk copy into a
 // shared-memory ring (two items ahead when the window fits 8 tokens), split it into tensor memory, and one
 // thread issues the product into one of two accumulators; the output epilogue of item n runs after the
 // split of item n + 1.  The groups hand over through mbarriers with bounded waits.
@@ -66,8 +67,8 @@ struct Work {
   alignas(16) float P[WP][WP];  // q_t . k_s e^{G_t - G_s}, s <= t
 };
 
-struct VMaps {  // [B*W][H][128] token rows, box = one head x W rows
-  CUtensorMap q, k, v, g;
+struct VMaps {  // [B*W][H][128] token rows, box = one head x W rows: inputs, then the record's k, v, g
+  CUtensorMap q, k, v, g, rk, rv, rg;
 };
 
 template <int WP>
@@ -237,6 +238,7 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       Raw<WP>& r = raw_of(n);
       uint64_t* fb = &full_r[n & 1];
       if (mtid == 0) {
+        tc::bulk_wait_read1();  // the record stores of item n-1 have read this buffer
         tc::bar_arrive_expect_tx(fb, (uint32_t)W * (3 * D * 2 + D * 4));
         const int y = it.h, z = it.b * W;
         tc::tma_load_3d(r.k, &maps.k, 0, y, z, fb);
@@ -259,6 +261,14 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       const bool ok = slot >= 0 && slot < num_slots;
       Raw<WP>& r = raw_of(n);
       if (!tc::bar_wait(&full_r[n & 1], (n >> 1) & 1) && mtid == 0) flag_status(status, KDA_DEV_TIMEOUT);
+      if (mtid == 0) {  // the raw-input record: the exact stored bits the fold consumes
+        if (ok) {
+          tc::tma_store_3d(&maps.rk, 0, it.h, it.b * W, r.k);
+          tc::tma_store_3d(&maps.rv, 0, it.h, it.b * W, r.v);
+          tc::tma_store_3d(&maps.rg, 0, it.h, it.b * W, r.g);
+        }
+        tc::bulk_commit();  // one group per item (empty when skipped): "all but the latest" is item n-1's
+      }
       tc::named_bar(BAR_MATH, MT);  // every math thread is done with item n-1 (and its buffers)
       if (n + 1 < cnt) fetch(n + 1);
       if (!ok && mtid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
@@ -348,22 +358,10 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       }
       tc::bar_arrive(&full_w[n & 1]);
 
-      // 4. the raw-input record: the exact stored bits the fold consumes
-      if (ok) {
-        for (int e = mtid; e < W * 64; e += MT) {
-          const int t = e >> 6, x = e & 63;
-          const size_t row = it.row0 + (size_t)t * H;
-          if (x < 16)
-            reinterpret_cast<uint4*>(static_cast<bf16*>(rec.k) + row * D)[x] = reinterpret_cast<const uint4*>(r.k[t])[x];
-          else if (x < 32)
-            reinterpret_cast<uint4*>(static_cast<bf16*>(rec.v) + row * D)[x - 16] =
-                reinterpret_cast<const uint4*>(r.v[t])[x - 16];
-          else
-            reinterpret_cast<uint4*>(rec.g + row * D)[x - 32] = reinterpret_cast<const uint4*>(r.g[t])[x - 32];
-        }
-        if (mtid < W) rec.beta[it.row0 + (size_t)mtid * H] = r.beta[mtid];
-      }
+      // 4. the record's beta (k, v and g went out by tensor stores)
+      if (ok && mtid < W) rec.beta[it.row0 + (size_t)mtid * H] = r.beta[mtid];
     }
+    if (mtid == 0) tc::bulk_wait_all();  // the record stores are complete before the CTA exits
   } else {
     // ------------------------------------------------------------------ state warps
     const int sidx = tid - MT, half = sidx >> 7, c = sidx & (D - 1);
@@ -471,7 +469,10 @@ cudaError_t launch_wp(const VerifyArgs& a, cudaStream_t st) {
   if (rows > 0x7fffffff) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   VMaps maps;
   if (!encode_token_map(&maps.q, a.q, false, rows, a.H, a.W) || !encode_token_map(&maps.k, a.k, false, rows, a.H, a.W) ||
-      !encode_token_map(&maps.v, a.v, false, rows, a.H, a.W) || !encode_token_map(&maps.g, a.g, true, rows, a.H, a.W))
+      !encode_token_map(&maps.v, a.v, false, rows, a.H, a.W) || !encode_token_map(&maps.g, a.g, true, rows, a.H, a.W) ||
+      !encode_token_map(&maps.rk, a.rec.k, false, rows, a.H, a.W) ||
+      !encode_token_map(&maps.rv, a.rec.v, false, rows, a.H, a.W) ||
+      !encode_token_map(&maps.rg, a.rec.g, true, rows, a.H, a.W))
     return cudaErrorNotSupported;
   const int grid = items < sms ? items : sms;
   verify_tc_kernel<WP, Tout><<<grid, NT, L::BYTES, st>>>(maps, a.beta, a.B, a.W, a.H, a.pool, a.num_slots, a.slot_ids,
