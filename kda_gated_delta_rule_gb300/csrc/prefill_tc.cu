@@ -99,7 +99,8 @@ constexpr uint32_t PS_G = 180224;       // g, then G (in place) [64][128] fp32
 constexpr uint32_t PS_BETA = 212992;    // beta [2][64], double-buffered by task parity
 constexpr uint32_t PS_BAR = 213760;     // three mbarriers: inputs, Gram product, W/U products
 constexpr uint32_t PS_SLOT = 213784;
-constexpr uint32_t PS_BYTES = 213800 + 1024;
+constexpr uint32_t PS_NEXT = 213800;    // the task after next (looked up by the duty thread): index, n, h, i, t0
+constexpr uint32_t PS_BYTES = 213824 + 1024;
 constexpr int PREP_NT = 512;
 constexpr int PREP_PARTS = PREP_NT / D;  // threads per channel in the per-channel phases
 
@@ -233,21 +234,25 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     int64_t t0;
     int n, h, i;  // n = valid tokens (0: empty slot or malformed cu_seqlens)
   };
-  auto task_at = [&](int t) {
+  // task t given its sequence's bounds s0 = cu[i], s1 = cu[i + 1]
+  auto task_from = [&](int t, int64_t s0, int64_t s1) {
     Task r;
     const int cidx = t % nchunk;
     r.h = (t / nchunk) % a.H;
     r.i = t / (nchunk * a.H);
     r.n = 0;
     r.t0 = 0;
-    const int64_t s0 = a.cu[r.i], s1 = a.cu[r.i + 1];
     if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
-      if (tid == 0 && cidx == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
+      if (tid == DUTY && cidx == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
       return r;
     }
     r.t0 = s0 + (int64_t)cidx * C;
     if (r.t0 < s1) r.n = (int)((s1 - r.t0) < C ? (s1 - r.t0) : C);
     return r;
+  };
+  auto task_at = [&](int t) {
+    const int i = t / (nchunk * a.H);
+    return task_from(t, a.cu[i], a.cu[i + 1]);
   };
   auto next_task = [&](int t) {
     while (t < total && task_at(t).n == 0) t += (int)gridDim.x;
@@ -285,18 +290,24 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   tc::fence_after_sync();
   const uint32_t tm = *tslot;
   uint32_t gram_uses = 0;
+  // the current and the next task; the one after is looked up mid-task (its cu_seqlens loads then overlap
+  // the inverse instead of sitting at the top of the loop)
   int cur = next_task((int)blockIdx.x);
+  Task tcur{};
+  if (cur < total) tcur = task_at(cur);
+  int nxt = cur < total ? next_task(cur + (int)gridDim.x) : total;
+  Task tnxt{};
+  if (nxt < total) tnxt = task_at(nxt);
   int inflight = -1;  // local index of a task whose inputs are requested but not yet waited for
   if (cur < total) {
-    fetch(task_at(cur), 0);
+    fetch(tcur, 0);
     inflight = 0;
   }
   bool ok = true;
   int k = 0;
 #pragma unroll 1
   for (; cur < total; ++k) {
-  const Task tk = task_at(cur);
-  const int nxt = next_task(cur + (int)gridDim.x);
+  const Task tk = tcur;
   const int h = tk.h, i = tk.i, n = tk.n;
   const int64_t t0 = tk.t0;
   uint8_t* rec = ws + ((size_t)(t0 / C + i) * a.H + h) * REC_BYTES;
@@ -314,7 +325,6 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     *reinterpret_cast<float4*>(sG + t * D + cc * 8) = make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4*>(sG + t * D + cc * 8 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's staged tiles (X, Y regions) have been read
   __syncthreads();
   // cumulative log-decay in place: thread (j, part) scans 16 tokens and adds the totals of the parts
   // before it; the decay span of channel j (including the chunk start, G = 0) decides the path
@@ -322,8 +332,9 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   {
     constexpr int TQ = C / PREP_PARTS;
     const int j = tid & (D - 1), part = tid / D;
-    float* ext = reinterpret_cast<float*>(sm + PS_XHI);           // extremes, before X is built
-    float* gpart = reinterpret_cast<float*>(sm + PS_XHI + 8192);  // part totals [PREP_PARTS][D]
+    // scratch in the Y region (free here; the X region may still be read by the previous task's stores)
+    float* ext = reinterpret_cast<float*>(sm + PS_YHI);           // extremes
+    float* gpart = reinterpret_cast<float*>(sm + PS_YHI + 8192);  // part totals [PREP_PARTS][D]
     float x[TQ];
 #pragma unroll
     for (int u = 0; u < TQ; ++u) x[u] = sG[(TQ * part + u) * D + j];
@@ -353,6 +364,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       span = gmax - gmin;
     }
   }
+  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's staged W, U~ tiles (X region) have been read
   tc::fence_before_sync();
   const bool slow = __syncthreads_or(span > SPAN_MAX);
   tc::fence_after_sync();
@@ -503,8 +515,17 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   }
   // raw k, q, v, g are dead: the next task's inputs
   if (ok && nxt < total) {
-    fetch(task_at(nxt), k + 1);
+    fetch(tnxt, k + 1);
     inflight = k + 1;
+  }
+  // the duty thread starts looking up the task after next: the candidate's cu_seqlens loads are issued
+  // here and consumed before the W/U product, thousands of cycles later
+  const int cand = nxt < total ? nxt + (int)gridDim.x : total;
+  int64_t cs0 = 0, cs1 = 0;
+  if (tid == DUTY && cand < total) {
+    const int ci = cand / (nchunk * a.H);
+    cs0 = __ldg(a.cu + ci);
+    cs1 = __ldg(a.cu + ci + 1);
   }
 
   if (ok) {
@@ -523,27 +544,29 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       for (int r = 0; r < 16; ++r) sT[(16 * b + r) * 64 + 16 * b + cc] = x[r];
     }
     __syncthreads();
-    // off-diagonal blocks by distance d: Z = sum_k A_ik T_kj (kept in the unused upper block (j, i)),
-    // then T_ij = -T_ii Z
+    // off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  First
+    // M_ik = T_ii A_ik for all six pairs k < i at once (kept in the unused upper block (k, i)), then block
+    // row by block row T_ij = -sum_k M_ik T_kj
+    for (int o = tid; o < 6 * 256; o += PREP_NT) {
+      const int pr = o >> 8, r = (o >> 4) & 15, c = o & 15;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+      const int bi = pr == 0 ? 1 : (pr < 3 ? 2 : 3);
+      const int bk = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);
+      float acc = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (u <= r) acc = fmaf(sT[(16 * bi + r) * 64 + 16 * bi + u], sA[(16 * bi + u) * 64 + 16 * bk + c], acc);
+      sT[(16 * bk + r) * 64 + 16 * bi + c] = acc;
+    }
+    __syncthreads();
 #pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-      const int nb = 4 - d;
-      for (int o = tid; o < nb * 256; o += PREP_NT) {
-        const int bi = d + (o >> 8), bj = bi - d, r = (o >> 4) & 15, c = o & 15;
+    for (int bi = 1; bi < 4; ++bi) {
+      for (int o = tid; o < bi * 256; o += PREP_NT) {
+        const int bj = o >> 8, r = (o >> 4) & 15, c = o & 15;
         float acc = 0.f;
         for (int bk = bj; bk < bi; ++bk)
 #pragma unroll
           for (int u = 0; u < 16; ++u)
-            acc = fmaf(sA[(16 * bi + r) * 64 + 16 * bk + u], sT[(16 * bk + u) * 64 + 16 * bj + c], acc);
-        sT[(16 * bj + r) * 64 + 16 * bi + c] = acc;
-      }
-      __syncthreads();
-      for (int o = tid; o < nb * 256; o += PREP_NT) {
-        const int bi = d + (o >> 8), bj = bi - d, r = (o >> 4) & 15, c = o & 15;
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-          if (u <= r) acc = fmaf(sT[(16 * bi + r) * 64 + 16 * bi + u], sT[(16 * bj + u) * 64 + 16 * bi + c], acc);
+            acc = fmaf(sT[(16 * bk + r) * 64 + 16 * bi + u], sT[(16 * bk + u) * 64 + 16 * bj + c], acc);
         sT[(16 * bi + r) * 64 + 16 * bj + c] = -acc;
       }
       __syncthreads();
@@ -558,6 +581,23 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
         v[e] = s <= t ? sT[t * 64 + s] * sbeta[s] : 0.f;
       }
       split8_store(sm + PS_TBHI + tc::sw128_chunk(t, cc), sm + PS_TBLO + tc::sw128_chunk(t, cc), v);
+    }
+    if (tid == DUTY) {  // the task after next (an empty candidate falls back to the full search)
+      int n2 = cand;
+      Task t2{};
+      if (n2 < total) {
+        t2 = task_from(n2, cs0, cs1);
+        if (t2.n == 0) {
+          n2 = next_task(n2 + (int)gridDim.x);
+          if (n2 < total) t2 = task_at(n2);
+        }
+      }
+      int* nx = reinterpret_cast<int*>(sm + PS_NEXT);
+      nx[0] = n2;
+      nx[1] = t2.n;
+      nx[2] = t2.h;
+      nx[3] = t2.i;
+      *reinterpret_cast<int64_t*>(sm + PS_NEXT + 16) = t2.t0;
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
@@ -606,6 +646,17 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   }
   if (!ok) break;
   cur = nxt;
+  tcur = tnxt;
+  {
+    const int* nx = reinterpret_cast<const int*>(sm + PS_NEXT);
+    nxt = nx[0];
+    if (nxt < total) {
+      tnxt.n = nx[1];
+      tnxt.h = nx[2];
+      tnxt.i = nx[3];
+      tnxt.t0 = *reinterpret_cast<const int64_t*>(sm + PS_NEXT + 16);
+    }
+  }
   }  // task loop
   if (!ok) {
     if (tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
