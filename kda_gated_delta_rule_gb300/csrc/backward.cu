@@ -124,6 +124,25 @@ __device__ __forceinline__ void load_rows(float* dst, int ld, const bf16* src, i
   }
 }
 
+// acc += sum_{r < 8} x[r * xs] * y4[r * ys .. + 3]: the 8 scalar and 8 16-byte shared loads are issued
+// before the FMAs, so one group of a loop waits on shared-memory latency once
+__device__ __forceinline__ void dot8x4(const float* x, int xs, const float* y, int ys, float (&acc)[4]) {
+  float xv[8];
+  float4 yv[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    xv[r] = x[r * xs];
+    yv[r] = *reinterpret_cast<const float4*>(y + r * ys);
+  }
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    acc[0] = fmaf(xv[r], yv[r].x, acc[0]);
+    acc[1] = fmaf(xv[r], yv[r].y, acc[1]);
+    acc[2] = fmaf(xv[r], yv[r].z, acc[2]);
+    acc[3] = fmaf(xv[r], yv[r].w, acc[3]);
+  }
+}
+
 struct Seq {
   int bos, eos;
 };
@@ -337,7 +356,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
 //    The next chunk's operands are copied in while the current one is processed (two stages).
 // ---------------------------------------------------------------------------------------------------
 constexpr int FS_STAGE = 2 * C * LD + C * CB + D;  // W, K^, U~ columns, e^G_C
-constexpr size_t FWD_SMEM = (2 * FS_STAGE + D * CB + C * CB) * sizeof(float);
+constexpr int FS_PART = 20;                        // row stride of the partial sums (16 columns, padded)
+constexpr size_t FWD_SMEM = (2 * FS_STAGE + D * CB + C * CB + 4 * D * FS_PART) * sizeof(float);
 
 __global__ void __launch_bounds__(NTC, 1) bwd_fwd_chain_kernel(BackwardArgs a) {
   const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
@@ -346,6 +366,7 @@ __global__ void __launch_bounds__(NTC, 1) bwd_fwd_chain_kernel(BackwardArgs a) {
   extern __shared__ float sm[];
   float* sS = sm + 2 * FS_STAGE;  // state columns [128][CB]
   float* sU = sS + D * CB;        // U columns [64][CB]
+  float* sPart = sU + C * CB;     // K^^T U over four 16-token quarters [4][128][FS_PART]
   const float* s0 = nullptr;
   if (!a.init_zero) {
     const int slot = a.slot_ids[i];
@@ -380,50 +401,72 @@ __global__ void __launch_bounds__(NTC, 1) bwd_fwd_chain_kernel(BackwardArgs a) {
     const float* sUt = sKh + C * LD;
     const float* sGam = sUt + C * CB;
     float* w = record(a, sq.bos + c * C, i, h);
-    for (int e = tid; e < D * CB; e += NTC) w[BW_H + (e / CB) * D + c0 + e % CB] = sS[e];
-    {  // U = U~ - W S: row t = tid / 8, columns tid % 8 + 8m
-      const int t = tid >> 3, cl = tid & 7;
-      float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < D; ++j) {
-        const float x = sW[t * LD + j];
-        acc0 = fmaf(x, sS[j * CB + cl], acc0);
-        acc1 = fmaf(x, sS[j * CB + cl + 8], acc1);
-      }
-      const float u0 = sUt[t * CB + cl] - acc0, u1 = sUt[t * CB + cl + 8] - acc1;
-      sU[t * CB + cl] = u0;
-      sU[t * CB + cl + 8] = u1;
-      w[BW_U + t * D + c0 + cl] = u0;
-      w[BW_U + t * D + c0 + cl + 8] = u1;
+    {  // the entry state, 16-byte stores
+      const int j = tid >> 2, c4 = (tid & 3) * 4;
+      *reinterpret_cast<float4*>(w + BW_H + j * D + c0 + c4) = *reinterpret_cast<const float4*>(sS + j * CB + c4);
+    }
+    // register tiles of 4 contiguous columns (16-byte shared loads of the state / U rows)
+    if (tid < 256) {  // U = U~ - W S: row t = tid / 4
+      const int t = tid >> 2, c4 = (tid & 3) * 4;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int j = 0; j < D; j += 8) dot8x4(sW + t * LD + j, 1, sS + j * CB + c4, CB, acc);
+      const float4 ut = *reinterpret_cast<const float4*>(sUt + t * CB + c4);
+      const float4 u = make_float4(ut.x - acc[0], ut.y - acc[1], ut.z - acc[2], ut.w - acc[3]);
+      *reinterpret_cast<float4*>(sU + t * CB + c4) = u;
+      *reinterpret_cast<float4*>(w + BW_U + t * D + c0 + c4) = u;
     }
     __syncthreads();
-    {  // S = Diag(e^G_C) S + K^^T U: row j = tid / 4, columns tid % 4 + 4m (own elements only: in place)
-      const int j = tid >> 2, cl = tid & 3;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-      for (int t = 0; t < C; ++t) {
-        const float x = sKh[t * LD + j];
+    {  // K^^T U: lane = row j of a 32-row group, all 16 columns in registers, tokens split in four quarters
+       // (each token's U row is read once per warp, as a broadcast)
+      const int warp = tid >> 5, lane = tid & 31;
+      const int j = 32 * (warp & 3) + lane, tq = warp >> 2;
+      float acc[16];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, sU[t * CB + cl + 4 * m], acc[m]);
+      for (int m = 0; m < 16; ++m) acc[m] = 0.f;
+#pragma unroll 4
+      for (int t = 16 * tq; t < 16 * tq + 16; ++t) {
+        const float x = sKh[t * LD + j];
+        const float4* u = reinterpret_cast<const float4*>(sU + t * CB);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 y = u[q];
+          acc[4 * q] = fmaf(x, y.x, acc[4 * q]);
+          acc[4 * q + 1] = fmaf(x, y.y, acc[4 * q + 1]);
+          acc[4 * q + 2] = fmaf(x, y.z, acc[4 * q + 2]);
+          acc[4 * q + 3] = fmaf(x, y.w, acc[4 * q + 3]);
+        }
+      }
+      float4* dst = reinterpret_cast<float4*>(sPart + (tq * D + j) * FS_PART);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    }
+    __syncthreads();
+    {  // S = Diag(e^G_C) S + the four quarters: row j = tid / 4 (own elements only: in place)
+      const int j = tid >> 2, c4 = (tid & 3) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int tq = 0; tq < 4; ++tq) {
+        const float4 p = *reinterpret_cast<const float4*>(sPart + (tq * D + j) * FS_PART + c4);
+        acc.x += p.x, acc.y += p.y, acc.z += p.z, acc.w += p.w;
       }
       const float gm = sGam[j];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int cc = cl + 4 * m;
-        sS[j * CB + cc] = fmaf(gm, sS[j * CB + cc], acc[m]);
-      }
+      float4* sp = reinterpret_cast<float4*>(sS + j * CB + c4);
+      const float4 sv = *sp;
+      *sp = make_float4(fmaf(gm, sv.x, acc.x), fmaf(gm, sv.y, acc.y), fmaf(gm, sv.z, acc.z), fmaf(gm, sv.w, acc.w));
     }
     __syncthreads();
   }
 }
 
 // ---------------------------------------------------------------------------------------------------
-// 3. reverse chain: dS' at every chunk exit, dU, and dS_0.  Stage A (P, K^, dO columns, e^G_C) is
-//    double-buffered and copied in a chunk ahead; stage B (Q+, W) is copied in during the previous
-//    chunk's dU step.
+// 3. reverse chain: dS' at every chunk exit, dU, and dS_0.  Stage A (P, K^, Q+, dO columns, e^G_C) is
+//    double-buffered and copied in a chunk ahead; stage B (W) is copied in during the previous chunk's
+//    dU step.  Threads 0-255 form dU while threads 256-511 form Q+^T dO for rows j and j + 64, and then
+//    finish dS for those rows; register tiles of 4 contiguous columns read 16-byte rows of dS', dU, dO.
 // ---------------------------------------------------------------------------------------------------
-constexpr int RS_A = C * LC + C * LD + C * CB + D;  // P, K^, raw dO columns (<= 64 x 16 fp32), e^G_C
-constexpr int RS_B = 2 * C * LD;                    // Q+, W
+constexpr int RS_A = C * LC + 2 * C * LD + C * CB + D;  // P, K^, Q+, raw dO columns (<= 64 x 16 fp32), e^G_C
+constexpr int RS_B = C * LD;                            // W
 constexpr size_t REV_SMEM = (2 * RS_A + RS_B + D * CB + C * CB) * sizeof(float);
 
 template <typename Tin>
@@ -432,8 +475,8 @@ __global__ void __launch_bounds__(NTC, 1) bwd_rev_chain_kernel(BackwardArgs a) {
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
   extern __shared__ float sm[];
-  float* sB = sm + 2 * RS_A;     // Q+, W
-  float* sdS = sB + RS_B;        // dS columns [128][CB]
+  float* sW = sm + 2 * RS_A;     // W
+  float* sdS = sW + RS_B;        // dS columns [128][CB]
   float* sdU = sdS + D * CB;     // dU columns [64][CB]
   const float* dfin = a.d_final ? a.d_final + ((size_t)i * a.H + h) * D * D : nullptr;
   for (int e = tid; e < D * CB; e += NTC) sdS[e] = dfin ? dfin[(e / CB) * D + c0 + e % CB] : 0.f;
@@ -446,89 +489,123 @@ __global__ void __launch_bounds__(NTC, 1) bwd_rev_chain_kernel(BackwardArgs a) {
     const float* w = record(a, t0, i, h);
     load_rows<NTC>(st, LC, w + BW_P, C, C, C, 0, C);
     load_rows<NTC>(st + C * LC, LD, w + BW_KH, D, C, C, 0, D);
+    load_rows<NTC>(st + C * LC + C * LD, LD, w + BW_QP, D, C, C, 0, D);
     const Tin* src = reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D + c0;
-    Tin* dst = reinterpret_cast<Tin*>(st + C * LC + C * LD);
+    Tin* dst = reinterpret_cast<Tin*>(st + C * LC + 2 * C * LD);
     for (int e = tid; e < C * DO_Q; e += NTC) {
       const int r = e / DO_Q, q = e % DO_Q;
       cp_async16(reinterpret_cast<float*>(dst + r * CB + q * (16 / (int)sizeof(Tin))),
                  reinterpret_cast<const float*>(src + (r < n ? r : 0) * rs + q * (16 / (int)sizeof(Tin))),
                  r < n ? 16 : 0);
     }
-    load_rows<NTC>(st + C * LC + C * LD + C * CB, D, w + BW_GAM, D, 1, 1, 0, D);
+    load_rows<NTC>(st + C * LC + 2 * C * LD + C * CB, D, w + BW_GAM, D, 1, 1, 0, D);
     cp_async_commit();
   };
   auto issue_b = [&](int c) {
     const float* w = record(a, sq.bos + c * C, i, h);
-    load_rows<NTC>(sB, LD, w + BW_QP, D, C, C, 0, D);
-    load_rows<NTC>(sB + C * LD, LD, w + BW_W, D, C, C, 0, D);
+    load_rows<NTC>(sW, LD, w + BW_W, D, C, C, 0, D);
     cp_async_commit();
   };
   if (nc > 0) {
     issue_a(nc - 1, 0);
     issue_b(nc - 1);
   }
+  auto fma4 = [](float x, const float (&y)[4], float (&acc)[4]) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[m] = fmaf(x, y[m], acc[m]);
+  };
   for (int c = nc - 1, k = 0; c >= 0; --c, ++k) {
     cp_async_wait<1>();  // stage A of chunk c has landed (stage B may still be in flight)
     __syncthreads();
     if (c > 0) issue_a(c - 1, (k + 1) & 1);
     const float* sP = sm + (k & 1) * RS_A;
     const float* sKh = sP + C * LC;
-    const Tin* sDO = reinterpret_cast<const Tin*>(sKh + C * LD);
-    const float* sGam = sKh + C * LD + C * CB;
-    const float* sQp = sB;
-    const float* sW = sB + C * LD;
+    const float* sQp = sKh + C * LD;
+    const Tin* sDO = reinterpret_cast<const Tin*>(sQp + C * LD);
+    const float* sGam = sQp + C * LD + C * CB;
     float* w = record(a, sq.bos + c * C, i, h);
-    for (int e = tid; e < D * CB; e += NTC) w[BW_DS + (e / CB) * D + c0 + e % CB] = sdS[e];
-    {  // dU = P^T dO + K^ dS': row t = tid / 8, columns tid % 8 + 8m
-      const int t = tid >> 3, cl = tid & 7;
-      float acc0 = 0.f, acc1 = 0.f;
-      for (int s = t; s < C; ++s) {
-        const float x = sP[s * LC + t];
-        acc0 = fmaf(x, to_f32(sDO[s * CB + cl]), acc0);
-        acc1 = fmaf(x, to_f32(sDO[s * CB + cl + 8]), acc1);
+    {  // dS' of this chunk, 16-byte stores
+      const int j = tid >> 2, c4 = (tid & 3) * 4;
+      *reinterpret_cast<float4*>(w + BW_DS + j * D + c0 + c4) = *reinterpret_cast<const float4*>(sdS + j * CB + c4);
+    }
+    const int c4 = (tid & 3) * 4;
+    float y0[4] = {0.f, 0.f, 0.f, 0.f}, y1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (tid < 256) {  // dU = P^T dO + K^ dS': row t = tid / 4
+      const int t = tid >> 2;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int s = t & ~7; s < C; s += 8) {  // P[s][t] = 0 for s < t
+        float pv[8], ov[8][4];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          pv[r] = sP[(s + r) * LC + t];
+          ld4(sDO + (s + r) * CB + c4, ov[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) fma4(pv[r], ov[r], acc);
       }
-#pragma unroll 8
-      for (int j = 0; j < D; ++j) {
-        const float x = sKh[t * LD + j];
-        acc0 = fmaf(x, sdS[j * CB + cl], acc0);
-        acc1 = fmaf(x, sdS[j * CB + cl + 8], acc1);
+#pragma unroll 1
+      for (int j = 0; j < D; j += 8) dot8x4(sKh + t * LD + j, 1, sdS + j * CB + c4, CB, acc);
+      const float4 u = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(sdU + t * CB + c4) = u;
+      *reinterpret_cast<float4*>(w + BW_DU + t * D + c0 + c4) = u;
+    } else {  // Q+^T dO for rows j and j + 64
+      const int j = (tid - 256) >> 2;
+#pragma unroll 1
+      for (int t = 0; t < C; t += 8) {
+        float q0[8], q1[8], ov[8][4];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          q0[r] = sQp[(t + r) * LD + j];
+          q1[r] = sQp[(t + r) * LD + j + 64];
+          ld4(sDO + (t + r) * CB + c4, ov[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          fma4(q0[r], ov[r], y0);
+          fma4(q1[r], ov[r], y1);
+        }
       }
-      sdU[t * CB + cl] = acc0;
-      sdU[t * CB + cl + 8] = acc1;
-      w[BW_DU + t * D + c0 + cl] = acc0;
-      w[BW_DU + t * D + c0 + cl + 8] = acc1;
     }
     if (c > 0)
       cp_async_wait<1>();  // stage B of chunk c has landed (the next stage A may still be in flight)
     else
       cp_async_wait<0>();
     __syncthreads();
-    {  // dS = Q+^T dO + Diag(e^G_C) dS' - W^T dU: row j = tid / 4, columns tid % 4 + 4m (in place)
-      const int j = tid >> 2, cl = tid & 3;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-      for (int t = 0; t < C; ++t) {
-        const float x = sQp[t * LD + j], y = sW[t * LD + j];
+    if (tid >= 256) {  // dS = Q+^T dO + Diag(e^G_C) dS' - W^T dU for rows j and j + 64 (in place)
+      const int j = (tid - 256) >> 2;
+#pragma unroll 1
+      for (int t = 0; t < C; t += 8) {
+        float w0[8], w1[8], uv[8][4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const int cc = cl + 4 * m;
-          acc[m] = fmaf(x, to_f32(sDO[t * CB + cc]), acc[m]);
-          acc[m] = fmaf(-y, sdU[t * CB + cc], acc[m]);
+        for (int r = 0; r < 8; ++r) {
+          w0[r] = -sW[(t + r) * LD + j];
+          w1[r] = -sW[(t + r) * LD + j + 64];
+          ld4(sdU + (t + r) * CB + c4, uv[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          fma4(w0[r], uv[r], y0);
+          fma4(w1[r], uv[r], y1);
         }
       }
-      const float gm = sGam[j];
+      float* s0p = sdS + j * CB + c4;
+      float* s1p = sdS + (j + 64) * CB + c4;
+      const float g0 = sGam[j], g1 = sGam[j + 64];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int cc = cl + 4 * m;
-        sdS[j * CB + cc] = fmaf(gm, sdS[j * CB + cc], acc[m]);
+        s0p[m] = fmaf(g0, s0p[m], y0[m]);
+        s1p[m] = fmaf(g1, s1p[m], y1[m]);
       }
     }
     __syncthreads();
     if (c > 0) issue_b(c - 1);
   }
+  __syncthreads();  // (a sequence without chunks: the fill above used another thread mapping)
   if (a.d_init) {
     float* dst = a.d_init + ((size_t)i * a.H + h) * D * D;
-    for (int e = tid; e < D * CB; e += NTC) dst[(e / CB) * D + c0 + e % CB] = sdS[e];
+    const int j = tid >> 2, c4 = (tid & 3) * 4;
+    *reinterpret_cast<float4*>(dst + j * D + c0 + c4) = *reinterpret_cast<const float4*>(sdS + j * CB + c4);
   }
 }
 
