@@ -200,6 +200,11 @@ __device__ __forceinline__ void cfbi_load_token(float* rows, Scratch& scr, int t
   __syncthreads();
 }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+
 struct CfbiSmem {
   alignas(16) float rows[CH * RF];
   Scratch scr;
@@ -291,11 +296,37 @@ __global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restric
     if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
     return;
   }
+  // every global load is issued before the first wait: the token's inputs (registers), the entry state
+  // (registers, consumed by the read-out) and the cached rows (asynchronous copies into shared memory)
+  const size_t row = (size_t)b * H + h;
+  const int c = tid & (D - 1);
+  float x0, x1, x2 = 0.f, xb = 0.f;
+  if (tid < D) {
+    x0 = to_f32(k[row * D + c]);
+    x1 = g[row * D + c];
+    x2 = to_f32(q[row * D + c]);
+  } else {
+    x0 = to_f32(v[row * D + c]);
+    x1 = 0.f;
+    if (c == 0) xb = beta[row];
+  }
   float sv[64];
   load_part(sv, Sg, tid);  // in flight while the row's own quantities are formed
-  for (int e = tid; e < L * RF / 4; e += NT) reinterpret_cast<float4*>(s.rows)[e] = reinterpret_cast<const float4*>(cg)[e];
-  const size_t row = (size_t)b * H + h;
-  cfbi_load_token(s.rows, s.scr, L, q, k, v, g, beta, row, tid);  // (ends with a barrier)
+  for (int e = tid; e < L * RF / 4; e += NT) cp_async16(reinterpret_cast<float4*>(s.rows) + e, reinterpret_cast<const float4*>(cg) + e);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  {
+    float* rt = s.rows + L * RF;
+    if (tid < D) {
+      rt[R_K + c] = x0;
+      rt[R_G + c] = x1;
+      s.scr.q[c] = x2;
+    } else {
+      rt[R_V + c] = x0;
+      if (c == 0) rt[R_BETA] = xb;
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
   const float o = cfbi_row(s.rows, s.scr, L, sv, tid);
   if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
   if (L + 1 == CH) {
