@@ -41,7 +41,7 @@ constexpr int D = 128;
 constexpr int MT = 256;  // math threads, warps 0-7
 constexpr int ST = 256;  // state threads, warps 8-15
 constexpr int NT = MT + ST;
-constexpr int BAR_MATH = 1, BAR_STATE = 2;  // named barriers
+constexpr int BAR_MATH = 1, BAR_STATE = 2, BAR_TEAM = 3;  // named barriers (BAR_TEAM + team: two-team math)
 constexpr float G_SPAN = 80.f;              // |G| bound of the factored decay path
 constexpr uint32_t STATE_BYTES = D * D * 4;
 
@@ -74,6 +74,9 @@ struct VMaps {  // [B*W][H][128] token rows, box = one head x W rows: inputs, th
 template <int WP>
 struct PLayout {
   static constexpr int STAGES = WP <= 8 ? 2 : 1;  // committed states in flight
+  // W <= 8: two math teams of four warps take alternate items (each with two raw-input buffers and its own
+  // work area); W > 8: one team of eight warps (shared memory holds no second set)
+  static constexpr int TEAMS = WP <= 8 ? 2 : 1;
   // B operand: rows 0..WP-1 = bf16 hi of Qh, rows WP..2WP-1 = bf16 lo, x 128 key channels: two 64-channel
   // K-blocks, 8-row groups 1024 bytes apart
   static constexpr uint32_t B_ROWS = 2 * WP, B_BLOCK = B_ROWS * 128, B_TILE = 2 * B_BLOCK;
@@ -81,9 +84,11 @@ struct PLayout {
   static constexpr uint32_t OH = BT + 2 * B_TILE;
   static constexpr uint32_t RAW_BYTES = (uint32_t)((sizeof(Raw<WP>) + 127) / 128 * 128);
   static constexpr uint32_t RAW = OH + 2 * WP * D * 4;
-  static constexpr uint32_t WORK = RAW + 2 * RAW_BYTES;
-  static constexpr uint32_t BARS = WORK + (uint32_t)((sizeof(Work<WP>) + 127) / 128 * 128);
+  static constexpr uint32_t WORK = RAW + 2 * TEAMS * RAW_BYTES;
+  static constexpr uint32_t WORK_BYTES = (uint32_t)((sizeof(Work<WP>) + 127) / 128 * 128);
+  static constexpr uint32_t BARS = WORK + TEAMS * WORK_BYTES;
   static constexpr uint32_t BYTES = BARS + 128 + 1024;  // + slack for the 1024-byte alignment
+  static_assert(BYTES <= 232448, "shared memory");
   static_assert(sizeof(Raw<WP>::k) % 16 == 0, "TMA destinations stay 16-byte aligned");
 };
 
@@ -203,8 +208,8 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
   uint64_t* full_w = full_s + 2;                                  // Qh / Oh written         [2]
   uint64_t* empty_w = full_s + 4;                                 // Qh / Oh consumed        [2]
   uint64_t* mma_bar = full_s + 6;                                 // product complete        [2]
-  uint64_t* full_r = full_s + 8;                                  // raw inputs landed       [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 80);
+  uint64_t* full_r = full_s + 8;                                  // raw inputs landed       [2 * TEAMS]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 112);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = B * H;
   const int cnt = (int)blockIdx.x < items ? (items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
@@ -212,25 +217,161 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
   auto raw_of = [&](int n) -> Raw<WP>& { return *reinterpret_cast<Raw<WP>*>(sm + L::RAW + (n & 1) * L::RAW_BYTES); };
 
   // setup: barriers, tensor memory, beta past the window
+  constexpr int TEAMS = L::TEAMS;
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       tc::bar_init(&full_s[i], 1);
-      tc::bar_init(&full_w[i], MT);
+      tc::bar_init(&full_w[i], MT / TEAMS);  // every thread of the team that computed the item
       tc::bar_init(&empty_w[i], ST);
       tc::bar_init(&mma_bar[i], 1);
-      tc::bar_init(&full_r[i], 1 + W);  // the TMA issuer + one cp.async arrival per beta
     }
+    for (int i = 0; i < 2 * TEAMS; ++i) tc::bar_init(&full_r[i], 1 + W);  // TMA issuer + a cp.async per beta
     tc::bar_fence_init();
   }
   if (warp == 8) tc::tmem_alloc(tslot, TMEM_COLS);
-  if (tid < 2 * WP && (tid % WP) >= W) raw_of(tid / WP).beta[tid % WP] = 0.f;
+  if (tid < 2 * TEAMS * WP && (tid % WP) >= W)
+    reinterpret_cast<Raw<WP>*>(sm + L::RAW + (tid / WP) * L::RAW_BYTES)->beta[tid % WP] = 0.f;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = *tslot;
 
-  if (warp < 8) {
-    // ------------------------------------------------------------------ math warps
+  if (TEAMS == 2 && warp < 8) {
+    // ------------------------------------------------------------------ math warps, two teams
+    // team t (warps 4t .. 4t+3) takes items n = t, t + 2, ...; its m-th item uses raw buffer 2t + m%2 and
+    // full_r barrier 2t + m%2 (parity (m/2)%2), its work area, and the B tile / Oh buffer n%2 = t
+    const int team = warp >> 2, ttid = tid & 127, tw = warp & 3, c = ttid;
+    const int bar_team = BAR_TEAM + team;
+    Work<WP>& wt = *reinterpret_cast<Work<WP>*>(sm + L::WORK + team * L::WORK_BYTES);
+    auto raw_t = [&](int m) -> Raw<WP>& {
+      return *reinterpret_cast<Raw<WP>*>(sm + L::RAW + (2 * team + (m & 1)) * L::RAW_BYTES);
+    };
+    auto fetch = [&](int m) {  // the team's m-th item
+      const Item it = item_at(item_index(2 * m + team), W, H);
+      Raw<WP>& r = raw_t(m);
+      uint64_t* fb = &full_r[2 * team + (m & 1)];
+      if (ttid == 0) {
+        tc::bulk_wait_read1();  // the record stores of the team's item m-2 have read this buffer
+        tc::bar_arrive_expect_tx(fb, (uint32_t)W * (3 * D * 2 + D * 4));
+        const int y = it.h, z = it.b * W;
+        tc::tma_load_3d(r.k, &maps.k, 0, y, z, fb);
+        tc::tma_load_3d(r.q, &maps.q, 0, y, z, fb);
+        tc::tma_load_3d(r.v, &maps.v, 0, y, z, fb);
+        tc::tma_load_3d(r.g, &maps.g, 0, y, z, fb);
+      }
+      if (ttid >= 32 && ttid < 32 + W) {
+        const int t = ttid - 32;
+        cp_async4(&r.beta[t], beta + it.row0 + (size_t)t * H);
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(fb)) : "memory");
+      }
+    };
+    if (team < cnt) fetch(0);
+    for (int m = 0; 2 * m + team < cnt; ++m) {
+      const int n = 2 * m + team;
+      const Item it = item_at(item_index(n), W, H);
+      const int slot = slot_ids[item_index(n) / H];
+      const bool ok = slot >= 0 && slot < num_slots;
+      Raw<WP>& r = raw_t(m);
+      if (!tc::bar_wait(&full_r[2 * team + (m & 1)], (m >> 1) & 1) && ttid == 0) flag_status(status, KDA_DEV_TIMEOUT);
+      if (ttid == 0) {  // the raw-input record: the exact stored bits the fold consumes
+        if (ok) {
+          tc::tma_store_3d(&maps.rk, 0, it.h, it.b * W, r.k);
+          tc::tma_store_3d(&maps.rv, 0, it.h, it.b * W, r.v);
+          tc::tma_store_3d(&maps.rg, 0, it.h, it.b * W, r.g);
+        }
+        tc::bulk_commit();  // one group per item (empty when skipped)
+      }
+      tc::named_bar(bar_team, 128);  // the team is done with its previous item (and its buffers)
+      if (n + 2 < cnt) fetch(m + 1);
+      if (!ok && ttid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+
+      // 1. per channel c: G, K o e^G, Q o e^G, Y = K o e^-G; is the factored path valid?
+      bool out_of_span = false;
+      {
+        float gv[WP], kv[WP], qv[WP];
+#pragma unroll
+        for (int t = 0; t < WP; ++t) {
+          const bool in = t < W;
+          gv[t] = in ? r.g[t][c] : 0.f;
+          kv[t] = in ? __bfloat162float(r.k[t][c]) : 0.f;
+          qv[t] = in ? __bfloat162float(r.q[t][c]) : 0.f;
+        }
+        float run = 0.f;
+#pragma unroll
+        for (int t = 0; t < WP; ++t) {
+          run = __fadd_rn(run, gv[t]);
+          gv[t] = run;
+        }
+#pragma unroll
+        for (int t = 0; t < WP; ++t) {
+          const float ep = __expf(gv[t]);
+          wt.Kp[t][c] = kv[t] * ep;
+          wt.Qp[t][c] = qv[t] * ep;
+          wt.G[t][c] = gv[t];
+          wt.Y[t][c] = kv[t] * __expf(-gv[t]);
+          out_of_span |= !(fabsf(gv[t]) <= G_SPAN);
+        }
+      }
+      const bool pairwise = tc::named_bar_or(bar_team, 128, out_of_span);
+
+      // 2. A and P, rows tw and 7 - tw per warp of the team
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int t = rr ? 7 - tw : tw;
+        if (pairwise) gram_row<WP, false>(r, wt, t, W, lane);
+        else gram_row<WP, true>(r, wt, t, W, lane);
+      }
+      tc::named_bar(bar_team, 128);
+
+      // 3. per channel, both paths: x = (I + A)^-1 diag(beta) y by forward substitution, then P x, for y = K o e^G
+      //    (Qh = Q o e^G - P x, into B tile n%2) and y = V (Oh = P x, into its buffer)
+      if (n >= 2 && !tc::bar_wait(&empty_w[n & 1], ((n >> 1) + 1) & 1) && ttid == 0)
+        flag_status(status, KDA_DEV_TIMEOUT);
+      {
+        float xk[WP], xv[WP], rk[WP], rv[WP];
+#pragma unroll
+        for (int t = 0; t < WP; ++t) {
+          const float bt = r.beta[t];
+          float ak = bt * wt.Kp[t][c], av = bt * (t < W ? __bfloat162float(r.v[t][c]) : 0.f);
+#pragma unroll
+          for (int u = 0; u < t; ++u) {
+            const float a = wt.A[t][u];
+            ak = fmaf(-a, xk[u], ak);
+            av = fmaf(-a, xv[u], av);
+          }
+          xk[t] = ak;
+          xv[t] = av;
+          rk[t] = wt.Qp[t][c];
+          rv[t] = 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < WP; ++t)
+#pragma unroll
+          for (int u = 0; u <= t; ++u) {
+            const float pp = wt.P[t][u];
+            rk[t] = fmaf(-pp, xk[u], rk[t]);
+            rv[t] = fmaf(pp, xv[u], rv[t]);
+          }
+        uint8_t* bt = sm + L::BT + (n & 1) * L::B_TILE + (uint32_t)(c >> 6) * L::B_BLOCK;
+        float* oh = reinterpret_cast<float*>(sm + L::OH) + (n & 1) * WP * D;
+#pragma unroll
+        for (int t = 0; t < WP; ++t) {
+          const bf16 hh = __float2bfloat16_rn(rk[t]);
+          const bf16 ll = __float2bfloat16_rn(rk[t] - __bfloat162float(hh));
+          *reinterpret_cast<bf16*>(bt + tc::sw128(t, c & 63)) = hh;
+          *reinterpret_cast<bf16*>(bt + tc::sw128(WP + t, c & 63)) = ll;
+          oh[t * D + c] = rv[t];
+        }
+        tc::fence_proxy_async();
+      }
+      tc::bar_arrive(&full_w[n & 1]);
+
+      // 4. the record's beta (k, v and g went out by tensor stores)
+      if (ok && ttid < W) rec.beta[it.row0 + (size_t)ttid * H] = r.beta[ttid];
+    }
+    if (ttid == 0) tc::bulk_wait_all();  // the record stores are complete before the CTA exits
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------ math warps, one team
     const int mtid = tid, half = mtid >> 7, c = mtid & (D - 1);
     // raw inputs of item n into buffer n%2: four tensor-map loads (one thread) and W beta words
     auto fetch = [&](int n) {
