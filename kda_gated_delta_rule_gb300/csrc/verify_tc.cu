@@ -45,8 +45,9 @@ constexpr int BAR_MATH = 1, BAR_STATE = 2, BAR_TEAM = 3;  // named barriers (BAR
 constexpr float G_SPAN = 80.f;              // |G| bound of the factored decay path
 constexpr uint32_t STATE_BYTES = D * D * 4;
 
-// tensor memory: two buffers of [S0^T hi (64 columns of bf16 pairs) | lo | 2*WP fp32 accumulator columns]
-constexpr uint32_t TMEM_COLS = 512, BUF_COLS = 256, COL_AHI = 0, COL_ALO = 64, COL_ACC = 128;
+// tensor memory: two buffers of [S0^T hi (64 columns of bf16 pairs) | lo | two accumulators of 2*WP fp32
+// columns: S0 hi and S0 lo against the stacked Qh rows, issued by two threads]
+constexpr uint32_t TMEM_COLS = 512, BUF_COLS = 256, COL_AHI = 0, COL_ALO = 64, COL_ACC = 128, COL_ACC2 = 192;
 
 template <int WP>
 struct Raw {  // one window's raw inputs (cp.async targets); rows at or past W are stale
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       tc::bar_init(&full_s[i], 1);
       tc::bar_init(&full_w[i], MT / TEAMS);  // every thread of the team that computed the item
       tc::bar_init(&empty_w[i], ST);
-      tc::bar_init(&mma_bar[i], 1);
+      tc::bar_init(&mma_bar[i], 2);  // one commit per issuing thread
     }
     for (int i = 0; i < 2 * TEAMS; ++i) tc::bar_init(&full_r[i], 1 + W);  // TMA issuer + a cp.async per beta
     tc::bar_fence_init();
@@ -522,10 +523,17 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       const bool done = __all_sync(0xffffffffu, tc::bar_wait(&mma_bar[m & 1], (m >> 1) & 1));
       if (!done && lane == 0) flag_status(status, KDA_DEV_TIMEOUT);
       tc::fence_after_sync();
-      // accumulator column t = S0 (hi + lo) against Qh hi of token t, column WP + t against its lo part
-      float d[2 * WP];
+      // accumulator column t = S0 hi (first accumulator) or S0 lo (second) against Qh hi of token t, column
+      // WP + t against its lo part
+      float d[2 * WP], d2[2 * WP];
       tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC, d);
-      if constexpr (WP > 8) tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC + 16, d + 16);
+      tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC2, d2);
+      if constexpr (WP > 8) {
+        tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC + 16, d + 16);
+        tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC2 + 16, d2 + 16);
+      }
+#pragma unroll
+      for (int e = 0; e < 2 * WP; ++e) d[e] += d2[e];
       const float* oh = reinterpret_cast<const float*>(sm + L::OH) + (m & 1) * WP * D;
       if (ok && done) {
         constexpr int TH = WP / 2;
@@ -574,20 +582,20 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       if (sidx == 0 && n + STAGES < cnt) issue_state(n + STAGES, slot_ahead);
       if (n >= 1) epilogue(n - 1, ok_prev);  // frees item n-1's Qh / Oh buffers before waiting on item n's
       ok_prev = slot_n >= 0 && slot_n < num_slots;
-      if (sidx == 0) {
+      if (sidx == 0 || sidx == 32) {
         if (!tc::bar_wait(&full_w[n & 1], (n >> 1) & 1)) flag_status(status, KDA_DEV_TIMEOUT);
         tc::fence_after_sync();
-        // D = S0^T [Qh hi; Qh lo]^T (128 value columns x 2WP): S0 hi, then S0 lo, 8 K-steps each.  A
+        // D = S0^T [Qh hi; Qh lo]^T (128 value columns x 2WP), 8 K-steps: S0 hi by thread 0 of warp 8 into
+        // the first accumulator, S0 lo by thread 0 of warp 9 into the second, issued side by side.  A
         // descriptor of base + off equals the base descriptor + off/16 (the start-address field).
+        const int part = sidx == 32;
         const uint64_t bdesc = tc::sdesc(tc::smem_u32(sm + L::BT + (n & 1) * L::B_TILE));
         const uint32_t buf = tm + (n & 1) * BUF_COLS;
         constexpr uint32_t idesc = tc::idesc_bf16(128, L::B_ROWS);
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ts(buf + COL_ACC, buf + (part ? COL_ALO : COL_AHI) + 8 * ks,
-                       bdesc + (((ks >> 2) * L::B_BLOCK + (ks & 3) * 32u) >> 4), idesc, (part | ks) != 0);
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_ts(buf + (part ? COL_ACC2 : COL_ACC), buf + (part ? COL_ALO : COL_AHI) + 8 * ks,
+                     bdesc + (((ks >> 2) * L::B_BLOCK + (ks & 3) * 32u) >> 4), idesc, ks != 0);
         tc::commit(&mma_bar[n & 1]);
       }
     }
