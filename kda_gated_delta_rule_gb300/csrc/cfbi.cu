@@ -296,8 +296,9 @@ __global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restric
     if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
     return;
   }
-  // every global load is issued before the first wait: the token's inputs (registers), the entry state
-  // (registers, consumed by the read-out) and the cached rows (asynchronous copies into shared memory)
+  // the token's inputs (registers) and the cached rows (asynchronous copies into shared memory) first; once
+  // the token is in shared memory, the entry state's loads (registers) are issued and stay in flight
+  // through the row's own algebra, which does not read them, until the read-out
   const size_t row = (size_t)b * H + h;
   const int c = tid & (D - 1);
   float x0, x1, x2 = 0.f, xb = 0.f;
@@ -310,8 +311,6 @@ __global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restric
     x1 = 0.f;
     if (c == 0) xb = beta[row];
   }
-  float sv[64];
-  load_part(sv, Sg, tid);  // in flight while the row's own quantities are formed
   for (int e = tid; e < L * RF / 4; e += NT) cp_async16(reinterpret_cast<float4*>(s.rows) + e, reinterpret_cast<const float4*>(cg) + e);
   asm volatile("cp.async.commit_group;" ::: "memory");
   {
@@ -325,6 +324,9 @@ __global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restric
       if (c == 0) rt[R_BETA] = xb;
     }
   }
+  asm volatile("" ::: "memory");  // the state loads below are not hoisted above the token's stores
+  float sv[64];
+  load_part(sv, Sg, tid);  // in flight while the row's own quantities are formed
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   const float o = cfbi_row(s.rows, s.scr, L, sv, tid);
