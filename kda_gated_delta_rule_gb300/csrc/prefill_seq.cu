@@ -160,20 +160,40 @@ __global__ void __launch_bounds__(SeqCfg<D>::NT) prefill_seq_kernel(const Prefil
 
 // Fragment scan: for each (sequence, head, column tile of the state), sequentially over segments,
 // entry_{p+1} = M_p entry_p + S~_p, with entry_0 the initial state.
+//
+// Only the running entry tile is on the dependent path: M_p and this tile's columns of S~_p do not depend
+// on earlier steps, so the next segment's are copied into the other half of a double buffer (cp.async)
+// while the current product runs.  Thread (kq, rgp, cgp) holds rows rgp + RGS r (r = 0..3) and columns
+// 4 cgp..4 cgp + 3 over the kq-th of KS slices of the contraction; slices 1.. leave partial sums in shared
+// memory for slice 0 to add in slice order.  With rows D + 4 floats apart the eight rows a warp reads fall
+// in eight bank groups.
 template <int D>
 struct ScanCfg {
   static constexpr int CT = 16;  // state columns per CTA (D / 16 CTAs per head)
-  static constexpr int RGS = D / 4, CGS = CT / 4, NT = RGS * CGS;
-  static constexpr size_t SMEM = sizeof(float) * ((size_t)D * (D + 1) + (size_t)D * CT);
+  static constexpr int KS = D >= 64 ? 4 : 1;  // contraction slices: more warps to cover shared-load latency
+  static constexpr int RGS = D / 4, CGS = CT / 4, NTS = RGS * CGS, NT = NTS * KS;
+  static constexpr int MS = D + 4;  // row stride of the staged M (16-byte aligned rows)
+  static constexpr size_t M_FLOATS = (size_t)D * MS, B_FLOATS = (size_t)D * CT;
+  // two staged (M, S~ tile) pairs, the running entry tile, the partial sums of slices 1..KS-1
+  static constexpr size_t SMEM = sizeof(float) * (2 * (M_FLOATS + B_FLOATS) + B_FLOATS + (KS - 1) * B_FLOATS);
 };
+
+__device__ __forceinline__ void scan_cp16(float* dst, const float* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void scan_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void scan_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(ScanCfg<D>::NT) seg_scan_kernel(const PrefillArgs a) {
   using C = ScanCfg<D>;
-  constexpr int CT = C::CT;
-  extern __shared__ float smem[];
-  float* Ms = smem;                    // [D][D+1]
-  float* Sin = smem + D * (D + 1);     // [D][CT]
+  constexpr int CT = C::CT, MS = C::MS;
+  extern __shared__ __align__(16) float smem[];
+  float* const Sin = smem + 2 * (C::M_FLOATS + C::B_FLOATS);  // [D][CT]
   const int tid = threadIdx.x;
   const int ct = blockIdx.x % (D / CT), h = blockIdx.x / (D / CT), i = blockIdx.y;
   const size_t head_elems = (size_t)D * D;
@@ -200,66 +220,86 @@ __global__ void __launch_bounds__(ScanCfg<D>::NT) seg_scan_kernel(const PrefillA
   }
   const int c0 = ct * CT;
   float* entry_i = a.entry + (size_t)i * a.P * a.H * head_elems;
+  // segment p's M (columns D..2D-1 of its fragment [D][2D]) and S~ columns c0..c0+CT-1 into buffer p & 1
+  auto stage = [&](int p) {
+    const float* fr = a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2;
+    float* Mb = smem + (p & 1) * (C::M_FLOATS + C::B_FLOATS);
+    float* Bb = Mb + C::M_FLOATS;
+#pragma unroll 4
+    for (int e = tid; e < D * (D / 4); e += C::NT) {
+      const int r = e / (D / 4), l4 = e % (D / 4);
+      scan_cp16(Mb + r * MS + 4 * l4, fr + (size_t)r * 2 * D + D + 4 * l4);
+    }
+    for (int e = tid; e < D * (CT / 4); e += C::NT) {
+      const int r = e / (CT / 4), q4 = e % (CT / 4);
+      scan_cp16(Bb + r * CT + 4 * q4, fr + (size_t)r * 2 * D + c0 + 4 * q4);
+    }
+    scan_commit();
+  };
+  if (nseg > 1) stage(0);
   for (int e = tid; e < D * CT; e += C::NT) {
     const int r = e / CT, c = e % CT;
     const float x = init ? init[(size_t)r * D + c0 + c] : 0.f;
     Sin[r * CT + c] = x;
     entry_i[(size_t)h * head_elems + (size_t)r * D + c0 + c] = x;
   }
-  const int rgp = tid / C::CGS, cgp = tid % C::CGS;
+  float* const Part = Sin + C::B_FLOATS;  // [KS - 1][D][CT]
+  const int kq = tid / C::NTS, rgp = (tid % C::NTS) / C::CGS, cgp = tid % C::CGS;
+  constexpr int LK = D / C::KS;
   for (int p = 0; p + 1 < nseg; ++p) {
-    const float* fr = a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2;  // [D][2D]
-    __syncthreads();  // Sin complete; previous Ms reads done
-    // stage M (columns D..2D-1 of the fragment) with independent 128-bit loads
-    constexpr int V4 = D * D / 4 / C::NT;  // float4 per thread
-#pragma unroll
-    for (int b = 0; b < V4; b += 8) {
-      float4 x[8];
-#pragma unroll
-      for (int u = 0; u < 8 && b + u < V4; ++u) {
-        const int e = (b + u) * C::NT + tid;
-        const int r = e / (D / 4), l4 = e % (D / 4);
-        x[u] = *reinterpret_cast<const float4*>(fr + (size_t)r * 2 * D + D + 4 * l4);
-      }
-#pragma unroll
-      for (int u = 0; u < 8 && b + u < V4; ++u) {
-        const int e = (b + u) * C::NT + tid;
-        const int r = e / (D / 4), l4 = e % (D / 4);
-        float* dst = Ms + r * (D + 1) + 4 * l4;
-        dst[0] = x[u].x;
-        dst[1] = x[u].y;
-        dst[2] = x[u].z;
-        dst[3] = x[u].w;
-      }
+    if (p + 2 < nseg) {
+      stage(p + 1);  // buffer (p + 1) & 1 was last read in step p - 1, before its closing barrier
+      scan_wait<1>();
+    } else {
+      scan_wait<0>();
     }
+    __syncthreads();  // staged buffer p & 1 and the entry tile visible to all threads
+    const float* Mb = smem + (p & 1) * (C::M_FLOATS + C::B_FLOATS);
+    const float* Bb = Mb + C::M_FLOATS;
     float acc[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const float4 x = *reinterpret_cast<const float4*>(fr + (size_t)(4 * rgp + r) * 2 * D + c0 + 4 * cgp);
+      const float4 x = kq == 0 ? *reinterpret_cast<const float4*>(Bb + (rgp + C::RGS * r) * CT + 4 * cgp)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
       acc[r][0] = x.x;
       acc[r][1] = x.y;
       acc[r][2] = x.z;
       acc[r][3] = x.w;
     }
-    __syncthreads();
 #pragma unroll 4
-    for (int l = 0; l < D; ++l) {
+    for (int l = kq * LK; l < (kq + 1) * LK; ++l) {
       const float4 s4 = *reinterpret_cast<const float4*>(&Sin[l * CT + 4 * cgp]);
       const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const float m = Ms[(4 * rgp + r) * (D + 1) + l];
+        const float m = Mb[(rgp + C::RGS * r) * MS + l];
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = __fmaf_rn(m, sv[c], acc[r][c]);
       }
     }
-    __syncthreads();  // all reads of Sin done
+    if (kq > 0) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4*>(Part + (kq - 1) * C::B_FLOATS + (rgp + C::RGS * r) * CT + 4 * cgp) =
+            make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    }
+    __syncthreads();  // all reads of the entry tile and of buffer p & 1 done; partial sums visible
+    if (kq > 0) continue;
     float* dst = entry_i + ((size_t)(p + 1) * a.H + h) * head_elems;
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
+      const int row = rgp + C::RGS * r;
+#pragma unroll
+      for (int k = 1; k < C::KS; ++k) {
+        const float4 y = *reinterpret_cast<const float4*>(Part + (k - 1) * C::B_FLOATS + row * CT + 4 * cgp);
+        acc[r][0] = __fadd_rn(acc[r][0], y.x);
+        acc[r][1] = __fadd_rn(acc[r][1], y.y);
+        acc[r][2] = __fadd_rn(acc[r][2], y.z);
+        acc[r][3] = __fadd_rn(acc[r][3], y.w);
+      }
       const float4 x = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      *reinterpret_cast<float4*>(&Sin[(4 * rgp + r) * CT + 4 * cgp]) = x;
-      *reinterpret_cast<float4*>(dst + (size_t)(4 * rgp + r) * D + c0 + 4 * cgp) = x;
+      *reinterpret_cast<float4*>(&Sin[row * CT + 4 * cgp]) = x;
+      *reinterpret_cast<float4*>(dst + (size_t)row * D + c0 + 4 * cgp) = x;
     }
   }
 }
