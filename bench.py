@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--path", choices=["auto", "varlen", "segmented"], default="segmented")
     ap.add_argument("--segment-len", type=int, default=0,
                     help="tokens per segment of the segmented path (multiple of 64); 0 = the shortest segment whose "
-                         "fragment phase (2 CTAs per head and segment but the last) fits one wave on this GPU")
+                         "output phase (one CTA per head and segment) fits one wave on this GPU")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -192,8 +192,9 @@ def run_ours(args):
     pargs = (q, k, v, g, beta, cu, T, pool, slot, out)
     seg_len = args.segment_len
     if seg_len <= 0:
-        # fragment phase: 2 x H CTAs for each segment but the last, one CTA per SM
-        segments = props.multi_processor_count // (2 * H) + 1
+        # output phase: H CTAs per segment, one CTA per SM (the fragment phase, 2 x H CTAs per segment but
+        # the last, then takes two waves; the scan grows by one short step per segment)
+        segments = max(1, props.multi_processor_count // H)
         per_segment = -(-T // segments)
         seg_len = -(-per_segment // 64) * 64
     ws = torch.empty(max(kda.kda_segmented_workspace_size(*pargs, seg_len), 256), dtype=torch.uint8, device=dev)

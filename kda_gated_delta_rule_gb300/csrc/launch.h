@@ -177,6 +177,8 @@ cudaError_t launch_prefill_seq(const PrefillArgs& a, cudaStream_t s);
 // Segmented path phases.
 cudaError_t launch_seg_fragments(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_seg_scan(const PrefillArgs& a, cudaStream_t s);
+// the same scan on the tensor cores (d = 128)
+cudaError_t launch_seg_scan_tc(const PrefillArgs& a, cudaStream_t s);
 cudaError_t launch_seg_outputs(const PrefillArgs& a, cudaStream_t s);
 
 // Tensor-core chunked path (bf16 inputs, d = 128).

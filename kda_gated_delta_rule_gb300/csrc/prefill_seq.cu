@@ -369,7 +369,7 @@ cudaError_t launch_seg_scan(const PrefillArgs& a, cudaStream_t s) {
     case 16: return launch_scan_t<16>(a, s);
     case 32: return launch_scan_t<32>(a, s);
     case 64: return launch_scan_t<64>(a, s);
-    case 128: return launch_scan_t<128>(a, s);
+    case 128: return launch_seg_scan_tc(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
