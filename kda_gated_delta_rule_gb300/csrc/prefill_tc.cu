@@ -680,19 +680,32 @@ constexpr uint32_t COL_UTHI = 448;  // U^T as the A operand: 32 columns each
 constexpr uint32_t COL_UTLO = 480;
 
 constexpr uint32_t CS_GAMMA = 2 * REC_STAGE;      // gamma [2][128] fp32
-constexpr uint32_t CS_BAR = CS_GAMMA + 1024;      // full[2], ws, state, out[2]
-constexpr uint32_t CS_SLOT = CS_BAR + 64;
+constexpr uint32_t CS_BAR = CS_GAMMA + 1024;      // full[2], ws, state, out[2], e1, e2, o1
+constexpr uint32_t CS_SLOT = CS_BAR + 128;
 constexpr uint32_t CS_BYTES = CS_SLOT + 16 + 1024;
-constexpr int CHAIN_NT = 256;
+constexpr int CHAIN_MATH = 256;                   // warps 0-7: the state and output arithmetic
+constexpr int CHAIN_ISS_A = CHAIN_MATH;           // lane 0 of warp 8: issues (W S)^T and the state update
+constexpr int CHAIN_ISS_B = CHAIN_MATH + 32;      // lane 0 of warp 9: issues the two output products
+constexpr int CHAIN_ISS_C = CHAIN_MATH + 64;      // lane 0 of warp 10: fragment mode, third of (W S)^T
+constexpr int CHAIN_NT = CHAIN_MATH + 96;
+constexpr int BAR_MATH = 1;                       // named barrier of the math warps
+static_assert(CS_BYTES <= 232448, "chain shared memory");
 
 enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2 };
 
-// Two warpgroups: thread (value channel c = TMEM lane, warpgroup wg) handles half of every TMEM row it
+// Two math warpgroups: thread (value channel c = TMEM lane, warpgroup wg) handles half of every TMEM row it
 // touches.  Per chunk: split the state (E1) -> [W; Q o gamma] S -> U = U~ - W S (E2) -> state update
 // K^T U and output P U; the outputs of a chunk are read back while the next chunk's first product runs.
+// The products are issued by two threads outside the math warps (a tcgen05.mma costs its issuing thread
+// tens of cycles, which a math thread would add to every barrier): A issues (W S)^T and the state update
+// (the dependent chain), B the output products Q^ S (after (W S)^T has completed, so as not to delay it)
+// and P U.  The math warps hand each phase over with an mbarrier arrive (one per warp).  In fragment mode
+// (no outputs) the output accumulators are free: (W S)^T is then issued as its three split products by A, B
+// and C into three accumulators, which E2 adds.
 template <typename Tout, int MODE>
 __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs a, const uint8_t* __restrict__ ws) {
   constexpr bool WANT_O = MODE != MODE_FRAG;
+  constexpr int WS_PARTS = WANT_O ? 1 : 3;  // issuers (and accumulators) of (W S)^T
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   float* sgam = reinterpret_cast<float*>(sm + CS_GAMMA);
@@ -700,6 +713,9 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
   uint64_t* bar_ws = full + 2;
   uint64_t* bar_st = full + 3;
   uint64_t* bar_o = full + 4;
+  uint64_t* rdy_e1 = full + 6;  // the split state of the chunk is in tensor memory (8 warp arrivals)
+  uint64_t* rdy_e2 = full + 7;  // U of the chunk is in tensor memory; the previous outputs are read
+  uint64_t* bar_o1 = full + 8;  // Q^ S of the chunk has completed (its reads of the split state are done)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CS_SLOT);
   const int tid = threadIdx.x, warp = tid >> 5, wg = warp >> 2;
   const int c = tid & 127;  // value channel = TMEM lane
@@ -738,7 +754,10 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
 
   if (warp == 0) tc::tmem_alloc(tslot, 512);
   if (tid == 0) {
-    for (int b = 0; b < 6; ++b) tc::bar_init(full + b, 1);
+    for (int b = 0; b < 6; ++b) tc::bar_init(full + b, b == 2 ? WS_PARTS : 1);
+    tc::bar_init(rdy_e1, CHAIN_MATH / 32);
+    tc::bar_init(rdy_e2, CHAIN_MATH / 32);
+    tc::bar_init(bar_o1, 1);
     tc::bar_fence_init();
   }
   tc::fence_before_sync();
@@ -752,36 +771,30 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     return ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * REC_BYTES;
   };
   int issued = 0;  // chunks whose stage copies have been issued (thread 0's view)
+  // the chunk's record tiles into stage cc & 1 (same offsets as in the record); fragment mode has no
+  // outputs and copies only the W rows of the stacked [W; Q o gamma] tile and (K o exp(G_C - G))^T
   auto issue = [&](int cc) {
     const int st = cc & 1;
     const uint8_t* rec = rec_of(cc);
-    tc::bar_arrive_expect_tx(full + st, REC_STAGE + 512);
-    tc::bulk_g2s(sm + st * REC_STAGE, rec, REC_STAGE, full + st);
+    uint8_t* stage = sm + st * REC_STAGE;
+    if (WANT_O) {
+      tc::bar_arrive_expect_tx(full + st, REC_STAGE + 512);
+      tc::bulk_g2s(stage, rec, REC_STAGE, full + st);
+    } else {
+      tc::bar_arrive_expect_tx(full + st, 4 * 8192 + (REC_STAGE - REC_KHHI) + 512);
+#pragma unroll
+      for (int kb = 0; kb < 2; ++kb) {  // W: rows 0..63 = the first 8 KB of each 16 KB K-block
+        tc::bulk_g2s(stage + REC_B1HI + kb * 16384, rec + REC_B1HI + kb * 16384, 8192, full + st);
+        tc::bulk_g2s(stage + REC_B1LO + kb * 16384, rec + REC_B1LO + kb * 16384, 8192, full + st);
+      }
+      tc::bulk_g2s(stage + REC_KHHI, rec + REC_KHHI, REC_STAGE - REC_KHHI, full + st);
+    }
     tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
     issued = cc + 1;
   };
   if (tid == 0) {
     if (nch > 0) issue(0);
     if (nch > 1) issue(1);
-  }
-
-  // initial state, transposed into tensor memory: lane c holds column c of S
-  {
-    const float* src = nullptr;
-    if (MODE == MODE_PLAIN && !a.init_zero) src = a.pool + ((size_t)slot * a.H + h) * head_elems;
-    if (MODE == MODE_SEGOUT) src = a.entry + (((size_t)i * a.P + p) * a.H + h) * head_elems;
-#pragma unroll 1
-    for (int jb = 0; jb < 2; ++jb) {
-      const int j0 = 64 * wg + 32 * jb;
-      float v[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = j0 + e;
-        v[e] = src ? src[(size_t)j * D + c] : ((MODE == MODE_FRAG && tile == 1 && j == c) ? 1.f : 0.f);
-      }
-      tc::tmem_st32f(trow + COL_S + j0, v);
-    }
-    tc::tmem_wait_st();
   }
 
   // state S^T -> global [j][c] rows j in this thread's half (dst points at column c)
@@ -823,57 +836,143 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     for (int e = 0; e < 32; ++e)
       if (32 * wg + e < nv) out[(size_t)(32 * wg + e) * a.H * D] = from_f32<Tout>(o[e]);
   };
+  // the math warps' agreement on `ok` at a phase boundary (a named barrier over the math warps only)
+  auto math_all = [&](bool p) { return !tc::named_bar_or(BAR_MATH, CHAIN_MATH, !p); };
+  // one arrival per math warp on a hand-over barrier, after the warp's tensor-memory work of the phase
+  auto hand_over = [&](uint64_t* bar) {
+    tc::fence_before_sync();
+    __syncwarp();
+    if ((tid & 31) == 0) tc::bar_arrive(bar);
+  };
 
-  const bool zero_u = (MODE == MODE_FRAG && tile == 1);  // transition columns: V = 0
   bool ok = true;
   int cc = 0;
-#pragma unroll 1
-  for (; cc < nch; ++cc) {
-    const int st = cc & 1;
-    const uint32_t par = (uint32_t)cc & 1u;
-    float ut[32];
+  if (tid < CHAIN_MATH) {
+    // initial state, transposed into tensor memory: lane c holds column c of S
     {
-      const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D + (c ^ ((e & 7) << 2))];
-    }
-    bool w_ok = tc::bar_wait(full + st, (uint32_t)(cc >> 1) & 1u);
-    if (cc > 0) w_ok = w_ok && tc::bar_wait(bar_st, par ^ 1u);  // the previous chunk's state update
-    ok = __syncthreads_and(w_ok);
-    if (!ok) break;
-    tc::fence_after_sync();
-    if (cc > 0) {
-      snapshot(cc - 1);
-      if (!WANT_O && tid == 0 && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
-    }
-    // E1: split the state into the MMA operand, then apply this chunk's decay to the fp32 copy
+      const float* src = nullptr;
+      if (MODE == MODE_PLAIN && !a.init_zero) src = a.pool + ((size_t)slot * a.H + h) * head_elems;
+      if (MODE == MODE_SEGOUT) src = a.entry + (((size_t)i * a.P + p) * a.H + h) * head_elems;
 #pragma unroll 1
-    for (int jb = 0; jb < 2; ++jb) {
-      const int j0 = 64 * wg + 32 * jb;
-      float s[32];
-      tc::tmem_ld32(trow + COL_S + j0, s);
-      uint32_t hi[16], lo[16];
+      for (int jb = 0; jb < 2; ++jb) {
+        const int j0 = 64 * wg + 32 * jb;
+        float v[32];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) split_pair(s[2 * e], s[2 * e + 1], hi[e], lo[e]);
-      tc::tmem_st16(trow + COL_STHI + j0 / 2, hi);
-      tc::tmem_st16(trow + COL_STLO + j0 / 2, lo);
-      const float* gm = sgam + 128 * st + j0;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) s[e] *= gm[e];
-      tc::tmem_st32f(trow + COL_S + j0, s);
+        for (int e = 0; e < 32; ++e) {
+          const int j = j0 + e;
+          v[e] = src ? src[(size_t)j * D + c] : ((MODE == MODE_FRAG && tile == 1 && j == c) ? 1.f : 0.f);
+        }
+        tc::tmem_st32f(trow + COL_S + j0, v);
+      }
+      tc::tmem_wait_st();
     }
-    tc::tmem_wait_st();
-    tc::fence_before_sync();
-    __syncthreads();
-    const uint32_t sbase = tc::smem_u32(sm + st * REC_STAGE);
-    // shared-memory descriptors of this stage's tiles: a descriptor of base + off is the base descriptor
-    // + off / 16 (start-address field), so each K step is a constant offset
-    const uint64_t dstage = tc::sdesc(sbase);
-    if (tid == 0) {
-      tc::fence_after_sync();
-      // (W S)^T = S^T W^T, then (Q o gamma S)^T into this chunk's output accumulator
+    const bool zero_u = (MODE == MODE_FRAG && tile == 1);  // transition columns: V = 0
+#pragma unroll 1
+    for (; cc < nch; ++cc) {
+      const int st = cc & 1;
+      const uint32_t par = (uint32_t)cc & 1u;
+      float ut[32];
+      {
+        const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D;
 #pragma unroll
-      for (int part = 0; part < 3; ++part) {
+        for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D + (c ^ ((e & 7) << 2))];
+      }
+      bool w_ok = tc::bar_wait(full + st, (uint32_t)(cc >> 1) & 1u);
+      if (cc > 0) w_ok = w_ok && tc::bar_wait(bar_st, par ^ 1u);  // the previous chunk's state update
+      if (WANT_O && cc > 0) w_ok = w_ok && tc::bar_wait(bar_o1, par ^ 1u);  // its Q^ S: the split state is free
+      ok = math_all(w_ok);
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (cc > 0) {
+        snapshot(cc - 1);
+        if (!WANT_O && tid == 0 && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
+      }
+      // E1: split the state into the MMA operand and hand it over; then apply this chunk's decay to the fp32
+      // copy (needed only by the state update, after E2)
+      {
+        const int j0 = 64 * wg;
+        float s[64];
+        tc::tmem_ld64(trow + COL_S + j0, s);
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) split_pair(s[32 * jb + 2 * e], s[32 * jb + 2 * e + 1], hi[e], lo[e]);
+          tc::tmem_st16(trow + COL_STHI + j0 / 2 + 16 * jb, hi);
+          tc::tmem_st16(trow + COL_STLO + j0 / 2 + 16 * jb, lo);
+        }
+        tc::tmem_wait_st();
+        hand_over(rdy_e1);
+        const float* gm = sgam + 128 * st + j0;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) s[e] *= gm[e];
+        tc::tmem_st32f(trow + COL_S + j0, s);
+        tc::tmem_st32f(trow + COL_S + j0 + 32, s + 32);
+      }
+      if (WANT_O && cc > 0) {  // the previous chunk's outputs, while this chunk's products run
+        ok = __all_sync(0xffffffffu, tc::bar_wait(bar_o + (st ^ 1), (uint32_t)((cc - 1) >> 1) & 1u));
+        tc::fence_after_sync();
+        if (ok) emit(cc - 1);
+        if (tid == 0 && ok && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
+      }
+      ok = math_all(ok && tc::bar_wait(bar_ws, par));
+      if (!ok) break;
+      tc::fence_after_sync();
+      // E2: U = U~ - W S for this thread's 32 tokens, split into the A operand of the next two products
+      {
+        float w[32];
+        tc::tmem_ld32(trow + COL_WS + 32 * wg, w);
+        if (WS_PARTS == 3) {  // the other two split products, in the (unused) output accumulators
+          float w1[32], w2[32];
+          tc::tmem_ld32(trow + COL_O + 32 * wg, w1);
+          tc::tmem_ld32(trow + COL_O + 64 + 32 * wg, w2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = (w[e] + w1[e]) + w2[e];
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
+        tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
+        tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
+      }
+      tc::tmem_wait_st();
+      hand_over(rdy_e2);
+    }
+    if (ok && nch > 0) {  // drain: the last chunk's state update and outputs
+      const int last = nch - 1;
+      bool w_ok = tc::bar_wait(bar_st, (uint32_t)last & 1u);
+      if (WANT_O) w_ok = w_ok && tc::bar_wait(bar_o + (last & 1), (uint32_t)(last >> 1) & 1u);
+      ok = math_all(w_ok);
+      if (ok) {
+        tc::fence_after_sync();
+        snapshot(last);
+        if (WANT_O) emit(last);
+      }
+    }
+    if (ok) {
+      if (MODE == MODE_FRAG)
+        store_state(a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2 + (size_t)tile * D + c, 2 * D);
+      else if (writes_pool)
+        store_state(a.pool + ((size_t)slot * a.H + h) * head_elems + c, D);
+      if (tid == 0 && tile == 0) add_work(a.status, (int32_t)(t1 - t0));
+    } else if (tid == 0) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      // wait (bounded) for the copies still in flight into this CTA's shared memory before it is released
+      for (int q = cc; q < issued; ++q) tc::bar_wait(full + (q & 1), (uint32_t)(q >> 1) & 1u);
+    }
+  }
+  else if (tid == CHAIN_ISS_A) {  // (W S)^T and the state update of every chunk, in order
+    int k = 0;
+#pragma unroll 1
+    for (; k < nch; ++k) {
+      const int st = k & 1;
+      if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u)) break;
+      tc::fence_after_sync();
+      // shared-memory descriptors of this stage's tiles: a descriptor of base + off is the base descriptor
+      // + off / 16 (start-address field), so each K step is a constant offset
+      const uint64_t dstage = tc::sdesc(tc::smem_u32(sm + st * REC_STAGE));
+#pragma unroll
+      for (int part = 0; part < (WS_PARTS == 3 ? 1 : 3); ++part) {  // (W S)^T = S^T W^T
         const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
         const uint64_t bd = dstage + ((part == 1 ? REC_B1LO : REC_B1HI) >> 4);
 #pragma unroll
@@ -882,41 +981,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
                      tc::idesc_bf16(128, 64), (part | ks) != 0);
       }
       tc::commit(bar_ws);
-      if (WANT_O) {
-#pragma unroll
-        for (int part = 0; part < 3; ++part) {
-          const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
-          const uint64_t bd = dstage + (((part == 1 ? REC_B1LO : REC_B1HI) + 64u * 128u) >> 4);  // rows 64..127
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4),
-                       tc::idesc_bf16(128, 64), (part | ks) != 0);
-        }
-      }
-    }
-    if (WANT_O && cc > 0) {  // the previous chunk's outputs, while this chunk's products run
-      ok = tc::bar_wait(bar_o + (st ^ 1), (uint32_t)((cc - 1) >> 1) & 1u);
-      tc::fence_after_sync();
-      if (ok) emit(cc - 1);
-      if (tid == 0 && ok && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
-    }
-    ok = __syncthreads_and(ok && tc::bar_wait(bar_ws, par));
-    if (!ok) break;
-    tc::fence_after_sync();
-    // E2: U = U~ - W S for this thread's 32 tokens, split into the A operand of the next two products
-    {
-      float w[32];
-      tc::tmem_ld32(trow + COL_WS + 32 * wg, w);
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
-      tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
-      tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
-    }
-    tc::tmem_wait_st();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
+      if (!tc::bar_wait(rdy_e2, (uint32_t)k & 1u)) break;
       tc::fence_after_sync();
 #pragma unroll
       for (int part = 0; part < 3; ++part) {  // state: S^T += U^T (K o exp(G_C - G))
@@ -926,41 +991,61 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         for (int ks = 0; ks < 4; ++ks) tc::mma_ts(tm + COL_S, acol + ks * 8, kd + 2u * ks, tc::idesc_bf16(128, 128), 1);
       }
       tc::commit(bar_st);
-      if (WANT_O) {
-#pragma unroll
-        for (int part = 0; part < 3; ++part) {  // outputs: O^T += U^T P^T
-          const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
-          const uint64_t pd = dstage + ((part == 1 ? REC_PLO : REC_PHI) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, pd + 2u * ks, tc::idesc_bf16(128, 64), 1);
-        }
-        tc::commit(bar_o + st);
-      }
     }
-  }
-
-  if (ok && nch > 0) {  // drain: the last chunk's state update and outputs
-    const int last = nch - 1;
-    bool w_ok = tc::bar_wait(bar_st, (uint32_t)last & 1u);
-    if (WANT_O) w_ok = w_ok && tc::bar_wait(bar_o + (last & 1), (uint32_t)(last >> 1) & 1u);
-    ok = __syncthreads_and(w_ok);
-    if (ok) {
+    if (k < nch) flag_status(a.status, KDA_DEV_TIMEOUT);
+  } else if (WANT_O && tid == CHAIN_ISS_B) {  // the output products of every chunk, in order
+    int k = 0;
+#pragma unroll 1
+    for (; k < nch; ++k) {
+      const int st = k & 1;
+      // (W S)^T of the chunk first: Q^ S goes to the tensor core after it, not interleaved with it
+      if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u) ||
+          !tc::bar_wait(bar_ws, (uint32_t)k & 1u))
+        break;
       tc::fence_after_sync();
-      snapshot(last);
-      if (WANT_O) emit(last);
+      const uint64_t dstage = tc::sdesc(tc::smem_u32(sm + st * REC_STAGE));
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {  // (Q o gamma S)^T into this chunk's output accumulator
+        const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
+        const uint64_t bd = dstage + (((part == 1 ? REC_B1LO : REC_B1HI) + 64u * 128u) >> 4);  // rows 64..127
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4),
+                     tc::idesc_bf16(128, 64), (part | ks) != 0);
+      }
+      tc::commit(bar_o1);
+      if (!tc::bar_wait(rdy_e2, (uint32_t)k & 1u)) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {  // outputs: O^T += U^T P^T
+        const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
+        const uint64_t pd = dstage + ((part == 1 ? REC_PLO : REC_PHI) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, pd + 2u * ks, tc::idesc_bf16(128, 64), 1);
+      }
+      tc::commit(bar_o + st);
     }
-  }
-  if (ok) {
-    if (MODE == MODE_FRAG)
-      store_state(a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2 + (size_t)tile * D + c, 2 * D);
-    else if (writes_pool)
-      store_state(a.pool + ((size_t)slot * a.H + h) * head_elems + c, D);
-    if (tid == 0 && tile == 0) add_work(a.status, (int32_t)(t1 - t0));
-  } else if (tid == 0) {
-    flag_status(a.status, KDA_DEV_TIMEOUT);
-    // wait (bounded) for the copies still in flight into this CTA's shared memory before it is released
-    for (int q = cc; q < issued; ++q) tc::bar_wait(full + (q & 1), (uint32_t)(q >> 1) & 1u);
+    if (k < nch) flag_status(a.status, KDA_DEV_TIMEOUT);
+  } else if (WS_PARTS == 3 && (tid == CHAIN_ISS_B || tid == CHAIN_ISS_C)) {
+    // fragment mode: (hi, lo) (B) or (lo, hi) (C) of (W S)^T, into an output accumulator
+    const int part = tid == CHAIN_ISS_B ? 1 : 2;
+    int k = 0;
+#pragma unroll 1
+    for (; k < nch; ++k) {
+      const int st = k & 1;
+      if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u)) break;
+      tc::fence_after_sync();
+      const uint64_t dstage = tc::sdesc(tc::smem_u32(sm + st * REC_STAGE));
+      const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
+      const uint64_t bd = dstage + ((part == 1 ? REC_B1LO : REC_B1HI) >> 4);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_ts(tm + COL_O + 64u * (uint32_t)(part - 1), acol + ks * 8,
+                   bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4), tc::idesc_bf16(128, 64), ks != 0);
+      tc::commit(bar_ws);
+    }
+    if (k < nch) flag_status(a.status, KDA_DEV_TIMEOUT);
   }
   tc::fence_before_sync();
   __syncthreads();
