@@ -314,21 +314,59 @@ def run_ours(args):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb, hs0))
     d2h = ho.numel() * ho.element_size() + hsf.numel() * hsf.element_size()
 
-    def e2e_step():
-        q.view(torch.int16).copy_(hq.view(torch.int16), non_blocking=True)
-        k.view(torch.int16).copy_(hk.view(torch.int16), non_blocking=True)
-        v.view(torch.int16).copy_(hv.view(torch.int16), non_blocking=True)
-        g.copy_(hg, non_blocking=True)
-        beta.copy_(hb, non_blocking=True)
-        ckpt.copy_(hs0, non_blocking=True)
-        step()
-        ho.copy_(out, non_blocking=True)
-        hsf.copy_(pool, non_blocking=True)
-
+    # Steps are pipelined over three streams (host->device, compute, device->host) with double-buffered device
+    # inputs and outputs, so step k+1's inputs upload while step k computes; every step still carries its own
+    # copies.  L2 is flushed on the compute stream before each step's kernels.
+    sets = []
     for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(time_calls(e2e_step, max(5, min(args.steps, 20))))
+        sets.append({"x": [torch.empty_like(t) for t in (q, k, v, g, beta)], "ckpt": torch.empty_like(ckpt),
+                     "pool": torch.empty_like(pool), "out": torch.empty_like(out)})
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_run(n):
+        ev_in, ev_cmp, ev_out = ([torch.cuda.Event() for _ in range(n)] for _ in range(3))
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t_start.record(s_in)
+        for i in range(n):
+            st = sets[i % 2]
+            dx = st["x"]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_cmp[i - 2])  # this set's inputs were consumed by step i - 2
+                for dst, src in zip(dx, (hq, hk, hv, hg, hb)):
+                    if dst.dtype == torch.bfloat16:  # host bf16 inputs are held as raw 16-bit words
+                        dst.view(torch.int16).copy_(src.view(torch.int16), non_blocking=True)
+                    else:
+                        dst.copy_(src, non_blocking=True)
+                st["ckpt"].copy_(hs0, non_blocking=True)
+                ev_in[i].record(s_in)
+            with torch.cuda.stream(s_cmp):
+                s_cmp.wait_event(ev_in[i])
+                if i >= 2:
+                    s_cmp.wait_event(ev_out[i - 2])  # this set's outputs were read back
+                flush.zero_()
+                kda.kda_state_copy(st["ckpt"], slot, st["pool"], slot)
+                eargs = (*dx, cu, T, st["pool"], slot, st["out"])
+                if path == "varlen":
+                    kda.kda_prefill_varlen(*eargs, workspace=ws_var, dev_status=status)
+                else:
+                    kda.kda_prefill_segmented(*eargs, seg_len, ws, dev_status=status)
+                ev_cmp[i].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[i])
+                ho.copy_(st["out"], non_blocking=True)
+                hsf.copy_(st["pool"], non_blocking=True)
+                ev_out[i].record(s_out)
+        t_end.record(s_out)
+        torch.cuda.synchronize()
+        return t_start.elapsed_time(t_end) / n
+
+    e2e_run(3)
+    e2e_steps = max(5, min(args.steps, 20))
+    e2e_ms = e2e_run(e2e_steps)
+    if not torch.equal(ho.view(torch.int16), out.view(torch.int16).cpu()):  # same inputs, same kernels: same bits
+        raise RuntimeError("the end-to-end outputs differ from the device-resident run's")
     e2e_value = whole_job_value(T, world, max_over_ranks(e2e_ms, world, dev) / 1e3)
 
     # ---- decode / verify / fold on the batched workload
@@ -363,7 +401,9 @@ def run_ours(args):
         },
         "roofline": roofline,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s/layer", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "pipeline": "host->device, compute and device->host streams, two device buffer sets; L2 flushed "
+                            "on the compute stream before each step"},
         "gpu_launches": args.steps * kernels_per_step[path],
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
