@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       tc::bar_init(&full_s[i], 1);
       tc::bar_init(&full_w[i], MT / TEAMS);  // every thread of the team that computed the item
       tc::bar_init(&empty_w[i], ST);
-      tc::bar_init(&mma_bar[i], 2);  // one commit per issuing thread
+      tc::bar_init(&mma_bar[i], 4);  // one commit per issuing thread
     }
     for (int i = 0; i < 2 * TEAMS; ++i) tc::bar_init(&full_r[i], 1 + W);  // TMA issuer + a cp.async per beta
     tc::bar_fence_init();
@@ -525,15 +525,19 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       tc::fence_after_sync();
       // accumulator column t = S0 hi (first accumulator) or S0 lo (second) against Qh hi of token t, column
       // WP + t against its lo part
-      float d[2 * WP], d2[2 * WP];
-      tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC, d);
-      tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC2, d2);
-      if constexpr (WP > 8) {
-        tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC + 16, d + 16);
-        tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC2 + 16, d2 + 16);
-      }
+      // (four accumulators: S0 hi / lo x the two halves of the K range, 32 columns apart)
+      float d[2 * WP];
 #pragma unroll
-      for (int e = 0; e < 2 * WP; ++e) d[e] += d2[e];
+      for (int q = 0; q < 2 * WP; q += 16) {
+        tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + COL_ACC + q, d + q);
+#pragma unroll
+        for (int a = 1; a < 4; ++a) {  // the other three partial products, in a fixed order
+          float d2[16];
+          tc::tmem_ld16(tm + tlane + (m & 1) * BUF_COLS + ((a & 1) ? COL_ACC2 : COL_ACC) + 32 * (a >> 1) + q, d2);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) d[q + e] += d2[e];
+        }
+      }
       const float* oh = reinterpret_cast<const float*>(sm + L::OH) + (m & 1) * WP * D;
       if (ok && done) {
         constexpr int TH = WP / 2;
@@ -582,20 +586,24 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
       if (sidx == 0 && n + STAGES < cnt) issue_state(n + STAGES, slot_ahead);
       if (n >= 1) epilogue(n - 1, ok_prev);  // frees item n-1's Qh / Oh buffers before waiting on item n's
       ok_prev = slot_n >= 0 && slot_n < num_slots;
-      if (sidx == 0 || sidx == 32) {
+      if (sidx < 128 && (sidx & 31) == 0) {
         if (!tc::bar_wait(&full_w[n & 1], (n >> 1) & 1)) flag_status(status, KDA_DEV_TIMEOUT);
         tc::fence_after_sync();
-        // D = S0^T [Qh hi; Qh lo]^T (128 value columns x 2WP), 8 K-steps: S0 hi by thread 0 of warp 8 into
-        // the first accumulator, S0 lo by thread 0 of warp 9 into the second, issued side by side.  A
-        // descriptor of base + off equals the base descriptor + off/16 (the start-address field).
-        const int part = sidx == 32;
+        // D = S0^T [Qh hi; Qh lo]^T (128 value columns x 2WP), 8 K-steps, from four threads side by side:
+        // thread 0 of warp 8 + 2 kh + part issues S0 hi (part 0) or lo (part 1) over K-steps 4 kh .. 4 kh + 3
+        // into an accumulator of its own (a chain of dependent MMAs advances ~90 cycles a step, so four
+        // 4-deep chains finish well before two 8-deep ones).  A descriptor of base + off equals the base
+        // descriptor + off/16 (the start-address field).
+        const int part = (sidx >> 5) & 1, kh = sidx >> 6;
         const uint64_t bdesc = tc::sdesc(tc::smem_u32(sm + L::BT + (n & 1) * L::B_TILE));
         const uint32_t buf = tm + (n & 1) * BUF_COLS;
         constexpr uint32_t idesc = tc::idesc_bf16(128, L::B_ROWS);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc::mma_ts(buf + (part ? COL_ACC2 : COL_ACC), buf + (part ? COL_ALO : COL_AHI) + 8 * ks,
-                     bdesc + (((ks >> 2) * L::B_BLOCK + (ks & 3) * 32u) >> 4), idesc, ks != 0);
+        for (int kk = 0; kk < 4; ++kk) {
+          const int ks = 4 * kh + kk;
+          tc::mma_ts(buf + (part ? COL_ACC2 : COL_ACC) + 32u * kh, buf + (part ? COL_ALO : COL_AHI) + 8 * ks,
+                     bdesc + (((ks >> 2) * L::B_BLOCK + (ks & 3) * 32u) >> 4), idesc, kk != 0);
+        }
         tc::commit(&mma_bar[n & 1]);
       }
     }
