@@ -79,8 +79,10 @@ __device__ __forceinline__ void unpack8(uint4 r, float* x) {
 constexpr uint32_t PS_XHI = 0;          // X [128][128] bf16: (K; Q) o exp(G_t - G_ref), hi then lo
 constexpr uint32_t PS_XLO = 32768;
 // once the Gram product has completed, the X region is reused for:
-constexpr uint32_t PS_A = 0;            // A [64][64] fp32 (beta folded in, strictly lower)
-constexpr uint32_t PS_T = 16384;        // T = (I + A)^-1 [64][64] fp32 (upper blocks: scratch)
+constexpr int LT = 68;                  // row stride (floats) of A and T: 8 consecutive rows, 8 bank groups
+constexpr uint32_t PS_A = 0;            // A [64][LT] fp32 (beta folded in, strictly lower)
+constexpr uint32_t PS_T = 64 * LT * 4;  // T = (I + A)^-1 [64][LT] fp32 (upper blocks: scratch); its last 2 KB
+                                        // overlap T diag(beta), which is written from registers after T is read
 constexpr uint32_t PS_TBHI = 32768;     // T diag(beta) [64 t][K = 64 s] bf16, hi then lo
 constexpr uint32_t PS_TBLO = 40960;
 constexpr uint32_t PS_VT = 49152;       // V^T [128 c][K = 64 s] bf16
@@ -468,7 +470,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
           r.y = s0c + 1 < t ? bt * v[i + 1] : 0.f;
           r.z = s0c + 2 < t ? bt * v[i + 2] : 0.f;
           r.w = s0c + 3 < t ? bt * v[i + 3] : 0.f;
-          *reinterpret_cast<float4*>(sA + t * 64 + s0c) = r;
+          *reinterpret_cast<float4*>(sA + t * LT + s0c) = r;
         }
       } else {
         const int t = row - 64;
@@ -537,37 +539,53 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       for (int r = 0; r < 16; ++r) {
         float acc = 0.f;
 #pragma unroll
-        for (int u = 0; u < r; ++u) acc = fmaf(sA[(16 * b + r) * 64 + 16 * b + u], x[u], acc);
+        for (int u = 0; u < r; ++u) acc = fmaf(sA[(16 * b + r) * LT + 16 * b + u], x[u], acc);
         x[r] = r == cc ? 1.f : (r < cc ? 0.f : -acc);
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) sT[(16 * b + r) * 64 + 16 * b + cc] = x[r];
+      for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LT + 16 * b + cc] = x[r];
     }
     __syncthreads();
     // off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  First
     // M_ik = T_ii A_ik for all six pairs k < i at once (kept in the unused upper block (k, i)), then block
-    // row by block row T_ij = -sum_k M_ik T_kj
-    for (int o = tid; o < 6 * 256; o += PREP_NT) {
-      const int pr = o >> 8, r = (o >> 4) & 15, c = o & 15;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+    // row by block row T_ij = -sum_k M_ik T_kj.  Each thread owns a 1 x 4 strip (row r, columns 4 cg ..):
+    // per step one conflict-free scalar load (a warp's eight rows sit in eight bank groups) and one
+    // 16-byte load feed four FMAs.  T_ii is stored with its zero upper triangle, so the sums run over all 16.
+    if (tid < 6 * 64) {
+      const int pr = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
       const int bi = pr == 0 ? 1 : (pr < 3 ? 2 : 3);
       const int bk = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);
-      float acc = 0.f;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int u = 0; u < 16; ++u)
-        if (u <= r) acc = fmaf(sT[(16 * bi + r) * 64 + 16 * bi + u], sA[(16 * bi + u) * 64 + 16 * bk + c], acc);
-      sT[(16 * bk + r) * 64 + 16 * bi + c] = acc;
+      for (int u = 0; u < 16; ++u) {
+        const float tv = sT[(16 * bi + r) * LT + 16 * bi + u];
+        const float4 a4 = *reinterpret_cast<const float4*>(sA + (16 * bi + u) * LT + 16 * bk + 4 * cg);
+        acc[0] = fmaf(tv, a4.x, acc[0]);
+        acc[1] = fmaf(tv, a4.y, acc[1]);
+        acc[2] = fmaf(tv, a4.z, acc[2]);
+        acc[3] = fmaf(tv, a4.w, acc[3]);
+      }
+      *reinterpret_cast<float4*>(sT + (16 * bk + r) * LT + 16 * bi + 4 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
     __syncthreads();
 #pragma unroll 1
     for (int bi = 1; bi < 4; ++bi) {
-      for (int o = tid; o < bi * 256; o += PREP_NT) {
-        const int bj = o >> 8, r = (o >> 4) & 15, c = o & 15;
-        float acc = 0.f;
-        for (int bk = bj; bk < bi; ++bk)
+      if (tid < bi * 64) {
+        const int bj = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int bk = bj; bk < bi; ++bk) {
 #pragma unroll
-          for (int u = 0; u < 16; ++u)
-            acc = fmaf(sT[(16 * bk + r) * 64 + 16 * bi + u], sT[(16 * bk + u) * 64 + 16 * bj + c], acc);
-        sT[(16 * bi + r) * 64 + 16 * bj + c] = -acc;
+          for (int u = 0; u < 16; ++u) {
+            const float mv = sT[(16 * bk + r) * LT + 16 * bi + u];
+            const float4 t4 = *reinterpret_cast<const float4*>(sT + (16 * bk + u) * LT + 16 * bj + 4 * cg);
+            acc[0] = fmaf(mv, t4.x, acc[0]);
+            acc[1] = fmaf(mv, t4.y, acc[1]);
+            acc[2] = fmaf(mv, t4.z, acc[2]);
+            acc[3] = fmaf(mv, t4.w, acc[3]);
+          }
+        }
+        *reinterpret_cast<float4*>(sT + (16 * bi + r) * LT + 16 * bj + 4 * cg) =
+            make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
       }
       __syncthreads();
     }
@@ -578,8 +596,10 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int s = 8 * cc + e;
-        v[e] = s <= t ? sT[t * 64 + s] * sbeta[s] : 0.f;
+        v[e] = s <= t ? sT[t * LT + s] * sbeta[s] : 0.f;
       }
+      static_assert(C * 8 == PREP_NT, "one task per thread: every read of T precedes every write");
+      __syncthreads();  // T's last rows and the T diag(beta) tile share memory
       split8_store(sm + PS_TBHI + tc::sw128_chunk(t, cc), sm + PS_TBLO + tc::sw128_chunk(t, cc), v);
     }
     if (tid == DUTY) {  // the task after next (an empty candidate falls back to the full search)
