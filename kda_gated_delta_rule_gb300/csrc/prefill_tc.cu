@@ -706,7 +706,8 @@ constexpr uint32_t CS_BYTES = CS_SLOT + 16 + 1024;
 constexpr int CHAIN_MATH = 256;                   // warps 0-7: the state and output arithmetic
 constexpr int CHAIN_ISS_A = CHAIN_MATH;           // lane 0 of warp 8: issues (W S)^T and the state update
 constexpr int CHAIN_ISS_B = CHAIN_MATH + 32;      // lane 0 of warp 9: issues the two output products
-constexpr int CHAIN_ISS_C = CHAIN_MATH + 64;      // lane 0 of warp 10: fragment mode, third of (W S)^T
+constexpr int CHAIN_ISS_C = CHAIN_MATH + 64;      // lane 0 of warp 10: fragment mode, third of (W S)^T;
+                                                  // output modes, the stage copies
 constexpr int CHAIN_NT = CHAIN_MATH + 96;
 constexpr int BAR_MATH = 1;                       // named barrier of the math warps
 static_assert(CS_BYTES <= 232448, "chain shared memory");
@@ -719,7 +720,9 @@ enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2 };
 // The products are issued by two threads outside the math warps (a tcgen05.mma costs its issuing thread
 // tens of cycles, which a math thread would add to every barrier): A issues (W S)^T and the state update
 // (the dependent chain), B the output products Q^ S (after (W S)^T has completed, so as not to delay it)
-// and P U.  The math warps hand each phase over with an mbarrier arrive (one per warp).  In fragment mode
+// and P U.  The math warps hand each phase over with an mbarrier arrive (one per warp).  The stage copies
+// are issued outside the math warps too (a math thread issuing them held its warp, and so every
+// hand-over, back): by A in fragment mode, while the math warps split the state, by C in output modes.  In fragment mode
 // (no outputs) the output accumulators are free: (W S)^T is then issued as its three split products by A, B
 // and C into three accumulators, which E2 adds.
 template <typename Tout, int MODE>
@@ -790,7 +793,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
   auto rec_of = [&](int cc) -> const uint8_t* {
     return ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * REC_BYTES;
   };
-  int issued = 0;  // chunks whose stage copies have been issued (thread 0's view)
+  int issued = 0;  // chunks whose stage copies have been issued (the copy thread's view)
   // the chunk's record tiles into stage cc & 1 (same offsets as in the record); fragment mode has no
   // outputs and copies only the W rows of the stacked [W; Q o gamma] tile and (K o exp(G_C - G))^T
   auto issue = [&](int cc) {
@@ -812,10 +815,6 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
     issued = cc + 1;
   };
-  if (tid == 0) {
-    if (nch > 0) issue(0);
-    if (nch > 1) issue(1);
-  }
 
   // state S^T -> global [j][c] rows j in this thread's half (dst points at column c)
   auto store_state = [&](float* dst, size_t ld) {
@@ -905,7 +904,6 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       tc::fence_after_sync();
       if (cc > 0) {
         snapshot(cc - 1);
-        if (!WANT_O && tid == 0 && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
       }
       // E1: split the state into the MMA operand and hand it over; then apply this chunk's decay to the fp32
       // copy (needed only by the state update, after E2)
@@ -933,7 +931,6 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         ok = __all_sync(0xffffffffu, tc::bar_wait(bar_o + (st ^ 1), (uint32_t)((cc - 1) >> 1) & 1u));
         tc::fence_after_sync();
         if (ok) emit(cc - 1);
-        if (tid == 0 && ok && cc + 1 < nch) issue(cc + 1);  // stage of chunk cc - 1 is free
       }
       ok = math_all(ok && tc::bar_wait(bar_ws, par));
       if (!ok) break;
@@ -977,15 +974,22 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       if (tid == 0 && tile == 0) add_work(a.status, (int32_t)(t1 - t0));
     } else if (tid == 0) {
       flag_status(a.status, KDA_DEV_TIMEOUT);
-      // wait (bounded) for the copies still in flight into this CTA's shared memory before it is released
-      for (int q = cc; q < issued; ++q) tc::bar_wait(full + (q & 1), (uint32_t)(q >> 1) & 1u);
     }
   }
   else if (tid == CHAIN_ISS_A) {  // (W S)^T and the state update of every chunk, in order
+    if (!WANT_O) {  // fragment mode: the stage copies too
+      if (nch > 0) issue(0);
+      if (nch > 1) issue(1);
+    }
     int k = 0;
 #pragma unroll 1
     for (; k < nch; ++k) {
       const int st = k & 1;
+      if (!WANT_O && k >= 1 && k + 1 < nch) {  // stage k + 1 reuses stage k - 1's buffer, free once its
+                                               // state update has completed
+        if (!tc::bar_wait(bar_st, (uint32_t)(k - 1) & 1u)) break;
+        issue(k + 1);
+      }
       if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u)) break;
       tc::fence_after_sync();
       // shared-memory descriptors of this stage's tiles: a descriptor of base + off is the base descriptor
@@ -1012,7 +1016,11 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       }
       tc::commit(bar_st);
     }
-    if (k < nch) flag_status(a.status, KDA_DEV_TIMEOUT);
+    if (k < nch) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      if (!WANT_O)  // wait (bounded) for the copies still in flight into this CTA's shared memory
+        for (int q = issued >= 2 ? issued - 2 : 0; q < issued; ++q) tc::bar_wait(full + (q & 1), (uint32_t)(q >> 1) & 1u);
+    }
   } else if (WANT_O && tid == CHAIN_ISS_B) {  // the output products of every chunk, in order
     int k = 0;
 #pragma unroll 1
@@ -1047,6 +1055,24 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       tc::commit(bar_o + st);
     }
     if (k < nch) flag_status(a.status, KDA_DEV_TIMEOUT);
+  } else if (WANT_O && tid == CHAIN_ISS_C) {
+    // stage k + 1 reuses stage k - 1's buffer: issued once every read of it is done (chunk k - 1's state
+    // update and output products have completed; its gamma was read before its split was handed over)
+    if (nch > 0) issue(0);
+    if (nch > 1) issue(1);
+    bool cok = true;
+#pragma unroll 1
+    for (int k = 1; k + 1 < nch; ++k) {
+      cok = tc::bar_wait(bar_st, (uint32_t)(k - 1) & 1u) &&
+            tc::bar_wait(bar_o + ((k - 1) & 1), (uint32_t)((k - 1) >> 1) & 1u);
+      if (!cok) break;
+      issue(k + 1);
+    }
+    if (!cok) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      // wait (bounded) for the copies still in flight into this CTA's shared memory before it is released
+      for (int q = issued >= 2 ? issued - 2 : 0; q < issued; ++q) tc::bar_wait(full + (q & 1), (uint32_t)(q >> 1) & 1u);
+    }
   } else if (WS_PARTS == 3 && (tid == CHAIN_ISS_B || tid == CHAIN_ISS_C)) {
     // fragment mode: (hi, lo) (B) or (lo, hi) (C) of (W S)^T, into an output accumulator
     const int part = tid == CHAIN_ISS_B ? 1 : 2;
