@@ -545,7 +545,11 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 #pragma unroll
       for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LT + 16 * b + cc] = x[r];
     }
-    __syncthreads();
+    // The inverse's inner barriers leave out warp 15: it computes nothing here, and its duty thread may
+    // still be waiting for the record stores to read their staging and issuing the next task's loads.  It
+    // rejoins at the last round's barrier, before it reads T.
+    constexpr int INV_THREADS = PREP_NT - 32;
+    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
     // off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  First
     // M_ik = T_ii A_ik for all six pairs k < i at once (kept in the unused upper block (k, i)), then block
     // row by block row T_ij = -sum_k M_ik T_kj.  Each thread owns a 1 x 4 strip (row r, columns 4 cg ..):
@@ -567,7 +571,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       }
       *reinterpret_cast<float4*>(sT + (16 * bk + r) * LT + 16 * bi + 4 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
-    __syncthreads();
+    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
 #pragma unroll 1
     for (int bi = 1; bi < 4; ++bi) {
       if (tid < bi * 64) {
@@ -587,7 +591,11 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
         *reinterpret_cast<float4*>(sT + (16 * bi + r) * LT + 16 * bj + 4 * cg) =
             make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
       }
-      __syncthreads();
+      if (bi < 3) {
+        if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+      } else {
+        __syncthreads();
+      }
     }
     // T diag(beta) as the A operand (lower triangle only)
     for (int task = tid; task < C * 8; task += PREP_NT) {
