@@ -254,18 +254,21 @@ def run_ours(args):
         for _, fn in phase_fns:
             fn()
 
-    def time_steps(n):
+    def time_steps(n, phases=False):
+        # events around every step; with `phases`, also between its kernels (an event between two kernels
+        # holds the second back until the first has finished, so the step times are taken without them)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phase_fns) + 1)] for _ in range(n)]
         for i in range(n):
             flush.zero_()
             evs[i][0].record(stream)
             for j, (_, fn) in enumerate(phase_fns):
                 fn()
-                evs[i][j + 1].record(stream)
+                if phases or j + 1 == len(phase_fns):
+                    evs[i][j + 1].record(stream)
         torch.cuda.synchronize()
         steps_ms = [e[0].elapsed_time(e[-1]) for e in evs]
         per_phase = {name: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
-                     for j, (name, _) in enumerate(phase_fns)}
+                     for j, (name, _) in enumerate(phase_fns)} if phases else None
         return steps_ms, per_phase
 
     for _ in range(max(args.warmup, 3)):
@@ -277,10 +280,12 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    step_ms, phases = time_steps(args.steps)
+    step_ms, _ = time_steps(args.steps)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
+    # per-kernel durations: the same steps again, with an event between their kernels
+    phase_step_ms, phases = time_steps(args.steps, phases=True)
     clk = clocks.stop()
     st = status.cpu().numpy()
     if st[0] != 0 or st[1] == 0:
@@ -289,7 +294,7 @@ def run_ours(args):
     ms_max = max_over_ranks(ms, world, dev)
     value = whole_job_value(T, world, ms_max / 1e3)
 
-    # ---- per-kernel durations: events between the launches of the timed steps (phases above)
+    # ---- per-kernel durations: events between the launches of a second pass of the timed steps (above)
     dominant = max((kname for kname in phases if kname != "kda_state_copy"), key=lambda kname: phases[kname])
     # algorithmic bytes of the prefill: 1540 B per token and head (q, k, v, o bf16; g, beta fp32) plus the
     # initial and final state of every head; achieved = those bytes / the dominant kernel's duration
@@ -302,6 +307,7 @@ def run_ours(args):
                 "peak_source": pk_kind, "algorithmic_bytes": alg_bytes,
                 "kernel_ms": round(phases[dominant], 4),
                 "phase_ms": {kk: round(vv, 4) for kk, vv in phases.items()},
+                "phase_pass_ms_per_step": round(statistics.mean(phase_step_ms), 4),
                 "step_gbs": round(path_gbs, 2), "step_frac": round(path_gbs / pk["hbm_gbs"], 5),
                 "algorithmic_tflops_step": round(T * H * ALG_FLOP_PER_TOKEN_HEAD / (ms_max / 1e3) / 1e12, 3)}
 

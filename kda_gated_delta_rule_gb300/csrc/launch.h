@@ -189,4 +189,23 @@ cudaError_t launch_tc_chain_plain(const PrefillArgs& a, const uint8_t* records, 
 cudaError_t launch_tc_chain_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 
+// Launches `kernel` so that it may be scheduled while the previous kernel in the stream finishes
+// (programmatic dependent launch).  The kernel must call griddepcontrol.wait before it touches global
+// memory, and trigger its own dependents only after that.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace kda

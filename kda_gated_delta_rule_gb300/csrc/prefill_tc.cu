@@ -230,6 +230,8 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + PS_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + PS_SLOT);
   const int tid = threadIdx.x, warp = tid >> 5;
+  tc::pdl_wait();  // the previous kernel in the stream (inputs, and any reader of the record buffer) is done
+  tc::pdl_launch_dependents();
   constexpr int DUTY = PREP_NT - 1;  // issues the bulk stores and the next task's tensor-map loads
   const int total = nchunk * a.H * a.N;
   struct Task {
@@ -753,6 +755,8 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
   const int tile = (MODE == MODE_FRAG) ? (blockIdx.x & 1) : 0;
   const int h = (MODE == MODE_FRAG) ? (blockIdx.x >> 1) : blockIdx.x;
   const int p = blockIdx.y, i = blockIdx.z;
+  tc::pdl_wait();  // the previous kernel in the stream (the records, fragments or entry states) is done
+  tc::pdl_launch_dependents();
 
   const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
   if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
@@ -1112,8 +1116,7 @@ cudaError_t launch_chain_t(const PrefillArgs& a, const uint8_t* ws, cudaStream_t
                                        (int)CS_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(MODE == MODE_FRAG ? 2 * a.H : a.H, MODE == MODE_PLAIN ? 1 : a.P, a.N);
-  tc_chain_kernel<Tout, MODE><<<grid, CHAIN_NT, CS_BYTES, s>>>(a, ws);
-  return cudaGetLastError();
+  return launch_pdl(tc_chain_kernel<Tout, MODE>, grid, dim3(CHAIN_NT), CS_BYTES, s, a, ws);
 }
 
 template <int MODE>
@@ -1143,7 +1146,8 @@ cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t 
   const long long tasks = (long long)nchunk * a.H * a.N;
   if (tasks > 0x7fffffff) return cudaErrorInvalidValue;
   const int grid = tasks < sms ? (int)tasks : sms;
-  tc_prep_kernel<<<grid, PREP_NT, PS_BYTES, s>>>(a, records, maps, nchunk);
+  cudaError_t le = launch_pdl(tc_prep_kernel, dim3(grid), dim3(PREP_NT), PS_BYTES, s, a, records, maps, nchunk);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

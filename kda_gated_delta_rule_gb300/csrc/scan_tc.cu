@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(SCAN_NT, 1) seg_scan_tc_kernel(const PrefillAr
   uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + SC_BAR);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SC_SLOT);
   const int tid = threadIdx.x, warp = tid >> 5;
+  tc::pdl_wait();  // the previous kernel in the stream (the fragments) is done
+  tc::pdl_launch_dependents();
   const int ct = blockIdx.x % (SD / SCT), h = blockIdx.x / (SD / SCT), i = blockIdx.y;
   const size_t head_elems = (size_t)SD * SD;
   int nseg;
@@ -276,8 +278,7 @@ cudaError_t launch_seg_scan_tc(const PrefillArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(seg_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC_BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid((SD / SCT) * a.H, a.N);
-  seg_scan_tc_kernel<<<grid, SCAN_NT, SC_BYTES, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(seg_scan_tc_kernel, grid, dim3(SCAN_NT), SC_BYTES, s, a);
 }
 
 }  // namespace kda

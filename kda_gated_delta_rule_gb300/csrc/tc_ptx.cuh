@@ -169,6 +169,12 @@ __device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// ---- programmatic dependent launch: the next kernel in the stream may be scheduled once every CTA of
+// this one has called launch_dependents (or exited); wait blocks until the previous kernel in the stream
+// has completed and its memory is visible (it returns at once when there is no such kernel)
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- named barriers over a subset of the block's warps (ids 1..15; n a multiple of 32)
 __device__ __forceinline__ void named_bar(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // barrier that also returns whether any participating thread passed p = true
