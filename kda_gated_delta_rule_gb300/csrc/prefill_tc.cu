@@ -554,44 +554,42 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
     // off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  First
     // M_ik = T_ii A_ik for all six pairs k < i at once (kept in the unused upper block (k, i)), then block
-    // row by block row T_ij = -sum_k M_ik T_kj.  Each thread owns a 1 x 4 strip (row r, columns 4 cg ..):
-    // per step one conflict-free scalar load (a warp's eight rows sit in eight bank groups) and one
-    // 16-byte load feed four FMAs.  T_ii is stored with its zero upper triangle, so the sums run over all 16.
-    if (tid < 6 * 64) {
-      const int pr = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+    // row by block row T_ij = -sum_k M_ik T_kj.  One warp per 16 x 16 block; lane (rp, cg) owns rows rp and
+    // rp + 8, columns 4 cg .. 4 cg + 3: per step two conflict-free scalar loads (a warp's eight rows sit in
+    // eight bank groups) and one 16-byte load feed eight FMAs (the rounds are bound by their shared loads).
+    // T_ii is stored with its zero upper triangle, so the sums run over all 16.
+    if (tid < 6 * 32) {
+      const int pr = tid >> 5, rp = (tid >> 2) & 7, cg = tid & 3;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
       const int bi = pr == 0 ? 1 : (pr < 3 ? 2 : 3);
       const int bk = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        const float tv = sT[(16 * bi + r) * LT + 16 * bi + u];
+        const float t0 = sT[(16 * bi + rp) * LT + 16 * bi + u], t1 = sT[(16 * bi + rp + 8) * LT + 16 * bi + u];
         const float4 a4 = *reinterpret_cast<const float4*>(sA + (16 * bi + u) * LT + 16 * bk + 4 * cg);
-        acc[0] = fmaf(tv, a4.x, acc[0]);
-        acc[1] = fmaf(tv, a4.y, acc[1]);
-        acc[2] = fmaf(tv, a4.z, acc[2]);
-        acc[3] = fmaf(tv, a4.w, acc[3]);
+        a0[0] = fmaf(t0, a4.x, a0[0]); a0[1] = fmaf(t0, a4.y, a0[1]); a0[2] = fmaf(t0, a4.z, a0[2]); a0[3] = fmaf(t0, a4.w, a0[3]);
+        a1[0] = fmaf(t1, a4.x, a1[0]); a1[1] = fmaf(t1, a4.y, a1[1]); a1[2] = fmaf(t1, a4.z, a1[2]); a1[3] = fmaf(t1, a4.w, a1[3]);
       }
-      *reinterpret_cast<float4*>(sT + (16 * bk + r) * LT + 16 * bi + 4 * cg) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(sT + (16 * bk + rp) * LT + 16 * bi + 4 * cg) = make_float4(a0[0], a0[1], a0[2], a0[3]);
+      *reinterpret_cast<float4*>(sT + (16 * bk + rp + 8) * LT + 16 * bi + 4 * cg) = make_float4(a1[0], a1[1], a1[2], a1[3]);
     }
     if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
 #pragma unroll 1
     for (int bi = 1; bi < 4; ++bi) {
-      if (tid < bi * 64) {
-        const int bj = tid >> 6, r = (tid >> 2) & 15, cg = tid & 3;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (tid < bi * 32) {
+        const int bj = tid >> 5, rp = (tid >> 2) & 7, cg = tid & 3;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
         for (int bk = bj; bk < bi; ++bk) {
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
-            const float mv = sT[(16 * bk + r) * LT + 16 * bi + u];
+            const float m0 = sT[(16 * bk + rp) * LT + 16 * bi + u], m1 = sT[(16 * bk + rp + 8) * LT + 16 * bi + u];
             const float4 t4 = *reinterpret_cast<const float4*>(sT + (16 * bk + u) * LT + 16 * bj + 4 * cg);
-            acc[0] = fmaf(mv, t4.x, acc[0]);
-            acc[1] = fmaf(mv, t4.y, acc[1]);
-            acc[2] = fmaf(mv, t4.z, acc[2]);
-            acc[3] = fmaf(mv, t4.w, acc[3]);
+            a0[0] = fmaf(m0, t4.x, a0[0]); a0[1] = fmaf(m0, t4.y, a0[1]); a0[2] = fmaf(m0, t4.z, a0[2]); a0[3] = fmaf(m0, t4.w, a0[3]);
+            a1[0] = fmaf(m1, t4.x, a1[0]); a1[1] = fmaf(m1, t4.y, a1[1]); a1[2] = fmaf(m1, t4.z, a1[2]); a1[3] = fmaf(m1, t4.w, a1[3]);
           }
         }
-        *reinterpret_cast<float4*>(sT + (16 * bi + r) * LT + 16 * bj + 4 * cg) =
-            make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+        *reinterpret_cast<float4*>(sT + (16 * bi + rp) * LT + 16 * bj + 4 * cg) = make_float4(-a0[0], -a0[1], -a0[2], -a0[3]);
+        *reinterpret_cast<float4*>(sT + (16 * bi + rp + 8) * LT + 16 * bj + 4 * cg) = make_float4(-a1[0], -a1[1], -a1[2], -a1[3]);
       }
       if (bi < 3) {
         if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
