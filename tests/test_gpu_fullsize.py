@@ -17,7 +17,7 @@ from tests._gpu import PrefillRun, expected_extra_pool, host, oracle_prefill, re
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-3
-SEGMENT_8K = 1024  # the segment length the benchmark uses for the single 8K request
+SEGMENT_8K = 704  # the segment length the benchmark uses for the single 8K request (12 segments)
 
 
 @pytest.fixture(scope="module")
