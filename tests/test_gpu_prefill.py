@@ -159,6 +159,43 @@ def test_segment_fragments_and_scan(cuda):
             assert rel_err(entry[i, p], expect[p]) <= 1e-5
 
 
+@pytest.mark.parametrize("dtype,tol", [(synth.F32, 1e-5), (synth.BF16, 2e-3)], ids=["f32", "bf16"])
+def test_segment_scan_d128(cuda, dtype, tol):
+    """The fragment scan at d = 128 (the tensor-core kernel): every entry state equals the oracle's state
+    at that segment's start, for sequences of three, two and one segments (each with a ragged tail).  With
+    bf16 inputs the fragments come from the tensor-core chain, whose operand records lead the workspace."""
+    kda = cuda
+    seg = 128
+    prob = synth.varlen(seed=37, H=2, d=128, num_slots=4, num_extra=8, snapshot_every_chunks=0,
+                        lengths=[300, 200, 70], dtype=dtype)
+    run = PrefillRun(prob)
+    ws = run.workspace_for(kda, seg)
+    c = {k: v for k, v in run.common().items()}
+    rec_bytes = kda.kda_prefill_workspace_size(*run.args(), **{k: v for k, v in c.items() if k != "dev_status"})
+    kda.kda_prefill_records(*run.args(), workspace=ws, **c)  # records (nothing on the CUDA-core path)
+    kda.kda_segment_fragments(*run.args(), seg, ws, **c)
+    kda.kda_fragment_scan(*run.args(), seg, ws, **c)
+    torch.cuda.synchronize()
+    assert status(run.status)[0] == 0
+    N, H, d = prob.N, prob.H, prob.dk
+    P = -(-int(prob.lengths.max()) // seg)
+    frag_elems = N * P * H * d * 2 * d
+    frag_bytes = -(-frag_elems * 4 // 256) * 256
+    base = (rec_bytes + frag_bytes) // 4  # workspace: [records][fragments][entry states]
+    wsf = ws.view(torch.float32)
+    entry = host(wsf[base:base + N * P * H * d * d]).reshape(N, P, H, d, d)
+    cu = prob.cu_seqlens.astype(np.int64)
+    for i in range(N):
+        n_seg = -(-int(prob.lengths[i]) // seg)
+        full = oracle.recurrence(prob.q[cu[i]:cu[i + 1]], prob.k[cu[i]:cu[i + 1]], prob.v[cu[i]:cu[i + 1]],
+                                 prob.g[cu[i]:cu[i + 1]], prob.beta[cu[i]:cu[i + 1]], [0, int(prob.lengths[i])],
+                                 s0=prob.pool[prob.slot_ids[i]][None].astype(np.float64), snap_every=seg,
+                                 want_o=False)
+        expect = [prob.pool[prob.slot_ids[i]].astype(np.float64)] + list(full["snaps"][0])
+        for p in range(n_seg):
+            assert rel_err(entry[i, p], expect[p]) <= tol
+
+
 def test_bad_cu_seqlens_flagged(cuda):
     kda = cuda
     prob = synth.varlen(seed=35, H=2, d=16, num_slots=4, num_extra=4, snapshot_every_chunks=0,
