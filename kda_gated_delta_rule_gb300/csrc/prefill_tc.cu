@@ -405,8 +405,9 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       split8_store(sm + PS_YHI + yo, sm + PS_YLO + yo, v);
     }
   }
-  // (K o gamma)^T, the B operand of W: row j, PREP_PARTS threads per row
-  {
+  // (K o gamma)^T, the B operand of W: row j, PREP_PARTS threads per row; and gamma_C for the record.  Needed
+  // only by the W / U~ product, so in the common case it runs while the Gram product is on the tensor core.
+  auto kp_pass = [&]() {
     constexpr int SCP = 8 / PREP_PARTS;
     const int j = tid & (D - 1), part = tid / D;
 #pragma unroll
@@ -419,8 +420,8 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       }
       split8_store(sm + PS_KPHI + tc::sw128_chunk(j, sc), sm + PS_KPLO + tc::sw128_chunk(j, sc), v);
     }
-  }
-  if (tid < D) reinterpret_cast<float*>(rec + REC_GAMMA)[tid] = __expf(sG[(C - 1) * D + tid]);
+    if (tid < D) reinterpret_cast<float*>(rec + REC_GAMMA)[tid] = __expf(sG[(C - 1) * D + tid]);
+  };
 
   // Gram matrices in TMEM columns 0..63: lanes 0..63 = A rows (before beta), lanes 64..127 = P rows
   if (ok && !slow) {
@@ -431,9 +432,11 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       issue_gram(sm, tm, 0, 64);
       tc::commit(bar);
     }
+    kp_pass();
     ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));
     ++gram_uses;
   } else if (ok) {
+    kp_pass();
     for (int e = tid; e < C * 16; e += PREP_NT) {
       const int s = e >> 4;
       build_y_chunk(sm, s, e & 15, (s & ~15) + 15);
