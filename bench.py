@@ -38,9 +38,9 @@ RECORD_BYTES = 256 + 256 + 512 + 4  # k, v bf16 + g fp32 + beta fp32
 # chunk-form algorithmic FLOPs per token and head at d = 128, C = 64: 2 (3 d^2 + 2.5 C d + C^2 / 6)
 ALG_FLOP_PER_TOKEN_HEAD = 2 * (3 * 128 * 128 + 2.5 * 64 * 128 + 64 * 64 / 6)
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one tc_prep_kernel launch on the 8K
-# workload, from one ncu --set full capture of the current kernel (126.74 MB read + 168.56 MB written; the
+# workload, from one ncu --set full capture of the current kernel (126.78 MB read + 168.23 MB written; the
 # command is in profiles/tc_prefill_8k.md); reported as the roofline's traffic while that kernel is unchanged
-PREP_DRAM_BYTES = 126_735_872 + 168_560_640
+PREP_DRAM_BYTES = 126_777_600 + 168_227_584
 
 
 def parse():
