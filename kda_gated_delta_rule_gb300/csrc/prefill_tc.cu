@@ -106,22 +106,13 @@ constexpr uint32_t PS_BYTES = 213824 + 1024;
 constexpr int PREP_NT = 512;
 constexpr int PREP_PARTS = PREP_NT / D;  // threads per channel in the per-channel phases
 
-// two-term split of a pair: (a, b) ~= hi + lo, packed bf16x2 (a in the low half)
-__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 // splits 8 floats and stores the hi and lo 16-byte chunks
 __device__ __forceinline__ void split8_store(void* hi_dst, void* lo_dst, const float* v) {
   uint4 h, l;
-  split_pair(v[0], v[1], h.x, l.x);
-  split_pair(v[2], v[3], h.y, l.y);
-  split_pair(v[4], v[5], h.z, l.z);
-  split_pair(v[6], v[7], h.w, l.w);
+  tc::split_pair(v[0], v[1], h.x, l.x);
+  tc::split_pair(v[2], v[3], h.y, l.y);
+  tc::split_pair(v[4], v[5], h.z, l.z);
+  tc::split_pair(v[6], v[7], h.w, l.w);
   *reinterpret_cast<uint4*>(hi_dst) = h;
   *reinterpret_cast<uint4*>(lo_dst) = l;
 }
@@ -928,7 +919,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         for (int jb = 0; jb < 2; ++jb) {
           uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) split_pair(s[32 * jb + 2 * e], s[32 * jb + 2 * e + 1], hi[e], lo[e]);
+          for (int e = 0; e < 16; ++e) tc::split_pair(s[32 * jb + 2 * e], s[32 * jb + 2 * e + 1], hi[e], lo[e]);
           tc::tmem_st16(trow + COL_STHI + j0 / 2 + 16 * jb, hi);
           tc::tmem_st16(trow + COL_STLO + j0 / 2 + 16 * jb, lo);
         }
@@ -961,7 +952,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         }
         uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
+        for (int e = 0; e < 16; ++e) tc::split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
         tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
         tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
       }

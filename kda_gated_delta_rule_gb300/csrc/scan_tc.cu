@@ -61,14 +61,6 @@ __device__ __forceinline__ uint8_t* align_1k(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// x = hi + lo (two bf16 terms) for a pair of values, packed as (first, second)
-__device__ __forceinline__ void split_two(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
 
 __global__ void __launch_bounds__(SCAN_NT, 1) seg_scan_tc_kernel(const PrefillArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -126,7 +118,7 @@ __global__ void __launch_bounds__(SCAN_NT, 1) seg_scan_tc_kernel(const PrefillAr
       const float mine = odd ? x[EC / 2 + j] : x[j];
       const float other = __shfl_xor_sync(0xffffffffu, odd ? x[j] : x[EC / 2 + j], 1);
       uint32_t hi, lo;
-      split_two(odd ? other : mine, odd ? mine : other, hi, lo);  // (row k, row k + 1)
+      tc::split_pair(odd ? other : mine, odd ? mine : other, hi, lo);  // (row k, row k + 1)
       const uint32_t o = tc::sw128(ce + (odd ? EC / 2 : 0) + j, k);
       *reinterpret_cast<uint32_t*>(bh + o) = hi;
       *reinterpret_cast<uint32_t*>(bh + 4096 + o) = lo;
@@ -173,8 +165,8 @@ __global__ void __launch_bounds__(SCAN_NT, 1) seg_scan_tc_kernel(const PrefillAr
     uint32_t hi[SK / 2], lo[SK / 2];
 #pragma unroll
     for (int q = 0; q < SK / 4; ++q) {
-      split_two(x[q].x, x[q].y, hi[2 * q], lo[2 * q]);
-      split_two(x[q].z, x[q].w, hi[2 * q + 1], lo[2 * q + 1]);
+      tc::split_pair(x[q].x, x[q].y, hi[2 * q], lo[2 * q]);
+      tc::split_pair(x[q].z, x[q].w, hi[2 * q + 1], lo[2 * q + 1]);
     }
     static_assert(SK == 32, "one 16-column store of hi and of lo per staging thread");
     const uint32_t col = COL_A + (uint32_t)(p & 1) * 128u + (uint32_t)(SK / 2) * (uint32_t)sq;
