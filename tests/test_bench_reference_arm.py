@@ -1,0 +1,54 @@
+"""The baseline arm of bench.py (`--impl reference`: the fp64 oracle on the host cores) keeps the JSON-line
+contract: one line from rank 0, the same metric, unit and direction as the GPU arm, and a cpu_baseline and
+e2e object describing the run.  It needs no GPU, so it runs here."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+METRIC = "KDA prefill tokens/s/layer (H=12,d=128); decode+verify state GB/s vs HBM peak"
+
+
+def _json_lines(stdout: str):
+    return [json.loads(ln) for ln in stdout.splitlines() if ln.startswith("{")]
+
+
+def _check_line(d: dict, n_gpus: int, steps: int, warmup: int):
+    assert d["impl"] == "reference"
+    assert d["metric"] == METRIC and d["unit"] == "tokens/s/layer" and d["higher_is_better"] is True
+    assert d["n_gpus"] == n_gpus and d["steps"] == steps and d["warmup"] == warmup
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["vs_baseline"] is None and d["data"] == "synthetic" and d["dtype"] == "f64"
+    assert "T=8192" in d["config"]["workload"] and "H=12" in d["config"]["workload"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_single_process():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "3"],
+                       cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_line(lines[0], n_gpus=1, steps=1, warmup=3)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Two ranks: rank 0 alone times the oracle and prints; the other rank exits 0 without work."""
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port),
+           "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_line(lines[0], n_gpus=2, steps=1, warmup=3)
