@@ -1,8 +1,9 @@
 """Python binding of the KDA CUDA library (libkda.so, C ABI in include/kda.h).
 
-Argument marshalling only: every function takes torch CUDA tensors, passes their device pointers and the
-current CUDA stream to the C entry point of the same name, and raises KdaError on a non-OK status.  There
-is no CPU fallback: if the library is not built, every call fails.
+Argument marshalling only: every function checks its tensors' shapes and dtypes against the layouts the
+header states, passes their device pointers and the current CUDA stream to the C entry point of the same
+name, and raises KdaError on a non-OK status.  There is no CPU fallback: if the library is not built,
+every call fails.
 """
 from __future__ import annotations
 
@@ -183,6 +184,75 @@ def _check(*ts):
             raise ValueError("expected contiguous CUDA tensors")
 
 
+# Shapes and dtypes, checked on the host before the device check and before any call into the library.
+# The C ABI takes bare pointers and the kernels trust the extents they are given, so a tensor of the wrong
+# shape or dtype would be read or written out of bounds on the device instead of raising here.  A shape
+# entry of None accepts any extent.
+
+_FP = (torch.float32,)
+_IN = (torch.float32, torch.bfloat16)
+_I32 = (torch.int32,)
+
+
+def _need(name, t, shape, dtypes):
+    if t is None:
+        return
+    if t.dim() != len(shape) or any(s is not None and t.shape[i] != s for i, s in enumerate(shape)):
+        want = ", ".join("*" if s is None else str(s) for s in shape)
+        raise ValueError(f"{name}: expected shape [{want}], got {list(t.shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: expected dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
+
+
+def _need_status(t):
+    if t is not None and (t.dtype != torch.int32 or t.numel() < 2):
+        raise ValueError(f"dev_status: expected an int32 tensor of at least 2 elements, got {t.dtype} "
+                         f"x {t.numel()}")
+
+
+def _rank(name, t, n):
+    if t.dim() != n:
+        raise ValueError(f"{name}: expected {n} dimensions, got shape {list(t.shape)}")
+    return tuple(t.shape)
+
+
+def _need_tokens(q, k, v, g, beta, lead):
+    """q, k, g [*lead, H, dk]; v [*lead, H, dv] in q's dtype (fp32 or bf16); g fp32; beta [*lead, H] fp32.
+    Returns (H, dk, dv)."""
+    n = len(lead)
+    H, dk = _rank("q", q, n + 2)[n:]
+    _need("q", q, (*lead, H, dk), _IN)
+    _need("k", k, (*lead, H, dk), (q.dtype,))
+    _need("v", v, (*lead, H, None), (q.dtype,))
+    dv = v.shape[-1]
+    _need("g", g, (*lead, H, dk), _FP)
+    _need("beta", beta, (*lead, H), _FP)
+    return H, dk, dv
+
+
+def _need_prefill(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out, extra_pool=None, extra_slot_ids=None):
+    T = _rank("q", q, 3)[0]
+    H, dk, dv = _need_tokens(q, k, v, g, beta, (T,))
+    _need("cu_seqlens", cu_seqlens, (None,), _I32)
+    if cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens: expected N + 1 >= 1 offsets")
+    N = cu_seqlens.numel() - 1
+    _need("pool", pool, (None, H, dk, dv), _FP)
+    _need("slot_ids", slot_ids, (N,), _I32)
+    _need("out", out, (T, H, dv), _IN)
+    if (extra_pool is None) != (extra_slot_ids is None):
+        raise ValueError("extra_pool and extra_slot_ids go together")
+    _need("extra_pool", extra_pool, (None, H, dk, dv), _FP)
+    _need("extra_slot_ids", extra_slot_ids, (N, 2), _I32)
+    return T, N, H, dk, dv
+
+
+def _need_cfbi_cache(pool, cache, counts):
+    S, H = pool.shape[:2]
+    _need("cache", cache, (S, H, CFBI_CHUNK, CFBI_ROW_FLOATS), _FP)
+    _need("counts", counts, (S, H), _I32)
+
+
 def _ok(fn: str, code: int):
     if code != KDA_OK:
         raise KdaError(fn, code)
@@ -204,6 +274,12 @@ def kda_state_bytes_per_head(dk: int, dv: int) -> int:
 
 def kda_state_copy(src_pool, src_slots, dst_pool, dst_slots, dev_status=None, stream=None):
     """dst_pool[dst_slots[i]] = src_pool[src_slots[i]] (pools [slots, H, dk, dv] fp32)."""
+    head = _rank("src_pool", src_pool, 4)[1:]
+    _need("src_pool", src_pool, (None, *head), _FP)
+    _need("dst_pool", dst_pool, (None, *head), _FP)
+    _need("src_slots", src_slots, (None,), _I32)
+    _need("dst_slots", dst_slots, (src_slots.numel(),), _I32)
+    _need_status(dev_status)
     _check(src_pool, src_slots, dst_pool, dst_slots, dev_status)
     n = src_slots.numel()
     elems = src_pool[0].numel() if src_pool.shape[0] else dst_pool[0].numel()
@@ -214,6 +290,12 @@ def kda_state_copy(src_pool, src_slots, dst_pool, dst_slots, dev_status=None, st
 
 def kda_decode_step(q, k, v, g, beta, pool, slot_ids, out, dev_status=None, stream=None):
     """One token per request; q, k, g [B, H, dk]; v, out [B, H, dv]; beta [B, H]; pool updated in place."""
+    B = _rank("q", q, 3)[0]
+    H, dk, dv = _need_tokens(q, k, v, g, beta, (B,))
+    _need("pool", pool, (None, H, dk, dv), _FP)
+    _need("slot_ids", slot_ids, (B,), _I32)
+    _need("out", out, (B, H, dv), _IN)
+    _need_status(dev_status)
     _check(q, k, v, g, beta, pool, slot_ids, out, dev_status)
     B, H, dk = q.shape
     dv = v.shape[-1]
@@ -230,6 +312,9 @@ def kda_cfbi_prefill(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, cache, coun
                      stream=None):
     """CF-BI prefill over packed sequences: q, k, g [T, H, 128]; v, out [T, H, 128]; beta [T, H];
     cu_seqlens int32 [N + 1]; pool [S, H, 128, 128]; cache [S, H, 16, 420] fp32; counts [S, H] int32."""
+    _need_prefill(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out)
+    _need_cfbi_cache(pool, cache, counts)
+    _need_status(dev_status)
     _check(q, k, v, g, beta, cu_seqlens, pool, cache, counts, slot_ids, out, dev_status)
     T, H, dk = q.shape
     dv = v.shape[-1]
@@ -242,6 +327,13 @@ def kda_cfbi_prefill(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, cache, coun
 
 def kda_cfbi_decode(q, k, v, g, beta, pool, cache, counts, slot_ids, out, dev_status=None, stream=None):
     """CF-BI decode, one token per request: q, k, g [B, H, 128]; v, out [B, H, 128]; beta [B, H]."""
+    B = _rank("q", q, 3)[0]
+    H, dk, dv = _need_tokens(q, k, v, g, beta, (B,))
+    _need("pool", pool, (None, H, dk, dv), _FP)
+    _need("slot_ids", slot_ids, (B,), _I32)
+    _need("out", out, (B, H, dv), _IN)
+    _need_cfbi_cache(pool, cache, counts)
+    _need_status(dev_status)
     _check(q, k, v, g, beta, pool, cache, counts, slot_ids, out, dev_status)
     B, H, dk = q.shape
     dv = v.shape[-1]
@@ -256,6 +348,13 @@ def kda_replay_bytes(B: int, W: int, H: int, dk: int, dv: int, in_dtype: int) ->
 
 def kda_verify(q, k, v, g, beta, pool, slot_ids, out, replay, snapshot_out=None, dev_status=None, stream=None):
     """Draft window: q, k, g [B, W, H, dk]; v, out [B, W, H, dv]; beta [B, W, H]; replay: uint8 record buffer."""
+    B, W = _rank("q", q, 4)[:2]
+    H, dk, dv = _need_tokens(q, k, v, g, beta, (B, W))
+    _need("pool", pool, (None, H, dk, dv), _FP)
+    _need("slot_ids", slot_ids, (B,), _I32)
+    _need("out", out, (B, W, H, dv), _IN)
+    _need("snapshot_out", snapshot_out, (B, W, H, dk, dv), _FP)
+    _need_status(dev_status)
     _check(q, k, v, g, beta, pool, slot_ids, out, replay, snapshot_out, dev_status)
     B, W, H, dk = q.shape
     dv = v.shape[-1]
@@ -267,6 +366,10 @@ def kda_verify(q, k, v, g, beta, pool, slot_ids, out, replay, snapshot_out=None,
 
 def kda_verify_replay(pool, slot_ids, replay, accepted_len, W, H, dk, dv, in_dtype, dev_status=None, stream=None):
     """Commits tokens 1..accepted_len[b] of each window into pool[slot_ids[b]]."""
+    _need("pool", pool, (None, H, dk, dv), _FP)
+    _need("slot_ids", slot_ids, (None,), _I32)
+    _need("accepted_len", accepted_len, (slot_ids.numel(),), _I32)
+    _need_status(dev_status)
     _check(pool, slot_ids, replay, accepted_len, dev_status)
     B = slot_ids.numel()
     _ok("kda_verify_replay", load().kda_verify_replay(_p(pool), pool.shape[0], _p(slot_ids), B, W, H, dk, dv,
@@ -276,6 +379,8 @@ def kda_verify_replay(pool, slot_ids, replay, accepted_len, W, H, dk, dv, in_dty
 
 def _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, init_zero=False,
                     extra_pool=None, extra_slot_ids=None, snapshot_every_chunks=0, workspace=None, dev_status=None):
+    _need_prefill(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out, extra_pool, extra_slot_ids)
+    _need_status(dev_status)
     _check(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out, extra_pool, extra_slot_ids, workspace, dev_status)
     T, H, dk = q.shape
     a = PrefillArgs()
@@ -375,6 +480,23 @@ def kda_prefill_segmented_noalloc(q, k, v, g, beta, cu_seqlens, max_seqlen, pool
 
 def _backward_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, d_out, dq, dk, dv, dg, dbeta, pool=None,
                      slot_ids=None, d_final=None, d_init=None, workspace=None, dev_status=None):
+    T = _rank("q", q, 3)[0]
+    H, d_k, d_v = _need_tokens(q, k, v, g, beta, (T,))
+    _need("cu_seqlens", cu_seqlens, (None,), _I32)
+    if cu_seqlens.numel() < 1:
+        raise ValueError("cu_seqlens: expected N + 1 >= 1 offsets")
+    N = cu_seqlens.numel() - 1
+    if (pool is None) != (slot_ids is None):
+        raise ValueError("pool and slot_ids go together (both None: zero initial states)")
+    _need("pool", pool, (None, H, d_k, d_v), _FP)
+    _need("slot_ids", slot_ids, (N,), _I32)
+    _need("d_out", d_out, (T, H, d_v), (q.dtype,))
+    for name, t, w in (("dq", dq, d_k), ("dk", dk, d_k), ("dg", dg, d_k), ("dv", dv, d_v)):
+        _need(name, t, (T, H, w), _FP)
+    _need("dbeta", dbeta, (T, H), _FP)
+    _need("d_final", d_final, (N, H, d_k, d_v), _FP)
+    _need("d_init", d_init, (N, H, d_k, d_v), _FP)
+    _need_status(dev_status)
     _check(q, k, v, g, beta, cu_seqlens, d_out, dq, dk, dv, dg, dbeta, pool, slot_ids, d_final, d_init, workspace,
            dev_status)
     T, H, dkk = q.shape
@@ -428,6 +550,19 @@ def kda_fused_decode(xq, xk, xv, a, b, z, pool, slot_ids, conv_state, conv_w, no
     xq, xk, xv, z, out [B, H, 128]; a [B, H, 128]; b [B, H]; pool [S, H, 128, 128];
     conv_state [S, H, 3, 3, 128] fp32 (advanced in place); conv_w [3, H, 128, 4]; norm_w [128].
     """
+    B, H, d = _rank("xq", xq, 3)
+    _need("xq", xq, (B, H, d), _IN)
+    for name, t in (("xk", xk), ("xv", xv), ("z", z)):
+        _need(name, t, (B, H, d), (xq.dtype,))
+    _need("a", a, (B, H, d), _FP)
+    _need("b", b, (B, H), _FP)
+    _need("pool", pool, (None, H, d, d), _FP)
+    _need("slot_ids", slot_ids, (B,), _I32)
+    _need("conv_state", conv_state, (pool.shape[0], H, 3, 3, d), _FP)
+    _need("conv_w", conv_w, (3, H, d, 4), _FP)
+    _need("norm_w", norm_w, (d,), _FP)
+    _need("out", out, (B, H, d), _IN)
+    _need_status(dev_status)
     _check(xq, xk, xv, a, b, z, pool, slot_ids, conv_state, conv_w, norm_w, out, dev_status)
     B, H, d = xq.shape
     f = FusedDecodeArgs()
@@ -447,6 +582,8 @@ def kda_kcp_fragments(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, 
                       dev_status=None, stream=None):
     """Fragments (S~ | M) of every segment of the shard's sequences, the last included, into frag_out
     [N, P, H, dk, dv + dk]; run kda_prefill_records on the same workspace first (tensor-core path)."""
+    _, N, H, dk, dv = _need_prefill(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out)
+    _need("frag_out", frag_out, (N, None, H, dk, dv + dk), _FP)
     _check(frag_out)
     a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, workspace=workspace,
                         dev_status=dev_status)
@@ -456,6 +593,12 @@ def kda_kcp_fragments(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, 
 
 def kda_kcp_scan(frags, s0, entries, dev_status=None, stream=None):
     """entries[0] = s0, entries[p + 1] = M_p entries[p] + S~_p over gathered fragments [P, H, dk, dv + dk]."""
+    P, H, dk, w = _rank("frags", frags, 4)
+    dv = w - dk
+    _need("frags", frags, (P, H, dk, dv + dk), _FP)
+    _need("s0", s0, (H, dk, dv), _FP)
+    _need("entries", entries, (P, H, dk, dv), _FP)
+    _need_status(dev_status)
     _check(frags, s0, entries, dev_status)
     P, H, dk, w = frags.shape
     _ok("kda_kcp_scan", load().kda_kcp_scan(_p(frags), P, H, dk, w - dk, _p(s0), _p(entries), _p(dev_status),
@@ -465,6 +608,8 @@ def kda_kcp_scan(frags, s0, entries, dev_status=None, stream=None):
 def kda_kcp_outputs(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, segment_len, workspace, entries,
                     dev_status=None, stream=None):
     """Outputs and final states of the shard from its entry states [N, P, H, dk, dv]."""
+    _, N, H, dk, dv = _need_prefill(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out)
+    _need("entries", entries, (N, None, H, dk, dv), _FP)
     _check(entries)
     a = _prefill_struct(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, slot_ids, out, workspace=workspace,
                         dev_status=dev_status)
