@@ -326,3 +326,59 @@ def test_planted_mistakes_are_caught(mut):
         except (AssertionError, ValueError):
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake '{mut}'"
+
+
+# ---------------------------------------------------------------- packing, snapshot and sampling bookkeeping
+#
+# The varlen contract ("SGLang and Miles: day-0 support for Kimi K3", hybrid KDA memory section: every
+# sequence has its own slot; snapshots at fixed token boundaries of each sequence) fixes these by
+# construction: a packed run is N independent runs, snapshot m of a sequence is its state after m x every
+# of its own tokens, and a sampled output is the same output computed in full.  Each test compares two
+# different outputs of the oracle (packed vs separate runs, snapshot vs final state, sample vs full), so a
+# slip in the offsets (a state carried across a sequence boundary, boundaries counted on packed positions,
+# an off-by-one in the sample index) fails one of them.
+
+VARLEN = [300, 64, 0, 530, 63, 1]
+
+
+def _varlen_problem(seed, H=2, dk=8, dv=8):
+    rng = np.random.default_rng(seed)
+    cu = np.concatenate([[0], np.cumsum(VARLEN)]).astype(np.int64)
+    q, k, v, g, beta = _problem(rng, int(cu[-1]), H, dk, dv)
+    s0 = rng.standard_normal((len(VARLEN), H, dk, dv)) * 0.1
+    return cu, (q, k, v, g, beta), s0
+
+
+def test_packed_sequences_are_independent_runs():
+    cu, x, s0 = _varlen_problem(51)
+    r = oracle.recurrence(*x, cu, s0=s0)
+    for i in range(len(VARLEN)):
+        sl = slice(cu[i], cu[i + 1])
+        alone = oracle.recurrence(*(a[sl] for a in x), [0, VARLEN[i]], s0=s0[i:i + 1])
+        np.testing.assert_array_equal(r["o"][sl], alone["o"])
+        np.testing.assert_array_equal(r["s_final"][i], alone["s_final"][0])
+    # an empty sequence hands its initial state back unchanged
+    np.testing.assert_array_equal(r["s_final"][VARLEN.index(0)], s0[VARLEN.index(0)])
+
+
+@pytest.mark.parametrize("every", [1, 64, 256])
+def test_snapshots_count_from_each_sequence_start(every):
+    cu, x, s0 = _varlen_problem(52)
+    r = oracle.recurrence(*x, cu, s0=s0, snap_every=every)
+    for i, L in enumerate(VARLEN):
+        snaps = r["snaps"][i]
+        assert snaps.shape[0] == L // every
+        for m in range(1, L // every + 1):
+            sl = slice(cu[i], cu[i] + m * every)
+            prefix = oracle.recurrence(*(a[sl] for a in x), [0, m * every], s0=s0[i:i + 1], want_o=False)
+            np.testing.assert_array_equal(snaps[m - 1], prefix["s_final"][0])
+
+
+def test_sampled_outputs_equal_the_full_outputs():
+    cu, x, s0 = _varlen_problem(53)
+    T = int(cu[-1])
+    sample = np.array([0, 1, 299, 300, 363, 364, 893, T - 1], np.int64)
+    full = oracle.recurrence(*x, cu, s0=s0)
+    part = oracle.recurrence(*x, cu, s0=s0, want_o=False, sample_t=sample)
+    np.testing.assert_array_equal(part["o_samples"], full["o"][sample])
+    np.testing.assert_array_equal(part["s_final"], full["s_final"])
