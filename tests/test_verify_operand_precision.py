@@ -16,29 +16,9 @@ import numpy as np
 
 import oracle
 import synth
+from tests._precision import bf16 as bf16_rne, tf32_round, tf32_trunc
 
 BOUND = 2e-3
-
-
-def _round_bits(x, keep_mask, half):
-    b = x.astype(np.float32).view(np.uint32)
-    if half:
-        b = b + np.uint32(half)
-    return (b & np.uint32(keep_mask)).view(np.float32).astype(np.float64)
-
-
-def tf32_trunc(x):
-    return _round_bits(x, 0xFFFFE000, 0)
-
-
-def tf32_round(x):  # to nearest, ties away from zero
-    return _round_bits(x, 0xFFFFE000, 0x1000)
-
-
-def bf16_rne(x):
-    b = x.astype(np.float32).view(np.uint32)
-    b = b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))
-    return (b & np.uint32(0xFFFF0000)).view(np.float32).astype(np.float64)
 
 
 def _window_terms(p):
