@@ -180,3 +180,50 @@ def chunked_backward(q, k, v, g, beta, S0, dO, dST, C=64):
         dS = dS_entry
     out["ds0"] = dS
     return out
+
+
+def segment_reverse_fragments(q, k, v, g, beta, dO, C=64, seg_chunks=2):
+    """The backward's state-gradient carry in segment form, for one head (fp64).
+
+    Per chunk, dS_in = M_c^T dS_out + b_c with M_c^T = Diag(e^{G_C}) - W^T K^ (the transpose of the
+    forward chunk transition S' = (Diag(e^{G_C}) - K^^T W) S + K^^T U~) and b_c = (Q+ - P W)^T dO, which
+    depends on the chunk's inputs and dO only, not on the forward state.  A segment of `seg_chunks`
+    chunks composes to dS_in = N dS_out + b~, found by running [b | X] backwards through its chunks from
+    [0 | I].  Returns the list of (N, b~) per segment, in token order.
+    """
+    f = lambda x: np.asarray(x, np.float64)
+    q, k, v, g, beta, dO = f(q), f(k), f(v), f(g), f(beta), f(dO)
+    T, dk = q.shape
+    chunk_terms = []
+    for c0 in range(0, T, C):
+        c1 = min(c0 + C, T)
+        n = c1 - c0
+        kc, qc, bc = k[c0:c1], q[c0:c1], beta[c0:c1]
+        G = np.cumsum(g[c0:c1], axis=0)
+        E = np.exp(G[:, None, :] - G[None, :, :])
+        A = bc[:, None] * np.einsum("tj,sj,tsj->ts", kc, kc, E) * np.tril(np.ones((n, n)), -1)
+        P = np.einsum("tj,sj,tsj->ts", qc, kc, E) * np.tril(np.ones((n, n)))
+        W = np.linalg.inv(np.eye(n) + A) @ (bc[:, None] * kc * np.exp(G))
+        kh = kc * np.exp(G[-1] - G)
+        Mt = np.diag(np.exp(G[-1])) - W.T @ kh
+        b = (qc * np.exp(G) - P @ W).T @ dO[c0:c1]
+        chunk_terms.append((Mt, b))
+    frags = []
+    for s0 in range(0, len(chunk_terms), seg_chunks):
+        X, y = np.eye(dk), np.zeros_like(chunk_terms[0][1])
+        for Mt, b in reversed(chunk_terms[s0:s0 + seg_chunks]):
+            X, y = Mt @ X, Mt @ y + b
+        frags.append((X, y))
+    return frags
+
+
+def reverse_scan(frags, dST):
+    """Exit gradients of every segment from the last one's (dST): exit_{p-1} = N_p exit_p + b~_p.
+    Returns [exit_0, ..., exit_{P-1}, entry_0] (entry_0 = dL/dS_0)."""
+    exits = [None] * len(frags)
+    d = np.asarray(dST, np.float64)
+    for p in range(len(frags) - 1, -1, -1):
+        exits[p] = d
+        N, b = frags[p]
+        d = N @ d + b
+    return exits + [d]

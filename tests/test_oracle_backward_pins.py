@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests._bruteforce import chunked_backward
+from tests._bruteforce import chunked_backward, reverse_scan, segment_reverse_fragments
 
 
 def _unit_rows(rng, shape):
@@ -149,3 +149,36 @@ def test_planted_backward_mistakes_are_caught(mut):
         except AssertionError:
             caught.append(pin.__name__)
     assert caught, f"no pin caught the planted mistake {mut}"
+
+
+def test_segmented_reverse_carry_matches_suffix_backwards():
+    """The backward's state-gradient carry splits into segments like the forward's state: per segment a
+    fragment (N, b~) with dS_in = N dS_out + b~, composed by a scan from dS_T (tests/_bruteforce.py).  At
+    every segment boundary t_p the scan's gradient must equal dL/dS_{t_p} from the oracle's own backward
+    over the suffix [t_p, T) started from the forward state at t_p (outputs before t_p do not depend on
+    S_{t_p}), and at t = 0 the oracle's dS_0 over the whole sequence; then each segment's reverse pass from
+    its exact exit gradient and forward entry state reproduces the whole backward's gradients."""
+    p, cu, do, dsT, _ = _problem(16, [300], H=2, dk=8, dv=6)
+    T, C, seg = 300, 64, 2
+    names = ("q", "k", "v", "g", "beta")
+    gr = _grads(p, cu, do, dsT, "none")
+    bounds = list(range(0, T, C * seg))  # segment starts: 0, 128, 256
+    for h in range(2):
+        frags = segment_reverse_fragments(*(p[n][:, h] for n in names), do[:, h], C=C, seg_chunks=seg)
+        grads = reverse_scan(frags, dsT[0, h])  # exit gradient of each segment, then dL/dS_0
+        assert len(frags) == len(bounds)
+        np.testing.assert_allclose(grads[-1], gr["ds0"][0, h], rtol=1e-10, atol=1e-12)
+        for sp, t_p in enumerate(bounds[1:]):  # the exit gradient of segment sp is dL/dS_{t_p}
+            head = oracle.recurrence(*(p[n][:t_p] for n in names), [0, t_p], s0=p["s0"][:1])
+            suffix = oracle.backward(*(p[n][t_p:] for n in names), [0, T - t_p], do[t_p:],
+                                     s0=head["s_final"], ds_final=dsT[:1])
+            np.testing.assert_allclose(grads[sp], suffix["ds0"][0, h], rtol=1e-10, atol=1e-12)
+        # each segment's reverse pass from its exact exit gradient and forward entry state
+        for sp, t0 in enumerate(bounds):
+            t1 = min(t0 + C * seg, T)
+            entry = p["s0"][0, h] if t0 == 0 else oracle.recurrence(
+                *(p[n][:t0, h:h + 1] for n in names), [0, t0], s0=p["s0"][:1, h:h + 1])["s_final"][0, 0]
+            cb = chunked_backward(*(p[n][t0:t1, h] for n in names), entry, do[t0:t1, h], grads[sp])
+            for n in ("dq", "dk", "dv", "dg", "dbeta"):
+                ref = gr[n][t0:t1, h]
+                assert np.abs(cb[n] - ref).max() <= 1e-10 * max(1.0, np.abs(ref).max()), (n, sp, h)
