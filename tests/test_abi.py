@@ -44,6 +44,17 @@ def test_status_strings_and_sizes(lib):
     assert b >= 256 * 8 * 12 * 1028 and b - 256 * 8 * 12 * 1028 < 4 * 256
 
 
+def test_stated_size_formulas(lib):
+    """The sizes the header states in closed form: the backward's workspace is (ceil(T/64) + N) x H x
+    574720 bytes; a CF-BI row cache is 16 rows x 420 fp32 per head at d = 128 and 0 elsewhere."""
+    for T, N, H in ((8192, 1, 12), (300, 3, 2), (64, 1, 1), (65, 2, 4)):
+        assert kda.kda_backward_workspace_size(T, N, H) == (-(-T // 64) + N) * H * 574720
+    assert kda.kda_cfbi_cache_bytes_per_head(128, 128) == kda.CFBI_CHUNK * kda.CFBI_ROW_FLOATS * 4 == 26880
+    assert kda.kda_cfbi_cache_bytes_per_head(64, 64) == 0
+    assert lib.kda_backward_args_bytes() == ctypes.sizeof(kda.BackwardArgs)
+    assert lib.kda_fused_decode_args_bytes() == ctypes.sizeof(kda.FusedDecodeArgs)
+
+
 def test_host_validation_rejects_before_launch(lib):
     """Invalid arguments return an error code; nothing is launched (no GPU is needed to check this)."""
     null = None
