@@ -52,3 +52,18 @@ def test_reference_arm_under_torchrun_prints_once():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_line(lines[0], n_gpus=2, steps=1, warmup=3)
+
+
+def test_cpu_baseline_object():
+    """The GPU arm's cpu_baseline: the oracle repeated over the sample until the time floor is reached,
+    value = tokens processed / seconds timed, with the threads it used."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    prob = synth.varlen(seed=5, H=12, d=128, num_slots=2, num_extra=2, lengths=[256])
+    cb = bench.cpu_baseline(prob, sample_tokens=256, min_seconds=0.5)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s/layer" and cb["cores"] >= 1
+    assert cb["repeats"] >= 1 and cb["seconds"] >= 0.5
+    # seconds is reported to the millisecond (>= 0.5 s timed): the value agrees to 0.2 %
+    assert abs(cb["value"] - cb["repeats"] * 256 / cb["seconds"]) <= 2e-3 * cb["value"]
+    assert f"{cb['repeats']} passes" in cb["sample"]
