@@ -26,7 +26,10 @@ Functions follow these passages:
   prefix from the committed state.
 
 Pins: every function here is checked against closed forms, invariants, the
-pages' worked example and brute force in ``tests/test_oracle_pins.py``.
+pages' worked example, brute force and finite differences, in
+``tests/test_oracle_pins.py`` (recurrence, transition, decode / verify / fold,
+and the packing, snapshot and sampling bookkeeping), ``tests/test_oracle_backward_pins.py``
+(backward) and ``tests/test_oracle_fused_pins.py`` (short convolution, fused decode).
 """
 from __future__ import annotations
 
