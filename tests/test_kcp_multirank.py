@@ -102,3 +102,17 @@ def test_two_ranks_reproduce_the_unsplit_recurrence():
     # the scan's entry state of rank 1 is the state after rank 0's tokens
     head = oracle.recurrence(*(full[n][:b[1]] for n in ("q", "k", "v", "g", "beta")), [0, b[1]], s0=s0[None])
     np.testing.assert_allclose(res[0][1][1], head["s_final"][0], rtol=0, atol=1e-11)
+
+
+def test_shard_bounds_cover_the_sequence_evenly():
+    """Contiguous shards in rank order that cover [0, T) exactly, none empty, sizes within one token."""
+    sys.path.insert(0, ROOT)
+    from kda_gated_delta_rule_gb300.kcp import shard_bounds
+    for T in (1, 7, 150, 8192, 1_048_579):
+        for world in range(1, 9):
+            if T < world:
+                continue
+            b = shard_bounds(T, world)
+            sizes = np.diff(b)
+            assert len(b) == world + 1 and b[0] == 0 and b[-1] == T
+            assert sizes.min() >= 1 and sizes.max() - sizes.min() <= 1
