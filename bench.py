@@ -37,10 +37,57 @@ STATE_BYTES = 128 * 128 * 4
 RECORD_BYTES = 256 + 256 + 512 + 4  # k, v bf16 + g fp32 + beta fp32
 # chunk-form algorithmic FLOPs per token and head at d = 128, C = 64: 2 (3 d^2 + 2.5 C d + C^2 / 6)
 ALG_FLOP_PER_TOKEN_HEAD = 2 * (3 * 128 * 128 + 2.5 * 64 * 128 + 64 * 64 / 6)
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one tc_prep_kernel launch on the 8K
-# workload, from one ncu --set full capture of the current kernel (126.78 MB read + 168.23 MB written; the
-# command is in profiles/tc_prefill_8k.md); reported as the roofline's traffic while that kernel is unchanged
-PREP_DRAM_BYTES = 126_777_600 + 168_227_584
+# DRAM traffic per launch of a kernel, from one ncu capture, keyed by the SHA-256 of the kernel's source
+# files: reported as the roofline's traffic only while the committed sources still hash to that value
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+CSRC = os.path.join(ROOT, "kda_gated_delta_rule_gb300", "csrc")
+
+
+def source_sha256(files) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str, table: str = TRAFFIC_TABLE):
+    """DRAM bytes (read + write) of one launch of `kernel` on `workload` from the traffic table, or None when
+    the table has no row for it or the kernel's sources changed since the capture."""
+    if not os.path.exists(table):
+        return None
+    for line in open(table):
+        if not line.strip() or line.startswith("#"):
+            continue
+        f = line.rstrip("\n").split("\t")
+        if len(f) < 6 or f[0] != kernel or f[1] != workload:
+            continue
+        try:
+            if source_sha256(f[2].split(",")) != f[3]:
+                return None
+        except OSError:
+            return None
+        return int(f[4]) + int(f[5])
+    return None
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine() or "unknown"
 
 
 def parse():
@@ -55,6 +102,8 @@ def parse():
                          "output phase (one CTA per head and segment) fits one wave on this GPU")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the varlen packed-prefill workload")
+    ap.add_argument("--no-long", action="store_true", help="skip the 1M-token segmented prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -303,7 +352,7 @@ def run_ours(args):
     path_gbs = alg_bytes / (ms_max / 1e3) / 1e9
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5),
-                "traffic": PREP_DRAM_BYTES if dominant == "tc_prep_kernel" and T == 8192 else None,
+                "traffic": measured_traffic(dominant, "prefill_8k"),
                 "peak_source": pk_kind, "algorithmic_bytes": alg_bytes,
                 "kernel_ms": round(phases[dominant], 4),
                 "phase_ms": {kk: round(vv, 4) for kk, vv in phases.items()},
@@ -384,6 +433,30 @@ def run_ours(args):
     if not args.no_backward:
         bw_report = backward_report(kda, torch, dev, to_dev, time_calls, pk, prob)
 
+    # ---- the varlen packed prefill and the 1M-token segmented prefill (tokens/s, fraction of HBM)
+    del ws, ws_var, sets
+    torch.cuda.empty_cache()
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    varlen_report = long_report = None
+    if not args.no_varlen:
+        vprob = synth.varlen()
+        varlen_report = prefill_workload_report(
+            kda, torch, dev, to_dev, vprob, varlen_candidates(vprob, props.multi_processor_count),
+            steps=max(5, min(args.steps, 20)), warmup=args.warmup, pk=pk, oracle_tokens=16384, oracle_seconds=5.0,
+            with_cpu=with_cpu)
+        varlen_report["workload"] = ("varlen packed prefill: 16 sequences, lengths log-uniform in [512, 32768] "
+                                     f"({vprob.T} tokens), H=12, d=128, bf16 q/k/v, 256-slot fp32 pool gathered and "
+                                     "scattered by slot id, snapshots every 4 chunks into a ping-pong extra pool")
+        del vprob
+    if not args.no_long:
+        lprob = synth.long_1m()
+        long_report = prefill_workload_report(
+            kda, torch, dev, to_dev, lprob, [("segmented", lprob.segment_len)], steps=5, warmup=2, pk=pk,
+            oracle_tokens=16384, oracle_seconds=5.0, with_cpu=with_cpu)
+        long_report["workload"] = ("long-context prefill: B=1, T=1,048,576, H=12, d=128, bf16 q/k/v, fp32 gates and "
+                                   "state, 64 segments of 16,384 tokens composed by the on-GPU fragment scan")
+        del lprob
+
     line = {
         "metric": "KDA prefill tokens/s/layer (H=12,d=128); decode+verify state GB/s vs HBM peak",
         "value": round(value, 1),
@@ -418,6 +491,10 @@ def run_ours(args):
         line["decode_verify"] = dv_report
     if bw_report:
         line["backward"] = bw_report
+    if varlen_report:
+        line["varlen_prefill"] = varlen_report
+    if long_report:
+        line["long_prefill"] = long_report
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(prob, sample_tokens=T)
     if rank == 0:
@@ -438,7 +515,9 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
     wout = torch.empty(B, W, H, d, dtype=torch.bfloat16, device=dev)
     rec = torch.empty(kda.kda_replay_bytes(B, W, H, d, d, p.in_dtype), dtype=torch.uint8, device=dev)
     acc = to_dev(p.accepted)
-    ckpt_slots = to_dev(synth.distinct_slots(p.seed, 99, B, p.pool.shape[0]))
+    # checkpoint slots drawn from the slots the requests do not hold: a copy's source and destination never alias
+    free = np.setdiff1d(np.arange(p.pool.shape[0], dtype=np.int32), p.slot_ids)
+    ckpt_slots = to_dev(free[synth.distinct_slots(p.seed, 99, B, free.size)].astype(np.int32))
 
     def dec():
         kda.kda_decode_step(q, k, v, g, beta, pool, slots, out)
@@ -506,6 +585,98 @@ def decode_verify_report(kda, torch, dev, to_dev, time_calls, pk, world):
     return rep
 
 
+def prefill_workload_report(kda, torch, dev, to_dev, prob, candidates, steps, warmup, pk, oracle_tokens,
+                            oracle_seconds, with_cpu):
+    """Tokens/s of one packed prefill workload on the device: each step restores the sequences' initial
+    states from a checkpoint pool (a state copy of N slots) and runs the prefill over the whole batch
+    (gather from the pool, chunk path, snapshots, scatter back).  `candidates` are (path, segment length)
+    pairs, each timed over a few untimed steps; the fastest is timed over `steps`.  The inputs are larger
+    than L2, so no flush between steps.  Algorithmic bytes: 1540 per token and head, the initial and final
+    state of every (sequence, head), and the snapshot states left in the extra pool."""
+    T, H, d, N = prob.T, prob.H, prob.dk, prob.N
+    q, k, v, g, beta = (to_dev(x) for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    cu = to_dev(prob.cu_seqlens.astype(np.int32))
+    ckpt = to_dev(prob.pool)
+    pool = ckpt.clone()
+    slots = to_dev(prob.slot_ids.astype(np.int32))
+    out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(2, dtype=torch.int32, device=dev)
+    max_len = int(prob.lengths.max())
+    common = {}
+    every = 0
+    if prob.extra_pool is not None and prob.snapshot_every_chunks:
+        common = dict(extra_pool=to_dev(prob.extra_pool), extra_slot_ids=to_dev(prob.extra_slot_ids.astype(np.int32)),
+                      snapshot_every_chunks=prob.snapshot_every_chunks)
+        every = 64 * prob.snapshot_every_chunks
+    pargs = (q, k, v, g, beta, cu, max_len, pool, slots, out)
+
+    def restore():
+        kda.kda_state_copy(ckpt, slots, pool, slots)
+
+    def make(path, seg):
+        if path == "varlen":
+            ws = torch.empty(max(kda.kda_prefill_workspace_size(*pargs, **common), 256), dtype=torch.uint8, device=dev)
+            return ws, lambda: kda.kda_prefill_varlen(*pargs, workspace=ws, dev_status=status, **common)
+        ws = torch.empty(max(kda.kda_segmented_workspace_size(*pargs, seg, **common), 256), dtype=torch.uint8,
+                         device=dev)
+        return ws, lambda: kda.kda_prefill_segmented(*pargs, seg, ws, dev_status=status, **common)
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            a.record()
+            restore()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    trial = {}
+    for path, seg in candidates:
+        ws, fn = make(path, seg)
+        timed(fn, 1)
+        trial[(path, seg)] = statistics.median(timed(fn, 2))
+        del ws, fn
+        torch.cuda.empty_cache()
+    path, seg = min(trial, key=trial.get)
+    ws, fn = make(path, seg)
+    timed(fn, max(warmup, 3))
+    status.zero_()
+    step_ms = statistics.mean(timed(fn, steps))
+    st = status.cpu().numpy()
+    if st[0] != 0 or st[1] == 0:
+        raise RuntimeError(f"{prob.name}: device status {st.tolist()} (flags set or no work done)")
+    n_snapshots = sum(min(int(n) // every, 2) for n in prob.lengths) if every else 0
+    alg = T * H * BYTES_PER_TOKEN_HEAD + 2 * N * H * STATE_BYTES + n_snapshots * H * STATE_BYTES
+    gbs = alg / (step_ms / 1e3) / 1e9
+    rep = {"tokens": T, "sequences": N, "path": path, "segment_len": seg if path == "segmented" else None,
+           "path_trial_ms": {f"{pp}/{sg}" if pp == "segmented" else pp: round(tt, 4) for (pp, sg), tt in trial.items()},
+           "steps": steps, "ms_per_step": round(step_ms, 4), "tokens_per_s": round(T / (step_ms / 1e3), 1),
+           "algorithmic_bytes": alg, "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 5),
+           "algorithmic_tflops": round(T * H * ALG_FLOP_PER_TOKEN_HEAD / (step_ms / 1e3) / 1e12, 3),
+           "l2": "inputs larger than L2 (no flush)", "step": "state restore of the N slots + prefill"}
+    if every:
+        rep["snapshot_states_written"] = n_snapshots * H
+        rep["snapshot_note"] = (f"only the last two snapshots of each sequence survive the call and only they are "
+                                f"written: {n_snapshots * H * STATE_BYTES} B; writing every one of the "
+                                f"{sum(int(n) // every for n in prob.lengths) * H} snapshot states would add "
+                                f"{(sum(int(n) // every for n in prob.lengths) - n_snapshots) * H * STATE_BYTES} B")
+    del ws, fn
+    torch.cuda.empty_cache()
+    if with_cpu:
+        rep["cpu_baseline"] = cpu_baseline(prob, sample_tokens=oracle_tokens, min_seconds=oracle_seconds,
+                                           snap_every=every)
+    return rep
+
+
+def varlen_candidates(prob, sms):
+    """The varlen path (one chain per sequence and head) and the segmented path at segment lengths around the
+    one that spreads the token-heads evenly over one CTA per SM."""
+    even = max(64, -(-int(prob.T) * prob.H // (sms * prob.H)) // 64 * 64)
+    segs = sorted({max(256, s // 64 * 64) for s in (even // 2, even, 2 * even, 4 * even)})
+    return [("varlen", 0)] + [("segmented", s) for s in segs]
+
+
 # gradient bytes per token and head of the backward: q, k, v, d_out bf16 + g, beta fp32 in; dq, dk, dv, dg, dbeta
 # fp32 out (d = 128)
 BW_BYTES_PER_TOKEN_HEAD = 4 * 256 + 512 + 4 + 4 * 512 + 4
@@ -544,24 +715,30 @@ def backward_report(kda, torch, dev, to_dev, time_calls, pk, prob):
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
 
-def cpu_baseline(prob, sample_tokens, min_seconds=10.0, max_repeats=2000):
-    """The oracle as it stands, timed on the host cores over the sample, repeated until about
-    `min_seconds` of work have been timed; value = tokens processed / seconds."""
+def cpu_baseline(prob, sample_tokens, min_seconds=10.0, max_repeats=2000, snap_every=0):
+    """The oracle as it stands, timed on the host cores over the sample (the first `sample_tokens` tokens of
+    the longest sequence), repeated until about `min_seconds` of work have been timed; value = tokens
+    processed / seconds."""
     import oracle
-    q, k, v, g, beta = (x[:sample_tokens] for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
-    s0 = prob.pool[prob.slot_ids].astype(np.float64)
+    i = int(np.argmax(prob.lengths))
+    a = int(prob.cu_seqlens[i])
+    sample_tokens = min(sample_tokens, int(prob.lengths[i]))
+    q, k, v, g, beta = (x[a:a + sample_tokens] for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    s0 = prob.pool[prob.slot_ids[i:i + 1]].astype(np.float64)
     reps = 0
     t0 = time.perf_counter()
     while True:
-        r = oracle.recurrence(q, k, v, g, beta, [0, sample_tokens], s0=s0)
+        r = oracle.recurrence(q, k, v, g, beta, [0, sample_tokens], s0=s0, snap_every=snap_every)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= min_seconds or reps >= max_repeats:
             break
     return {"value": round(reps * sample_tokens / dt, 2), "unit": "tokens/s/layer", "cores": r["threads"],
-            "kind": "oracle", "seconds": round(dt, 3), "repeats": reps,
-            "sample": f"first {sample_tokens} tokens x 12 heads of the single-request prefill workload (fp64 "
-                      f"sequential recurrence, all outputs + final state), {reps} passes in {dt:.1f} s"}
+            "cpu_model": cpu_model(), "kind": "oracle", "seconds": round(dt, 3), "repeats": reps,
+            "sample": f"first {sample_tokens} tokens x {prob.H} heads of the longest sequence of the {prob.name} workload (fp64 "
+                      f"sequential recurrence, all outputs + final state"
+                      f"{', snapshots every %d tokens' % snap_every if snap_every else ''}), {reps} passes in "
+                      f"{dt:.1f} s"}
 
 
 def run_reference(args):
@@ -597,7 +774,8 @@ def run_reference(args):
         "config": {"workload": "single-request prefill: B=1, T=8192, H=12, dk=dv=128 (bounded sample: first "
                                f"{sample} tokens per step)", "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s/layer", "cores": r["threads"],
-                         "kind": "oracle", "sample": f"first {sample} tokens x 12 heads per step"},
+                         "cpu_model": cpu_model(), "kind": "oracle",
+                         "sample": f"first {sample} tokens x 12 heads per step"},
         "e2e": {"value": round(value, 2), "unit": "tokens/s/layer", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "wall_s_timed_region": round(wall, 3),
@@ -607,6 +785,18 @@ def run_reference(args):
 
 def main():
     args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and world == 1 and "LOCAL_RANK" not in os.environ:
+        # --gpus N without a launcher: start N ranks on this node (one per GPU) and exit with their status
+        import socket
+        with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={args.gpus}",
+               "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.call(cmd))
+    if world != args.gpus:
+        sys.exit(f"bench.py: --gpus {args.gpus} but the launcher started {world} rank(s)")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -28,7 +28,8 @@
  *   to dev_status[1] (wrapping 32-bit counter; a test that sees 0 work knows it tested nothing).
  *   A slot id or accepted length out of range sets its flag; that unit is skipped without touching memory.
  * * Slot ids within one call must be distinct; a source and a destination slot of one copy must not be
- *   the same memory.  Violations are not detected and give undefined results.
+ *   the same memory.  By default violations are not detected and give undefined results; with the debug
+ *   checks on (kda_set_debug_checks below) the calls that take slot ids check this on the host first.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -67,6 +68,42 @@ int kda_version(void);
 /* Bytes of one head's state: dk*dv*4 (64 KB at dk = dv = 128, the figure the ReplaySSM section of
  * "SGLang and Miles: day-0 support for Kimi K3" gives per request, layer and head). */
 size_t kda_state_bytes_per_head(int dk, int dv);
+
+/*
+ * kda_set_test_fault -- a test hook for the kernels' bounded waits (failure detection without a GPU fault).
+ * KDA_TEST_FAULT_STALL_RECORD_INPUTS makes later kda_prefill_records calls launch the prep kernel with its
+ * input copies left out: no copy is issued, so its first wait for the inputs finds nothing to wait for,
+ * gives up after a short bounded poll, and every CTA flags KDA_DEV_TIMEOUT in dev_status and returns (its
+ * tensor memory freed, nothing in flight).  The records are then not written; nothing else is touched.
+ * KDA_TEST_FAULT_NONE (the initial value) restores normal calls.  Process-wide, not thread-safe; for tests.
+ * Returns KDA_ERR_INVALID_ARG for an unknown value.
+ */
+#define KDA_TEST_FAULT_NONE 0
+#define KDA_TEST_FAULT_STALL_RECORD_INPUTS 1
+kda_status kda_set_test_fault(int fault);
+
+/*
+ * Debug checks of the slot-id contract.  Source: "SGLang and Miles: day-0 support for Kimi K3", three
+ * state movements on the forward stream (each request owns its slot; a snapshot's target slot is never the
+ * slot it copies).
+ * kda_check_slot_ids -- HOST arrays: KDA_OK when the n ids are distinct and (other_ids not NULL) none of them
+ *   is among the n_other other_ids; KDA_ERR_INVALID_ARG otherwise or for a negative count.  Range is not
+ *   checked here (out-of-range ids are flagged on the device, KDA_DEV_SLOT_OOB).
+ * kda_set_debug_checks(on) / kda_debug_checks() -- switch / read the debug mode (process-wide; initially on
+ *   when the environment variable KDA_DEBUG_CHECKS is set to a value other than 0).  In debug mode the calls
+ *   that take slot ids (kda_state_copy, kda_decode_step, kda_verify_replay, kda_prefill_varlen,
+ *   kda_prefill_segmented, kda_cfbi_prefill, kda_cfbi_decode, kda_fused_decode) copy their ids to the host
+ *   on their stream, wait for the copy (so the call is no longer asynchronous and cannot be captured in a
+ *   CUDA graph), and return KDA_ERR_INVALID_ARG with nothing enqueued when:
+ *     - two ids of the call are equal (kda_state_copy: two destination ids; a source may feed several);
+ *     - kda_state_copy with src_pool == dst_pool: a destination id is also a source id;
+ *     - a prefill with snapshots: two extra_slot_ids are equal, or (extra_pool == pool) an extra slot is
+ *       also one of the sequences' slots.
+ *   A failed copy or wait returns KDA_ERR_CUDA.
+ */
+kda_status kda_check_slot_ids(const int32_t* ids, int32_t n, const int32_t* other_ids, int32_t n_other);
+void kda_set_debug_checks(int on);
+int kda_debug_checks(void);
 
 /*
  * kda_state_copy -- copy whole slot states: dst_pool[dst_slots[i]] = src_pool[src_slots[i]], i < n.
@@ -237,9 +274,12 @@ kda_status kda_segment_outputs(const kda_prefill_args* a, int32_t segment_len, k
  * The pages have no counterpart: this is a deployment convenience of this library.
  * Some callers cannot pass a workspace: a plugin inside an inference server that owns all device memory
  * through its own pool and offers plugins no allocation hook, or a serving loop that must not call
- * cudaMalloc after start-up.  This call takes its scratch (the fragment and entry-state arrays described
- * above) from a fixed 32 MiB array inside the library instead; a->workspace and a->workspace_bytes are
- * ignored.  Everything else (arguments, results, errors) is as for kda_prefill_segmented.
+ * cudaMalloc after start-up.  This call takes the whole workspace of kda_prefill_segmented (on the
+ * tensor-core path: the per-chunk operand records, 145 KiB per 64-token chunk and head and most of the
+ * total, then the segment fragments and the entry states, as kda_segmented_workspace_size counts them)
+ * from a fixed 32 MiB array inside the library instead; a->workspace and a->workspace_bytes are ignored.
+ * It launches the same kernels as kda_prefill_segmented (records, fragments, scan, outputs).  Everything
+ * else (arguments, results, errors) is as for kda_prefill_segmented.
  *   * A problem whose scratch (kda_segmented_workspace_size) exceeds 32 MiB returns KDA_ERR_WORKSPACE.
  *     Example: one 1024-token sequence, H = 4, d = 128 (bf16), segment_len = 256 needs about 13 MiB.
  *   * The array occupies 32 MiB of device memory on every GPU that loads this code, until the process

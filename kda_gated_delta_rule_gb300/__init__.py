@@ -22,11 +22,12 @@ __all__ = [
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
     "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "kda_fused_decode",
-    "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs", "CFBI_CHUNK",
-    "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
+    "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs", "kda_check_slot_ids", "kda_set_debug_checks",
+    "kda_debug_checks", "kda_set_test_fault", "KDA_TEST_FAULT_NONE", "KDA_TEST_FAULT_STALL_RECORD_INPUTS", "CFBI_CHUNK", "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
 ]
 
 KDA_OK = 0
+KDA_TEST_FAULT_NONE, KDA_TEST_FAULT_STALL_RECORD_INPUTS = 0, 1
 KDA_DEV_SLOT_OOB, KDA_DEV_SEQ_OOB, KDA_DEV_TIMEOUT, KDA_DEV_ACCEPT_OOB = 1, 2, 4, 8
 F32, BF16 = 0, 1
 CFBI_CHUNK, CFBI_ROW_FLOATS = 16, 420  # KDA_CFBI_CHUNK, KDA_CFBI_ROW_FLOATS
@@ -40,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
     "kda_cfbi_decode", "kda_backward_args_bytes", "kda_backward_workspace_size", "kda_prefill_backward",
     "kda_fused_decode_args_bytes", "kda_fused_decode", "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs",
+    "kda_check_slot_ids", "kda_set_debug_checks", "kda_debug_checks", "kda_set_test_fault",
 )
 
 
@@ -143,6 +145,10 @@ def load(build_if_missing: bool = False):
         "kda_kcp_fragments": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp, vp]),
         "kda_kcp_scan": (c_int, [vp, i32, c_int, c_int, c_int, vp, vp, vp, vp]),
         "kda_kcp_outputs": (c_int, [ctypes.POINTER(PrefillArgs), i32, vp, vp]),
+        "kda_check_slot_ids": (c_int, [vp, i32, vp, i32]),
+        "kda_set_debug_checks": (None, [c_int]),
+        "kda_debug_checks": (c_int, []),
+        "kda_set_test_fault": (c_int, [c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -266,6 +272,31 @@ def kda_status_string(code: int) -> str:
 
 def kda_version() -> int:
     return load().kda_version()
+
+
+def kda_check_slot_ids(ids, other_ids=None) -> int:
+    """Host-side slot-id contract check on int32 host arrays (numpy or CPU tensors): KDA_OK when the ids are
+    distinct and none is among other_ids, else the error code (include/kda.h)."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(ids), dtype=np.int32)
+    b = None if other_ids is None else np.ascontiguousarray(np.asarray(other_ids), dtype=np.int32)
+    return load().kda_check_slot_ids(a.ctypes.data if a.size else None, a.size,
+                                     None if b is None or not b.size else b.ctypes.data, 0 if b is None else b.size)
+
+
+def kda_set_debug_checks(on: bool):
+    """Switch the library's debug mode (host-side slot-id checks before every call that takes slot ids)."""
+    load().kda_set_debug_checks(1 if on else 0)
+
+
+def kda_set_test_fault(fault: int):
+    """Test hook for the kernels' bounded waits (include/kda.h): KDA_TEST_FAULT_STALL_RECORD_INPUTS makes
+    kda_prefill_records' first input wait give up and flag KDA_DEV_TIMEOUT; KDA_TEST_FAULT_NONE restores."""
+    _ok("kda_set_test_fault", load().kda_set_test_fault(int(fault)))
+
+
+def kda_debug_checks() -> bool:
+    return bool(load().kda_debug_checks())
 
 
 def kda_state_bytes_per_head(dk: int, dv: int) -> int:

@@ -3,11 +3,14 @@
 #include <stdint.h>
 
 #include "../../include/kda.h"
+#include "debug_checks.h"
 #include "launch.h"
 
 namespace {
 
 constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+
+int g_test_fault = KDA_TEST_FAULT_NONE;  // kda_set_test_fault
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool dtype_ok(kda_dtype t) { return t == KDA_DTYPE_F32 || t == KDA_DTYPE_BF16; }
@@ -152,6 +155,16 @@ kda_status varlen_prepare(const kda_prefill_args* a, kda::PrefillArgs* p) {
   return KDA_OK;
 }
 
+// Debug mode: sequences own distinct slots, snapshots go to distinct extra slots, and (one pool for both)
+// no snapshot lands in a slot a sequence reads or writes.
+kda_status prefill_debug_check(const kda_prefill_args* a, cudaStream_t s) {
+  kda_status st = kda::debug_check_slots(a->slot_ids, a->N, nullptr, 0, s);
+  if (st != KDA_OK || !a->extra_pool || a->snapshot_every_chunks <= 0) return st;
+  st = kda::debug_check_slots(a->extra_slot_ids, 2 * a->N, nullptr, 0, s);
+  if (st != KDA_OK || a->extra_pool != a->pool) return st;
+  return kda::debug_check_slots(a->slot_ids, a->N, a->extra_slot_ids, 2 * a->N, s);
+}
+
 cudaError_t run_outputs(const kda::PrefillArgs& p, cudaStream_t s) {
   return p.records ? kda::launch_tc_chain_segout(p, p.records, s) : kda::launch_seg_outputs(p, s);
 }
@@ -173,6 +186,12 @@ const char* kda_status_string(kda_status s) {
 
 int kda_version(void) { return kVersion; }
 
+kda_status kda_set_test_fault(int fault) {
+  if (fault != KDA_TEST_FAULT_NONE && fault != KDA_TEST_FAULT_STALL_RECORD_INPUTS) return KDA_ERR_INVALID_ARG;
+  g_test_fault = fault;
+  return KDA_OK;
+}
+
 size_t kda_state_bytes_per_head(int dk, int dv) { return (dk > 0 && dv > 0) ? (size_t)dk * dv * 4 : 0; }
 
 kda_status kda_state_copy(const float* src_pool, int32_t src_num_slots, const int32_t* src_slots, float* dst_pool,
@@ -184,8 +203,12 @@ kda_status kda_state_copy(const float* src_pool, int32_t src_num_slots, const in
   if (!src_pool || !dst_pool || !src_slots || !dst_slots) return KDA_ERR_INVALID_ARG;
   if (!aligned16(src_pool) || !aligned16(dst_pool) || !aligned16(src_slots) || !aligned16(dst_slots))
     return KDA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // debug mode: destinations distinct; within one pool, no destination is also a source
+  kda_status dbg = kda::debug_check_slots(dst_slots, n, src_pool == dst_pool ? src_slots : nullptr, n, s);
+  if (dbg != KDA_OK) return dbg;
   kda::CopyArgs c{src_pool, src_num_slots, src_slots, dst_pool, dst_num_slots, dst_slots, n, state_elems, dev_status};
-  return from_cuda(kda::launch_state_copy(c, reinterpret_cast<cudaStream_t>(stream)));
+  return from_cuda(kda::launch_state_copy(c, s));
 }
 
 kda_status kda_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta, int B,
@@ -199,6 +222,8 @@ kda_status kda_decode_step(const void* q, const void* k, const void* v, const fl
   const void* ptrs[] = {q, k, v, g, beta, pool, slot_ids, out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda_status dbg = kda::debug_check_slots(slot_ids, B, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (dbg != KDA_OK) return dbg;
   kda::DecodeArgs a{q,    k,         v,        g,   beta,      B, H, dk, in_dtype == KDA_DTYPE_BF16,
                     out_dtype == KDA_DTYPE_BF16, pool, num_slots, slot_ids, out, dev_status};
   return from_cuda(kda::launch_decode(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -242,6 +267,8 @@ kda_status kda_verify_replay(float* pool, int32_t num_slots, const int32_t* slot
     if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
   const ReplayLayout L = replay_layout(B, W, H, dk, dv, in_dtype);
   if (replay_bytes < L.total) return KDA_ERR_WORKSPACE;
+  kda_status dbg = kda::debug_check_slots(slot_ids, B, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (dbg != KDA_OK) return dbg;
   kda::FoldArgs a{pool, num_slots, slot_ids, B, W, H, dk, in_dtype == KDA_DTYPE_BF16,
                   replay_ptrs(const_cast<void*>(replay), L), accepted_len, dev_status};
   return from_cuda(kda::launch_fold(a, reinterpret_cast<cudaStream_t>(stream)));
@@ -258,6 +285,8 @@ kda_status kda_prefill_varlen(const kda_prefill_args* a, kda_stream_t stream) {
   kda::PrefillArgs p;
   kda_status st = varlen_prepare(a, &p);
   if (st != KDA_OK || a->N == 0) return st;
+  st = prefill_debug_check(a, reinterpret_cast<cudaStream_t>(stream));
+  if (st != KDA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!p.records) return from_cuda(kda::launch_prefill_seq(p, s));
   cudaError_t e = kda::launch_tc_prep(p, p.records, s);
@@ -269,6 +298,7 @@ kda_status kda_prefill_records(const kda_prefill_args* a, kda_stream_t stream) {
   kda::PrefillArgs p;
   kda_status st = varlen_prepare(a, &p);
   if (st != KDA_OK || a->N == 0 || !p.records) return st;
+  p.test_stall_inputs = g_test_fault == KDA_TEST_FAULT_STALL_RECORD_INPUTS;
   return from_cuda(kda::launch_tc_prep(p, p.records, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -311,6 +341,8 @@ kda_status kda_prefill_segmented(const kda_prefill_args* a, int32_t segment_len,
   kda::PrefillArgs p;
   kda_status st = seg_prepare(a, segment_len, &p);
   if (st != KDA_OK || a->N == 0) return st;
+  st = prefill_debug_check(a, reinterpret_cast<cudaStream_t>(stream));
+  if (st != KDA_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = p.records ? kda::launch_tc_prep(p, p.records, s) : cudaSuccess;
   if (e == cudaSuccess) e = run_fragments(p, s);
@@ -341,6 +373,8 @@ kda_status kda_cfbi_prefill(const void* q, const void* k, const void* v, const f
     for (const void* p : tp)
       if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
   }
+  kda_status dbg = kda::debug_check_slots(slot_ids, N, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (dbg != KDA_OK) return dbg;
   kda::CfbiArgs a{q,   k,    v,     g,     beta,  0,         N,        T,     max_seqlen,
                   cu_seqlens, H, in_dtype == KDA_DTYPE_BF16, out_dtype == KDA_DTYPE_BF16, pool, cache, counts,
                   num_slots,   slot_ids,  out,   dev_status};
@@ -358,6 +392,8 @@ kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const fl
   const void* ptrs[] = {q, k, v, g, beta, pool, cache, counts, slot_ids, out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda_status dbg = kda::debug_check_slots(slot_ids, B, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (dbg != KDA_OK) return dbg;
   kda::CfbiArgs a{q,       k,        v,    g,        beta, B,         0,  0,         0,
                   nullptr, H, in_dtype == KDA_DTYPE_BF16, out_dtype == KDA_DTYPE_BF16, pool, cache, counts,
                   num_slots, slot_ids, out,  dev_status};
@@ -439,6 +475,8 @@ kda_status kda_fused_decode(const kda_fused_decode_args* a, kda_stream_t stream)
                         a->norm_w, a->out};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  kda_status dbg = kda::debug_check_slots(a->slot_ids, a->B, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (dbg != KDA_OK) return dbg;
   kda::FusedDecodeArgs f{};
   f.xq = a->xq;
   f.xk = a->xk;

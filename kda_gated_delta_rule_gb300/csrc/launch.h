@@ -95,6 +95,9 @@ struct PrefillArgs {
   bool frag_all;
   int scan_nseg;
   const float* scan_s0;
+  // test hook (kda_set_test_fault): the prep kernel issues no input copies and waits for them with a short
+  // poll limit, so its first wait gives up and the kernel reports KDA_DEV_TIMEOUT; 0 in normal calls
+  int test_stall_inputs;
 };
 
 // Batch-invariant (CF-BI) prefill and decode (d = 128).

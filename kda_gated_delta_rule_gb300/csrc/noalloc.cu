@@ -3,8 +3,11 @@
 // Some callers cannot hand this library a workspace: a plugin inside an inference server that owns all
 // device memory through its own pool and gives plugins no allocation hook, or a serving loop that may
 // not call cudaMalloc after start-up (cudaMalloc can synchronise the device and its latency is not
-// bounded).  kda_prefill_segmented_noalloc serves them: it runs the same three kernels as
-// kda_prefill_segmented, with the fragment and entry-state scratch taken from the fixed array below.
+// bounded).  kda_prefill_segmented_noalloc serves them: it runs exactly the kernels of
+// kda_prefill_segmented (on the tensor-core path four: operand records, fragments, scan, outputs), with
+// that call's whole workspace taken from the fixed array below.  The workspace is laid out as
+// [per-chunk operand records][segment fragments][entry states] (kda_segmented_workspace_size); the
+// records, 145 KiB per 64-token chunk and head, are most of it.
 //
 // The array is 32 MiB.  Every GPU that loads this code holds it until the process exits.  Calls share
 // it and it keeps the last call's contents; nothing in it needs to start at zero (every byte the kernels

@@ -155,9 +155,9 @@ __device__ __forceinline__ void bar_arrive(uint64_t* bar) {
 
 // Waits for the phase with the given parity to complete; gives up after a bounded number of polls and
 // returns false (the caller reports a timeout instead of hanging).
-__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity, uint32_t max_polls = 1u << 22) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t it = 0; it < (1u << 22); ++it) {
+  for (uint32_t it = 0; it < max_polls; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"

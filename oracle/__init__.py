@@ -308,6 +308,10 @@ def short_conv_step(x, conv_state, w):
 def fused_decode(pool, conv_state, slot_ids, xq, xk, xv, a, b, z, conv_w, norm_w, eps, threads=0):
     """One decode token per request through the short convolution, the KDA step and the gated output norm.
 
+    The pages print no formula for the convolution, the normalisations or the gates; what follows is the
+    plainest reading, pinned by its properties (stepwise = full causal convolution, the read-back identity
+    through the composed path, unit rms and scale invariance of the output norm, the gates' limits and
+    midpoints checked through the state and the output) rather than by a second copy of the expressions.
     Reading of "SGLang and Miles: day-0 support for Kimi K3" (kernels: the fused Conv + KDA + Onorm decode
     kernel), "Kimi K3: Architecture and SGLang Day-0 Support" (KDA math box: the log-decay kept above
     g_min = -5 by a scaled sigmoid; the output gate a full-rank projection of the input) and "Kimi K3

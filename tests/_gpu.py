@@ -101,3 +101,13 @@ def expected_extra_pool(prob: synth.Prefill, ref) -> np.ndarray:
         for m in range(1, len(snaps) + 1):
             extra[prob.extra_slot_ids[i, (m - 1) & 1]] = snaps[m - 1]
     return extra
+
+
+def prefix_problem(prob, i: int, ntok: int):
+    """Sequence i of `prob` cut to its first ntok tokens, alone in the batch, from the same initial state
+    (same pool and slot), with no snapshots."""
+    a = int(prob.cu_seqlens[i])
+    sl = lambda x: np.ascontiguousarray(x[a:a + ntok])
+    return synth.Prefill("prefix", prob.seed, prob.H, prob.dk, prob.dv, prob.in_dtype, sl(prob.q), sl(prob.k),
+                         sl(prob.v), sl(prob.g), sl(prob.beta), np.array([0, ntok], np.int32), prob.pool,
+                         prob.slot_ids[i:i + 1].copy(), init_zero=prob.init_zero)

@@ -113,3 +113,35 @@ def test_library_fails_loudly_when_missing(tmp_path, monkeypatch):
     monkeypatch.setattr(kda, "_lib", None)
     with pytest.raises(RuntimeError):
         kda.load()
+
+
+def test_slot_id_contract_check_on_the_host(lib):
+    """kda_check_slot_ids (host arrays): distinct ids pass; a repeated id, or an id shared with the other set
+    (a copy whose destination is also its source, a snapshot into a sequence's own slot), is rejected."""
+    import numpy as np
+    ok, bad = kda.KDA_OK, 1  # KDA_ERR_INVALID_ARG
+    assert kda.kda_check_slot_ids(np.array([3, 0, 7, 1])) == ok
+    assert kda.kda_check_slot_ids(np.array([], np.int32)) == ok
+    assert kda.kda_check_slot_ids(np.array([3, 0, 7, 3])) == bad
+    assert kda.kda_check_slot_ids(np.array([5, 6]), other_ids=np.array([1, 2, 3])) == ok
+    assert kda.kda_check_slot_ids(np.array([5, 6]), other_ids=np.array([1, 6, 3])) == bad
+    # out-of-range ids are the device's to flag (KDA_DEV_SLOT_OOB), not this check's
+    assert kda.kda_check_slot_ids(np.array([-1, 10 ** 6])) == ok
+    assert lib.kda_check_slot_ids(None, -1, None, 0) == bad
+
+
+def test_debug_checks_switch(lib):
+    was = kda.kda_debug_checks()
+    try:
+        kda.kda_set_debug_checks(True)
+        assert kda.kda_debug_checks() is True
+        kda.kda_set_debug_checks(False)
+        assert kda.kda_debug_checks() is False
+    finally:
+        kda.kda_set_debug_checks(was)
+
+
+def test_test_fault_hook_values(lib):
+    assert lib.kda_set_test_fault(99) == 1  # unknown value: KDA_ERR_INVALID_ARG
+    assert lib.kda_set_test_fault(kda.KDA_TEST_FAULT_STALL_RECORD_INPUTS) == 0
+    assert lib.kda_set_test_fault(kda.KDA_TEST_FAULT_NONE) == 0

@@ -67,3 +67,18 @@ def test_cpu_baseline_object():
     # seconds is reported to the millisecond (>= 0.5 s timed): the value agrees to 0.2 %
     assert abs(cb["value"] - cb["repeats"] * 256 / cb["seconds"]) <= 2e-3 * cb["value"]
     assert f"{cb['repeats']} passes" in cb["sample"]
+
+
+def test_traffic_table_follows_the_kernel_sources(tmp_path):
+    """A traffic row counts only while the kernel's sources hash to the value recorded at capture time."""
+    sys.path.insert(0, ROOT)
+    import bench
+    files = "copy.cu,common.cuh"
+    sha = bench.source_sha256(files.split(","))
+    table = tmp_path / "t.txt"
+    table.write_text("# header\n" + "\t".join(["state_copy_kernel", "w", files, sha, "100", "23", "cmd"]) + "\n" +
+                     "\t".join(["stale_kernel", "w", files, "0" * 64, "5", "5", "cmd"]) + "\n")
+    assert bench.measured_traffic("state_copy_kernel", "w", str(table)) == 123
+    assert bench.measured_traffic("stale_kernel", "w", str(table)) is None   # sources changed since the capture
+    assert bench.measured_traffic("state_copy_kernel", "other", str(table)) is None
+    assert bench.measured_traffic("missing", "w", str(tmp_path / "none.txt")) is None

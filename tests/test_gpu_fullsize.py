@@ -12,7 +12,7 @@ import pytest
 import torch
 
 import synth
-from tests._gpu import PrefillRun, expected_extra_pool, host, oracle_prefill, rel_err, status
+from tests._gpu import PrefillRun, expected_extra_pool, host, oracle_prefill, prefix_problem, rel_err, status
 
 pytestmark = pytest.mark.gpu
 
@@ -54,6 +54,14 @@ def test_varlen_full(cuda):
     exp = expected_extra_pool(prob, ref)
     used = np.unique(prob.extra_slot_ids.ravel())
     assert rel_err(host(run.extra)[used], exp[used]) <= TOL
+    # the latest snapshot of the longest sequence is, bit for bit, the final state of a prefill of that prefix
+    i = int(np.argmax(prob.lengths))
+    every = prob.snapshot_every_chunks * 64
+    m = int(prob.lengths[i]) // every
+    pre = PrefillRun(prefix_problem(prob, i, m * every)).run_varlen(cuda)
+    assert status(pre.status)[0] == 0
+    want = pre.pool[int(prob.slot_ids[i])]
+    assert torch.equal(run.extra[int(prob.extra_slot_ids[i, (m - 1) & 1])], want)
 
 
 @pytest.mark.slow

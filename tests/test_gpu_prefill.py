@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import synth
-from tests._gpu import PrefillRun, bf16_bits, dev, expected_extra_pool, host, oracle_prefill, rel_err, status
+from tests._gpu import (PrefillRun, bf16_bits, dev, expected_extra_pool, host, oracle_prefill, prefix_problem, rel_err,
+                        status)
 
 pytestmark = pytest.mark.gpu
 
@@ -208,3 +209,45 @@ def test_bad_cu_seqlens_flagged(cuda):
     flags, work = status(run.status)
     assert flags & kda.KDA_DEV_SEQ_OOB
     assert torch.equal(run.pool[int(prob.slot_ids[1])], pool0[int(prob.slot_ids[1])])
+
+
+SNAP_EXACT_CASES = [
+    # tcgen05 chunk path (bf16, d = 128) and the token-sequential path (fp32 or d < 128); every sequence but
+    # one has a length that is a multiple of the snapshot interval, so its last snapshot is its final state
+    dict(d=128, dtype=synth.BF16, lengths=[512, 300, 1024, 128], snap=2, H=2),
+    dict(d=64, dtype=synth.F32, lengths=[256, 200, 448], snap=1, H=2),
+    dict(d=32, dtype=synth.BF16, lengths=[384, 576, 200, 64], snap=3, H=2),
+]
+
+
+@pytest.mark.parametrize("case", SNAP_EXACT_CASES, ids=_vid)
+@pytest.mark.parametrize("path", ["varlen", "segmented"])
+def test_snapshots_bit_exact(cuda, case, path):
+    """Each snapshot the prefill leaves in the ping-pong pool is, bit for bit, the final state of a prefill
+    of exactly that prefix (m x interval tokens) on the same path (same segment length); for a sequence
+    whose length is a multiple of the interval, the last snapshot equals its final pool state byte for
+    byte.  Snapshots are copies of the carried state ("SGLang and Miles: day-0 support for Kimi K3", three
+    state movements on the forward stream), so no tolerance applies."""
+    seg = 192
+    prob = _varlen(case, seed=38)
+    full = PrefillRun(prob)
+    full = full.run_varlen(cuda) if path == "varlen" else full.run_segmented(cuda, seg)
+    assert status(full.status)[0] == 0
+    every = case["snap"] * 64
+    extra = full.extra.cpu().numpy()
+    pool = full.pool.cpu().numpy()
+    checked = 0
+    for i, n in enumerate(prob.lengths):
+        n_snap = int(n) // every
+        for m in range(max(1, n_snap - 1), n_snap + 1):  # the two snapshots that survive the call
+            pre = PrefillRun(prefix_problem(prob, i, m * every))
+            pre = pre.run_varlen(cuda) if path == "varlen" else pre.run_segmented(cuda, seg)
+            assert status(pre.status)[0] == 0
+            want = pre.pool.cpu().numpy()[prob.slot_ids[i]]
+            got = extra[prob.extra_slot_ids[i, (m - 1) & 1]]
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), f"seq {i} snapshot {m}"
+            checked += 1
+        if n_snap and int(n) % every == 0:
+            last = extra[prob.extra_slot_ids[i, (n_snap - 1) & 1]]
+            assert np.array_equal(last.view(np.uint32), pool[prob.slot_ids[i]].view(np.uint32)), f"seq {i}"
+    assert checked == sum(min(int(n) // every, 2) for n in prob.lengths) > 0

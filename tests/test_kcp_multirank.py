@@ -28,19 +28,28 @@ def _problem():
 
 
 class OracleOps:
-    """The per-rank compute of KCP by the fp64 oracle (test stand-in for the GPU kernels)."""
+    """The per-rank compute of KCP by the fp64 oracle (test stand-in for the GPU kernels), with the shard cut
+    into segments of `seg` tokens like LibraryOps."""
 
-    def __init__(self, shard):
+    def __init__(self, shard, seg):
         self.shard = shard
+        L = shard["q"].shape[0]
+        self.bounds = list(range(0, L, seg)) + [L]
         self.out = self.final = None
+
+    def _seg(self, p):
+        return {n: x[self.bounds[p]:self.bounds[p + 1]] for n, x in self.shard.items()}
 
     def fragments(self):
         import oracle
-        s = self.shard
-        L = s["q"].shape[0]
-        zero = oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], [0, L])["s_final"][0]
-        M = oracle.transition(s["k"], s["g"], s["beta"], [0, L])[0]
-        return torch.from_numpy(np.concatenate([zero, M], axis=-1))  # [H, d, 2d]: S~ | M
+        out = []
+        for p in range(len(self.bounds) - 1):
+            s = self._seg(p)
+            L = s["q"].shape[0]
+            zero = oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], [0, L])["s_final"][0]
+            M = oracle.transition(s["k"], s["g"], s["beta"], [0, L])[0]
+            out.append(np.concatenate([zero, M], axis=-1))  # [H, d, 2d]: S~ | M
+        return torch.from_numpy(np.stack(out))
 
     def scan(self, frags, s0):
         f = frags.numpy()
@@ -50,12 +59,16 @@ class OracleOps:
             e.append(np.einsum("hij,hjc->hic", f[p, :, :, d:], e[-1]) + f[p, :, :, :d])
         return torch.from_numpy(np.stack(e))
 
-    def outputs(self, entry):
+    def outputs(self, entries):
         import oracle
-        s = self.shard
-        r = oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], [0, s["q"].shape[0]],
-                              s0=entry.numpy()[None])
-        self.out, self.final = r["o"], r["s_final"][0]
+        outs = []
+        for p in range(len(self.bounds) - 1):  # each segment from its own entry state
+            s = self._seg(p)
+            r = oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], [0, s["q"].shape[0]],
+                                  s0=entries[p].numpy()[None])
+            outs.append(r["o"])
+            self.final = r["s_final"][0]
+        self.out = np.concatenate(outs)
 
 
 def _rank(rank, world, port, q):
@@ -63,12 +76,14 @@ def _rank(rank, world, port, q):
     sys.path.insert(0, ROOT)
     import torch.distributed as dist
 
-    from kda_gated_delta_rule_gb300.kcp import kcp_prefill, shard_bounds
+    from kda_gated_delta_rule_gb300.kcp import kcp_prefill, kcp_segment_len, shard_bounds
 
     dist.init_process_group("gloo", rank=rank, world_size=world)
     full, s0 = _problem()
-    b = shard_bounds(full["q"].shape[0], world)
-    ops = OracleOps({n: x[b[rank]:b[rank + 1]] for n, x in full.items()})
+    T = full["q"].shape[0]
+    b = shard_bounds(T, world)
+    seg = kcp_segment_len(T, world, 3)  # 75-token shards: two segments of 64 and 11 tokens each
+    ops = OracleOps({n: x[b[rank]:b[rank + 1]] for n, x in full.items()}, seg)
     entries = kcp_prefill(ops, torch.from_numpy(s0))
     q.put((rank, entries.numpy(), ops.out, ops.final))
     dist.destroy_process_group()
@@ -116,3 +131,15 @@ def test_shard_bounds_cover_the_sequence_evenly():
             sizes = np.diff(b)
             assert len(b) == world + 1 and b[0] == 0 and b[-1] == T
             assert sizes.min() >= 1 and sizes.max() - sizes.min() <= 1
+
+
+def test_common_segment_length_gives_every_rank_the_same_count():
+    sys.path.insert(0, ROOT)
+    from kda_gated_delta_rule_gb300.kcp import kcp_segment_len, shard_bounds
+    for T in (150, 8192, 8193, 64 * 24 + 1, 1 << 20, 1_048_579):
+        for world in (1, 2, 3, 8):
+            for per_rank in (1, 3, 12):
+                seg = kcp_segment_len(T, world, per_rank)
+                assert seg % 64 == 0
+                counts = {-(-int(n) // seg) for n in np.diff(shard_bounds(T, world))}
+                assert len(counts) == 1
