@@ -39,29 +39,24 @@ constexpr int C = 64;   // chunk length
 constexpr int D = 128;  // dk = dv
 constexpr float SPAN_MAX = 80.f;
 
-// workspace record of one (chunk, head); the first REC_STAGE bytes are the chain's shared-memory stage
-constexpr uint32_t REC_B1HI = 0;        // [128 rows (W: 0..63, Q o gamma: 64..127)][K = 128], two 16 KB K-blocks
-constexpr uint32_t REC_B1LO = 32768;
-constexpr uint32_t REC_PHI = 65536;     // P [64 t][K = 64 s]
-constexpr uint32_t REC_PLO = 73728;
-constexpr uint32_t REC_KHHI = 81920;    // (K o exp(G_C - G))^T [128 j][K = 64 s]
-constexpr uint32_t REC_KHLO = 98304;
+// workspace record of one (chunk, head); the first REC_STAGE bytes are the chain's shared-memory stage and
+// the first REC_FRAG bytes all the fragment mode reads of it.  Tiles are 128-byte swizzled bf16 (hi, lo).
+constexpr uint32_t REC_WHI = 0;         // W^T [128 j][64 t]: MN-major B of (W S)^T (n = t, k = j)
+constexpr uint32_t REC_WLO = 16384;
+constexpr uint32_t REC_KHI = 32768;     // K^ = K o exp(G_C - G) [64 s][128 j] as two [64][64] blocks (j 0..63,
+constexpr uint32_t REC_KLO = 49152;     // 64..127), 8 KB apart: MN-major B of the state update (n = j, k = s)
+constexpr uint32_t REC_FRAG = 65536;
+constexpr uint32_t REC_QHI = 65536;     // Q o gamma [64 t][128 j] as two 8 KB blocks: K-major B of (Q^ S)^T
+constexpr uint32_t REC_QLO = 81920;
+constexpr uint32_t REC_PHI = 98304;     // P [64 t][64 s]: K-major B of (P U)^T
+constexpr uint32_t REC_PLO = 106496;
 constexpr uint32_t REC_STAGE = 114688;
-constexpr uint32_t REC_U = 114688;      // U~ [64 t][128 c] fp32, row t's 16-byte chunk q stored at q ^ (t % 8)
+constexpr uint32_t REC_U = 114688;      // U~ [64 t][128 c] fp32, row-major
 constexpr uint32_t REC_GAMMA = 147456;  // gamma_C [128] fp32
 constexpr uint32_t REC_BYTES = 148480;
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-__device__ __forceinline__ uint4 pack8(const __nv_bfloat16* v) {
-  uint4 r;
-  r.x = tc::pack2(v[0], v[1]);
-  r.y = tc::pack2(v[2], v[3]);
-  r.z = tc::pack2(v[4], v[5]);
-  r.w = tc::pack2(v[6], v[7]);
-  return r;
 }
 
 __device__ __forceinline__ void unpack8(uint4 r, float* x) {
@@ -76,33 +71,36 @@ __device__ __forceinline__ void unpack8(uint4 r, float* x) {
 // ---------------------------------------------------------------- prep
 
 // shared-memory layout of the prep kernel (offsets from a 1024-aligned base)
-constexpr uint32_t PS_XHI = 0;          // X [128][128] bf16: (K; Q) o exp(G_t - G_ref), hi then lo
+// X [128 rows][128 channels] bf16, hi then lo: rows 0..63 K o exp(G - G_ref), rows 64..127 Q o exp(G - G_ref);
+// channel block kb (64 channels) at kb * PS_XBLK, row r of a block at r * 128 bytes (128-byte swizzle).
+constexpr uint32_t PS_XHI = 0;
 constexpr uint32_t PS_XLO = 32768;
-// once the Gram product has completed, the X region is reused for:
+constexpr uint32_t PS_XBLK = 16384;
+// Once the Gram product has completed the Q rows of X are dead: T diag(beta) hi and lo go to the Q rows of the
+// two channel blocks of X hi, and the P record tile (hi, lo) is staged in those of X lo.  The K rows stay: in
+// the common case (reference token = chunk end) they hold K o exp(G - G_C), after the block-referenced Gram
+// they are rebuilt as K o gamma, and either way they are the A operand (MN-major) of W^T.
+constexpr uint32_t PS_TBHI = PS_XHI + 8192;
+constexpr uint32_t PS_TBLO = PS_XHI + PS_XBLK + 8192;
+constexpr uint32_t PS_PHI = PS_XLO + 8192;
+constexpr uint32_t PS_PLO = PS_XLO + PS_XBLK + 8192;
+constexpr uint32_t PS_YHI = 65536;      // Y [64][128] bf16 (hi, lo; blocks of 8 KB): K o exp(G_ref - G).  In the
+constexpr uint32_t PS_YLO = 81920;      // common case it is the record's K^ tile as it stands.
 constexpr int LT = 68;                  // row stride (floats) of A and T: 8 consecutive rows, 8 bank groups
-constexpr uint32_t PS_A = 0;            // A [64][LT] fp32 (beta folded in, strictly lower)
-constexpr uint32_t PS_T = 64 * LT * 4;  // T = (I + A)^-1 [64][LT] fp32 (upper blocks: scratch); its last 2 KB
-                                        // overlap T diag(beta), which is written from registers after T is read
-constexpr uint32_t PS_TBHI = 32768;     // T diag(beta) [64 t][K = 64 s] bf16, hi then lo
-constexpr uint32_t PS_TBLO = 40960;
-constexpr uint32_t PS_VT = 49152;       // V^T [128 c][K = 64 s] bf16
-constexpr uint32_t PS_YHI = 65536;      // Y [64][128] bf16: K o exp(G_ref - G_s), hi then lo
-constexpr uint32_t PS_YLO = 81920;
-constexpr uint32_t PS_KPHI = 98304;     // (K o gamma)^T [128 j][K = 64 s] bf16, hi then lo
-constexpr uint32_t PS_KPLO = 114688;
-// after the Gram product the dead regions stage record tiles for bulk stores: P hi and lo in the raw q
-// region, (K o exp(G_C - G))^T hi and lo in the Y region; after the W / U~ product, W hi and lo rows in the
-// first 32 KB (A and T) and U~ in the next 32 KB (T diag(beta), V^T).  The raw k, q, v, g regions are free
-// once the A / P epilogue is done: the next task's inputs land there while this task finishes.
-constexpr uint32_t PS_K = 131072;       // raw k [64][128] bf16
-constexpr uint32_t PS_Q = 147456;       // raw q [64][128] bf16
-constexpr uint32_t PS_V = 163840;       // raw v [64][128] bf16
-constexpr uint32_t PS_G = 180224;       // g, then G (in place) [64][128] fp32
-constexpr uint32_t PS_BETA = 212992;    // beta [2][64], double-buffered by task parity
-constexpr uint32_t PS_BAR = 213760;     // three mbarriers: inputs, Gram product, W/U products
-constexpr uint32_t PS_SLOT = 213784;
-constexpr uint32_t PS_NEXT = 213800;    // the task after next (looked up by the duty thread): index, n, h, i, t0
-constexpr uint32_t PS_BYTES = 213824 + 1024;
+constexpr uint32_t PS_A = 98304;        // A [64][LT] fp32 (beta folded in, strictly lower)
+constexpr uint32_t PS_T = PS_A + 64 * LT * 4;  // T = (I + A)^-1 [64][LT] fp32 (upper blocks: scratch)
+constexpr uint32_t PS_WHI = PS_A;       // after T diag(beta) is built, A and T are dead: W^T staging (hi, lo)
+constexpr uint32_t PS_WLO = PS_A + 16384;
+constexpr uint32_t PS_K = 133120;       // raw k [64][128] bf16
+constexpr uint32_t PS_Q = 149504;       // raw q [64][128] bf16
+constexpr uint32_t PS_G = 165888;       // g, then G (in place) [64][128] fp32
+constexpr uint32_t PS_V = 198656;       // raw v as two [64 t][64 c] 128-byte-swizzled blocks: MN-major A of U~^T
+constexpr uint32_t PS_BETA = 215040;    // beta [2][64], double-buffered by task parity
+constexpr uint32_t PS_BAR = 215552;     // mbarriers: Gram product, W/U products, inputs (k, q, g, beta), v
+constexpr uint32_t PS_SLOT = 215584;
+constexpr uint32_t PS_NEXT = 215592;    // the task after next (looked up by the duty thread): index, n, h, i, t0
+constexpr uint32_t PS_BYTES = 215616 + 1024;
+static_assert(PS_T + 64 * LT * 4 <= PS_K, "prep shared memory");
 constexpr int PREP_NT = 512;
 constexpr int PREP_PARTS = PREP_NT / D;  // threads per channel in the per-channel phases
 
@@ -122,39 +120,20 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-// X rows r = 0..127 (K part, then Q part) for decay reference ref_row; rows t < row_min are zero.
-__device__ __forceinline__ void build_x_chunk(uint8_t* sm, int r, int cc, int ref_row, int row_min) {
-  const int t = r & 63;
-  float v[8];
-  if (t < row_min) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = 0.f;
-  } else {
-    const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(sm + (r < 64 ? PS_K : PS_Q));
-    const float* G = reinterpret_cast<const float*>(sm + PS_G);
-    float gt[8], gr[8];
-    unpack8(*reinterpret_cast<const uint4*>(src + t * D + cc * 8), v);
-    load8f(G + t * D + cc * 8, gt);
-    load8f(G + ref_row * D + cc * 8, gr);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] *= __expf(gt[e] - gr[e]);
-  }
-  const uint32_t off = (uint32_t)(cc >> 3) * 16384u + tc::sw128_chunk(r, cc & 7);
-  split8_store(sm + PS_XHI + off, sm + PS_XLO + off, v);
-}
+// offset of the 16-byte chunk cc (channels 8cc..8cc+7) of row r in X (r < 128) or Y (r < 64)
+__device__ __forceinline__ uint32_t x_off(int r, int cc) { return (uint32_t)(cc >> 3) * PS_XBLK + tc::sw128_chunk(r, cc & 7); }
+__device__ __forceinline__ uint32_t y_off(int r, int cc) { return (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(r, cc & 7); }
 
-// Y row s (key s rescaled to reference token ref_row), 16-byte chunk cc.
-__device__ __forceinline__ void build_y_chunk(uint8_t* sm, int s, int cc, int ref_row) {
-  const __nv_bfloat16* K = reinterpret_cast<const __nv_bfloat16*>(sm + PS_K);
+// 8 channels (chunk cc) of raw row t of k or q, times exp(G_t - G_ref) (sign = +1) or exp(G_ref - G_t)
+__device__ __forceinline__ void decayed8(const uint8_t* sm, uint32_t src, int t, int cc, int ref_row, float sign,
+                                         float* v) {
   const float* G = reinterpret_cast<const float*>(sm + PS_G);
-  float v[8], gs[8], gr[8];
-  unpack8(*reinterpret_cast<const uint4*>(K + s * D + cc * 8), v);
-  load8f(G + s * D + cc * 8, gs);
+  float gt[8], gr[8];
+  unpack8(*reinterpret_cast<const uint4*>(sm + src + (uint32_t)(t * D + cc * 8) * 2u), v);
+  load8f(G + t * D + cc * 8, gt);
   load8f(G + ref_row * D + cc * 8, gr);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) v[e] *= __expf(gr[e] - gs[e]);
-  const uint32_t off = (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(s, cc & 7);
-  split8_store(sm + PS_YHI + off, sm + PS_YLO + off, v);
+  for (int e = 0; e < 8; ++e) v[e] *= __expf(sign * (gt[e] - gr[e]));
 }
 
 // D[:, col0 : col0 + N] = X Y[row0 : row0 + N]^T with the three split products (A, B from shared memory).
@@ -167,36 +146,39 @@ __device__ __forceinline__ void issue_gram(uint8_t* sm, uint32_t d_tmem, int row
     const uint32_t yb = base + (part == 1 ? PS_YLO : PS_YHI) + (uint32_t)row0 * 128u;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+      const uint32_t koff = (uint32_t)(ks >> 2) * PS_XBLK + (uint32_t)(ks & 3) * 32u;
       const uint32_t koff_y = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
       tc::mma_ss(d_tmem, tc::sdesc(xa + koff), tc::sdesc(yb + koff_y), idesc, (part | ks) != 0);
     }
   }
 }
 
-// [W | U~] = T diag(beta) [K o gamma | V]: M = 64 rows t, N = 128, K = 64 tokens s.
-__device__ __forceinline__ void issue_wu(uint8_t* sm, uint32_t tm) {
+// W^T (tensor memory columns d_w ..) = X_K^T (T diag(beta))^T and U~^T (columns d_u ..) = V^T (T diag(beta))^T:
+// M = 128 channels, N = 64 tokens t, K = 64 tokens s; X_K and V are MN-major A operands read in place.
+__device__ __forceinline__ void issue_wu(uint8_t* sm, uint32_t d_w, uint32_t d_u) {
   const uint32_t base = tc::smem_u32(sm);
-  const uint32_t idesc = tc::idesc_bf16(64, 128);
+  constexpr uint32_t idesc = tc::idesc_bf16(128, 64) | tc::IDESC_A_MN;
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
-    const uint32_t ta = base + (part == 2 ? PS_TBLO : PS_TBHI);
-    const uint32_t kb = base + (part == 1 ? PS_KPLO : PS_KPHI);
+    const uint32_t xa = base + (part == 2 ? PS_XLO : PS_XHI);
+    const uint32_t tb = base + (part == 1 ? PS_TBLO : PS_TBHI);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_ss(tm, tc::sdesc(ta + (uint32_t)ks * 32u), tc::sdesc(kb + (uint32_t)ks * 32u), idesc, (part | ks) != 0);
+      tc::mma_ss(d_w, tc::sdesc_mn(xa + (uint32_t)ks * 2048u, PS_XBLK), tc::sdesc(tb + (uint32_t)ks * 32u), idesc,
+                 (part | ks) != 0);
   }
 #pragma unroll
   for (int part = 0; part < 2; ++part) {  // V is exact in bf16: split T diag(beta) only
-    const uint32_t ta = base + (part == 1 ? PS_TBLO : PS_TBHI);
+    const uint32_t tb = base + (part == 1 ? PS_TBLO : PS_TBHI);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_ss(tm + 128, tc::sdesc(ta + (uint32_t)ks * 32u), tc::sdesc(base + PS_VT + (uint32_t)ks * 32u), idesc,
-                 (part | ks) != 0);
+      tc::mma_ss(d_u, tc::sdesc_mn(base + PS_V + (uint32_t)ks * 2048u, 8192u), tc::sdesc(tb + (uint32_t)ks * 32u),
+                 idesc, (part | ks) != 0);
   }
 }
 
-// Tensor maps of the token-major inputs, each viewed as [T][H][128] with a 64-token x 1-head x 128 box.
+// Tensor maps of the token-major inputs, each viewed as [T][H][128]: k, q, g with a 64-token x 1-head x 128
+// box; v with a 64 x 1 x 64 box and the 128-byte swizzle (two loads per chunk).
 struct PrepMaps {
   CUtensorMap q, k, v, g;
 };
@@ -207,7 +189,8 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 
 // Persistent: each CTA walks the task list (task = (sequence i, head h, chunk slot cidx)) with stride
-// gridDim.x, skipping empty chunk slots, and prefetches the next task's inputs while it finishes one.
+// gridDim.x, skipping empty chunk slots, and prefetches the next task's inputs while it finishes one (k, q,
+// g once the Gram product has consumed them, v once the W / U~ products have).
 __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a, uint8_t* __restrict__ ws,
                                                               const __grid_constant__ PrepMaps maps, int nchunk) {
   extern __shared__ uint8_t smem_raw[];
@@ -223,7 +206,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   const int tid = threadIdx.x, warp = tid >> 5;
   tc::pdl_wait();  // the previous kernel in the stream (inputs, and any reader of the record buffer) is done
   tc::pdl_launch_dependents();
-  constexpr int DUTY = PREP_NT - 1;  // issues the bulk stores and the next task's tensor-map loads
+  constexpr int DUTY = PREP_NT - 1;  // issues the bulk stores and the tensor-map loads
   const int total = nchunk * a.H * a.N;
   struct Task {
     int64_t t0;
@@ -253,15 +236,14 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     while (t < total && task_at(t).n == 0) t += (int)gridDim.x;
     return t;
   };
-  // the chunk's k, q, v and g tiles (64 tokens x 128 channels of head h) with four TMA loads; beta with
-  // 4-byte copies that arrive on the same barrier
-  auto fetch = [&](const Task& tk, int k) {
+  // the chunk's k, q and g tiles (64 tokens x 128 channels of head h) with three TMA loads, beta with 4-byte
+  // copies that arrive on the same barrier
+  auto fetch_main = [&](const Task& tk, int k) {
     uint64_t* fb = bar + 2;
     if (tid == DUTY) {
-      tc::bar_arrive_expect_tx(fb, 3 * 16384 + 32768);
+      tc::bar_arrive_expect_tx(fb, 2 * 16384 + 32768);
       tc::tma_load_3d(sK, &maps.k, 0, tk.h, (int)tk.t0, fb);
       tc::tma_load_3d(sQ, &maps.q, 0, tk.h, (int)tk.t0, fb);
-      tc::tma_load_3d(sm + PS_V, &maps.v, 0, tk.h, (int)tk.t0, fb);
       tc::tma_load_3d(sG, &maps.g, 0, tk.h, (int)tk.t0, fb);
     }
     if (tid >= D && tid < D + C) {
@@ -272,18 +254,26 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(fb)) : "memory");
     }
   };
+  // the chunk's v tile as two 64-channel swizzled blocks (duty thread only)
+  auto fetch_v = [&](const Task& tk) {
+    tc::bar_arrive_expect_tx(bar + 3, 16384);
+    tc::tma_load_3d(sm + PS_V, &maps.v, 0, tk.h, (int)tk.t0, bar + 3);
+    tc::tma_load_3d(sm + PS_V + 8192, &maps.v, 64, tk.h, (int)tk.t0, bar + 3);
+  };
 
   if (warp == 0) tc::tmem_alloc(tslot, 256);
   if (tid == 0) {
     tc::bar_init(bar + 0, 1);
     tc::bar_init(bar + 1, 1);
     tc::bar_init(bar + 2, 1 + C);  // the TMA issuer + one arrival per beta thread
+    tc::bar_init(bar + 3, 1);
     tc::bar_fence_init();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = *tslot;
+  constexpr uint32_t COL_W = 64, COL_U = 128;  // W^T and U~^T accumulators; the Gram product uses columns 0..63
   uint32_t gram_uses = 0;
   // the current and the next task; the one after is looked up mid-task (its cu_seqlens loads then overlap
   // the inverse instead of sitting at the top of the loop)
@@ -293,12 +283,15 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   int nxt = cur < total ? next_task(cur + (int)gridDim.x) : total;
   Task tnxt{};
   if (nxt < total) tnxt = task_at(nxt);
-  int inflight = -1;  // local index of a task whose inputs are requested but not yet waited for
+  // local indices of tasks whose inputs (k, q, g, beta) or v are requested but not yet waited for
+  int inflight = -1, inflight_v = -1;
   // the test hook issues nothing here, so the first wait below gives up with no copy in flight
   const uint32_t input_polls = a.test_stall_inputs ? (1u << 12) : (1u << 22);
   if (cur < total && !a.test_stall_inputs) {
-    fetch(tcur, 0);
+    fetch_main(tcur, 0);
     inflight = 0;
+    if (tid == DUTY) fetch_v(tcur);
+    inflight_v = 0;
   }
   bool ok = true;
   int k = 0;
@@ -312,13 +305,12 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   ok = __syncthreads_and(tc::bar_wait(bar + 2, (uint32_t)k & 1u, input_polls));
   if (!ok) break;
   inflight = -1;
-  // rows past the chunk's valid tokens (the next sequence's, or beyond T) are zero: k = q = v = g = 0
+  // rows past the chunk's valid tokens (the next sequence's, or beyond T) are zero: k = q = g = 0 (v below)
   for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
     const int t = n + (e >> 4), cc = e & 15;
     const uint4 z = make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(sK + t * D + cc * 8) = z;
     *reinterpret_cast<uint4*>(sQ + t * D + cc * 8) = z;
-    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(sm + PS_V) + t * D + cc * 8) = z;
     *reinterpret_cast<float4*>(sG + t * D + cc * 8) = make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4*>(sG + t * D + cc * 8 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -329,9 +321,10 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   {
     constexpr int TQ = C / PREP_PARTS;
     const int j = tid & (D - 1), part = tid / D;
-    // scratch in the Y region (free here; the X region may still be read by the previous task's stores)
-    float* ext = reinterpret_cast<float*>(sm + PS_YHI);           // extremes
-    float* gpart = reinterpret_cast<float*>(sm + PS_YHI + 8192);  // part totals [PREP_PARTS][D]
+    // scratch in the Q rows of X hi's first channel block (T diag(beta) there was read by the previous
+    // task's W / U~ products, which have completed; the X build follows only after the next barriers)
+    float* ext = reinterpret_cast<float*>(sm + PS_TBHI);  // extremes [PREP_NT][2]
+    float* gpart = ext + 2 * PREP_NT;                      // part totals [PREP_PARTS][D]
     float x[TQ];
 #pragma unroll
     for (int u = 0; u < TQ; ++u) x[u] = sG[(TQ * part + u) * D + j];
@@ -361,60 +354,41 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       span = gmax - gmin;
     }
   }
-  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's staged W, U~ tiles (X region) have been read
+  // gamma_C of channel tid & 127: the W^T epilogue's scale and the record's gamma
+  const float gamma_c = __expf(sG[(C - 1) * D + (tid & (D - 1))]);
+  if (tid < D) reinterpret_cast<float*>(rec + REC_GAMMA)[tid] = gamma_c;
+  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's P, K^ and W^T stores have read their staging
   tc::fence_before_sync();
   const bool slow = __syncthreads_or(span > SPAN_MAX);
   tc::fence_after_sync();
 
-  // per (token t, 8 channels): Q o gamma (output), (K o gamma)^T (operand), and in the common case X, Y
+  // per (token t, 8 channels): Q o gamma (record), and in the common case X and Y (reference = chunk end)
   for (int task = tid; task < C * 16; task += PREP_NT) {
     const int t = task >> 4, cc = task & 15;
-    float kx[8], qx[8], gt[8], e2[8], v[8];
+    float kx[8], qx[8], gt[8], v[8];
     unpack8(*reinterpret_cast<const uint4*>(sK + t * D + cc * 8), kx);
     unpack8(*reinterpret_cast<const uint4*>(sQ + t * D + cc * 8), qx);
     load8f(sG + t * D + cc * 8, gt);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) e2[e] = __expf(gt[e]);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = qx[e] * e2[e];
-    const uint32_t ob = (uint32_t)(cc >> 3) * 16384u + tc::sw128_chunk(64 + t, cc & 7);
-    split8_store(rec + REC_B1HI + ob, rec + REC_B1LO + ob, v);
+    for (int e = 0; e < 8; ++e) v[e] = qx[e] * __expf(gt[e]);
+    const uint32_t ob = y_off(t, cc);
+    split8_store(rec + REC_QHI + ob, rec + REC_QLO + ob, v);
     if (!slow) {
       float gc[8], e1[8];
       load8f(sG + (C - 1) * D + cc * 8, gc);
 #pragma unroll
       for (int e = 0; e < 8; ++e) e1[e] = __expf(gt[e] - gc[e]);
-      const uint32_t xo = (uint32_t)(cc >> 3) * 16384u;
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = kx[e] * e1[e];
-      split8_store(sm + PS_XHI + xo + tc::sw128_chunk(t, cc & 7), sm + PS_XLO + xo + tc::sw128_chunk(t, cc & 7), v);
+      split8_store(sm + PS_XHI + x_off(t, cc), sm + PS_XLO + x_off(t, cc), v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = qx[e] * e1[e];
-      split8_store(sm + PS_XHI + xo + tc::sw128_chunk(64 + t, cc & 7), sm + PS_XLO + xo + tc::sw128_chunk(64 + t, cc & 7),
-                   v);
+      split8_store(sm + PS_XHI + x_off(64 + t, cc), sm + PS_XLO + x_off(64 + t, cc), v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = kx[e] * __expf(gc[e] - gt[e]);
-      const uint32_t yo = (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(t, cc & 7);
-      split8_store(sm + PS_YHI + yo, sm + PS_YLO + yo, v);
+      split8_store(sm + PS_YHI + y_off(t, cc), sm + PS_YLO + y_off(t, cc), v);
     }
   }
-  // (K o gamma)^T, the B operand of W: row j, PREP_PARTS threads per row; and gamma_C for the record.  Needed
-  // only by the W / U~ product, so in the common case it runs while the Gram product is on the tensor core.
-  auto kp_pass = [&]() {
-    constexpr int SCP = 8 / PREP_PARTS;
-    const int j = tid & (D - 1), part = tid / D;
-#pragma unroll
-    for (int sc = SCP * part; sc < SCP * part + SCP; ++sc) {
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int s2 = 8 * sc + e;
-        v[e] = __bfloat162float(sK[s2 * D + j]) * __expf(sG[s2 * D + j]);
-      }
-      split8_store(sm + PS_KPHI + tc::sw128_chunk(j, sc), sm + PS_KPLO + tc::sw128_chunk(j, sc), v);
-    }
-    if (tid < D) reinterpret_cast<float*>(rec + REC_GAMMA)[tid] = __expf(sG[(C - 1) * D + tid]);
-  };
 
   // Gram matrices in TMEM columns 0..63: lanes 0..63 = A rows (before beta), lanes 64..127 = P rows
   if (ok && !slow) {
@@ -425,17 +399,28 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       issue_gram(sm, tm, 0, 64);
       tc::commit(bar);
     }
-    kp_pass();
     ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));
     ++gram_uses;
   } else if (ok) {
-    kp_pass();
+    // decay span above the limit: per 16-token block b, pair factors referenced at the block's last token
     for (int e = tid; e < C * 16; e += PREP_NT) {
-      const int s = e >> 4;
-      build_y_chunk(sm, s, e & 15, (s & ~15) + 15);
+      const int s = e >> 4, cc = e & 15;
+      float v[8];
+      decayed8(sm, PS_K, s, cc, (s & ~15) + 15, -1.f, v);
+      split8_store(sm + PS_YHI + y_off(s, cc), sm + PS_YLO + y_off(s, cc), v);
     }
     for (int b = 0; b < 4; ++b) {
-      for (int e = tid; e < 128 * 16; e += PREP_NT) build_x_chunk(sm, e >> 4, e & 15, 16 * b + 15, 16 * b);
+      for (int e = tid; e < 128 * 16; e += PREP_NT) {
+        const int r = e >> 4, cc = e & 15, t = r & 63;
+        float v[8];
+        if (t < 16 * b) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] = 0.f;
+        } else {
+          decayed8(sm, r < 64 ? PS_K : PS_Q, t, cc, 16 * b + 15, 1.f, v);
+        }
+        split8_store(sm + PS_XHI + x_off(r, cc), sm + PS_XLO + x_off(r, cc), v);
+      }
       tc::fence_proxy_async();
       __syncthreads();
       if (tid == 0) {
@@ -447,12 +432,29 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       ++gram_uses;
       if (!ok) break;
     }
+    // X and Y are free again: the K rows of X become K o gamma (A operand of W^T, no rescale) and Y the
+    // record's K^ = K o exp(G_C - G)
+    if (ok) {
+      for (int e = tid; e < C * 16; e += PREP_NT) {
+        const int t = e >> 4, cc = e & 15;
+        float kx[8], gt[8], gc[8], v[8];
+        unpack8(*reinterpret_cast<const uint4*>(sK + t * D + cc * 8), kx);
+        load8f(sG + t * D + cc * 8, gt);
+        load8f(sG + (C - 1) * D + cc * 8, gc);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = kx[q] * __expf(gt[q]);
+        split8_store(sm + PS_XHI + x_off(t, cc), sm + PS_XLO + x_off(t, cc), v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = kx[q] * __expf(gc[q] - gt[q]);
+        split8_store(sm + PS_YHI + y_off(t, cc), sm + PS_YLO + y_off(t, cc), v);
+      }
+    }
   }
 
   if (ok) {
     tc::fence_after_sync();
     if (warp < 8) {
-      // A (beta, strictly lower) to shared memory and P (lower incl. diagonal) to the record: lane row
+      // A (beta, strictly lower) to shared memory and P (lower incl. diagonal) to its staging: lane row
       // 32 (warp % 4) + lane (rows 0..63 = A, 64..127 = P), columns 32 (warp / 4) .. + 31
       const int q = warp & 3, ch = warp >> 2, row = 32 * q + (tid & 31);
       float v[32];
@@ -478,44 +480,23 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
           float pv[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) pv[e] = 8 * cc + e <= t ? v[8 * i + e] : 0.f;
-          split8_store(sm + PS_Q + tc::sw128_chunk(t, cc), sm + PS_Q + (REC_PLO - REC_PHI) + tc::sw128_chunk(t, cc), pv);
+          split8_store(sm + PS_PHI + tc::sw128_chunk(t, cc), sm + PS_PLO + tc::sw128_chunk(t, cc), pv);
         }
-      }
-    } else {
-      // V^T operand (raw bf16) and the (K o exp(G_C - G))^T record tile: row c, two threads per row
-      const int c = (tid - 256) & (D - 1), sh = (tid - 256) >> 7;
-#pragma unroll
-      for (int sc = 4 * sh; sc < 4 * sh + 4; ++sc) {
-        __nv_bfloat16 vv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) vv[e] = reinterpret_cast<const __nv_bfloat16*>(sm + PS_V)[(8 * sc + e) * D + c];
-        *reinterpret_cast<uint4*>(sm + PS_VT + tc::sw128_chunk(c, sc)) = pack8(vv);
-      }
-      const float gc = sG[(C - 1) * D + c];
-#pragma unroll
-      for (int sc = 4 * sh; sc < 4 * sh + 4; ++sc) {
-        float kv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = 8 * sc + e;
-          kv[e] = __bfloat162float(sK[s * D + c]) * __expf(gc - sG[s * D + c]);
-        }
-        split8_store(sm + PS_YHI + tc::sw128_chunk(c, sc), sm + PS_YHI + (REC_KHLO - REC_KHHI) + tc::sw128_chunk(c, sc),
-                     kv);
       }
     }
     tc::fence_proxy_async();
   }
   __syncthreads();
   if (ok && tid == DUTY) {
-    tc::bulk_s2g(rec + REC_PHI, sm + PS_Q, REC_KHHI - REC_PHI);
-    tc::bulk_s2g(rec + REC_KHHI, sm + PS_YHI, REC_STAGE - REC_KHHI);
+    tc::bulk_s2g(rec + REC_PHI, sm + PS_PHI, 8192);
+    tc::bulk_s2g(rec + REC_PLO, sm + PS_PLO, 8192);
+    tc::bulk_s2g(rec + REC_KHI, sm + PS_YHI, 16384);
+    tc::bulk_s2g(rec + REC_KLO, sm + PS_YLO, 16384);
     tc::bulk_commit();
-    tc::bulk_wait_read0();  // P (staged in the raw q region) read before the next task's loads land there
   }
-  // raw k, q, v, g are dead: the next task's inputs
+  // raw k, q, g are dead: the next task's (v follows once the W / U~ products have read this one's)
   if (ok && nxt < total) {
-    fetch(tnxt, k + 1);
+    fetch_main(tnxt, k + 1);
     inflight = k + 1;
   }
   // the duty thread starts looking up the task after next: the candidate's cu_seqlens loads are issued
@@ -544,8 +525,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LT + 16 * b + cc] = x[r];
     }
     // The inverse's inner barriers leave out warp 15: it computes nothing here, and its duty thread may
-    // still be waiting for the record stores to read their staging and issuing the next task's loads.  It
-    // rejoins at the last round's barrier, before it reads T.
+    // still be issuing the bulk stores and the next task's loads.  It rejoins at the last round's barrier.
     constexpr int INV_THREADS = PREP_NT - 32;
     if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
     // off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  First
@@ -593,17 +573,16 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
         __syncthreads();
       }
     }
-    // T diag(beta) as the A operand (lower triangle only)
-    for (int task = tid; task < C * 8; task += PREP_NT) {
-      const int t = task >> 3, cc = task & 7;
+    // T diag(beta) as the B operand of W^T and U~^T (lower triangle only), into the Q rows of X hi
+    {
+      const int t = tid >> 3, cc = tid & 7;
+      static_assert(C * 8 == PREP_NT, "one 8-column strip of T diag(beta) per thread");
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const int s = 8 * cc + e;
         v[e] = s <= t ? sT[t * LT + s] * sbeta[s] : 0.f;
       }
-      static_assert(C * 8 == PREP_NT, "one task per thread: every read of T precedes every write");
-      __syncthreads();  // T's last rows and the T diag(beta) tile share memory
       split8_store(sm + PS_TBHI + tc::sw128_chunk(t, cc), sm + PS_TBLO + tc::sw128_chunk(t, cc), v);
     }
     if (tid == DUTY) {  // the task after next (an empty candidate falls back to the full search)
@@ -623,49 +602,58 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       nx[3] = t2.i;
       *reinterpret_cast<int64_t*>(sm + PS_NEXT + 16) = t2.t0;
     }
+    // this task's v: its rows past the valid tokens are zero (each 128-byte row of both blocks)
+    ok = __syncthreads_and(tc::bar_wait(bar + 3, (uint32_t)k & 1u));
+    if (ok) {
+      inflight_v = -1;
+      for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
+        const int t = n + (e >> 4), q = e & 15;
+        *reinterpret_cast<uint4*>(sm + PS_V + (uint32_t)(q >> 3) * 8192u + (uint32_t)t * 128u + (uint32_t)(q & 7) * 16u) =
+            make_uint4(0, 0, 0, 0);
+      }
+    }
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0) {
+    if (ok && tid == 0) {
       tc::fence_after_sync();
-      issue_wu(sm, tm);
+      issue_wu(sm, tm + COL_W, tm + COL_U);
       tc::commit(bar + 1);
     }
-    ok = __syncthreads_and(tc::bar_wait(bar + 1, (uint32_t)k & 1u));
+    if (ok) ok = __syncthreads_and(tc::bar_wait(bar + 1, (uint32_t)k & 1u));
   }
 
   if (ok) {
-    // W rows t of the stacked B operand and U~ rows t; M = 64 accumulator rows sit in lanes 0..15 of each
-    // 32-lane quarter.  The four warps of a quarter split the columns: 32 of W and 32 of U~ each.
+    // v has been read: the next task's may land
+    if (tid == DUTY && nxt < total) fetch_v(tnxt);
+    if (nxt < total) inflight_v = k + 1;
+    // W^T and U~^T rows (lane = channel r), 32 tokens per warp: warps 4g + q read lanes 32 q .. 32 q + 31 and
+    // columns 32 (g & 1) .. of W^T (g < 2) or U~^T (g >= 2).  W^T (split) is staged in the dead A / T region
+    // for two bulk stores; U~ goes straight to the record, one coalesced 128-byte token row per warp store.
     tc::fence_after_sync();
-    const int q = warp & 3, part = warp >> 2, l = tid & 31;
-    const uint32_t trow = tm + ((uint32_t)(q * 32) << 16);
-    float w[32], u[32];
-    tc::tmem_ld32(trow + 32 * part, w);
-    tc::tmem_ld32(trow + 128 + 32 * part, u);
-    if (l < 16) {
-      // staging: W rows 0..63 of K-block kb at (hi: 0, lo: 16 KB) + kb * 8 KB; U~ rows at 512 B each
-      const int t = 16 * q + l;
+    const int q = warp & 3, g = warp >> 2, r = tid & (D - 1);
+    float v[32];
+    tc::tmem_ld32(tm + ((uint32_t)(q * 32) << 16) + (g < 2 ? COL_W : COL_U) + 32 * (g & 1), v);
+    if (g < 2) {
+      const float sc = slow ? 1.f : gamma_c;  // X_K = K o exp(G - G_C) in the common case
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t o = (uint32_t)(part >> 1) * 8192u + tc::sw128_chunk(t, 4 * (part & 1) + i);
-        split8_store(sm + o, sm + 16384 + o, w + 8 * i);
+      for (int e = 0; e < 32; ++e) v[e] *= sc;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t o = tc::sw128_chunk(r, 4 * (g & 1) + ch);
+        split8_store(sm + PS_WHI + o, sm + PS_WLO + o, v + 8 * ch);
       }
-      float4* U = reinterpret_cast<float4*>(sm + PS_TBHI + t * D * 4);
+      tc::fence_proxy_async();
+    } else {
+      float* U = reinterpret_cast<float*>(rec + REC_U) + (size_t)32 * (g & 1) * D + r;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) U[(8 * part + e) ^ (t & 7)] = make_float4(u[4 * e], u[4 * e + 1], u[4 * e + 2], u[4 * e + 3]);
+      for (int e = 0; e < 32; ++e) U[(size_t)e * D] = v[e];
     }
-    tc::fence_proxy_async();
   }
-  tc::fence_before_sync();
   __syncthreads();
   if (ok && tid == DUTY) {
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      tc::bulk_s2g(rec + REC_B1HI + kb * 16384, sm + kb * 8192, 8192);
-      tc::bulk_s2g(rec + REC_B1LO + kb * 16384, sm + 16384 + kb * 8192, 8192);
-    }
-    tc::bulk_s2g(rec + REC_U, sm + PS_TBHI, REC_GAMMA - REC_U);
+    tc::bulk_s2g(rec + REC_WHI, sm + PS_WHI, 16384);
+    tc::bulk_s2g(rec + REC_WLO, sm + PS_WLO, 16384);
     tc::bulk_commit();
   }
   if (!ok) break;
@@ -684,7 +672,9 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   }  // task loop
   if (!ok) {
     if (tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
-    if (inflight >= 0) tc::bar_wait(bar + 2, (uint32_t)inflight & 1u);  // bounded: let loads in flight land
+    // bounded: let the loads in flight land before the shared memory is released
+    if (inflight >= 0) tc::bar_wait(bar + 2, (uint32_t)inflight & 1u);
+    if (inflight_v >= 0) tc::bar_wait(bar + 3, (uint32_t)inflight_v & 1u);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -801,23 +791,14 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
   };
   int issued = 0;  // chunks whose stage copies have been issued (the copy thread's view)
   // the chunk's record tiles into stage cc & 1 (same offsets as in the record); fragment mode has no
-  // outputs and copies only the W rows of the stacked [W; Q o gamma] tile and (K o exp(G_C - G))^T
+  // outputs and copies only W^T and K^, the first REC_FRAG bytes
   auto issue = [&](int cc) {
     const int st = cc & 1;
     const uint8_t* rec = rec_of(cc);
     uint8_t* stage = sm + st * REC_STAGE;
-    if (WANT_O) {
-      tc::bar_arrive_expect_tx(full + st, REC_STAGE + 512);
-      tc::bulk_g2s(stage, rec, REC_STAGE, full + st);
-    } else {
-      tc::bar_arrive_expect_tx(full + st, 4 * 8192 + (REC_STAGE - REC_KHHI) + 512);
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {  // W: rows 0..63 = the first 8 KB of each 16 KB K-block
-        tc::bulk_g2s(stage + REC_B1HI + kb * 16384, rec + REC_B1HI + kb * 16384, 8192, full + st);
-        tc::bulk_g2s(stage + REC_B1LO + kb * 16384, rec + REC_B1LO + kb * 16384, 8192, full + st);
-      }
-      tc::bulk_g2s(stage + REC_KHHI, rec + REC_KHHI, REC_STAGE - REC_KHHI, full + st);
-    }
+    const uint32_t bytes = WANT_O ? REC_STAGE : REC_FRAG;
+    tc::bar_arrive_expect_tx(full + st, bytes + 512);
+    tc::bulk_g2s(stage, rec, bytes, full + st);
     tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
     issued = cc + 1;
   };
@@ -897,10 +878,10 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       const int st = cc & 1;
       const uint32_t par = (uint32_t)cc & 1u;
       float ut[32];
-      {
-        const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D;
+      {  // U~ column c, this thread's 32 tokens (a warp reads 128 contiguous bytes per token)
+        const float* U = reinterpret_cast<const float*>(rec_of(cc) + REC_U) + (size_t)32 * wg * D + c;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D + (c ^ ((e & 7) << 2))];
+        for (int e = 0; e < 32; ++e) ut[e] = zero_u ? 0.f : U[(size_t)e * D];
       }
       bool w_ok = tc::bar_wait(full + st, (uint32_t)(cc >> 1) & 1u);
       if (cc > 0) w_ok = w_ok && tc::bar_wait(bar_st, par ^ 1u);  // the previous chunk's state update
@@ -998,17 +979,18 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       }
       if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u)) break;
       tc::fence_after_sync();
-      // shared-memory descriptors of this stage's tiles: a descriptor of base + off is the base descriptor
-      // + off / 16 (start-address field), so each K step is a constant offset
-      const uint64_t dstage = tc::sdesc(tc::smem_u32(sm + st * REC_STAGE));
+      // shared-memory descriptor of this stage's W^T and K^ tiles (MN-major; K^'s two 64-channel blocks 8 KB
+      // apart): a descriptor of base + off is the base descriptor + off / 16 (start-address field), so each K
+      // step is a constant offset
+      const uint64_t dmn = tc::sdesc_mn(tc::smem_u32(sm + st * REC_STAGE), 8192u);
 #pragma unroll
       for (int part = 0; part < (WS_PARTS == 3 ? 1 : 3); ++part) {  // (W S)^T = S^T W^T
         const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
-        const uint64_t bd = dstage + ((part == 1 ? REC_B1LO : REC_B1HI) >> 4);
+        const uint64_t bd = dmn + ((part == 1 ? REC_WLO : REC_WHI) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc::mma_ts(tm + COL_WS, acol + ks * 8, bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4),
-                     tc::idesc_bf16(128, 64), (part | ks) != 0);
+          tc::mma_ts(tm + COL_WS, acol + ks * 8, bd + ((ks * 2048u) >> 4), tc::idesc_bf16(128, 64) | tc::IDESC_B_MN,
+                     (part | ks) != 0);
       }
       tc::commit(bar_ws);
       if (!tc::bar_wait(rdy_e2, (uint32_t)k & 1u)) break;
@@ -1016,9 +998,10 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
 #pragma unroll
       for (int part = 0; part < 3; ++part) {  // state: S^T += U^T (K o exp(G_C - G))
         const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
-        const uint64_t kd = dstage + ((part == 1 ? REC_KHLO : REC_KHHI) >> 4);
+        const uint64_t kd = dmn + ((part == 1 ? REC_KLO : REC_KHI) >> 4);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) tc::mma_ts(tm + COL_S, acol + ks * 8, kd + 2u * ks, tc::idesc_bf16(128, 128), 1);
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_ts(tm + COL_S, acol + ks * 8, kd + ((ks * 2048u) >> 4), tc::idesc_bf16(128, 128) | tc::IDESC_B_MN, 1);
       }
       tc::commit(bar_st);
     }
@@ -1041,10 +1024,10 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
 #pragma unroll
       for (int part = 0; part < 3; ++part) {  // (Q o gamma S)^T into this chunk's output accumulator
         const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
-        const uint64_t bd = dstage + (((part == 1 ? REC_B1LO : REC_B1HI) + 64u * 128u) >> 4);  // rows 64..127
+        const uint64_t bd = dstage + ((part == 1 ? REC_QLO : REC_QHI) >> 4);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4),
+          tc::mma_ts(tm + COL_O + 64 * st, acol + ks * 8, bd + (((ks >> 2) * 8192u + (ks & 3) * 32u) >> 4),
                      tc::idesc_bf16(128, 64), (part | ks) != 0);
       }
       tc::commit(bar_o1);
@@ -1088,13 +1071,13 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
       const int st = k & 1;
       if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u)) break;
       tc::fence_after_sync();
-      const uint64_t dstage = tc::sdesc(tc::smem_u32(sm + st * REC_STAGE));
+      const uint64_t dmn = tc::sdesc_mn(tc::smem_u32(sm + st * REC_STAGE), 8192u);
       const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
-      const uint64_t bd = dstage + ((part == 1 ? REC_B1LO : REC_B1HI) >> 4);
+      const uint64_t bd = dmn + ((part == 1 ? REC_WLO : REC_WHI) >> 4);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_ts(tm + COL_O + 64u * (uint32_t)(part - 1), acol + ks * 8,
-                   bd + (((ks >> 2) * 16384u + (ks & 3) * 32u) >> 4), tc::idesc_bf16(128, 64), ks != 0);
+        tc::mma_ts(tm + COL_O + 64u * (uint32_t)(part - 1), acol + ks * 8, bd + ((ks * 2048u) >> 4),
+                   tc::idesc_bf16(128, 64) | tc::IDESC_B_MN, ks != 0);
       tc::commit(bar_ws);
     }
     if (k < nch) flag_status(a.status, KDA_DEV_TIMEOUT);
@@ -1131,7 +1114,7 @@ cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t 
   if (a.T > 0x7fffffff) return cudaErrorInvalidValue;  // TMA coordinates are 32-bit
   PrepMaps maps;
   if (!encode_token_map(&maps.q, a.q, false, a.T, a.H, C) || !encode_token_map(&maps.k, a.k, false, a.T, a.H, C) ||
-      !encode_token_map(&maps.v, a.v, false, a.T, a.H, C) || !encode_token_map(&maps.g, a.g, true, a.T, a.H, C))
+      !encode_token_map_sw128(&maps.v, a.v, a.T, a.H, C) || !encode_token_map(&maps.g, a.g, true, a.T, a.H, C))
     return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_BYTES);
   if (e != cudaSuccess) return e;

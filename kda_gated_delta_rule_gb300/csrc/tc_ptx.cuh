@@ -37,10 +37,27 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
   return d;
 }
 
+// shared-memory matrix descriptor for an MN-major operand (128B swizzle): the tile is stored as rows along K,
+// each row 64 bf16 of the M (or N) dimension; 8-row K groups 1024 bytes apart (stride byte offset), and
+// the next 64 elements of M (N) `atom_stride` bytes further (leading byte offset).  One MMA (K = 16)
+// reads two K groups: the k-th K step starts 2048 * k bytes in.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t atom_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((atom_stride >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// operand-major bits of the instruction descriptor: A (resp. B) stored MN-major
+constexpr uint32_t IDESC_A_MN = 1u << 15;
+constexpr uint32_t IDESC_B_MN = 1u << 16;
 
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {
