@@ -239,25 +239,27 @@ def run_ours(args):
     out = torch.empty(T, H, d, dtype=torch.bfloat16, device=dev)
     status = torch.zeros(2, dtype=torch.int32, device=dev)
     pargs = (q, k, v, g, beta, cu, T, pool, slot, out)
-    seg_len = args.segment_len
-    if seg_len <= 0:
-        # output phase: H CTAs per segment, one CTA per SM (the fragment phase, 2 x H CTAs per segment but
-        # the last, then takes two waves; the scan grows by one short step per segment)
-        segments = max(1, props.multi_processor_count // H)
-        per_segment = -(-T // segments)
-        seg_len = -(-per_segment // 64) * 64
-    ws = torch.empty(max(kda.kda_segmented_workspace_size(*pargs, seg_len), 256), dtype=torch.uint8, device=dev)
+    if args.segment_len > 0:
+        seg_candidates = [args.segment_len]
+    else:
+        # segment lengths from one output-phase CTA per SM and head (H CTAs per segment) down to about half
+        # as many segments; the fastest on a few untimed steps is taken
+        one_wave = max(1, props.multi_processor_count // H)
+        ceil_div = lambda x, y: -(-x // y)
+        seg_candidates = sorted({64 * ceil_div(ceil_div(T, P), 64) for P in range(max(1, one_wave // 2), one_wave + 2)})
+    ws_bytes = max(kda.kda_segmented_workspace_size(*pargs, sl) for sl in seg_candidates)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
     ws_var = torch.empty(max(kda.kda_prefill_workspace_size(*pargs), 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
     def restore():
         kda.kda_state_copy(ckpt, slot, pool, slot)
 
-    def prefill(path):
+    def prefill(path, sl=None):
         if path == "varlen":
             kda.kda_prefill_varlen(*pargs, workspace=ws_var, dev_status=status)
         else:
-            kda.kda_prefill_segmented(*pargs, seg_len, ws, dev_status=status)
+            kda.kda_prefill_segmented(*pargs, sl, ws, dev_status=status)
 
     kernels_per_step = {"varlen": 3, "segmented": 5}  # state copy + the path's kernels
 
@@ -272,16 +274,17 @@ def run_ours(args):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
 
-    # choose the path (both are parity-tested): the faster one on a few untimed calls
+    # choose the path and segment length (all are parity-tested): the fastest on a few untimed calls
     paths = ["varlen", "segmented"] if args.path == "auto" else [args.path]
     trial = {}
     for pth in paths:
-        for _ in range(2):
-            restore()
-            prefill(pth)
-        torch.cuda.synchronize()
-        trial[pth] = statistics.median(time_calls(lambda: (restore(), prefill(pth)), 3))
-    path = min(trial, key=trial.get)
+        for sl in (seg_candidates if pth == "segmented" else [None]):
+            for _ in range(2):
+                restore()
+                prefill(pth, sl)
+            torch.cuda.synchronize()
+            trial[(pth, sl)] = statistics.median(time_calls(lambda: (restore(), prefill(pth, sl)), 5))
+    path, seg_len = min(trial, key=trial.get)
 
     # the step's launches, phase by phase (exactly the kernels kda_prefill_varlen / kda_prefill_segmented
     # enqueue), so the timed steps also give each kernel's duration from events between its launches
@@ -474,7 +477,7 @@ def run_ours(args):
             "workload": "single-request prefill: B=1, T=8192, H=12, dk=dv=128, bf16 q/k/v, fp32 g/beta, "
                         "fp32 state S0~N(0,0.02), bf16 o + final fp32 state; step = COW restore + prefill",
             "path": path, "segment_len": seg_len if path == "segmented" else None,
-            "path_trial_ms": {kk: round(vv, 4) for kk, vv in trial.items()},
+            "path_trial_ms": {(f"{kk[0]}/{kk[1]}" if kk[1] else kk[0]): round(vv, 4) for kk, vv in trial.items()},
             "l2": "flushed between timed steps (512 MB write)",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
         },

@@ -9,7 +9,9 @@
 // One CTA per (request, head) holds the whole D x D state in registers (D/16 warps, each owning 16 value
 // columns; 128-bit loads of row segments), so each 64 KB state (D = 128) is read once and written at most
 // once per launch.  The window's inputs are staged in shared memory before the dependent token steps.
+#include "device.h"
 #include "launch.h"
+#include "tc_ptx.cuh"
 #include "wstep.cuh"
 
 namespace kda {
@@ -210,6 +212,113 @@ __global__ void __launch_bounds__(WCfg<D>::NT, 2) fold_kernel(float* pool, int n
   if (tid == 0) add_work(status, n);
 }
 
+// Loads a lane's rows of the warp's 16 columns from a row-major [D][D] fp32 state in shared memory.
+template <int D>
+__device__ __forceinline__ void wload_shared(float2 (&S)[WRows<D>::P][4], const float* src, int warp, int lane) {
+  const float* p = src + (lane >> 2) * D + 16 * warp + 4 * (lane & 3);
+#pragma unroll
+  for (int i = 0; i < WRows<D>::P; ++i) {
+    const float4 x0 = *reinterpret_cast<const float4*>(p + 16 * i * D);
+    const float4 x1 = *reinterpret_cast<const float4*>(p + (16 * i + 8) * D);
+    S[i][0] = make_float2(x0.x, x1.x);
+    S[i][1] = make_float2(x0.y, x1.y);
+    S[i][2] = make_float2(x0.z, x1.z);
+    S[i][3] = make_float2(x0.w, x1.w);
+  }
+}
+
+// The fold as a stream: two persistent CTAs per SM walk the (request, head) units with stride gridDim.x,
+// skipping units with nothing accepted.  While a unit replays from registers, the next unit's state is on
+// its way into shared memory (one bulk copy) and its recorded tokens follow with cp.async, so every SM
+// keeps a state load in flight instead of starting each one cold.  The per-token arithmetic is the same
+// wstep as decode and the one-unit-per-CTA fold, so the committed state stays bit-identical to n decode
+// steps.  Windows of up to WGRP tokens, bf16 record.
+template <int D, typename Tin>
+struct FoldStreamSmem {
+  static constexpr size_t STAGE = (size_t)D * D * 4;
+  static constexpr size_t RAW = STAGE;
+  static constexpr size_t TOK = RAW + 2 * sizeof(RawGroup<D, Tin>);
+  static constexpr size_t BAR = TOK + WGRP * sizeof(WTok<D>);
+  static constexpr size_t BYTES = BAR + 16;
+};
+
+template <int D, typename Tin>
+__global__ void __launch_bounds__(WCfg<D>::NT, 2) fold_stream_kernel(float* pool, int num_slots,
+                                                                      const int32_t* __restrict__ slot_ids, int W,
+                                                                      int H, ReplayPtrs rec,
+                                                                      const int32_t* __restrict__ accepted,
+                                                                      int32_t* status, int units) {
+  using L = FoldStreamSmem<D, Tin>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* stage = reinterpret_cast<float*>(smem);
+  RawGroup<D, Tin>* raw = reinterpret_cast<RawGroup<D, Tin>*>(smem + L::RAW);
+  WTok<D>* tok = reinterpret_cast<WTok<D>*>(smem + L::TOK);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Tin* rk = static_cast<const Tin*>(rec.k);
+  const Tin* rv = static_cast<const Tin*>(rec.v);
+  // the first unit at or after u that has accepted tokens and a valid slot (every thread computes it)
+  auto next_unit = [&](int u) {
+    for (; u < units; u += (int)gridDim.x) {
+      const int b = u / H, n = accepted[b];
+      if (n < 0 || n > W) {
+        if (tid == 0) flag_status(status, KDA_DEV_ACCEPT_OOB);
+        continue;
+      }
+      if (n == 0) continue;
+      const int slot = slot_ids[b];
+      if (slot < 0 || slot >= num_slots) {
+        if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+        continue;
+      }
+      break;
+    }
+    return u;
+  };
+  // requests unit u's state (thread 0) and its recorded tokens into raw[buf]
+  auto prefetch = [&](int u, int buf) {
+    const int b = u / H, h = u % H;
+    if (tid == 0) {
+      tc::bar_arrive_expect_tx(bar, (uint32_t)L::STAGE);
+      tc::bulk_g2s(stage, pool + ((size_t)slot_ids[b] * H + h) * D * D, (uint32_t)L::STAGE, bar);
+    }
+    fetch_tokens<D, Tin, false>(raw + buf, rk, nullptr, rv, rec.g, rec.beta, ((size_t)b * W) * H + h, H, accepted[b],
+                                tid, WCfg<D>::NT);
+  };
+  if (tid == 0) {
+    tc::bar_init(bar, 1);
+    tc::bar_fence_init();
+  }
+  __syncthreads();
+  int u = next_unit((int)blockIdx.x);
+  if (u < units) prefetch(u, 0);
+  bool ok = true;
+  float2 S[WRows<D>::P][4];
+#pragma unroll 1
+  for (int it = 0; u < units; ++it) {
+    const int b = u / H, h = u % H, n = accepted[b];
+    const int buf = it & 1;
+    const bool landed = tc::bar_wait(bar, (uint32_t)it & 1u);
+    cp_async_wait_all();
+    ok = __syncthreads_and(landed) != 0;
+    if (!ok) break;
+    wload_shared<D>(S, stage, warp, lane);
+    unpack_tokens<D, Tin, false, false>(tok, raw + buf, 0, 0, n, tid, nullptr);
+    __syncthreads();  // the stage has been read and the tokens unpacked
+    const int un = next_unit(u + (int)gridDim.x);
+    if (un < units) prefetch(un, buf ^ 1);
+    for (int t = 0; t < n; ++t) wstep<D, false>(S, tok[t], warp, lane);
+    wstore<D>(S, pool + ((size_t)slot_ids[b] * H + h) * D * D, warp, lane);
+    if (tid == 0) add_work(status, n);
+    u = un;
+  }
+  if (!ok) {  // the state copy did not land in time: report it and give the copy one more bounded wait
+    if (tid == 0) flag_status(status, KDA_DEV_TIMEOUT);
+    tc::bar_wait(bar, 0u);
+    tc::bar_wait(bar, 1u);
+  }
+}
+
 // ---------------------------------------------------------------- launchers
 
 template <int D, typename Tin, typename Tout>
@@ -225,6 +334,20 @@ static cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t s) {
   verify_kernel<D, Tin, Tout><<<a.B * a.H, WCfg<D>::NT, 0, s>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.W, a.H,
       a.pool, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.rec, a.snapshot_out, a.status);
+  return cudaGetLastError();
+}
+
+template <int D, typename Tin>
+static cudaError_t launch_fold_stream_t(const FoldArgs& a, cudaStream_t s) {
+  using L = FoldStreamSmem<D, Tin>;
+  cudaError_t e = cudaFuncSetAttribute(fold_stream_kernel<D, Tin>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)L::BYTES);
+  if (e != cudaSuccess) return e;
+  const int units = a.B * a.H, sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = units < 2 * sms ? units : 2 * sms;
+  fold_stream_kernel<D, Tin><<<grid, WCfg<D>::NT, L::BYTES, s>>>(a.pool, a.num_slots, a.slot_ids, a.W, a.H, a.rec,
+                                                                 a.accepted, a.status, units);
   return cudaGetLastError();
 }
 
@@ -279,6 +402,9 @@ cudaError_t launch_verify(const VerifyArgs& a, cudaStream_t s) {
   return a.out_bf16 ? verify_d<float, bf16>(a, s) : verify_d<float, float>(a, s);
 }
 
-cudaError_t launch_fold(const FoldArgs& a, cudaStream_t s) { return a.in_bf16 ? fold_d<bf16>(a, s) : fold_d<float>(a, s); }
+cudaError_t launch_fold(const FoldArgs& a, cudaStream_t s) {
+  if (a.in_bf16 && a.d == 128 && a.W <= WGRP) return launch_fold_stream_t<128, bf16>(a, s);
+  return a.in_bf16 ? fold_d<bf16>(a, s) : fold_d<float>(a, s);
+}
 
 }  // namespace kda
