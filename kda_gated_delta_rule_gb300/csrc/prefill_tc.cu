@@ -120,6 +120,18 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// a0 / a1 (rows r and r + 8 of a 16 x 16 block product, 4 columns) += m[r or r + 8][u] * b[u][.], u < 16;
+// m points at row r of the left block, b at the 4 columns of the right block (row stride LT for both)
+__device__ __forceinline__ void inv_mac(const float* m, const float* b, float (&a0)[4], float (&a1)[4]) {
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const float m0 = m[u], m1 = m[8 * LT + u];
+    const float4 b4 = *reinterpret_cast<const float4*>(b + u * LT);
+    a0[0] = fmaf(m0, b4.x, a0[0]); a0[1] = fmaf(m0, b4.y, a0[1]); a0[2] = fmaf(m0, b4.z, a0[2]); a0[3] = fmaf(m0, b4.w, a0[3]);
+    a1[0] = fmaf(m1, b4.x, a1[0]); a1[1] = fmaf(m1, b4.y, a1[1]); a1[2] = fmaf(m1, b4.z, a1[2]); a1[3] = fmaf(m1, b4.w, a1[3]);
+  }
+}
+
 // offset of the 16-byte chunk cc (channels 8cc..8cc+7) of row r in X (r < 128) or Y (r < 64)
 __device__ __forceinline__ uint32_t x_off(int r, int cc) { return (uint32_t)(cc >> 3) * PS_XBLK + tc::sw128_chunk(r, cc & 7); }
 __device__ __forceinline__ uint32_t y_off(int r, int cc) { return (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(r, cc & 7); }
@@ -391,6 +403,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   }
 
   // Gram matrices in TMEM columns 0..63: lanes 0..63 = A rows (before beta), lanes 64..127 = P rows
+  bool fetched = false;  // the next task's k, q, g requested already
   if (ok && !slow) {
     tc::fence_proxy_async();
     __syncthreads();
@@ -398,6 +411,12 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       tc::fence_after_sync();
       issue_gram(sm, tm, 0, 64);
       tc::commit(bar);
+    }
+    // in the common case raw k, q, g are dead once X and Y are built: the next task's inputs may land
+    if (nxt < total) {
+      fetch_main(tnxt, k + 1);
+      inflight = k + 1;
+      fetched = true;
     }
     ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));
     ++gram_uses;
@@ -495,7 +514,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     tc::bulk_commit();
   }
   // raw k, q, g are dead: the next task's (v follows once the W / U~ products have read this one's)
-  if (ok && nxt < total) {
+  if (ok && nxt < total && !fetched) {
     fetch_main(tnxt, k + 1);
     inflight = k + 1;
   }
@@ -510,7 +529,10 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   }
 
   if (ok) {
-    // T = (I + A)^-1, blocked by 16: diagonal blocks by forward substitution (threads 0..63, one column each)
+    // T = (I + A)^-1, blocked by 16, on warps 0..7 (warps 8..15 compute nothing here; the duty thread may
+    // still be issuing the bulk stores and the next task's loads).
+    // Diagonal blocks by forward substitution (threads 0..63, one column each).
+    constexpr int INV_THREADS = 256;
     if (tid < 64) {
       const int b = tid >> 4, cc = tid & 15;
       float x[16];
@@ -524,53 +546,84 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 #pragma unroll
       for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LT + 16 * b + cc] = x[r];
     }
-    // The inverse's inner barriers leave out warp 15: it computes nothing here, and its duty thread may
-    // still be issuing the bulk stores and the next task's loads.  It rejoins at the last round's barrier.
-    constexpr int INV_THREADS = PREP_NT - 32;
     if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
-    // off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.  First
-    // M_ik = T_ii A_ik for all six pairs k < i at once (kept in the unused upper block (k, i)), then block
-    // row by block row T_ij = -sum_k M_ik T_kj.  One warp per 16 x 16 block; lane (rp, cg) owns rows rp and
-    // rp + 8, columns 4 cg .. 4 cg + 3: per step two conflict-free scalar loads (a warp's eight rows sit in
-    // eight bank groups) and one 16-byte load feed eight FMAs (the rounds are bound by their shared loads).
+    // Off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -sum_{k=j}^{i-1} M_ik T_kj with
+    // M_ik = T_ii A_ik.  Every 16 x 16 block product is one warp's: lane (rp, cg) owns rows rp and rp + 8,
+    // columns 4 cg .. 4 cg + 3, and per step two conflict-free scalar loads (a warp's eight rows sit in eight
+    // bank groups) and one 16-byte load feed eight FMAs.  Rounds, each one product deep:
+    //   1. M_ik for all six pairs (kept in the unused upper block (k, i) of T);
+    //   2. T_10, T_21, T_32 (one term each);
+    //   3. the six products M_20 T_00, M_21 T_10, M_31 T_11, M_32 T_21, M_30 T_00, M_31 T_10 (into A's
+    //      dead storage);
+    //   4. T_20 and T_31 as sums of two of them, and T_30 = -(M_30 T_00 + M_31 T_10) + M_32 (M_20 T_00 + M_21 T_10).
     // T_ii is stored with its zero upper triangle, so the sums run over all 16.
-    if (tid < 6 * 32) {
-      const int pr = tid >> 5, rp = (tid >> 2) & 7, cg = tid & 3;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-      const int bi = pr == 0 ? 1 : (pr < 3 ? 2 : 3);
-      const int bk = pr == 0 ? 0 : (pr < 3 ? pr - 1 : pr - 3);
+    const int rp = (tid >> 2) & 7, cg = tid & 3, wv = tid >> 5;
+    auto mac = [&](const float* mb, const float* bb, float (&a0)[4], float (&a1)[4]) {
+      inv_mac(mb + rp * LT, bb + 4 * cg, a0, a1);
+    };
+    auto tblk = [&](int r, int c) { return sT + 16 * r * LT + 16 * c; };  // block (r, c) of T
+    constexpr int PLD = 20;                                               // row stride of the partial products
+    auto pblk = [&](int s) { return sA + s * 16 * PLD; };
+    auto put = [&](float* dst, int ld, const float (&a0)[4], const float (&a1)[4], float sg) {
+      *reinterpret_cast<float4*>(dst + rp * ld + 4 * cg) = make_float4(sg * a0[0], sg * a0[1], sg * a0[2], sg * a0[3]);
+      *reinterpret_cast<float4*>(dst + (rp + 8) * ld + 4 * cg) = make_float4(sg * a1[0], sg * a1[1], sg * a1[2], sg * a1[3]);
+    };
+    if (wv < 6) {  // round 1: M_ik = T_ii A_ik; pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+      const int bi = wv == 0 ? 1 : (wv < 3 ? 2 : 3);
+      const int bk = wv == 0 ? 0 : (wv < 3 ? wv - 1 : wv - 3);
       float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float t0 = sT[(16 * bi + rp) * LT + 16 * bi + u], t1 = sT[(16 * bi + rp + 8) * LT + 16 * bi + u];
-        const float4 a4 = *reinterpret_cast<const float4*>(sA + (16 * bi + u) * LT + 16 * bk + 4 * cg);
-        a0[0] = fmaf(t0, a4.x, a0[0]); a0[1] = fmaf(t0, a4.y, a0[1]); a0[2] = fmaf(t0, a4.z, a0[2]); a0[3] = fmaf(t0, a4.w, a0[3]);
-        a1[0] = fmaf(t1, a4.x, a1[0]); a1[1] = fmaf(t1, a4.y, a1[1]); a1[2] = fmaf(t1, a4.z, a1[2]); a1[3] = fmaf(t1, a4.w, a1[3]);
-      }
-      *reinterpret_cast<float4*>(sT + (16 * bk + rp) * LT + 16 * bi + 4 * cg) = make_float4(a0[0], a0[1], a0[2], a0[3]);
-      *reinterpret_cast<float4*>(sT + (16 * bk + rp + 8) * LT + 16 * bi + 4 * cg) = make_float4(a1[0], a1[1], a1[2], a1[3]);
+      mac(tblk(bi, bi), sA + 16 * bi * LT + 16 * bk, a0, a1);
+      put(tblk(bk, bi), LT, a0, a1, 1.f);
     }
     if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
-#pragma unroll 1
-    for (int bi = 1; bi < 4; ++bi) {
-      if (tid < bi * 32) {
-        const int bj = tid >> 5, rp = (tid >> 2) & 7, cg = tid & 3;
-        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int bk = bj; bk < bi; ++bk) {
+    if (wv < 3) {  // round 2: T_{w+1,w} = -M_{w+1,w} T_ww
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+      mac(tblk(wv, wv + 1), tblk(wv, wv), a0, a1);
+      put(tblk(wv + 1, wv), LT, a0, a1, -1.f);
+    }
+    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+    if (wv < 6) {  // round 3: (i, j, k) = (2,0,0) (2,0,1) (3,1,1) (3,1,2) (3,0,0) (3,0,1): M_ik T_kj into slot wv
+      const int bi = wv < 2 ? 2 : 3, bj = wv < 2 ? 0 : (wv < 4 ? 1 : 0);
+      const int bk = wv == 0 ? 0 : (wv == 1 ? 1 : (wv == 2 ? 1 : (wv == 3 ? 2 : (wv == 4 ? 0 : 1))));
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+      mac(tblk(bk, bi), tblk(bk, bj), a0, a1);
+      put(pblk(wv), PLD, a0, a1, 1.f);
+    }
+    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+    if (wv < 3) {  // round 4
+      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+      if (wv == 2) {  // M_32 (M_20 T_00 + M_21 T_10): the second operand summed on the fly
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            const float m0 = sT[(16 * bk + rp) * LT + 16 * bi + u], m1 = sT[(16 * bk + rp + 8) * LT + 16 * bi + u];
-            const float4 t4 = *reinterpret_cast<const float4*>(sT + (16 * bk + u) * LT + 16 * bj + 4 * cg);
-            a0[0] = fmaf(m0, t4.x, a0[0]); a0[1] = fmaf(m0, t4.y, a0[1]); a0[2] = fmaf(m0, t4.z, a0[2]); a0[3] = fmaf(m0, t4.w, a0[3]);
-            a1[0] = fmaf(m1, t4.x, a1[0]); a1[1] = fmaf(m1, t4.y, a1[1]); a1[2] = fmaf(m1, t4.z, a1[2]); a1[3] = fmaf(m1, t4.w, a1[3]);
-          }
+        for (int u = 0; u < 16; ++u) {
+          const float m0 = tblk(2, 3)[rp * LT + u], m1 = tblk(2, 3)[(rp + 8) * LT + u];
+          const float4 p0 = *reinterpret_cast<const float4*>(pblk(0) + u * PLD + 4 * cg);
+          const float4 p1 = *reinterpret_cast<const float4*>(pblk(1) + u * PLD + 4 * cg);
+          const float4 b4 = make_float4(p0.x + p1.x, p0.y + p1.y, p0.z + p1.z, p0.w + p1.w);
+          a0[0] = fmaf(m0, b4.x, a0[0]); a0[1] = fmaf(m0, b4.y, a0[1]); a0[2] = fmaf(m0, b4.z, a0[2]); a0[3] = fmaf(m0, b4.w, a0[3]);
+          a1[0] = fmaf(m1, b4.x, a1[0]); a1[1] = fmaf(m1, b4.y, a1[1]); a1[2] = fmaf(m1, b4.z, a1[2]); a1[3] = fmaf(m1, b4.w, a1[3]);
         }
-        *reinterpret_cast<float4*>(sT + (16 * bi + rp) * LT + 16 * bj + 4 * cg) = make_float4(-a0[0], -a0[1], -a0[2], -a0[3]);
-        *reinterpret_cast<float4*>(sT + (16 * bi + rp + 8) * LT + 16 * bj + 4 * cg) = make_float4(-a1[0], -a1[1], -a1[2], -a1[3]);
       }
-      if (bi < 3) {
-        if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
-      } else {
-        __syncthreads();
+      // wv 0: T_20 = -(slot 0 + slot 1); wv 1: T_31 = -(slot 2 + slot 3); wv 2: T_30 = acc - (slot 4 + slot 5)
+      const int sa = 2 * wv, dr = wv == 1 ? 3 : (wv == 0 ? 2 : 3), dc = wv == 1 ? 1 : 0;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int row = rp + 8 * h2;
+        const float4 x0 = *reinterpret_cast<const float4*>(pblk(sa) + row * PLD + 4 * cg);
+        const float4 x1 = *reinterpret_cast<const float4*>(pblk(sa + 1) + row * PLD + 4 * cg);
+        const float* ac = h2 ? a1 : a0;
+        *reinterpret_cast<float4*>(tblk(dr, dc) + row * LT + 4 * cg) =
+            make_float4(ac[0] - (x0.x + x1.x), ac[1] - (x0.y + x1.y), ac[2] - (x0.z + x1.z), ac[3] - (x0.w + x1.w));
+      }
+    }
+    // this task's v (requested during the previous task) has landed: its rows past the valid tokens are zeroed
+    // below, while T diag(beta) is formed
+    ok = __syncthreads_and(tc::bar_wait(bar + 3, (uint32_t)k & 1u));
+    if (ok) {
+      inflight_v = -1;
+      for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
+        const int t = n + (e >> 4), q = e & 15;
+        *reinterpret_cast<uint4*>(sm + PS_V + (uint32_t)(q >> 3) * 8192u + (uint32_t)t * 128u + (uint32_t)(q & 7) * 16u) =
+            make_uint4(0, 0, 0, 0);
       }
     }
     // T diag(beta) as the B operand of W^T and U~^T (lower triangle only), into the Q rows of X hi
@@ -601,16 +654,6 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       nx[2] = t2.h;
       nx[3] = t2.i;
       *reinterpret_cast<int64_t*>(sm + PS_NEXT + 16) = t2.t0;
-    }
-    // this task's v: its rows past the valid tokens are zero (each 128-byte row of both blocks)
-    ok = __syncthreads_and(tc::bar_wait(bar + 3, (uint32_t)k & 1u));
-    if (ok) {
-      inflight_v = -1;
-      for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
-        const int t = n + (e >> 4), q = e & 15;
-        *reinterpret_cast<uint4*>(sm + PS_V + (uint32_t)(q >> 3) * 8192u + (uint32_t)t * 128u + (uint32_t)(q & 7) * 16u) =
-            make_uint4(0, 0, 0, 0);
-      }
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
