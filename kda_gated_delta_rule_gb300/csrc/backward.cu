@@ -19,12 +19,15 @@
 // e^(G_t - G_s) = e^(G_t - G_r) e^(G_r - G_s), while every factor stays below e^80 (always when g >= -5, the
 // pages' floor); a block that would exceed it takes the pair decays one by one.
 //
-// Six kernels, all in fp32 on the CUDA cores, handing over through a per-(chunk, head) fp32 workspace
-// (tiles move into shared memory by asynchronous 16-byte copies):
+// Six kernels handing over through a per-(chunk, head) fp32 workspace (tiles move into shared memory by
+// asynchronous 16-byte copies):
 //   prep (chunk-parallel) -> forward chain (entry states, U) -> reverse chain (dS', dU)
 //   -> state products -> WY backward -> per-channel assembly (chunk-parallel).
+// The state products run on the tensor cores (split-bf16 tcgen05 MMAs, fp32 accumulation); the others
+// are fp32 on the CUDA cores.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -610,114 +613,183 @@ __global__ void __launch_bounds__(NTC, 1) bwd_rev_chain_kernel(BackwardArgs a) {
 }
 
 // ---------------------------------------------------------------------------------------------------
-// 4. state products of one (chunk, head): dQ+ = dO S^T, dW = -dU S^T, d(e^G_C), dP = tril(dO U^T), dK^ = U dS'^T
+// 4. state products of one (chunk, head): dQ+ = dO S^T, dW = -dU S^T, d(e^G_C), dP = tril(dO U^T), dK^ = U dS'^T,
+// as two split-bf16 tcgen05 MMAs:
+//   set 1: D1 = S [dO; dU]^T          (M = 128 key channels j, N = 128, K = 128 value channels)
+//          columns 0..63 = dQ+^T [j][t], columns 64..127 = (dU S^T)^T = -dW^T [j][t]
+//   set 2: D2 = [U; dO] [dS'; U]^T    (M = 128, N = 192, K = 128)
+//          rows 0..63, columns 0..127 = U dS'^T = dK^ [s][j]; rows 64..127, columns 128..191 = dO U^T -> dP
+// Every fp32 operand enters as bf16 hi + lo and the products hi*hi + hi*lo + lo*hi accumulate in fp32
+// (relative operand error ~2^-16; the gradients are held to 1e-4 of their rms).  d(e^G_C) stays on the CUDA
+// cores, read from the same loads that build the operands.
 // ---------------------------------------------------------------------------------------------------
-constexpr size_t STATE_SMEM = (D * LD + 2 * C * LD) * sizeof(float);
+constexpr uint32_t SG_A = 0;            // A1 = S (hi, lo), later A2 = [U; dO]: [128][128] bf16, two 16 KB K-blocks each
+constexpr uint32_t SG_B1 = 65536;       // B1 = [dO; dU] (hi, lo): [128][128]
+constexpr uint32_t SG_B2 = 131072;      // B2 = [dS'; U] (hi, lo): [192][128], two 24 KB K-blocks each
+constexpr uint32_t SG_BAR = 229376;
+constexpr size_t STATE_TC_SMEM = SG_BAR + 64 + 1024;
+
+// offset of the 16-byte chunk cc (channels 8cc .. 8cc + 7) of row r in a [rows][128] K-major tile
+__device__ __forceinline__ uint32_t kt_off(int r, int cc, int rows) {
+  return (uint32_t)(cc >> 3) * (uint32_t)(rows * 128) + tc::sw128_chunk(r, cc & 7);
+}
+__device__ __forceinline__ void split8(uint8_t* hi, uint8_t* lo, const float* v) {
+  uint4 h, l;
+  tc::split_pair(v[0], v[1], h.x, l.x);
+  tc::split_pair(v[2], v[3], h.y, l.y);
+  tc::split_pair(v[4], v[5], h.z, l.z);
+  tc::split_pair(v[6], v[7], h.w, l.w);
+  *reinterpret_cast<uint4*>(hi) = h;
+  *reinterpret_cast<uint4*>(lo) = l;
+}
+__device__ __forceinline__ void load8(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void load8(const bf16* p, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = __uint_as_float(w[e] << 16);
+    v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+// D (tensor memory) = sum over the three split products of A [128][128] and B [N][128], both K-major
+__device__ __forceinline__ void issue_split(uint32_t d, uint32_t a, uint32_t b, int brows, uint32_t idesc) {
+  const uint32_t ablk = 128 * 128, bblk = (uint32_t)brows * 128;
+#pragma unroll
+  for (int part = 0; part < 3; ++part) {
+    const uint32_t aa = a + (part == 2 ? 2 * ablk : 0), bb = b + (part == 1 ? 2 * bblk : 0);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+      tc::mma_ss(d, tc::sdesc(aa + (uint32_t)(ks >> 2) * ablk + (uint32_t)(ks & 3) * 32u),
+                 tc::sdesc(bb + (uint32_t)(ks >> 2) * bblk + (uint32_t)(ks & 3) * 32u), idesc, (part | ks) != 0);
+  }
+}
 
 template <typename Tin>
-__global__ void __launch_bounds__(NT, 1) bwd_state_grads_kernel(BackwardArgs a) {
-  const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x;
+__global__ void __launch_bounds__(NT, 1) bwd_state_grads_tc_kernel(BackwardArgs a) {
+  const int c = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
   const int t0 = sq.bos + c * C;
   if (t0 >= sq.eos) return;
   const int n = min(C, sq.eos - t0);
   float* w = record(a, t0, i, h);
-  extern __shared__ float sm[];
-  float* sH = sm;               // S, later dS' [128][LD]
-  float* sD = sH + D * LD;      // dO [64][LD]
-  float* sE = sD + C * LD;      // dU, later U [64][LD]
-  load_rows<NT>(sH, LD, w + BW_H, D, D, D, 0, D);
-  load_rows<NT>(sD, LD, reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D, (int64_t)a.H * D, C, n, 0,
-            D);
-  load_rows<NT>(sE, LD, w + BW_DU, D, C, C, 0, D);
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  const int ty = tid >> 4, tx = tid & 15;  // rows ty + 16i, columns tx + 16m
-  {
-    float aq[4][8] = {}, aw[4][8] = {};
-    for (int l = 0; l < D; ++l) {
-      float x[4], y[4], z[8];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sD[(ty + 16 * ii) * LD + l], y[ii] = sE[(ty + 16 * ii) * LD + l];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) z[m] = sH[(tx + 16 * m) * LD + l];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          aq[ii][m] = fmaf(x[ii], z[m], aq[ii][m]);
-          aw[ii][m] = fmaf(y[ii], z[m], aw[ii][m]);
-        }
-    }
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-      for (int m = 0; m < 8; ++m) {
-        const int o = (ty + 16 * ii) * D + tx + 16 * m;
-        w[BW_DQP + o] = aq[ii][m];
-        w[BW_DW + o] = -aw[ii][m];
-      }
+  extern __shared__ uint8_t sgraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sgraw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + SG_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + SG_BAR + 16);
+  const Tin* dO = reinterpret_cast<const Tin*>(a.d_out) + ((int64_t)t0 * a.H + h) * D;
+  const int64_t ldo = (int64_t)a.H * D;
+  constexpr uint32_t AH = 2 * 16384, B1H = 2 * 16384, B2H = 2 * 24576;  // bytes of a hi (or lo) tile
+  if (warp == 0) tc::tmem_alloc(tslot, 512);
+  if (tid == 0) {
+    tc::bar_init(bar, 1);
+    tc::bar_fence_init();
   }
-  {  // d(e^G_C)_j = sum_l dS'_jl S_jl: warp per row, dS' streamed from the record
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int j = warp; j < D; j += NT / 32) {
-      float x[4];
-      ld4(w + BW_DS + j * D + 4 * lane, x);
+  // set 1 and set 2's B operand: S and dS' rows j (with d(e^G_C)_j = sum_l dS'_jl S_jl), dU, dO, U
+  {
+    const int cc = tid & 15;
+    for (int j = tid >> 4; j < D; j += NT / 16) {
+      float x[8], y[8];
+      load8(w + BW_H + j * D + 8 * cc, x);
+      load8(w + BW_DS + j * D + 8 * cc, y);
+      split8(sm + SG_A + kt_off(j, cc, 128), sm + SG_A + AH + kt_off(j, cc, 128), x);
+      split8(sm + SG_B2 + kt_off(j, cc, 192), sm + SG_B2 + B2H + kt_off(j, cc, 192), y);
       float s = 0.f;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) s = fmaf(x[u], sH[j * LD + 4 * lane + u], s);
+      for (int e = 0; e < 8; ++e) s = fmaf(x[e], y[e], s);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) w[BW_DGAM + j] = s;
+      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (cc == 0) w[BW_DGAM + j] = s;
+    }
+    for (int t = tid >> 4; t < C; t += NT / 16) {
+      float x[8], y[8], z[8];
+      if (t < n) load8(dO + t * ldo + 8 * cc, x);
+      else for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      load8(w + BW_DU + t * D + 8 * cc, y);
+      load8(w + BW_U + t * D + 8 * cc, z);
+      split8(sm + SG_B1 + kt_off(t, cc, 128), sm + SG_B1 + B1H + kt_off(t, cc, 128), x);
+      split8(sm + SG_B1 + kt_off(64 + t, cc, 128), sm + SG_B1 + B1H + kt_off(64 + t, cc, 128), y);
+      split8(sm + SG_B2 + kt_off(128 + t, cc, 192), sm + SG_B2 + B2H + kt_off(128 + t, cc, 192), z);
     }
   }
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
   __syncthreads();
-  load_rows<NT>(sE, LD, w + BW_U, D, C, C, 0, D);
-  load_rows<NT>(sH, LD, w + BW_DS, D, D, D, 0, D);
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  {  // dP = tril(dO U^T)
-    float acc[4][4] = {};
-    for (int l = 0; l < D; ++l) {
-      float x[4], y[4];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sD[(ty + 16 * ii) * LD + l];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) y[m] = sE[(tx + 16 * m) * LD + l];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+  tc::fence_after_sync();
+  const uint32_t tm = *tslot;
+  const uint32_t base = tc::smem_u32(sm);
+  if (tid == 0) {
+    issue_split(tm, base + SG_A, base + SG_B1, 128, tc::idesc_bf16(128, 128));
+    tc::commit(bar);
+  }
+  bool ok = __syncthreads_and(tc::bar_wait(bar, 0u)) != 0;
+  // set 2's A operand over set 1's: [U; dO]
+  if (ok) {
+    tc::fence_after_sync();
+    const int cc = tid & 15;
+    for (int t = tid >> 4; t < C; t += NT / 16) {
+      float x[8], z[8];
+      if (t < n) load8(dO + t * ldo + 8 * cc, x);
+      else for (int e = 0; e < 8; ++e) x[e] = 0.f;
+      load8(w + BW_U + t * D + 8 * cc, z);
+      split8(sm + SG_A + kt_off(t, cc, 128), sm + SG_A + AH + kt_off(t, cc, 128), z);
+      split8(sm + SG_A + kt_off(64 + t, cc, 128), sm + SG_A + AH + kt_off(64 + t, cc, 128), x);
     }
+    tc::fence_proxy_async();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (ok && tid == 0) {
+    issue_split(tm + 128, base + SG_A, base + SG_B2, 192, tc::idesc_bf16(128, 192));
+    tc::commit(bar);
+  }
+  const int q = warp & 3, g = warp >> 2, r = 32 * q + (tid & 31);
+  const uint32_t trow = tm + ((uint32_t)(q * 32) << 16);
+  if (ok) {  // set 1 (complete): dQ+ [t][j] and dW [t][j], one coalesced row per warp store
+    float v[32];
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      tc::tmem_ld32(trow + 64 * g + 32 * half, v);
+      float* dst = w + (g ? BW_DW : BW_DQP) + (size_t)(32 * half) * D + r;
 #pragma unroll
-    for (int ii = 0; ii < 4; ++ii)
+      for (int e = 0; e < 32; ++e) dst[(size_t)e * D] = g ? -v[e] : v[e];
+    }
+  }
+  ok = __syncthreads_and(ok && tc::bar_wait(bar, 1u)) != 0;
+  if (ok) {  // set 2: dK^ rows (lanes 0..63), dP rows (lanes 64..127)
+    tc::fence_after_sync();
+    float v[32];
+    if (q < 2) {
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        tc::tmem_ld32(trow + 128 + 64 * g + 32 * half, v);
+        float4* dst = reinterpret_cast<float4*>(w + BW_DKH + (size_t)r * D + 64 * g + 32 * half);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int t = ty + 16 * ii, s = tx + 16 * m;
-        w[BW_DP + t * C + s] = s <= t ? acc[ii][m] : 0.f;
+        for (int e = 0; e < 8; ++e) dst[e] = make_float4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
       }
-  }
-  {  // dK^ = U dS'^T
-    float acc[4][8] = {};
-    for (int l = 0; l < D; ++l) {
-      float x[4], z[8];
+    } else {
+      const int t = r - 64;
+      tc::tmem_ld32(trow + 256 + 32 * g, v);
+      float4* dst = reinterpret_cast<float4*>(w + BW_DP + (size_t)t * C + 32 * g);
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sE[(ty + 16 * ii) * LD + l];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) z[m] = sH[(tx + 16 * m) * LD + l];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) acc[ii][m] = fmaf(x[ii], z[m], acc[ii][m]);
+      for (int e = 0; e < 8; ++e) {
+        const int s0 = 32 * g + 4 * e;
+        dst[e] = make_float4(s0 <= t ? v[4 * e] : 0.f, s0 + 1 <= t ? v[4 * e + 1] : 0.f, s0 + 2 <= t ? v[4 * e + 2] : 0.f,
+                             s0 + 3 <= t ? v[4 * e + 3] : 0.f);
+      }
     }
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-      for (int m = 0; m < 8; ++m) w[BW_DKH + (ty + 16 * ii) * D + tx + 16 * m] = acc[ii][m];
+  } else if (tid == 0) {
+    flag_status(a.status, KDA_DEV_TIMEOUT);
   }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tm, 512);
 }
 
 // ---------------------------------------------------------------------------------------------------
@@ -1059,7 +1131,7 @@ cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
   if ((e = set_smem(bwd_prep_kernel<Tin>, PREP_SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(bwd_fwd_chain_kernel, FWD_SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(bwd_rev_chain_kernel<Tin>, REV_SMEM)) != cudaSuccess) return e;
-  if ((e = set_smem(bwd_state_grads_kernel<Tin>, STATE_SMEM)) != cudaSuccess) return e;
+  if ((e = set_smem(bwd_state_grads_tc_kernel<Tin>, STATE_TC_SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(bwd_wy_grads_kernel<Tin>, WY_SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(bwd_assemble_kernel<Tin>, ASM_SMEM)) != cudaSuccess) return e;
   const int nch = (a.max_seqlen + C - 1) / C;
@@ -1070,7 +1142,7 @@ cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
   }
   bwd_rev_chain_kernel<Tin><<<chains, NTC, REV_SMEM, s>>>(a);
   if (nch > 0) {
-    bwd_state_grads_kernel<Tin><<<chunks, NT, STATE_SMEM, s>>>(a);
+    bwd_state_grads_tc_kernel<Tin><<<chunks, NT, STATE_TC_SMEM, s>>>(a);
     bwd_wy_grads_kernel<Tin><<<chunks, NT, WY_SMEM, s>>>(a);
     bwd_assemble_kernel<Tin><<<halves, NT, ASM_SMEM, s>>>(a);
   }
