@@ -83,8 +83,11 @@ struct PLayout {
   static constexpr uint32_t B_ROWS = 2 * WP, B_BLOCK = B_ROWS * 128, B_TILE = 2 * B_BLOCK;
   static constexpr uint32_t BT = STAGES * STATE_BYTES;
   static constexpr uint32_t OH = BT + 2 * B_TILE;
+  // Oh buffers: four with two math teams (item n uses n % 4, so a team's item waits for the epilogue of
+  // the item four back, not two back, which the state warps reach one item late), two with one team
+  static constexpr int OHB = TEAMS == 2 ? 4 : 2;
   static constexpr uint32_t RAW_BYTES = (uint32_t)((sizeof(Raw<WP>) + 127) / 128 * 128);
-  static constexpr uint32_t RAW = OH + 2 * WP * D * 4;
+  static constexpr uint32_t RAW = OH + OHB * WP * D * 4;
   static constexpr uint32_t WORK = RAW + 2 * TEAMS * RAW_BYTES;
   static constexpr uint32_t WORK_BYTES = (uint32_t)((sizeof(Work<WP>) + 127) / 128 * 128);
   static constexpr uint32_t BARS = WORK + TEAMS * WORK_BYTES;
@@ -207,9 +210,10 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
   Work<WP>& wk = *reinterpret_cast<Work<WP>*>(sm + L::WORK);
   uint64_t* full_s = reinterpret_cast<uint64_t*>(sm + L::BARS);  // state copy landed      [2]
   uint64_t* full_w = full_s + 2;                                  // Qh / Oh written         [2]
-  uint64_t* empty_w = full_s + 4;                                 // Qh / Oh consumed        [2]
-  uint64_t* mma_bar = full_s + 6;                                 // product complete        [2]
-  uint64_t* full_r = full_s + 8;                                  // raw inputs landed       [2 * TEAMS]
+  uint64_t* empty_w = full_s + 4;                                 // Oh consumed             [4]
+  uint64_t* mma_bar = full_s + 8;                                 // product complete        [2]
+  uint64_t* full_r = full_s + 10;                                 // raw inputs landed       [2 * TEAMS]
+  constexpr int OHM = L::OHB - 1;                                 // Oh buffer of item n: n & OHM
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + L::BARS + 112);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = B * H;
@@ -220,10 +224,10 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
   // setup: barriers, tensor memory, beta past the window
   constexpr int TEAMS = L::TEAMS;
   if (tid == 0) {
+    for (int i = 0; i < 4; ++i) tc::bar_init(&empty_w[i], ST);
     for (int i = 0; i < 2; ++i) {
       tc::bar_init(&full_s[i], 1);
       tc::bar_init(&full_w[i], MT / TEAMS);  // every thread of the team that computed the item
-      tc::bar_init(&empty_w[i], ST);
       tc::bar_init(&mma_bar[i], 4);  // one commit per issuing thread
     }
     for (int i = 0; i < 2 * TEAMS; ++i) tc::bar_init(&full_r[i], 1 + W);  // TMA issuer + a cp.async per beta
@@ -326,7 +330,10 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
 
       // 3. per channel, both paths: x = (I + A)^-1 diag(beta) y by forward substitution, then P x, for y = K o e^G
       //    (Qh = Q o e^G - P x, into B tile n%2) and y = V (Oh = P x, into its buffer)
-      if (n >= 2 && !tc::bar_wait(&empty_w[n & 1], ((n >> 1) + 1) & 1) && ttid == 0)
+      // B tile n % 2 was read by item n-2's product; Oh buffer n % 4 by item n-4's epilogue
+      if (n >= 2 && !tc::bar_wait(&mma_bar[n & 1], ((n >> 1) + 1) & 1) && ttid == 0)
+        flag_status(status, KDA_DEV_TIMEOUT);
+      if (n >= 4 && !tc::bar_wait(&empty_w[n & OHM], ((n >> 2) + 1) & 1) && ttid == 0)
         flag_status(status, KDA_DEV_TIMEOUT);
       {
         float xk[WP], xv[WP], rk[WP], rv[WP];
@@ -354,7 +361,7 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
             rv[t] = fmaf(pp, xv[u], rv[t]);
           }
         uint8_t* bt = sm + L::BT + (n & 1) * L::B_TILE + (uint32_t)(c >> 6) * L::B_BLOCK;
-        float* oh = reinterpret_cast<float*>(sm + L::OH) + (n & 1) * WP * D;
+        float* oh = reinterpret_cast<float*>(sm + L::OH) + (n & OHM) * WP * D;
 #pragma unroll
         for (int t = 0; t < WP; ++t) {
           const bf16 hh = __float2bfloat16_rn(rk[t]);
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
           for (int e = 0; e < 16; ++e) d[q + e] += d2[e];
         }
       }
-      const float* oh = reinterpret_cast<const float*>(sm + L::OH) + (m & 1) * WP * D;
+      const float* oh = reinterpret_cast<const float*>(sm + L::OH) + (m & OHM) * WP * D;
       if (ok && done) {
         constexpr int TH = WP / 2;
 #pragma unroll
@@ -550,7 +557,7 @@ __global__ void __launch_bounds__(NT, 1) verify_tc_kernel(const __grid_constant_
         if (sidx == 0) add_work(status, W);
       }
       tc::fence_before_sync();
-      tc::bar_arrive(&empty_w[m & 1]);
+      tc::bar_arrive(&empty_w[m & OHM]);
     };
     if (sidx == 0)
       for (int n = 0; n < STAGES && n < cnt; ++n) issue_state(n, slot_ids[item_index(n) / H]);
