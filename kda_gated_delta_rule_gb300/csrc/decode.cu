@@ -212,21 +212,6 @@ __global__ void __launch_bounds__(WCfg<D>::NT, 2) fold_kernel(float* pool, int n
   if (tid == 0) add_work(status, n);
 }
 
-// Loads a lane's rows of the warp's 16 columns from a row-major [D][D] fp32 state in shared memory.
-template <int D>
-__device__ __forceinline__ void wload_shared(float2 (&S)[WRows<D>::P][4], const float* src, int warp, int lane) {
-  const float* p = src + (lane >> 2) * D + 16 * warp + 4 * (lane & 3);
-#pragma unroll
-  for (int i = 0; i < WRows<D>::P; ++i) {
-    const float4 x0 = *reinterpret_cast<const float4*>(p + 16 * i * D);
-    const float4 x1 = *reinterpret_cast<const float4*>(p + (16 * i + 8) * D);
-    S[i][0] = make_float2(x0.x, x1.x);
-    S[i][1] = make_float2(x0.y, x1.y);
-    S[i][2] = make_float2(x0.z, x1.z);
-    S[i][3] = make_float2(x0.w, x1.w);
-  }
-}
-
 // The fold as a stream: two persistent CTAs per SM walk the (request, head) units with stride gridDim.x,
 // skipping units with nothing accepted.  While a unit replays from registers, the next unit's state is on
 // its way into shared memory (one bulk copy) and its recorded tokens follow with cp.async, so every SM
@@ -319,6 +304,87 @@ __global__ void __launch_bounds__(WCfg<D>::NT, 2) fold_stream_kernel(float* pool
   }
 }
 
+// Decode as a stream, the same scheme as the fold stream: two persistent CTAs per SM walk the
+// (request, head) units with stride gridDim.x; the next unit's state is bulk-copied into shared memory and
+// its token follows with cp.async while the current unit steps and stores from registers.  The step is the
+// same wstep as the one-unit-per-CTA decode, so outputs and state bits do not depend on which ran.
+template <int D, typename Tin>
+struct DecodeStreamSmem {
+  static constexpr size_t STAGE = (size_t)D * D * 4;
+  static constexpr size_t RAW = STAGE;
+  static constexpr size_t TOK = RAW + 2 * sizeof(RawGroup<D, Tin>);
+  static constexpr size_t BAR = TOK + sizeof(WTok<D>);
+  static constexpr size_t BYTES = BAR + 16;
+};
+
+template <int D, typename Tin, typename Tout>
+__global__ void __launch_bounds__(WCfg<D>::NT, 2) decode_stream_kernel(const Tin* __restrict__ q,
+                                                                        const Tin* __restrict__ k,
+                                                                        const Tin* __restrict__ v,
+                                                                        const float* __restrict__ g,
+                                                                        const float* __restrict__ beta, int H,
+                                                                        float* pool, int num_slots,
+                                                                        const int32_t* __restrict__ slot_ids,
+                                                                        Tout* __restrict__ out, int32_t* status,
+                                                                        int units) {
+  using L = DecodeStreamSmem<D, Tin>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* stage = reinterpret_cast<float*>(smem);
+  RawGroup<D, Tin>* raw = reinterpret_cast<RawGroup<D, Tin>*>(smem + L::RAW);
+  WTok<D>* tok = reinterpret_cast<WTok<D>*>(smem + L::TOK);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L::BAR);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the first unit at or after u whose request has a valid slot (every thread computes it)
+  auto next_unit = [&](int u) {
+    for (; u < units; u += (int)gridDim.x) {
+      const int slot = slot_ids[u / H];
+      if (slot >= 0 && slot < num_slots) break;
+      if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    }
+    return u;
+  };
+  // requests unit u's state (thread 0) and its token (row u of the [B, H] inputs) into raw[buf]
+  auto prefetch = [&](int u, int buf) {
+    if (tid == 0) {
+      tc::bar_arrive_expect_tx(bar, (uint32_t)L::STAGE);
+      tc::bulk_g2s(stage, pool + ((size_t)slot_ids[u / H] * H + u % H) * D * D, (uint32_t)L::STAGE, bar);
+    }
+    fetch_tokens<D, Tin, true>(raw + buf, k, q, v, g, beta, (size_t)u, 0, 1, tid, WCfg<D>::NT);
+  };
+  if (tid == 0) {
+    tc::bar_init(bar, 1);
+    tc::bar_fence_init();
+  }
+  __syncthreads();
+  int u = next_unit((int)blockIdx.x);
+  if (u < units) prefetch(u, 0);
+  bool ok = true;
+  float2 S[WRows<D>::P][4];
+#pragma unroll 1
+  for (int it = 0; u < units; ++it) {
+    const int buf = it & 1;
+    const bool landed = tc::bar_wait(bar, (uint32_t)it & 1u);
+    cp_async_wait_all();
+    ok = __syncthreads_and(landed) != 0;
+    if (!ok) break;
+    wload_shared<D>(S, stage, warp, lane);
+    unpack_tokens<D, Tin, true, false>(tok, raw + buf, 0, 0, 1, tid, nullptr);
+    __syncthreads();  // the stage has been read and the token unpacked
+    const int un = next_unit(u + (int)gridDim.x);
+    if (un < units) prefetch(un, buf ^ 1);
+    const float o = wstep<D, true>(S, tok[0], warp, lane);
+    if (((lane >> 2) & 1) == 0) out[(size_t)u * D + wstep_out_col(warp, lane)] = from_f32<Tout>(o);
+    wstore<D>(S, pool + ((size_t)slot_ids[u / H] * H + u % H) * D * D, warp, lane);
+    if (tid == 0) add_work(status, 1);
+    u = un;
+  }
+  if (!ok) {  // the state copy did not land in time: report it and give the copy one more bounded wait
+    if (tid == 0) flag_status(status, KDA_DEV_TIMEOUT);
+    tc::bar_wait(bar, 0u);
+    tc::bar_wait(bar, 1u);
+  }
+}
+
 // ---------------------------------------------------------------- launchers
 
 template <int D, typename Tin, typename Tout>
@@ -326,6 +392,21 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   decode_kernel<D, Tin, Tout><<<a.B * a.H, WCfg<D>::NT, 0, s>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.H,
       a.pool, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.status);
+  return cudaGetLastError();
+}
+
+template <int D, typename Tin, typename Tout>
+static cudaError_t launch_decode_stream_t(const DecodeArgs& a, cudaStream_t s) {
+  using L = DecodeStreamSmem<D, Tin>;
+  cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<D, Tin, Tout>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::BYTES);
+  if (e != cudaSuccess) return e;
+  const int units = a.B * a.H, sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = units < 2 * sms ? units : 2 * sms;
+  decode_stream_kernel<D, Tin, Tout><<<grid, WCfg<D>::NT, L::BYTES, s>>>(
+      static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.H,
+      a.pool, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.status, units);
   return cudaGetLastError();
 }
 
@@ -364,7 +445,7 @@ static cudaError_t decode_d(const DecodeArgs& a, cudaStream_t s) {
     case 16: return launch_decode_t<16, Tin, Tout>(a, s);
     case 32: return launch_decode_t<32, Tin, Tout>(a, s);
     case 64: return launch_decode_t<64, Tin, Tout>(a, s);
-    case 128: return launch_decode_t<128, Tin, Tout>(a, s);
+    case 128: return launch_decode_stream_t<128, Tin, Tout>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

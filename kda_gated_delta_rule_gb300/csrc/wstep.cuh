@@ -136,6 +136,21 @@ __device__ __forceinline__ void wload(float2 (&S)[WRows<D>::P][4], const float* 
   }
 }
 
+// Loads a lane's rows of the warp's 16 columns from a row-major [D][D] fp32 state in shared memory.
+template <int D>
+__device__ __forceinline__ void wload_shared(float2 (&S)[WRows<D>::P][4], const float* src, int warp, int lane) {
+  const float* p = src + (lane >> 2) * D + 16 * warp + 4 * (lane & 3);
+#pragma unroll
+  for (int i = 0; i < WRows<D>::P; ++i) {
+    const float4 x0 = *reinterpret_cast<const float4*>(p + 16 * i * D);
+    const float4 x1 = *reinterpret_cast<const float4*>(p + (16 * i + 8) * D);
+    S[i][0] = make_float2(x0.x, x1.x);
+    S[i][1] = make_float2(x0.y, x1.y);
+    S[i][2] = make_float2(x0.z, x1.z);
+    S[i][3] = make_float2(x0.w, x1.w);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void wstore(const float2 (&S)[WRows<D>::P][4], float* dst, int warp, int lane) {
   float* p = dst + (size_t)(lane >> 2) * D + 16 * warp + 4 * (lane & 3);

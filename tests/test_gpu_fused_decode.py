@@ -17,9 +17,11 @@ pytestmark = pytest.mark.gpu
 TOL = 2e-3
 
 
+@pytest.mark.parametrize("B,H,S,steps", [(6, 3, 10, 4), (48, 8, 64, 2)], ids=["B6H3", "B48H8"])
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F32], ids=["bf16", "f32"])
-def test_fused_decode_steps_match_oracle(cuda, dtype):
-    B, H, d, S, steps = 6, 3, 128, 10, 4
+def test_fused_decode_steps_match_oracle(cuda, dtype, B, H, S, steps):
+    """B48H8: 384 (request, head) units, more than the two persistent CTAs per SM take in one round."""
+    d = 128
     p = synth.fused_decode_inputs(71, B, H, d, S, steps, dtype)
     pool, cstate = dev(p["pool"]), dev(p["conv_state"])
     slots, cw, nw = dev(p["slot_ids"]), dev(p["conv_w"]), dev(p["norm_w"])
