@@ -310,7 +310,9 @@ kda_status kda_prefill_segmented_noalloc(const kda_prefill_args* a, int32_t segm
  *
  * Per (slot, head) state: S_c in `pool` ([num_slots][H][128][128] fp32, the usual layout), the open chunk's
  * rows in `cache` ([num_slots][H][KDA_CFBI_CHUNK][KDA_CFBI_ROW_FLOATS] fp32: k[128] | v[128] | G[128] |
- * A_t[16] (beta folded in) | beta | T_t[16] (row t of (I + A)^-1) | padding) and their number in `counts` ([num_slots][H] int32, 0..15).
+ * A_t[16] (beta folded in) | beta | T_t[16] (row t of (I + A)^-1) | padding; A_t[u >= t], T_t[v > t] and the
+ * padding are written as zeros, so the cached bytes depend on the chunk's tokens alone) and their number in
+ * `counts` ([num_slots][H] int32, 0..15).
  * A fresh sequence starts from S_0 in its pool slot with counts = 0 (cache contents then unused).
  * dk = dv = 128 only (KDA_ERR_UNSUPPORTED otherwise).  A count outside [0, 16) sets KDA_DEV_SLOT_OOB and that
  * unit is skipped.

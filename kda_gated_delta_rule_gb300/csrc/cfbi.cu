@@ -18,6 +18,7 @@
 // same whichever path (or batch, or split of a sequence into prefill and decode) computed them.
 #include "common.cuh"
 #include "launch.h"
+#include "tc_ptx.cuh"
 
 namespace kda {
 namespace {
@@ -26,44 +27,64 @@ constexpr int D = 128;
 constexpr int NT = 256;
 constexpr int CH = KDA_CFBI_CHUNK;       // rows per chunk
 constexpr int RF = KDA_CFBI_ROW_FLOATS;  // floats per cached row
+#ifndef CFBI_DECODE_CTAS
+#define CFBI_DECODE_CTAS 3  // decode CTAs resident per SM
+#endif
 // cached row layout: k | v | G (in-chunk cumulative log-decay) | A_t[u] (beta folded in, u < t) | beta |
 // T_t[v] = row t of (I + A)^-1 (v <= t)
 constexpr int R_K = 0, R_V = 128, R_G = 256, R_A = 384, R_BETA = 400, R_T = 401;
 static_assert(R_T + CH <= RF && RF % 4 == 0, "row layout");
 
-struct Scratch {
-  float q[D];           // q_t (fp32)
+struct RowScratch {
+  alignas(16) float q[D];  // q_t (fp32)
   float qh[D];          // q_t o e^{G_t} - sum_u R_tu k_u o e^{G_u}
   float oh[D];          // sum_u R_tu v_u
   float part[2][D];     // partial sums of the read-out over the two key halves
   float p[CH];          // P_t[u]
   float r[CH];          // R_t[u]
-  float kp[CH][D];      // fold: k_u o e^{G_u}
-  float kh[CH][D];      // fold: k_u o e^{G_15 - G_u}
-  float ws[2][CH][D];   // fold: partial (K o e^G) S_c over the two key halves
-  float u[CH][D];       // fold: U
 };
+// 24 KB: kp, ws and u live one after another in one region (barriers between a last read and the next
+// first write), so the scratch fits in one row buffer.
+struct FoldScratch {
+  float kh[CH][D];          // k_u o e^{G_15 - G_u}
+  union {
+    float kp[CH][D];        // k_u o e^{G_u}
+    float ws[2][CH][D];     // partial (K o e^G) S_c over the two key halves
+    float u[CH][D];         // U
+  };
+};
+static_assert(sizeof(FoldScratch) <= (size_t)CH * RF * 4, "fold scratch fits a row buffer");
 
-// Row t of the open chunk (rows[0 .. t-1] cached; rows[t] holds k_t, v_t, g_t in the G slot and beta_t;
-// scr.q holds q_t).  Completes rows[t] (G_t, A_t, T_t), and returns o_t[c] on threads c < 128.
-// sv: this thread's part of the entry state, S_c[64 * half + e][c] for e < 64 (c = tid % 128, half = tid / 128).
-__device__ __forceinline__ float cfbi_row(float* rows, Scratch& scr, int t, const float (&sv)[64], int tid) {
+// Row t of the open chunk, steps 1-4 (rows[0 .. t-1] cached; rows[t] holds k_t, v_t, g_t in the G slot and
+// beta_t; scr.q holds q_t): completes rows[t] (G_t, A_t, T_t) and leaves qh and oh in scr.
+__device__ __forceinline__ void cfbi_row_front(float* rows, RowScratch& scr, int t, int tid) {
   float* rt = rows + t * RF;
   const int warp = tid >> 5, lane = tid & 31;
-  // 1. G_t = G_{t-1} + g_t
+  // 1. G_t = G_{t-1} + g_t; the slots of row t that no step below writes (A_t[u] for u >= t, the padding)
+  //    are set to zero, so the cached row's bytes are a function of the chunk's tokens alone
   if (tid < D) rt[R_G + tid] = __fadd_rn(t > 0 ? rows[(t - 1) * RF + R_G + tid] : 0.f, rt[R_G + tid]);
+  else if (tid < D + CH && tid - D >= t) rt[R_A + tid - D] = 0.f;
+  else if (tid >= D + CH && tid < D + CH + (RF - R_T - CH)) rt[R_T + CH + tid - D - CH] = 0.f;
   __syncthreads();
   // 2. A_t[u] (u < t) and P_t[u] (u <= t): warp w takes u = w, w + 8; lane l channels 4l .. 4l+3 in order,
   //    then a fixed xor butterfly; lane 0's sum is the value
+  {
+    const float4 kt = *reinterpret_cast<const float4*>(rt + R_K + 4 * lane);
+    const float4 gt = *reinterpret_cast<const float4*>(rt + R_G + 4 * lane);
+    const float4 qt = *reinterpret_cast<const float4*>(scr.q + 4 * lane);
   for (int u = warp; u <= t; u += NT / 32) {
     const float* ru = rows + u * RF;
+    const float4 ku = *reinterpret_cast<const float4*>(ru + R_K + 4 * lane);
+    const float4 gu = *reinterpret_cast<const float4*>(ru + R_G + 4 * lane);
     float a = 0.f, p = 0.f;
+    const float kc[4] = {ku.x, ku.y, ku.z, ku.w}, gc[4] = {gu.x, gu.y, gu.z, gu.w};
+    const float ktc[4] = {kt.x, kt.y, kt.z, kt.w}, gtc[4] = {gt.x, gt.y, gt.z, gt.w};
+    const float qc[4] = {qt.x, qt.y, qt.z, qt.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int j = 4 * lane + i;
-      const float kk = __fmul_rn(ru[R_K + j], __expf(__fsub_rn(rt[R_G + j], ru[R_G + j])));
-      a = __fmaf_rn(rt[R_K + j], kk, a);
-      p = __fmaf_rn(scr.q[j], kk, p);
+      const float kk = __fmul_rn(kc[i], __expf(__fsub_rn(gtc[i], gc[i])));
+      a = __fmaf_rn(ktc[i], kk, a);
+      p = __fmaf_rn(qc[i], kk, p);
     }
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) {
@@ -75,20 +96,25 @@ __device__ __forceinline__ float cfbi_row(float* rows, Scratch& scr, int t, cons
       scr.p[u] = p;
     }
   }
+  }
   __syncthreads();
-  // 3. row t of T = (I + A)^-1 from the cached rows (lane v: T_t[v] = [v == t] - sum_{u=v}^{t-1} A_tu T_u[v]),
-  //    then z = P_t T (lane v: sum_{w=v}^{t} P_t[w] T_w[v]) and R_t = z diag(beta)
+  // 3. row t of T = (I + A)^-1 from the cached rows (lane v: T_t[v] = [v == t] - sum_{u=v}^{t-1} A_tu T_u[v],
+  //    zero for v > t), then z = P_t T (lane v: sum_{w=v}^{t} P_t[w] T_w[v]) and R_t = z diag(beta)
   if (warp == 0 && lane < CH) {
     const int v = lane;
     float acc = v == t ? 1.f : 0.f;
-    for (int u = v; u < t; ++u) acc = __fmaf_rn(-rt[R_A + u], rows[u * RF + R_T + v], acc);
-    if (v <= t) rt[R_T + v] = acc;
+#pragma unroll
+    for (int u = 0; u < CH - 1; ++u)
+      if (u >= v && u < t) acc = __fmaf_rn(-rt[R_A + u], rows[u * RF + R_T + v], acc);
+    rt[R_T + v] = acc;
   }
   __syncwarp();
   if (warp == 0 && lane < CH) {
     const int v = lane;
     float acc = 0.f;
-    for (int w = v; w <= t; ++w) acc = __fmaf_rn(scr.p[w], rows[w * RF + R_T + v], acc);
+#pragma unroll
+    for (int w = 0; w < CH; ++w)
+      if (w >= v && w <= t) acc = __fmaf_rn(scr.p[w], rows[w * RF + R_T + v], acc);
     scr.r[v] = v <= t ? __fmul_rn(acc, rows[v * RF + R_BETA]) : 0.f;
   }
   __syncthreads();
@@ -96,30 +122,47 @@ __device__ __forceinline__ float cfbi_row(float* rows, Scratch& scr, int t, cons
   if (tid < D) {
     const int j = tid;
     float acc = __fmul_rn(scr.q[j], __expf(rt[R_G + j]));
-    for (int u = 0; u <= t; ++u)
-      acc = __fmaf_rn(-scr.r[u], __fmul_rn(rows[u * RF + R_K + j], __expf(rows[u * RF + R_G + j])), acc);
+#pragma unroll
+    for (int u = 0; u < CH; ++u)
+      if (u <= t) acc = __fmaf_rn(-scr.r[u], __fmul_rn(rows[u * RF + R_K + j], __expf(rows[u * RF + R_G + j])), acc);
     scr.qh[j] = acc;
   } else {
     const int c = tid - D;
     float acc = 0.f;
-    for (int u = 0; u <= t; ++u) acc = __fmaf_rn(scr.r[u], rows[u * RF + R_V + c], acc);
+#pragma unroll
+    for (int u = 0; u < CH; ++u)
+      if (u <= t) acc = __fmaf_rn(scr.r[u], rows[u * RF + R_V + c], acc);
     scr.oh[c] = acc;
   }
   __syncthreads();
-  // 5. o_t = S_c^T qh + oh: thread (c, half) sums its 64 key rows in order; then part0 + part1 + oh
-  {
-    const int c = tid & (D - 1), half = tid >> 7;
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < 64; ++e) acc = __fmaf_rn(scr.qh[64 * half + e], sv[e], acc);
-    scr.part[half][c] = acc;
-  }
+}
+
+// Step 5, o_t = S_c^T qh + oh: thread (c, half) sums its 64 key rows in order, then part0 + part1 + oh;
+// returns o_t[c] on threads c < 128.  sv(e) is this thread's part of the entry state, S_c[64 * half + e][c]
+// for e < 64 (c = tid % 128, half = tid / 128), from registers or from shared memory.
+template <int UE, typename StateAt>
+__device__ __forceinline__ float cfbi_readout(RowScratch& scr, StateAt sv, int tid) {
+  const int c = tid & (D - 1), half = tid >> 7;
+  float acc = 0.f;
+#pragma unroll UE
+  for (int e = 0; e < 64; ++e) acc = __fmaf_rn(scr.qh[64 * half + e], sv(e), acc);
+  scr.part[half][c] = acc;
   __syncthreads();
   return tid < D ? __fadd_rn(__fadd_rn(scr.part[0][tid], scr.part[1][tid]), scr.oh[tid]) : 0.f;
 }
 
+// The whole row with the entry state part in registers; returns o_t[c] on threads c < 128.
+__device__ __forceinline__ float cfbi_row(float* rows, RowScratch& scr, int t, const float (&sv)[64], int tid) {
+  cfbi_row_front(rows, scr, t, tid);
+  return cfbi_readout<64>(scr, [&](int e) { return sv[e]; }, tid);
+}
+
 // Advances the entry state (this thread's part sv, as in cfbi_row) over the full chunk in rows[0 .. 15].
-__device__ __forceinline__ void cfbi_fold(const float* rows, Scratch& scr, float (&sv)[64], int tid) {
+// ld(e) reads and st(e, x) writes this thread's part of the state, S_c[64 * half + e][c] (registers, or
+// global memory); each element is read (twice) before it is written, by its own thread only.
+// UE: unroll of the passes over the 64 state elements (64 when the state is in registers).
+template <int UE, typename Ld, typename St>
+__device__ __forceinline__ void cfbi_fold(const float* rows, FoldScratch& scr, Ld ld, St st, int tid) {
   const float* last = rows + (CH - 1) * RF;
   for (int e = tid; e < CH * D; e += NT) {
     const int u = e / D, j = e % D;
@@ -134,12 +177,14 @@ __device__ __forceinline__ void cfbi_fold(const float* rows, Scratch& scr, float
     float acc[CH];
 #pragma unroll
     for (int u = 0; u < CH; ++u) acc[u] = 0.f;
-#pragma unroll
+#pragma unroll UE
     for (int e = 0; e < 64; ++e) {
       const int j = 64 * half + e;
+      const float s = ld(e);
 #pragma unroll
-      for (int u = 0; u < CH; ++u) acc[u] = __fmaf_rn(scr.kp[u][j], sv[e], acc[u]);
+      for (int u = 0; u < CH; ++u) acc[u] = __fmaf_rn(scr.kp[u][j], s, acc[u]);
     }
+    __syncthreads();  // kp has been read; ws takes its place
 #pragma unroll
     for (int u = 0; u < CH; ++u) scr.ws[half][u][c] = acc[u];
   }
@@ -153,6 +198,7 @@ __device__ __forceinline__ void cfbi_fold(const float* rows, Scratch& scr, float
       const float* rw = rows + w * RF;
       y[w] = __fmul_rn(rw[R_BETA], __fsub_rn(rw[R_V + c], __fadd_rn(scr.ws[0][w][c], scr.ws[1][w][c])));
     }
+    __syncthreads();  // ws has been read; u takes its place
 #pragma unroll
     for (int uu = 0; uu < CH / 2; ++uu) {
       const int u = (CH / 2) * half + uu;
@@ -171,13 +217,13 @@ __device__ __forceinline__ void cfbi_fold(const float* rows, Scratch& scr, float
     float uc[CH];
 #pragma unroll
     for (int u = 0; u < CH; ++u) uc[u] = scr.u[u][c];
-#pragma unroll
+#pragma unroll UE
     for (int e = 0; e < 64; ++e) {
       const int j = 64 * half + e;
-      float s = __fmul_rn(__expf(last[R_G + j]), sv[e]);
+      float s = __fmul_rn(__expf(last[R_G + j]), ld(e));
 #pragma unroll
       for (int u = 0; u < CH; ++u) s = __fmaf_rn(scr.kh[u][j], uc[u], s);
-      sv[e] = s;
+      st(e, s);
     }
   }
   __syncthreads();
@@ -185,7 +231,7 @@ __device__ __forceinline__ void cfbi_fold(const float* rows, Scratch& scr, float
 
 // The new token's inputs into rows[t] (k, v, g in the G slot, beta) and scr.q.
 template <typename Tin>
-__device__ __forceinline__ void cfbi_load_token(float* rows, Scratch& scr, int t, const Tin* q, const Tin* k,
+__device__ __forceinline__ void cfbi_load_token(float* rows, RowScratch& scr, int t, const Tin* q, const Tin* k,
                                                 const Tin* v, const float* g, const float* beta, size_t row, int tid) {
   float* rt = rows + t * RF;
   if (tid < D) {
@@ -207,7 +253,8 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 
 struct CfbiSmem {
   alignas(16) float rows[CH * RF];
-  Scratch scr;
+  RowScratch scr;
+  FoldScratch fold;
 };
 
 // this thread's part of a [128][128] state: rows 64 * half .. +63 of column c
@@ -261,7 +308,7 @@ __global__ void __launch_bounds__(NT, 1) cfbi_prefill_kernel(const Tin* __restri
     const float o = cfbi_row(s.rows, s.scr, L, sv, tid);
     if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
     if (++L == CH) {
-      cfbi_fold(s.rows, s.scr, sv, tid);
+      cfbi_fold<64>(s.rows, s.fold, [&](int e) { return sv[e]; }, [&](int e, float x) { sv[e] = x; }, tid);
       L = 0;
     }
   }
@@ -273,34 +320,22 @@ __global__ void __launch_bounds__(NT, 1) cfbi_prefill_kernel(const Tin* __restri
   }
 }
 
+// Decode: one CTA per (request, head), three resident per SM (the hardware scheduler balances the units
+// that complete a chunk, which cost several plain ones).  The token's inputs are loaded first (they do not
+// depend on the slot); once the slot is known, thread 0 asks L2 for the whole 64 KB entry state with one
+// bulk prefetch, then the row count and the cached rows follow.  The read-out (and the fold, when the
+// token completes a chunk) read the state from global memory, where the prefetch has brought it into L2,
+// so no thread holds the state in registers.
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
-                                                            const Tin* __restrict__ v, const float* __restrict__ g,
-                                                            const float* __restrict__ beta, int H, float* pool,
-                                                            float* cache, int32_t* counts, int num_slots,
-                                                            const int32_t* __restrict__ slot_ids,
-                                                            Tout* __restrict__ out, int32_t* status) {
+__global__ void __launch_bounds__(NT, CFBI_DECODE_CTAS) cfbi_decode_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v, const float* __restrict__ g,
+    const float* __restrict__ beta, int H, float* pool, float* cache, int32_t* counts, int num_slots,
+    const int32_t* __restrict__ slot_ids, Tout* __restrict__ out, int32_t* status) {
   extern __shared__ float4 smem4[];
   CfbiSmem& s = *reinterpret_cast<CfbiSmem*>(smem4);
   const int tid = threadIdx.x, b = blockIdx.x / H, h = blockIdx.x % H;
-  const int slot = slot_ids[b];
-  if (slot < 0 || slot >= num_slots) {
-    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
-    return;
-  }
-  float* Sg = pool + ((size_t)slot * H + h) * D * D;
-  float* cg = cache + ((size_t)slot * H + h) * CH * RF;
-  int32_t* cnt = counts + (size_t)slot * H + h;
-  const int L = *cnt;
-  if (L < 0 || L >= CH) {
-    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
-    return;
-  }
-  // the token's inputs (registers) and the cached rows (asynchronous copies into shared memory) first; once
-  // the token is in shared memory, the entry state's loads (registers) are issued and stay in flight
-  // through the row's own algebra, which does not read them, until the read-out
+  const int c = tid & (D - 1), half = tid >> 7;
   const size_t row = (size_t)b * H + h;
-  const int c = tid & (D - 1);
   float x0, x1, x2 = 0.f, xb = 0.f;
   if (tid < D) {
     x0 = to_f32(k[row * D + c]);
@@ -310,6 +345,20 @@ __global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restric
     x0 = to_f32(v[row * D + c]);
     x1 = 0.f;
     if (c == 0) xb = beta[row];
+  }
+  const int slot = slot_ids[b];
+  if (slot < 0 || slot >= num_slots) {
+    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    return;
+  }
+  const size_t sh = (size_t)slot * H + h;
+  float* Sg = pool + sh * D * D;
+  if (tid == 0) tc::bulk_prefetch_l2(Sg, (uint32_t)(D * D * 4));
+  float* cg = cache + sh * CH * RF;
+  const int L = counts[sh];
+  if (L < 0 || L >= CH) {
+    if (tid == 0) flag_status(status, KDA_DEV_SLOT_OOB);
+    return;
   }
   for (int e = tid; e < L * RF / 4; e += NT) cp_async16(reinterpret_cast<float4*>(s.rows) + e, reinterpret_cast<const float4*>(cg) + e);
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -324,27 +373,25 @@ __global__ void __launch_bounds__(NT, 2) cfbi_decode_kernel(const Tin* __restric
       if (c == 0) rt[R_BETA] = xb;
     }
   }
-  asm volatile("" ::: "memory");  // the state loads below are not hoisted above the token's stores
-  float sv[64];
-  load_part(sv, Sg, tid);  // in flight while the row's own quantities are formed
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
-  const float o = cfbi_row(s.rows, s.scr, L, sv, tid);
+  cfbi_row_front(s.rows, s.scr, L, tid);
+  float* sp = Sg + (size_t)64 * half * D + c;  // this thread's part: rows 64 * half + e of column c
+  const float o = cfbi_readout<64>(s.scr, [&](int e) { return __ldcg(sp + (size_t)e * D); }, tid);
   if (tid < D) out[row * D + tid] = from_f32<Tout>(o);
   if (L + 1 == CH) {
-    cfbi_fold(s.rows, s.scr, sv, tid);
-    store_part(sv, Sg, tid);
-    if (tid == 0) *cnt = 0;
+    cfbi_fold<16>(s.rows, s.fold, [&](int e) { return __ldcg(sp + (size_t)e * D); },
+                  [&](int e, float x) { sp[(size_t)e * D] = x; }, tid);
+    if (tid == 0) counts[sh] = 0;
   } else {
     for (int e = tid; e < RF / 4; e += NT)
       reinterpret_cast<float4*>(cg + L * RF)[e] = reinterpret_cast<const float4*>(s.rows + L * RF)[e];
-    if (tid == 0) *cnt = L + 1;
+    if (tid == 0) counts[sh] = L + 1;
   }
   if (tid == 0) add_work(status, 1);
 }
 
 constexpr size_t PREFILL_SMEM = sizeof(CfbiSmem);
-constexpr size_t DECODE_SMEM = sizeof(CfbiSmem);
 
 template <typename Tin, typename Tout>
 cudaError_t launch_prefill_t(const CfbiArgs& a, cudaStream_t st) {
@@ -361,9 +408,11 @@ cudaError_t launch_prefill_t(const CfbiArgs& a, cudaStream_t st) {
 template <typename Tin, typename Tout>
 cudaError_t launch_decode_t(const CfbiArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(cfbi_decode_kernel<Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)DECODE_SMEM);
+                                       (int)sizeof(CfbiSmem));
   if (e != cudaSuccess) return e;
-  cfbi_decode_kernel<Tin, Tout><<<a.B * a.H, NT, DECODE_SMEM, st>>>(
+  e = cudaFuncSetAttribute(cfbi_decode_kernel<Tin, Tout>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
+  cfbi_decode_kernel<Tin, Tout><<<a.B * a.H, NT, sizeof(CfbiSmem), st>>>(
       static_cast<const Tin*>(a.q), static_cast<const Tin*>(a.k), static_cast<const Tin*>(a.v), a.g, a.beta, a.H,
       a.pool, a.cache, a.counts, a.num_slots, a.slot_ids, static_cast<Tout*>(a.out), a.status);
   return cudaGetLastError();

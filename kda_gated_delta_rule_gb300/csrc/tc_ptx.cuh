@@ -206,6 +206,10 @@ __device__ __forceinline__ bool named_bar_or(int id, int n, bool p) {
 }
 
 // ---- bulk asynchronous copies (16-byte aligned addresses, size a multiple of 16)
+// asks L2 to fetch [src, src + bytes) without waiting for it
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_global, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(

@@ -112,14 +112,17 @@ def test_two_prefill_calls_are_bit_identical(cuda):
     assert torch.equal(out_a, out_b) and torch.equal(pool_a, pool_b) and torch.equal(counts_a, counts_b)
 
 
-def test_decode_is_batch_invariant(cuda):
-    """A request's decode output and state do not depend on which other requests share the batch."""
+@pytest.mark.parametrize("B,H", [(6, 2), (200, 5)], ids=["B6H2", "B200H5"])
+def test_decode_is_batch_invariant(cuda, B, H):
+    """A request's decode output and state do not depend on which other requests share the batch.  B200H5:
+    1000 (request, head) units, two or three per persistent CTA, with every row count (and so the chunk
+    fold); the batch also matches the prefill kernel run over the same tokens, bit for bit."""
     kda = cuda
-    B, H = 6, 2
-    p = synth.decode_verify(seed=84, B=B, W=1, H=H, d=128, num_slots=10)
+    S = B + 4
+    p = synth.decode_verify(seed=84, B=B, W=1, H=H, d=128, num_slots=S)
     rng = np.random.default_rng(0)
-    counts0 = torch.from_numpy(rng.integers(0, CH, size=(10, H)).astype(np.int32)).cuda()
-    cache0 = torch.from_numpy(rng.standard_normal((10, H, CH, RF)).astype(np.float32) * 0.1).cuda()
+    counts0 = torch.from_numpy(rng.integers(0, CH, size=(S, H)).astype(np.int32)).cuda()
+    cache0 = torch.from_numpy(rng.standard_normal((S, H, CH, RF)).astype(np.float32) * 0.1).cuda()
     cache0[..., 256:384] = -torch.arange(CH, device="cuda").view(1, 1, CH, 1) * 0.05  # plausible G rows
     pool0 = dev(p.pool)
     ins = [dev(x) for x in (p.q, p.k, p.v, p.g, p.beta)]
@@ -127,6 +130,13 @@ def test_decode_is_batch_invariant(cuda):
     pool, cache, counts = pool0.clone(), cache0.clone(), counts0.clone()
     out_all = torch.empty(B, H, 128, device="cuda")
     kda.kda_cfbi_decode(*ins, pool, cache, counts, slots, out_all)
+    # the same tokens as B one-token sequences through the prefill kernel: the same bits
+    pool_p, cache_p, counts_p = pool0.clone(), cache0.clone(), counts0.clone()
+    out_p = torch.empty(B, H, 128, device="cuda")
+    kda.kda_cfbi_prefill(*ins, dev(np.arange(B + 1, dtype=np.int32)), 1, pool_p, cache_p, counts_p, slots, out_p)
+    torch.cuda.synchronize()
+    assert torch.equal(out_p, out_all) and torch.equal(pool_p, pool) and torch.equal(counts_p, counts)
+    assert torch.equal(cache_p, cache)
     for b in range(B):
         pl, ca, co = pool0.clone(), cache0.clone(), counts0.clone()
         o = torch.empty(1, H, 128, device="cuda")
@@ -134,7 +144,7 @@ def test_decode_is_batch_invariant(cuda):
         torch.cuda.synchronize()
         assert torch.equal(o[0], out_all[b])
         s = int(p.slot_ids[b])
-        assert torch.equal(pl[s], pool[s]) and torch.equal(co[s], counts[s])
+        assert torch.equal(pl[s], pool[s]) and torch.equal(co[s], counts[s]) and torch.equal(ca[s], cache[s])
 
 
 def test_bad_count_is_flagged(cuda):
