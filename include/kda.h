@@ -336,6 +336,28 @@ kda_status kda_cfbi_prefill(const void* q, const void* k, const void* v, const f
                             int32_t* dev_status, kda_stream_t stream);
 
 /*
+ * kda_cfbi_prefill_chunked -- kda_cfbi_prefill's operation (same arguments, same results bit for bit:
+ * outputs, states, row caches and counts), with the chunks of every sequence worked on in parallel.
+ * Source: "Kimi K3.1 inference zero mismatch" (LLMNews), section 6.1: a position's output depends only on
+ * its chunk's entry state and the rows before it in the chunk, so the rows of all chunks (and the parts of
+ * each output that do not involve the state) are formed at once, one CTA per (chunk, sequence, head); the
+ * state then walks the chunks in order, one CTA per (8 value columns, sequence, head), each value column of
+ * the state evolving on its own.  Every element is formed by the same fp32 round-to-nearest operations in
+ * the same order as in kda_cfbi_prefill / kda_cfbi_decode.
+ * workspace: device memory of at least kda_cfbi_prefill_chunked_workspace_size(T, N, H, dk, dv) bytes,
+ * 16-byte aligned, owned by the caller, contents ignored on entry and meaningless after; smaller: returns
+ * KDA_ERR_WORKSPACE without launching.  max_seqlen bounds the sequence lengths (KDA_DEV_SEQ_OOB for a longer
+ * one, as for kda_cfbi_prefill) and sizes the grid; at most 65535 * 16 - 32.
+ */
+size_t kda_cfbi_prefill_chunked_workspace_size(int64_t T, int32_t N, int H, int dk, int dv);
+kda_status kda_cfbi_prefill_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                    const int32_t* cu_seqlens, int32_t N, int64_t T, int32_t max_seqlen, int H,
+                                    int dk, int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
+                                    int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    kda_stream_t stream);
+
+/*
  * kda_cfbi_decode -- one token per request through the CF-BI contract.  q, k, v [B][H][128] (in_dtype),
  * g [B][H][128], beta [B][H] fp32, out [B][H][128] (out_dtype).  Reads the entry state; writes it only when
  * the token completes a chunk (then counts returns to 0).

@@ -21,6 +21,7 @@ __all__ = [
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
+    "kda_cfbi_prefill_chunked_workspace_size", "kda_cfbi_prefill_chunked",
     "kda_cfbi_decode", "kda_backward_workspace_size", "kda_prefill_backward", "kda_fused_decode",
     "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs", "kda_check_slot_ids", "kda_set_debug_checks",
     "kda_debug_checks", "kda_set_test_fault", "KDA_TEST_FAULT_NONE", "KDA_TEST_FAULT_STALL_RECORD_INPUTS", "CFBI_CHUNK", "CFBI_ROW_FLOATS", "EXPORTED_SYMBOLS",
@@ -39,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "kda_prefill_workspace_size", "kda_prefill_segmented", "kda_segmented_workspace_size",
     "kda_segment_fragments", "kda_fragment_scan", "kda_segment_outputs", "kda_prefill_segmented_noalloc",
     "kda_prefill_records", "kda_prefill_chain", "kda_cfbi_cache_bytes_per_head", "kda_cfbi_prefill",
+    "kda_cfbi_prefill_chunked_workspace_size", "kda_cfbi_prefill_chunked",
     "kda_cfbi_decode", "kda_backward_args_bytes", "kda_backward_workspace_size", "kda_prefill_backward",
     "kda_fused_decode_args_bytes", "kda_fused_decode", "kda_kcp_fragments", "kda_kcp_scan", "kda_kcp_outputs",
     "kda_check_slot_ids", "kda_set_debug_checks", "kda_debug_checks", "kda_set_test_fault",
@@ -135,6 +137,9 @@ def load(build_if_missing: bool = False):
         "kda_cfbi_cache_bytes_per_head": (sz, [c_int, c_int]),
         "kda_cfbi_prefill": (c_int, [vp, vp, vp, vp, vp, vp, i32, i64, i32, c_int, c_int, c_int, c_int, vp, vp, vp,
                                      i32, vp, vp, c_int, vp, vp]),
+        "kda_cfbi_prefill_chunked_workspace_size": (sz, [i64, i32, c_int, c_int, c_int]),
+        "kda_cfbi_prefill_chunked": (c_int, [vp, vp, vp, vp, vp, vp, i32, i64, i32, c_int, c_int, c_int, c_int, vp,
+                                             vp, vp, i32, vp, vp, c_int, vp, sz, vp, vp]),
         "kda_cfbi_decode": (c_int, [vp, vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int, vp, vp, vp, i32, vp, vp,
                                     c_int, vp, vp]),
         "kda_backward_args_bytes": (sz, []),
@@ -354,6 +359,29 @@ def kda_cfbi_prefill(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, cache, coun
                                                     int(max_seqlen), H, dk, dv, _dt(q), _p(pool), _p(cache),
                                                     _p(counts), pool.shape[0], _p(slot_ids), _p(out), _dt(out),
                                                     _p(dev_status), _stream(stream)))
+
+
+def kda_cfbi_prefill_chunked_workspace_size(T: int, N: int, H: int, dk: int = 128, dv: int = 128) -> int:
+    return load().kda_cfbi_prefill_chunked_workspace_size(int(T), int(N), int(H), int(dk), int(dv))
+
+
+def kda_cfbi_prefill_chunked(q, k, v, g, beta, cu_seqlens, max_seqlen, pool, cache, counts, slot_ids, out,
+                             workspace, dev_status=None, stream=None):
+    """kda_cfbi_prefill with the chunks worked on in parallel (same arguments and the same bits); workspace is
+    a uint8 device tensor of at least kda_cfbi_prefill_chunked_workspace_size(T, N, H) bytes."""
+    _need_prefill(q, k, v, g, beta, cu_seqlens, pool, slot_ids, out)
+    _need_cfbi_cache(pool, cache, counts)
+    _need_status(dev_status)
+    _check(q, k, v, g, beta, cu_seqlens, pool, cache, counts, slot_ids, out, dev_status, workspace)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    _ok("kda_cfbi_prefill_chunked",
+        load().kda_cfbi_prefill_chunked(_p(q), _p(k), _p(v), _p(g), _p(beta), _p(cu_seqlens), N, T, int(max_seqlen),
+                                        H, dk, dv, _dt(q), _p(pool), _p(cache), _p(counts), pool.shape[0],
+                                        _p(slot_ids), _p(out), _dt(out), _p(workspace),
+                                        workspace.numel() * workspace.element_size(), _p(dev_status),
+                                        _stream(stream)))
 
 
 def kda_cfbi_decode(q, k, v, g, beta, pool, cache, counts, slot_ids, out, dev_status=None, stream=None):

@@ -381,6 +381,59 @@ kda_status kda_cfbi_prefill(const void* q, const void* k, const void* v, const f
   return from_cuda(kda::launch_cfbi_prefill(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+struct CfbiChunkedLayout {
+  size_t qh, oh, rows, count, total;
+};
+CfbiChunkedLayout cfbi_chunked_layout(int64_t T, int32_t N, int H) {
+  CfbiChunkedLayout L{};
+  L.qh = 0;
+  L.oh = align256((size_t)T * H * kda::cfbi_chunked_qh_row_floats() * 4);
+  L.rows = L.oh + align256((size_t)T * H * 128 * 4);
+  L.count = L.rows + align256(kda::cfbi_chunked_records(T, N) * H * kda::cfbi_chunked_record_bytes());
+  L.total = L.count + align256((size_t)N * H * 4);
+  return L;
+}
+}  // namespace
+
+size_t kda_cfbi_prefill_chunked_workspace_size(int64_t T, int32_t N, int H, int dk, int dv) {
+  if (T < 0 || N < 0 || H <= 0 || dk != 128 || dv != 128) return 0;
+  return cfbi_chunked_layout(T, N, H).total;
+}
+
+kda_status kda_cfbi_prefill_chunked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                    const int32_t* cu_seqlens, int32_t N, int64_t T, int32_t max_seqlen, int H,
+                                    int dk, int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
+                                    int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,
+                                    void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                    kda_stream_t stream) {
+  if (N < 0 || T < 0 || max_seqlen < 0 || H <= 0 || num_slots < 0 || !dtype_ok(in_dtype) || !dtype_ok(out_dtype))
+    return KDA_ERR_INVALID_ARG;
+  if (dk != 128 || dv != 128) return KDA_ERR_UNSUPPORTED;
+  if (N == 0) return KDA_OK;
+  if (N > 65535 || H > 65535 || max_seqlen > 65535 * KDA_CFBI_CHUNK - 2 * KDA_CFBI_CHUNK)
+    return KDA_ERR_INVALID_ARG;
+  const void* ptrs[] = {cu_seqlens, pool, cache, counts, slot_ids, workspace};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  if (T > 0) {
+    const void* tp[] = {q, k, v, g, beta, out};
+    for (const void* p : tp)
+      if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+  }
+  const CfbiChunkedLayout L = cfbi_chunked_layout(T, N, H);
+  if (workspace_bytes < L.total) return KDA_ERR_WORKSPACE;
+  kda_status dbg = kda::debug_check_slots(slot_ids, N, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (dbg != KDA_OK) return dbg;
+  kda::CfbiArgs a{q,   k,    v,     g,     beta,  0,         N,        T,     max_seqlen,
+                  cu_seqlens, H, in_dtype == KDA_DTYPE_BF16, out_dtype == KDA_DTYPE_BF16, pool, cache, counts,
+                  num_slots,   slot_ids,  out,   dev_status};
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  kda::CfbiWorkspace w{reinterpret_cast<float*>(ws + L.qh), reinterpret_cast<float*>(ws + L.oh),
+                       reinterpret_cast<float*>(ws + L.rows), reinterpret_cast<int32_t*>(ws + L.count)};
+  return from_cuda(kda::launch_cfbi_prefill_chunked(a, w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const float* g, const float* beta, int B,
                            int H, int dk, int dv, kda_dtype in_dtype, float* pool, float* cache, int32_t* counts,
                            int32_t num_slots, const int32_t* slot_ids, void* out, kda_dtype out_dtype,

@@ -16,6 +16,7 @@
 // Every operation is an explicit round-to-nearest fp32 intrinsic in a fixed order and the two kernels run
 // the same device functions with the same thread mapping, so a token's output and the state bits are the
 // same whichever path (or batch, or split of a sequence into prefill and decode) computed them.
+#include "cfbi_rows.h"
 #include "common.cuh"
 #include "launch.h"
 #include "tc_ptx.cuh"
@@ -23,17 +24,19 @@
 namespace kda {
 namespace {
 
-constexpr int D = 128;
+using cfbi::CH;
+using cfbi::D;
+using cfbi::R_A;
+using cfbi::R_BETA;
+using cfbi::R_G;
+using cfbi::R_K;
+using cfbi::R_T;
+using cfbi::R_V;
+using cfbi::RF;
 constexpr int NT = 256;
-constexpr int CH = KDA_CFBI_CHUNK;       // rows per chunk
-constexpr int RF = KDA_CFBI_ROW_FLOATS;  // floats per cached row
 #ifndef CFBI_DECODE_CTAS
 #define CFBI_DECODE_CTAS 3  // decode CTAs resident per SM
 #endif
-// cached row layout: k | v | G (in-chunk cumulative log-decay) | A_t[u] (beta folded in, u < t) | beta |
-// T_t[v] = row t of (I + A)^-1 (v <= t)
-constexpr int R_K = 0, R_V = 128, R_G = 256, R_A = 384, R_BETA = 400, R_T = 401;
-static_assert(R_T + CH <= RF && RF % 4 == 0, "row layout");
 
 struct RowScratch {
   alignas(16) float q[D];  // q_t (fp32)

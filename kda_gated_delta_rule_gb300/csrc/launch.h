@@ -120,6 +120,18 @@ struct CfbiArgs {
   int32_t* status;
 };
 
+// Workspace of the chunk-parallel CF-BI prefill (layout in cfbi_chunked.cu).
+struct CfbiWorkspace {
+  float* qh;       // [H][T][cfbi_chunked_qh_row_floats()]
+  float* oh;       // [H][T][128] (by 8-column group)
+  float* rows;     // [cfbi_chunked_records(T, N)][H] records of cfbi_chunked_record_bytes()
+  int32_t* count;  // [N][H]
+};
+size_t cfbi_chunked_records(int64_t T, int N);
+size_t cfbi_chunked_record_bytes();
+size_t cfbi_chunked_qh_row_floats();
+cudaError_t launch_cfbi_prefill_chunked(const CfbiArgs& a, const CfbiWorkspace& w, cudaStream_t s);
+
 // Chunked backward (d = 128): gradients of sum <d_out, o> + <d_final, S_T> through a packed prefill.
 struct BackwardArgs {
   const void *q, *k, *v;

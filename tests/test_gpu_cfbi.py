@@ -162,3 +162,135 @@ def test_bad_count_is_flagged(cuda):
     flags, work = status(st)
     assert flags == kda.KDA_DEV_SLOT_OOB and work == 1
     assert not out[1].any()
+
+
+def _chunked(kda, p, lo, hi, cu, max_len, pool, cache, counts, slots, out, st=None):
+    """kda_cfbi_prefill_chunked over tokens [lo, hi) of p with its own workspace."""
+    N = cu.numel() - 1
+    ws = torch.empty(kda.kda_cfbi_prefill_chunked_workspace_size(hi - lo, N, p.H), dtype=torch.uint8, device="cuda")
+    kda.kda_cfbi_prefill_chunked(*_tok(p, lo, hi), cu, max_len, pool, cache, counts, slots, out, ws, dev_status=st)
+
+
+@pytest.mark.parametrize("dtype,out_dtype", [(synth.BF16, torch.bfloat16), (synth.F32, torch.float32),
+                                             (synth.BF16, torch.float32)], ids=["bf16", "f32", "bf16_in_f32_out"])
+def test_chunked_prefill_is_bit_identical_to_sequential(cuda, dtype, out_dtype):
+    """Ragged sequences (1 to 200 tokens, one empty) continuing from open chunks of every length: outputs,
+    states, counts and open-chunk rows of the chunk-parallel prefill equal the token-sequential prefill's."""
+    kda = cuda
+    lengths = [37, 1, 200, 16, 0, 15, 64, 129, 33, 48]
+    p = _problem(lengths, H=3, dtype=dtype, seed=86)
+    N, T = len(lengths), p.T
+    slots = dev(p.slot_ids)
+    # open chunks of different lengths: a first token-sequential prefill of a few tokens per sequence
+    pre = [3, 0, 15, 7, 1, 14, 0, 9, 12, 5]
+    pool0, cache0, counts0 = _state(p)
+    pre_tok = np.concatenate([np.arange(p.cu_seqlens[i], p.cu_seqlens[i] + min(pre[i], lengths[i])) for i in range(N)])
+    cu_pre = np.concatenate([[0], np.cumsum([min(pre[i], lengths[i]) for i in range(N)])]).astype(np.int32)
+    xs = [dev(np.ascontiguousarray(x[pre_tok])) for x in (p.q, p.k, p.v, p.g, p.beta)]
+    kda.kda_cfbi_prefill(*xs, dev(cu_pre), 16, pool0, cache0, counts0, slots,
+                         torch.empty(len(pre_tok), p.H, 128, dtype=out_dtype, device="cuda"))
+    rest = np.concatenate([np.arange(p.cu_seqlens[i] + min(pre[i], lengths[i]), p.cu_seqlens[i + 1]) for i in range(N)])
+    cu_rest = np.concatenate([[0], np.cumsum([lengths[i] - min(pre[i], lengths[i]) for i in range(N)])]).astype(np.int32)
+    ys = [dev(np.ascontiguousarray(x[rest])) for x in (p.q, p.k, p.v, p.g, p.beta)]
+    TR = len(rest)
+    st_a = torch.zeros(2, dtype=torch.int32, device="cuda")
+    st_b = torch.zeros(2, dtype=torch.int32, device="cuda")
+    pool_a, cache_a, counts_a = pool0.clone(), cache0.clone(), counts0.clone()
+    out_a = torch.empty(TR, p.H, 128, dtype=out_dtype, device="cuda")
+    kda.kda_cfbi_prefill(*ys, dev(cu_rest), 200, pool_a, cache_a, counts_a, slots, out_a, dev_status=st_a)
+    pool_b, cache_b, counts_b = pool0.clone(), cache0.clone(), counts0.clone()
+    out_b = torch.empty(TR, p.H, 128, dtype=out_dtype, device="cuda")
+    ws = torch.empty(kda.kda_cfbi_prefill_chunked_workspace_size(TR, N, p.H), dtype=torch.uint8, device="cuda")
+    kda.kda_cfbi_prefill_chunked(*ys, dev(cu_rest), 200, pool_b, cache_b, counts_b, slots, out_b, ws, dev_status=st_b)
+    torch.cuda.synchronize()
+    assert status(st_b) == status(st_a) == (0, TR * p.H)
+    assert torch.equal(out_a, out_b)
+    assert torch.equal(pool_a, pool_b)
+    assert torch.equal(counts_a, counts_b)
+    for i in range(N):
+        sl = int(p.slot_ids[i])
+        for h in range(p.H):
+            n = int(counts_a[sl, h])
+            assert torch.equal(cache_a[sl, h, :n], cache_b[sl, h, :n])
+    # and against the fp64 recurrence at the chunk-boundary states (values, not bits)
+    tol = 2e-3 if dtype == synth.BF16 else 1e-5
+    s0 = p.pool[p.slot_ids].astype(np.float64)
+    for i in (2, 7):
+        full = (lengths[i] // CH) * CH
+        r = oracle.recurrence(*(x[p.cu_seqlens[i]:p.cu_seqlens[i] + full] for x in (p.q, p.k, p.v, p.g, p.beta)),
+                              [0, full], s0=s0[i:i + 1])
+        assert rel_err(host(pool_b[int(p.slot_ids[i])]), r["s_final"][0]) <= tol
+
+
+@pytest.mark.parametrize("split", [0, 5, 16, 41])
+def test_chunked_prefill_then_decode_is_bit_identical(cuda, split):
+    """A sequence prefilled by the chunk-parallel kernels up to `split` and decoded after it gives the bits of
+    one token-sequential prefill over the whole sequence."""
+    kda = cuda
+    T = 60
+    p = _problem([T], H=2, dtype=synth.BF16, seed=87)
+    slots = dev(p.slot_ids)
+    pool_a, cache_a, counts_a = _state(p)
+    out_a = torch.empty(T, p.H, 128, dtype=torch.bfloat16, device="cuda")
+    kda.kda_cfbi_prefill(*_tok(p, 0, T), dev(np.array([0, T], np.int32)), T, pool_a, cache_a, counts_a, slots, out_a)
+    pool_b, cache_b, counts_b = _state(p)
+    out_b = torch.empty(T, p.H, 128, dtype=torch.bfloat16, device="cuda")
+    if split:
+        _chunked(kda, p, 0, split, dev(np.array([0, split], np.int32)), split, pool_b, cache_b, counts_b, slots,
+                 out_b[:split])
+    for t in range(split, T):
+        o = torch.empty(1, p.H, 128, dtype=torch.bfloat16, device="cuda")
+        kda.kda_cfbi_decode(*_tok(p, t, t + 1), pool_b, cache_b, counts_b, slots, o)
+        out_b[t] = o[0]
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b) and torch.equal(pool_a, pool_b) and torch.equal(counts_a, counts_b)
+    sl = int(p.slot_ids[0])
+    n = int(counts_a[sl, 0])
+    assert torch.equal(cache_a[sl, :, :n], cache_b[sl, :, :n])
+
+
+def test_chunked_prefill_long_sequence(cuda):
+    """3000 tokens in one sequence (188 chunks) and a short one: bits equal to the token-sequential prefill."""
+    kda = cuda
+    p = _problem([3000, 21], H=2, dtype=synth.BF16, seed=88)
+    slots = dev(p.slot_ids)
+    cu = dev(p.cu_seqlens.astype(np.int32))
+    pool_a, cache_a, counts_a = _state(p)
+    out_a = torch.empty(p.T, p.H, 128, dtype=torch.bfloat16, device="cuda")
+    kda.kda_cfbi_prefill(*_tok(p, 0, p.T), cu, 3000, pool_a, cache_a, counts_a, slots, out_a)
+    pool_b, cache_b, counts_b = _state(p)
+    out_b = torch.empty(p.T, p.H, 128, dtype=torch.bfloat16, device="cuda")
+    _chunked(kda, p, 0, p.T, cu, 3000, pool_b, cache_b, counts_b, slots, out_b)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b) and torch.equal(pool_a, pool_b) and torch.equal(counts_a, counts_b)
+
+
+def test_chunked_prefill_errors(cuda):
+    """A short workspace is refused before any launch; a bad slot or row count is flagged and that sequence
+    left untouched; a sequence longer than max_seqlen is flagged."""
+    kda = cuda
+    p = _problem([20, 30], H=1, dtype=synth.F32, seed=89)
+    slots = dev(p.slot_ids)
+    cu = dev(p.cu_seqlens.astype(np.int32))
+    pool, cache, counts = _state(p)
+    out = torch.zeros(p.T, 1, 128, device="cuda")
+    need = kda.kda_cfbi_prefill_chunked_workspace_size(p.T, 2, 1)
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kda.KdaError):
+        kda.kda_cfbi_prefill_chunked(*_tok(p, 0, p.T), cu, 30, pool, cache, counts, slots, out, small)
+    # sequence 1's row count out of range
+    counts[int(p.slot_ids[1]), 0] = CH
+    pool0 = pool.clone()
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    _chunked(kda, p, 0, p.T, cu, 30, pool, cache, counts, slots, out, st)
+    torch.cuda.synchronize()
+    flags, work = status(st)
+    assert flags == kda.KDA_DEV_SLOT_OOB and work == 20
+    assert torch.equal(pool[int(p.slot_ids[1])], pool0[int(p.slot_ids[1])])
+    assert not out[20:].any()
+    # max_seqlen below the longest sequence
+    counts[int(p.slot_ids[1]), 0] = 0
+    st.zero_()
+    _chunked(kda, p, 0, p.T, cu, 25, pool, cache, counts, slots, out, st)
+    torch.cuda.synchronize()
+    assert status(st)[0] == kda.KDA_DEV_SEQ_OOB
