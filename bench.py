@@ -102,6 +102,7 @@ def parse():
                          "output phase (one CTA per head and segment) fits one wave on this GPU")
     ap.add_argument("--no-decode", action="store_true", help="skip the decode/verify/fold measurements")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--no-cfbi", action="store_true", help="skip the batch-invariant prefill measurement")
     ap.add_argument("--no-varlen", action="store_true", help="skip the varlen packed-prefill workload")
     ap.add_argument("--no-long", action="store_true", help="skip the 1M-token segmented prefill workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -436,6 +437,10 @@ def run_ours(args):
     if not args.no_backward:
         bw_report = backward_report(kda, torch, dev, to_dev, time_calls, pk, prob)
 
+    cf_report = None
+    if not args.no_cfbi:
+        cf_report = cfbi_prefill_report(kda, torch, dev, to_dev, time_calls, pk, prob)
+
     # ---- the varlen packed prefill and the 1M-token segmented prefill (tokens/s, fraction of HBM)
     del ws, ws_var, sets
     torch.cuda.empty_cache()
@@ -494,6 +499,8 @@ def run_ours(args):
         line["decode_verify"] = dv_report
     if bw_report:
         line["backward"] = bw_report
+    if cf_report:
+        line["cfbi_prefill"] = cf_report
     if varlen_report:
         line["varlen_prefill"] = varlen_report
     if long_report:
@@ -714,6 +721,51 @@ def backward_report(kda, torch, dev, to_dev, time_calls, pk, prob):
             "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "algorithmic_bytes": alg,
             "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "kernels_per_call": 6,
             "workspace_bytes": ws.numel()}
+
+
+def cfbi_prefill_report(kda, torch, dev, to_dev, time_calls, pk, prob):
+    """The batch-invariant (CF-BI) prefill on the single-request workload: the chunk-parallel call (rows, then
+    the state walk; one call = two kernels) and, for reference, the token-sequential call, which must give
+    the same bits.  Each call first restores the pool and zeroes the row counts (a 6 MB copy and a memset,
+    timed with the call)."""
+    T, H, N = prob.T, prob.H, prob.N
+    q, k, v, g, beta = (to_dev(x) for x in (prob.q, prob.k, prob.v, prob.g, prob.beta))
+    cu = to_dev(prob.cu_seqlens.astype(np.int32))
+    pool0, slots = to_dev(prob.pool), to_dev(prob.slot_ids)
+    pool = pool0.clone()
+    cache = torch.zeros(prob.pool.shape[0], H, kda.CFBI_CHUNK, kda.CFBI_ROW_FLOATS, device=dev)
+    counts = torch.zeros(prob.pool.shape[0], H, dtype=torch.int32, device=dev)
+    out = torch.empty(T, H, 128, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(kda.kda_cfbi_prefill_chunked_workspace_size(T, N, H), dtype=torch.uint8, device=dev)
+    max_len = int(prob.lengths.max())
+
+    def chunked():
+        pool.copy_(pool0)
+        counts.zero_()
+        kda.kda_cfbi_prefill_chunked(q, k, v, g, beta, cu, max_len, pool, cache, counts, slots, out, ws)
+
+    def sequential():
+        pool.copy_(pool0)
+        counts.zero_()
+        kda.kda_cfbi_prefill(q, k, v, g, beta, cu, max_len, pool, cache, counts, slots, out)
+
+    for _ in range(3):
+        chunked()
+    torch.cuda.synchronize()
+    ms = statistics.mean(time_calls(chunked, 10))
+    o_chunked, p_chunked = out.clone(), pool.clone()
+    ms_seq = statistics.mean(time_calls(sequential, 2))
+    same = bool(torch.equal(o_chunked, out) and torch.equal(p_chunked, pool))
+    if not same:
+        raise RuntimeError("the chunk-parallel CF-BI prefill differs from the token-sequential one")
+    alg = T * H * BYTES_PER_TOKEN_HEAD + 2 * N * H * STATE_BYTES
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"workload": "batch-invariant (CF-BI, 16-token chunks) prefill: B=1, T=8192, H=12, d=128, bf16 q/k/v, "
+                        "fp32 gates and state, bf16 o; fresh open chunk; L2 flushed between calls",
+            "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "algorithmic_bytes": alg,
+            "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "kernels_per_call": 2,
+            "workspace_bytes": ws.numel(), "token_sequential_ms": round(ms_seq, 3),
+            "bit_identical_to_token_sequential": same}
 
 
 # ---------------------------------------------------------------- CPU baseline (the oracle)
