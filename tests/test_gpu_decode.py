@@ -239,6 +239,55 @@ def test_verify_out_of_range_slot_is_flagged_and_skipped(cuda):
     assert np.array_equal(kbytes[good], p.wk[good])
 
 
+def test_streams_skip_bad_units_mid_stream(cuda):
+    """Decode and fold at full width (256 requests x 12 heads: several units per persistent CTA) with bad
+    slot ids and bad accepted lengths scattered through the batch: the bad units are flagged and left alone,
+    every other unit gets the bits of a call without them (the same kernels on the good requests only)."""
+    kda = cuda
+    p = synth.decode_verify(seed=62, B=256, W=8, H=12, d=128, num_slots=1024, dtype=synth.BF16)
+    B, W, H, d = p.B, p.W, p.H, p.dk
+    bad_rows = np.array([0, 5, 77, 130, 255])
+    good = np.setdiff1d(np.arange(B), bad_rows)
+    bad = p.slot_ids.copy()
+    bad[bad_rows] = [1024, -1, 5000, -7, 1024]
+    x = [dev(a) for a in (p.q, p.k, p.v, p.g, p.beta)]
+    pool0 = dev(p.pool)
+    # decode: all requests with the bad slots, against the good requests alone
+    pool, st = pool0.clone(), torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = torch.zeros(B, H, d, dtype=torch.bfloat16, device="cuda")
+    kda.kda_decode_step(*x, pool, dev(bad), out, dev_status=st)
+    pool_g = pool0.clone()
+    out_g = torch.zeros(len(good), H, d, dtype=torch.bfloat16, device="cuda")
+    gi = torch.from_numpy(good).cuda()
+    kda.kda_decode_step(*(t[gi].contiguous() for t in x), pool_g, dev(p.slot_ids[good]), out_g)
+    torch.cuda.synchronize()
+    assert status(st) == (kda.KDA_DEV_SLOT_OOB, len(good) * H)
+    assert torch.equal(out[gi], out_g) and not out[torch.from_numpy(bad_rows).cuda()].any()
+    assert torch.equal(pool, pool_g)  # bad slots touched nothing; good ones got the same bits
+    # fold: bad accepted lengths (and the bad slots) scattered through the batch
+    rec = torch.zeros(kda.kda_replay_bytes(B, W, H, d, d, p.in_dtype), dtype=torch.uint8, device="cuda")
+    wout = torch.zeros(B, W, H, d, dtype=torch.bfloat16, device="cuda")
+    kda.kda_verify(*(dev(a) for a in (p.wq, p.wk, p.wv, p.wg, p.wbeta)), pool0, dev(p.slot_ids), wout, rec)
+    acc = p.accepted.copy()
+    acc[[10, 200]] = [W + 1, -2]
+    skip = np.zeros(B, bool)
+    skip[[10, 200]] = True
+    skip[bad_rows] = True
+    pool, st = pool0.clone(), torch.zeros(2, dtype=torch.int32, device="cuda")
+    kda.kda_verify_replay(pool, dev(bad), rec, dev(acc), W, H, d, d, p.in_dtype, dev_status=st)
+    acc_g = acc.copy()
+    acc_g[skip] = 0  # nothing accepted: the same units left alone
+    pool_g = pool0.clone()
+    kda.kda_verify_replay(pool_g, dev(p.slot_ids), rec, dev(acc_g), W, H, d, d, p.in_dtype)
+    torch.cuda.synchronize()
+    flags, work = status(st)
+    # a unit with nothing accepted is skipped before its slot is looked at
+    expect = kda.KDA_DEV_ACCEPT_OOB | (kda.KDA_DEV_SLOT_OOB if (acc[bad_rows] > 0).any() else 0)
+    assert flags == expect
+    assert work == int(acc_g.sum()) * H
+    assert torch.equal(pool, pool_g)
+
+
 def test_state_copy(cuda):
     kda = cuda
     H, d = 12, 128

@@ -62,3 +62,28 @@ def test_fused_decode_bad_slot_is_flagged_and_skipped(cuda):
     untouched = [s for s in range(S) if s != slots[0]]
     np.testing.assert_array_equal(host(pool)[untouched], p["pool"][untouched])
     np.testing.assert_array_equal(host(cstate)[untouched], p["conv_state"][untouched])
+
+
+def test_fused_decode_skips_bad_units_mid_stream(cuda):
+    """512 (request, head) units, several per persistent CTA, with bad slot ids scattered through the batch:
+    flagged and left alone; every other unit gets the bits of a call on the good requests only."""
+    B, H, d, S = 64, 8, 128, 80
+    p = synth.fused_decode_inputs(73, B, H, d, S)
+    bad_rows = np.array([0, 31, 63])
+    good = np.setdiff1d(np.arange(B), bad_rows)
+    slots = p["slot_ids"].copy()
+    slots[bad_rows] = [S, -1, S + 100]
+    xs = [dev(p[n][0]) for n in ("xq", "xk", "xv", "a", "b", "z")]
+    cw, nw = dev(p["conv_w"]), dev(p["norm_w"])
+    pool, cstate = dev(p["pool"]), dev(p["conv_state"])
+    out = torch.zeros(B, H, d, device="cuda")
+    st = torch.zeros(2, dtype=torch.int32, device="cuda")
+    cuda.kda_fused_decode(*xs, pool, dev(slots), cstate, cw, nw, out, dev_status=st)
+    gi = torch.from_numpy(good).cuda()
+    pool_g, cstate_g = dev(p["pool"]), dev(p["conv_state"])
+    out_g = torch.zeros(len(good), H, d, device="cuda")
+    cuda.kda_fused_decode(*(x[gi].contiguous() for x in xs), pool_g, dev(p["slot_ids"][good]), cstate_g, cw, nw, out_g)
+    torch.cuda.synchronize()
+    assert status(st) == (cuda.KDA_DEV_SLOT_OOB, len(good) * H)
+    assert torch.equal(out[gi], out_g) and not out[torch.from_numpy(bad_rows).cuda()].any()
+    assert torch.equal(pool, pool_g) and torch.equal(cstate, cstate_g)
