@@ -19,13 +19,20 @@
 // e^(G_t - G_s) = e^(G_t - G_r) e^(G_r - G_s), while every factor stays below e^80 (always when g >= -5, the
 // pages' floor); a block that would exceed it takes the pair decays one by one.
 //
-// Six kernels handing over through a per-(chunk, head) fp32 workspace (tiles move into shared memory by
+// Kernels handing over through a per-(chunk, head) fp32 workspace (tiles move into shared memory by
 // asynchronous 16-byte copies):
-//   prep (chunk-parallel) -> forward chain (entry states, U) -> reverse chain (dS', dU)
+//   prep (chunk-parallel) -> forward pass (entry states, U) -> reverse chain (dS', dU)
 //   -> state products -> WY backward -> per-channel assembly (chunk-parallel).
-// The state products run on the tensor cores (split-bf16 tcgen05 MMAs, fp32 accumulation); the others
-// are fp32 on the CUDA cores.
+// With bf16 inputs the forward pass is the tensor-core segmented prefill (operand records, segment
+// fragments, the fragment scan, then every segment from its exact entry state, writing each chunk's entry
+// state and U into this workspace); otherwise it is the CUDA-core chain below.  With bf16 inputs the prep
+// also flags each (sequence, head) holding a 16-token block whose decay span passes e^80 (g below the
+// floor), where the tensor-core pass's block references overflow; the CUDA-core chain then runs for the
+// flagged (sequence, head)s only and overwrites their entry states and U.  The state products run on
+// the tensor cores (split-bf16 tcgen05 MMAs, fp32 accumulation); the remaining kernels are fp32 on the
+// CUDA cores.
 #include "common.cuh"
+#include "device.h"
 #include "launch.h"
 #include "tc_ptx.cuh"
 
@@ -219,6 +226,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
       for (int s = b0; s <= r; ++s) wide |= gr - sG[s * LD + tid] > SPAN_MAX;
     }
     wide = __syncthreads_or(wide);
+    if (wide && tid == 0 && a.steep) atomicOr(a.steep + (size_t)i * a.H + h, 1);
     // thread -> row t = b0 + tid / 4, columns s = b0 + tid % 4 + 4m
     const int t = b0 + (tid >> 2), sl = tid & 3;
     if (!wide) {
@@ -364,6 +372,7 @@ constexpr size_t FWD_SMEM = (2 * FS_STAGE + D * CB + C * CB + 4 * D * FS_PART) *
 
 __global__ void __launch_bounds__(NTC, 1) bwd_fwd_chain_kernel(BackwardArgs a) {
   const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
+  if (a.steep && !a.steep[(size_t)i * a.H + h]) return;  // the tensor-core forward pass covered it
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
   extern __shared__ float sm[];
@@ -1125,9 +1134,69 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// The tensor-core forward pass's layout after the per-chunk records: operand records, fragments, entry
+// states.  Segments: about one output-chain CTA per SM pair and head (P_target = SMs / (2 H)), so the
+// fragment pass (two CTAs per segment and head) fills the GPU once.
+struct FwdLayout {
+  int P;
+  size_t rec_off, frag_off, entry_off, steep_off, total;
+};
+int fwd_segments_target(int H) {
+  const int sms = sm_count();
+  const int p = sms > 0 ? sms / (2 * H) : 1;
+  return p < 1 ? 1 : p;
+}
+FwdLayout fwd_layout(int64_t T, int N, int H) {
+  FwdLayout L{};
+  L.P = fwd_segments_target(H);
+  const size_t heads = (size_t)N * L.P * H;
+  L.rec_off = ((size_t)((T + C - 1) / C + N) * H * BW_FLOATS * sizeof(float) + 1023) & ~(size_t)1023;
+  L.frag_off = L.rec_off + ((tc_record_bytes(T, N, H) + 1023) & ~(size_t)1023);
+  L.entry_off = L.frag_off + heads * D * 2 * D * sizeof(float);
+  L.steep_off = L.entry_off + heads * D * D * sizeof(float);
+  L.total = L.steep_off + (((size_t)N * H * sizeof(int32_t) + 255) & ~(size_t)255);
+  return L;
+}
+
+// The forward pass on the tensor cores (bf16 inputs): records -> fragments -> scan -> per-chunk states.
+cudaError_t forward_pass_tc(const BackwardArgs& a, cudaStream_t s) {
+  const FwdLayout L = fwd_layout(a.T, a.N, a.H);
+  const int pt = L.P;
+  int seg = (int)((((int64_t)a.max_seqlen + pt - 1) / pt + C - 1) / C * C);
+  if (seg < C) seg = C;
+  PrefillArgs p{};
+  p.q = a.q, p.k = a.k, p.v = a.v, p.g = a.g, p.beta = a.beta;
+  p.in_bf16 = true, p.out_bf16 = false;
+  p.T = a.T, p.H = a.H, p.d = D, p.N = a.N, p.cu = a.cu, p.max_seqlen = a.max_seqlen;
+  p.pool = const_cast<float*>(a.pool), p.num_slots = a.num_slots, p.slot_ids = a.slot_ids;
+  p.init_zero = a.init_zero;
+  p.status = a.status;
+  p.seg_len = seg;
+  p.P = (int)(((int64_t)a.max_seqlen + seg - 1) / seg);
+  if (p.P < 1) p.P = 1;
+  uint8_t* base = reinterpret_cast<uint8_t*>(a.ws);
+  p.records = base + L.rec_off;
+  p.frag = reinterpret_cast<float*>(base + L.frag_off);
+  p.entry = reinterpret_cast<float*>(base + L.entry_off);
+  p.bw_ws = a.ws, p.bw_rec_floats = (int)BW_FLOATS, p.bw_off_h = (int)BW_H, p.bw_off_u = (int)BW_U;
+  p.no_work_count = true;
+  p.zero_bad_slot = true;  // this call's contract: a bad slot is flagged and differentiated from zero
+  cudaError_t e = launch_tc_prep(p, p.records, s);
+  if (e == cudaSuccess) e = launch_tc_chain_frag(p, p.records, s);
+  if (e == cudaSuccess) e = launch_seg_scan(p, s);
+  if (e == cudaSuccess) e = launch_tc_chain_states(p, p.records, s);
+  return e;
+}
+
 template <typename Tin>
-cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
+cudaError_t launch_backward_t(const BackwardArgs& a_in, cudaStream_t s) {
   cudaError_t e;
+  BackwardArgs a = a_in;
+  a.steep = nullptr;
+  if (a.in_bf16) {  // the tensor-core forward pass, with the CUDA-core chain for steep (sequence, head)s
+    a.steep = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(a.ws) + fwd_layout(a.T, a.N, a.H).steep_off);
+    if ((e = cudaMemsetAsync(a.steep, 0, (size_t)a.N * a.H * sizeof(int32_t), s)) != cudaSuccess) return e;
+  }
   if ((e = set_smem(bwd_prep_kernel<Tin>, PREP_SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(bwd_fwd_chain_kernel, FWD_SMEM)) != cudaSuccess) return e;
   if ((e = set_smem(bwd_rev_chain_kernel<Tin>, REV_SMEM)) != cudaSuccess) return e;
@@ -1138,7 +1207,11 @@ cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
   const dim3 chunks(nch, a.H, a.N), halves(nch, 2 * a.H, a.N), chains(D / CB, a.H, a.N);
   if (nch > 0) {
     bwd_prep_kernel<Tin><<<chunks, NT, PREP_SMEM, s>>>(a);
-    bwd_fwd_chain_kernel<<<chains, NTC, FWD_SMEM, s>>>(a);
+    if (a.in_bf16) {
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = forward_pass_tc(a, s)) != cudaSuccess) return e;
+    }
+    bwd_fwd_chain_kernel<<<chains, NTC, FWD_SMEM, s>>>(a);  // (bf16: only the steep (sequence, head)s)
   }
   bwd_rev_chain_kernel<Tin><<<chains, NTC, REV_SMEM, s>>>(a);
   if (nch > 0) {
@@ -1152,7 +1225,9 @@ cudaError_t launch_backward_t(const BackwardArgs& a, cudaStream_t s) {
 }  // namespace
 
 size_t backward_ws_bytes(int64_t T, int N, int H) {
-  return (size_t)((T + C - 1) / C + N) * H * BW_FLOATS * sizeof(float);
+  // the per-chunk records, then (the bf16 inputs' tensor-core forward pass) operand records, fragments and
+  // entry states
+  return fwd_layout(T, N, H).total;
 }
 
 cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t s) {

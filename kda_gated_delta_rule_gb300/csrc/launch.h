@@ -98,6 +98,13 @@ struct PrefillArgs {
   // test hook (kda_set_test_fault): the prep kernel issues no input copies and waits for them with a short
   // poll limit, so its first wait gives up and the kernel reports KDA_DEV_TIMEOUT; 0 in normal calls
   int test_stall_inputs;
+  // the backward's forward pass (launch_tc_chain_states): every chunk's entry state and U into the
+  // backward's per-(chunk, head) records (bw_rec_floats floats each, indexed like the backward's: chunk
+  // starting at token t0 of sequence i -> (t0 / 64 + i) * H + h), at float offsets bw_off_h / bw_off_u
+  float* bw_ws;
+  int bw_rec_floats, bw_off_h, bw_off_u;
+  bool no_work_count;  // the chain adds nothing to the work counter (a pass inside another call)
+  bool zero_bad_slot;  // the scan starts a sequence whose slot id is out of range from zero (flagged)
 };
 
 // Batch-invariant (CF-BI) prefill and decode (d = 128).
@@ -151,6 +158,10 @@ struct BackwardArgs {
   float* d_init;         // [N][H][128][128] or null
   float* ws;             // backward_ws_bytes(T, N, H)
   int32_t* status;
+  // set by the launcher on the tensor-core forward pass: per (sequence, head), nonzero when a 16-token block
+  // of some chunk spans more decay than the block references allow (g below the pages' floor); the
+  // CUDA-core chain then recomputes that (sequence, head)'s entry states and U
+  int32_t* steep;
 };
 
 size_t backward_ws_bytes(int64_t T, int N, int H);
@@ -202,6 +213,9 @@ size_t tc_record_bytes(int64_t T, int N, int H);
 cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t s);
 cudaError_t launch_tc_chain_plain(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 cudaError_t launch_tc_chain_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
+// the backward's forward pass: like the segment outputs, but every chunk's entry state and U go to the
+// backward's records (a.bw_*) instead of outputs, and the pool is not written
+cudaError_t launch_tc_chain_states(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 
 // Launches `kernel` so that it may be scheduled while the previous kernel in the stream finishes

@@ -749,7 +749,10 @@ constexpr int CHAIN_NT = CHAIN_MATH + 96;
 constexpr int BAR_MATH = 1;                       // named barrier of the math warps
 static_assert(CS_BYTES <= 232448, "chain shared memory");
 
-enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2 };
+// MODE_STATES: the backward's forward pass -- segments from their exact entry states like MODE_SEGOUT,
+// no outputs (the fragment mode's product schedule), every chunk's entry state and U written to the
+// backward's per-chunk records, the pool not written.
+enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2, MODE_STATES = 3 };
 
 // Two math warpgroups: thread (value channel c = TMEM lane, warpgroup wg) handles half of every TMEM row it
 // touches.  Per chunk: split the state (E1) -> [W; Q o gamma] S -> U = U~ - W S (E2) -> state update
@@ -764,7 +767,7 @@ enum { MODE_PLAIN = 0, MODE_FRAG = 1, MODE_SEGOUT = 2 };
 // and C into three accumulators, which E2 adds.
 template <typename Tout, int MODE>
 __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs a, const uint8_t* __restrict__ ws) {
-  constexpr bool WANT_O = MODE != MODE_FRAG;
+  constexpr bool WANT_O = MODE != MODE_FRAG && MODE != MODE_STATES;
   constexpr int WS_PARTS = WANT_O ? 1 : 3;  // issuers (and accumulators) of (W S)^T
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -901,7 +904,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     {
       const float* src = nullptr;
       if (MODE == MODE_PLAIN && !a.init_zero) src = a.pool + ((size_t)slot * a.H + h) * head_elems;
-      if (MODE == MODE_SEGOUT) src = a.entry + (((size_t)i * a.P + p) * a.H + h) * head_elems;
+      if (MODE == MODE_SEGOUT || MODE == MODE_STATES) src = a.entry + (((size_t)i * a.P + p) * a.H + h) * head_elems;
 #pragma unroll 1
       for (int jb = 0; jb < 2; ++jb) {
         const int j0 = 64 * wg + 32 * jb;
@@ -941,6 +944,12 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         const int j0 = 64 * wg;
         float s[64];
         tc::tmem_ld64(trow + COL_S + j0, s);
+        if (MODE == MODE_STATES) {  // the chunk's entry state, rows j0 .. j0 + 63 of column c
+          float* dst = a.bw_ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * a.bw_rec_floats + a.bw_off_h +
+                       (size_t)j0 * D + c;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) dst[(size_t)e * D] = s[e];
+        }
 #pragma unroll
         for (int jb = 0; jb < 2; ++jb) {
           uint32_t hi[16], lo[16];
@@ -981,6 +990,12 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         for (int e = 0; e < 16; ++e) tc::split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
         tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
         tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
+        if (MODE == MODE_STATES) {  // U = U~ - W S of this thread's 32 tokens, column c
+          float* du = a.bw_ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * a.bw_rec_floats + a.bw_off_u +
+                      (size_t)(32 * wg) * D + c;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) du[(size_t)e * D] = ut[e] - w[e];
+        }
       }
       tc::tmem_wait_st();
       hand_over(rdy_e2);
@@ -1001,7 +1016,7 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         store_state(a.frag + (((size_t)i * a.P + p) * a.H + h) * head_elems * 2 + (size_t)tile * D + c, 2 * D);
       else if (writes_pool)
         store_state(a.pool + ((size_t)slot * a.H + h) * head_elems + c, D);
-      if (tid == 0 && tile == 0) add_work(a.status, (int32_t)(t1 - t0));
+      if (tid == 0 && tile == 0 && !a.no_work_count) add_work(a.status, (int32_t)(t1 - t0));
     } else if (tid == 0) {
       flag_status(a.status, KDA_DEV_TIMEOUT);
     }
@@ -1176,6 +1191,9 @@ cudaError_t launch_tc_chain_plain(const PrefillArgs& a, const uint8_t* records, 
 }
 cudaError_t launch_tc_chain_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
   return launch_chain<MODE_FRAG>(a, records, s);
+}
+cudaError_t launch_tc_chain_states(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
+  return launch_chain<MODE_STATES>(a, records, s);
 }
 cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
   return launch_chain<MODE_SEGOUT>(a, records, s);

@@ -88,9 +88,10 @@ __global__ void __launch_bounds__(SCAN_NT, 1) seg_scan_tc_kernel(const PrefillAr
       const int slot = a.slot_ids[i];
       if (slot < 0 || slot >= a.num_slots) {
         if (tid == 0) flag_status(a.status, KDA_DEV_SLOT_OOB);
-        return;
+        if (!a.zero_bad_slot) return;
+      } else {
+        init = a.pool + ((size_t)slot * a.H + h) * head_elems;
       }
-      init = a.pool + ((size_t)slot * a.H + h) * head_elems;
     }
   }
   const int c0 = ct * SCT;

@@ -105,6 +105,19 @@ def test_backward_steep_gates_take_pairwise_decays(cuda):
     check(got, oracle_grads(prob, d_out, d_final), tol_dg=5e-4)
 
 
+def test_backward_steep_block_in_one_head_only(cuda):
+    """Steep gates in one block of one (sequence, head) among ordinary ones: with bf16 inputs the forward
+    pass runs on the tensor cores for every (sequence, head), and the flagged one alone is recomputed by the
+    CUDA-core chain; every gradient of every sequence and head still matches."""
+    prob = synth.varlen(seed=66, lengths=[150, 200, 90], H=3, num_slots=8, num_extra=8)
+    assert prob.in_dtype == synth.BF16
+    t0 = 150 + 100  # sequence 1, tokens 100..129, head 2
+    prob.g[t0:t0 + 30, 2, :] = (-7.0 + 0.5 * np.cos(np.arange(30 * prob.g.shape[2]))).reshape(30, -1)
+    d_out, d_final = synth.output_grads(prob, 66)
+    got = BackwardRun(cuda, prob, d_out, d_final).run(cuda)
+    check(got, oracle_grads(prob, d_out, d_final), tol_dg=5e-4)
+
+
 def test_backward_bad_slot_is_flagged(cuda):
     prob = synth.varlen(seed=65, lengths=[10, 10], H=1, num_slots=4, num_extra=4)
     prob.slot_ids = np.array([1, 99], np.int32)
