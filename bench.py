@@ -723,7 +723,7 @@ def backward_report(kda, torch, dev, to_dev, time_calls, pk, prob):
     return {"workload": "prefill backward: B=1, T=8192, H=12, d=128, bf16 q/k/v/d_out, fp32 gradients out, "
                         "S0 and dL/dS_T given, dL/dS0 out; L2 flushed between calls",
             "ms": round(ms, 4), "tokens_per_s": round(T / (ms / 1e3), 1), "algorithmic_bytes": alg,
-            "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "kernels_per_call": 10,
+            "gbs": round(gbs, 1), "frac": round(gbs / pk["hbm_gbs"], 4), "kernels_per_call": 13,
             "workspace_bytes": ws.numel()}
 
 

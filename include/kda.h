@@ -410,10 +410,10 @@ typedef struct {
 /* sizeof(kda_backward_args), so a binding can check its mirror of the struct. */
 size_t kda_backward_args_bytes(void);
 
-/* Workspace of kda_prefill_backward: (ceil(T/64) + N) * H * 574720 bytes of fp32 intermediates per chunk,
- * then the tensor-core forward pass's scratch: (ceil(T/64) + N) * H * 148480 bytes of operand records and
- * N * P * H * 196608 bytes of segment fragments and entry states, P = max(1, SM count / (2 H)) on the
- * current device, then N * H int32 flags (each part 1024-byte aligned; the last 256). */
+/* Workspace of kda_prefill_backward, with n = (ceil(T/64) + N) * H chunk records: n * 574720 bytes of fp32
+ * intermediates, then the tensor-core passes' scratch: n * 148480 bytes of operand records and
+ * N * P * H * 196608 bytes of segment maps and entry states (P = max(1, 76 / H) segments per sequence), then
+ * N * H int32 flags; the first two parts are rounded up to 1024 bytes, the last to 256. */
 size_t kda_backward_workspace_size(const kda_backward_args* a);
 
 /*

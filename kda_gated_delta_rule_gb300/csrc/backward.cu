@@ -28,11 +28,12 @@
 // state and U into this workspace); otherwise it is the CUDA-core chain below.  With bf16 inputs the prep
 // also flags each (sequence, head) holding a 16-token block whose decay span passes e^80 (g below the
 // floor), where the tensor-core pass's block references overflow; the CUDA-core chain then runs for the
-// flagged (sequence, head)s only and overwrites their entry states and U.  The state products run on
+// flagged (sequence, head)s only and overwrites their entry states and U.  The reverse chain likewise: on
+// the tensor cores over the same operand records (segmented, the fragment scan run from dL/dS_T), with the
+// CUDA-core reverse chain below for fp32 inputs and the flagged (sequence, head)s.  The state products run on
 // the tensor cores (split-bf16 tcgen05 MMAs, fp32 accumulation); the remaining kernels are fp32 on the
 // CUDA cores.
 #include "common.cuh"
-#include "device.h"
 #include "launch.h"
 #include "tc_ptx.cuh"
 
@@ -484,6 +485,7 @@ constexpr size_t REV_SMEM = (2 * RS_A + RS_B + D * CB + C * CB) * sizeof(float);
 template <typename Tin>
 __global__ void __launch_bounds__(NTC, 1) bwd_rev_chain_kernel(BackwardArgs a) {
   const int cb = blockIdx.x, h = blockIdx.y, i = blockIdx.z, tid = threadIdx.x, c0 = cb * CB;
+  if (a.steep && !a.steep[(size_t)i * a.H + h]) return;  // the tensor-core reverse pass covered it
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
   extern __shared__ float sm[];
@@ -1141,11 +1143,9 @@ struct FwdLayout {
   int P;
   size_t rec_off, frag_off, entry_off, steep_off, total;
 };
-int fwd_segments_target(int H) {
-  const int sms = sm_count();
-  const int p = sms > 0 ? sms / (2 * H) : 1;
-  return p < 1 ? 1 : p;
-}
+// segments per (sequence, head) of the tensor-core passes: the fragment phase runs 2 H P CTAs, one per SM of a
+// 152-SM GPU; a constant, so that the workspace size depends on the problem alone
+int fwd_segments_target(int H) { return H >= 76 ? 1 : 76 / H; }
 FwdLayout fwd_layout(int64_t T, int N, int H) {
   FwdLayout L{};
   L.P = fwd_segments_target(H);
@@ -1158,8 +1158,10 @@ FwdLayout fwd_layout(int64_t T, int N, int H) {
   return L;
 }
 
-// The forward pass on the tensor cores (bf16 inputs): records -> fragments -> scan -> per-chunk states.
-cudaError_t forward_pass_tc(const BackwardArgs& a, cudaStream_t s) {
+// The forward and reverse passes on the tensor cores (bf16 inputs): operand records -> fragments -> scan ->
+// every chunk's entry state and U; then over the same records the state gradient's per-segment maps ->
+// their scan from dL/dS_T -> every chunk's dS' and dU, and dL/dS_0.
+cudaError_t chain_passes_tc(const BackwardArgs& a, cudaStream_t s) {
   const FwdLayout L = fwd_layout(a.T, a.N, a.H);
   const int pt = L.P;
   int seg = (int)((((int64_t)a.max_seqlen + pt - 1) / pt + C - 1) / C * C);
@@ -1185,6 +1187,13 @@ cudaError_t forward_pass_tc(const BackwardArgs& a, cudaStream_t s) {
   if (e == cudaSuccess) e = launch_tc_chain_frag(p, p.records, s);
   if (e == cudaSuccess) e = launch_seg_scan(p, s);
   if (e == cudaSuccess) e = launch_tc_chain_states(p, p.records, s);
+  p.d_out = a.d_out, p.d_final = a.d_final, p.d_init = a.d_init;
+  p.bw_off_ds = (int)BW_DS, p.bw_off_du = (int)BW_DU;
+  p.scan_init = a.d_final;  // the reverse scan starts from dL/dS_T (zero when not given)
+  p.init_zero = a.d_final == nullptr;
+  if (e == cudaSuccess) e = launch_tc_rev_frag(p, p.records, s);
+  if (e == cudaSuccess) e = launch_seg_scan(p, s);
+  if (e == cudaSuccess) e = launch_tc_rev_pass(p, p.records, s);
   return e;
 }
 
@@ -1209,11 +1218,11 @@ cudaError_t launch_backward_t(const BackwardArgs& a_in, cudaStream_t s) {
     bwd_prep_kernel<Tin><<<chunks, NT, PREP_SMEM, s>>>(a);
     if (a.in_bf16) {
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
-      if ((e = forward_pass_tc(a, s)) != cudaSuccess) return e;
+      if ((e = chain_passes_tc(a, s)) != cudaSuccess) return e;
     }
     bwd_fwd_chain_kernel<<<chains, NTC, FWD_SMEM, s>>>(a);  // (bf16: only the steep (sequence, head)s)
   }
-  bwd_rev_chain_kernel<Tin><<<chains, NTC, REV_SMEM, s>>>(a);
+  bwd_rev_chain_kernel<Tin><<<chains, NTC, REV_SMEM, s>>>(a);  // (bf16: only the steep (sequence, head)s)
   if (nch > 0) {
     bwd_state_grads_tc_kernel<Tin><<<chunks, NT, STATE_TC_SMEM, s>>>(a);
     bwd_wy_grads_kernel<Tin><<<chunks, NT, WY_SMEM, s>>>(a);

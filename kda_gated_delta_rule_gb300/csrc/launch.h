@@ -105,6 +105,17 @@ struct PrefillArgs {
   int bw_rec_floats, bw_off_h, bw_off_u;
   bool no_work_count;  // the chain adds nothing to the work counter (a pass inside another call)
   bool zero_bad_slot;  // the scan starts a sequence whose slot id is out of range from zero (flagged)
+  // the scan starts sequence i from scan_init + i * H * d * d (per head: + h * d * d) instead of the pool
+  // (null: not used)
+  const float* scan_init;
+  // the backward's reverse pass (launch_tc_rev_frag / launch_tc_rev_pass): upstream gradients dL/do
+  // [T][H][d] bf16, dL/dS_T [N][H][d][d] (null: zero) and dL/dS_0 out [N][H][d][d] (null: not written);
+  // every chunk's exit gradient dS' and dU go to the backward's records at float offsets bw_off_ds /
+  // bw_off_du
+  const void* d_out;
+  const float* d_final;
+  float* d_init;
+  int bw_off_ds, bw_off_du;
 };
 
 // Batch-invariant (CF-BI) prefill and decode (d = 128).
@@ -217,6 +228,11 @@ cudaError_t launch_tc_chain_frag(const PrefillArgs& a, const uint8_t* records, c
 // backward's records (a.bw_*) instead of outputs, and the pool is not written
 cudaError_t launch_tc_chain_states(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
+// the backward's reverse pass over the same records: per-segment affine maps of the state gradient (stored
+// in reverse segment order, for launch_seg_scan from d_final via scan_init), then every segment from its
+// exit gradient, writing each chunk's dS' and dU (a.bw_*) and dL/dS_0
+cudaError_t launch_tc_rev_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
+cudaError_t launch_tc_rev_pass(const PrefillArgs& a, const uint8_t* records, cudaStream_t s);
 
 // Launches `kernel` so that it may be scheduled while the previous kernel in the stream finishes
 // (programmatic dependent launch).  The kernel must call griddepcontrol.wait before it touches global

@@ -1159,6 +1159,330 @@ cudaError_t launch_chain(const PrefillArgs& a, const uint8_t* ws, cudaStream_t s
   return a.out_bf16 ? launch_chain_t<bf16, MODE>(a, ws, s) : launch_chain_t<float, MODE>(a, ws, s);
 }
 
+// ---------------------------------------------------------------- reverse chain (the backward's carry)
+//
+// With R the gradient at a chunk's exit state (dS') and dO the gradients of the chunk's outputs, the chunk
+// step of the recurrence above has the reverse
+//   dU = P^T dO + K^ R,   R_entry = Diag(gamma_C) R - W^T dU + (Q o gamma)^T dO,
+// the forward step with the parts of W and K^ exchanged.  R^T sits in tensor memory like S^T (lane = value
+// channel c, column = key channel j), and the forward's records serve as they are, each tile read with the
+// other major-ness: W^T [j][s] is the K-major B operand of W, K^ [t][j] the K-major B of (K^ R)^T, P [t][s]
+// and Q o gamma [t][j] the MN-major B operands of (P^T dO)^T and ((Q o gamma)^T dO)^T.  dO is bf16 as
+// given (exact), transposed into tensor memory as an A operand by the math warps a chunk ahead, so the
+// product P^T dO (independent of R) is issued into the dU accumulator while the previous chunk's split
+// runs, and (Q o gamma)^T dO into the gradient once its decay is applied.  Segmented like the forward:
+// REV_FRAG runs every segment but the first from [R | X] = [0 | I] (X without dO) to the affine map
+// R_entry = M R_exit + b of the segment, stored in reverse segment order, so that the forward's fragment
+// scan started from dL/dS_T yields every segment's exit gradient; REV_PASS runs each segment from that exit
+// gradient and writes every chunk's dS' and dU, and the first segment dL/dS_0.
+enum { REV_FRAG = 0, REV_PASS = 1 };
+constexpr uint32_t COL_DO = 64;  // dO^T (bf16 pairs), double-buffered by chunk parity: 2 x 32 columns
+
+template <int RMODE>
+__global__ void __launch_bounds__(CHAIN_NT, 1) tc_rev_kernel(const PrefillArgs a, const uint8_t* __restrict__ ws) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  float* sgam = reinterpret_cast<float*>(sm + CS_GAMMA);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + CS_BAR);
+  uint64_t* bar_du = full + 2;  // dU^T of the chunk has completed
+  uint64_t* bar_st = full + 3;  // the chunk's gradient update has completed
+  uint64_t* rdy_e1 = full + 4;  // the split gradient is in tensor memory (8 warp arrivals)
+  uint64_t* rdy_sc = full + 5;  // the fp32 gradient carries the chunk's decay
+  uint64_t* rdy_e2 = full + 6;  // -dU (split) and the next chunk's dO^T are in tensor memory
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sm + CS_SLOT);
+  const int tid = threadIdx.x, warp = tid >> 5, wg = warp >> 2;
+  const int c = tid & 127;  // value channel = TMEM lane
+  const int tile = (RMODE == REV_FRAG) ? (blockIdx.x & 1) : 0;
+  const int h = (RMODE == REV_FRAG) ? (blockIdx.x >> 1) : blockIdx.x;
+  const int p = blockIdx.y, i = blockIdx.z;
+  const bool with_do = tile == 0;  // the transition columns (tile 1) carry no output gradients
+  tc::pdl_wait();  // the previous kernel in the stream (the forward pass, the fragments or the scan) is done
+  tc::pdl_launch_dependents();
+
+  const int64_t s0 = a.cu[i], s1 = a.cu[i + 1];
+  if (s0 < 0 || s1 < s0 || s1 > a.T || s1 - s0 > (int64_t)a.max_seqlen) {
+    if (tid == 0) flag_status(a.status, KDA_DEV_SEQ_OOB);
+    return;
+  }
+  const int64_t t0 = s0 + (int64_t)p * a.seg_len;
+  const int64_t t1 = t0 + a.seg_len < s1 ? t0 + a.seg_len : s1;
+  if (RMODE == REV_FRAG) {
+    if (p == 0 || t0 >= s1) return;  // the first segment's map is not needed
+  } else if (t0 >= s1 && !(p == 0 && s1 == s0)) {
+    return;
+  }
+  const int nseg = (int)((s1 - s0 + a.seg_len - 1) / a.seg_len);
+  const int q = nseg - 1 - p;  // the segment's place in reverse order
+  const int nch = t0 < s1 ? (int)((t1 - t0 + C - 1) / C) : 0;
+  const int c_first = (int)((t0 - s0) / C);
+  const size_t head_elems = (size_t)D * D;
+
+  if (warp == 0) tc::tmem_alloc(tslot, 512);
+  if (tid == 0) {
+    tc::bar_init(full, 1);
+    tc::bar_init(full + 1, 1);
+    tc::bar_init(bar_du, 1);
+    tc::bar_init(bar_st, 1);
+    tc::bar_init(rdy_e1, CHAIN_MATH / 32);
+    tc::bar_init(rdy_sc, CHAIN_MATH / 32);
+    tc::bar_init(rdy_e2, CHAIN_MATH / 32);
+    tc::bar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tm = *tslot;
+  const uint32_t trow = tm + ((uint32_t)((warp & 3) * 32) << 16);
+
+  // the k-th chunk walked is the segment's (nch - 1 - k)-th
+  auto chunk_t0 = [&](int k) -> int64_t { return s0 + (int64_t)(c_first + nch - 1 - k) * C; };
+  auto rec_index = [&](int k) -> size_t { return (size_t)(chunk_t0(k) / C + i) * a.H + h; };
+  int issued = 0;
+  auto issue = [&](int k) {  // the chunk's record tiles into stage k & 1 (tile 1 reads only W^T and K^)
+    const int st = k & 1;
+    const uint8_t* rec = ws + rec_index(k) * REC_BYTES;
+    const uint32_t bytes = with_do ? REC_STAGE : REC_FRAG;
+    tc::bar_arrive_expect_tx(full + st, bytes + 512);
+    tc::bulk_g2s(sm + st * REC_STAGE, rec, bytes, full + st);
+    tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
+    issued = k + 1;
+  };
+  // dO of the k-th chunk, column c, this thread's 32 tokens as bf16 pairs (tokens past the end: zero)
+  auto load_do = [&](int k, uint32_t (&d)[16]) {
+    const int64_t tb = chunk_t0(k) + 32 * wg;
+    const uint16_t* src = static_cast<const uint16_t*>(a.d_out) + ((size_t)tb * a.H + h) * D + c;
+    const size_t rs = (size_t)a.H * D;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const uint32_t x0 = tb + 2 * e < t1 ? src[(size_t)(2 * e) * rs] : 0u;
+      const uint32_t x1 = tb + 2 * e + 1 < t1 ? src[(size_t)(2 * e + 1) * rs] : 0u;
+      d[e] = x0 | (x1 << 16);
+    }
+  };
+  auto store_state = [&](float* dst, size_t ld) {
+#pragma unroll 1
+    for (int jb = 0; jb < 2; ++jb) {
+      const int j0 = 64 * wg + 32 * jb;
+      float v[32];
+      tc::tmem_ld32(trow + COL_S + j0, v);
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dst[(size_t)(j0 + e) * ld] = v[e];
+    }
+  };
+  auto math_all = [&](bool ok_) { return !tc::named_bar_or(BAR_MATH, CHAIN_MATH, !ok_); };
+  auto hand_over = [&](uint64_t* bar) {
+    tc::fence_before_sync();
+    __syncwarp();
+    if ((tid & 31) == 0) tc::bar_arrive(bar);
+  };
+  // (P^T dO)^T = dO^T P into the dU accumulator: A = dO^T, B = P [t][s] (MN-major), hi and lo
+  auto issue_pdo = [&](int k) {
+    const uint64_t dp = tc::sdesc_mn(tc::smem_u32(sm + (k & 1) * REC_STAGE), 8192u);
+#pragma unroll
+    for (int part = 0; part < 2; ++part)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        tc::mma_ts(tm + COL_WS, tm + COL_DO + 32 * (k & 1) + ks * 8,
+                   dp + (((part ? REC_PLO : REC_PHI) + ks * 2048u) >> 4), tc::idesc_bf16(128, 64) | tc::IDESC_B_MN,
+                   (part | ks) != 0);
+  };
+
+  bool ok = true;
+  if (tid < CHAIN_MATH) {
+    {  // the starting gradient, transposed into tensor memory: lane c holds column c of R
+      const float* src = nullptr;
+      if (RMODE == REV_PASS) {
+        if (q <= 0)
+          src = a.d_final ? a.d_final + ((size_t)i * a.H + h) * head_elems : nullptr;
+        else
+          src = a.entry + (((size_t)i * a.P + q) * a.H + h) * head_elems;
+      }
+#pragma unroll 1
+      for (int jb = 0; jb < 2; ++jb) {
+        const int j0 = 64 * wg + 32 * jb;
+        float v[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = j0 + e;
+          v[e] = src ? src[(size_t)j * D + c] : ((RMODE == REV_FRAG && tile == 1 && j == c) ? 1.f : 0.f);
+        }
+        tc::tmem_st32f(trow + COL_S + j0, v);
+      }
+    }
+    uint32_t dn[16];
+    if (with_do && nch > 0) {
+      load_do(0, dn);
+      tc::tmem_st16(trow + COL_DO + 16 * wg, dn);
+    }
+    tc::tmem_wait_st();
+#pragma unroll 1
+    for (int k = 0; k < nch; ++k) {
+      const int st = k & 1;
+      const uint32_t par = (uint32_t)k & 1u;
+      if (with_do && k + 1 < nch) load_do(k + 1, dn);  // lands while this chunk's phases run
+      bool w_ok = tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u);
+      if (k > 0) w_ok = w_ok && tc::bar_wait(bar_st, par ^ 1u);  // the previous chunk's update
+      ok = math_all(w_ok);
+      if (!ok) break;
+      tc::fence_after_sync();
+      // E1: the chunk's exit gradient out (pass), split into the A operand, then its decay applied
+      {
+        const int j0 = 64 * wg;
+        float r[64];
+        tc::tmem_ld64(trow + COL_S + j0, r);
+        if (RMODE == REV_PASS) {
+          float* dst = a.bw_ws + rec_index(k) * a.bw_rec_floats + a.bw_off_ds + (size_t)j0 * D + c;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) dst[(size_t)e * D] = r[e];
+        }
+#pragma unroll
+        for (int jb = 0; jb < 2; ++jb) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) tc::split_pair(r[32 * jb + 2 * e], r[32 * jb + 2 * e + 1], hi[e], lo[e]);
+          tc::tmem_st16(trow + COL_STHI + j0 / 2 + 16 * jb, hi);
+          tc::tmem_st16(trow + COL_STLO + j0 / 2 + 16 * jb, lo);
+        }
+        tc::tmem_wait_st();
+        hand_over(rdy_e1);
+        const float* gm = sgam + 128 * st + j0;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) r[e] *= gm[e];
+        tc::tmem_st32f(trow + COL_S + j0, r);
+        tc::tmem_st32f(trow + COL_S + j0 + 32, r + 32);
+        if (with_do) {
+          tc::tmem_wait_st();
+          hand_over(rdy_sc);
+        }
+      }
+      ok = math_all(tc::bar_wait(bar_du, par));
+      if (!ok) break;
+      tc::fence_after_sync();
+      // E2: dU of this thread's 32 tokens out (pass); -dU split into the A operand of the update; the next
+      // chunk's dO^T into the other buffer (free: the previous chunk's products have completed)
+      {
+        float u[32];
+        tc::tmem_ld32(trow + COL_WS + 32 * wg, u);
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) tc::split_pair(-u[2 * e], -u[2 * e + 1], hi[e], lo[e]);
+        tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
+        tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
+        if (with_do && k + 1 < nch) tc::tmem_st16(trow + COL_DO + 32 * ((k + 1) & 1) + 16 * wg, dn);
+        if (RMODE == REV_PASS) {
+          float* du = a.bw_ws + rec_index(k) * a.bw_rec_floats + a.bw_off_du + (size_t)(32 * wg) * D + c;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) du[(size_t)e * D] = u[e];
+        }
+      }
+      tc::tmem_wait_st();
+      hand_over(rdy_e2);
+    }
+    if (ok && nch > 0) {
+      ok = math_all(tc::bar_wait(bar_st, (uint32_t)(nch - 1) & 1u));
+      tc::fence_after_sync();
+    }
+    if (ok) {
+      if (RMODE == REV_FRAG)
+        store_state(a.frag + (((size_t)i * a.P + q) * a.H + h) * head_elems * 2 + (size_t)tile * D + c, 2 * D);
+      else if (p == 0 && a.d_init)
+        store_state(a.d_init + ((size_t)i * a.H + h) * head_elems + c, D);
+    } else if (tid == 0) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+    }
+  } else if (tid == CHAIN_ISS_A) {  // every product, in order
+    int k = 0;
+    bool a_ok = true;
+#pragma unroll 1
+    for (; k < nch; ++k) {
+      const int st = k & 1;
+      if (!tc::bar_wait(full + st, (uint32_t)(k >> 1) & 1u) || !tc::bar_wait(rdy_e1, (uint32_t)k & 1u)) {
+        a_ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      if (k == 0 && with_do) issue_pdo(0);  // (later chunks': issued after the previous update)
+      const uint32_t base = tc::smem_u32(sm + st * REC_STAGE);
+      const uint64_t dk = tc::sdesc(base);
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {  // (K^ R)^T = R^T K^^T: B = K^ [t][j], K-major (two 64-channel blocks)
+        const uint32_t acol = tm + (part == 2 ? COL_STLO : COL_STHI);
+        const uint64_t bd = dk + ((part == 1 ? REC_KLO : REC_KHI) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc::mma_ts(tm + COL_WS, acol + ks * 8, bd + (((ks >> 2) * 8192u + (ks & 3) * 32u) >> 4),
+                     tc::idesc_bf16(128, 64), (with_do || part || ks) ? 1u : 0u);
+      }
+      tc::commit(bar_du);
+      if (with_do) {  // R^T += dO^T (Q o gamma): B = Q o gamma [t][j], MN-major (two 64-channel atoms 8 KB apart)
+        if (!tc::bar_wait(rdy_sc, (uint32_t)k & 1u)) {
+          a_ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t dq = tc::sdesc_mn(base, 8192u);
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            tc::mma_ts(tm + COL_S, tm + COL_DO + 32 * st + ks * 8,
+                       dq + (((part ? REC_QLO : REC_QHI) + ks * 2048u) >> 4), tc::idesc_bf16(128, 128) | tc::IDESC_B_MN, 1);
+      }
+      if (!tc::bar_wait(rdy_e2, (uint32_t)k & 1u)) {
+        a_ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+#pragma unroll
+      for (int part = 0; part < 3; ++part) {  // R^T += (-dU)^T W: B = W, K-major (the W^T tile's rows j)
+        const uint32_t acol = tm + (part == 2 ? COL_UTLO : COL_UTHI);
+        const uint64_t bd = dk + ((part == 1 ? REC_WLO : REC_WHI) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          tc::mma_ts(tm + COL_S, acol + ks * 8, bd + ((ks * 32u) >> 4), tc::idesc_bf16(128, 128), 1);
+      }
+      tc::commit(bar_st);
+      if (with_do && k + 1 < nch) {  // the next chunk's P^T dO, while its split is made
+        if (!tc::bar_wait(full + ((k + 1) & 1), (uint32_t)((k + 1) >> 1) & 1u)) {
+          a_ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        issue_pdo(k + 1);
+      }
+    }
+    if (!a_ok) flag_status(a.status, KDA_DEV_TIMEOUT);
+  } else if (tid == CHAIN_ISS_C) {
+    // stage k + 1 reuses stage k - 1's buffer: free once chunk k - 1's update has completed (its gamma was
+    // read before that update was issued)
+    if (nch > 0) issue(0);
+    if (nch > 1) issue(1);
+    bool cok = true;
+#pragma unroll 1
+    for (int k = 1; k + 1 < nch; ++k) {
+      cok = tc::bar_wait(bar_st, (uint32_t)(k - 1) & 1u);
+      if (!cok) break;
+      issue(k + 1);
+    }
+    if (!cok) {
+      flag_status(a.status, KDA_DEV_TIMEOUT);
+      for (int m = issued >= 2 ? issued - 2 : 0; m < issued; ++m) tc::bar_wait(full + (m & 1), (uint32_t)(m >> 1) & 1u);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tm, 512);
+}
+
+template <int RMODE>
+cudaError_t launch_rev(const PrefillArgs& a, const uint8_t* ws, cudaStream_t s) {
+  if (!a.d_out || !a.bw_ws) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc_rev_kernel<RMODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CS_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(RMODE == REV_FRAG ? 2 * a.H : a.H, a.P, a.N);
+  return launch_pdl(tc_rev_kernel<RMODE>, grid, dim3(CHAIN_NT), CS_BYTES, s, a, ws);
+}
+
 }  // namespace
 
 bool tc_supported(const PrefillArgs& a) { return a.in_bf16 && a.d == D; }
@@ -1197,6 +1521,12 @@ cudaError_t launch_tc_chain_states(const PrefillArgs& a, const uint8_t* records,
 }
 cudaError_t launch_tc_chain_segout(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
   return launch_chain<MODE_SEGOUT>(a, records, s);
+}
+cudaError_t launch_tc_rev_frag(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
+  return launch_rev<REV_FRAG>(a, records, s);
+}
+cudaError_t launch_tc_rev_pass(const PrefillArgs& a, const uint8_t* records, cudaStream_t s) {
+  return launch_rev<REV_PASS>(a, records, s);
 }
 
 }  // namespace kda

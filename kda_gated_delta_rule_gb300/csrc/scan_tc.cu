@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(SCAN_NT, 1) seg_scan_tc_kernel(const PrefillAr
       return;
     }
     nseg = (int)((s1 - s0 + a.seg_len - 1) / a.seg_len);
-    if (!a.init_zero) {
+    if (a.scan_init) {
+      init = a.scan_init + ((size_t)i * a.H + h) * head_elems;
+    } else if (!a.init_zero) {
       const int slot = a.slot_ids[i];
       if (slot < 0 || slot >= a.num_slots) {
         if (tid == 0) flag_status(a.status, KDA_DEV_SLOT_OOB);

@@ -3,12 +3,13 @@
 The loss is L = sum_t <d_out_t, o_t> + sum_i <d_final_i, S_T(i)> with seeded upstream gradients; every
 gradient the library returns (dq, dk, dv, dg, dbeta, dS_0) is compared element by element with the oracle's
 on the same input bits.  Tolerance: max |difference| <= TOL x rms(oracle) per gradient tensor.  The library
-computes in fp32 from exactly widened inputs, except the state products (dO S^T, dU S^T, U dS'^T, dO U^T),
-which run on the tensor cores with every fp32 operand split into bf16 hi + lo (relative operand error
-~2^-16); the error is that and fp32 rounding accumulated over sums of up to 128 terms per product, a few
-products per chunk and the carry through the chunk chain: measured 4e-6 to 6e-5 of the rms on the
-8192-token workload (dg the largest), so TOL = 1e-4 still holds with margin, while a wrong term (a dropped
-product, a wrong decay factor) gives errors of order 1.
+computes in fp32 from exactly widened inputs, except the products that run on the tensor cores with every
+fp32 operand split into bf16 hi + lo (hi*hi + hi*lo + lo*hi, relative operand error ~2^-17): the state
+products (dO S^T, dU S^T, U dS'^T, dO U^T) for every input type and, with bf16 inputs, the forward and
+reverse chunk chains that produce the entry states, U, dS' and dU.  The chains carry that error through up
+to 128 chunk steps (a random walk of ~1e-5 per step in the state).  Measured on the 8192-token workload:
+fp32 chains 4e-6 to 6e-5 of the rms, tensor-core chains 2.7e-5 (dS_0) to 9.6e-5 (dg, where the gradient is
+a small sum of large terms); a wrong term (a dropped product, a wrong decay factor) gives errors of order 1.
 """
 import numpy as np
 import pytest
