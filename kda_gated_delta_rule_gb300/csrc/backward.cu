@@ -941,10 +941,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
 // ---------------------------------------------------------------------------------------------------
 // 6. assembly of one (chunk, head, 64 channels): pair-decay terms, dq, dk, dg, dbeta
 // ---------------------------------------------------------------------------------------------------
-constexpr size_t ASM_SMEM = (6 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
+constexpr int NTA = 512;  // threads of the assembly kernel
+constexpr size_t ASM_SMEM = (7 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
 
 template <typename Tin>
-__global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
+__global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   const int c = blockIdx.x, h = blockIdx.y >> 1, half = blockIdx.y & 1, i = blockIdx.z, tid = threadIdx.x;
   Seq sq;
   if (!seq_bounds(a, i, sq, false)) return;
@@ -960,18 +961,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
   float* sEp = sG + C * LC;     // e^(G_t - G_r) of the current block; later dG
   float* sDP = sEp + C * LC;    // dP; later the G_C terms dK^ o K^
   float* sDA = sDP + C * LC;    // dA (beta not folded in)
-  float* sKm = sDA + C * LC;    // k o e^(G_r - G_s) of the current block [16][LC]
+  float* sDKC = sDA + C * LC;   // the sums over t >= s of dk_s (each row written by its own block)
+  float* sKm = sDKC + C * LC;   // k o e^(G_r - G_s) of the current block [16][LC]
   float* sEm = sKm + 16 * LC;   // e^(G_r - G_s) [16][LC]
   float* sB = sEm + 16 * LC;    // beta [64]
   float* sDiag = sB + C;        // dP_tt [64] (the diagonal is kept out of the pair sums: in dG its two
                                 // contributions, through q_t and through k_t, cancel exactly)
   const int64_t rs = (int64_t)a.H * D;
   const int64_t in0 = ((int64_t)t0 * a.H + h) * D;
-  load_rows<NT>(sK, LC, reinterpret_cast<const Tin*>(a.k) + in0, rs, C, n, j0, HC);
-  load_rows<NT>(sQ, LC, reinterpret_cast<const Tin*>(a.q) + in0, rs, C, n, j0, HC);
-  load_rows<NT>(sG, LC, w + BW_G, D, C, C, j0, HC);
-  load_rows<NT>(sDP, LC, w + BW_DP, C, C, C, 0, C);
-  load_rows<NT>(sDA, LC, w + BW_DA, C, C, C, 0, C);
+  load_rows<NTA>(sK, LC, reinterpret_cast<const Tin*>(a.k) + in0, rs, C, n, j0, HC);
+  load_rows<NTA>(sQ, LC, reinterpret_cast<const Tin*>(a.q) + in0, rs, C, n, j0, HC);
+  load_rows<NTA>(sG, LC, w + BW_G, D, C, C, j0, HC);
+  load_rows<NTA>(sDP, LC, w + BW_DP, C, C, C, 0, C);
+  load_rows<NTA>(sDA, LC, w + BW_DA, C, C, C, 0, C);
   if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
   cp_async_commit();
   cp_async_wait<0>();
@@ -981,8 +983,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
     sDP[tid * LC + tid] = 0.f;
   }
   __syncthreads();
-  const int ty = tid >> 4, tx = tid & 15;  // own elements: rows ty + 16i, channels tx + 16m
-  float dqp[4][4] = {}, dkr[4][4] = {}, dkc[4][4] = {};
+  const int ty = tid >> 4, tx = tid & 15;    // own elements: rows ty + 32 ii, channels tx + 16 m
+  const int orow = tid >> 5, ocol = tid & 31;  // in block b0: row b0 + orow, channels ocol + 32 mm
+  float dqp[2][4] = {}, dkr[2][4] = {};
   for (int bi = 0; bi * 16 < n; ++bi) {
     const int b0 = bi * 16, r = min(b0 + 15, n - 1);
     bool wide = false;
@@ -993,11 +996,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
     }
     wide = __syncthreads_or(wide);
     if (!wide) {
-      for (int e = tid; e < (C - b0) * HC; e += NT) {
+      for (int e = tid; e < (C - b0) * HC; e += NTA) {
         const int t = b0 + e / HC, j = e % HC;
         sEp[t * LC + j] = __expf(sG[t * LC + j] - sG[r * LC + j]);
       }
-      for (int e = tid; e < 16 * HC; e += NT) {
+      for (int e = tid; e < 16 * HC; e += NTA) {
         const int s = e / HC, j = e % HC;
         const float em = __expf(sG[r * LC + j] - sG[(b0 + s) * LC + j]);
         sEm[s * LC + j] = em;
@@ -1005,8 +1008,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
       }
       __syncthreads();
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        const int t = ty + 16 * ii;
+      for (int ii = 0; ii < 2; ++ii) {
+        const int t = ty + 32 * ii;
         if (t >= b0) {  // rows t: sum over s in the block (dP, dA masked below the diagonal already)
           float r1[4] = {}, r2[4] = {};
           for (int s = 0; s < 16; ++s) {
@@ -1027,26 +1030,26 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
           }
         }
       }
-      {  // own row s = ty + 16 bi lies in this block: sums over t >= b0
-        const int s = ty + 16 * bi;
-        float r3[4] = {};
+      {  // rows s of this block: sums over t >= b0
+        const int s = b0 + orow;
+        float r3[2] = {};
         for (int t = b0; t < C; ++t) {
           const float p = sDP[t * LC + s], q = sB[t] * sDA[t * LC + s];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const int j = tx + 16 * m;
+          for (int mm = 0; mm < 2; ++mm) {
+            const int j = ocol + 32 * mm;
             const float ep = sEp[t * LC + j];
-            r3[m] = fmaf(p, sQ[t * LC + j] * ep, fmaf(q, sK[t * LC + j] * ep, r3[m]));
+            r3[mm] = fmaf(p, sQ[t * LC + j] * ep, fmaf(q, sK[t * LC + j] * ep, r3[mm]));
           }
         }
 #pragma unroll
-        for (int m = 0; m < 4; ++m) dkc[bi][m] = fmaf(r3[m], sEm[(s - b0) * LC + tx + 16 * m], dkc[bi][m]);
+        for (int mm = 0; mm < 2; ++mm) sDKC[s * LC + ocol + 32 * mm] = r3[mm] * sEm[orow * LC + ocol + 32 * mm];
       }
       __syncthreads();
     } else {  // pair decays one by one
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) {
-        const int t = ty + 16 * ii;
+      for (int ii = 0; ii < 2; ++ii) {
+        const int t = ty + 32 * ii;
         if (t >= b0) {
           const float bt = sB[t];
 #pragma unroll
@@ -1063,16 +1066,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
           }
         }
       }
-      const int s = ty + 16 * bi;
+      const int s = b0 + orow;
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int j = tx + 16 * m;
+      for (int mm = 0; mm < 2; ++mm) {
+        const int j = ocol + 32 * mm;
         float r3 = 0.f;
         for (int t = s; t < C; ++t) {
           const float e = __expf(sG[t * LC + j] - sG[s * LC + j]);
           r3 = fmaf(sDP[t * LC + s], sQ[t * LC + j] * e, fmaf(sB[t] * sDA[t * LC + s], sK[t * LC + j] * e, r3));
         }
-        dkc[bi][m] += r3;
+        sDKC[s * LC + j] = r3;
       }
       __syncthreads();
     }
@@ -1082,13 +1085,14 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
   float* sXC = sDP;
   __syncthreads();
 #pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int t = ty + 16 * ii;
+  for (int ii = 0; ii < 2; ++ii) {
+    const int t = ty + 32 * ii;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int jl = tx + 16 * m, j = j0 + jl;
       float dG = 0.f, xc = 0.f;
       if (t < n) {
+        const float dkc = sDKC[t * LC + jl];
         const float G = sG[t * LC + jl], GC = sG[(n - 1) * LC + jl];
         const float e0 = __expf(G), ec = __expf(GC - G);
         const float kk = sK[t * LC + jl], qq = sQ[t * LC + jl];
@@ -1096,9 +1100,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_assemble_kernel(BackwardArgs a) {
         const int64_t o = ((int64_t)(t0 + t) * a.H + h) * D + j;
         const float dpt = sDiag[t];
         a.dq[o] = fmaf(dpt, kk, fmaf(gq, e0, dqp[ii][m]));
-        a.dk[o] = fmaf(dpt, qq, fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkc[ii][m])));
+        a.dk[o] = fmaf(dpt, qq, fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkc)));
         xc = gh * kk * ec;
-        dG = (gq * qq + gk * kk) * e0 + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkc[ii][m]);
+        dG = (gq * qq + gk * kk) * e0 + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkc);
       }
       sDG[t * LC + jl] = dG;
       sXC[t * LC + jl] = xc;
@@ -1226,7 +1230,7 @@ cudaError_t launch_backward_t(const BackwardArgs& a_in, cudaStream_t s) {
   if (nch > 0) {
     bwd_state_grads_tc_kernel<Tin><<<chunks, NT, STATE_TC_SMEM, s>>>(a);
     bwd_wy_grads_kernel<Tin><<<chunks, NT, WY_SMEM, s>>>(a);
-    bwd_assemble_kernel<Tin><<<halves, NT, ASM_SMEM, s>>>(a);
+    bwd_assemble_kernel<Tin><<<halves, NTA, ASM_SMEM, s>>>(a);
   }
   return cudaGetLastError();
 }
