@@ -16,10 +16,10 @@
 // hi*hi + hi*lo + lo*hi on the tensor cores (fp32 accumulate); raw bf16 operands are used as they are.
 //
 // Two kernels:
-//  * prep (one CTA per chunk and head, all chunks in parallel): G, the Gram matrices A and P as one
-//    tcgen05 MMA, the forward substitution in fp32, and the chunk's operand tiles written to a workspace
-//    record already split and swizzled: [W; Q o gamma] (hi, lo), P (hi, lo), (K o exp(G_C - G))^T (hi, lo),
-//    U~ (fp32) and gamma_C.
+//  * prep (persistent, two CTAs per SM walking the (chunk, head) tasks, all chunks in parallel): G, the Gram
+//    matrices A and P as tcgen05 MMAs (in two channel halves), the forward substitution in fp32, W^T and U~^T
+//    as MMAs, and the chunk's operand tiles written to a workspace record already split and swizzled:
+//    [W; Q o gamma] (hi, lo), P (hi, lo), (K o exp(G_C - G))^T (hi, lo), U~ (fp32) and gamma_C.
 //  * chain (one CTA per sequence or segment and head): walks the chunks in order with the transposed state
 //    S^T in tensor memory (lane = value channel c, column = key channel j); each chunk's record is
 //    bulk-copied into a double-buffered shared-memory stage ahead of use.
@@ -70,39 +70,40 @@ __device__ __forceinline__ void unpack8(uint4 r, float* x) {
 
 // ---------------------------------------------------------------- prep
 
-// shared-memory layout of the prep kernel (offsets from a 1024-aligned base)
-// X [128 rows][128 channels] bf16, hi then lo: rows 0..63 K o exp(G - G_ref), rows 64..127 Q o exp(G - G_ref);
-// channel block kb (64 channels) at kb * PS_XBLK, row r of a block at r * 128 bytes (128-byte swizzle).
-constexpr uint32_t PS_XHI = 0;
-constexpr uint32_t PS_XLO = 32768;
-constexpr uint32_t PS_XBLK = 16384;
-// Once the Gram product has completed the Q rows of X are dead: T diag(beta) hi and lo go to the Q rows of the
-// two channel blocks of X hi, and the P record tile (hi, lo) is staged in those of X lo.  The K rows stay: in
-// the common case (reference token = chunk end) they hold K o exp(G - G_C), after the block-referenced Gram
-// they are rebuilt as K o gamma, and either way they are the A operand (MN-major) of W^T.
-constexpr uint32_t PS_TBHI = PS_XHI + 8192;
-constexpr uint32_t PS_TBLO = PS_XHI + PS_XBLK + 8192;
-constexpr uint32_t PS_PHI = PS_XLO + 8192;
-constexpr uint32_t PS_PLO = PS_XLO + PS_XBLK + 8192;
-constexpr uint32_t PS_YHI = 65536;      // Y [64][128] bf16 (hi, lo; blocks of 8 KB): K o exp(G_ref - G).  In the
-constexpr uint32_t PS_YLO = 81920;      // common case it is the record's K^ tile as it stands.
-constexpr int LT = 68;                  // row stride (floats) of A and T: 8 consecutive rows, 8 bank groups
-constexpr uint32_t PS_A = 98304;        // A [64][LT] fp32 (beta folded in, strictly lower)
-constexpr uint32_t PS_T = PS_A + 64 * LT * 4;  // T = (I + A)^-1 [64][LT] fp32 (upper blocks: scratch)
-constexpr uint32_t PS_WHI = PS_A;       // after T diag(beta) is built, A and T are dead: W^T staging (hi, lo)
-constexpr uint32_t PS_WLO = PS_A + 16384;
-constexpr uint32_t PS_K = 133120;       // raw k [64][128] bf16
-constexpr uint32_t PS_Q = 149504;       // raw q [64][128] bf16
-constexpr uint32_t PS_G = 165888;       // g, then G (in place) [64][128] fp32
-constexpr uint32_t PS_V = 198656;       // raw v as two [64 t][64 c] 128-byte-swizzled blocks: MN-major A of U~^T
-constexpr uint32_t PS_BETA = 215040;    // beta [2][64], double-buffered by task parity
-constexpr uint32_t PS_BAR = 215552;     // mbarriers: Gram product, W/U products, inputs (k, q, g, beta), v
-constexpr uint32_t PS_SLOT = 215584;
-constexpr uint32_t PS_NEXT = 215592;    // the task after next (looked up by the duty thread): index, n, h, i, t0
-constexpr uint32_t PS_BYTES = 215616 + 1024;
-static_assert(PS_T + 64 * LT * 4 <= PS_K, "prep shared memory");
-constexpr int PREP_NT = 512;
+// Two 256-thread CTAs per SM, each within half of the SM's shared and tensor memory, so that one task's
+// latency-bound phases (the products, the inverse, the loads) run under the other CTA's arithmetic.
+// Shared memory (offsets from the 1024-aligned base):
+constexpr uint32_t PS_K = 0;          // raw k [64][128] bf16
+constexpr uint32_t PS_Q = 16384;      // raw q [64][128] bf16; once the Gram operands are built, the chunk's v
+                                      // as two [64 t][64 c] 128-byte-swizzled blocks (MN-major A of U~^T)
+constexpr uint32_t PS_G = 32768;      // g, then G (in place) [64][128] fp32
+constexpr uint32_t PS_H = 65536;      // 48 KB work region, in turn: the cumulative sum's scratch, the Gram
+                                      // operands of one 64-channel half, A and T, T diag(beta), W^T staging
+// Gram operands of one channel half, 128-byte rows (bf16 hi then lo): X [128 rows][64 channels] (rows
+// 0..63 k, 64..127 q, times the decay from the reference token) and Y [64][64] (k times the decay to it)
+constexpr uint32_t PS_XHI = PS_H;
+constexpr uint32_t PS_XLO = PS_H + 16384;
+constexpr uint32_t PS_YHI = PS_H + 32768;
+constexpr uint32_t PS_YLO = PS_H + 40960;
+constexpr int LT = 68;                          // row stride (floats) of A and T: 8 consecutive rows, 8 bank groups
+constexpr uint32_t PS_A = PS_H;                 // A [64][LT] fp32 (beta folded in, strictly lower)
+constexpr uint32_t PS_T = PS_A + 64 * LT * 4;   // T = (I + A)^-1 [64][LT] fp32 (upper blocks: scratch)
+constexpr uint32_t PS_TBHI = PS_H;              // T diag(beta) [64 t][64 s] bf16 (hi, lo), over the dead A
+constexpr uint32_t PS_TBLO = PS_H + 8192;
+constexpr uint32_t PS_WHI = PS_H;               // W^T staging [128 j][64 t] bf16 (hi, lo)
+constexpr uint32_t PS_WLO = PS_H + 16384;
+constexpr uint32_t PS_BETA = PS_H + 49152;      // beta [2][64], double-buffered by task parity
+constexpr uint32_t PS_BAR = PS_BETA + 512;      // mbarriers: Gram, W / U~, inputs (k, g, beta), q, v
+constexpr uint32_t PS_SLOT = PS_BAR + 40;
+constexpr uint32_t PS_NEXT = PS_SLOT + 8;       // the task after next (looked up by the duty thread): index, n, h, i, t0
+constexpr uint32_t PS_BYTES = PS_NEXT + 24;
+static_assert(PS_T + 64 * LT * 4 <= PS_BETA, "A and T in the work region");
+static_assert(PS_BYTES + 1024 <= 233472 / 2, "two CTAs per SM (1 KB of each CTA's shared memory is reserved)");
+constexpr int PREP_NT = 256;
 constexpr int PREP_PARTS = PREP_NT / D;  // threads per channel in the per-channel phases
+// tensor memory, 256 columns per CTA: the Gram product (lanes 0..63 A, 64..127 P), W^T, U~^T, and X_K^T
+// (lane = channel j, bf16 pairs of tokens) as the A operand of W^T
+constexpr uint32_t COL_GRAM = 0, COL_W = 64, COL_U = 128, COL_XKHI = 192, COL_XKLO = 224;
 
 // splits 8 floats and stores the hi and lo 16-byte chunks
 __device__ __forceinline__ void split8_store(void* hi_dst, void* lo_dst, const float* v) {
@@ -132,8 +133,7 @@ __device__ __forceinline__ void inv_mac(const float* m, const float* b, float (&
   }
 }
 
-// offset of the 16-byte chunk cc (channels 8cc..8cc+7) of row r in X (r < 128) or Y (r < 64)
-__device__ __forceinline__ uint32_t x_off(int r, int cc) { return (uint32_t)(cc >> 3) * PS_XBLK + tc::sw128_chunk(r, cc & 7); }
+// offset of the 16-byte chunk cc (channels 8cc..8cc+7) of row r in a record tile of two 64-channel blocks
 __device__ __forceinline__ uint32_t y_off(int r, int cc) { return (uint32_t)(cc >> 3) * 8192u + tc::sw128_chunk(r, cc & 7); }
 
 // 8 channels (chunk cc) of raw row t of k or q, times exp(G_t - G_ref) (sign = +1) or exp(G_ref - G_t)
@@ -148,8 +148,8 @@ __device__ __forceinline__ void decayed8(const uint8_t* sm, uint32_t src, int t,
   for (int e = 0; e < 8; ++e) v[e] *= __expf(sign * (gt[e] - gr[e]));
 }
 
-// D[:, col0 : col0 + N] = X Y[row0 : row0 + N]^T with the three split products (A, B from shared memory).
-__device__ __forceinline__ void issue_gram(uint8_t* sm, uint32_t d_tmem, int row0, int N) {
+// D[:, col0 : col0 + N] (+)= X Y[row0 : row0 + N]^T over one 64-channel half, the three split products
+__device__ __forceinline__ void issue_gram_half(uint8_t* sm, uint32_t d_tmem, int row0, int N, int acc0) {
   const uint32_t base = tc::smem_u32(sm);
   const uint32_t idesc = tc::idesc_bf16(128, N);
 #pragma unroll
@@ -157,35 +157,33 @@ __device__ __forceinline__ void issue_gram(uint8_t* sm, uint32_t d_tmem, int row
     const uint32_t xa = base + (part == 2 ? PS_XLO : PS_XHI);
     const uint32_t yb = base + (part == 1 ? PS_YLO : PS_YHI) + (uint32_t)row0 * 128u;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t koff = (uint32_t)(ks >> 2) * PS_XBLK + (uint32_t)(ks & 3) * 32u;
-      const uint32_t koff_y = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
-      tc::mma_ss(d_tmem, tc::sdesc(xa + koff), tc::sdesc(yb + koff_y), idesc, (part | ks) != 0);
-    }
+    for (int ks = 0; ks < 4; ++ks)
+      tc::mma_ss(d_tmem, tc::sdesc(xa + (uint32_t)ks * 32u), tc::sdesc(yb + (uint32_t)ks * 32u), idesc,
+                 (acc0 | part | ks) != 0);
   }
 }
 
-// W^T (tensor memory columns d_w ..) = X_K^T (T diag(beta))^T and U~^T (columns d_u ..) = V^T (T diag(beta))^T:
-// M = 128 channels, N = 64 tokens t, K = 64 tokens s; X_K and V are MN-major A operands read in place.
-__device__ __forceinline__ void issue_wu(uint8_t* sm, uint32_t d_w, uint32_t d_u) {
+// W^T (columns COL_W..) = X_K^T (T diag(beta))^T with X_K^T in tensor memory, and U~^T (columns COL_U..) =
+// V^T (T diag(beta))^T with V an MN-major A operand read in place: M = 128 channels, N = 64 tokens t,
+// K = 64 tokens s
+__device__ __forceinline__ void issue_wu(uint8_t* sm, uint32_t tm) {
   const uint32_t base = tc::smem_u32(sm);
-  constexpr uint32_t idesc = tc::idesc_bf16(128, 64) | tc::IDESC_A_MN;
+  constexpr uint32_t idesc = tc::idesc_bf16(128, 64);
 #pragma unroll
   for (int part = 0; part < 3; ++part) {
-    const uint32_t xa = base + (part == 2 ? PS_XLO : PS_XHI);
+    const uint32_t acol = tm + (part == 2 ? COL_XKLO : COL_XKHI);
     const uint32_t tb = base + (part == 1 ? PS_TBLO : PS_TBHI);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_ss(d_w, tc::sdesc_mn(xa + (uint32_t)ks * 2048u, PS_XBLK), tc::sdesc(tb + (uint32_t)ks * 32u), idesc,
-                 (part | ks) != 0);
+      tc::mma_ts(tm + COL_W, acol + (uint32_t)ks * 8u, tc::sdesc(tb + (uint32_t)ks * 32u), idesc, (part | ks) != 0);
   }
 #pragma unroll
   for (int part = 0; part < 2; ++part) {  // V is exact in bf16: split T diag(beta) only
     const uint32_t tb = base + (part == 1 ? PS_TBLO : PS_TBHI);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      tc::mma_ss(d_u, tc::sdesc_mn(base + PS_V + (uint32_t)ks * 2048u, 8192u), tc::sdesc(tb + (uint32_t)ks * 32u),
-                 idesc, (part | ks) != 0);
+      tc::mma_ss(tm + COL_U, tc::sdesc_mn(base + PS_Q + (uint32_t)ks * 2048u, 8192u), tc::sdesc(tb + (uint32_t)ks * 32u),
+                 idesc | tc::IDESC_A_MN, (part | ks) != 0);
   }
 }
 
@@ -201,12 +199,14 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 
 // Persistent: each CTA walks the task list (task = (sequence i, head h, chunk slot cidx)) with stride
-// gridDim.x, skipping empty chunk slots, and prefetches the next task's inputs while it finishes one (k, q,
-// g once the Gram product has consumed them, v once the W / U~ products have).
-__global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a, uint8_t* __restrict__ ws,
+// gridDim.x, skipping empty chunk slots.  Per task: the cumulative sum; X_K^T into tensor memory and the Gram
+// product in two channel halves (the operands of one half at a time); A and P out of tensor memory; the
+// inverse; W^T and U~^T; the record.  The next task's k, g and beta are requested once this task's operands
+// are built, its q once this task's U~ product has read v (which took q's place).
+__global__ void __launch_bounds__(PREP_NT, 2) tc_prep_kernel(const PrefillArgs a, uint8_t* __restrict__ ws,
                                                               const __grid_constant__ PrepMaps maps, int nchunk) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(sm + PS_K);
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm + PS_Q);
   float* sG = reinterpret_cast<float*>(sm + PS_G);
@@ -218,6 +218,10 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   const int tid = threadIdx.x, warp = tid >> 5;
   tc::pdl_wait();  // the previous kernel in the stream (inputs, and any reader of the record buffer) is done
   tc::pdl_launch_dependents();
+  if (tc::smem_u32(sm) & 1023u) {  // the swizzled operand tiles need a 1024-byte aligned base (not expected)
+    if (tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
+    return;
+  }
   constexpr int DUTY = PREP_NT - 1;  // issues the bulk stores and the tensor-map loads
   const int total = nchunk * a.H * a.N;
   struct Task {
@@ -248,14 +252,13 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     while (t < total && task_at(t).n == 0) t += (int)gridDim.x;
     return t;
   };
-  // the chunk's k, q and g tiles (64 tokens x 128 channels of head h) with three TMA loads, beta with 4-byte
-  // copies that arrive on the same barrier
-  auto fetch_main = [&](const Task& tk, int k) {
+  // the chunk's k and g tiles (64 tokens x 128 channels of head h) with two tensor-map loads, beta with
+  // 4-byte copies that arrive on the same barrier (all threads call this)
+  auto fetch_kg = [&](const Task& tk, int k) {
     uint64_t* fb = bar + 2;
     if (tid == DUTY) {
-      tc::bar_arrive_expect_tx(fb, 2 * 16384 + 32768);
+      tc::bar_arrive_expect_tx(fb, 16384 + 32768);
       tc::tma_load_3d(sK, &maps.k, 0, tk.h, (int)tk.t0, fb);
-      tc::tma_load_3d(sQ, &maps.q, 0, tk.h, (int)tk.t0, fb);
       tc::tma_load_3d(sG, &maps.g, 0, tk.h, (int)tk.t0, fb);
     }
     if (tid >= D && tid < D + C) {
@@ -266,26 +269,50 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(tc::smem_u32(fb)) : "memory");
     }
   };
-  // the chunk's v tile as two 64-channel swizzled blocks (duty thread only)
-  auto fetch_v = [&](const Task& tk) {
+  // the chunk's q tile; its v tile as two 64-channel swizzled blocks in the same place (duty thread only)
+  auto fetch_q = [&](const Task& tk) {
     tc::bar_arrive_expect_tx(bar + 3, 16384);
-    tc::tma_load_3d(sm + PS_V, &maps.v, 0, tk.h, (int)tk.t0, bar + 3);
-    tc::tma_load_3d(sm + PS_V + 8192, &maps.v, 64, tk.h, (int)tk.t0, bar + 3);
+    tc::tma_load_3d(sQ, &maps.q, 0, tk.h, (int)tk.t0, bar + 3);
+  };
+  auto fetch_v = [&](const Task& tk) {
+    tc::bar_arrive_expect_tx(bar + 4, 16384);
+    tc::tma_load_3d(sm + PS_Q, &maps.v, 0, tk.h, (int)tk.t0, bar + 4);
+    tc::tma_load_3d(sm + PS_Q + 8192, &maps.v, 64, tk.h, (int)tk.t0, bar + 4);
   };
 
   if (warp == 0) tc::tmem_alloc(tslot, 256);
   if (tid == 0) {
     tc::bar_init(bar + 0, 1);
     tc::bar_init(bar + 1, 1);
-    tc::bar_init(bar + 2, 1 + C);  // the TMA issuer + one arrival per beta thread
+    tc::bar_init(bar + 2, 1 + C);  // the tensor-map issuer + one arrival per beta thread
     tc::bar_init(bar + 3, 1);
+    tc::bar_init(bar + 4, 1);
     tc::bar_fence_init();
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tm = *tslot;
-  constexpr uint32_t COL_W = 64, COL_U = 128;  // W^T and U~^T accumulators; the Gram product uses columns 0..63
+  const uint32_t tlane = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's quarter of the tensor-memory lanes
+  // X_K^T into tensor memory: lane j = channel, tokens 32 (warp / 4) .. + 31 as bf16 pairs (hi, lo);
+  // k o exp(G - G_C) in the common case, k o gamma when the Gram took block references
+  auto xk_to_tmem = [&](bool gamma_ref) {
+    const int j = 32 * (warp & 3) + (tid & 31), tg = warp >> 2;
+    const float gcj = sG[(C - 1) * D + j];
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int t = 32 * tg + 2 * e;
+      const float g0 = sG[t * D + j], g1 = sG[(t + 1) * D + j];
+      const float x0 = __bfloat162float(sK[t * D + j]) * __expf(gamma_ref ? g0 : g0 - gcj);
+      const float x1 = __bfloat162float(sK[(t + 1) * D + j]) * __expf(gamma_ref ? g1 : g1 - gcj);
+      tc::split_pair(x0, x1, hi[e], lo[e]);
+    }
+    tc::tmem_st16(tm + tlane + COL_XKHI + 16 * tg, hi);
+    tc::tmem_st16(tm + tlane + COL_XKLO + 16 * tg, lo);
+    tc::tmem_wait_st();
+    tc::fence_before_sync();
+  };
   uint32_t gram_uses = 0;
   // the current and the next task; the one after is looked up mid-task (its cu_seqlens loads then overlap
   // the inverse instead of sitting at the top of the loop)
@@ -295,15 +322,14 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   int nxt = cur < total ? next_task(cur + (int)gridDim.x) : total;
   Task tnxt{};
   if (nxt < total) tnxt = task_at(nxt);
-  // local indices of tasks whose inputs (k, q, g, beta) or v are requested but not yet waited for
-  int inflight = -1, inflight_v = -1;
+  // local indices of tasks whose copies are requested but not yet waited for
+  int inflight_kg = -1, inflight_q = -1, inflight_v = -1;
   // the test hook issues nothing here, so the first wait below gives up with no copy in flight
   const uint32_t input_polls = a.test_stall_inputs ? (1u << 12) : (1u << 22);
   if (cur < total && !a.test_stall_inputs) {
-    fetch_main(tcur, 0);
-    inflight = 0;
-    if (tid == DUTY) fetch_v(tcur);
-    inflight_v = 0;
+    fetch_kg(tcur, 0);
+    if (tid == DUTY) fetch_q(tcur);
+    inflight_kg = inflight_q = 0;
   }
   bool ok = true;
   int k = 0;
@@ -314,9 +340,11 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   const int64_t t0 = tk.t0;
   uint8_t* rec = ws + ((size_t)(t0 / C + i) * a.H + h) * REC_BYTES;
   float* const sbeta = sbeta_all + C * (k & 1);
-  ok = __syncthreads_and(tc::bar_wait(bar + 2, (uint32_t)k & 1u, input_polls));
+  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's W^T stores have read their staging
+  ok = __syncthreads_and(tc::bar_wait(bar + 2, (uint32_t)k & 1u, input_polls) &&
+                         tc::bar_wait(bar + 3, (uint32_t)k & 1u, input_polls));
   if (!ok) break;
-  inflight = -1;
+  inflight_kg = inflight_q = -1;
   // rows past the chunk's valid tokens (the next sequence's, or beyond T) are zero: k = q = g = 0 (v below)
   for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
     const int t = n + (e >> 4), cc = e & 15;
@@ -327,16 +355,14 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     *reinterpret_cast<float4*>(sG + t * D + cc * 8 + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
-  // cumulative log-decay in place: thread (j, part) scans 16 tokens and adds the totals of the parts
+  // cumulative log-decay in place: thread (j, part) scans 32 tokens and adds the totals of the parts
   // before it; the decay span of channel j (including the chunk start, G = 0) decides the path
   float span = 0.f;
   {
     constexpr int TQ = C / PREP_PARTS;
     const int j = tid & (D - 1), part = tid / D;
-    // scratch in the Q rows of X hi's first channel block (T diag(beta) there was read by the previous
-    // task's W / U~ products, which have completed; the X build follows only after the next barriers)
-    float* ext = reinterpret_cast<float*>(sm + PS_TBHI);  // extremes [PREP_NT][2]
-    float* gpart = ext + 2 * PREP_NT;                      // part totals [PREP_PARTS][D]
+    float* ext = reinterpret_cast<float*>(sm + PS_H);  // extremes [PREP_NT][2] (the work region is free)
+    float* gpart = ext + 2 * PREP_NT;                  // part totals [PREP_PARTS][D]
     float x[TQ];
 #pragma unroll
     for (int u = 0; u < TQ; ++u) x[u] = sG[(TQ * part + u) * D + j];
@@ -369,155 +395,151 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   // gamma_C of channel tid & 127: the W^T epilogue's scale and the record's gamma
   const float gamma_c = __expf(sG[(C - 1) * D + (tid & (D - 1))]);
   if (tid < D) reinterpret_cast<float*>(rec + REC_GAMMA)[tid] = gamma_c;
-  if (tid == DUTY) tc::bulk_wait_read0();  // the previous task's P, K^ and W^T stores have read their staging
-  tc::fence_before_sync();
-  const bool slow = __syncthreads_or(span > SPAN_MAX);
-  tc::fence_after_sync();
+  const bool slow = __syncthreads_or(span > SPAN_MAX);  // (also: every thread is done with the scratch)
 
-  // per (token t, 8 channels): Q o gamma (record), and in the common case X and Y (reference = chunk end)
-  for (int task = tid; task < C * 16; task += PREP_NT) {
-    const int t = task >> 4, cc = task & 15;
-    float kx[8], qx[8], gt[8], v[8];
-    unpack8(*reinterpret_cast<const uint4*>(sK + t * D + cc * 8), kx);
-    unpack8(*reinterpret_cast<const uint4*>(sQ + t * D + cc * 8), qx);
-    load8f(sG + t * D + cc * 8, gt);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = qx[e] * __expf(gt[e]);
-    const uint32_t ob = y_off(t, cc);
-    split8_store(rec + REC_QHI + ob, rec + REC_QLO + ob, v);
-    if (!slow) {
-      float gc[8], e1[8];
-      load8f(sG + (C - 1) * D + cc * 8, gc);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) e1[e] = __expf(gt[e] - gc[e]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = kx[e] * e1[e];
-      split8_store(sm + PS_XHI + x_off(t, cc), sm + PS_XLO + x_off(t, cc), v);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = qx[e] * e1[e];
-      split8_store(sm + PS_XHI + x_off(64 + t, cc), sm + PS_XLO + x_off(64 + t, cc), v);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = kx[e] * __expf(gc[e] - gt[e]);
-      split8_store(sm + PS_YHI + y_off(t, cc), sm + PS_YLO + y_off(t, cc), v);
-    }
-  }
-
-  // Gram matrices in TMEM columns 0..63: lanes 0..63 = A rows (before beta), lanes 64..127 = P rows
-  bool fetched = false;  // the next task's k, q, g requested already
-  if (ok && !slow) {
-    tc::fence_proxy_async();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      issue_gram(sm, tm, 0, 64);
-      tc::commit(bar);
-    }
-    // in the common case raw k, q, g are dead once X and Y are built: the next task's inputs may land
+  // the next task's k, g and beta, and this task's v, once this task's raw k, q, g are dead
+  auto prefetch = [&]() {
+    if (tid == DUTY) fetch_v(tk);
+    inflight_v = k;
     if (nxt < total) {
-      fetch_main(tnxt, k + 1);
-      inflight = k + 1;
-      fetched = true;
+      fetch_kg(tnxt, k + 1);
+      inflight_kg = k + 1;
     }
-    ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));
-    ++gram_uses;
-  } else if (ok) {
-    // decay span above the limit: per 16-token block b, pair factors referenced at the block's last token
-    for (int e = tid; e < C * 16; e += PREP_NT) {
-      const int s = e >> 4, cc = e & 15;
-      float v[8];
-      decayed8(sm, PS_K, s, cc, (s & ~15) + 15, -1.f, v);
-      split8_store(sm + PS_YHI + y_off(s, cc), sm + PS_YLO + y_off(s, cc), v);
-    }
-    for (int b = 0; b < 4; ++b) {
-      for (int e = tid; e < 128 * 16; e += PREP_NT) {
-        const int r = e >> 4, cc = e & 15, t = r & 63;
-        float v[8];
-        if (t < 16 * b) {
+  };
+  if (!slow) {
+    // Gram matrices in tensor memory columns 0..63, one 64-channel half at a time (reference = chunk end);
+    // the record's Q o gamma and K^ = K o exp(G_C - G) (= Y) of the half on the way
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      for (int task = tid; task < C * 8; task += PREP_NT) {
+        const int t = task >> 3, c8 = task & 7, cc = 8 * hh + c8;
+        float kx[8], qx[8], gt[8], gc[8], e1[8], v[8];
+        unpack8(*reinterpret_cast<const uint4*>(sK + t * D + cc * 8), kx);
+        unpack8(*reinterpret_cast<const uint4*>(sQ + t * D + cc * 8), qx);
+        load8f(sG + t * D + cc * 8, gt);
+        load8f(sG + (C - 1) * D + cc * 8, gc);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) v[q] = 0.f;
-        } else {
-          decayed8(sm, r < 64 ? PS_K : PS_Q, t, cc, 16 * b + 15, 1.f, v);
-        }
-        split8_store(sm + PS_XHI + x_off(r, cc), sm + PS_XLO + x_off(r, cc), v);
+        for (int e = 0; e < 8; ++e) v[e] = qx[e] * __expf(gt[e]);
+        split8_store(rec + REC_QHI + y_off(t, cc), rec + REC_QLO + y_off(t, cc), v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) e1[e] = __expf(gt[e] - gc[e]);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = kx[e] * e1[e];
+        split8_store(sm + PS_XHI + tc::sw128_chunk(t, c8), sm + PS_XLO + tc::sw128_chunk(t, c8), v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = qx[e] * e1[e];
+        split8_store(sm + PS_XHI + tc::sw128_chunk(64 + t, c8), sm + PS_XLO + tc::sw128_chunk(64 + t, c8), v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = kx[e] * __expf(gc[e] - gt[e]);
+        split8_store(sm + PS_YHI + tc::sw128_chunk(t, c8), sm + PS_YLO + tc::sw128_chunk(t, c8), v);
+        split8_store(rec + REC_KHI + y_off(t, cc), rec + REC_KLO + y_off(t, cc), v);
       }
       tc::fence_proxy_async();
       __syncthreads();
       if (tid == 0) {
         tc::fence_after_sync();
-        issue_gram(sm, tm + 16 * b, 16 * b, 16);
+        issue_gram_half(sm, tm + COL_GRAM, 0, 64, hh);
         tc::commit(bar);
       }
-      ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));  // block-uniform: no thread leaves alone
+      if (hh == 0)
+        xk_to_tmem(false);  // while the first half's product runs
+      else
+        prefetch();  // raw k, q, g are dead: X_K^T is in tensor memory, the records' tiles are written
+      ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));
       ++gram_uses;
       if (!ok) break;
     }
-    // X and Y are free again: the K rows of X become K o gamma (A operand of W^T, no rescale) and Y the
-    // record's K^ = K o exp(G_C - G)
-    if (ok) {
+  } else {
+    // decay span above the limit: per 16-token block b, pair factors referenced at the block's last token,
+    // one channel half at a time
+#pragma unroll 1
+    for (int hh = 0; hh < 2 && ok; ++hh) {
+      for (int e = tid; e < C * 8; e += PREP_NT) {
+        const int s = e >> 3, c8 = e & 7;
+        float v[8];
+        decayed8(sm, PS_K, s, 8 * hh + c8, (s & ~15) + 15, -1.f, v);
+        split8_store(sm + PS_YHI + tc::sw128_chunk(s, c8), sm + PS_YLO + tc::sw128_chunk(s, c8), v);
+      }
+#pragma unroll 1
+      for (int b = 0; b < 4; ++b) {
+        for (int e = tid; e < 128 * 8; e += PREP_NT) {
+          const int r = e >> 3, c8 = e & 7, t = r & 63;
+          float v[8];
+          if (t < 16 * b) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = 0.f;
+          } else {
+            decayed8(sm, r < 64 ? PS_K : PS_Q, t, 8 * hh + c8, 16 * b + 15, 1.f, v);
+          }
+          split8_store(sm + PS_XHI + tc::sw128_chunk(r, c8), sm + PS_XLO + tc::sw128_chunk(r, c8), v);
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+        if (tid == 0) {
+          tc::fence_after_sync();
+          issue_gram_half(sm, tm + COL_GRAM + 16 * b, 16 * b, 16, hh);
+          tc::commit(bar);
+        }
+        ok = __syncthreads_and(tc::bar_wait(bar, gram_uses & 1u));  // block-uniform: no thread leaves alone
+        ++gram_uses;
+        if (!ok) break;
+      }
+    }
+    if (ok) {  // X_K^T = K o gamma (no rescale); the record's Q o gamma and K^ = K o exp(G_C - G)
+      xk_to_tmem(true);
       for (int e = tid; e < C * 16; e += PREP_NT) {
         const int t = e >> 4, cc = e & 15;
-        float kx[8], gt[8], gc[8], v[8];
+        float kx[8], qx[8], gt[8], gc[8], v[8];
         unpack8(*reinterpret_cast<const uint4*>(sK + t * D + cc * 8), kx);
+        unpack8(*reinterpret_cast<const uint4*>(sQ + t * D + cc * 8), qx);
         load8f(sG + t * D + cc * 8, gt);
         load8f(sG + (C - 1) * D + cc * 8, gc);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) v[q] = kx[q] * __expf(gt[q]);
-        split8_store(sm + PS_XHI + x_off(t, cc), sm + PS_XLO + x_off(t, cc), v);
+        for (int q = 0; q < 8; ++q) v[q] = qx[q] * __expf(gt[q]);
+        split8_store(rec + REC_QHI + y_off(t, cc), rec + REC_QLO + y_off(t, cc), v);
 #pragma unroll
         for (int q = 0; q < 8; ++q) v[q] = kx[q] * __expf(gc[q] - gt[q]);
-        split8_store(sm + PS_YHI + y_off(t, cc), sm + PS_YLO + y_off(t, cc), v);
+        split8_store(rec + REC_KHI + y_off(t, cc), rec + REC_KLO + y_off(t, cc), v);
       }
+      tc::fence_proxy_async();
+      __syncthreads();
+      prefetch();
     }
   }
 
   if (ok) {
+    // A (beta, strictly lower) to shared memory (the Gram operands are dead) and P (lower incl. diagonal)
+    // to the record: lane row 32 (warp % 4) + lane (rows 0..63 = A, 64..127 = P), columns 32 (warp / 4) ..
     tc::fence_after_sync();
-    if (warp < 8) {
-      // A (beta, strictly lower) to shared memory and P (lower incl. diagonal) to its staging: lane row
-      // 32 (warp % 4) + lane (rows 0..63 = A, 64..127 = P), columns 32 (warp / 4) .. + 31
-      const int q = warp & 3, ch = warp >> 2, row = 32 * q + (tid & 31);
-      float v[32];
-      tc::tmem_ld32(tm + ((uint32_t)(q * 32) << 16) + 32 * ch, v);
-      if (row < 64) {
-        const int t = row;
-        const float bt = sbeta[t];
+    const int q = warp & 3, ch = warp >> 2, row = 32 * q + (tid & 31);
+    float v[32];
+    tc::tmem_ld32(tm + tlane + COL_GRAM + 32 * ch, v);
+    if (row < 64) {
+      const int t = row;
+      const float bt = sbeta[t];
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const int s0c = 32 * ch + i;
-          float4 r;
-          r.x = s0c + 0 < t ? bt * v[i + 0] : 0.f;
-          r.y = s0c + 1 < t ? bt * v[i + 1] : 0.f;
-          r.z = s0c + 2 < t ? bt * v[i + 2] : 0.f;
-          r.w = s0c + 3 < t ? bt * v[i + 3] : 0.f;
-          *reinterpret_cast<float4*>(sA + t * LT + s0c) = r;
-        }
-      } else {
-        const int t = row - 64;
+      for (int u = 0; u < 32; u += 4) {
+        const int s0c = 32 * ch + u;
+        float4 r;
+        r.x = s0c + 0 < t ? bt * v[u + 0] : 0.f;
+        r.y = s0c + 1 < t ? bt * v[u + 1] : 0.f;
+        r.z = s0c + 2 < t ? bt * v[u + 2] : 0.f;
+        r.w = s0c + 3 < t ? bt * v[u + 3] : 0.f;
+        *reinterpret_cast<float4*>(sA + t * LT + s0c) = r;
+      }
+    } else {
+      const int t = row - 64;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int cc = 4 * ch + i;
-          float pv[8];
+      for (int u = 0; u < 4; ++u) {
+        const int cc = 4 * ch + u;
+        float pv[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) pv[e] = 8 * cc + e <= t ? v[8 * i + e] : 0.f;
-          split8_store(sm + PS_PHI + tc::sw128_chunk(t, cc), sm + PS_PLO + tc::sw128_chunk(t, cc), pv);
-        }
+        for (int e = 0; e < 8; ++e) pv[e] = 8 * cc + e <= t ? v[8 * u + e] : 0.f;
+        split8_store(rec + REC_PHI + tc::sw128_chunk(t, cc), rec + REC_PLO + tc::sw128_chunk(t, cc), pv);
       }
     }
-    tc::fence_proxy_async();
   }
   __syncthreads();
-  if (ok && tid == DUTY) {
-    tc::bulk_s2g(rec + REC_PHI, sm + PS_PHI, 8192);
-    tc::bulk_s2g(rec + REC_PLO, sm + PS_PLO, 8192);
-    tc::bulk_s2g(rec + REC_KHI, sm + PS_YHI, 16384);
-    tc::bulk_s2g(rec + REC_KLO, sm + PS_YLO, 16384);
-    tc::bulk_commit();
-  }
-  // raw k, q, g are dead: the next task's (v follows once the W / U~ products have read this one's)
-  if (ok && nxt < total && !fetched) {
-    fetch_main(tnxt, k + 1);
-    inflight = k + 1;
-  }
   // the duty thread starts looking up the task after next: the candidate's cu_seqlens loads are issued
   // here and consumed before the W/U product, thousands of cycles later
   const int cand = nxt < total ? nxt + (int)gridDim.x : total;
@@ -529,10 +551,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   }
 
   if (ok) {
-    // T = (I + A)^-1, blocked by 16, on warps 0..7 (warps 8..15 compute nothing here; the duty thread may
-    // still be issuing the bulk stores and the next task's loads).
-    // Diagonal blocks by forward substitution (threads 0..63, one column each).
-    constexpr int INV_THREADS = 256;
+    // T = (I + A)^-1, blocked by 16.  Diagonal blocks by forward substitution (threads 0..63, one column each).
     if (tid < 64) {
       const int b = tid >> 4, cc = tid & 15;
       float x[16];
@@ -546,7 +565,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
 #pragma unroll
       for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LT + 16 * b + cc] = x[r];
     }
-    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+    __syncthreads();
     // Off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -sum_{k=j}^{i-1} M_ik T_kj with
     // M_ik = T_ii A_ik.  Every 16 x 16 block product is one warp's: lane (rp, cg) owns rows rp and rp + 8,
     // columns 4 cg .. 4 cg + 3, and per step two conflict-free scalar loads (a warp's eight rows sit in eight
@@ -575,13 +594,13 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       mac(tblk(bi, bi), sA + 16 * bi * LT + 16 * bk, a0, a1);
       put(tblk(bk, bi), LT, a0, a1, 1.f);
     }
-    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+    __syncthreads();
     if (wv < 3) {  // round 2: T_{w+1,w} = -M_{w+1,w} T_ww
       float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
       mac(tblk(wv, wv + 1), tblk(wv, wv), a0, a1);
       put(tblk(wv + 1, wv), LT, a0, a1, -1.f);
     }
-    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+    __syncthreads();
     if (wv < 6) {  // round 3: (i, j, k) = (2,0,0) (2,0,1) (3,1,1) (3,1,2) (3,0,0) (3,0,1): M_ik T_kj into slot wv
       const int bi = wv < 2 ? 2 : 3, bj = wv < 2 ? 0 : (wv < 4 ? 1 : 0);
       const int bk = wv == 0 ? 0 : (wv == 1 ? 1 : (wv == 2 ? 1 : (wv == 3 ? 2 : (wv == 4 ? 0 : 1))));
@@ -589,7 +608,7 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
       mac(tblk(bk, bi), tblk(bk, bj), a0, a1);
       put(pblk(wv), PLD, a0, a1, 1.f);
     }
-    if (tid < INV_THREADS) tc::named_bar(1, INV_THREADS);
+    __syncthreads();
     if (wv < 3) {  // round 4
       float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
       if (wv == 2) {  // M_32 (M_20 T_00 + M_21 T_10): the second operand summed on the fly
@@ -615,28 +634,27 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
             make_float4(ac[0] - (x0.x + x1.x), ac[1] - (x0.y + x1.y), ac[2] - (x0.z + x1.z), ac[3] - (x0.w + x1.w));
       }
     }
-    // this task's v (requested during the previous task) has landed: its rows past the valid tokens are zeroed
-    // below, while T diag(beta) is formed
-    ok = __syncthreads_and(tc::bar_wait(bar + 3, (uint32_t)k & 1u));
+    // this task's v (requested once its operands were built) has landed: its rows past the valid tokens
+    // are zeroed below, and T diag(beta) then takes the place of the dead A
+    ok = __syncthreads_and(tc::bar_wait(bar + 4, (uint32_t)k & 1u));
     if (ok) {
       inflight_v = -1;
       for (int e = tid; e < (C - n) * 16; e += PREP_NT) {
         const int t = n + (e >> 4), q = e & 15;
-        *reinterpret_cast<uint4*>(sm + PS_V + (uint32_t)(q >> 3) * 8192u + (uint32_t)t * 128u + (uint32_t)(q & 7) * 16u) =
+        *reinterpret_cast<uint4*>(sm + PS_Q + (uint32_t)(q >> 3) * 8192u + (uint32_t)t * 128u + (uint32_t)(q & 7) * 16u) =
             make_uint4(0, 0, 0, 0);
       }
-    }
-    // T diag(beta) as the B operand of W^T and U~^T (lower triangle only), into the Q rows of X hi
-    {
-      const int t = tid >> 3, cc = tid & 7;
-      static_assert(C * 8 == PREP_NT, "one 8-column strip of T diag(beta) per thread");
-      float v[8];
+      // T diag(beta) as the B operand of W^T and U~^T (lower triangle only)
+      for (int st = tid; st < C * 8; st += PREP_NT) {
+        const int t = st >> 3, cc = st & 7;
+        float v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int s = 8 * cc + e;
-        v[e] = s <= t ? sT[t * LT + s] * sbeta[s] : 0.f;
+        for (int e = 0; e < 8; ++e) {
+          const int s = 8 * cc + e;
+          v[e] = s <= t ? sT[t * LT + s] * sbeta[s] : 0.f;
+        }
+        split8_store(sm + PS_TBHI + tc::sw128_chunk(t, cc), sm + PS_TBLO + tc::sw128_chunk(t, cc), v);
       }
-      split8_store(sm + PS_TBHI + tc::sw128_chunk(t, cc), sm + PS_TBLO + tc::sw128_chunk(t, cc), v);
     }
     if (tid == DUTY) {  // the task after next (an empty candidate falls back to the full search)
       int n2 = cand;
@@ -660,38 +678,36 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
     __syncthreads();
     if (ok && tid == 0) {
       tc::fence_after_sync();
-      issue_wu(sm, tm + COL_W, tm + COL_U);
+      issue_wu(sm, tm);
       tc::commit(bar + 1);
     }
     if (ok) ok = __syncthreads_and(tc::bar_wait(bar + 1, (uint32_t)k & 1u));
   }
 
   if (ok) {
-    // v has been read: the next task's may land
-    if (tid == DUTY && nxt < total) fetch_v(tnxt);
-    if (nxt < total) inflight_v = k + 1;
-    // W^T and U~^T rows (lane = channel r), 32 tokens per warp: warps 4g + q read lanes 32 q .. 32 q + 31 and
-    // columns 32 (g & 1) .. of W^T (g < 2) or U~^T (g >= 2).  W^T (split) is staged in the dead A / T region
-    // for two bulk stores; U~ goes straight to the record, one coalesced 128-byte token row per warp store.
+    // v has been read: the next task's q may land in its place
+    if (tid == DUTY && nxt < total) fetch_q(tnxt);
+    if (nxt < total) inflight_q = k + 1;
+    // W^T and U~^T rows (lane = channel r), 32 tokens per warp: warp 4 g + q reads lanes 32 q .. 32 q + 31
+    // and columns 32 g .. of both.  W^T (split) is staged in the work region for two bulk stores; U~ goes
+    // straight to the record, one coalesced 128-byte token row per warp store.
     tc::fence_after_sync();
-    const int q = warp & 3, g = warp >> 2, r = tid & (D - 1);
+    const int g = warp >> 2, r = tid & (D - 1);
     float v[32];
-    tc::tmem_ld32(tm + ((uint32_t)(q * 32) << 16) + (g < 2 ? COL_W : COL_U) + 32 * (g & 1), v);
-    if (g < 2) {
-      const float sc = slow ? 1.f : gamma_c;  // X_K = K o exp(G - G_C) in the common case
+    tc::tmem_ld32(tm + tlane + COL_W + 32 * g, v);
+    const float sc = slow ? 1.f : gamma_c;  // X_K = K o exp(G - G_C) in the common case
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] *= sc;
+    for (int e = 0; e < 32; ++e) v[e] *= sc;
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t o = tc::sw128_chunk(r, 4 * (g & 1) + ch);
-        split8_store(sm + PS_WHI + o, sm + PS_WLO + o, v + 8 * ch);
-      }
-      tc::fence_proxy_async();
-    } else {
-      float* U = reinterpret_cast<float*>(rec + REC_U) + (size_t)32 * (g & 1) * D + r;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) U[(size_t)e * D] = v[e];
+    for (int ch = 0; ch < 4; ++ch) {
+      const uint32_t o = tc::sw128_chunk(r, 4 * g + ch);
+      split8_store(sm + PS_WHI + o, sm + PS_WLO + o, v + 8 * ch);
     }
+    tc::fence_proxy_async();
+    tc::tmem_ld32(tm + tlane + COL_U + 32 * g, v);
+    float* U = reinterpret_cast<float*>(rec + REC_U) + (size_t)32 * g * D + r;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) U[(size_t)e * D] = v[e];
   }
   __syncthreads();
   if (ok && tid == DUTY) {
@@ -716,8 +732,9 @@ __global__ void __launch_bounds__(PREP_NT, 1) tc_prep_kernel(const PrefillArgs a
   if (!ok) {
     if (tid == 0) flag_status(a.status, KDA_DEV_TIMEOUT);
     // bounded: let the loads in flight land before the shared memory is released
-    if (inflight >= 0) tc::bar_wait(bar + 2, (uint32_t)inflight & 1u);
-    if (inflight_v >= 0) tc::bar_wait(bar + 3, (uint32_t)inflight_v & 1u);
+    if (inflight_kg >= 0) tc::bar_wait(bar + 2, (uint32_t)inflight_kg & 1u);
+    if (inflight_q >= 0) tc::bar_wait(bar + 3, (uint32_t)inflight_q & 1u);
+    if (inflight_v >= 0) tc::bar_wait(bar + 4, (uint32_t)inflight_v & 1u);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1499,12 +1516,14 @@ cudaError_t launch_tc_prep(const PrefillArgs& a, uint8_t* records, cudaStream_t 
       !encode_token_map_sw128(&maps.v, a.v, a.T, a.H, C) || !encode_token_map(&maps.g, a.g, true, a.T, a.H, C))
     return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)PS_BYTES);
+  if (e == cudaSuccess)  // two CTAs' shared memory per SM: all of the unified data cache that can be shared
+    e = cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   const int nchunk = (a.max_seqlen + C - 1) / C, sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const long long tasks = (long long)nchunk * a.H * a.N;
   if (tasks > 0x7fffffff) return cudaErrorInvalidValue;
-  const int grid = tasks < sms ? (int)tasks : sms;
+  const int grid = tasks < 2LL * sms ? (int)tasks : 2 * sms;
   cudaError_t le = launch_pdl(tc_prep_kernel, dim3(grid), dim3(PREP_NT), PS_BYTES, s, a, records, maps, nchunk);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
