@@ -105,13 +105,17 @@ constexpr int PREP_PARTS = PREP_NT / D;  // threads per channel in the per-chann
 // (lane = channel j, bf16 pairs of tokens) as the A operand of W^T
 constexpr uint32_t COL_GRAM = 0, COL_W = 64, COL_U = 128, COL_XKHI = 192, COL_XKLO = 224;
 
-// splits 8 floats and stores the hi and lo 16-byte chunks
-__device__ __forceinline__ void split8_store(void* hi_dst, void* lo_dst, const float* v) {
-  uint4 h, l;
+// splits 8 floats into their bf16 hi and lo 16-byte chunks
+__device__ __forceinline__ void split8(const float* v, uint4& h, uint4& l) {
   tc::split_pair(v[0], v[1], h.x, l.x);
   tc::split_pair(v[2], v[3], h.y, l.y);
   tc::split_pair(v[4], v[5], h.z, l.z);
   tc::split_pair(v[6], v[7], h.w, l.w);
+}
+// splits 8 floats and stores the hi and lo 16-byte chunks
+__device__ __forceinline__ void split8_store(void* hi_dst, void* lo_dst, const float* v) {
+  uint4 h, l;
+  split8(v, h, l);
   *reinterpret_cast<uint4*>(hi_dst) = h;
   *reinterpret_cast<uint4*>(lo_dst) = l;
 }
@@ -411,6 +415,7 @@ __global__ void __launch_bounds__(PREP_NT, 2) tc_prep_kernel(const PrefillArgs a
     // the record's Q o gamma and K^ = K o exp(G_C - G) (= Y) of the half on the way
 #pragma unroll 1
     for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll 1
       for (int task = tid; task < C * 8; task += PREP_NT) {
         const int t = task >> 3, c8 = task & 7, cc = 8 * hh + c8;
         float kx[8], qx[8], gt[8], gc[8], e1[8], v[8];
@@ -431,8 +436,12 @@ __global__ void __launch_bounds__(PREP_NT, 2) tc_prep_kernel(const PrefillArgs a
         split8_store(sm + PS_XHI + tc::sw128_chunk(64 + t, c8), sm + PS_XLO + tc::sw128_chunk(64 + t, c8), v);
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = kx[e] * __expf(gc[e] - gt[e]);
-        split8_store(sm + PS_YHI + tc::sw128_chunk(t, c8), sm + PS_YLO + tc::sw128_chunk(t, c8), v);
-        split8_store(rec + REC_KHI + y_off(t, cc), rec + REC_KLO + y_off(t, cc), v);
+        uint4 yh, yl;  // Y is the record's K^ tile as it stands
+        split8(v, yh, yl);
+        *reinterpret_cast<uint4*>(sm + PS_YHI + tc::sw128_chunk(t, c8)) = yh;
+        *reinterpret_cast<uint4*>(sm + PS_YLO + tc::sw128_chunk(t, c8)) = yl;
+        *reinterpret_cast<uint4*>(rec + REC_KHI + y_off(t, cc)) = yh;
+        *reinterpret_cast<uint4*>(rec + REC_KLO + y_off(t, cc)) = yl;
       }
       tc::fence_proxy_async();
       __syncthreads();
@@ -645,6 +654,7 @@ __global__ void __launch_bounds__(PREP_NT, 2) tc_prep_kernel(const PrefillArgs a
             make_uint4(0, 0, 0, 0);
       }
       // T diag(beta) as the B operand of W^T and U~^T (lower triangle only)
+#pragma unroll 1
       for (int st = tid; st < C * 8; st += PREP_NT) {
         const int t = st >> 3, cc = st & 7;
         float v[8];
