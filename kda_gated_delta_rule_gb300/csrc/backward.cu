@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tc_ptx.cuh"
+#include "wy_inverse.cuh"
 
 namespace kda {
 namespace {
@@ -278,28 +279,21 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
     __syncthreads();
   }
 
-  // T = (I + diag(beta) a)^-1 by forward substitution, one column per lane of warps 0-1 (no barriers:
-  // column v only reads its own earlier entries).  Warps 2-7 meanwhile form diag(beta) K+ in sX.
-  if (tid < C) {
-    const int v = tid;
-    for (int u = 0; u < C; ++u) sT[u * LC + v] = u == v ? 1.f : 0.f;
-    for (int t = 1; t < C; ++t) {
-      float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-      int u = 0;
-      for (; u + 3 < t; u += 4) {
-        s0 = fmaf(sA[t * LC + u], sT[u * LC + v], s0);
-        s1 = fmaf(sA[t * LC + u + 1], sT[(u + 1) * LC + v], s1);
-        s2 = fmaf(sA[t * LC + u + 2], sT[(u + 2) * LC + v], s2);
-        s3 = fmaf(sA[t * LC + u + 3], sT[(u + 3) * LC + v], s3);
-      }
-      for (; u < t; ++u) s0 = fmaf(sA[t * LC + u], sT[u * LC + v], s0);
-      if (t > v) sT[t * LC + v] = -sB[t] * ((s0 + s1) + (s2 + s3));
-    }
-  } else {
-    for (int e = tid - C; e < C * D; e += NT - C) {
-      const int s = e / D, j = e % D;
-      sX[s * LD + j] = sB[s] * sK[s * LD + j] * __expf(sG[s * LD + j]);
-    }
+  // the record's a; then A = diag(beta) a in place (the inverse's scratch) and T = (I + A)^-1, blocked by
+  // 16 (T's upper blocks, the inverse's scratch, cleared after); then diag(beta) K+ in sX
+  for (int e = tid; e < C * C; e += NT) w[BW_A + e] = sA[(e / C) * LC + e % C];
+  __syncthreads();
+  for (int e = tid; e < C * C; e += NT) sA[(e / C) * LC + e % C] *= sB[e / C];
+  __syncthreads();
+  unit_lower_inverse64<LC>(sA, sT, tid);
+  __syncthreads();
+  for (int e = tid; e < 6 * 256; e += NT) {  // upper blocks (r, c), r < c: (0,1) (0,2) (1,2) (0,3) (1,3) (2,3)
+    const int blk = e >> 8, r = blk == 0 ? 0 : (blk < 3 ? blk - 1 : blk - 3), cb = blk == 0 ? 1 : (blk < 3 ? 2 : 3);
+    sT[(16 * r + ((e >> 4) & 15)) * LC + 16 * cb + (e & 15)] = 0.f;
+  }
+  for (int e = tid; e < C * D; e += NT) {
+    const int s = e / D, j = e % D;
+    sX[s * LD + j] = sB[s] * sK[s * LD + j] * __expf(sG[s * LD + j]);
   }
   __syncthreads();
 
@@ -315,7 +309,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
     const int t = e / C, s = e % C;
     w[BW_P + e] = sP[t * LC + s];
     w[BW_T + e] = sT[t * LC + s];
-    w[BW_A + e] = sA[t * LC + s];
   }
   if (tid < D) w[BW_GAM + tid] = __expf(sG[(n - 1) * LD + tid]);
   const int ty = tid >> 4, tx = tid & 15;  // rows ty + 16i, columns tx + 16m

@@ -31,6 +31,7 @@
 #include "device.h"
 #include "tc_ptx.cuh"
 #include "tmap.h"
+#include "wy_inverse.cuh"
 
 namespace kda {
 namespace {
@@ -123,18 +124,6 @@ __device__ __forceinline__ void split8_store(void* hi_dst, void* lo_dst, const f
 __device__ __forceinline__ void load8f(const float* p, float* v) {
   const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-
-// a0 / a1 (rows r and r + 8 of a 16 x 16 block product, 4 columns) += m[r or r + 8][u] * b[u][.], u < 16;
-// m points at row r of the left block, b at the 4 columns of the right block (row stride LT for both)
-__device__ __forceinline__ void inv_mac(const float* m, const float* b, float (&a0)[4], float (&a1)[4]) {
-#pragma unroll
-  for (int u = 0; u < 16; ++u) {
-    const float m0 = m[u], m1 = m[8 * LT + u];
-    const float4 b4 = *reinterpret_cast<const float4*>(b + u * LT);
-    a0[0] = fmaf(m0, b4.x, a0[0]); a0[1] = fmaf(m0, b4.y, a0[1]); a0[2] = fmaf(m0, b4.z, a0[2]); a0[3] = fmaf(m0, b4.w, a0[3]);
-    a1[0] = fmaf(m1, b4.x, a1[0]); a1[1] = fmaf(m1, b4.y, a1[1]); a1[2] = fmaf(m1, b4.z, a1[2]); a1[3] = fmaf(m1, b4.w, a1[3]);
-  }
 }
 
 // offset of the 16-byte chunk cc (channels 8cc..8cc+7) of row r in a record tile of two 64-channel blocks
@@ -560,89 +549,7 @@ __global__ void __launch_bounds__(PREP_NT, 2) tc_prep_kernel(const PrefillArgs a
   }
 
   if (ok) {
-    // T = (I + A)^-1, blocked by 16.  Diagonal blocks by forward substitution (threads 0..63, one column each).
-    if (tid < 64) {
-      const int b = tid >> 4, cc = tid & 15;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int u = 0; u < r; ++u) acc = fmaf(sA[(16 * b + r) * LT + 16 * b + u], x[u], acc);
-        x[r] = r == cc ? 1.f : (r < cc ? 0.f : -acc);
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) sT[(16 * b + r) * LT + 16 * b + cc] = x[r];
-    }
-    __syncthreads();
-    // Off-diagonal blocks: block row i of (I + A) T = I gives T_ij = -sum_{k=j}^{i-1} M_ik T_kj with
-    // M_ik = T_ii A_ik.  Every 16 x 16 block product is one warp's: lane (rp, cg) owns rows rp and rp + 8,
-    // columns 4 cg .. 4 cg + 3, and per step two conflict-free scalar loads (a warp's eight rows sit in eight
-    // bank groups) and one 16-byte load feed eight FMAs.  Rounds, each one product deep:
-    //   1. M_ik for all six pairs (kept in the unused upper block (k, i) of T);
-    //   2. T_10, T_21, T_32 (one term each);
-    //   3. the six products M_20 T_00, M_21 T_10, M_31 T_11, M_32 T_21, M_30 T_00, M_31 T_10 (into A's
-    //      dead storage);
-    //   4. T_20 and T_31 as sums of two of them, and T_30 = -(M_30 T_00 + M_31 T_10) + M_32 (M_20 T_00 + M_21 T_10).
-    // T_ii is stored with its zero upper triangle, so the sums run over all 16.
-    const int rp = (tid >> 2) & 7, cg = tid & 3, wv = tid >> 5;
-    auto mac = [&](const float* mb, const float* bb, float (&a0)[4], float (&a1)[4]) {
-      inv_mac(mb + rp * LT, bb + 4 * cg, a0, a1);
-    };
-    auto tblk = [&](int r, int c) { return sT + 16 * r * LT + 16 * c; };  // block (r, c) of T
-    constexpr int PLD = 20;                                               // row stride of the partial products
-    auto pblk = [&](int s) { return sA + s * 16 * PLD; };
-    auto put = [&](float* dst, int ld, const float (&a0)[4], const float (&a1)[4], float sg) {
-      *reinterpret_cast<float4*>(dst + rp * ld + 4 * cg) = make_float4(sg * a0[0], sg * a0[1], sg * a0[2], sg * a0[3]);
-      *reinterpret_cast<float4*>(dst + (rp + 8) * ld + 4 * cg) = make_float4(sg * a1[0], sg * a1[1], sg * a1[2], sg * a1[3]);
-    };
-    if (wv < 6) {  // round 1: M_ik = T_ii A_ik; pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-      const int bi = wv == 0 ? 1 : (wv < 3 ? 2 : 3);
-      const int bk = wv == 0 ? 0 : (wv < 3 ? wv - 1 : wv - 3);
-      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      mac(tblk(bi, bi), sA + 16 * bi * LT + 16 * bk, a0, a1);
-      put(tblk(bk, bi), LT, a0, a1, 1.f);
-    }
-    __syncthreads();
-    if (wv < 3) {  // round 2: T_{w+1,w} = -M_{w+1,w} T_ww
-      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      mac(tblk(wv, wv + 1), tblk(wv, wv), a0, a1);
-      put(tblk(wv + 1, wv), LT, a0, a1, -1.f);
-    }
-    __syncthreads();
-    if (wv < 6) {  // round 3: (i, j, k) = (2,0,0) (2,0,1) (3,1,1) (3,1,2) (3,0,0) (3,0,1): M_ik T_kj into slot wv
-      const int bi = wv < 2 ? 2 : 3, bj = wv < 2 ? 0 : (wv < 4 ? 1 : 0);
-      const int bk = wv == 0 ? 0 : (wv == 1 ? 1 : (wv == 2 ? 1 : (wv == 3 ? 2 : (wv == 4 ? 0 : 1))));
-      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      mac(tblk(bk, bi), tblk(bk, bj), a0, a1);
-      put(pblk(wv), PLD, a0, a1, 1.f);
-    }
-    __syncthreads();
-    if (wv < 3) {  // round 4
-      float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-      if (wv == 2) {  // M_32 (M_20 T_00 + M_21 T_10): the second operand summed on the fly
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const float m0 = tblk(2, 3)[rp * LT + u], m1 = tblk(2, 3)[(rp + 8) * LT + u];
-          const float4 p0 = *reinterpret_cast<const float4*>(pblk(0) + u * PLD + 4 * cg);
-          const float4 p1 = *reinterpret_cast<const float4*>(pblk(1) + u * PLD + 4 * cg);
-          const float4 b4 = make_float4(p0.x + p1.x, p0.y + p1.y, p0.z + p1.z, p0.w + p1.w);
-          a0[0] = fmaf(m0, b4.x, a0[0]); a0[1] = fmaf(m0, b4.y, a0[1]); a0[2] = fmaf(m0, b4.z, a0[2]); a0[3] = fmaf(m0, b4.w, a0[3]);
-          a1[0] = fmaf(m1, b4.x, a1[0]); a1[1] = fmaf(m1, b4.y, a1[1]); a1[2] = fmaf(m1, b4.z, a1[2]); a1[3] = fmaf(m1, b4.w, a1[3]);
-        }
-      }
-      // wv 0: T_20 = -(slot 0 + slot 1); wv 1: T_31 = -(slot 2 + slot 3); wv 2: T_30 = acc - (slot 4 + slot 5)
-      const int sa = 2 * wv, dr = wv == 1 ? 3 : (wv == 0 ? 2 : 3), dc = wv == 1 ? 1 : 0;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        const int row = rp + 8 * h2;
-        const float4 x0 = *reinterpret_cast<const float4*>(pblk(sa) + row * PLD + 4 * cg);
-        const float4 x1 = *reinterpret_cast<const float4*>(pblk(sa + 1) + row * PLD + 4 * cg);
-        const float* ac = h2 ? a1 : a0;
-        *reinterpret_cast<float4*>(tblk(dr, dc) + row * LT + 4 * cg) =
-            make_float4(ac[0] - (x0.x + x1.x), ac[1] - (x0.y + x1.y), ac[2] - (x0.z + x1.z), ac[3] - (x0.w + x1.w));
-      }
-    }
+    unit_lower_inverse64<LT>(sA, sT, tid);
     // this task's v (requested once its operands were built) has landed: its rows past the valid tokens
     // are zeroed below, and T diag(beta) then takes the place of the dead A
     ok = __syncthreads_and(tc::bar_wait(bar + 4, (uint32_t)k & 1u));
