@@ -208,18 +208,82 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
+  float gspan = 0.f;  // the channel's decay span over the chunk (including its start, G = 0)
   if (tid < D) {  // in-chunk cumulative sum, one thread per channel
-    float acc = 0.f;
+    float acc = 0.f, gmin = 0.f, gmax = 0.f;
     for (int t = 0; t < C; ++t) {
       acc += sG[t * LD + tid];
       sG[t * LD + tid] = acc;
+      gmin = fminf(gmin, acc);
+      gmax = fmaxf(gmax, acc);
     }
+    gspan = gmax - gmin;
   }
-  __syncthreads();
+  const bool chunk_wide = __syncthreads_or(gspan > SPAN_MAX);
   if (tid == 0) add_work(a.status, n);
 
-  // a and P, one 16-column block of s at a time
-  for (int b0 = 0; b0 < n; b0 += 16) {
+  if (!chunk_wide) {
+    // Common case: one reference token, the chunk's last, for every pair: a = X Y^T and P = Xq Y^T with
+    // X = k o e^(G - G_C), Xq = q o e^(G - G_C) and Y = k o e^(G_C - G) (the record's K^), every factor within
+    // e^SPAN_MAX.  The records' G, K^ and Q+ are written on the way; Y takes q's place.
+    for (int e = tid; e < C * D / 4; e += NT) {
+      const int t = e >> 5, j = (e & 31) * 4;
+      const float4 k4 = *reinterpret_cast<const float4*>(sK + t * LD + j);
+      const float4 q4 = *reinterpret_cast<const float4*>(sQ + t * LD + j);
+      const float4 g4 = *reinterpret_cast<const float4*>(sG + t * LD + j);
+      const float4 c4 = *reinterpret_cast<const float4*>(sG + (C - 1) * LD + j);
+      const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+      const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, gc[4] = {c4.x, c4.y, c4.z, c4.w};
+      float x[4], xq[4], y[4], qp[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float e1 = __expf(gg[u] - gc[u]);
+        x[u] = kk[u] * e1;
+        xq[u] = qq[u] * e1;
+        y[u] = kk[u] * __expf(gc[u] - gg[u]);
+        qp[u] = qq[u] * __expf(gg[u]);
+      }
+      *reinterpret_cast<float4*>(sX + t * LD + j) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(sY + t * LD + j) = make_float4(xq[0], xq[1], xq[2], xq[3]);
+      *reinterpret_cast<float4*>(sQ + t * LD + j) = make_float4(y[0], y[1], y[2], y[3]);
+      *reinterpret_cast<float4*>(w + BW_G + t * D + j) = g4;
+      *reinterpret_cast<float4*>(w + BW_KH + t * D + j) = make_float4(y[0], y[1], y[2], y[3]);
+      *reinterpret_cast<float4*>(w + BW_QP + t * D + j) = make_float4(qp[0], qp[1], qp[2], qp[3]);
+    }
+    __syncthreads();
+    // thread (tr, tc): rows t = 4 tr + r, columns s = tc + 16 r' (a warp's Y rows in eight bank groups)
+    const int tr = tid >> 4, tc = tid & 15;
+    float aa[4][4] = {}, pp[4][4] = {};
+#pragma unroll 2
+    for (int j = 0; j < D; j += 4) {
+      float4 x[4], xq[4], y[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        x[r] = *reinterpret_cast<const float4*>(sX + (4 * tr + r) * LD + j);
+        xq[r] = *reinterpret_cast<const float4*>(sY + (4 * tr + r) * LD + j);
+        y[r] = *reinterpret_cast<const float4*>(sQ + (tc + 16 * r) * LD + j);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          aa[r][q] = fmaf(x[r].w, y[q].w, fmaf(x[r].z, y[q].z, fmaf(x[r].y, y[q].y, fmaf(x[r].x, y[q].x, aa[r][q]))));
+          pp[r][q] = fmaf(xq[r].w, y[q].w, fmaf(xq[r].z, y[q].z, fmaf(xq[r].y, y[q].y, fmaf(xq[r].x, y[q].x, pp[r][q]))));
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int t = 4 * tr + r, s = tc + 16 * q;
+        sA[t * LC + s] = s < t ? aa[r][q] : 0.f;
+        sP[t * LC + s] = s <= t ? pp[r][q] : 0.f;
+      }
+    __syncthreads();
+  }
+
+  // a and P when the chunk's span is wider: one 16-column block of s at a time, each at its own reference
+  for (int b0 = 0; chunk_wide && b0 < n; b0 += 16) {
     const int r = min(b0 + 15, n - 1);
     bool wide = false;
     if (tid < D) {
@@ -297,8 +361,9 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
   }
   __syncthreads();
 
-  // records: G, a, P, T, e^G_C, K^, Q+ (elementwise), then W = T diag(beta) K+ and U~ = T diag(beta) V
-  for (int e = tid; e < C * D; e += NT) {
+  // records: G, a, P, T, e^G_C, K^, Q+ (elementwise; G, K^ and Q+ already in the common case), then
+  // W = T diag(beta) K+ and U~ = T diag(beta) V
+  for (int e = tid; chunk_wide && e < C * D; e += NT) {
     const int t = e / D, j = e % D;
     const float G = sG[t * LD + j], GC = sG[(n - 1) * LD + j];
     w[BW_G + e] = G;
