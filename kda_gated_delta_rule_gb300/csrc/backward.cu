@@ -1000,7 +1000,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
 // 6. assembly of one (chunk, head, 64 channels): pair-decay terms, dq, dk, dg, dbeta
 // ---------------------------------------------------------------------------------------------------
 constexpr int NTA = 512;  // threads of the assembly kernel
-constexpr size_t ASM_SMEM = (7 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
+constexpr size_t ASM_SMEM = (8 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
@@ -1022,7 +1022,8 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   float* sDKC = sDA + C * LC;   // the sums over t >= s of dk_s (each row written by its own block)
   float* sKm = sDKC + C * LC;   // k o e^(G_r - G_s) of the current block [16][LC]
   float* sEm = sKm + 16 * LC;   // e^(G_r - G_s) [16][LC]
-  float* sB = sEm + 16 * LC;    // beta [64]
+  float* sYc = sEm + 16 * LC;   // common case: k o e^(G_C - G) [64][LC]
+  float* sB = sYc + C * LC;     // beta [64]
   float* sDiag = sB + C;        // dP_tt [64] (the diagonal is kept out of the pair sums: in dG its two
                                 // contributions, through q_t and through k_t, cancel exactly)
   const int64_t rs = (int64_t)a.H * D;
@@ -1041,10 +1042,87 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
     sDP[tid * LC + tid] = 0.f;
   }
   __syncthreads();
-  const int ty = tid >> 4, tx = tid & 15;    // own elements: rows ty + 32 ii, channels tx + 16 m
+  const int ty = tid >> 4, tx = tid & 15;    // own elements: rows ty + 32 ii, channels (own_col)
   const int orow = tid >> 5, ocol = tid & 31;  // in block b0: row b0 + orow, channels ocol + 32 mm
-  float dqp[2][4] = {}, dkr[2][4] = {};
-  for (int bi = 0; bi * 16 < n; ++bi) {
+  float dqp[2][4] = {}, dkr[2][4] = {}, dkc[2][4] = {};
+  bool chunk_wide = false;  // some channel's decay span over the chunk (with its start, G = 0) above SPAN_MAX
+  if (tid < HC) {
+    float gmin = 0.f, gmax = 0.f;
+    for (int t = 0; t < C; ++t) gmin = fminf(gmin, sG[t * LC + tid]), gmax = fmaxf(gmax, sG[t * LC + tid]);
+    chunk_wide = gmax - gmin > SPAN_MAX;
+  }
+  chunk_wide = __syncthreads_or(chunk_wide);
+  // own channels: 4 tx + m in the common case (16-byte loads), tx + 16 m when the blocks take their own references
+  auto own_col = [&](int m) { return chunk_wide ? tx + 16 * m : 4 * tx + m; };
+  if (!chunk_wide) {
+    // Common case: every pair decay through the chunk's last token, e^(G_t - G_s) = e^(G_t - G_C) e^(G_C - G_s):
+    //   dq~_t = e^(G_t - G_C) (dP Y)_t,  dk_r,t = beta_t e^(G_t - G_C) (dA Y)_t,
+    //   dk_c,s = e^(G_C - G_s) (dP^T Xq + (diag(beta) dA)^T X)_s
+    // with X = k o e^(G - G_C), Xq = q o e^(G - G_C), Y = k o e^(G_C - G) (dP without its diagonal, dA strictly
+    // lower: the sums run over s < t and t > s).
+    float* sXc = sEp;    // X
+    float* sXq = sDKC;   // Xq
+    for (int e = tid; e < C * HC / 4; e += NTA) {
+      const int t = e >> 4, j = (e & 15) * 4;
+      const float4 k4 = *reinterpret_cast<const float4*>(sK + t * LC + j);
+      const float4 q4 = *reinterpret_cast<const float4*>(sQ + t * LC + j);
+      const float4 g4 = *reinterpret_cast<const float4*>(sG + t * LC + j);
+      const float4 c4 = *reinterpret_cast<const float4*>(sG + (C - 1) * LC + j);
+      const float kk[4] = {k4.x, k4.y, k4.z, k4.w}, qq[4] = {q4.x, q4.y, q4.z, q4.w};
+      const float gg[4] = {g4.x, g4.y, g4.z, g4.w}, gc[4] = {c4.x, c4.y, c4.z, c4.w};
+      float x[4], xq[4], y[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float e1 = __expf(gg[u] - gc[u]);
+        x[u] = kk[u] * e1;
+        xq[u] = qq[u] * e1;
+        y[u] = kk[u] * __expf(gc[u] - gg[u]);
+      }
+      *reinterpret_cast<float4*>(sXc + t * LC + j) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(sXq + t * LC + j) = make_float4(xq[0], xq[1], xq[2], xq[3]);
+      *reinterpret_cast<float4*>(sYc + t * LC + j) = make_float4(y[0], y[1], y[2], y[3]);
+    }
+    __syncthreads();
+    const int jc = 4 * tx, r0 = ty, r1 = ty + 32;
+    for (int s = 0; s < r1; ++s) {  // row sums (entries at s >= t are zero)
+      const float4 y4 = *reinterpret_cast<const float4*>(sYc + s * LC + jc);
+      const float y[4] = {y4.x, y4.y, y4.z, y4.w};
+      const float p0 = sDP[r0 * LC + s], p1 = sDP[r1 * LC + s], q0 = sDA[r0 * LC + s], q1 = sDA[r1 * LC + s];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dqp[0][u] = fmaf(p0, y[u], dqp[0][u]);
+        dqp[1][u] = fmaf(p1, y[u], dqp[1][u]);
+        dkr[0][u] = fmaf(q0, y[u], dkr[0][u]);
+        dkr[1][u] = fmaf(q1, y[u], dkr[1][u]);
+      }
+    }
+    for (int t = r0 + 1; t < C; ++t) {  // column sums (entries at t <= s are zero)
+      const float4 x4 = *reinterpret_cast<const float4*>(sXc + t * LC + jc);
+      const float4 z4 = *reinterpret_cast<const float4*>(sXq + t * LC + jc);
+      const float x[4] = {x4.x, x4.y, x4.z, x4.w}, xq[4] = {z4.x, z4.y, z4.z, z4.w};
+      const float bt = sB[t];
+      const float p0 = sDP[t * LC + r0], p1 = sDP[t * LC + r1], q0 = bt * sDA[t * LC + r0], q1 = bt * sDA[t * LC + r1];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dkc[0][u] = fmaf(p0, xq[u], fmaf(q0, x[u], dkc[0][u]));
+        dkc[1][u] = fmaf(p1, xq[u], fmaf(q1, x[u], dkc[1][u]));
+      }
+    }
+#pragma unroll
+    for (int ii = 0; ii < 2; ++ii) {
+      const int t = ty + 32 * ii;
+      const float bt = sB[t];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float gt = sG[t * LC + jc + u], gcu = sG[(C - 1) * LC + jc + u];
+        const float ep = __expf(gt - gcu), em = __expf(gcu - gt);
+        dqp[ii][u] *= ep;
+        dkr[ii][u] *= bt * ep;
+        dkc[ii][u] *= em;
+      }
+    }
+  }
+  for (int bi = 0; chunk_wide && bi * 16 < n; ++bi) {
     const int b0 = bi * 16, r = min(b0 + 15, n - 1);
     bool wide = false;
     if (tid < HC) {
@@ -1147,10 +1225,10 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
     const int t = ty + 32 * ii;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-      const int jl = tx + 16 * m, j = j0 + jl;
+      const int jl = own_col(m), j = j0 + jl;
       float dG = 0.f, xc = 0.f;
       if (t < n) {
-        const float dkc = sDKC[t * LC + jl];
+        const float dkcv = chunk_wide ? sDKC[t * LC + jl] : dkc[ii][m];
         const float G = sG[t * LC + jl], GC = sG[(n - 1) * LC + jl];
         const float e0 = __expf(G), ec = __expf(GC - G);
         const float kk = sK[t * LC + jl], qq = sQ[t * LC + jl];
@@ -1158,9 +1236,9 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
         const int64_t o = ((int64_t)(t0 + t) * a.H + h) * D + j;
         const float dpt = sDiag[t];
         a.dq[o] = fmaf(dpt, kk, fmaf(gq, e0, dqp[ii][m]));
-        a.dk[o] = fmaf(dpt, qq, fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkc)));
+        a.dk[o] = fmaf(dpt, qq, fmaf(gk, e0, fmaf(gh, ec, dkr[ii][m] + dkcv)));
         xc = gh * kk * ec;
-        dG = (gq * qq + gk * kk) * e0 + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkc);
+        dG = (gq * qq + gk * kk) * e0 + qq * dqp[ii][m] + kk * (dkr[ii][m] - dkcv);
       }
       sDG[t * LC + jl] = dG;
       sXC[t * LC + jl] = xc;
