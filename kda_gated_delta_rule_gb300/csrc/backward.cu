@@ -896,18 +896,31 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
   for (int e = tid; e < C * D; e += NT) sKp[(e / D) * LD + e % D] *= __expf(w[BW_G + e]);
   __syncthreads();
   const int ty = tid >> 4, tx = tid & 15;
-  {  // dT_ts = beta_s (dW_t . K+_s + dU_t . V_s)
+  {  // dT_ts = beta_s (dW_t . K+_s + dU_t . V_s), 16-byte loads along j
     float acc[4][4] = {};
-    for (int j = 0; j < D; ++j) {
-      float x[4], y[4], p[4], q[4];
+#pragma unroll 2
+    for (int j = 0; j < D; j += 4) {
+      float4 x[4], y[4], p[4], q[4];
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sDW[(ty + 16 * ii) * LD + j], y[ii] = sDU[(ty + 16 * ii) * LD + j];
+      for (int ii = 0; ii < 4; ++ii) {
+        x[ii] = *reinterpret_cast<const float4*>(sDW + (ty + 16 * ii) * LD + j);
+        y[ii] = *reinterpret_cast<const float4*>(sDU + (ty + 16 * ii) * LD + j);
+      }
 #pragma unroll
-      for (int m = 0; m < 4; ++m) p[m] = sKp[(tx + 16 * m) * LD + j], q[m] = sV[(tx + 16 * m) * LD + j];
+      for (int m = 0; m < 4; ++m) {
+        p[m] = *reinterpret_cast<const float4*>(sKp + (tx + 16 * m) * LD + j);
+        q[m] = *reinterpret_cast<const float4*>(sV + (tx + 16 * m) * LD + j);
+      }
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], p[m], fmaf(y[ii], q[m], acc[ii][m]));
+        for (int m = 0; m < 4; ++m) {
+          float v = acc[ii][m];
+          v = fmaf(x[ii].x, p[m].x, fmaf(y[ii].x, q[m].x, v));
+          v = fmaf(x[ii].y, p[m].y, fmaf(y[ii].y, q[m].y, v));
+          v = fmaf(x[ii].z, p[m].z, fmaf(y[ii].z, q[m].z, v));
+          acc[ii][m] = fmaf(x[ii].w, p[m].w, fmaf(y[ii].w, q[m].w, v));
+        }
     }
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii)
@@ -917,20 +930,31 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
         sM[(ty + 16 * ii) * LC + s] = sB[s] * acc[ii][m];
       }
   }
-  {  // dB_K = T^T dW, dB_V = T^T dU (rows s, columns j); dK+ = beta dB_K, dv = beta dB_V, dbeta part
+  {  // dB_K = T^T dW, dB_V = T^T dU (rows s, columns j = 4 tx + 64 (m / 4) + m % 4, T lower: t >= s);
+     // dK+ = beta dB_K, dv = beta dB_V, dbeta part
     float bk[4][8] = {}, bv[4][8] = {};
-    for (int t = 0; t < C; ++t) {
-      float x[4], y[8], z[8];
+    for (int t = ty; t < C; ++t) {
+      float x[4];
+      float4 y[2], z[2];
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii) x[ii] = sT[t * LC + ty + 16 * ii];
 #pragma unroll
-      for (int m = 0; m < 8; ++m) y[m] = sDW[t * LD + tx + 16 * m], z[m] = sDU[t * LD + tx + 16 * m];
+      for (int mm = 0; mm < 2; ++mm) {
+        y[mm] = *reinterpret_cast<const float4*>(sDW + t * LD + 4 * tx + 64 * mm);
+        z[mm] = *reinterpret_cast<const float4*>(sDU + t * LD + 4 * tx + 64 * mm);
+      }
 #pragma unroll
       for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
-        for (int m = 0; m < 8; ++m) {
-          bk[ii][m] = fmaf(x[ii], y[m], bk[ii][m]);
-          bv[ii][m] = fmaf(x[ii], z[m], bv[ii][m]);
+        for (int mm = 0; mm < 2; ++mm) {
+          bk[ii][4 * mm + 0] = fmaf(x[ii], y[mm].x, bk[ii][4 * mm + 0]);
+          bk[ii][4 * mm + 1] = fmaf(x[ii], y[mm].y, bk[ii][4 * mm + 1]);
+          bk[ii][4 * mm + 2] = fmaf(x[ii], y[mm].z, bk[ii][4 * mm + 2]);
+          bk[ii][4 * mm + 3] = fmaf(x[ii], y[mm].w, bk[ii][4 * mm + 3]);
+          bv[ii][4 * mm + 0] = fmaf(x[ii], z[mm].x, bv[ii][4 * mm + 0]);
+          bv[ii][4 * mm + 1] = fmaf(x[ii], z[mm].y, bv[ii][4 * mm + 1]);
+          bv[ii][4 * mm + 2] = fmaf(x[ii], z[mm].z, bv[ii][4 * mm + 2]);
+          bv[ii][4 * mm + 3] = fmaf(x[ii], z[mm].w, bv[ii][4 * mm + 3]);
         }
     }
 #pragma unroll
@@ -940,7 +964,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
       float part = 0.f;
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
-        const int j = tx + 16 * m;
+        const int j = 4 * tx + 64 * (m >> 2) + (m & 3);
         part = fmaf(bk[ii][m], sKp[s * LD + j], part);
         part = fmaf(bv[ii][m], sV[s * LD + j], part);
         w[BW_DKP + s * D + j] = b * bk[ii][m];

@@ -878,12 +878,6 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         const int j0 = 64 * wg;
         float s[64];
         tc::tmem_ld64(trow + COL_S + j0, s);
-        if (MODE == MODE_STATES) {  // the chunk's entry state, rows j0 .. j0 + 63 of column c
-          float* dst = a.bw_ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * a.bw_rec_floats + a.bw_off_h +
-                       (size_t)j0 * D + c;
-#pragma unroll
-          for (int e = 0; e < 64; ++e) dst[(size_t)e * D] = s[e];
-        }
 #pragma unroll
         for (int jb = 0; jb < 2; ++jb) {
           uint32_t hi[16], lo[16];
@@ -894,6 +888,12 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         }
         tc::tmem_wait_st();
         hand_over(rdy_e1);
+        if (MODE == MODE_STATES) {  // the chunk's entry state, rows j0 .. j0 + 63 of column c (while (W S)^T runs)
+          float* dst = a.bw_ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * a.bw_rec_floats + a.bw_off_h +
+                       (size_t)j0 * D + c;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) dst[(size_t)e * D] = s[e];
+        }
         const float* gm = sgam + 128 * st + j0;
 #pragma unroll
         for (int e = 0; e < 64; ++e) s[e] *= gm[e];
@@ -924,15 +924,15 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
         for (int e = 0; e < 16; ++e) tc::split_pair(ut[2 * e] - w[2 * e], ut[2 * e + 1] - w[2 * e + 1], hi[e], lo[e]);
         tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
         tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
-        if (MODE == MODE_STATES) {  // U = U~ - W S of this thread's 32 tokens, column c
+        tc::tmem_wait_st();
+        hand_over(rdy_e2);
+        if (MODE == MODE_STATES) {  // U = U~ - W S of this thread's 32 tokens, column c (while the update runs)
           float* du = a.bw_ws + ((size_t)(chunk_t0(cc) / C + i) * a.H + h) * a.bw_rec_floats + a.bw_off_u +
                       (size_t)(32 * wg) * D + c;
 #pragma unroll
           for (int e = 0; e < 32; ++e) du[(size_t)e * D] = ut[e] - w[e];
         }
       }
-      tc::tmem_wait_st();
-      hand_over(rdy_e2);
     }
     if (ok && nch > 0) {  // drain: the last chunk's state update and outputs
       const int last = nch - 1;
@@ -1264,11 +1264,6 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_rev_kernel(const PrefillArgs a
         const int j0 = 64 * wg;
         float r[64];
         tc::tmem_ld64(trow + COL_S + j0, r);
-        if (RMODE == REV_PASS) {
-          float* dst = a.bw_ws + rec_index(k) * a.bw_rec_floats + a.bw_off_ds + (size_t)j0 * D + c;
-#pragma unroll
-          for (int e = 0; e < 64; ++e) dst[(size_t)e * D] = r[e];
-        }
 #pragma unroll
         for (int jb = 0; jb < 2; ++jb) {
           uint32_t hi[16], lo[16];
@@ -1279,6 +1274,11 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_rev_kernel(const PrefillArgs a
         }
         tc::tmem_wait_st();
         hand_over(rdy_e1);
+        if (RMODE == REV_PASS) {  // while (K^ R)^T runs
+          float* dst = a.bw_ws + rec_index(k) * a.bw_rec_floats + a.bw_off_ds + (size_t)j0 * D + c;
+#pragma unroll
+          for (int e = 0; e < 64; ++e) dst[(size_t)e * D] = r[e];
+        }
         const float* gm = sgam + 128 * st + j0;
 #pragma unroll
         for (int e = 0; e < 64; ++e) r[e] *= gm[e];
@@ -1303,14 +1303,14 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_rev_kernel(const PrefillArgs a
         tc::tmem_st16(trow + COL_UTHI + 16 * wg, hi);
         tc::tmem_st16(trow + COL_UTLO + 16 * wg, lo);
         if (with_do && k + 1 < nch) tc::tmem_st16(trow + COL_DO + 32 * ((k + 1) & 1) + 16 * wg, dn);
-        if (RMODE == REV_PASS) {
+        tc::tmem_wait_st();
+        hand_over(rdy_e2);
+        if (RMODE == REV_PASS) {  // while the update runs
           float* du = a.bw_ws + rec_index(k) * a.bw_rec_floats + a.bw_off_du + (size_t)(32 * wg) * D + c;
 #pragma unroll
           for (int e = 0; e < 32; ++e) du[(size_t)e * D] = u[e];
         }
       }
-      tc::tmem_wait_st();
-      hand_over(rdy_e2);
     }
     if (ok && nch > 0) {
       ok = math_all(tc::bar_wait(bar_st, (uint32_t)(nch - 1) & 1u));
