@@ -412,7 +412,7 @@ size_t kda_backward_args_bytes(void);
 
 /* Workspace of kda_prefill_backward, with n = (ceil(T/64) + N) * H chunk records: n * 574720 bytes of fp32
  * intermediates, then the tensor-core passes' scratch: n * 148480 bytes of operand records and
- * N * P * H * 196608 bytes of segment maps and entry states (P = max(1, 76 / H) segments per sequence), then
+ * N * P * H * 196608 bytes of segment maps and entry states (P = max(1, 152 / H) segments per sequence), then
  * N * H int32 flags; the first two parts are rounded up to 1024 bytes, the last to 256. */
 size_t kda_backward_workspace_size(const kda_backward_args* a);
 

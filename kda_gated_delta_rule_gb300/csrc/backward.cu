@@ -1307,9 +1307,10 @@ struct FwdLayout {
   int P;
   size_t rec_off, frag_off, entry_off, steep_off, total;
 };
-// segments per (sequence, head) of the tensor-core passes: the fragment phase runs 2 H P CTAs, one per SM of a
-// 152-SM GPU; a constant, so that the workspace size depends on the problem alone
-int fwd_segments_target(int H) { return H >= 76 ? 1 : 76 / H; }
+// segments per (sequence, head) of the tensor-core passes: the per-segment passes run H P CTAs, one per SM of
+// a 152-SM GPU (the fragment phases two waves); a constant, so that the workspace size depends on the
+// problem alone
+int fwd_segments_target(int H) { return H >= 152 ? 1 : 152 / H; }
 FwdLayout fwd_layout(int64_t T, int N, int H) {
   FwdLayout L{};
   L.P = fwd_segments_target(H);

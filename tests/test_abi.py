@@ -47,12 +47,12 @@ def test_status_strings_and_sizes(lib):
 def test_stated_size_formulas(lib):
     """The sizes the header states in closed form: the backward's workspace is n = (ceil(T/64) + N) x H
     records of 574720 bytes, n operand records of 148480 bytes (each part rounded up to 1024 bytes), N x P x H
-    x 196608 bytes of segment maps and entry states with P = max(1, 76 // H), and N x H int32 flags (rounded
+    x 196608 bytes of segment maps and entry states with P = max(1, 152 // H), and N x H int32 flags (rounded
     up to 256 bytes); a CF-BI row cache is 16 rows x 420 fp32 per head at d = 128 and 0 elsewhere."""
     up = lambda x, m: -(-x // m) * m
     for T, N, H in ((8192, 1, 12), (300, 3, 2), (64, 1, 1), (65, 2, 4), (1000, 1, 100)):
         n = (-(-T // 64) + N) * H
-        P = max(1, 76 // H)
+        P = max(1, 152 // H)
         want = up(n * 574720, 1024) + up(n * 148480, 1024) + N * P * H * 196608 + up(4 * N * H, 256)
         assert kda.kda_backward_workspace_size(T, N, H) == want
     assert kda.kda_cfbi_cache_bytes_per_head(128, 128) == kda.CFBI_CHUNK * kda.CFBI_ROW_FLOATS * 4 == 26880
