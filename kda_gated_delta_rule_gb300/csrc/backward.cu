@@ -1013,7 +1013,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
 // 6. assembly of one (chunk, head, 64 channels): pair-decay terms, dq, dk, dg, dbeta
 // ---------------------------------------------------------------------------------------------------
 constexpr int NTA = 512;  // threads of the assembly kernel
-constexpr size_t ASM_SMEM = (8 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
+constexpr size_t ASM_SMEM = (11 * C * LC + 2 * 16 * LC + 2 * C) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
@@ -1036,7 +1036,10 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   float* sKm = sDKC + C * LC;   // k o e^(G_r - G_s) of the current block [16][LC]
   float* sEm = sKm + 16 * LC;   // e^(G_r - G_s) [16][LC]
   float* sYc = sEm + 16 * LC;   // common case: k o e^(G_C - G) [64][LC]
-  float* sB = sYc + C * LC;     // beta [64]
+  float* sGQ = sYc + C * LC;    // the records' dQ+, dK+, dK^ of this CTA's 64 channels [64][LC] each
+  float* sGK = sGQ + C * LC;
+  float* sGH = sGK + C * LC;
+  float* sB = sGH + C * LC;     // beta [64]
   float* sDiag = sB + C;        // dP_tt [64] (the diagonal is kept out of the pair sums: in dG its two
                                 // contributions, through q_t and through k_t, cancel exactly)
   const int64_t rs = (int64_t)a.H * D;
@@ -1048,20 +1051,36 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   load_rows<NTA>(sDA, LC, w + BW_DA, C, C, C, 0, C);
   if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
   cp_async_commit();
-  cp_async_wait<0>();
+  load_rows<NTA>(sGQ, LC, w + BW_DQP, D, C, C, j0, HC);  // used at the end: left in flight until then
+  load_rows<NTA>(sGK, LC, w + BW_DKP, D, C, C, j0, HC);
+  load_rows<NTA>(sGH, LC, w + BW_DKH, D, C, C, j0, HC);
+  cp_async_commit();
+  cp_async_wait<1>();
   __syncthreads();
   if (tid < C) {
     sDiag[tid] = sDP[tid * LC + tid];
     sDP[tid * LC + tid] = 0.f;
   }
+  {  // each channel's decay span over the chunk (with its start, G = 0): eight tokens per thread, then per channel
+    const int jj = tid & (HC - 1), part = tid / HC;
+    float gmin = 0.f, gmax = 0.f;
+#pragma unroll
+    for (int u = 0; u < C / 8; ++u) {
+      const float g = sG[(8 * part + u) * LC + jj];
+      gmin = fminf(gmin, g), gmax = fmaxf(gmax, g);
+    }
+    sKm[part * HC + jj] = gmin;
+    sEm[part * HC + jj] = gmax;
+  }
   __syncthreads();
   const int ty = tid >> 4, tx = tid & 15;    // own elements: rows ty + 32 ii, channels (own_col)
   const int orow = tid >> 5, ocol = tid & 31;  // in block b0: row b0 + orow, channels ocol + 32 mm
   float dqp[2][4] = {}, dkr[2][4] = {}, dkc[2][4] = {};
-  bool chunk_wide = false;  // some channel's decay span over the chunk (with its start, G = 0) above SPAN_MAX
+  bool chunk_wide = false;  // some channel's decay span over the chunk above SPAN_MAX
   if (tid < HC) {
     float gmin = 0.f, gmax = 0.f;
-    for (int t = 0; t < C; ++t) gmin = fminf(gmin, sG[t * LC + tid]), gmax = fmaxf(gmax, sG[t * LC + tid]);
+#pragma unroll
+    for (int part = 0; part < NTA / HC; ++part) gmin = fminf(gmin, sKm[part * HC + tid]), gmax = fmaxf(gmax, sEm[part * HC + tid]);
     chunk_wide = gmax - gmin > SPAN_MAX;
   }
   chunk_wide = __syncthreads_or(chunk_wide);
@@ -1097,6 +1116,7 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
     }
     __syncthreads();
     const int jc = 4 * tx, r0 = ty, r1 = ty + 32;
+#pragma unroll 4
     for (int s = 0; s < r1; ++s) {  // row sums (entries at s >= t are zero)
       const float4 y4 = *reinterpret_cast<const float4*>(sYc + s * LC + jc);
       const float y[4] = {y4.x, y4.y, y4.z, y4.w};
@@ -1109,6 +1129,7 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
         dkr[1][u] = fmaf(q1, y[u], dkr[1][u]);
       }
     }
+#pragma unroll 4
     for (int t = r0 + 1; t < C; ++t) {  // column sums (entries at t <= s are zero)
       const float4 x4 = *reinterpret_cast<const float4*>(sXc + t * LC + jc);
       const float4 z4 = *reinterpret_cast<const float4*>(sXq + t * LC + jc);
@@ -1232,6 +1253,7 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   // final values of the own elements; dG and the G_C terms go to shared memory for the reverse cumsum
   float* sDG = sEp;
   float* sXC = sDP;
+  cp_async_wait<0>();  // the records' dQ+, dK+, dK^
   __syncthreads();
 #pragma unroll
   for (int ii = 0; ii < 2; ++ii) {
@@ -1245,7 +1267,7 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
         const float G = sG[t * LC + jl], GC = sG[(n - 1) * LC + jl];
         const float e0 = __expf(G), ec = __expf(GC - G);
         const float kk = sK[t * LC + jl], qq = sQ[t * LC + jl];
-        const float gq = w[BW_DQP + t * D + j], gk = w[BW_DKP + t * D + j], gh = w[BW_DKH + t * D + j];
+        const float gq = sGQ[t * LC + jl], gk = sGK[t * LC + jl], gh = sGH[t * LC + jl];
         const int64_t o = ((int64_t)(t0 + t) * a.H + h) * D + j;
         const float dpt = sDiag[t];
         a.dq[o] = fmaf(dpt, kk, fmaf(gq, e0, dqp[ii][m]));
@@ -1258,29 +1280,45 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
     }
   }
   __syncthreads();
-  if (tid < HC) {
+  {
     // dg_u = sum_{t >= u} (dG_t - X_t) + dG_C with X_t = dK^_t K^_t and dG_C = sum_t X_t + d(e^G_C) e^G_C;
     // the X terms are summed directly as sum_{t < u} X_t (a prefix, not the total minus a suffix), and
-    // sDG holds dG_t without -X_t
-    const int j = j0 + tid;
-    float pre = 0.f;
-    for (int t = 0; t < n; ++t) {
-      const float x = sXC[t * LC + tid];
-      sXC[t * LC + tid] = pre;
-      pre += x;
+    // sDG holds dG_t without -X_t.  Thread (channel jj, part): tokens 8 part .. 8 part + 7, the parts'
+    // totals combined through shared memory (the block scratch is free).
+    const int jj = tid & (HC - 1), part = tid / HC, j = j0 + jj, tb = 8 * part;
+    float xs = 0.f, ds = 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) xs += sXC[(tb + u) * LC + jj];
+#pragma unroll
+    for (int u = 7; u >= 0; --u) ds += sDG[(tb + u) * LC + jj];
+    sKm[part * HC + jj] = xs;
+    sEm[part * HC + jj] = ds;
+    __syncthreads();
+    float pre = 0.f, run = w[BW_DGAM + j] * w[BW_GAM + j];
+    for (int pp = 0; pp < part; ++pp) pre += sKm[pp * HC + jj];
+    for (int pp = NTA / HC - 1; pp > part; --pp) run += sEm[pp * HC + jj];
+    float px[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      px[u] = pre;
+      pre += sXC[(tb + u) * LC + jj];
     }
-    float run = w[BW_DGAM + j] * w[BW_GAM + j];
-    for (int t = n - 1; t >= 0; --t) {
-      run += sDG[t * LC + tid];
-      a.dg[((int64_t)(t0 + t) * a.H + h) * D + j] = run + sXC[t * LC + tid];
+#pragma unroll
+    for (int u = 7; u >= 0; --u) {
+      const int t = tb + u;
+      run += sDG[t * LC + jj];
+      if (t < n) a.dg[((int64_t)(t0 + t) * a.H + h) * D + j] = run + px[u];
     }
-  } else if (half == 0 && tid < HC + C) {  // dbeta_t = (W, U~ part) + sum_s dA_ts a_ts
-    const int t = tid - HC;
-    if (t < n) {
-      float s = w[BW_DBETA + t];
-      for (int u = 0; u < t; ++u) s = fmaf(sDA[t * LC + u], w[BW_A + t * C + u], s);
-      a.dbeta[(int64_t)(t0 + t) * a.H + h] = s;
-    }
+  }
+  if (half == 0) {  // dbeta_t = (W, U~ part) + sum_s dA_ts a_ts: thread (row t, eight columns), lanes summed
+    const int t = tid >> 3, part = tid & 7;
+    float s = 0.f;
+#pragma unroll
+    for (int u = 8 * part; u < 8 * part + 8; ++u)
+      if (u < t) s = fmaf(sDA[t * LC + u], w[BW_A + t * C + u], s);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (part == 0 && t < n) a.dbeta[(int64_t)(t0 + t) * a.H + h] = w[BW_DBETA + t] + s;
   }
 }
 
