@@ -780,6 +780,8 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_chain_kernel(const PrefillArgs
     tc::bar_arrive_expect_tx(full + st, bytes + 512);
     tc::bulk_g2s(stage, rec, bytes, full + st);
     tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
+    // U~, which the math threads read straight from global memory a chunk later, into L2 meanwhile
+    if (!(MODE == MODE_FRAG && tile == 1)) tc::bulk_prefetch_l2(rec + REC_U, 32768);
     issued = cc + 1;
   };
 
@@ -1179,6 +1181,12 @@ __global__ void __launch_bounds__(CHAIN_NT, 1) tc_rev_kernel(const PrefillArgs a
     tc::bar_arrive_expect_tx(full + st, bytes + 512);
     tc::bulk_g2s(sm + st * REC_STAGE, rec, bytes, full + st);
     tc::bulk_g2s(sgam + 128 * st, rec + REC_GAMMA, 512, full + st);
+    if (with_do) {  // the chunk's dO rows, which the math threads load a chunk later, into L2 meanwhile
+      const int64_t tb = chunk_t0(k);
+      const int nr = (int)(t1 - tb < C ? t1 - tb : C);
+      const uint8_t* src = static_cast<const uint8_t*>(a.d_out) + ((size_t)tb * a.H + h) * D * 2;
+      for (int r = 0; r < nr; ++r) tc::bulk_prefetch_l2(src + (size_t)r * a.H * D * 2, D * 2);
+    }
     issued = k + 1;
   };
   // dO of the k-th chunk, column c, this thread's 32 tokens as bf16 pairs (tokens past the end: zero)
