@@ -1327,9 +1327,8 @@ cudaError_t set_smem(K kernel, size_t bytes) {
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// The tensor-core forward pass's layout after the per-chunk records: operand records, fragments, entry
-// states.  Segments: about one output-chain CTA per SM pair and head (P_target = SMs / (2 H)), so the
-// fragment pass (two CTAs per segment and head) fills the GPU once.
+// The tensor-core passes' layout after the per-chunk records: operand records, fragments and entry states
+// (used by the forward pass, then by the reverse one), and the steep flags.
 struct FwdLayout {
   int P;
   size_t rec_off, frag_off, entry_off, steep_off, total;
