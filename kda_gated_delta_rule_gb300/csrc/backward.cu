@@ -748,31 +748,50 @@ __global__ void __launch_bounds__(NT, 1) bwd_state_grads_tc_kernel(BackwardArgs 
     tc::bar_init(bar, 1);
     tc::bar_fence_init();
   }
-  // set 1 and set 2's B operand: S and dS' rows j (with d(e^G_C)_j = sum_l dS'_jl S_jl), dU, dO, U
+  // set 1 and set 2's B operand: S and dS' rows j (with d(e^G_C)_j = sum_l dS'_jl S_jl), dU, dO, U.  Each
+  // thread's global loads go out in groups of four rows before any of them is split (one memory latency
+  // per group instead of one per row)
   {
     const int cc = tid & 15;
-    for (int j = tid >> 4; j < D; j += NT / 16) {
-      float x[8], y[8];
-      load8(w + BW_H + j * D + 8 * cc, x);
-      load8(w + BW_DS + j * D + 8 * cc, y);
-      split8(sm + SG_A + kt_off(j, cc, 128), sm + SG_A + AH + kt_off(j, cc, 128), x);
-      split8(sm + SG_B2 + kt_off(j, cc, 192), sm + SG_B2 + B2H + kt_off(j, cc, 192), y);
-      float s = 0.f;
+#pragma unroll 1
+    for (int jb = tid >> 4; jb < D; jb += 4 * (NT / 16)) {
+      float x[4][8], y[4][8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) s = fmaf(x[e], y[e], s);
+      for (int u = 0; u < 4; ++u) {
+        const int j = jb + u * (NT / 16);
+        load8(w + BW_H + j * D + 8 * cc, x[u]);
+        load8(w + BW_DS + j * D + 8 * cc, y[u]);
+      }
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (cc == 0) w[BW_DGAM + j] = s;
+      for (int u = 0; u < 4; ++u) {
+        const int j = jb + u * (NT / 16);
+        split8(sm + SG_A + kt_off(j, cc, 128), sm + SG_A + AH + kt_off(j, cc, 128), x[u]);
+        split8(sm + SG_B2 + kt_off(j, cc, 192), sm + SG_B2 + B2H + kt_off(j, cc, 192), y[u]);
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s = fmaf(x[u][e], y[u][e], s);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (cc == 0) w[BW_DGAM + j] = s;
+      }
     }
-    for (int t = tid >> 4; t < C; t += NT / 16) {
-      float x[8], y[8], z[8];
-      if (t < n) load8(dO + t * ldo + 8 * cc, x);
-      else for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      load8(w + BW_DU + t * D + 8 * cc, y);
-      load8(w + BW_U + t * D + 8 * cc, z);
-      split8(sm + SG_B1 + kt_off(t, cc, 128), sm + SG_B1 + B1H + kt_off(t, cc, 128), x);
-      split8(sm + SG_B1 + kt_off(64 + t, cc, 128), sm + SG_B1 + B1H + kt_off(64 + t, cc, 128), y);
-      split8(sm + SG_B2 + kt_off(128 + t, cc, 192), sm + SG_B2 + B2H + kt_off(128 + t, cc, 192), z);
+    {  // rows t = tid / 16 + 16 u, u < 4: all of C = 64
+      float x[4][8], y[4][8], z[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = (tid >> 4) + u * (NT / 16);
+        if (t < n) load8(dO + t * ldo + 8 * cc, x[u]);
+        else for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
+        load8(w + BW_DU + t * D + 8 * cc, y[u]);
+        load8(w + BW_U + t * D + 8 * cc, z[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = (tid >> 4) + u * (NT / 16);
+        split8(sm + SG_B1 + kt_off(t, cc, 128), sm + SG_B1 + B1H + kt_off(t, cc, 128), x[u]);
+        split8(sm + SG_B1 + kt_off(64 + t, cc, 128), sm + SG_B1 + B1H + kt_off(64 + t, cc, 128), y[u]);
+        split8(sm + SG_B2 + kt_off(128 + t, cc, 192), sm + SG_B2 + B2H + kt_off(128 + t, cc, 192), z[u]);
+      }
     }
   }
   tc::fence_proxy_async();
@@ -786,17 +805,23 @@ __global__ void __launch_bounds__(NT, 1) bwd_state_grads_tc_kernel(BackwardArgs 
     tc::commit(bar);
   }
   bool ok = __syncthreads_and(tc::bar_wait(bar, 0u)) != 0;
-  // set 2's A operand over set 1's: [U; dO]
+  // set 2's A operand over set 1's: [U; dO] (loads grouped as above)
   if (ok) {
     tc::fence_after_sync();
     const int cc = tid & 15;
-    for (int t = tid >> 4; t < C; t += NT / 16) {
-      float x[8], z[8];
-      if (t < n) load8(dO + t * ldo + 8 * cc, x);
-      else for (int e = 0; e < 8; ++e) x[e] = 0.f;
-      load8(w + BW_U + t * D + 8 * cc, z);
-      split8(sm + SG_A + kt_off(t, cc, 128), sm + SG_A + AH + kt_off(t, cc, 128), z);
-      split8(sm + SG_A + kt_off(64 + t, cc, 128), sm + SG_A + AH + kt_off(64 + t, cc, 128), x);
+    float x[4][8], z[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = (tid >> 4) + u * (NT / 16);
+      if (t < n) load8(dO + t * ldo + 8 * cc, x[u]);
+      else for (int e = 0; e < 8; ++e) x[u][e] = 0.f;
+      load8(w + BW_U + t * D + 8 * cc, z[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = (tid >> 4) + u * (NT / 16);
+      split8(sm + SG_A + kt_off(t, cc, 128), sm + SG_A + AH + kt_off(t, cc, 128), z[u]);
+      split8(sm + SG_A + kt_off(64 + t, cc, 128), sm + SG_A + AH + kt_off(64 + t, cc, 128), x[u]);
     }
     tc::fence_proxy_async();
   }
