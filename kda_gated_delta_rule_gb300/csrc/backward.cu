@@ -1109,8 +1109,10 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
     chunk_wide = gmax - gmin > SPAN_MAX;
   }
   chunk_wide = __syncthreads_or(chunk_wide);
-  // own channels: 4 tx + m in the common case (16-byte loads), tx + 16 m when the blocks take their own references
+  // own elements: rows 2 ty + ii and channels 4 tx + m in the common case (16-byte loads), rows ty + 32 ii and
+  // channels tx + 16 m when the blocks take their own references
   auto own_col = [&](int m) { return chunk_wide ? tx + 16 * m : 4 * tx + m; };
+  auto own_row = [&](int ii) { return chunk_wide ? ty + 32 * ii : 2 * ty + ii; };
   if (!chunk_wide) {
     // Common case: every pair decay through the chunk's last token, e^(G_t - G_s) = e^(G_t - G_C) e^(G_C - G_s):
     //   dq~_t = e^(G_t - G_C) (dP Y)_t,  dk_r,t = beta_t e^(G_t - G_C) (dA Y)_t,
@@ -1140,18 +1142,29 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
       *reinterpret_cast<float4*>(sYc + t * LC + j) = make_float4(y[0], y[1], y[2], y[3]);
     }
     __syncthreads();
-    const int jc = 4 * tx, r0 = ty, r1 = ty + 32;
-#pragma unroll 4
-    for (int s = 0; s < r1; ++s) {  // row sums (entries at s >= t are zero)
-      const float4 y4 = *reinterpret_cast<const float4*>(sYc + s * LC + jc);
-      const float y[4] = {y4.x, y4.y, y4.z, y4.w};
-      const float p0 = sDP[r0 * LC + s], p1 = sDP[r1 * LC + s], q0 = sDA[r0 * LC + s], q1 = sDA[r1 * LC + s];
+    // own rows r0 = 2 ty, r1 = 2 ty + 1: their dP and dA entries come four columns (row sums) or two rows
+    // (column sums) per 16-byte or 8-byte load
+    const int jc = 4 * tx, r0 = 2 * ty, r1 = r0 + 1;
+    const int send = (r1 + 4) & ~3;  // row sums over s < t, in steps of four (entries at s >= t are zero)
+#pragma unroll 2
+    for (int sb = 0; sb < send; sb += 4) {
+      const float4 p04 = *reinterpret_cast<const float4*>(sDP + r0 * LC + sb);
+      const float4 p14 = *reinterpret_cast<const float4*>(sDP + r1 * LC + sb);
+      const float4 q04 = *reinterpret_cast<const float4*>(sDA + r0 * LC + sb);
+      const float4 q14 = *reinterpret_cast<const float4*>(sDA + r1 * LC + sb);
+      const float p0[4] = {p04.x, p04.y, p04.z, p04.w}, p1[4] = {p14.x, p14.y, p14.z, p14.w};
+      const float q0[4] = {q04.x, q04.y, q04.z, q04.w}, q1[4] = {q14.x, q14.y, q14.z, q14.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        dqp[0][u] = fmaf(p0, y[u], dqp[0][u]);
-        dqp[1][u] = fmaf(p1, y[u], dqp[1][u]);
-        dkr[0][u] = fmaf(q0, y[u], dkr[0][u]);
-        dkr[1][u] = fmaf(q1, y[u], dkr[1][u]);
+      for (int v = 0; v < 4; ++v) {
+        const float4 y4 = *reinterpret_cast<const float4*>(sYc + (sb + v) * LC + jc);
+        const float y[4] = {y4.x, y4.y, y4.z, y4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          dqp[0][u] = fmaf(p0[v], y[u], dqp[0][u]);
+          dqp[1][u] = fmaf(p1[v], y[u], dqp[1][u]);
+          dkr[0][u] = fmaf(q0[v], y[u], dkr[0][u]);
+          dkr[1][u] = fmaf(q1[v], y[u], dkr[1][u]);
+        }
       }
     }
 #pragma unroll 4
@@ -1160,7 +1173,9 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
       const float4 z4 = *reinterpret_cast<const float4*>(sXq + t * LC + jc);
       const float x[4] = {x4.x, x4.y, x4.z, x4.w}, xq[4] = {z4.x, z4.y, z4.z, z4.w};
       const float bt = sB[t];
-      const float p0 = sDP[t * LC + r0], p1 = sDP[t * LC + r1], q0 = bt * sDA[t * LC + r0], q1 = bt * sDA[t * LC + r1];
+      const float2 pp = *reinterpret_cast<const float2*>(sDP + t * LC + r0);
+      const float2 qq = *reinterpret_cast<const float2*>(sDA + t * LC + r0);
+      const float p0 = pp.x, p1 = pp.y, q0 = bt * qq.x, q1 = bt * qq.y;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         dkc[0][u] = fmaf(p0, xq[u], fmaf(q0, x[u], dkc[0][u]));
@@ -1169,7 +1184,7 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
     }
 #pragma unroll
     for (int ii = 0; ii < 2; ++ii) {
-      const int t = ty + 32 * ii;
+      const int t = r0 + ii;
       const float bt = sB[t];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -1282,7 +1297,7 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   __syncthreads();
 #pragma unroll
   for (int ii = 0; ii < 2; ++ii) {
-    const int t = ty + 32 * ii;
+    const int t = own_row(ii);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int jl = own_col(m), j = j0 + jl;
