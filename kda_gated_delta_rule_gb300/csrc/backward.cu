@@ -944,14 +944,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
         sM[(ty + 16 * ii) * LC + s] = sB[s] * acc[ii][m];
       }
   }
-  {  // dB_K = T^T dW, dB_V = T^T dU (rows s, columns j = 4 tx + 64 (m / 4) + m % 4, T lower: t >= s);
-     // dK+ = beta dB_K, dv = beta dB_V, dbeta part
+  {  // dB_K = T^T dW, dB_V = T^T dU (rows s = 4 ty + i, columns j = 4 tx + 64 (m / 4) + m % 4, T lower:
+     // t >= s); dK+ = beta dB_K, dv = beta dB_V, dbeta part
     float bk[4][8] = {}, bv[4][8] = {};
-    for (int t = ty; t < C; ++t) {
-      float x[4];
+    for (int t = 4 * ty; t < C; ++t) {
       float4 y[2], z[2];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[t * LC + ty + 16 * ii];
+      const float4 x4 = *reinterpret_cast<const float4*>(sT + t * LC + 4 * ty);
+      const float x[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm) {
         y[mm] = *reinterpret_cast<const float4*>(sDW + t * LD + 4 * tx + 64 * mm);
@@ -973,7 +972,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
     }
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii) {
-      const int s = ty + 16 * ii;
+      const int s = 4 * ty + ii;
       const float b = sB[s];
       float part = 0.f;
 #pragma unroll
@@ -991,12 +990,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
   }
   __syncthreads();
   float* sN = sKp;  // T^T dT [64][LC]
-  {
+  {  // T^T dT: rows s = 4 ty + i (T lower: t >= s), columns tx + 16 m
     float acc[4][4] = {};
-    for (int t = 0; t < C; ++t) {
-      float x[4], y[4];
-#pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[t * LC + ty + 16 * ii];
+    for (int t = 4 * ty; t < C; ++t) {
+      float y[4];
+      const float4 x4 = *reinterpret_cast<const float4*>(sT + t * LC + 4 * ty);
+      const float x[4] = {x4.x, x4.y, x4.z, x4.w};
 #pragma unroll
       for (int m = 0; m < 4; ++m) y[m] = sM[t * LC + tx + 16 * m];
 #pragma unroll
@@ -1008,27 +1007,36 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
-      for (int m = 0; m < 4; ++m) sN[(ty + 16 * ii) * LC + tx + 16 * m] = acc[ii][m];
+      for (int m = 0; m < 4; ++m) sN[(4 * ty + ii) * LC + tx + 16 * m] = acc[ii][m];
   }
   __syncthreads();
-  {  // dA = -(T^T dT) T^T, strictly lower
+  {  // dA = -(T^T dT) T^T, strictly lower: rows s = 4 ty + i, columns u = tx + 16 m, four t per 16-byte load
     float acc[4][4] = {};
-    for (int t = 0; t < C; ++t) {
-      float x[4], y[4];
+#pragma unroll 2
+    for (int tb = 0; tb < C; tb += 4) {
+      float x[4][4], y[4][4];
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sN[(ty + 16 * ii) * LC + t];
+      for (int ii = 0; ii < 4; ++ii) {
+        const float4 v = *reinterpret_cast<const float4*>(sN + (4 * ty + ii) * LC + tb);
+        x[ii][0] = v.x, x[ii][1] = v.y, x[ii][2] = v.z, x[ii][3] = v.w;
+      }
 #pragma unroll
-      for (int m = 0; m < 4; ++m) y[m] = sT[(tx + 16 * m) * LC + t];
+      for (int m = 0; m < 4; ++m) {
+        const float4 v = *reinterpret_cast<const float4*>(sT + (tx + 16 * m) * LC + tb);
+        y[m][0] = v.x, y[m][1] = v.y, y[m][2] = v.z, y[m][3] = v.w;
+      }
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
+      for (int e = 0; e < 4; ++e)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+        for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+          for (int m = 0; m < 4; ++m) acc[ii][m] = fmaf(x[ii][e], y[m][e], acc[ii][m]);
     }
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int s = ty + 16 * ii, u = tx + 16 * m;
+        const int s = 4 * ty + ii, u = tx + 16 * m;
         w[BW_DA + s * C + u] = u < s ? -acc[ii][m] : 0.f;
       }
   }
