@@ -376,29 +376,39 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
     w[BW_T + e] = sT[t * LC + s];
   }
   if (tid < D) w[BW_GAM + tid] = __expf(sG[(n - 1) * LD + tid]);
-  // W = T (diag(beta) K+) and U~ = T diag(beta) V: rows t = ty + 16 i, columns 4 tx + 64 mm + u (16-byte
-  // loads and stores); T is lower, so s runs to the thread's last row
+  // W = T (diag(beta) K+) and U~ = T diag(beta) V: rows t = 4 ty + i, columns 4 tx + 64 mm + u; T's rows read
+  // four columns s per 16-byte load; T is lower, so s runs to the thread's last row
   const int ty = tid >> 4, tx = tid & 15;
   auto t_product = [&](const float* sRhs, bool scale_beta, float* dst) {
     float acc[4][8] = {};
-    for (int s = 0; s <= ty + 48; ++s) {
-      const float bs = scale_beta ? sB[s] : 1.f;
-      float x[4];
+#pragma unroll 1
+    for (int sb = 0; sb < 4 * ty + 4; sb += 4) {
+      float x[4][4];
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii) x[ii] = sT[(ty + 16 * ii) * LC + s] * bs;
-      const float4 y0 = *reinterpret_cast<const float4*>(sRhs + s * LD + 4 * tx);
-      const float4 y1 = *reinterpret_cast<const float4*>(sRhs + s * LD + 4 * tx + 64);
-      const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+      for (int ii = 0; ii < 4; ++ii) {
+        const float4 v = *reinterpret_cast<const float4*>(sT + (4 * ty + ii) * LC + sb);
+        x[ii][0] = v.x, x[ii][1] = v.y, x[ii][2] = v.z, x[ii][3] = v.w;
+      }
 #pragma unroll
-      for (int ii = 0; ii < 4; ++ii)
+      for (int e = 0; e < 4; ++e) {
+        const int s = sb + e;
+        const float bs = scale_beta ? sB[s] : 1.f;
+        const float4 y0 = *reinterpret_cast<const float4*>(sRhs + s * LD + 4 * tx);
+        const float4 y1 = *reinterpret_cast<const float4*>(sRhs + s * LD + 4 * tx + 64);
+        const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int m = 0; m < 8; ++m) acc[ii][m] = fmaf(x[ii], y[m], acc[ii][m]);
+        for (int ii = 0; ii < 4; ++ii) {
+          const float xs = x[ii][e] * bs;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) acc[ii][m] = fmaf(xs, y[m], acc[ii][m]);
+        }
+      }
     }
 #pragma unroll
     for (int ii = 0; ii < 4; ++ii)
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm)
-        *reinterpret_cast<float4*>(dst + (ty + 16 * ii) * D + 4 * tx + 64 * mm) =
+        *reinterpret_cast<float4*>(dst + (4 * ty + ii) * D + 4 * tx + 64 * mm) =
             make_float4(acc[ii][4 * mm], acc[ii][4 * mm + 1], acc[ii][4 * mm + 2], acc[ii][4 * mm + 3]);
   };
   t_product(sX, false, w + BW_W);
