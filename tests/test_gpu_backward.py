@@ -8,7 +8,7 @@ fp32 operand split into bf16 hi + lo (hi*hi + hi*lo + lo*hi, relative operand er
 products (dO S^T, dU S^T, U dS'^T, dO U^T) for every input type and, with bf16 inputs, the forward and
 reverse chunk chains that produce the entry states, U, dS' and dU.  The chains carry that error through up
 to 128 chunk steps (a random walk of ~1e-5 per step in the state).  Measured on the 8192-token workload:
-fp32 chains 4e-6 to 6e-5 of the rms, tensor-core chains 2.7e-5 (dS_0) to 9.6e-5 (dg, where the gradient is
+fp32 chains 4e-6 to 6e-5 of the rms, tensor-core chains 2.7e-5 (dS_0) to 9.2e-5 (dg, where the gradient is
 a small sum of large terms); a wrong term (a dropped product, a wrong decay factor) gives errors of order 1.
 """
 import numpy as np
