@@ -1313,8 +1313,44 @@ __global__ void __launch_bounds__(NTA, 1) bwd_assemble_kernel(BackwardArgs a) {
   float* sXC = sDP;
   cp_async_wait<0>();  // the records' dQ+, dK+, dK^
   __syncthreads();
+  if (!chunk_wide) {  // own channels 4 tx .. 4 tx + 3: every operand by 16-byte loads, dq and dk by 16-byte stores
+    const int jc = 4 * tx;
 #pragma unroll
-  for (int ii = 0; ii < 2; ++ii) {
+    for (int ii = 0; ii < 2; ++ii) {
+      const int t = own_row(ii);
+      float dGv[4] = {0.f, 0.f, 0.f, 0.f}, xcv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t < n) {
+        auto ld = [&](const float* base) {
+          const float4 v = *reinterpret_cast<const float4*>(base + t * LC + jc);
+          return v;
+        };
+        const float4 g4 = ld(sG), k4 = ld(sK), q4 = ld(sQ), gq4 = ld(sGQ), gk4 = ld(sGK), gh4 = ld(sGH);
+        const float4 c4 = *reinterpret_cast<const float4*>(sG + (n - 1) * LC + jc);
+        const float Gv[4] = {g4.x, g4.y, g4.z, g4.w}, Cv[4] = {c4.x, c4.y, c4.z, c4.w};
+        const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+        const float gqv[4] = {gq4.x, gq4.y, gq4.z, gq4.w}, gkv[4] = {gk4.x, gk4.y, gk4.z, gk4.w};
+        const float ghv[4] = {gh4.x, gh4.y, gh4.z, gh4.w};
+        const float dpt = sDiag[t];
+        float dqo[4], dko[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float e0 = __expf(Gv[u]), ec = __expf(Cv[u] - Gv[u]);
+          const float kk = kv[u], qq = qv[u], gq = gqv[u], gk = gkv[u], gh = ghv[u], dkcv = dkc[ii][u];
+          dqo[u] = fmaf(dpt, kk, fmaf(gq, e0, dqp[ii][u]));
+          dko[u] = fmaf(dpt, qq, fmaf(gk, e0, fmaf(gh, ec, dkr[ii][u] + dkcv)));
+          xcv[u] = gh * kk * ec;
+          dGv[u] = (gq * qq + gk * kk) * e0 + qq * dqp[ii][u] + kk * (dkr[ii][u] - dkcv);
+        }
+        const int64_t o = ((int64_t)(t0 + t) * a.H + h) * D + j0 + jc;
+        *reinterpret_cast<float4*>(a.dq + o) = make_float4(dqo[0], dqo[1], dqo[2], dqo[3]);
+        *reinterpret_cast<float4*>(a.dk + o) = make_float4(dko[0], dko[1], dko[2], dko[3]);
+      }
+      *reinterpret_cast<float4*>(sDG + t * LC + jc) = make_float4(dGv[0], dGv[1], dGv[2], dGv[3]);
+      *reinterpret_cast<float4*>(sXC + t * LC + jc) = make_float4(xcv[0], xcv[1], xcv[2], xcv[3]);
+    }
+  }
+#pragma unroll
+  for (int ii = 0; chunk_wide && ii < 2; ++ii) {
     const int t = own_row(ii);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
