@@ -888,7 +888,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_state_grads_tc_kernel(BackwardArgs 
 // ---------------------------------------------------------------------------------------------------
 // 5. WY backward of one (chunk, head): dT, dA, dK+ = diag(beta) T^T dW, dv = diag(beta) T^T dU, dbeta part
 // ---------------------------------------------------------------------------------------------------
-constexpr size_t WY_SMEM = (2 * C * LC + 4 * C * LD + C) * sizeof(float);
+constexpr size_t WY_SMEM = (2 * C * LC + 5 * C * LD + C) * sizeof(float);
 
 template <typename Tin>
 __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
@@ -906,18 +906,20 @@ __global__ void __launch_bounds__(NT, 1) bwd_wy_grads_kernel(BackwardArgs a) {
   float* sV = sKp + C * LD;      // V [64][LD]
   float* sDW = sV + C * LD;      // dW [64][LD]
   float* sDU = sDW + C * LD;     // dU [64][LD]
-  float* sB = sDU + C * LD;      // beta [64]
+  float* sGw = sDU + C * LD;     // G [64][LD] (for K+ = K o e^G)
+  float* sB = sGw + C * LD;      // beta [64]
   const int64_t rs = (int64_t)a.H * D;
   load_rows<NT>(sT, LC, w + BW_T, C, C, C, 0, C);
   load_rows<NT>(sKp, LD, reinterpret_cast<const Tin*>(a.k) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
   load_rows<NT>(sV, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
   load_rows<NT>(sDW, LD, w + BW_DW, D, C, C, 0, D);
   load_rows<NT>(sDU, LD, w + BW_DU, D, C, C, 0, D);
+  load_rows<NT>(sGw, LD, w + BW_G, D, C, C, 0, D);
   if (tid < C) sB[tid] = tid < n ? a.beta[(int64_t)(t0 + tid) * a.H + h] : 0.f;
   cp_async_commit();
   cp_async_wait<0>();
   __syncthreads();
-  for (int e = tid; e < C * D; e += NT) sKp[(e / D) * LD + e % D] *= __expf(w[BW_G + e]);
+  for (int e = tid; e < C * D; e += NT) sKp[(e / D) * LD + e % D] *= __expf(sGw[(e / D) * LD + e % D]);
   __syncthreads();
   const int ty = tid >> 4, tx = tid & 15;
   {  // dT_ts = beta_s (dW_t . K+_s + dU_t . V_s), 16-byte loads along j
