@@ -374,9 +374,13 @@ kda_status kda_cfbi_decode(const void* q, const void* k, const void* v, const fl
  * For the loss L = sum_t <d_out_t, o_t> + sum_i <d_final_i, S_T(i)>, where o and S_T(i) are the outputs and
  * final states kda_prefill_varlen computes from the same inputs, it returns dL/dq, dL/dk, dL/dv, dL/dg,
  * dL/dbeta and dL/dS_0.  The forward is recomputed inside the call (nothing is saved between the two);
- * the chunk algebra it differentiates is the one of kda_prefill_varlen, taken in fp32 on the CUDA cores.
- * Pair decays e^(G_t - G_s) are split at 16-token references while every factor stays below e^80, which
- * holds whenever g >= -5; a block of a chunk that would exceed it takes them one by one.
+ * the chunk algebra it differentiates is the one of kda_prefill_varlen.  With bf16 inputs the chunk-to-chunk
+ * chains (the entry states and U forward, the state gradient dS' and dU in reverse) run on the tensor cores
+ * in segments (split-bf16 products, fp32 accumulation) and the state products dO S^T, dU S^T, U dS'^T and
+ * dO U^T likewise; the chunk-parallel rest is fp32 on the CUDA cores (fp32 inputs: all but the state
+ * products).  Pair decays e^(G_t - G_s) are taken through the chunk's last token while the chunk's decay
+ * span stays within e^80, else at 16-token references, and a block that would exceed e^80 takes them one
+ * by one (its (sequence, head) then runs the CUDA-core chains); g >= -5 keeps every block within range.
  */
 typedef struct {
   const void* q;             /* [T][H][dk] in_dtype */
