@@ -15,9 +15,10 @@
 //   dT = dW (diag(beta) K+)^T + dU (diag(beta) V)^T,  dA = -T^T dT T^T (strictly lower)
 //   dK+ = diag(beta) T^T dW,  dv = diag(beta) T^T dU
 // and the chain rule through beta, the e^G factors and the pair decays e^(G_t - G_s); dg is the in-chunk
-// reverse cumulative sum of dG.  Pair decays are split at a reference token r per 16-token block of s,
-// e^(G_t - G_s) = e^(G_t - G_r) e^(G_r - G_s), while every factor stays below e^80 (always when g >= -5, the
-// pages' floor); a block that would exceed it takes the pair decays one by one.
+// reverse cumulative sum of dG.  Pair decays are split at a reference token r, e^(G_t - G_s) =
+// e^(G_t - G_r) e^(G_r - G_s): the chunk's last token when the chunk's decay span stays within e^80, else the
+// last token of s's 16-token block while every factor stays below e^80 (always when g >= -5, the pages'
+// floor); a block that would exceed it takes the pair decays one by one.
 //
 // Kernels handing over through a per-(chunk, head) fp32 workspace (tiles move into shared memory by
 // asynchronous 16-byte copies):
