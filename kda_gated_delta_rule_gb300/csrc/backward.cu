@@ -344,6 +344,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
     __syncthreads();
   }
 
+  // the chunk's v into sY (free once a and P are formed), asynchronously, while the inverse and W run: fp32
+  // inputs as they are (row stride LD), bf16 inputs as raw bf16 rows (widened before U~); rows past n zero
+  {
+    const Tin* vsrc = reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D;
+    constexpr int Q16 = D * (int)sizeof(Tin) / 16;  // 16-byte pieces of a row
+    for (int e = tid; e < C * Q16; e += NT) {
+      const int r = e / Q16, qq = e % Q16;
+      float* dst = sizeof(Tin) == 4 ? sY + r * LD + 4 * qq : sY + r * (D / 2) + 4 * qq;
+      cp_async16(dst, reinterpret_cast<const float*>(vsrc + (r < n ? r : 0) * rs) + 4 * qq, r < n ? 16 : 0);
+    }
+    cp_async_commit();
+  }
+
   // the record's a; then A = diag(beta) a in place (the inverse's scratch) and T = (I + A)^-1, blocked by
   // 16 (T's upper blocks, the inverse's scratch, cleared after); then diag(beta) K+ in sX
   for (int e = tid; e < C * C; e += NT) w[BW_A + e] = sA[(e / C) * LC + e % C];
@@ -413,12 +426,27 @@ __global__ void __launch_bounds__(NT, 1) bwd_prep_kernel(BackwardArgs a) {
             make_float4(acc[ii][4 * mm], acc[ii][4 * mm + 1], acc[ii][4 * mm + 2], acc[ii][4 * mm + 3]);
   };
   t_product(sX, false, w + BW_W);
+  cp_async_wait<0>();  // v
   __syncthreads();
-  load_rows<NT>(sX, LD, reinterpret_cast<const Tin*>(a.v) + ((int64_t)t0 * a.H + h) * D, rs, C, n, 0, D);
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-  t_product(sX, true, w + BW_UT);
+  if constexpr (sizeof(Tin) == 4) {
+    t_product(sY, true, w + BW_UT);
+  } else {  // widen the raw bf16 rows into sX (free: W is done)
+    for (int e = tid; e < C * D / 8; e += NT) {
+      const int r = e / (D / 8), cc = e % (D / 8);
+      const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(sY) + r * D + 8 * cc);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // bf16 pairs, the lower element in the low half
+        x[2 * q] = __uint_as_float(wv[q] << 16);
+        x[2 * q + 1] = __uint_as_float(wv[q] & 0xFFFF0000u);
+      }
+      *reinterpret_cast<float4*>(sX + r * LD + 8 * cc) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(sX + r * LD + 8 * cc + 4) = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    __syncthreads();
+    t_product(sX, true, w + BW_UT);
+  }
 }
 
 // ---------------------------------------------------------------------------------------------------
